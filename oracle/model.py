@@ -1,0 +1,340 @@
+"""Plain fp64 forward and hand-written backward of one GPT training step.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  Slow on purpose: every
+operation is the textbook definition, matrix products go through NumPy's
+``@`` (BLAS dgemm), attention loops over batch rows and heads, and nothing is
+fused or reordered.
+
+Readings of the pages used here (each is repeated where it applies):
+
+* pre-norm residual block ``x += attn(norm(x)); x += mlp(norm(x))`` and a final
+  ``norm`` before ``lm_head``: the pages say "standard decoder block with
+  normalisation" (devpress §4.1) for a GPT-2-lineage model;
+* no normalisation directly after the embedding lookup (not in the block
+  description);
+* RoPE frequencies ``omega_i = base**(-2 i / hd)`` for pair ``i`` of the
+  half-split layout, ``base = 10000`` (the pages give only the rotation);
+* attention scale ``1/sqrt(hd)`` with a causal mask;
+* GQA query head ``h`` reads key/value head ``h // (H / Hkv)``;
+* RMSNorm ``eps`` is a config field, float32 machine epsilon by default;
+* cross-entropy is the mean over all B*T positions, no ignore index, no
+  logit soft-cap (the pages' "logit stabilisation" is left undefined).
+"""
+from dataclasses import dataclass
+
+import numpy as np
+
+FLT_EPSILON = float(np.finfo(np.float32).eps)
+
+
+@dataclass(frozen=True)
+class Config:
+    depth: int
+    n_embd: int
+    n_head: int
+    n_kv_head: int
+    head_dim: int
+    mlp_hidden: int
+    vocab: int
+    rope_base: float = 10000.0
+    norm_eps: float = FLT_EPSILON
+    init_std: float = 0.02
+
+    @staticmethod
+    def from_workload(w, **kw):
+        return Config(w.depth, w.n_embd, w.n_head, w.n_kv_head, w.head_dim,
+                      w.mlp_hidden, w.vocab, **kw)
+
+
+def param_layout(cfg):
+    """Packed parameter order: (name, rows, cols, offset) per tensor.
+
+    Linear weights are stored ``W[out, in]`` and applied as ``y = x W^T``
+    (bias-free, cosmicrealm "noao-chat-0" §2.1 item 5).  The embedding and the
+    output head are separate tensors (untied, §2.1 item 3).
+    """
+    C, H, Hkv, hd, F, V = (cfg.n_embd, cfg.n_head, cfg.n_kv_head, cfg.head_dim,
+                           cfg.mlp_hidden, cfg.vocab)
+    shapes = [("wte", V, C)]
+    for l in range(cfg.depth):
+        shapes += [(f"h{l}.wq", H * hd, C), (f"h{l}.wk", Hkv * hd, C),
+                   (f"h{l}.wv", Hkv * hd, C), (f"h{l}.wo", C, H * hd),
+                   (f"h{l}.wfc", F, C), (f"h{l}.wproj", C, F)]
+    shapes.append(("lm_head", V, C))
+    out, off = [], 0
+    for name, r, c in shapes:
+        out.append((name, r, c, off))
+        off += r * c
+    return out
+
+
+def n_params(cfg):
+    return sum(r * c for _, r, c, _ in param_layout(cfg))
+
+
+def unpack(cfg, flat):
+    """Dict of fp64 matrices (copies) from a packed vector."""
+    return {name: np.array(flat[off:off + r * c], dtype=np.float64).reshape(r, c)
+            for name, r, c, off in param_layout(cfg)}
+
+
+def pack(cfg, mats):
+    flat = np.zeros(n_params(cfg), dtype=np.float64)
+    for name, r, c, off in param_layout(cfg):
+        flat[off:off + r * c] = mats[name].reshape(-1)
+    return flat
+
+
+# --------------------------------------------------------------------------
+# RMSNorm without gain: y = x / sqrt(mean(x^2) + eps) over the last axis.
+# cosmicrealm "noao-chat-0" §2.1 item 5 (a functional rms_norm, no parameters).
+
+def rms_norm(x, eps):
+    """Returns (y, rstd) with rstd = 1/sqrt(mean(x^2) + eps) per row."""
+    rstd = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return x * rstd, rstd
+
+
+def rms_norm_bwd(dy, y, rstd):
+    """dx = rstd * (dy - y * mean(dy * y)), the derivative of ``rms_norm``."""
+    return rstd * (dy - y * np.mean(dy * y, axis=-1, keepdims=True))
+
+
+# --------------------------------------------------------------------------
+# Rotary embedding by half-split rotation, cosmicrealm "noao-chat-0" §2.1
+# item 1 and §5.3: with x1, x2 the two halves of a head vector,
+# y1 = x1 cos + x2 sin and y2 = -x1 sin + x2 cos.
+
+def rope_tables(T, hd, base):
+    """cos, sin of theta[t, i] = t * base**(-2 i / hd), shapes [T, hd/2]."""
+    d = hd // 2
+    omega = base ** (-(2.0 * np.arange(d, dtype=np.float64)) / hd)
+    theta = np.arange(T, dtype=np.float64)[:, None] * omega[None, :]
+    return np.cos(theta), np.sin(theta)
+
+
+def rope(x, cos, sin):
+    """x: [..., T, hd]; cos, sin: [T, hd/2]."""
+    d = x.shape[-1] // 2
+    x1, x2 = x[..., :d], x[..., d:]
+    return np.concatenate([x1 * cos + x2 * sin, -x1 * sin + x2 * cos], axis=-1)
+
+
+def rope_bwd(dy, cos, sin):
+    """Transpose of ``rope``: the rotation by the opposite angle."""
+    d = dy.shape[-1] // 2
+    dy1, dy2 = dy[..., :d], dy[..., d:]
+    return np.concatenate([dy1 * cos - dy2 * sin, dy1 * sin + dy2 * cos], axis=-1)
+
+
+# --------------------------------------------------------------------------
+# Causal scaled-dot-product attention for one sequence and one head.
+
+def attention(q, k, v):
+    """q, k, v: [T, hd].  Returns (o [T, hd], lse [T]).
+
+    s[t, u] = q_t . k_u / sqrt(hd) for u <= t, -inf otherwise;
+    p = softmax over u; o = p v.  ``lse`` is the natural-log sum of
+    exp(s) per query row.
+    """
+    T, hd = q.shape
+    s = (q @ k.T) / np.sqrt(hd)
+    s = np.where(np.tril(np.ones((T, T), dtype=bool)), s, -np.inf)
+    m = np.max(s, axis=1, keepdims=True)
+    e = np.exp(s - m)
+    z = np.sum(e, axis=1, keepdims=True)
+    p = e / z
+    return p @ v, (m + np.log(z))[:, 0]
+
+
+def attention_bwd(q, k, v, do):
+    """Gradients (dq, dk, dv) of ``attention`` for upstream ``do``."""
+    T, hd = q.shape
+    scale = 1.0 / np.sqrt(hd)
+    s = (q @ k.T) * scale
+    s = np.where(np.tril(np.ones((T, T), dtype=bool)), s, -np.inf)
+    e = np.exp(s - np.max(s, axis=1, keepdims=True))
+    p = e / np.sum(e, axis=1, keepdims=True)
+    dv = p.T @ do
+    dp = do @ v.T
+    ds = p * (dp - np.sum(dp * p, axis=1, keepdims=True))
+    dq = (ds @ k) * scale
+    dk = (ds.T @ q) * scale
+    return dq, dk, dv
+
+
+# --------------------------------------------------------------------------
+# Next-token cross-entropy (devpress §2.2 item 2; cosmicrealm §6.2 snippet).
+
+def cross_entropy(z, tgt):
+    """z: [n, V] logits, tgt: [n].  Returns (per-row losses, dlogits of their sum)."""
+    m = np.max(z, axis=1, keepdims=True)
+    e = np.exp(z - m)
+    ssum = np.sum(e, axis=1, keepdims=True)
+    lse = (m + np.log(ssum))[:, 0]
+    rows = np.arange(z.shape[0])
+    loss = lse - z[rows, tgt]
+    dz = e / ssum
+    dz[rows, tgt] -= 1.0
+    return loss, dz
+
+
+# --------------------------------------------------------------------------
+# One block.  cosmicrealm §2.1 items 2, 4, 6 and devpress §4.1.
+
+def _kv_head_of(cfg, h):
+    return h // (cfg.n_head // cfg.n_kv_head)
+
+
+def block_forward(cfg, W, l, x, cos, sin, keep=False):
+    """x: [B, T, C] residual stream entering layer l; returns the stream leaving it."""
+    B, T, C = x.shape
+    H, Hkv, hd = cfg.n_head, cfg.n_kv_head, cfg.head_dim
+    p = f"h{l}."
+    a, rstd1 = rms_norm(x, cfg.norm_eps)
+    q = (a @ W[p + "wq"].T).reshape(B, T, H, hd).transpose(0, 2, 1, 3)
+    k = (a @ W[p + "wk"].T).reshape(B, T, Hkv, hd).transpose(0, 2, 1, 3)
+    v = (a @ W[p + "wv"].T).reshape(B, T, Hkv, hd).transpose(0, 2, 1, 3)
+    qr, kr = rope(q, cos, sin), rope(k, cos, sin)          # RoPE first ...
+    qn, rq = rms_norm(qr, cfg.norm_eps)                     # ... then QK norm
+    kn, rk = rms_norm(kr, cfg.norm_eps)
+    o = np.empty((B, H, T, hd))
+    for b in range(B):
+        for h in range(H):
+            g = _kv_head_of(cfg, h)
+            o[b, h], _ = attention(qn[b, h], kn[b, g], v[b, g])
+    o2 = o.transpose(0, 2, 1, 3).reshape(B, T, H * hd)
+    x1 = x + o2 @ W[p + "wo"].T
+    bn, rstd2 = rms_norm(x1, cfg.norm_eps)
+    u = bn @ W[p + "wfc"].T
+    r = np.maximum(u, 0.0)
+    hmid = r * r                                            # relu(u)^2
+    x2 = x1 + hmid @ W[p + "wproj"].T
+    if not keep:
+        return x2
+    return x2, dict(a=a, rstd1=rstd1, qn=qn, kn=kn, rq=rq, rk=rk, v=v, o2=o2,
+                    x1=x1, bn=bn, rstd2=rstd2, r=r, hmid=hmid)
+
+
+def block_backward(cfg, W, l, x, dx2, cos, sin, G):
+    """Backward of ``block_forward`` for layer l, recomputing its forward from x.
+
+    Adds the weight gradients into G and returns d(loss)/dx.
+    """
+    B, T, C = x.shape
+    H, Hkv, hd = cfg.n_head, cfg.n_kv_head, cfg.head_dim
+    p = f"h{l}."
+    _, s = block_forward(cfg, W, l, x, cos, sin, keep=True)
+    N = B * T
+    # MLP: x2 = x1 + relu(bn Wfc^T)^2 Wproj^T
+    G[p + "wproj"] += dx2.reshape(N, C).T @ s["hmid"].reshape(N, -1)
+    dh = dx2 @ W[p + "wproj"]
+    du = dh * 2.0 * s["r"]
+    G[p + "wfc"] += du.reshape(N, -1).T @ s["bn"].reshape(N, C)
+    dbn = du @ W[p + "wfc"]
+    dx1 = dx2 + rms_norm_bwd(dbn, s["bn"], s["rstd2"])
+    # attention output projection: x1 = x + o2 Wo^T
+    G[p + "wo"] += dx1.reshape(N, C).T @ s["o2"].reshape(N, -1)
+    do2 = dx1 @ W[p + "wo"]
+    do = do2.reshape(B, T, H, hd).transpose(0, 2, 1, 3)
+    dqn = np.zeros((B, H, T, hd))
+    dkn = np.zeros((B, Hkv, T, hd))
+    dv = np.zeros((B, Hkv, T, hd))
+    for b in range(B):
+        for h in range(H):
+            g = _kv_head_of(cfg, h)
+            dq_, dk_, dv_ = attention_bwd(s["qn"][b, h], s["kn"][b, g], s["v"][b, g], do[b, h])
+            dqn[b, h] = dq_
+            dkn[b, g] += dk_          # a shared kv head sums its group's gradients
+            dv[b, g] += dv_
+    dq = rope_bwd(rms_norm_bwd(dqn, s["qn"], s["rq"]), cos, sin)
+    dk = rope_bwd(rms_norm_bwd(dkn, s["kn"], s["rk"]), cos, sin)
+    dq2 = dq.transpose(0, 2, 1, 3).reshape(N, H * hd)
+    dk2 = dk.transpose(0, 2, 1, 3).reshape(N, Hkv * hd)
+    dv2 = dv.transpose(0, 2, 1, 3).reshape(N, Hkv * hd)
+    a = s["a"].reshape(N, C)
+    G[p + "wq"] += dq2.T @ a
+    G[p + "wk"] += dk2.T @ a
+    G[p + "wv"] += dv2.T @ a
+    da = dq2 @ W[p + "wq"] + dk2 @ W[p + "wk"] + dv2 @ W[p + "wv"]
+    return dx1 + rms_norm_bwd(da.reshape(B, T, C), s["a"], s["rstd1"])
+
+
+# --------------------------------------------------------------------------
+# Whole model.
+
+def _embed(W, tokens):
+    return W["wte"][tokens]
+
+
+def _trunk(cfg, W, tokens, keep_inputs):
+    B, T = tokens.shape
+    cos, sin = rope_tables(T, cfg.head_dim, cfg.rope_base)
+    x = _embed(W, tokens)
+    xs = []
+    for l in range(cfg.depth):
+        if keep_inputs:
+            xs.append(x)
+        x = block_forward(cfg, W, l, x, cos, sin)
+    return x, xs, cos, sin
+
+
+def forward_logits(cfg, params, tokens, rows=None):
+    """fp64 logits [B, T, V] (or only the flat rows listed in ``rows``)."""
+    W = unpack(cfg, params) if not isinstance(params, dict) else params
+    x, _, _, _ = _trunk(cfg, W, np.asarray(tokens), False)
+    xf, _ = rms_norm(x, cfg.norm_eps)
+    B, T, C = xf.shape
+    xf = xf.reshape(B * T, C)
+    if rows is not None:
+        return xf[np.asarray(rows)] @ W["lm_head"].T
+    return (xf @ W["lm_head"].T).reshape(B, T, -1)
+
+
+def row_losses(cfg, params, tokens, targets):
+    """Per-position cross-entropy [B, T] (forward only)."""
+    W = unpack(cfg, params) if not isinstance(params, dict) else params
+    tokens, targets = np.asarray(tokens), np.asarray(targets)
+    x, _, _, _ = _trunk(cfg, W, tokens, False)
+    xf, _ = rms_norm(x, cfg.norm_eps)
+    B, T, C = xf.shape
+    xf = xf.reshape(B * T, C)
+    t = targets.reshape(-1)
+    out = np.empty(B * T)
+    for a in range(0, B * T, 512):
+        z = xf[a:a + 512] @ W["lm_head"].T
+        out[a:a + 512], _ = cross_entropy(z, t[a:a + 512])
+    return out.reshape(B, T)
+
+
+def forward_backward(cfg, params, tokens, targets, chunk=512):
+    """Mean next-token cross-entropy and its gradient for every parameter.
+
+    Returns (loss, grads) with grads a dict of fp64 matrices in layout order
+    (use ``pack`` for the flat vector).  Only the residual stream entering
+    each layer is kept; each layer's forward is recomputed in the backward.
+    """
+    W = unpack(cfg, params) if not isinstance(params, dict) else params
+    tokens, targets = np.asarray(tokens), np.asarray(targets)
+    B, T = tokens.shape
+    N = B * T
+    G = {k: np.zeros_like(v) for k, v in W.items()}
+    x, xs, cos, sin = _trunk(cfg, W, tokens, True)
+    xf, rstd = rms_norm(x, cfg.norm_eps)
+    C = xf.shape[-1]
+    xf2 = xf.reshape(N, C)
+    t = targets.reshape(-1)
+    total = 0.0
+    dxf = np.empty((N, C))
+    for a in range(0, N, chunk):
+        z = xf2[a:a + chunk] @ W["lm_head"].T
+        l_rows, dz = cross_entropy(z, t[a:a + chunk])
+        total += float(np.sum(l_rows))
+        dz /= N                                   # the loss is a mean over B*T
+        G["lm_head"] += dz.T @ xf2[a:a + chunk]
+        dxf[a:a + chunk] = dz @ W["lm_head"]
+    dx = rms_norm_bwd(dxf.reshape(B, T, C), xf, rstd)
+    for l in reversed(range(cfg.depth)):
+        dx = block_backward(cfg, W, l, xs[l], dx, cos, sin, G)
+    np.add.at(G["wte"], tokens.reshape(-1), dx.reshape(N, C))
+    return total / N, G
