@@ -16,7 +16,8 @@ independent implementations produce the same numbers:
 * Box-Muller (Box & Muller, 1958), one normal per 64-bit output: the top 24
   bits give u1, bits 16..39 give u2, each as ``(k + 0.5) / 2**24``;
   ``z = sqrt(-2 ln u1) * cos(2 pi u2)`` in fp64, times ``std``, rounded once
-  to float32.
+  to float32.  ``std`` is the float32 value a model configuration carries
+  (0.02 becomes float32(0.02) = 0.0199999995529651...), widened exactly.
 """
 import numpy as np
 
@@ -54,6 +55,7 @@ def box_muller(u64):
 def normal_init(seed, tensor_index, count, std, chunk=1 << 24):
     """float32 N(0, std) values for one tensor of the packed layout."""
     out = np.empty(count, dtype=np.float32)
+    std = float(np.float32(std))
     s0 = stream_state(seed, tensor_index)
     for a in range(0, count, chunk):
         n = min(chunk, count - a)
