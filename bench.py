@@ -1,0 +1,310 @@
+"""Benchmark: training tokens/s and MFU of one forward+backward GPT step on B300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config d20] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  A step is one nc_forward_backward call over a
+full batch of the workload: weight cast, forward, chunked lm_head +
+cross-entropy, backward, fp32 gradient write, loss read-back.  `value` is
+timed with CUDA events on the launching stream with inputs already resident
+in HBM; `e2e` times the same step through nc_forward_backward_host from
+pinned host buffers (host->device token copies and the loss read inside the
+timed region).  The working set (GBs of activations) is far larger than L2,
+so no explicit L2 flush is needed between steps.
+
+With N > 1 (torchrun) every rank runs an independent replica on its own GPU
+(the step has no data-path exchange here); `value` sums all ranks' tokens over
+the slowest rank's time.
+
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload on this host's cores (rank 0 only).
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic as S  # noqa: E402
+
+METRIC = "train tokens/sec and MFU at 1 B300 (fwd+bwd step), vs CPU oracle tok/s"
+UNIT = "tokens/s"
+DESCR = {
+    "tiny": "tiny GPT L2 C128 H2/2 hd64 F512 V512 T64 B2 (fp32)",
+    "d12": "d12 GPT L12 C768 H6/6 hd128 F3072 V65536 T2048 B32 (bf16)",
+    "d20": "d20 GPT L20 C1280 H10/10 hd128 F5120 V65536 T2048 B32 (bf16)",
+    "d26": "d26 GPT L26 C1664 H13/13 hd128 F6656 V65536 T2048 B16 (bf16)",
+    "d24gqa": "d24 GQA GPT L24 C1536 H12/4 hd128 F6144 V65536 T4096 B8 (bf16)",
+}
+# CPU-oracle sample (tokens of one sequence) per workload: ~10-30 s of fp64 work
+CPU_SAMPLE_T = {"tiny": 64, "d12": 128, "d20": 64, "d26": 48, "d24gqa": 48}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("bf16_tflops", 1800.0), d.get("bf16_tflops_sustained", 1400.0), d.get("hbm_gbs", 6400.0), "measured"
+    return 1800.0, 1400.0, 6400.0, "fallback"
+
+
+def flops_per_token(w):
+    """Algorithmic training FLOPs per token (forward + backward).
+
+    6 * (matrix parameters: every weight except the embedding table, which is
+    a gather) + causal attention 6 * L * H * hd * T (QK^T and PV, forward x3,
+    each query attending to T/2 keys on average).  Also returns the
+    full-square attention and 6 * N_total conventions.
+    """
+    C, H, Hkv, hd, F, V, L, T = (w.n_embd, w.n_head, w.n_kv_head, w.head_dim, w.mlp_hidden, w.vocab,
+                                 w.depth, w.seq_len)
+    n_layer = C * H * hd + 2 * C * Hkv * hd + H * hd * C + 2 * C * F
+    n_mm = L * n_layer + V * C
+    n_total = n_mm + V * C
+    attn_causal = 6 * L * H * hd * T
+    return {"causal": 6 * n_mm + attn_causal, "full_square": 6 * n_mm + 2 * attn_causal,
+            "six_n_total": 6 * n_total, "n_mm": n_mm, "n_total": n_total}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        rows = [l.split(",") for l in open(self.f.name).read().strip().splitlines() if l.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(w, t_sample, steps, warmup):
+    """Time the fp64 oracle on one sequence of t_sample tokens (weights N(0, 0.02))."""
+    from oracle import model as OM
+    cfg = OM.Config.from_workload(w)
+    rng = np.random.default_rng(S.WEIGHT_SEED)
+    W = {name: rng.standard_normal((r, c)) * 0.02 for name, r, c, _ in OM.param_layout(cfg)}
+    tok, tgt = S.batch_tokens(w, batch=1, seq_len=t_sample)
+    times = []
+    for i in range(warmup + steps):
+        t0 = time.perf_counter()
+        OM.forward_backward(cfg, W, tok, tgt)
+        if i >= warmup:
+            times.append(time.perf_counter() - t0)
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([d.get("num_threads", 1) for d in threadpool_info()] or [1])
+    except Exception:
+        threads = os.cpu_count()
+    return t_sample / statistics.median(times), threads, times
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    t_sample = CPU_SAMPLE_T.get(args.config, 64)
+    tps, threads, times = oracle_sample(w, t_sample, args.steps, args.warmup)
+    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": DESCR[args.config], "sample": f"1 x {t_sample} tokens"},
+            "cpu_baseline": {"value": tps, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"one sequence of {t_sample} tokens of the {args.config} workload, "
+                                       f"fp64 NumPy forward+backward"},
+            "e2e": {"value": tps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="d20", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = S.workload(args.config)
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import decoder_only_transformer_07_b300 as nc
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+
+    model = nc.Model(nc.config_from_workload(w), seed=S.WEIGHT_SEED)
+    tok_np, tgt_np = S.batch_tokens(w)
+    tok = torch.from_numpy(tok_np).cuda()
+    tgt = torch.from_numpy(tgt_np).cuda()
+    grads = torch.empty(model.n_params, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        model.forward_backward(tok, tgt, grads)
+    launches_per_step = model.last_launch_count()
+
+    # ---- device-resident timing
+    clocks = ClockSampler(dev)
+    model_prof = nc.lib()
+    model_prof.nc_profile_enable(model.handle, 1)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    losses = []
+    for _ in range(args.steps):
+        loss, _ = model.forward_backward(tok, tgt, grads)
+        losses.append(loss)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    prof = {}
+    import ctypes
+    for cls, name in enumerate(["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "ce", "embed", "cast", "other"]):
+        t, n, fl, by = ctypes.c_double(), ctypes.c_int64(), ctypes.c_double(), ctypes.c_double()
+        model_prof.nc_profile_read(model.handle, cls, ctypes.byref(t), ctypes.byref(n), ctypes.byref(fl),
+                                   ctypes.byref(by))
+        prof[name] = {"ms": t.value, "launches": n.value, "flops": fl.value, "bytes": by.value}
+    model_prof.nc_profile_enable(model.handle, 0)
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    tokens_per_step = w.batch * w.seq_len
+    value = world * tokens_per_step * args.steps / (ms / 1e3)
+    ms_step = ms / args.steps
+
+    # ---- end-to-end through the host-buffer entry point
+    tok_h = torch.from_numpy(tok_np).pin_memory()
+    tgt_h = torch.from_numpy(tgt_np).pin_memory()
+    for _ in range(2):
+        model.forward_backward_host(tok_h, tgt_h, grads)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        model.forward_backward_host(tok_h, tgt_h, grads)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        tt = torch.tensor([e2e_s], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    e2e = {"value": world * tokens_per_step * args.steps / e2e_s, "unit": UNIT,
+           "h2d_bytes_per_step": int(tok_np.nbytes + tgt_np.nbytes), "d2h_bytes_per_step": 8}
+
+    peak_burst, peak_sust, hbm, peak_src = load_peaks()
+    fpt = flops_per_token(w)
+    per_gpu_tps = value / world
+    mfu = {k: per_gpu_tps * fpt[k] / (peak_burst * 1e12) for k in ("causal", "full_square", "six_n_total")}
+    mfu["causal_vs_sustained"] = per_gpu_tps * fpt["causal"] / (peak_sust * 1e12)
+
+    g = prof["gemm"]
+    gemm_tflops = g["flops"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else None
+    roofline = {"kernel": "k_gemm_tc (tcgen05 bf16 GEMM, all 5 linear layers fwd + dX + dW)",
+                "bound": "tensor", "achieved": gemm_tflops, "peak": peak_sust, "unit": "TFLOP/s",
+                "frac": (gemm_tflops / peak_sust) if gemm_tflops else None, "traffic": None,
+                "peak_kind": f"bf16 dense, sustained ({peak_src})"}
+    total_prof_ms = sum(v["ms"] for v in prof.values())
+    kernels = {k: {"ms_per_step": v["ms"] / args.steps, "share": (v["ms"] / total_prof_ms) if total_prof_ms else None,
+                   "launches_per_step": v["launches"] / args.steps,
+                   "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["ms"] > 0 and v["flops"] else None,
+                   "gbs": (v["bytes"] / (v["ms"] / 1e3) / 1e9) if v["ms"] > 0 and v["bytes"] else None}
+               for k, v in prof.items() if v["launches"]}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        t_sample = CPU_SAMPLE_T.get(args.config, 64)
+        tps, threads, _ = oracle_sample(w, t_sample, 1, 0)
+        cpu = {"value": tps, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"one sequence of {t_sample} tokens of the {args.config} workload, fp64 NumPy fwd+bwd"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+                "data": "synthetic: Zipf(1.1) token ids (seed 2), N(0,0.02) fp32 master weights (seed 1)",
+                "config": {"workload": DESCR[args.config], "global_batch": world * w.batch,
+                           "seq_len": w.seq_len, "parallelism": "replicas" if world > 1 else "single",
+                           "l2": "working set >> L2 (no flush needed)"},
+                "mfu": mfu, "flops_per_token": fpt["causal"], "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": e2e, "gpu_launches": int(launches_per_step * args.steps), "clocks": clk,
+                "kernels": kernels, "loss": losses[-1]}
+        print(json.dumps(line), flush=True)
+    model.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

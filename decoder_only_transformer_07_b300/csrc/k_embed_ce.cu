@@ -1,0 +1,303 @@
+// Token embedding gather and its deterministic scatter-add backward, and the
+// next-token cross-entropy with its gradient.
+//
+// The embedding `wte` is a separate (untied) table read by token id
+// (cosmicrealm "noao-chat-0-项目总体介绍" §2.1 item 3); the loss is next-token
+// cross-entropy (devpress "用不到100美元，亲手训练一个属于你的GPT-2" §2.2 item 2).
+#include "nc_kernels.cuh"
+
+// ---------------------------------------------------------------- gather
+// One warp per token row: x[i] = float(round_act(wte[tokens[i]])).  An id
+// outside [0, V) sets the token error bit and writes a zero row.
+template <typename T>
+__global__ void k_embed_fwd(int64_t n, int C, int V, const int32_t* __restrict__ tokens,
+                            const float* __restrict__ wte, float* __restrict__ x,
+                            int32_t* __restrict__ err) {
+  int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int lane = threadIdx.x & 31;
+  if (i >= n) return;
+  int tok = tokens[i];
+  bool ok = tok >= 0 && tok < V;
+  if (!ok && lane == 0 && err) atomicOr(err, NC_DEVERR_TOKEN);
+  const float4* src = reinterpret_cast<const float4*>(wte + (int64_t)(ok ? tok : 0) * C);
+  float4* dst = reinterpret_cast<float4*>(x + i * C);
+  for (int c = lane; c < C / 4; c += 32) {
+    float4 v = ok ? src[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    v.x = round_act<T>(v.x); v.y = round_act<T>(v.y);
+    v.z = round_act<T>(v.z); v.w = round_act<T>(v.w);
+    dst[c] = v;
+  }
+}
+
+nc_status launch_embed_fwd(int dtype, int64_t n, int C, int V, const int32_t* tokens,
+                           const float* wte, float* x, int32_t* err, cudaStream_t st) {
+  if (n <= 0) return NC_OK;
+  if (C % 4 || (((uintptr_t)wte) & 15) || (((uintptr_t)x) & 15)) return NC_ERR_ARG;
+  if (dtype == NC_BF16)
+    k_embed_fwd<bf16><<<cdiv(n, 8), 256, 0, st>>>(n, C, V, tokens, wte, x, err);
+  else
+    k_embed_fwd<float><<<cdiv(n, 8), 256, 0, st>>>(n, C, V, tokens, wte, x, err);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- scatter
+// dwte[v] = sum of dx[i] over i with tokens[i] == v, in increasing i.
+//  1. chunks of EMB_CH positions: sort (token, position) in shared memory,
+//     sum each run of equal tokens in position order into one partial row;
+//  2. count partial rows per token, exclusive scan -> offsets;
+//  3. list each token's partial rows (slot order arbitrary);
+//  4. per token row: sort its partial slots (= chunk order), add them in that
+//     order; ids that never occur get +0.0.
+// Every floating-point sum has a fixed order, so the result is bitwise
+// reproducible.
+#define EMB_CH 256
+#define EMB_MAXV4 8          // C <= 4 * 8 * EMB_CH = 8192
+#define EMB_MAX_CHUNKS 4096  // n <= 2^20
+
+struct EmbScratch {
+  float* partial;   // [n, C]
+  int* run_tok;     // [n]
+  int* nruns;       // [nchunks]
+  int* count;       // [V]
+  int* offs;        // [V]
+  int* cursor;      // [V]
+  int* list;        // [n]
+};
+
+static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+static EmbScratch emb_carve(void* base, int64_t n, int C, int V) {
+  EmbScratch s;
+  char* p = (char*)base;
+  int64_t nchunks = (n + EMB_CH - 1) / EMB_CH;
+  s.partial = (float*)p; p += align256((size_t)n * C * sizeof(float));
+  s.run_tok = (int*)p; p += align256((size_t)n * sizeof(int));
+  s.nruns = (int*)p; p += align256((size_t)nchunks * sizeof(int));
+  s.count = (int*)p; p += align256((size_t)V * sizeof(int));
+  s.offs = (int*)p; p += align256((size_t)V * sizeof(int));
+  s.cursor = (int*)p; p += align256((size_t)V * sizeof(int));
+  s.list = (int*)p; p += align256((size_t)n * sizeof(int));
+  return s;
+}
+
+size_t embed_bwd_scratch_bytes(int64_t n, int C, int V) {
+  int64_t nchunks = (n + EMB_CH - 1) / EMB_CH;
+  return align256((size_t)n * C * sizeof(float)) + 2 * align256((size_t)n * sizeof(int)) +
+         align256((size_t)nchunks * sizeof(int)) + 3 * align256((size_t)V * sizeof(int));
+}
+
+// Bitonic sort of `len` (power of two, <= blockDim.x * k) keys in shared memory.
+template <typename K>
+__device__ void block_bitonic_sort(K* keys, int len) {
+  for (int size = 2; size <= len; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < len; i += blockDim.x) {
+        int j = i ^ stride;
+        if (j > i) {
+          bool up = ((i & size) == 0);
+          K a = keys[i], b = keys[j];
+          if ((a > b) == up) { keys[i] = b; keys[j] = a; }
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(EMB_CH) k_emb_bwd_runs(int64_t n, int C, const int32_t* __restrict__ tokens,
+                                                          const float* __restrict__ dx, EmbScratch s) {
+  __shared__ unsigned long long keys[EMB_CH];
+  __shared__ int run_of[EMB_CH];
+  const int64_t base = (int64_t)blockIdx.x * EMB_CH;
+  const int tid = threadIdx.x;
+  int64_t i = base + tid;
+  keys[tid] = (i < n) ? (((unsigned long long)(unsigned)tokens[i] << 32) | (unsigned)tid) : ~0ull;
+  block_bitonic_sort(keys, EMB_CH);
+  const int valid = (int)((n - base < (int64_t)EMB_CH) ? (n - base) : (int64_t)EMB_CH);
+  // run index of each sorted position (inclusive scan of run starts; EMB_CH is small)
+  if (tid == 0) {
+    int r = -1;
+    for (int k = 0; k < valid; ++k) {
+      if (k == 0 || (keys[k] >> 32) != (keys[k - 1] >> 32)) {
+        ++r;
+        int v = (int)(keys[k] >> 32);
+        s.run_tok[base + r] = v;
+        atomicAdd(&s.count[v], 1);
+      }
+      run_of[k] = r;
+    }
+    s.nruns[blockIdx.x] = r + 1;
+  }
+  __syncthreads();
+  const int C4 = C / 4;
+  float4 acc[EMB_MAXV4];
+#pragma unroll
+  for (int k = 0; k < EMB_MAXV4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < valid; ++k) {
+    const float4* row = reinterpret_cast<const float4*>(dx + (base + (int)(keys[k] & 0xffffffffu)) * C);
+#pragma unroll
+    for (int q = 0; q < EMB_MAXV4; ++q) {
+      int c = tid + q * EMB_CH;
+      if (c < C4) {
+        float4 v = row[c];
+        acc[q].x += v.x; acc[q].y += v.y; acc[q].z += v.z; acc[q].w += v.w;
+      }
+    }
+    if (k == valid - 1 || run_of[k + 1] != run_of[k]) {
+      float4* dst = reinterpret_cast<float4*>(s.partial + (base + run_of[k]) * C);
+#pragma unroll
+      for (int q = 0; q < EMB_MAXV4; ++q) {
+        int c = tid + q * EMB_CH;
+        if (c < C4) dst[c] = acc[q];
+        acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  }
+}
+
+// Exclusive scan of count[V] into offs[V]; one block of 1024 threads.
+__global__ void __launch_bounds__(1024) k_emb_bwd_scan(int V, const int* __restrict__ count, int* __restrict__ offs) {
+  __shared__ int part[1024];
+  const int per = (V + 1023) / 1024;
+  const int a = threadIdx.x * per, b = min(V, a + per);
+  int sum = 0;
+  for (int v = a; v < b; ++v) sum += count[v];
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    int t = (threadIdx.x >= off) ? part[threadIdx.x - off] : 0;
+    __syncthreads();
+    part[threadIdx.x] += t;
+    __syncthreads();
+  }
+  int run = part[threadIdx.x] - sum;
+  for (int v = a; v < b; ++v) { offs[v] = run; run += count[v]; }
+}
+
+__global__ void k_emb_bwd_list(EmbScratch s) {
+  const int64_t base = (int64_t)blockIdx.x * EMB_CH;
+  int r = threadIdx.x;
+  if (r >= s.nruns[blockIdx.x]) return;
+  int v = s.run_tok[base + r];
+  int pos = atomicAdd(&s.cursor[v], 1);
+  s.list[s.offs[v] + pos] = (int)(base + r);
+}
+
+__global__ void __launch_bounds__(256) k_emb_bwd_rows(int V, int C, EmbScratch s, float* __restrict__ dwte) {
+  __shared__ int slots[EMB_MAX_CHUNKS];
+  const int v = blockIdx.x;
+  const int cnt = s.count[v];
+  float4* dst = reinterpret_cast<float4*>(dwte + (int64_t)v * C);
+  const int C4 = C / 4;
+  if (cnt == 0) {
+    for (int c = threadIdx.x; c < C4; c += blockDim.x) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const int o = s.offs[v];
+  if (cnt == 1) {
+    const float4* src = reinterpret_cast<const float4*>(s.partial + (int64_t)s.list[o] * C);
+    for (int c = threadIdx.x; c < C4; c += blockDim.x) dst[c] = src[c];
+    return;
+  }
+  int len = 1;
+  while (len < cnt) len <<= 1;
+  for (int k = threadIdx.x; k < len; k += blockDim.x) slots[k] = (k < cnt) ? s.list[o + k] : 0x7fffffff;
+  block_bitonic_sort(slots, len);
+  for (int c = threadIdx.x; c < C4; c += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < cnt; ++k) {
+      float4 p = reinterpret_cast<const float4*>(s.partial + (int64_t)slots[k] * C)[c];
+      acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
+    }
+    dst[c] = acc;
+  }
+}
+
+nc_status launch_embed_bwd(int64_t n, int C, int V, const int32_t* tokens, const float* dx,
+                           float* dwte, void* scratch, cudaStream_t st) {
+  if (C % 4 || C > 4 * EMB_MAXV4 * EMB_CH || V <= 0) return NC_ERR_ARG;
+  int64_t nchunks = (n + EMB_CH - 1) / EMB_CH;
+  if (nchunks > EMB_MAX_CHUNKS) return NC_ERR_UNSUPPORTED;
+  if (!scratch || (((uintptr_t)scratch) & 255)) return NC_ERR_ARG;
+  EmbScratch s = emb_carve(scratch, n, C, V);
+  NC_CUDA_TRY(cudaMemsetAsync(s.count, 0, sizeof(int) * (size_t)V, st));
+  NC_CUDA_TRY(cudaMemsetAsync(s.cursor, 0, sizeof(int) * (size_t)V, st));
+  if (nchunks > 0) {
+    k_emb_bwd_runs<<<(unsigned)nchunks, EMB_CH, 0, st>>>(n, C, tokens, dx, s);
+    NC_CUDA_TRY(cudaGetLastError());
+  }
+  k_emb_bwd_scan<<<1, 1024, 0, st>>>(V, s.count, s.offs);
+  NC_CUDA_TRY(cudaGetLastError());
+  if (nchunks > 0) {
+    k_emb_bwd_list<<<(unsigned)nchunks, EMB_CH, 0, st>>>(s);
+    NC_CUDA_TRY(cudaGetLastError());
+  }
+  k_emb_bwd_rows<<<V, 256, 0, st>>>(V, C, s, dwte);
+  NC_CUDA_TRY(cudaGetLastError());
+  return NC_OK;
+}
+
+// ---------------------------------------------------------------- cross-entropy
+// One block per row.  row_loss = logsumexp(z) - z[target];
+// z <- (softmax(z) - onehot(target)) * scale, in place.
+template <typename T>
+__global__ void __launch_bounds__(512) k_cross_entropy(int V, T* __restrict__ z, int64_t ldz,
+                                                       const int32_t* __restrict__ targets,
+                                                       float* __restrict__ row_loss, float scale,
+                                                       int32_t* __restrict__ err) {
+  __shared__ float sh[32];
+  const int64_t row = blockIdx.x;
+  T* zr = z + row * ldz;
+  float m = -INFINITY;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) m = fmaxf(m, to_f32(zr[v]));
+  m = block_max(m, sh);
+  float s = 0.f;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) s += expf(to_f32(zr[v]) - m);
+  s = block_sum(s, sh);
+  const float lse = m + logf(s);
+  const int tgt = targets[row];
+  const bool ok = tgt >= 0 && tgt < V;
+  if (threadIdx.x == 0) {
+    if (!ok && err) atomicOr(err, NC_DEVERR_TOKEN);
+    row_loss[row] = ok ? lse - to_f32(zr[tgt]) : 0.f;
+  }
+  __syncthreads();   // z[tgt] is read above before any thread overwrites it
+  const float inv = 1.f / s;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    float p = expf(to_f32(zr[v]) - m) * inv;
+    if (v == tgt) p -= 1.f;
+    zr[v] = from_f32<T>(p * scale);
+  }
+}
+
+nc_status launch_cross_entropy(int dtype, int64_t rows, int V, void* z, int64_t ldz,
+                               const int32_t* targets, float* row_loss, float scale, int32_t* err,
+                               cudaStream_t st) {
+  if (rows <= 0) return NC_OK;
+  if (rows > 0x7fffffff) return NC_ERR_ARG;
+  if (dtype == NC_BF16)
+    k_cross_entropy<bf16><<<(unsigned)rows, 512, 0, st>>>(V, (bf16*)z, ldz, targets, row_loss, scale, err);
+  else
+    k_cross_entropy<float><<<(unsigned)rows, 512, 0, st>>>(V, (float*)z, ldz, targets, row_loss, scale, err);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+// Mean of row_loss[0..n) in a fixed order (fp64 partials), written to out[0].
+__global__ void __launch_bounds__(1024) k_mean(int64_t n, const float* __restrict__ x, float* __restrict__ out) {
+  __shared__ double part[1024];
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < n; i += 1024) s += (double)x[i];
+  part[threadIdx.x] = s;
+  __syncthreads();
+  for (int off = 512; off > 0; off >>= 1) {
+    if (threadIdx.x < off) part[threadIdx.x] += part[threadIdx.x + off];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) out[0] = (float)(part[0] / (double)n);
+}
+
+nc_status launch_mean(int64_t n, const float* x, float* out, cudaStream_t st) {
+  k_mean<<<1, 1024, 0, st>>>(n, x, out);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}

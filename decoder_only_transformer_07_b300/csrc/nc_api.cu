@@ -1,0 +1,667 @@
+// The C ABI of libnc: model lifetime, parameter layout, the forward+backward
+// training step and the kernel-level entry points.  See include/nc.h.
+//
+// One step enqueues, on the caller's stream: the weight cast, the embedding
+// gather, per layer {RMSNorm, QKV GEMM, RoPE + QK-norm, attention, output
+// projection GEMM + residual, RMSNorm, fc GEMM + relu^2, c_proj GEMM +
+// residual}, the final RMSNorm, the chunked lm_head + cross-entropy (forward
+// and backward per chunk), then per layer in reverse the matching backward
+// kernels, and the embedding scatter.  The only synchronisation is the final
+// read of the loss and the device error flag.
+#include <cfloat>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "nc_kernels.cuh"
+
+extern uint64_t g_tc_wait_ns;
+
+struct ParamTensor {
+  std::string name;
+  int64_t rows, cols, off;
+};
+
+struct nc_model {
+  nc_config cfg;
+  int L, C, H, Hkv, hd, F, V, Tmax, Bmax, qkvw, dtype;
+  int64_t Nmax, P;
+  size_t act;                        // bytes per compute-dtype element
+  std::vector<ParamTensor> layout;
+  std::vector<void*> allocs;
+  float* master = nullptr;           // fp32 [P]
+  void* wact = nullptr;              // compute-dtype weights [P] (== master in fp32 mode)
+  float* rope_tab = nullptr;         // [Tmax, hd/2, 2]
+  int32_t* err = nullptr;            // device error flag
+  float* result = nullptr;           // device: [0] loss, [1] error flag copy
+  float* result_host = nullptr;      // pinned host copy
+  // forward activations (per layer, strides sized for Nmax tokens)
+  float* x = nullptr;                // residual stream [N, C]
+  uint8_t *xn1, *xn2, *qkv, *o, *r, *h;
+  float *rstd1, *rstd2, *rstdqk, *lse;
+  void* xf = nullptr;
+  float* rstd_f = nullptr;
+  void* logits = nullptr;            // [Nc, V] chunk of logits / dlogits
+  int64_t chunk_rows = 0;
+  float* rowloss = nullptr;
+  // backward scratch
+  float* dx = nullptr;
+  void* dx_act = nullptr;
+  void* du = nullptr;
+  float* dxn = nullptr;
+  void* dout = nullptr;
+  void* dqkv = nullptr;
+  float* Dv = nullptr;
+  void* emb_scratch = nullptr;
+  int32_t *tok_dev = nullptr, *tgt_dev = nullptr;
+  int64_t launches = 0;
+  // profiling (nc_profile_enable)
+  struct Rec { int cls; int ev; double flops, bytes; };
+  bool prof_on = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  std::vector<Rec> recs;
+  double prof_ms[NC_PROF_CLASSES] = {}, prof_flops[NC_PROF_CLASSES] = {}, prof_bytes[NC_PROF_CLASSES] = {};
+  int64_t prof_n[NC_PROF_CLASSES] = {};
+};
+
+// ------------------------------------------------------------------ profiling
+
+static int prof_event(nc_model* m) {
+  if (m->ev_used == m->ev_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return -1;
+    m->ev_pool.push_back(e);
+  }
+  return (int)m->ev_used++;
+}
+
+static int prof_begin(nc_model* m, cudaStream_t st) {
+  if (!m->prof_on) return -1;
+  int e = prof_event(m);
+  if (e >= 0) cudaEventRecord(m->ev_pool[e], st);
+  return e;
+}
+
+static void prof_end(nc_model* m, int e0, int cls, double flops, double bytes, cudaStream_t st) {
+  if (!m->prof_on || e0 < 0) return;
+  int e1 = prof_event(m);
+  if (e1 < 0) return;
+  cudaEventRecord(m->ev_pool[e1], st);
+  m->recs.push_back({cls, e0, flops, bytes});
+  (void)e1;
+}
+
+// Fold recorded event pairs into the per-class totals and recycle the events.
+static void prof_flush(nc_model* m) {
+  if (m->recs.empty()) { m->ev_used = 0; return; }
+  cudaEventSynchronize(m->ev_pool[m->ev_used - 1]);
+  for (const auto& r : m->recs) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, m->ev_pool[r.ev], m->ev_pool[r.ev + 1]) == cudaSuccess) {
+      m->prof_ms[r.cls] += ms;
+      m->prof_flops[r.cls] += r.flops;
+      m->prof_bytes[r.cls] += r.bytes;
+      m->prof_n[r.cls] += 1;
+    }
+  }
+  m->recs.clear();
+  m->ev_used = 0;
+}
+
+#define PROF(cls, flops, bytes, call)                                      \
+  do {                                                                     \
+    int e0_ = prof_begin(m, st);                                           \
+    nc_status s_ = (call);                                                 \
+    prof_end(m, e0_, (cls), (double)(flops), (double)(bytes), st);         \
+    if (s_ != NC_OK) return s_;                                            \
+  } while (0)
+
+// ------------------------------------------------------------------ helpers
+
+static nc_status dalloc(nc_model* m, size_t bytes, void** out) {
+  void* p = nullptr;
+  if (bytes == 0) bytes = 256;
+  if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    *out = nullptr;
+    return NC_ERR_ALLOC;
+  }
+  m->allocs.push_back(p);
+  *out = p;
+  return NC_OK;
+}
+template <typename T>
+static nc_status dalloc_t(nc_model* m, size_t count, T** out) {
+  void* p;
+  nc_status s = dalloc(m, count * sizeof(T), &p);
+  *out = (T*)p;
+  return s;
+}
+
+static const ParamTensor& tensor(const nc_model* m, int layer, int which) {
+  // which: 0 q, 1 k, 2 v, 3 o, 4 fc, 5 proj
+  return m->layout[1 + layer * 6 + which];
+}
+
+static nc_status gemm(nc_model* m, int M, int N, int K, const void* A, int64_t lda, int a_kmajor,
+                      const void* B, int64_t ldb, int b_kmajor, int ep, void* D, int64_t ldd, void* aux,
+                      int64_t ldaux, cudaStream_t st) {
+  m->launches += 1;
+  const double a = (double)m->act;
+  const double out = (ep == NC_EP_STORE_F32) ? 4.0 : (ep == NC_EP_ACCUM_F32) ? 8.0
+                   : (ep == NC_EP_STORE) ? a : 2.0 * a;
+  const double bytes = ((double)M * K + (double)N * K) * a + (double)M * N * out;
+  const double flops = 2.0 * M * N * K;
+  if (m->dtype == NC_BF16)
+    PROF(NC_PROF_GEMM, flops, bytes,
+         launch_gemm_tc(M, N, K, (const bf16*)A, lda, a_kmajor, (const bf16*)B, ldb, b_kmajor, ep, D, ldd, aux,
+                        ldaux, m->err, st));
+  else
+    PROF(NC_PROF_GEMM, flops, bytes,
+         launch_gemm_simt(NC_FP32, M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, ep, D, ldd, aux, ldaux, st));
+  return NC_OK;
+}
+
+static void* wptr(const nc_model* m, const ParamTensor& t) { return (uint8_t*)m->wact + t.off * m->act; }
+static uint8_t* layer_act(const nc_model* m, uint8_t* base, int l, int64_t width) {
+  return base + (size_t)l * m->Nmax * width * m->act;
+}
+
+// ------------------------------------------------------------------ config
+
+static nc_status validate(const nc_config* c, nc_config* out) {
+  if (!c) return NC_ERR_ARG;
+  nc_config k = *c;
+  if (k.rope_base <= 0.f) k.rope_base = 10000.f;
+  if (k.norm_eps < 0.f) k.norm_eps = FLT_EPSILON;
+  if (k.init_std <= 0.f) k.init_std = 0.02f;
+  if (k.depth <= 0 || k.n_embd <= 0 || k.n_head <= 0 || k.n_kv_head <= 0 || k.head_dim <= 0 ||
+      k.mlp_hidden <= 0 || k.vocab <= 0 || k.seq_len <= 0 || k.batch <= 0)
+    return NC_ERR_CONFIG;
+  if (k.dtype != NC_FP32 && k.dtype != NC_BF16) return NC_ERR_CONFIG;
+  if (k.n_embd != k.n_head * k.head_dim) return NC_ERR_CONFIG;
+  if (k.n_head % k.n_kv_head) return NC_ERR_CONFIG;
+  if (k.head_dim % 16 || k.head_dim > 256) return NC_ERR_CONFIG;
+  if (k.dtype == NC_BF16 && k.head_dim != 64 && k.head_dim != 128) return NC_ERR_CONFIG;
+  if (k.n_embd % 8 || k.mlp_hidden % 8 || k.vocab % 8) return NC_ERR_CONFIG;
+  if (k.n_embd > 8192) return NC_ERR_CONFIG;
+  if ((int64_t)k.batch * k.seq_len > (1 << 20)) return NC_ERR_CONFIG;
+  *out = k;
+  return NC_OK;
+}
+
+static void build_layout(nc_model* m) {
+  int64_t off = 0;
+  auto add = [&](const std::string& n, int64_t r, int64_t c) {
+    m->layout.push_back({n, r, c, off});
+    off += r * c;
+  };
+  add("wte", m->V, m->C);
+  for (int l = 0; l < m->L; ++l) {
+    std::string p = "h" + std::to_string(l) + ".";
+    add(p + "wq", (int64_t)m->H * m->hd, m->C);
+    add(p + "wk", (int64_t)m->Hkv * m->hd, m->C);
+    add(p + "wv", (int64_t)m->Hkv * m->hd, m->C);
+    add(p + "wo", m->C, (int64_t)m->H * m->hd);
+    add(p + "wfc", m->F, m->C);
+    add(p + "wproj", m->C, m->F);
+  }
+  add("lm_head", m->V, m->C);
+  m->P = off;
+}
+
+static nc_status allocate(nc_model* m) {
+  const int64_t N = m->Nmax;
+  const size_t a = m->act;
+  const int L = m->L;
+  NC_TRY(dalloc_t(m, (size_t)m->P, &m->master));
+  if (m->dtype == NC_BF16) NC_TRY(dalloc(m, (size_t)m->P * 2, &m->wact));
+  else m->wact = m->master;
+  NC_TRY(dalloc_t(m, (size_t)m->Tmax * m->hd, &m->rope_tab));
+  NC_TRY(dalloc_t(m, 4, &m->err));
+  NC_TRY(dalloc_t(m, 4, &m->result));
+  if (cudaMallocHost((void**)&m->result_host, 16) != cudaSuccess) { cudaGetLastError(); return NC_ERR_ALLOC; }
+  NC_TRY(dalloc_t(m, (size_t)N * m->C, &m->x));
+  NC_TRY(dalloc(m, (size_t)L * N * m->C * a, (void**)&m->xn1));
+  NC_TRY(dalloc(m, (size_t)L * N * m->C * a, (void**)&m->xn2));
+  NC_TRY(dalloc(m, (size_t)L * N * m->qkvw * a, (void**)&m->qkv));
+  NC_TRY(dalloc(m, (size_t)L * N * m->H * m->hd * a, (void**)&m->o));
+  NC_TRY(dalloc(m, (size_t)L * N * m->F * a, (void**)&m->r));
+  NC_TRY(dalloc(m, (size_t)L * N * m->F * a, (void**)&m->h));
+  NC_TRY(dalloc_t(m, (size_t)L * N, &m->rstd1));
+  NC_TRY(dalloc_t(m, (size_t)L * N, &m->rstd2));
+  NC_TRY(dalloc_t(m, (size_t)L * N * (m->H + m->Hkv), &m->rstdqk));
+  NC_TRY(dalloc_t(m, (size_t)L * N * m->H, &m->lse));
+  NC_TRY(dalloc(m, (size_t)N * m->C * a, &m->xf));
+  NC_TRY(dalloc_t(m, (size_t)N, &m->rstd_f));
+  // logits chunk: at most 1 GiB of compute-dtype logits per chunk, whole 128-row tiles
+  int64_t rows = ((int64_t)1 << 30) / ((int64_t)m->V * (int64_t)a);
+  rows = std::max<int64_t>(128, rows / 128 * 128);
+  m->chunk_rows = std::min<int64_t>(rows, N);
+  NC_TRY(dalloc(m, (size_t)m->chunk_rows * m->V * a, &m->logits));
+  NC_TRY(dalloc_t(m, (size_t)N, &m->rowloss));
+  NC_TRY(dalloc_t(m, (size_t)N * m->C, &m->dx));
+  if (m->dtype == NC_BF16) NC_TRY(dalloc(m, (size_t)N * m->C * a, &m->dx_act));
+  else m->dx_act = m->dx;
+  NC_TRY(dalloc(m, (size_t)N * m->F * a, &m->du));
+  NC_TRY(dalloc_t(m, (size_t)N * m->C, &m->dxn));
+  NC_TRY(dalloc(m, (size_t)N * m->H * m->hd * a, &m->dout));
+  NC_TRY(dalloc(m, (size_t)N * m->qkvw * a, &m->dqkv));
+  NC_TRY(dalloc_t(m, (size_t)N * m->H, &m->Dv));
+  NC_TRY(dalloc(m, embed_bwd_scratch_bytes(N, m->C, m->V), &m->emb_scratch));
+  NC_TRY(dalloc_t(m, (size_t)N, &m->tok_dev));
+  NC_TRY(dalloc_t(m, (size_t)N, &m->tgt_dev));
+  return NC_OK;
+}
+
+// ------------------------------------------------------------------ ABI: misc
+
+extern "C" const char* nc_status_string(nc_status s) {
+  switch (s) {
+    case NC_OK: return "ok";
+    case NC_ERR_CONFIG: return "invalid config";
+    case NC_ERR_ALLOC: return "device allocation failed";
+    case NC_ERR_ARG: return "invalid argument";
+    case NC_ERR_TOKEN_RANGE: return "token or target outside [0, vocab)";
+    case NC_ERR_CUDA: return "CUDA error";
+    case NC_ERR_TIMEOUT: return "bounded device wait expired";
+    case NC_ERR_UNSUPPORTED: return "unsupported shape or mode";
+  }
+  return "unknown status";
+}
+
+extern "C" const char* nc_version(void) { return "libnc 0.1 sm_103a (tcgen05 GEMM, SIMT attention)"; }
+
+extern "C" void nc_model_destroy(nc_model* m) {
+  if (!m) return;
+  for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
+  for (void* p : m->allocs) cudaFree(p);
+  if (m->result_host) cudaFreeHost(m->result_host);
+  delete m;
+}
+
+extern "C" nc_status nc_model_create(const nc_config* cfg, uint64_t seed, nc_model** out) {
+  if (!out) return NC_ERR_ARG;
+  *out = nullptr;
+  nc_config c;
+  NC_TRY(validate(cfg, &c));
+  nc_model* m = new (std::nothrow) nc_model();
+  if (!m) return NC_ERR_ALLOC;
+  m->cfg = c;
+  m->L = c.depth; m->C = c.n_embd; m->H = c.n_head; m->Hkv = c.n_kv_head; m->hd = c.head_dim;
+  m->F = c.mlp_hidden; m->V = c.vocab; m->Tmax = c.seq_len; m->Bmax = c.batch;
+  m->qkvw = (m->H + 2 * m->Hkv) * m->hd;
+  m->dtype = c.dtype;
+  m->act = (c.dtype == NC_BF16) ? 2 : 4;
+  m->Nmax = (int64_t)c.batch * c.seq_len;
+  build_layout(m);
+  nc_status s = allocate(m);
+  cudaStream_t st = 0;
+  if (s == NC_OK) {
+    for (size_t j = 0; j < m->layout.size() && s == NC_OK; ++j) {
+      const ParamTensor& t = m->layout[j];
+      s = launch_init_normal(m->master + t.off, t.rows * t.cols, seed, (int)j, c.init_std, st);
+    }
+  }
+  if (s == NC_OK) s = launch_rope_table(m->Tmax, m->hd, c.rope_base, m->rope_tab, st);
+  if (s == NC_OK && cudaMemsetAsync(m->err, 0, sizeof(int32_t), st) != cudaSuccess) s = NC_ERR_CUDA;
+  if (s == NC_OK && cudaStreamSynchronize(st) != cudaSuccess) s = NC_ERR_CUDA;
+  if (s != NC_OK) {
+    nc_model_destroy(m);
+    return s;
+  }
+  *out = m;
+  return NC_OK;
+}
+
+extern "C" nc_status nc_model_config(const nc_model* m, nc_config* out) {
+  if (!m || !out) return NC_ERR_ARG;
+  *out = m->cfg;
+  return NC_OK;
+}
+
+extern "C" nc_status nc_param_count(const nc_model* m, int32_t* n_tensors, int64_t* n_elems) {
+  if (!m) return NC_ERR_ARG;
+  if (n_tensors) *n_tensors = (int32_t)m->layout.size();
+  if (n_elems) *n_elems = m->P;
+  return NC_OK;
+}
+
+extern "C" nc_status nc_param_info(const nc_model* m, int32_t i, const char** name, int64_t* rows, int64_t* cols,
+                                   int64_t* offset) {
+  if (!m || i < 0 || i >= (int32_t)m->layout.size()) return NC_ERR_ARG;
+  const ParamTensor& t = m->layout[i];
+  if (name) *name = t.name.c_str();
+  if (rows) *rows = t.rows;
+  if (cols) *cols = t.cols;
+  if (offset) *offset = t.off;
+  return NC_OK;
+}
+
+extern "C" nc_status nc_get_params(const nc_model* m, float* dst, void* stream) {
+  if (!m || !dst) return NC_ERR_ARG;
+  NC_CUDA_TRY(cudaMemcpyAsync(dst, m->master, (size_t)m->P * 4, cudaMemcpyDeviceToDevice, as_stream(stream)));
+  return NC_OK;
+}
+
+extern "C" nc_status nc_set_params(nc_model* m, const float* src, void* stream) {
+  if (!m || !src) return NC_ERR_ARG;
+  NC_CUDA_TRY(cudaMemcpyAsync(m->master, src, (size_t)m->P * 4, cudaMemcpyDeviceToDevice, as_stream(stream)));
+  return NC_OK;
+}
+
+extern "C" int64_t nc_last_launch_count(const nc_model* m) { return m ? m->launches : 0; }
+
+static nc_status read_flag_status(nc_model* m, cudaStream_t st) {
+  NC_CUDA_TRY(cudaMemcpyAsync(m->result_host + 1, m->err, 4, cudaMemcpyDeviceToHost, st));
+  NC_CUDA_TRY(cudaStreamSynchronize(st));
+  int32_t f;
+  memcpy(&f, m->result_host + 1, 4);
+  NC_CUDA_TRY(cudaMemsetAsync(m->err, 0, 4, st));
+  if (f & NC_DEVERR_TIMEOUT) return NC_ERR_TIMEOUT;
+  if (f & NC_DEVERR_TOKEN) return NC_ERR_TOKEN_RANGE;
+  return NC_OK;
+}
+
+extern "C" nc_status nc_last_error(nc_model* m, void* stream) {
+  if (!m) return NC_ERR_ARG;
+  return read_flag_status(m, as_stream(stream));
+}
+
+// ------------------------------------------------------------------ the step
+
+static nc_status check_bt(const nc_model* m, int32_t B, int32_t T) {
+  if (B < 1 || B > m->Bmax || T < 1 || T > m->Tmax) return NC_ERR_ARG;
+  return NC_OK;
+}
+
+// Weight cast, embedding and all L blocks; leaves xf = norm(x) and rstd_f.
+static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T, cudaStream_t st) {
+  const int64_t N = (int64_t)B * T;
+  const int C = m->C, F = m->F, Hd = m->H * m->hd, W = m->qkvw;
+  const float eps = m->cfg.norm_eps;
+  if (m->dtype == NC_BF16) {
+    // every tensor except wte is read by a GEMM in bf16
+    const ParamTensor& w0 = m->layout[1];
+    PROF(NC_PROF_CAST, 0, 6.0 * (m->P - w0.off),
+         launch_cast_bf16(m->master + w0.off, (bf16*)m->wact + w0.off, m->P - w0.off, st));
+    m->launches += 1;
+  }
+  PROF(NC_PROF_EMBED, 0, (double)N * (8.0 * C + 4),
+       launch_embed_fwd(m->dtype, N, C, m->V, tokens, m->master, m->x, m->err, st));
+  m->launches += 1;
+  const double a = (double)m->act;
+  const int nh = m->H + m->Hkv;
+  const double attn_fl = 4.0 * B * m->H * m->hd * ((double)T * (T + 1) / 2.0);
+  const double nrm_by = (double)N * (4.0 * C + a * C + 4);
+  for (int l = 0; l < m->L; ++l) {
+    uint8_t* xn1 = layer_act(m, m->xn1, l, C);
+    uint8_t* xn2 = layer_act(m, m->xn2, l, C);
+    uint8_t* qkv = layer_act(m, m->qkv, l, W);
+    uint8_t* o = layer_act(m, m->o, l, Hd);
+    uint8_t* r = layer_act(m, m->r, l, F);
+    uint8_t* h = layer_act(m, m->h, l, F);
+    float* rstd1 = m->rstd1 + (size_t)l * m->Nmax;
+    float* rstd2 = m->rstd2 + (size_t)l * m->Nmax;
+    float* rstdqk = m->rstdqk + (size_t)l * m->Nmax * (m->H + m->Hkv);
+    float* lse = m->lse + (size_t)l * m->Nmax * m->H;
+    PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn1, rstd1, eps, st));
+    NC_TRY(gemm(m, (int)N, W, C, xn1, C, 1, wptr(m, tensor(m, l, 0)), C, 1, NC_EP_STORE, qkv, W, nullptr, 0, st));
+    PROF(NC_PROF_ROPE, 0, (double)N * nh * (2.0 * a * m->hd + 4),
+         launch_rope_qknorm_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, rstdqk, m->rope_tab, eps, st));
+    PROF(NC_PROF_ATTN_FWD, attn_fl, (double)N * (W + Hd) * a + 4.0 * N * m->H,
+         launch_attn_fwd_simt(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, st));
+    NC_TRY(gemm(m, (int)N, C, Hd, o, Hd, 1, wptr(m, tensor(m, l, 3)), Hd, 1, NC_EP_ACCUM_F32, m->x, C, nullptr, 0,
+                st));
+    PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn2, rstd2, eps, st));
+    NC_TRY(gemm(m, (int)N, F, C, xn2, C, 1, wptr(m, tensor(m, l, 4)), C, 1, NC_EP_RELU2, r, F, h, F, st));
+    NC_TRY(gemm(m, (int)N, C, F, h, F, 1, wptr(m, tensor(m, l, 5)), F, 1, NC_EP_ACCUM_F32, m->x, C, nullptr, 0, st));
+    m->launches += 4;
+  }
+  PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, m->xf, m->rstd_f, eps, st));
+  m->launches += 1;
+  return NC_OK;
+}
+
+static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int T, float* grads, cudaStream_t st) {
+  const int64_t N = (int64_t)B * T;
+  const int C = m->C, F = m->F, Hd = m->H * m->hd, W = m->qkvw;
+  const int n = (int)N;
+  const double a = (double)m->act;
+  const int nh = m->H + m->Hkv;
+  const double attn_fl = 8.0 * B * m->H * m->hd * ((double)T * (T + 1) / 2.0);
+  const double nb_by = (double)N * (4.0 * C + a * C + 4 + 8.0 * C + (m->dtype == NC_BF16 ? a * C : 0));
+  for (int l = m->L - 1; l >= 0; --l) {
+    uint8_t* xn1 = layer_act(m, m->xn1, l, C);
+    uint8_t* xn2 = layer_act(m, m->xn2, l, C);
+    uint8_t* qkv = layer_act(m, m->qkv, l, W);
+    uint8_t* o = layer_act(m, m->o, l, Hd);
+    uint8_t* r = layer_act(m, m->r, l, F);
+    uint8_t* h = layer_act(m, m->h, l, F);
+    float* rstd1 = m->rstd1 + (size_t)l * m->Nmax;
+    float* rstd2 = m->rstd2 + (size_t)l * m->Nmax;
+    float* rstdqk = m->rstdqk + (size_t)l * m->Nmax * (m->H + m->Hkv);
+    float* lse = m->lse + (size_t)l * m->Nmax * m->H;
+    const ParamTensor &tq = tensor(m, l, 0), &to = tensor(m, l, 3), &tfc = tensor(m, l, 4),
+                      &tpj = tensor(m, l, 5);
+    // MLP: x2 = x1 + relu(xn2 Wfc^T)^2 Wproj^T
+    NC_TRY(gemm(m, C, F, n, m->dx_act, C, 0, h, F, 0, NC_EP_STORE_F32, grads + tpj.off, F, nullptr, 0, st));
+    NC_TRY(gemm(m, n, F, C, m->dx_act, C, 1, wptr(m, tpj), F, 0, NC_EP_RELU2_BWD, m->du, F, r, F, st));
+    NC_TRY(gemm(m, F, C, n, m->du, F, 0, xn2, C, 0, NC_EP_STORE_F32, grads + tfc.off, C, nullptr, 0, st));
+    NC_TRY(gemm(m, n, C, F, m->du, F, 1, wptr(m, tfc), C, 0, NC_EP_STORE_F32, m->dxn, C, nullptr, 0, st));
+    PROF(NC_PROF_NORM, 0, nb_by,
+         launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, xn2, rstd2, m->dx, m->dtype == NC_BF16 ? m->dx_act : nullptr,
+                            st));
+    // attention: x1 = x + o Wo^T
+    NC_TRY(gemm(m, C, Hd, n, m->dx_act, C, 0, o, Hd, 0, NC_EP_STORE_F32, grads + to.off, Hd, nullptr, 0, st));
+    NC_TRY(gemm(m, n, Hd, C, m->dx_act, C, 1, wptr(m, to), Hd, 0, NC_EP_STORE, m->dout, Hd, nullptr, 0, st));
+    PROF(NC_PROF_ATTN_BWD, attn_fl, (double)N * (2.0 * W + 2.0 * Hd) * a + 8.0 * N * m->H,
+         launch_attn_bwd_simt(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, st));
+    PROF(NC_PROF_ROPE, 0, (double)N * nh * (3.0 * a * m->hd + 4),
+         launch_rope_qknorm_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, m->dqkv, qkv, rstdqk, m->rope_tab, st));
+    NC_TRY(gemm(m, W, C, n, m->dqkv, W, 0, xn1, C, 0, NC_EP_STORE_F32, grads + tq.off, C, nullptr, 0, st));
+    NC_TRY(gemm(m, n, C, W, m->dqkv, W, 1, wptr(m, tq), C, 0, NC_EP_STORE_F32, m->dxn, C, nullptr, 0, st));
+    PROF(NC_PROF_NORM, 0, nb_by,
+         launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, xn1, rstd1, m->dx, m->dtype == NC_BF16 ? m->dx_act : nullptr,
+                            st));
+    m->launches += 3 + 1 + 2;
+  }
+  const ParamTensor& te = m->layout[0];
+  PROF(NC_PROF_EMBED, 0, 4.0 * N * C + 4.0 * m->V * C,
+       launch_embed_bwd(N, C, m->V, tokens, m->dx, grads + te.off, m->emb_scratch, st));
+  m->launches += 4;
+  return NC_OK;
+}
+
+static nc_status step(nc_model* m, const int32_t* tokens, const int32_t* targets, int B, int T, float* loss_host,
+                      float* grads, cudaStream_t st) {
+  const int64_t N = (int64_t)B * T;
+  const int C = m->C, V = m->V;
+  m->launches = 0;
+  prof_flush(m);
+  NC_TRY(forward_trunk(m, tokens, B, T, st));
+  const ParamTensor& tl = m->layout.back();
+  const void* Wlm = wptr(m, tl);
+  NC_CUDA_TRY(cudaMemsetAsync(m->dx, 0, (size_t)N * C * sizeof(float), st));
+  const float scale = 1.f / (float)N;
+  for (int64_t c0 = 0; c0 < N; c0 += m->chunk_rows) {
+    const int nc = (int)std::min<int64_t>(m->chunk_rows, N - c0);
+    const void* xfc = (const uint8_t*)m->xf + (size_t)c0 * C * m->act;
+    NC_TRY(gemm(m, nc, V, C, xfc, C, 1, Wlm, C, 1, NC_EP_STORE, m->logits, V, nullptr, 0, st));
+    PROF(NC_PROF_CE, 0, (double)nc * (2.0 * V * m->act + 8),
+         launch_cross_entropy(m->dtype, nc, V, m->logits, V, targets + c0, m->rowloss + c0, scale, m->err, st));
+    NC_TRY(gemm(m, nc, C, V, m->logits, V, 1, Wlm, C, 0, NC_EP_STORE_F32, m->dxn + c0 * C, C, nullptr, 0, st));
+    NC_TRY(gemm(m, V, C, nc, m->logits, V, 0, xfc, C, 0, c0 == 0 ? NC_EP_STORE_F32 : NC_EP_ACCUM_F32,
+                grads + tl.off, C, nullptr, 0, st));
+    m->launches += 1;
+  }
+  PROF(NC_PROF_NORM, 0, (double)N * (4.0 * C + m->act * C + 4 + 8.0 * C + (m->dtype == NC_BF16 ? m->act * C : 0)),
+       launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, m->xf, m->rstd_f, m->dx, m->dtype == NC_BF16 ? m->dx_act : nullptr,
+                          st));
+  m->launches += 1;
+  NC_TRY(backward_layers(m, tokens, B, T, grads, st));
+  PROF(NC_PROF_OTHER, 0, 4.0 * N, launch_mean(N, m->rowloss, m->result, st));
+  m->launches += 1;
+  NC_CUDA_TRY(cudaMemcpyAsync(m->result_host, m->result, 4, cudaMemcpyDeviceToHost, st));
+  nc_status s = read_flag_status(m, st);   // synchronises the stream
+  if (loss_host) memcpy(loss_host, m->result_host, 4);
+  return s;
+}
+
+extern "C" nc_status nc_forward_backward(nc_model* m, const int32_t* tokens, const int32_t* targets, int32_t B,
+                                         int32_t T, float* loss_host, float* grads, void* stream) {
+  if (!m || !tokens || !targets || !loss_host || !grads) return NC_ERR_ARG;
+  NC_TRY(check_bt(m, B, T));
+  return step(m, tokens, targets, B, T, loss_host, grads, as_stream(stream));
+}
+
+extern "C" nc_status nc_forward_backward_host(nc_model* m, const int32_t* tokens_host, const int32_t* targets_host,
+                                              int32_t B, int32_t T, float* loss_host, float* grads, void* stream) {
+  if (!m || !tokens_host || !targets_host || !loss_host || !grads) return NC_ERR_ARG;
+  NC_TRY(check_bt(m, B, T));
+  cudaStream_t st = as_stream(stream);
+  size_t bytes = (size_t)B * T * sizeof(int32_t);
+  NC_CUDA_TRY(cudaMemcpyAsync(m->tok_dev, tokens_host, bytes, cudaMemcpyHostToDevice, st));
+  NC_CUDA_TRY(cudaMemcpyAsync(m->tgt_dev, targets_host, bytes, cudaMemcpyHostToDevice, st));
+  return step(m, m->tok_dev, m->tgt_dev, B, T, loss_host, grads, st);
+}
+
+extern "C" nc_status nc_forward_logits(nc_model* m, const int32_t* tokens, int32_t B, int32_t T, float* logits,
+                                       void* stream) {
+  if (!m || !tokens || !logits) return NC_ERR_ARG;
+  NC_TRY(check_bt(m, B, T));
+  cudaStream_t st = as_stream(stream);
+  m->launches = 0;
+  NC_TRY(forward_trunk(m, tokens, B, T, st));
+  const int64_t N = (int64_t)B * T;
+  NC_TRY(gemm(m, (int)N, m->V, m->C, m->xf, m->C, 1, wptr(m, m->layout.back()), m->C, 1, NC_EP_STORE_F32, logits,
+              m->V, nullptr, 0, st));
+  return NC_OK;
+}
+
+extern "C" nc_status nc_forward_row_losses(nc_model* m, const int32_t* tokens, const int32_t* targets, int32_t B,
+                                           int32_t T, float* losses, void* stream) {
+  if (!m || !tokens || !targets || !losses) return NC_ERR_ARG;
+  NC_TRY(check_bt(m, B, T));
+  cudaStream_t st = as_stream(stream);
+  m->launches = 0;
+  NC_TRY(forward_trunk(m, tokens, B, T, st));
+  const int64_t N = (int64_t)B * T;
+  for (int64_t c0 = 0; c0 < N; c0 += m->chunk_rows) {
+    const int nc = (int)std::min<int64_t>(m->chunk_rows, N - c0);
+    const void* xfc = (const uint8_t*)m->xf + (size_t)c0 * m->C * m->act;
+    NC_TRY(gemm(m, nc, m->V, m->C, xfc, m->C, 1, wptr(m, m->layout.back()), m->C, 1, NC_EP_STORE, m->logits, m->V,
+                nullptr, 0, st));
+    NC_TRY(launch_cross_entropy(m->dtype, nc, m->V, m->logits, m->V, targets + c0, losses + c0, 1.f, m->err, st));
+  }
+  return NC_OK;
+}
+
+// ------------------------------------------------------------------ kernel-level entry points
+
+static bool dtype_ok(int32_t d) { return d == NC_FP32 || d == NC_BF16; }
+
+extern "C" nc_status nc_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A, int64_t lda,
+                                int32_t a_kmajor, const void* B, int64_t ldb, int32_t b_kmajor, int32_t ep, void* D,
+                                int64_t ldd, void* aux, int64_t ldaux, void* stream) {
+  if (!dtype_ok(dtype) || !A || !B || !D || ep < 0 || ep > NC_EP_RELU2_BWD) return NC_ERR_ARG;
+  if (M < 0 || N < 0 || K < 0) return NC_ERR_ARG;
+  if (dtype == NC_BF16)
+    return launch_gemm_tc(M, N, K, (const bf16*)A, lda, a_kmajor, (const bf16*)B, ldb, b_kmajor, ep, D, ldd, aux,
+                          ldaux, nullptr, as_stream(stream));
+  return launch_gemm_simt(dtype, M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, ep, D, ldd, aux, ldaux,
+                          as_stream(stream));
+}
+
+extern "C" nc_status nc_op_rmsnorm_fwd(int32_t dtype, int64_t rows, int32_t C, const float* x, void* y, float* rstd,
+                                       float eps, void* stream) {
+  if (!dtype_ok(dtype) || !x || !y || !rstd || C <= 0) return NC_ERR_ARG;
+  return launch_rmsnorm_fwd(dtype, rows, C, x, y, rstd, eps, as_stream(stream));
+}
+
+extern "C" nc_status nc_op_rmsnorm_bwd(int32_t dtype, int64_t rows, int32_t C, const float* dy, const void* y,
+                                       const float* rstd, float* dx, void* dx_act, void* stream) {
+  if (!dtype_ok(dtype) || !dy || !y || !rstd || !dx || C <= 0) return NC_ERR_ARG;
+  return launch_rmsnorm_bwd(dtype, rows, C, dy, y, rstd, dx, dx_act, as_stream(stream));
+}
+
+extern "C" nc_status nc_op_rope_table(int32_t T, int32_t hd, float rope_base, float* cos_sin, void* stream) {
+  return launch_rope_table(T, hd, rope_base, cos_sin, as_stream(stream));
+}
+
+extern "C" nc_status nc_op_rope_qknorm_fwd(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
+                                           void* qkv, float* rstd, const float* cos_sin, float eps, void* stream) {
+  if (!dtype_ok(dtype) || !qkv || !rstd || !cos_sin || B <= 0 || T <= 0 || H <= 0 || Hkv <= 0) return NC_ERR_ARG;
+  return launch_rope_qknorm_fwd(dtype, B, T, H, Hkv, hd, qkv, rstd, cos_sin, eps, as_stream(stream));
+}
+
+extern "C" nc_status nc_op_rope_qknorm_bwd(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
+                                           void* dqkv, const void* qkv, const float* rstd, const float* cos_sin,
+                                           void* stream) {
+  if (!dtype_ok(dtype) || !dqkv || !qkv || !rstd || !cos_sin || B <= 0 || T <= 0 || H <= 0 || Hkv <= 0)
+    return NC_ERR_ARG;
+  return launch_rope_qknorm_bwd(dtype, B, T, H, Hkv, hd, dqkv, qkv, rstd, cos_sin, as_stream(stream));
+}
+
+extern "C" nc_status nc_op_attention_fwd(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
+                                         const void* qkv, void* o, float* lse, void* stream) {
+  if (!dtype_ok(dtype) || !qkv || !o || !lse) return NC_ERR_ARG;
+  return launch_attn_fwd_simt(dtype, B, T, H, Hkv, hd, qkv, o, lse, as_stream(stream));
+}
+
+extern "C" nc_status nc_op_attention_bwd(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
+                                         const void* qkv, const void* o, const float* lse, const void* do_,
+                                         void* dqkv, float* workspace, void* stream) {
+  if (!dtype_ok(dtype) || !qkv || !o || !lse || !do_ || !dqkv || !workspace) return NC_ERR_ARG;
+  return launch_attn_bwd_simt(dtype, B, T, H, Hkv, hd, qkv, o, lse, do_, dqkv, workspace, as_stream(stream));
+}
+
+extern "C" nc_status nc_op_cross_entropy(int32_t dtype, int64_t rows, int32_t V, void* z, const int32_t* targets,
+                                         float* row_loss, float grad_scale, int32_t* err_dev, void* stream) {
+  if (!dtype_ok(dtype) || !z || !targets || !row_loss || V <= 0) return NC_ERR_ARG;
+  return launch_cross_entropy(dtype, rows, V, z, V, targets, row_loss, grad_scale, err_dev, as_stream(stream));
+}
+
+extern "C" nc_status nc_op_embed_fwd(int32_t dtype, int64_t n, int32_t C, int32_t V, const int32_t* tokens,
+                                     const float* wte, float* x, int32_t* err_dev, void* stream) {
+  if (!dtype_ok(dtype) || !tokens || !wte || !x || C <= 0 || V <= 0) return NC_ERR_ARG;
+  return launch_embed_fwd(dtype, n, C, V, tokens, wte, x, err_dev, as_stream(stream));
+}
+
+extern "C" size_t nc_embed_bwd_scratch_bytes(int64_t n, int32_t C, int32_t V) {
+  return embed_bwd_scratch_bytes(n, C, V);
+}
+
+extern "C" nc_status nc_op_embed_bwd(int64_t n, int32_t C, int32_t V, const int32_t* tokens, const float* dx,
+                                     float* dwte, void* scratch, void* stream) {
+  if (!tokens || !dx || !dwte || !scratch || n < 0) return NC_ERR_ARG;
+  return launch_embed_bwd(n, C, V, tokens, dx, dwte, scratch, as_stream(stream));
+}
+
+extern "C" nc_status nc_profile_enable(nc_model* m, int32_t on) {
+  if (!m) return NC_ERR_ARG;
+  prof_flush(m);
+  for (int c = 0; c < NC_PROF_CLASSES; ++c) {
+    m->prof_ms[c] = m->prof_flops[c] = m->prof_bytes[c] = 0.0;
+    m->prof_n[c] = 0;
+  }
+  m->prof_on = on != 0;
+  return NC_OK;
+}
+
+extern "C" nc_status nc_profile_read(nc_model* m, int32_t cls, double* ms, int64_t* launches, double* flops,
+                                     double* bytes) {
+  if (!m || cls < 0 || cls >= NC_PROF_CLASSES) return NC_ERR_ARG;
+  prof_flush(m);
+  if (ms) *ms = m->prof_ms[cls];
+  if (launches) *launches = m->prof_n[cls];
+  if (flops) *flops = m->prof_flops[cls];
+  if (bytes) *bytes = m->prof_bytes[cls];
+  return NC_OK;
+}
+
+// Test hook: the time limit (ns) of every bounded wait in the tensor-core kernels.
+extern "C" void nc_debug_set_wait_limit_ns(uint64_t ns) { g_tc_wait_ns = ns; }

@@ -1,0 +1,43 @@
+// Launch functions of every kernel of the step (host side, enqueue only).
+#pragma once
+#include <algorithm>
+#include "nc_common.cuh"
+
+nc_status launch_init_normal(float* out, int64_t count, uint64_t seed, int tensor_index, float std,
+                             cudaStream_t st);
+nc_status launch_cast_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t st);
+nc_status launch_rope_table(int T, int hd, float base, float* tab, cudaStream_t st);
+
+nc_status launch_rmsnorm_fwd(int dtype, int64_t rows, int C, const float* x, void* y, float* rstd,
+                             float eps, cudaStream_t st);
+nc_status launch_rmsnorm_bwd(int dtype, int64_t rows, int C, const float* dy, const void* y,
+                             const float* rstd, float* dx, void* dx_act, cudaStream_t st);
+nc_status launch_rope_qknorm_fwd(int dtype, int B, int T, int H, int Hkv, int hd, void* qkv,
+                                 float* rstd, const float* tab, float eps, cudaStream_t st);
+nc_status launch_rope_qknorm_bwd(int dtype, int B, int T, int H, int Hkv, int hd, void* dqkv,
+                                 const void* qkv, const float* rstd, const float* tab,
+                                 cudaStream_t st);
+
+nc_status launch_embed_fwd(int dtype, int64_t n, int C, int V, const int32_t* tokens,
+                           const float* wte, float* x, int32_t* err, cudaStream_t st);
+size_t embed_bwd_scratch_bytes(int64_t n, int C, int V);
+nc_status launch_embed_bwd(int64_t n, int C, int V, const int32_t* tokens, const float* dx,
+                           float* dwte, void* scratch, cudaStream_t st);
+nc_status launch_cross_entropy(int dtype, int64_t rows, int V, void* z, int64_t ldz,
+                               const int32_t* targets, float* row_loss, float scale, int32_t* err,
+                               cudaStream_t st);
+nc_status launch_mean(int64_t n, const float* x, float* out, cudaStream_t st);
+
+nc_status launch_gemm_simt(int dtype, int M, int N, int K, const void* A, int64_t lda, int a_kmajor,
+                           const void* B, int64_t ldb, int b_kmajor, int ep, void* D, int64_t ldd,
+                           void* aux, int64_t ldaux, cudaStream_t st);
+// tcgen05 tensor-core GEMM (bf16 operands, fp32 accumulation in TMEM).
+nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_kmajor,
+                         const bf16* B, int64_t ldb, int b_kmajor, int ep, void* D, int64_t ldd,
+                         void* aux, int64_t ldaux, int32_t* err, cudaStream_t st);
+
+nc_status launch_attn_fwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv, void* o,
+                               float* lse, cudaStream_t st);
+nc_status launch_attn_bwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv,
+                               const void* o, const float* lse, const void* dout, void* dqkv, float* Dv,
+                               cudaStream_t st);

@@ -1,0 +1,259 @@
+/*
+ * nc.h -- C ABI of libnc: one forward+backward training step of a
+ * nanochat-style decoder-only GPT on one NVIDIA B300 (sm_103a).
+ *
+ * The model (all citations are to the nanochat pages this library restates):
+ *   - token embedding `wte` and an untied output head `lm_head`
+ *     (cosmicrealm "noao-chat-0-项目总体介绍" §2.1 item 3);
+ *   - per block, pre-norm: a = norm(x); q,k,v = a Wq^T, a Wk^T, a Wv^T
+ *     (bias-free, §2.1 item 5); half-split RoPE on q and k (§2.1 item 1:
+ *     y1 = x1 cos + x2 sin, y2 = -x1 sin + x2 cos), then RMSNorm of q and k
+ *     per head (§2.1 item 2); causal attention with grouped-query heads
+ *     (§2.1 item 6; query head h reads kv head h / (n_head / n_kv_head));
+ *     x += o Wo^T; x += relu(norm(x) Wfc^T)^2 Wproj^T (§2.1 item 4, with the
+ *     4x hidden layer of woshipm nanochat analysis §五.1);
+ *   - norm() is RMSNorm without gain, y = x / sqrt(mean(x^2) + eps)
+ *     (§2.1 item 5); a final norm precedes lm_head;
+ *   - loss: mean next-token cross-entropy over all B*T positions
+ *     (devpress "用不到100美元，亲手训练一个属于你的GPT-2" §2.2 item 2);
+ *   - fp32 master weights, cast to the compute dtype in the forward
+ *     (devpress §4.2 "精度管理"; feinterview "nanochat：低成本跑通大模型训练全流程").
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_dev are CUDA device pointers owned by the caller;
+ *     *_host are host pointers owned by the caller.  Nothing is retained
+ *     after a call returns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued on it; only calls that write a host pointer synchronise it.
+ *   - Matrices are row-major with the last index contiguous.  Linear
+ *     weights are stored W[out][in] and applied as y = x W^T.
+ *   - Errors are returned as nc_status; no call aborts the process.  A
+ *     model is not thread-safe: use one model per host thread / stream.
+ */
+#ifndef NC_H
+#define NC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { NC_FP32 = 0, NC_BF16 = 1 };
+
+typedef struct {
+  int32_t depth;       /* number of blocks L                                  */
+  int32_t n_embd;      /* residual width C = n_head * head_dim                */
+  int32_t n_head;      /* query heads H                                       */
+  int32_t n_kv_head;   /* key/value heads Hkv, H % Hkv == 0                   */
+  int32_t head_dim;    /* hd; even; 64 or 128 in NC_BF16 mode                 */
+  int32_t mlp_hidden;  /* F, the MLP width (4 * n_embd in the pages)          */
+  int32_t vocab;       /* V                                                   */
+  int32_t seq_len;     /* maximum T per call                                  */
+  int32_t batch;       /* maximum B per call                                  */
+  int32_t dtype;       /* compute dtype: NC_FP32 or NC_BF16                   */
+  float rope_base;     /* RoPE base; 10000 when <= 0                          */
+  float norm_eps;      /* RMSNorm eps; FLT_EPSILON when < 0                   */
+  float init_std;      /* std of the N(0, std) init; 0.02 when <= 0           */
+} nc_config;
+
+typedef struct nc_model nc_model;
+
+typedef enum {
+  NC_OK = 0,
+  NC_ERR_CONFIG = 1,       /* invalid nc_config                                  */
+  NC_ERR_ALLOC = 2,        /* device allocation failed                           */
+  NC_ERR_ARG = 3,          /* NULL pointer, bad size or index                    */
+  NC_ERR_TOKEN_RANGE = 4,  /* a token or target outside [0, vocab)               */
+  NC_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed                  */
+  NC_ERR_TIMEOUT = 6,      /* a bounded device-side wait expired                 */
+  NC_ERR_UNSUPPORTED = 7   /* shape or mode this build does not implement        */
+} nc_status;
+
+/* Human-readable name of a status.  Never NULL. */
+const char* nc_status_string(nc_status s);
+
+/* Version string of this build (kernel set and target architecture). */
+const char* nc_version(void);
+
+/* ------------------------------------------------------------------------
+ * Model lifetime.
+ * nc_model_create validates `cfg`, allocates fp32 master weights (packed,
+ * see nc_param_info), the compute-dtype weight copy and the activation
+ * workspace for batch*seq_len tokens, and initialises every weight i.i.d.
+ * N(0, init_std) from `seed` with the counter-based draw: SplitMix64
+ * (Steele, Lea & Flood 2014), tensor j of the packed order using the stream
+ * whose state starts at seed ^ ((j+1) * 0x9E3779B97F4A7C15), element e taking
+ * output e; Box-Muller on (top 24 bits, bits 16..39) + 0.5 over 2^24 in fp64,
+ * rounded once to float32.  Synchronous.  On failure *out is NULL.
+ * ---------------------------------------------------------------------- */
+nc_status nc_model_create(const nc_config* cfg, uint64_t seed, nc_model** out);
+void nc_model_destroy(nc_model* m);
+nc_status nc_model_config(const nc_model* m, nc_config* cfg_out);
+
+/* Packed parameter layout: wte[V,C]; per layer l: Wq[H*hd,C], Wk[Hkv*hd,C],
+ * Wv[Hkv*hd,C], Wo[C,H*hd], Wfc[F,C], Wproj[C,F]; lm_head[V,C].  Wq/Wk/Wv are
+ * adjacent, so together they form one [(H+2Hkv)*hd, C] matrix. */
+nc_status nc_param_count(const nc_model* m, int32_t* n_tensors, int64_t* n_elems);
+/* Tensor i: its name ("wte", "h3.wfc", "lm_head", ...), shape and element
+ * offset in the packed vector.  `name` points to storage owned by the model. */
+nc_status nc_param_info(const nc_model* m, int32_t i, const char** name,
+                        int64_t* rows, int64_t* cols, int64_t* offset);
+/* Copy all fp32 master weights (n_elems floats) to / from device memory. */
+nc_status nc_get_params(const nc_model* m, float* dst_dev, void* stream);
+nc_status nc_set_params(nc_model* m, const float* src_dev, void* stream);
+
+/* ------------------------------------------------------------------------
+ * The training step.
+ * tokens_dev, targets_dev: int32 [B, T] (device).  1 <= B <= cfg.batch,
+ * 1 <= T <= cfg.seq_len; position of token (b, t) is t.
+ * loss_host: receives the mean cross-entropy over the B*T positions.
+ * grads_dev: fp32, n_elems floats in the packed layout; OVERWRITTEN with
+ * d(loss)/d(weights).  The weights are not updated.
+ * Synchronises `stream` once at the end (to read the loss and the device
+ * error flag).  A token or target outside [0, vocab) gives
+ * NC_ERR_TOKEN_RANGE and leaves loss and grads unspecified.
+ * ---------------------------------------------------------------------- */
+nc_status nc_forward_backward(nc_model* m, const int32_t* tokens_dev,
+                              const int32_t* targets_dev, int32_t B, int32_t T,
+                              float* loss_host, float* grads_dev, void* stream);
+
+/* The same step with tokens and targets in (preferably pinned) host memory:
+ * they are copied to the model's device buffers on `stream` first. */
+nc_status nc_forward_backward_host(nc_model* m, const int32_t* tokens_host,
+                                   const int32_t* targets_host, int32_t B, int32_t T,
+                                   float* loss_host, float* grads_dev, void* stream);
+
+/* Forward only: fp32 logits [B, T, V] (device, caller-owned).  Does not
+ * synchronise; a token outside [0, vocab) sets the device error flag that
+ * nc_last_error() reads. */
+nc_status nc_forward_logits(nc_model* m, const int32_t* tokens_dev, int32_t B,
+                            int32_t T, float* logits_dev, void* stream);
+
+/* Forward only: per-position cross-entropy [B, T] fp32 (device). */
+nc_status nc_forward_row_losses(nc_model* m, const int32_t* tokens_dev,
+                                const int32_t* targets_dev, int32_t B, int32_t T,
+                                float* losses_dev, void* stream);
+
+/* Synchronise `stream` and turn the model's device error flag into a status
+ * (NC_OK, NC_ERR_TOKEN_RANGE or NC_ERR_TIMEOUT); clears the flag. */
+nc_status nc_last_error(nc_model* m, void* stream);
+
+/* Number of kernels the last nc_forward_backward / nc_forward_logits call
+ * enqueued (for launch accounting). */
+int64_t nc_last_launch_count(const nc_model* m);
+
+/* ------------------------------------------------------------------------
+ * Kernel-level entry points.  Each runs one kernel of the step on caller
+ * buffers so that it can be checked on its own.  `dtype` is NC_FP32 (float
+ * buffers) or NC_BF16 (bfloat16 buffers, passed as void*).  No allocation
+ * except where stated; all enqueue on `stream` without synchronising.
+ * ---------------------------------------------------------------------- */
+
+/* D[M,N] (op)= sum_k A(m,k) B(n,k).  A is [M][K] (a_kmajor=1) or [K][M]
+ * (a_kmajor=0) with leading dimension lda (elements); B is [N][K]
+ * (b_kmajor=1) or [K][N] (b_kmajor=0).  Epilogue `ep`:
+ *   NC_EP_STORE     D (dtype) = acc
+ *   NC_EP_STORE_F32 D (float) = acc
+ *   NC_EP_ACCUM_F32 D (float) += acc          (residual add, dW accumulate)
+ *   NC_EP_RELU2     D (dtype) = relu(acc), aux (dtype) = relu(acc)^2
+ *   NC_EP_RELU2_BWD D (dtype) = acc * 2 * aux   (aux holds relu(u))
+ * ldd / ldaux are leading dimensions in elements.  NC_BF16 runs the tcgen05
+ * tensor-core kernel (lda, ldb multiples of 8, 16-byte aligned bases);
+ * NC_FP32 runs exact fp32 FMA. */
+enum { NC_EP_STORE = 0, NC_EP_STORE_F32 = 1, NC_EP_ACCUM_F32 = 2,
+       NC_EP_RELU2 = 3, NC_EP_RELU2_BWD = 4 };
+nc_status nc_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K,
+                     const void* A, int64_t lda, int32_t a_kmajor,
+                     const void* B, int64_t ldb, int32_t b_kmajor,
+                     int32_t ep, void* D, int64_t ldd, void* aux, int64_t ldaux,
+                     void* stream);
+
+/* RMSNorm without gain over rows of x (float [rows, C]):
+ * y (dtype) = x * rstd, rstd (float [rows]) = 1/sqrt(mean(x^2) + eps). */
+nc_status nc_op_rmsnorm_fwd(int32_t dtype, int64_t rows, int32_t C, const float* x,
+                            void* y, float* rstd, float eps, void* stream);
+/* dx (float, accumulated: dx += ...) and dx_act (dtype copy of the result,
+ * may be NULL) from dy (float [rows, C]), y (dtype) and rstd:
+ * dx += rstd * (dy - y * mean(dy * y)). */
+nc_status nc_op_rmsnorm_bwd(int32_t dtype, int64_t rows, int32_t C, const float* dy,
+                            const void* y, const float* rstd, float* dx, void* dx_act,
+                            void* stream);
+
+/* RoPE angle table: cos_sin (float [T, hd/2, 2]) holds cos and sin of
+ * theta[t][i] = t * rope_base^(-2i/hd), evaluated in fp64 and rounded once. */
+nc_status nc_op_rope_table(int32_t T, int32_t hd, float rope_base, float* cos_sin,
+                           void* stream);
+/* In place on qkv (dtype [B*T, (H+2*Hkv)*hd]): RoPE on the H query and Hkv key
+ * heads at position t = row % T, then RMSNorm of each of those head vectors;
+ * rstd (float [B*T, H+Hkv]).  cos_sin from nc_op_rope_table with >= T rows. */
+nc_status nc_op_rope_qknorm_fwd(int32_t dtype, int32_t B, int32_t T, int32_t H,
+                                int32_t Hkv, int32_t hd, void* qkv, float* rstd,
+                                const float* cos_sin, float eps, void* stream);
+/* In place on dqkv: the backward of the above, given the saved (normalised)
+ * qkv and rstd. */
+nc_status nc_op_rope_qknorm_bwd(int32_t dtype, int32_t B, int32_t T, int32_t H,
+                                int32_t Hkv, int32_t hd, void* dqkv, const void* qkv,
+                                const float* rstd, const float* cos_sin, void* stream);
+
+/* Causal GQA attention over the q, k, v column blocks of qkv (dtype
+ * [B*T, (H+2*Hkv)*hd]); o (dtype [B*T, H*hd]); lse (float [B, H, T]). */
+nc_status nc_op_attention_fwd(int32_t dtype, int32_t B, int32_t T, int32_t H,
+                              int32_t Hkv, int32_t hd, const void* qkv, void* o,
+                              float* lse, void* stream);
+/* dqkv (dtype, same layout as qkv) from do_ (dtype [B*T, H*hd]).  workspace:
+ * float [B*H*T] for rowsum(do * o). */
+nc_status nc_op_attention_bwd(int32_t dtype, int32_t B, int32_t T, int32_t H,
+                              int32_t Hkv, int32_t hd, const void* qkv, const void* o,
+                              const float* lse, const void* do_, void* dqkv,
+                              float* workspace, void* stream);
+
+/* Cross-entropy on logits z (dtype [rows, V]) against targets (int32 [rows]):
+ * row_loss (float [rows]) = logsumexp(z) - z[target]; z is overwritten in
+ * place with (softmax(z) - onehot(target)) * grad_scale.  Targets outside
+ * [0, V) set *err_dev |= 1 (err_dev int32, device, may be NULL). */
+nc_status nc_op_cross_entropy(int32_t dtype, int64_t rows, int32_t V, void* z,
+                              const int32_t* targets, float* row_loss, float grad_scale,
+                              int32_t* err_dev, void* stream);
+
+/* x (float [n, C]) = float(round_dtype(wte[tokens[i]])) for wte float [V, C]. */
+nc_status nc_op_embed_fwd(int32_t dtype, int64_t n, int32_t C, int32_t V,
+                          const int32_t* tokens, const float* wte, float* x,
+                          int32_t* err_dev, void* stream);
+/* dwte (float [V, C]) = sum over i with tokens[i] == v of dx[i] (float [n, C]),
+ * summed in increasing i; rows of ids not present are +0.0.  Deterministic.
+ * scratch: at least nc_embed_bwd_scratch_bytes(n, C, V) bytes of device memory. */
+size_t nc_embed_bwd_scratch_bytes(int64_t n, int32_t C, int32_t V);
+nc_status nc_op_embed_bwd(int64_t n, int32_t C, int32_t V, const int32_t* tokens,
+                          const float* dx, float* dwte, void* scratch, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Per-kernel-class device timing of the step.  While enabled, every kernel
+ * the step enqueues is bracketed by CUDA events on the caller's stream, and
+ * its class, algorithmic FLOPs and algorithmic HBM bytes are recorded.
+ * nc_profile_enable(m, 1) starts (and zeroes) the accumulators, 0 stops.
+ * nc_profile_read synchronises the recorded events and returns, for class
+ * `cls`, the summed device milliseconds, the launch count and the summed
+ * algorithmic FLOPs and bytes.
+ * ---------------------------------------------------------------------- */
+enum { NC_PROF_GEMM = 0, NC_PROF_ATTN_FWD = 1, NC_PROF_ATTN_BWD = 2, NC_PROF_NORM = 3,
+       NC_PROF_ROPE = 4, NC_PROF_CE = 5, NC_PROF_EMBED = 6, NC_PROF_CAST = 7,
+       NC_PROF_OTHER = 8, NC_PROF_CLASSES = 9 };
+nc_status nc_profile_enable(nc_model* m, int32_t on);
+nc_status nc_profile_read(nc_model* m, int32_t cls, double* ms, int64_t* launches,
+                          double* flops, double* bytes);
+
+/* ------------------------------------------------------------------------
+ * Test hook.  Sets the time limit, in nanoseconds, of every bounded
+ * mbarrier wait inside the tensor-core kernels (default 4 s).  When a wait
+ * runs out, the kernel sets the timeout bit of the model's device error
+ * flag (reported as NC_ERR_TIMEOUT), finishes its own in-flight copies and
+ * MMAs (again bounded), frees its tensor memory and returns.
+ * ---------------------------------------------------------------------- */
+void nc_debug_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NC_H */

@@ -1,0 +1,38 @@
+"""Helpers shared by the GPU parity tests (no model arithmetic here)."""
+import numpy as np
+
+
+def torch_mod():
+    import torch
+    return torch
+
+
+def dev_tensor(a, dtype):
+    """numpy array -> CUDA tensor of `dtype` (rounded once if narrower)."""
+    torch = torch_mod()
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device="cuda", dtype=dtype)
+
+
+def to64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def rel_close(got, want, rtol, floor_frac=1e-3):
+    """Per element |got - want| <= rtol * max(|want|, floor_frac * rms(want))."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    rms = float(np.sqrt(np.mean(want * want))) if want.size else 0.0
+    bound = rtol * np.maximum(np.abs(want), floor_frac * rms)
+    err = np.abs(got - want)
+    bad = err > bound
+    worst = float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0
+    return (not bad.any()), worst
+
+
+def cosine(a, b):
+    a = np.asarray(a, dtype=np.float64).ravel()
+    b = np.asarray(b, dtype=np.float64).ravel()
+    na, nb = np.linalg.norm(a), np.linalg.norm(b)
+    if na == 0 and nb == 0:
+        return 1.0
+    return float(a @ b / (na * nb))

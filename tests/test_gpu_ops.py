@@ -1,0 +1,295 @@
+"""Kernel-level parity: each CUDA kernel, called through the C ABI, against the
+fp64 oracle definition of its operation on the same seeded inputs."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import model as OM
+from oracle import ops as OO
+from tests.gpu_util import dev_tensor, to64, rel_close
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import decoder_only_transformer_07_b300 as nc  # noqa: E402
+
+BF16, F32 = torch.bfloat16, torch.float32
+
+
+def rnd(seed, shape, scale=1.0):
+    return np.random.default_rng(seed).normal(0.0, scale, size=shape).astype(np.float32)
+
+
+# ---------------------------------------------------------------- GEMM
+
+def _gemm_case(M, N, K, a_kmajor, b_kmajor, ep, dt, seed=0):
+    a = rnd(seed, (M, K))
+    b = rnd(seed + 1, (N, K))
+    A = dev_tensor(a if a_kmajor else a.T.copy(), dt)
+    B = dev_tensor(b if b_kmajor else b.T.copy(), dt)
+    a64 = to64(A) if a_kmajor else to64(A).T
+    b64 = to64(B) if b_kmajor else to64(B).T
+    ref = OO.gemm(a64, b64)
+    out_dt = F32 if ep in (nc.EP_STORE_F32, nc.EP_ACCUM_F32) else dt
+    D = torch.zeros((M, N), dtype=out_dt, device="cuda")
+    aux = None
+    if ep == nc.EP_ACCUM_F32:
+        base = rnd(seed + 2, (M, N))
+        D.copy_(torch.from_numpy(base))
+        ref = ref + base
+    if ep == nc.EP_RELU2:
+        aux = torch.zeros((M, N), dtype=dt, device="cuda")
+    if ep == nc.EP_RELU2_BWD:
+        aux = dev_tensor(np.abs(rnd(seed + 3, (M, N))), dt)
+    nc.ops.gemm(A, a_kmajor, B, b_kmajor, M, N, K, D, ep=ep, aux=aux,
+                dtype=nc.NC_BF16 if dt == BF16 else nc.NC_FP32)
+    torch.cuda.synchronize()
+    if ep == nc.EP_RELU2:
+        h_ref, r_ref = OO.relu2(ref)
+        return [(to64(D), r_ref), (to64(aux), h_ref)]
+    if ep == nc.EP_RELU2_BWD:
+        return [(to64(D), OO.relu2_bwd(ref, to64(aux)))]
+    return [(to64(D), ref)]
+
+
+def _assert_gemm(pairs, dt, K, ep):
+    for got, want in pairs:
+        scale = float(np.max(np.abs(want))) + 1e-30
+        if dt == F32:
+            tol = 1e-5 * math.sqrt(K) * scale / 8 + 1e-6 * scale
+        elif ep in (nc.EP_STORE_F32, nc.EP_ACCUM_F32):
+            tol = 2e-6 * math.sqrt(K) * scale + 1e-5 * scale
+        else:
+            tol = None
+        if tol is not None:
+            err = float(np.max(np.abs(got - want)))
+            assert err <= tol, (err, tol)
+        else:   # bf16 output: one rounding of a correct fp32 value
+            err = np.abs(got - want)
+            bound = 2.0 ** -8 * np.abs(want) + 1e-4 * scale
+            assert np.all(err <= bound), float(np.max(err / bound))
+
+
+LAYOUTS = [(1, 1), (1, 0), (0, 0), (0, 1)]
+
+
+@pytest.mark.parametrize("a_kmajor,b_kmajor", LAYOUTS)
+@pytest.mark.parametrize("dt", [BF16, F32])
+def test_gemm_layouts_ragged(a_kmajor, b_kmajor, dt):
+    M, N, K = 200, 328, 136
+    _assert_gemm(_gemm_case(M, N, K, a_kmajor, b_kmajor, nc.EP_STORE_F32, dt), dt, K, nc.EP_STORE_F32)
+
+
+@pytest.mark.parametrize("ep", [nc.EP_STORE, nc.EP_STORE_F32, nc.EP_ACCUM_F32, nc.EP_RELU2, nc.EP_RELU2_BWD])
+@pytest.mark.parametrize("dt", [BF16, F32])
+def test_gemm_epilogues(ep, dt):
+    M, N, K = 256, 384, 192
+    _assert_gemm(_gemm_case(M, N, K, 1, 1, ep, dt, seed=10 + ep), dt, K, ep)
+
+
+@pytest.mark.parametrize("a_kmajor,b_kmajor", LAYOUTS)
+def test_gemm_bf16_many_tiles_long_k(a_kmajor, b_kmajor):
+    # 32 x 8 = 256 output tiles (> one per SM) and 64 k-blocks: exercises the
+    # persistent tile loop, both TMEM accumulators and many ring phases.
+    M, N, K = 4096, 2048, 4096
+    _assert_gemm(_gemm_case(M, N, K, a_kmajor, b_kmajor, nc.EP_STORE_F32, BF16, seed=7), BF16, K,
+                 nc.EP_STORE_F32)
+
+
+def test_gemm_bf16_narrow_n():
+    _assert_gemm(_gemm_case(384, 64, 256, 1, 1, nc.EP_STORE_F32, BF16, seed=3), BF16, 256, nc.EP_STORE_F32)
+    _assert_gemm(_gemm_case(136, 128, 72, 0, 0, nc.EP_STORE_F32, BF16, seed=4), BF16, 72, nc.EP_STORE_F32)
+
+
+# ---------------------------------------------------------------- RMSNorm
+
+@pytest.mark.parametrize("dt", [F32, BF16])
+def test_rmsnorm_fwd_bwd(dt):
+    rows, C, eps = 300, 768, 1.1920929e-07
+    x = rnd(20, (rows, C), 0.3)
+    X = dev_tensor(x, F32)
+    Y = torch.empty((rows, C), dtype=dt, device="cuda")
+    R = torch.empty(rows, dtype=F32, device="cuda")
+    nc.ops.rmsnorm_fwd(X, Y, R, eps)
+    y_ref, r_ref = OM.rms_norm(x.astype(np.float64), eps)
+    torch.cuda.synchronize()
+    rtol = 1e-5 if dt == F32 else 2.0 ** -8
+    ok, worst = rel_close(to64(Y), y_ref, rtol, 1e-2)
+    assert ok, worst
+    assert np.allclose(to64(R), r_ref[:, 0], rtol=1e-5)
+    dy = rnd(21, (rows, C))
+    dx0 = rnd(22, (rows, C))
+    DX = dev_tensor(dx0, F32)
+    DXA = torch.empty((rows, C), dtype=dt, device="cuda") if dt == BF16 else None
+    nc.ops.rmsnorm_bwd(dev_tensor(dy, F32), Y, R, DX, DXA)
+    want = dx0 + OM.rms_norm_bwd(dy.astype(np.float64), to64(Y), to64(R)[:, None])
+    torch.cuda.synchronize()
+    ok, worst = rel_close(to64(DX), want, 1e-4, 1e-2)
+    assert ok, worst
+    if DXA is not None:
+        assert torch.equal(DXA, DX.to(BF16))
+
+
+# ---------------------------------------------------------------- RoPE + QK-norm
+
+@pytest.mark.parametrize("hd", [64, 128])
+@pytest.mark.parametrize("dt", [F32, BF16])
+def test_rope_qknorm_fwd_bwd(hd, dt):
+    B, T, H, Hkv, eps, base = 2, 70, 4, 2, 1.1920929e-07, 10000.0
+    W = (H + 2 * Hkv) * hd
+    qkv = rnd(30, (B * T, W))
+    tab = torch.empty((T, hd // 2, 2), dtype=F32, device="cuda")
+    nc.ops.rope_table(T, hd, base, tab)
+    cos, sin = OM.rope_tables(T, hd, base)
+    torch.cuda.synchronize()
+    assert np.allclose(to64(tab)[..., 0], cos, atol=1e-7) and np.allclose(to64(tab)[..., 1], sin, atol=1e-7)
+    Q = dev_tensor(qkv, dt)
+    q_in = to64(Q).reshape(B, T, H + 2 * Hkv, hd)
+    R = torch.empty((B * T, H + Hkv), dtype=F32, device="cuda")
+    nc.ops.rope_qknorm_fwd(Q, B, T, H, Hkv, hd, R, tab, eps)
+    heads = q_in[:, :, :H + Hkv].transpose(0, 2, 1, 3)          # [B, nh, T, hd]
+    y_ref, r_ref = OM.rms_norm(OM.rope(heads, cos, sin), eps)
+    got = to64(Q).reshape(B, T, H + 2 * Hkv, hd)
+    rtol = 1e-5 if dt == F32 else 2.0 ** -8
+    ok, worst = rel_close(got[:, :, :H + Hkv].transpose(0, 2, 1, 3), y_ref, rtol, 1e-2)
+    assert ok, worst
+    assert np.array_equal(got[:, :, H + Hkv:], q_in[:, :, H + Hkv:])       # v untouched
+    assert np.allclose(to64(R).reshape(B, T, H + Hkv).transpose(0, 2, 1), r_ref[..., 0], rtol=1e-5)
+    # backward
+    g = rnd(31, (B * T, W))
+    G = dev_tensor(g, dt)
+    g_in = to64(G).reshape(B, T, H + 2 * Hkv, hd)
+    nc.ops.rope_qknorm_bwd(G, Q, B, T, H, Hkv, hd, R, tab)
+    gh = g_in[:, :, :H + Hkv].transpose(0, 2, 1, 3)
+    yh = got[:, :, :H + Hkv].transpose(0, 2, 1, 3)
+    rh = to64(R).reshape(B, T, H + Hkv).transpose(0, 2, 1)[..., None]
+    want = OM.rope_bwd(OM.rms_norm_bwd(gh, yh, rh), cos, sin)
+    got_g = to64(G).reshape(B, T, H + 2 * Hkv, hd)
+    rtol = 1e-4 if dt == F32 else 2e-2
+    ok, worst = rel_close(got_g[:, :, :H + Hkv].transpose(0, 2, 1, 3), want, rtol, 1e-2)
+    assert ok, worst
+
+
+# ---------------------------------------------------------------- attention
+
+def _attn_ref(qkv, B, T, H, Hkv, hd, do=None):
+    x = qkv.reshape(B, T, H + 2 * Hkv, hd)
+    G = H // Hkv
+    o = np.zeros((B, T, H, hd))
+    lse = np.zeros((B, H, T))
+    dqkv = np.zeros_like(x)
+    for b in range(B):
+        for h in range(H):
+            g = h // G
+            q, k, v = x[b, :, h], x[b, :, H + g], x[b, :, H + Hkv + g]
+            o[b, :, h], lse[b, h] = OM.attention(q, k, v)
+            if do is not None:
+                dq, dk, dv = OM.attention_bwd(q, k, v, do.reshape(B, T, H, hd)[b, :, h])
+                dqkv[b, :, h] = dq
+                dqkv[b, :, H + g] += dk
+                dqkv[b, :, H + Hkv + g] += dv
+    return o.reshape(B * T, H * hd), lse, dqkv.reshape(B * T, -1)
+
+
+@pytest.mark.parametrize("hd,H,Hkv", [(64, 4, 2), (128, 3, 1), (128, 2, 2)])
+@pytest.mark.parametrize("dt", [F32, BF16])
+def test_attention_fwd_bwd(hd, H, Hkv, dt):
+    B, T = 2, 100
+    W = (H + 2 * Hkv) * hd
+    QKV = dev_tensor(rnd(40, (B * T, W)), dt)
+    qkv = to64(QKV)
+    O = torch.empty((B * T, H * hd), dtype=dt, device="cuda")
+    L = torch.empty((B, H, T), dtype=F32, device="cuda")
+    nc.ops.attention_fwd(QKV, B, T, H, Hkv, hd, O, L)
+    DO = dev_tensor(rnd(41, (B * T, H * hd)), dt)
+    o_ref, lse_ref, d_ref = _attn_ref(qkv, B, T, H, Hkv, hd, to64(DO))
+    torch.cuda.synchronize()
+    rtol = 1e-4 if dt == F32 else 2.0 ** -7
+    ok, worst = rel_close(to64(O), o_ref, rtol, 1e-2)
+    assert ok, worst
+    assert np.allclose(to64(L), lse_ref, rtol=1e-5, atol=1e-5)
+    DQKV = torch.zeros((B * T, W), dtype=dt, device="cuda")
+    ws = torch.empty(B * H * T, dtype=F32, device="cuda")
+    nc.ops.attention_bwd(QKV, O, L, DO, B, T, H, Hkv, hd, DQKV, ws)
+    torch.cuda.synchronize()
+    if dt == F32:
+        # the oracle backward uses the oracle forward's o; the kernel uses its own
+        ok, worst = rel_close(to64(DQKV), d_ref, 1e-3, 1e-2)
+        assert ok, worst
+    else:
+        from tests.gpu_util import cosine
+        assert cosine(to64(DQKV), d_ref) > 0.9999
+
+
+# ---------------------------------------------------------------- cross-entropy
+
+@pytest.mark.parametrize("dt", [F32, BF16])
+def test_cross_entropy(dt):
+    rows, V = 64, 1000
+    Z = dev_tensor(rnd(50, (rows, V), 2.0), dt)
+    z = to64(Z)
+    tgt = np.random.default_rng(51).integers(0, V, size=rows).astype(np.int32)
+    TG = torch.from_numpy(tgt).cuda()
+    RL = torch.empty(rows, dtype=F32, device="cuda")
+    nc.ops.cross_entropy(Z, TG, RL, 0.5)
+    loss_ref, dz_ref = OM.cross_entropy(z, tgt)
+    torch.cuda.synchronize()
+    assert np.allclose(to64(RL), loss_ref, rtol=1e-5, atol=1e-5)
+    rtol = 1e-5 if dt == F32 else 2.0 ** -8
+    ok, worst = rel_close(to64(Z), 0.5 * dz_ref, rtol, 1e-3)
+    assert ok, worst
+
+
+def test_cross_entropy_flags_bad_target():
+    Z = torch.zeros((4, 64), dtype=F32, device="cuda")
+    TG = torch.tensor([0, 64, 3, -1], dtype=torch.int32, device="cuda")
+    RL = torch.empty(4, dtype=F32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nc.ops.cross_entropy(Z, TG, RL, 1.0, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 1
+
+
+# ---------------------------------------------------------------- embedding
+
+@pytest.mark.parametrize("dt_code", [nc.NC_FP32, nc.NC_BF16])
+def test_embed_gather_bit_exact(dt_code):
+    V, C, n = 5000, 256, 777
+    wte = rnd(60, (V, C), 0.02)
+    tok = np.random.default_rng(61).integers(0, V, size=n).astype(np.int32)
+    WTE = dev_tensor(wte, F32)
+    X = torch.empty((n, C), dtype=F32, device="cuda")
+    nc.ops.embed_fwd(torch.from_numpy(tok).cuda(), WTE, X, dt_code)
+    want = torch.from_numpy(OO.embed(wte, tok))
+    if dt_code == nc.NC_BF16:
+        want = want.to(BF16).float()
+    torch.cuda.synchronize()
+    assert torch.equal(X.cpu(), want)
+
+
+def test_embed_scatter_deterministic_and_exact_rows():
+    import synthetic as S
+    V, C = 4096, 384
+    n = 6000                                     # 24 chunks, ragged tail
+    tok = S.token_stream(V, 1, n - 1, "zipf", seed=62).reshape(-1)
+    dx = rnd(63, (n, C))
+    TOK = torch.from_numpy(tok).cuda()
+    DX = dev_tensor(dx, F32)
+    scratch = torch.empty(nc.ops.embed_bwd_scratch_bytes(n, C, V), dtype=torch.uint8, device="cuda")
+    out1 = torch.full((V, C), float("nan"), dtype=F32, device="cuda")
+    out2 = torch.full((V, C), float("nan"), dtype=F32, device="cuda")
+    nc.ops.embed_bwd(TOK, DX, out1, scratch)
+    nc.ops.embed_bwd(TOK, DX, out2, scratch)
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)                                   # bitwise reproducible
+    got = to64(out1)
+    want = OO.embed_bwd(tok, dx, V)
+    present = np.zeros(V, dtype=bool)
+    present[tok] = True
+    assert np.all(got[~present] == 0.0) and not np.any(np.signbit(got[~present]))
+    assert np.all(np.any(got[present] != 0.0, axis=1))
+    assert np.allclose(got, want, rtol=1e-5, atol=1e-5 * np.sqrt(np.bincount(tok).max()))
