@@ -41,3 +41,8 @@ nc_status launch_attn_fwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, 
 nc_status launch_attn_bwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv,
                                const void* o, const float* lse, const void* dout, void* dqkv, float* Dv,
                                cudaStream_t st);
+// bf16 flash attention on tensor cores (head_dim 64 or 128).
+nc_status launch_attn_fwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, bf16* o, float* lse,
+                             cudaStream_t st);
+nc_status launch_attn_bwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, const bf16* o, const float* lse,
+                             const bf16* dout, bf16* dqkv, float* Dv, cudaStream_t st);

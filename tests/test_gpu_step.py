@@ -8,7 +8,7 @@ import pytest
 import synthetic as S
 from oracle import model as OM
 from oracle import rng as OR
-from tests.gpu_util import rel_close, cosine
+from tests.gpu_util import rel_close, cosine, norm_rel
 
 pytestmark = pytest.mark.gpu
 
@@ -61,6 +61,7 @@ def test_tiny_fp32_step_matches_oracle():
     for name, r, c, off in m.layout:
         ok, worst = rel_close(g[off:off + r * c], g_ref[off:off + r * c], 1e-4)
         assert ok, (name, worst)
+        assert norm_rel(g[off:off + r * c], g_ref[off:off + r * c]) <= 1e-5, name
     logits = m.forward_logits(torch.from_numpy(tok).cuda()).cpu().numpy()
     z_ref = OM.forward_logits(cfg, params.astype(np.float64), tok)
     ok, worst = rel_close(logits, z_ref, 1e-4)
