@@ -169,6 +169,56 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_op(args):
+    """Single-kernel mode (for ncu captures of one kernel on a small case):
+    times --iters launches of one GEMM or one attention forward+backward."""
+    import torch
+    import decoder_only_transformer_07_b300 as nc
+    torch.cuda.set_device(0)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    times = []
+    if args.op == "gemm":
+        M, N, K = args.m, args.n, args.k
+        A = torch.randn((M, K) if args.a_major == "k" else (K, M), device="cuda", generator=g).to(torch.bfloat16)
+        B = torch.randn((N, K) if args.b_major == "k" else (K, N), device="cuda", generator=g).to(torch.bfloat16)
+        D = torch.empty((M, N), dtype=torch.float32 if args.ep in (1, 2) else torch.bfloat16, device="cuda")
+        aux = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda") if args.ep in (3, 4) else None
+        W = torch.empty(nc.ops.gemm_workspace_bytes(), dtype=torch.uint8, device="cuda")
+        flops = 2.0 * M * N * K
+
+        def once():
+            nc.ops.gemm(A, args.a_major == "k", B, args.b_major == "k", M, N, K, D, ep=args.ep, aux=aux,
+                        workspace=W)
+    else:
+        Bsz, T, H, Hkv, hd = args.batch, args.seq, args.heads, args.kv_heads, args.head_dim
+        W_ = (H + 2 * Hkv) * hd
+        qkv = (torch.randn((Bsz * T, W_), device="cuda", generator=g)).to(torch.bfloat16)
+        o = torch.empty((Bsz * T, H * hd), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((Bsz, H, T), dtype=torch.float32, device="cuda")
+        do = torch.randn((Bsz * T, H * hd), device="cuda", generator=g).to(torch.bfloat16)
+        dqkv = torch.empty_like(qkv)
+        ws = torch.empty(Bsz * H * T, dtype=torch.float32, device="cuda")
+        flops = 4.0 * Bsz * H * hd * T * (T + 1) / 2 * (3 if args.op == "attn" else 1)
+
+        def once():
+            nc.ops.attention_fwd(qkv, Bsz, T, H, Hkv, hd, o, lse)
+            if args.op == "attn":
+                nc.ops.attention_bwd(qkv, o, lse, do, Bsz, T, H, Hkv, hd, dqkv, ws)
+    for _ in range(args.warmup):
+        once()
+    torch.cuda.synchronize()
+    for _ in range(args.iters):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        once()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    print(json.dumps({"op": args.op, "ms": ms, "tflops": flops / (ms / 1e3) / 1e12, "iters": args.iters,
+                      "args": {k: v for k, v in vars(args).items() if k not in ("impl",)}}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -177,7 +227,23 @@ def main():
     ap.add_argument("--config", default="d20", choices=sorted(S.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    # single-op mode (profiling)
+    ap.add_argument("--op", choices=["gemm", "attn", "attn_fwd"])
+    ap.add_argument("--m", type=int, default=65536)
+    ap.add_argument("--n", type=int, default=3840)
+    ap.add_argument("--k", type=int, default=1280)
+    ap.add_argument("--a-major", choices=["k", "mn"], default="k")
+    ap.add_argument("--b-major", choices=["k", "mn"], default="k")
+    ap.add_argument("--ep", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=8)
+    ap.add_argument("--seq", type=int, default=2048)
+    ap.add_argument("--heads", type=int, default=10)
+    ap.add_argument("--kv-heads", type=int, default=10)
+    ap.add_argument("--head-dim", type=int, default=128)
+    ap.add_argument("--iters", type=int, default=5)
     args = ap.parse_args()
+    if args.op:
+        return run_op(args)
     w = S.workload(args.config)
     if args.impl == "reference":
         return run_reference(args, w)
@@ -229,7 +295,8 @@ def main():
     ms = e0.elapsed_time(e1)
     prof = {}
     import ctypes
-    for cls, name in enumerate(["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "ce", "embed", "cast", "other"]):
+    for cls, name in enumerate(["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "ce", "embed", "cast", "other",
+                                "gemm_fwd", "gemm_dx", "gemm_dw", "gemm_lm_head"]):
         t, n, fl, by = ctypes.c_double(), ctypes.c_int64(), ctypes.c_double(), ctypes.c_double()
         model_prof.nc_profile_read(model.handle, cls, ctypes.byref(t), ctypes.byref(n), ctypes.byref(fl),
                                    ctypes.byref(by))
@@ -275,7 +342,7 @@ def main():
                 "bound": "tensor", "achieved": gemm_tflops, "peak": peak_sust, "unit": "TFLOP/s",
                 "frac": (gemm_tflops / peak_sust) if gemm_tflops else None, "traffic": None,
                 "peak_kind": f"bf16 dense, sustained ({peak_src})"}
-    total_prof_ms = sum(v["ms"] for v in prof.values())
+    total_prof_ms = sum(v["ms"] for k, v in prof.items() if not k.startswith("gemm_"))
     kernels = {k: {"ms_per_step": v["ms"] / args.steps, "share": (v["ms"] / total_prof_ms) if total_prof_ms else None,
                    "launches_per_step": v["launches"] / args.steps,
                    "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["ms"] > 0 and v["flops"] else None,

@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(_HERE, "libnc.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with "
-                      "`python -m decoder_only_transformer_07_b300.build`")
+                      "`python decoder_only_transformer_07_b300/build.py`")
 
 _lib = ctypes.CDLL(LIB_PATH)
 
@@ -60,7 +60,9 @@ _SIGS = {
     "nc_forward_row_losses": (_i32, [_p, _p, _p, _i32, _i32, _p, _p]),
     "nc_last_error": (_i32, [_p, _p]),
     "nc_last_launch_count": (_i64, [_p]),
-    "nc_op_gemm": (_i32, [_i32, _i32, _i32, _i32, _p, _i64, _i32, _p, _i64, _i32, _i32, _p, _i64, _p, _i64, _p]),
+    "nc_op_gemm": (_i32, [_i32, _i32, _i32, _i32, _p, _i64, _i32, _p, _i64, _i32, _i32, _p, _i64, _p, _i64, _p,
+                          _sz, _p]),
+    "nc_gemm_workspace_bytes": (_sz, []),
     "nc_op_rmsnorm_fwd": (_i32, [_i32, _i64, _i32, _p, _p, _p, _f32, _p]),
     "nc_op_rmsnorm_bwd": (_i32, [_i32, _i64, _i32, _p, _p, _p, _p, _p, _p]),
     "nc_op_rope_table": (_i32, [_i32, _i32, _f32, _p, _p]),
@@ -224,14 +226,19 @@ class ops:
     """Single-kernel entry points on torch CUDA tensors (for parity tests)."""
 
     @staticmethod
-    def gemm(A, a_kmajor, B, b_kmajor, M, N, K, D, ep=EP_STORE, aux=None, dtype=None):
+    def gemm(A, a_kmajor, B, b_kmajor, M, N, K, D, ep=EP_STORE, aux=None, dtype=None, workspace=None):
         dt = _dtype_code(A) if dtype is None else dtype
         lda = A.stride(0)
         ldb = B.stride(0)
         ldd = D.stride(0)
         ldaux = aux.stride(0) if aux is not None else 0
+        wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
         _check(_lib.nc_op_gemm(dt, M, N, K, _ptr(A), lda, int(a_kmajor), _ptr(B), ldb, int(b_kmajor), ep,
-                               _ptr(D), ldd, _ptr(aux), ldaux, _stream()), "nc_op_gemm")
+                               _ptr(D), ldd, _ptr(aux), ldaux, _ptr(workspace), wsb, _stream()), "nc_op_gemm")
+
+    @staticmethod
+    def gemm_workspace_bytes():
+        return int(_lib.nc_gemm_workspace_bytes())
 
     @staticmethod
     def rmsnorm_fwd(x, y, rstd, eps):

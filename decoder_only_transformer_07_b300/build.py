@@ -1,6 +1,7 @@
 """Build libnc.so (the CUDA kernels and the C ABI) in-tree for sm_103a.
 
-Usage: ``python -m decoder_only_transformer_07_b300.build`` or ``build()``.
+Usage: ``python decoder_only_transformer_07_b300/build.py`` (by path: importing the package
+would load the previous libnc.so) or ``__graft_entry__.build()``.
 Each ``csrc/*.cu`` compiles to an object with nvcc (in parallel), then one
 shared library is linked with the CUDA runtime linked statically.
 """

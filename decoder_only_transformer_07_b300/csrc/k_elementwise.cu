@@ -86,6 +86,22 @@ nc_status launch_rope_table(int T, int hd, float base, float* tab, cudaStream_t 
 }
 
 // ---------------------------------------------------------------- RMSNorm
+// Four consecutive activation-type values <-> float4.
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const bf16* p) {
+  uint2 u = *reinterpret_cast<const uint2*>(p);
+  __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&u.x), b = *reinterpret_cast<__nv_bfloat162*>(&u.y);
+  return make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+}
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st4(bf16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
 // One warp per row; C % 4 == 0.  y = x * rstd, rstd = 1/sqrt(mean(x^2) + eps).
 template <typename T>
 __global__ void k_rmsnorm_fwd(int64_t rows, int C, const float* __restrict__ x,
@@ -105,14 +121,12 @@ __global__ void k_rmsnorm_fwd(int64_t rows, int C, const float* __restrict__ x,
   T* yr = y + row * C;
   for (int c = lane; c < C / 4; c += 32) {
     float4 v = xr[c];
-    yr[4 * c + 0] = from_f32<T>(v.x * r);
-    yr[4 * c + 1] = from_f32<T>(v.y * r);
-    yr[4 * c + 2] = from_f32<T>(v.z * r);
-    yr[4 * c + 3] = from_f32<T>(v.w * r);
+    st4(yr + 4 * c, make_float4(v.x * r, v.y * r, v.z * r, v.w * r));
   }
 }
 
-// dx += rstd * (dy - y * mean(dy * y)); dx_act = act(dx) if given.
+// dx += rstd * (dy - y * mean(dy * y)); dx_act = act(dx) if given.  One warp
+// per row, four columns per lane per step (C % 4 == 0).
 template <typename T>
 __global__ void k_rmsnorm_bwd(int64_t rows, int C, const float* __restrict__ dy,
                               const T* __restrict__ y, const float* __restrict__ rstd,
@@ -123,14 +137,21 @@ __global__ void k_rmsnorm_bwd(int64_t rows, int C, const float* __restrict__ dy,
   const float* dyr = dy + row * C;
   const T* yr = y + row * C;
   float dot = 0.f;
-  for (int c = lane; c < C; c += 32) dot += dyr[c] * to_f32(yr[c]);
+  for (int c = lane * 4; c < C; c += 128) {
+    float4 a = ld4(dyr + c), b = ld4(yr + c);
+    dot += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+  }
   dot = warp_sum(dot) / (float)C;
-  float r = rstd[row];
+  const float r = rstd[row];
   float* dxr = dx + row * C;
-  for (int c = lane; c < C; c += 32) {
-    float v = dxr[c] + r * (dyr[c] - to_f32(yr[c]) * dot);
-    dxr[c] = v;
-    if (dx_act) dx_act[row * C + c] = from_f32<T>(v);
+  for (int c = lane * 4; c < C; c += 128) {
+    float4 a = ld4(dyr + c), b = ld4(yr + c), d = ld4(dxr + c);
+    d.x += r * (a.x - b.x * dot);
+    d.y += r * (a.y - b.y * dot);
+    d.z += r * (a.z - b.z * dot);
+    d.w += r * (a.w - b.w * dot);
+    st4(dxr + c, d);
+    if (dx_act) st4(dx_act + row * C + c, d);
   }
 }
 
@@ -146,6 +167,7 @@ template <typename T>
 nc_status launch_rmsnorm_bwd_t(int64_t rows, int C, const float* dy, const T* y, const float* rstd,
                                float* dx, T* dx_act, cudaStream_t st) {
   if (rows <= 0) return NC_OK;
+  if (C % 4 || (((uintptr_t)dy) & 15) || (((uintptr_t)dx) & 15) || (((uintptr_t)y) & 7)) return NC_ERR_ARG;
   k_rmsnorm_bwd<T><<<cdiv(rows, 8), 256, 0, st>>>(rows, C, dy, y, rstd, dx, dx_act);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
@@ -165,6 +187,17 @@ nc_status launch_rmsnorm_bwd(int dtype, int64_t rows, int C, const float* dy, co
 // ---------------------------------------------------------------- RoPE + QK-norm
 // One warp per (token row, head j in [0, H + Hkv)): query heads occupy columns
 // [0, H*hd) of qkv and key heads [H*hd, (H+Hkv)*hd), so head j starts at j*hd.
+// Each lane owns pairs (i, i+1) of the first half and (i+d, i+d+1) of the
+// second, i = 2*lane + 64*k, so loads and stores are 2-element vectors.
+__device__ __forceinline__ float2 ld2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 ld2(const bf16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ void st2(float* p, float a, float b) { *reinterpret_cast<float2*>(p) = make_float2(a, b); }
+__device__ __forceinline__ void st2(bf16* p, float a, float b) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+}
+
 template <typename T>
 __global__ void k_rope_qknorm_fwd(int64_t rows, int T_, int nh, int hd, int64_t ld,
                                   T* __restrict__ qkv, float* __restrict__ rstd,
@@ -178,28 +211,30 @@ __global__ void k_rope_qknorm_fwd(int64_t rows, int T_, int nh, int hd, int64_t 
   const int d = hd / 2;
   T* p = qkv + row * ld + (int64_t)j * hd;
   const float2* cs = tab + (int64_t)t * d;
-  float y1[4], y2[4];   // hd <= 256
+  float y[2][4];   // [k][x1a, x1b, x2a, x2b] for hd <= 256
   float ss = 0.f;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    int i = lane + 32 * k;
-    y1[k] = y2[k] = 0.f;
+  for (int k = 0; k < 2; ++k) {
+    const int i = 2 * lane + 64 * k;
+    y[k][0] = y[k][1] = y[k][2] = y[k][3] = 0.f;
     if (i < d) {
-      float x1 = to_f32(p[i]), x2 = to_f32(p[i + d]);
-      float2 c = cs[i];
-      y1[k] = x1 * c.x + x2 * c.y;
-      y2[k] = -x1 * c.y + x2 * c.x;
-      ss += y1[k] * y1[k] + y2[k] * y2[k];
+      float2 a = ld2(p + i), b = ld2(p + i + d);
+      float4 c = *reinterpret_cast<const float4*>(cs + i);   // cos_i, sin_i, cos_i+1, sin_i+1
+      y[k][0] = a.x * c.x + b.x * c.y;
+      y[k][2] = -a.x * c.y + b.x * c.x;
+      y[k][1] = a.y * c.z + b.y * c.w;
+      y[k][3] = -a.y * c.w + b.y * c.z;
+      ss += y[k][0] * y[k][0] + y[k][1] * y[k][1] + y[k][2] * y[k][2] + y[k][3] * y[k][3];
     }
   }
   ss = warp_sum(ss);
-  float r = rsqrtf(ss / (float)hd + eps);
+  const float r = rsqrtf(ss / (float)hd + eps);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    int i = lane + 32 * k;
+  for (int k = 0; k < 2; ++k) {
+    const int i = 2 * lane + 64 * k;
     if (i < d) {
-      p[i] = from_f32<T>(y1[k] * r);
-      p[i + d] = from_f32<T>(y2[k] * r);
+      st2(p + i, y[k][0] * r, y[k][1] * r);
+      st2(p + i + d, y[k][2] * r, y[k][3] * r);
     }
   }
   if (lane == 0) rstd[row * nh + j] = r;
@@ -219,36 +254,41 @@ __global__ void k_rope_qknorm_bwd(int64_t rows, int T_, int nh, int hd, int64_t 
   T* g = dqkv + row * ld + (int64_t)j * hd;
   const T* y = qkv + row * ld + (int64_t)j * hd;
   const float2* cs = tab + (int64_t)t * d;
-  float dy1[4], dy2[4], yy1[4], yy2[4];
+  float dy[2][4], yy[2][4];
   float dot = 0.f;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    int i = lane + 32 * k;
-    dy1[k] = dy2[k] = yy1[k] = yy2[k] = 0.f;
+  for (int k = 0; k < 2; ++k) {
+    const int i = 2 * lane + 64 * k;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dy[k][e] = yy[k][e] = 0.f;
     if (i < d) {
-      dy1[k] = to_f32(g[i]); dy2[k] = to_f32(g[i + d]);
-      yy1[k] = to_f32(y[i]); yy2[k] = to_f32(y[i + d]);
-      dot += dy1[k] * yy1[k] + dy2[k] * yy2[k];
+      float2 g1 = ld2(g + i), g2 = ld2(g + i + d), y1 = ld2(y + i), y2 = ld2(y + i + d);
+      dy[k][0] = g1.x; dy[k][1] = g1.y; dy[k][2] = g2.x; dy[k][3] = g2.y;
+      yy[k][0] = y1.x; yy[k][1] = y1.y; yy[k][2] = y2.x; yy[k][3] = y2.y;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dot += dy[k][e] * yy[k][e];
     }
   }
   dot = warp_sum(dot) / (float)hd;
-  float r = rstd[row * nh + j];
+  const float r = rstd[row * nh + j];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    int i = lane + 32 * k;
+  for (int k = 0; k < 2; ++k) {
+    const int i = 2 * lane + 64 * k;
     if (i < d) {
-      float r1 = r * (dy1[k] - yy1[k] * dot);   // through the per-head RMSNorm
-      float r2 = r * (dy2[k] - yy2[k] * dot);
-      float2 c = cs[i];
-      g[i] = from_f32<T>(r1 * c.x - r2 * c.y);   // transpose of the rotation
-      g[i + d] = from_f32<T>(r1 * c.y + r2 * c.x);
+      float q[4];   // through the per-head RMSNorm
+#pragma unroll
+      for (int e = 0; e < 4; ++e) q[e] = r * (dy[k][e] - yy[k][e] * dot);
+      float4 c = *reinterpret_cast<const float4*>(cs + i);
+      // transpose of the rotation: dx1 = dr1 cos - dr2 sin, dx2 = dr1 sin + dr2 cos
+      st2(g + i, q[0] * c.x - q[2] * c.y, q[1] * c.z - q[3] * c.w);
+      st2(g + i + d, q[0] * c.y + q[2] * c.x, q[1] * c.w + q[3] * c.z);
     }
   }
 }
 
 nc_status launch_rope_qknorm_fwd(int dtype, int B, int T, int H, int Hkv, int hd, void* qkv,
                                  float* rstd, const float* tab, float eps, cudaStream_t st) {
-  if (hd > 256 || (hd & 1)) return NC_ERR_ARG;
+  if (hd > 256 || (hd & 3) || (((uintptr_t)qkv) & 7) || (((uintptr_t)tab) & 15)) return NC_ERR_ARG;
   int64_t rows = (int64_t)B * T;
   int nh = H + Hkv;
   int64_t ld = (int64_t)(H + 2 * Hkv) * hd;
@@ -266,7 +306,7 @@ nc_status launch_rope_qknorm_fwd(int dtype, int B, int T, int H, int Hkv, int hd
 nc_status launch_rope_qknorm_bwd(int dtype, int B, int T, int H, int Hkv, int hd, void* dqkv,
                                  const void* qkv, const float* rstd, const float* tab,
                                  cudaStream_t st) {
-  if (hd > 256 || (hd & 1)) return NC_ERR_ARG;
+  if (hd > 256 || (hd & 3) || (((uintptr_t)dqkv) & 7) || (((uintptr_t)tab) & 15)) return NC_ERR_ARG;
   int64_t rows = (int64_t)B * T;
   int nh = H + Hkv;
   int64_t ld = (int64_t)(H + 2 * Hkv) * hd;

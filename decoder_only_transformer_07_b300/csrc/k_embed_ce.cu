@@ -271,12 +271,86 @@ __global__ void __launch_bounds__(512) k_cross_entropy(int V, T* __restrict__ z,
   }
 }
 
+// bf16 rows with V % 8 == 0 and V <= 512 * 8 * CE_VEC: the row is read once
+// into registers (16-byte loads), reduced, and dz written from registers.
+#define CE_THREADS 512
+#define CE_VEC 16
+__global__ void __launch_bounds__(CE_THREADS) k_cross_entropy_bf16(int V, bf16* __restrict__ z, int64_t ldz,
+                                                                   const int32_t* __restrict__ targets,
+                                                                   float* __restrict__ row_loss, float scale,
+                                                                   int32_t* __restrict__ err) {
+  __shared__ float sh[32];
+  __shared__ float ztgt;
+  const int64_t row = blockIdx.x;
+  bf16* zr = z + row * ldz;
+  const int nv = V / 8;
+  uint4 v[CE_VEC];
+  float m = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < CE_VEC; ++k) {
+    const int i = threadIdx.x + k * CE_THREADS;
+    if (i < nv) {
+      v[k] = reinterpret_cast<const uint4*>(zr)[i];
+      const bf16* e = reinterpret_cast<const bf16*>(&v[k]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, __bfloat162float(e[j]));
+    }
+  }
+  const int tgt = targets[row];
+  const bool ok = tgt >= 0 && tgt < V;
+  if (threadIdx.x == 0) ztgt = ok ? __bfloat162float(zr[tgt]) : 0.f;
+  m = block_max(m, sh);
+  const float L2E = 1.4426950408889634f;
+  const float mb = m * L2E;
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < CE_VEC; ++k) {
+    const int i = threadIdx.x + k * CE_THREADS;
+    if (i < nv) {
+      const bf16* e = reinterpret_cast<const bf16*>(&v[k]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sum += exp2f(__bfloat162float(e[j]) * L2E - mb);
+    }
+  }
+  sum = block_sum(sum, sh);
+  const float lse = m + logf(sum);
+  if (threadIdx.x == 0) {
+    if (!ok && err) atomicOr(err, NC_DEVERR_TOKEN);
+    row_loss[row] = ok ? lse - ztgt : 0.f;
+  }
+  const float inv = scale / sum;
+#pragma unroll
+  for (int k = 0; k < CE_VEC; ++k) {
+    const int i = threadIdx.x + k * CE_THREADS;
+    if (i < nv) {
+      const bf16* e = reinterpret_cast<const bf16*>(&v[k]);
+      float p[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        p[j] = exp2f(__bfloat162float(e[j]) * L2E - mb) * inv;
+        if (i * 8 + j == tgt) p[j] -= scale;
+      }
+      uint4 o;
+      __nv_bfloat162 q0 = __floats2bfloat162_rn(p[0], p[1]), q1 = __floats2bfloat162_rn(p[2], p[3]);
+      __nv_bfloat162 q2 = __floats2bfloat162_rn(p[4], p[5]), q3 = __floats2bfloat162_rn(p[6], p[7]);
+      o.x = *reinterpret_cast<uint32_t*>(&q0);
+      o.y = *reinterpret_cast<uint32_t*>(&q1);
+      o.z = *reinterpret_cast<uint32_t*>(&q2);
+      o.w = *reinterpret_cast<uint32_t*>(&q3);
+      reinterpret_cast<uint4*>(zr)[i] = o;
+    }
+  }
+}
+
 nc_status launch_cross_entropy(int dtype, int64_t rows, int V, void* z, int64_t ldz,
                                const int32_t* targets, float* row_loss, float scale, int32_t* err,
                                cudaStream_t st) {
   if (rows <= 0) return NC_OK;
   if (rows > 0x7fffffff) return NC_ERR_ARG;
-  if (dtype == NC_BF16)
+  if (dtype == NC_BF16 && V % 8 == 0 && ldz % 8 == 0 && V <= 8 * CE_THREADS * CE_VEC &&
+      (((uintptr_t)z) & 15) == 0)
+    k_cross_entropy_bf16<<<(unsigned)rows, CE_THREADS, 0, st>>>(V, (bf16*)z, ldz, targets, row_loss, scale, err);
+  else if (dtype == NC_BF16)
     k_cross_entropy<bf16><<<(unsigned)rows, 512, 0, st>>>(V, (bf16*)z, ldz, targets, row_loss, scale, err);
   else
     k_cross_entropy<float><<<(unsigned)rows, 512, 0, st>>>(V, (float*)z, ldz, targets, row_loss, scale, err);

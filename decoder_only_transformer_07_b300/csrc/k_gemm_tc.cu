@@ -42,6 +42,55 @@ struct TcParams {
   int tiles_m, tiles_n, num_kb;
   int32_t* err;
   uint64_t wait_ns;
+  // stream-K: CTA c owns the flattened (tile, k-block) range [c*per, (c+1)*per);
+  // tiles it covers only in part go to ws[c][0 (first) or 1 (last)][128][BN] fp32
+  int streamk;
+  int64_t per;
+  float* ws;
+};
+
+// One unit of work of a CTA: k-blocks [k0, k1) of output tile t.
+struct TcSeg {
+  int t, k0, k1;
+  bool full, first;
+};
+
+// Iterates the segments a CTA owns, identically in every role.
+struct TcSegIter {
+  int64_t g, end;       // stream-K cursor in the flattened k-block space
+  int t, stride, tiles; // plain mode
+  bool sk, started;
+  __device__ TcSegIter(const TcParams& p, int cta, int grid) {
+    sk = p.streamk != 0;
+    tiles = p.tiles_m * p.tiles_n;
+    if (sk) {
+      const int64_t total = (int64_t)tiles * p.num_kb;
+      g = (int64_t)cta * p.per;
+      end = g + p.per < total ? g + p.per : total;
+    }
+    t = cta;
+    stride = grid;
+    started = false;
+  }
+  __device__ bool next(const TcParams& p, TcSeg& s) {
+    if (!sk) {
+      if (started) t += stride;
+      started = true;
+      if (t >= tiles) return false;
+      s.t = t; s.k0 = 0; s.k1 = p.num_kb; s.full = true; s.first = true;
+      return true;
+    }
+    if (g >= end) return false;
+    s.first = !started;
+    started = true;
+    s.t = (int)(g / p.num_kb);
+    s.k0 = (int)(g % p.num_kb);
+    const int64_t rem = end - g;
+    s.k1 = (int)((p.num_kb - s.k0) < rem ? p.num_kb : s.k0 + rem);
+    s.full = (s.k0 == 0 && s.k1 == p.num_kb);
+    g += s.k1 - s.k0;
+    return true;
+  }
 };
 
 template <int BN>
@@ -178,7 +227,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_tiles = p.tiles_m * p.tiles_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
@@ -208,10 +256,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     long long issued = 0;
-    for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
+    TcSegIter it(p, blockIdx.x, gridDim.x);
+    TcSeg sg;
+    while (!*abort_flag && it.next(p, sg)) {
       int tm, tn;
-      tile_coords(p, t, tm, tn);
-      for (int kb = 0; kb < p.num_kb; ++kb) {
+      tile_coords(p, sg.t, tm, tn);
+      for (int kb = sg.k0; kb < sg.k1; ++kb) {
         if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, p.wait_ns)) { fail(); break; }
         if (*abort_flag) break;
         uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
@@ -234,12 +284,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (++stage == S) { stage = 0; phase ^= 1; }
       }
     }
-    // Drain: every load this thread issued must land before the CTA exits.
-    if (*abort_flag) {
-      for (int s = 0; s < S; ++s) {
-        long long n_s = issued / S + ((issued % S) > s ? 1 : 0);
-        if (n_s > 0) mbar_wait_bounded(&full_bar[s], (uint32_t)((n_s - 1) & 1), p.wait_ns);
-      }
+    // Drain: every load this thread issued must land before the CTA exits
+    // (already true on the normal path, where the MMA issuer consumed them all).
+    for (int s = 0; s < S; ++s) {
+      long long n_s = issued / S + ((issued % S) > s ? 1 : 0);
+      if (n_s > 0) mbar_wait_bounded(&full_bar[s], (uint32_t)((n_s - 1) & 1), p.wait_ns);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
@@ -247,13 +296,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
-    for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x, ++local) {
+    TcSegIter it(p, blockIdx.x, gridDim.x);
+    TcSeg sg;
+    for (; !*abort_flag && it.next(p, sg); ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1, p.wait_ns)) { fail(); break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
-      for (int kb = 0; kb < p.num_kb; ++kb) {
+      for (int kb = sg.k0; kb < sg.k1; ++kb) {
         if (!mbar_wait_bounded(&full_bar[stage], phase, p.wait_ns)) { fail(); break; }
         if (*abort_flag) break;
         tc_fence_after();
@@ -262,7 +313,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
         for (int k = 0; k < TC_BK / 16; ++k) {
           tc_mma_f16(d_tmem, operand_desc(sa, p.a_mn, k), operand_desc(sb, p.b_mn, k), idesc,
-                     (kb > 0 || k > 0) ? 1u : 0u);
+                     (kb > sg.k0 || k > 0) ? 1u : 0u);
         }
         tc_commit(&empty_bar[stage]);
         if (++stage == S) { stage = 0; phase ^= 1; }
@@ -277,22 +328,36 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ---------------- epilogue
     const int quarter = warp & 3;
     int local = 0;
-    for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x, ++local) {
+    TcSegIter it(p, blockIdx.x, gridDim.x);
+    TcSeg sg;
+    for (; !*abort_flag && it.next(p, sg); ++local) {
       int tm, tn;
-      tile_coords(p, t, tm, tn);
+      tile_coords(p, sg.t, tm, tn);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait_bounded(&acc_full[acc], acc_phase, p.wait_ns)) { fail(); break; }
       tc_fence_after();
       const int64_t m = (int64_t)tm * TC_BM + quarter * 32 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      // a tile this CTA covers only in part: its fp32 partial goes to the workspace
+      float* part = sg.full ? nullptr
+                            : p.ws + ((size_t)blockIdx.x * 2 + (sg.first ? 0 : 1)) * TC_BM * BN +
+                                  (size_t)(quarter * 32 + lane) * BN;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + c, r);
         tmem_ld_wait();
         const int n0 = tn * BN + c;
-        if (m < p.M && n0 < p.N) tc_epilogue_row(p, m, n0, r);
+        if (part) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(part + c + i) =
+                make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
+                            __uint_as_float(r[i + 3]));
+        } else if (m < p.M && n0 < p.N) {
+          tc_epilogue_row(p, m, n0, r);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -303,6 +368,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
+// Stream-K fix-up: for every tile split across CTAs, add the partials in CTA
+// order (a fixed order, so results are bitwise reproducible) and apply the
+// fp32 epilogue (store or accumulate).  One block per tile.
+template <int BN>
+__global__ void __launch_bounds__(256) k_gemm_tc_fixup(TcParams p) {
+  const int t = blockIdx.x;
+  const int64_t lo = (int64_t)t * p.num_kb, hi = lo + p.num_kb - 1;
+  const int c0 = (int)(lo / p.per), c1 = (int)(hi / p.per);
+  if (c0 == c1) return;                     // written whole by one CTA
+  int tm, tn;
+  tile_coords(p, t, tm, tn);
+  for (int i = threadIdx.x; i < TC_BM * BN / 4; i += blockDim.x) {
+    const int r = (i * 4) / BN, cc = (i * 4) % BN;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = c0; c <= c1; ++c) {
+      const int first_tile = (int)(((int64_t)c * p.per) / p.num_kb);
+      const int slot = (t == first_tile) ? 0 : 1;
+      const float4 v = *reinterpret_cast<const float4*>(p.ws + ((size_t)c * 2 + slot) * TC_BM * BN + (size_t)r * BN + cc);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    const int64_t m = (int64_t)tm * TC_BM + r;
+    const int n = tn * BN + cc;
+    if (m >= p.M) continue;
+    float* d = (float*)p.D + m * p.ldd + n;
+    const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+    for (int j = 0; j < 4 && n + j < p.N; ++j) d[j] = (p.ep == NC_EP_ACCUM_F32) ? d[j] + a[j] : a[j];
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -338,22 +432,52 @@ static int g_num_sms = 0;
 uint64_t g_tc_wait_ns = 4000000000ull;   // bounded-wait limit of the tensor-core kernels
 
 template <int BN>
-static nc_status launch_tc_bn(const TcParams& p, const CUtensorMap& ta, const CUtensorMap& tb, cudaStream_t st) {
+static nc_status launch_tc_bn(TcParams p, const CUtensorMap& ta, const CUtensorMap& tb, size_t ws_bytes,
+                              cudaStream_t st) {
   static bool attr_set = false;
   auto kern = k_gemm_tc<BN>;
   if (!attr_set) {
     NC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<BN>::SMEM));
     attr_set = true;
   }
-  int tiles = p.tiles_m * p.tiles_n;
+  const int tiles = p.tiles_m * p.tiles_n;
   int grid = std::min(tiles, g_num_sms);
+  // Stream-K when whole tiles would leave the last wave badly filled (fp32
+  // outputs only: the weight gradients, whose K is the token count).
+  p.streamk = 0;
+  const bool f32_out = (p.ep == NC_EP_STORE_F32 || p.ep == NC_EP_ACCUM_F32);
+  if (f32_out && p.ws && tiles < 8 * g_num_sms && p.num_kb >= 8) {
+    const int waves = (tiles + g_num_sms - 1) / g_num_sms;
+    const double fill = (double)tiles / ((double)waves * g_num_sms);
+    if (fill < 0.9 && ws_bytes >= (size_t)g_num_sms * 2 * TC_BM * BN * sizeof(float)) {
+      const int64_t total = (int64_t)tiles * p.num_kb;
+      grid = g_num_sms;
+      p.per = (total + grid - 1) / grid;
+      p.streamk = 1;
+    }
+  }
   kern<<<grid, TC_THREADS, TcCfg<BN>::SMEM, st>>>(ta, tb, p);
-  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+  NC_CUDA_TRY(cudaGetLastError());
+  if (p.streamk) {
+    k_gemm_tc_fixup<BN><<<tiles, 256, 0, st>>>(p);
+    NC_CUDA_TRY(cudaGetLastError());
+  }
+  return NC_OK;
+}
+
+size_t gemm_tc_workspace_bytes() {
+  if (!g_num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return (size_t)160 * 2 * TC_BM * 256 * sizeof(float);
+  }
+  return (size_t)g_num_sms * 2 * TC_BM * 256 * sizeof(float);
 }
 
 nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_kmajor, const bf16* B,
                          int64_t ldb, int b_kmajor, int ep, void* D, int64_t ldd, void* aux, int64_t ldaux,
-                         int32_t* err, cudaStream_t st) {
+                         int32_t* err, void* ws, size_t ws_bytes, cudaStream_t st) {
   if (M <= 0 || N <= 0) return NC_OK;
   if (K <= 0) return NC_ERR_ARG;
   if ((lda % 8) || (ldb % 8) || (((uintptr_t)A) & 15) || (((uintptr_t)B) & 15)) return NC_ERR_ARG;
@@ -374,6 +498,10 @@ nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_
   p.num_kb = (K + TC_BK - 1) / TC_BK;
   p.err = err;
   p.wait_ns = g_tc_wait_ns;
+  p.ws = (float*)ws;
+  p.streamk = 0;
+  p.per = 0;
+  if (ws && (((uintptr_t)ws) & 15)) return NC_ERR_ARG;
   CUtensorMap ta, tb;
   bool ok;
   if (a_kmajor) ok = make_tmap(&ta, A, K, M, lda, TC_BK, TC_BM);
@@ -382,6 +510,6 @@ nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_
   if (b_kmajor) ok = make_tmap(&tb, B, K, N, ldb, TC_BK, BN);
   else ok = make_tmap(&tb, B, N, K, ldb, 64, TC_BK);
   if (!ok) return NC_ERR_CUDA;
-  if (BN == 256) return launch_tc_bn<256>(p, ta, tb, st);
-  return launch_tc_bn<128>(p, ta, tb, st);
+  if (BN == 256) return launch_tc_bn<256>(p, ta, tb, ws_bytes, st);
+  return launch_tc_bn<128>(p, ta, tb, ws_bytes, st);
 }

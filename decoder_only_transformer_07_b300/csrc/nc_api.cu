@@ -55,10 +55,12 @@ struct nc_model {
   void* dqkv = nullptr;
   float* Dv = nullptr;
   void* emb_scratch = nullptr;
+  void* gemm_ws = nullptr;           // stream-K partial tiles
+  size_t gemm_ws_bytes = 0;
   int32_t *tok_dev = nullptr, *tgt_dev = nullptr;
   int64_t launches = 0;
   // profiling (nc_profile_enable)
-  struct Rec { int cls; int ev; double flops, bytes; };
+  struct Rec { int cls, sub; int ev; double flops, bytes; };
   bool prof_on = false;
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_used = 0;
@@ -85,13 +87,12 @@ static int prof_begin(nc_model* m, cudaStream_t st) {
   return e;
 }
 
-static void prof_end(nc_model* m, int e0, int cls, double flops, double bytes, cudaStream_t st) {
+static void prof_end(nc_model* m, int e0, int cls, double flops, double bytes, cudaStream_t st, int sub = -1) {
   if (!m->prof_on || e0 < 0) return;
   int e1 = prof_event(m);
   if (e1 < 0) return;
   cudaEventRecord(m->ev_pool[e1], st);
-  m->recs.push_back({cls, e0, flops, bytes});
-  (void)e1;
+  m->recs.push_back({cls, sub, e0, flops, bytes});
 }
 
 // Fold recorded event pairs into the per-class totals and recycle the events.
@@ -101,23 +102,27 @@ static void prof_flush(nc_model* m) {
   for (const auto& r : m->recs) {
     float ms = 0.f;
     if (cudaEventElapsedTime(&ms, m->ev_pool[r.ev], m->ev_pool[r.ev + 1]) == cudaSuccess) {
-      m->prof_ms[r.cls] += ms;
-      m->prof_flops[r.cls] += r.flops;
-      m->prof_bytes[r.cls] += r.bytes;
-      m->prof_n[r.cls] += 1;
+      for (int c : {r.cls, r.sub}) {
+        if (c < 0) continue;
+        m->prof_ms[c] += ms;
+        m->prof_flops[c] += r.flops;
+        m->prof_bytes[c] += r.bytes;
+        m->prof_n[c] += 1;
+      }
     }
   }
   m->recs.clear();
   m->ev_used = 0;
 }
 
-#define PROF(cls, flops, bytes, call)                                      \
+#define PROF_SUB(cls, sub, flops, bytes, call)                            \
   do {                                                                     \
     int e0_ = prof_begin(m, st);                                           \
     nc_status s_ = (call);                                                 \
-    prof_end(m, e0_, (cls), (double)(flops), (double)(bytes), st);         \
+    prof_end(m, e0_, (cls), (double)(flops), (double)(bytes), st, (sub));  \
     if (s_ != NC_OK) return s_;                                            \
   } while (0)
+#define PROF(cls, flops, bytes, call) PROF_SUB(cls, -1, flops, bytes, call)
 
 // ------------------------------------------------------------------ helpers
 
@@ -146,7 +151,7 @@ static const ParamTensor& tensor(const nc_model* m, int layer, int which) {
   return m->layout[1 + layer * 6 + which];
 }
 
-static nc_status gemm(nc_model* m, int M, int N, int K, const void* A, int64_t lda, int a_kmajor,
+static nc_status gemm(nc_model* m, int role, int M, int N, int K, const void* A, int64_t lda, int a_kmajor,
                       const void* B, int64_t ldb, int b_kmajor, int ep, void* D, int64_t ldd, void* aux,
                       int64_t ldaux, cudaStream_t st) {
   m->launches += 1;
@@ -156,11 +161,11 @@ static nc_status gemm(nc_model* m, int M, int N, int K, const void* A, int64_t l
   const double bytes = ((double)M * K + (double)N * K) * a + (double)M * N * out;
   const double flops = 2.0 * M * N * K;
   if (m->dtype == NC_BF16)
-    PROF(NC_PROF_GEMM, flops, bytes,
+    PROF_SUB(NC_PROF_GEMM, role, flops, bytes,
          launch_gemm_tc(M, N, K, (const bf16*)A, lda, a_kmajor, (const bf16*)B, ldb, b_kmajor, ep, D, ldd, aux,
-                        ldaux, m->err, st));
+                        ldaux, m->err, m->gemm_ws, m->gemm_ws_bytes, st));
   else
-    PROF(NC_PROF_GEMM, flops, bytes,
+    PROF_SUB(NC_PROF_GEMM, role, flops, bytes,
          launch_gemm_simt(NC_FP32, M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, ep, D, ldd, aux, ldaux, st));
   return NC_OK;
 }
@@ -266,6 +271,10 @@ static nc_status allocate(nc_model* m) {
   NC_TRY(dalloc(m, (size_t)N * m->qkvw * a, &m->dqkv));
   NC_TRY(dalloc_t(m, (size_t)N * m->H, &m->Dv));
   NC_TRY(dalloc(m, embed_bwd_scratch_bytes(N, m->C, m->V), &m->emb_scratch));
+  if (m->dtype == NC_BF16) {
+    m->gemm_ws_bytes = gemm_tc_workspace_bytes();
+    NC_TRY(dalloc(m, m->gemm_ws_bytes, &m->gemm_ws));
+  }
   NC_TRY(dalloc_t(m, (size_t)N, &m->tok_dev));
   NC_TRY(dalloc_t(m, (size_t)N, &m->tgt_dev));
   return NC_OK;
@@ -423,16 +432,16 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
     float* rstdqk = m->rstdqk + (size_t)l * m->Nmax * (m->H + m->Hkv);
     float* lse = m->lse + (size_t)l * m->Nmax * m->H;
     PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn1, rstd1, eps, st));
-    NC_TRY(gemm(m, (int)N, W, C, xn1, C, 1, wptr(m, tensor(m, l, 0)), C, 1, NC_EP_STORE, qkv, W, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, (int)N, W, C, xn1, C, 1, wptr(m, tensor(m, l, 0)), C, 1, NC_EP_STORE, qkv, W, nullptr, 0, st));
     PROF(NC_PROF_ROPE, 0, (double)N * nh * (2.0 * a * m->hd + 4),
          launch_rope_qknorm_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, rstdqk, m->rope_tab, eps, st));
     PROF(NC_PROF_ATTN_FWD, attn_fl, (double)N * (W + Hd) * a + 4.0 * N * m->H,
          attn_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, st));
-    NC_TRY(gemm(m, (int)N, C, Hd, o, Hd, 1, wptr(m, tensor(m, l, 3)), Hd, 1, NC_EP_ACCUM_F32, m->x, C, nullptr, 0,
+    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, (int)N, C, Hd, o, Hd, 1, wptr(m, tensor(m, l, 3)), Hd, 1, NC_EP_ACCUM_F32, m->x, C, nullptr, 0,
                 st));
     PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn2, rstd2, eps, st));
-    NC_TRY(gemm(m, (int)N, F, C, xn2, C, 1, wptr(m, tensor(m, l, 4)), C, 1, NC_EP_RELU2, r, F, h, F, st));
-    NC_TRY(gemm(m, (int)N, C, F, h, F, 1, wptr(m, tensor(m, l, 5)), F, 1, NC_EP_ACCUM_F32, m->x, C, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, (int)N, F, C, xn2, C, 1, wptr(m, tensor(m, l, 4)), C, 1, NC_EP_RELU2, r, F, h, F, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, (int)N, C, F, h, F, 1, wptr(m, tensor(m, l, 5)), F, 1, NC_EP_ACCUM_F32, m->x, C, nullptr, 0, st));
     m->launches += 4;
   }
   PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, m->xf, m->rstd_f, eps, st));
@@ -462,22 +471,22 @@ static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int 
     const ParamTensor &tq = tensor(m, l, 0), &to = tensor(m, l, 3), &tfc = tensor(m, l, 4),
                       &tpj = tensor(m, l, 5);
     // MLP: x2 = x1 + relu(xn2 Wfc^T)^2 Wproj^T
-    NC_TRY(gemm(m, C, F, n, m->dx_act, C, 0, h, F, 0, NC_EP_STORE_F32, grads + tpj.off, F, nullptr, 0, st));
-    NC_TRY(gemm(m, n, F, C, m->dx_act, C, 1, wptr(m, tpj), F, 0, NC_EP_RELU2_BWD, m->du, F, r, F, st));
-    NC_TRY(gemm(m, F, C, n, m->du, F, 0, xn2, C, 0, NC_EP_STORE_F32, grads + tfc.off, C, nullptr, 0, st));
-    NC_TRY(gemm(m, n, C, F, m->du, F, 1, wptr(m, tfc), C, 0, NC_EP_STORE_F32, m->dxn, C, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, F, n, m->dx_act, C, 0, h, F, 0, NC_EP_STORE_F32, grads + tpj.off, F, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, F, C, m->dx_act, C, 1, wptr(m, tpj), F, 0, NC_EP_RELU2_BWD, m->du, F, r, F, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_DW, F, C, n, m->du, F, 0, xn2, C, 0, NC_EP_STORE_F32, grads + tfc.off, C, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, C, F, m->du, F, 1, wptr(m, tfc), C, 0, NC_EP_STORE_F32, m->dxn, C, nullptr, 0, st));
     PROF(NC_PROF_NORM, 0, nb_by,
          launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, xn2, rstd2, m->dx, m->dtype == NC_BF16 ? m->dx_act : nullptr,
                             st));
     // attention: x1 = x + o Wo^T
-    NC_TRY(gemm(m, C, Hd, n, m->dx_act, C, 0, o, Hd, 0, NC_EP_STORE_F32, grads + to.off, Hd, nullptr, 0, st));
-    NC_TRY(gemm(m, n, Hd, C, m->dx_act, C, 1, wptr(m, to), Hd, 0, NC_EP_STORE, m->dout, Hd, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, Hd, n, m->dx_act, C, 0, o, Hd, 0, NC_EP_STORE_F32, grads + to.off, Hd, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, Hd, C, m->dx_act, C, 1, wptr(m, to), Hd, 0, NC_EP_STORE, m->dout, Hd, nullptr, 0, st));
     PROF(NC_PROF_ATTN_BWD, attn_fl, (double)N * (2.0 * W + 2.0 * Hd) * a + 8.0 * N * m->H,
          attn_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, st));
     PROF(NC_PROF_ROPE, 0, (double)N * nh * (3.0 * a * m->hd + 4),
          launch_rope_qknorm_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, m->dqkv, qkv, rstdqk, m->rope_tab, st));
-    NC_TRY(gemm(m, W, C, n, m->dqkv, W, 0, xn1, C, 0, NC_EP_STORE_F32, grads + tq.off, C, nullptr, 0, st));
-    NC_TRY(gemm(m, n, C, W, m->dqkv, W, 1, wptr(m, tq), C, 0, NC_EP_STORE_F32, m->dxn, C, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_DW, W, C, n, m->dqkv, W, 0, xn1, C, 0, NC_EP_STORE_F32, grads + tq.off, C, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, C, W, m->dqkv, W, 1, wptr(m, tq), C, 0, NC_EP_STORE_F32, m->dxn, C, nullptr, 0, st));
     PROF(NC_PROF_NORM, 0, nb_by,
          launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, xn1, rstd1, m->dx, m->dtype == NC_BF16 ? m->dx_act : nullptr,
                             st));
@@ -504,11 +513,11 @@ static nc_status step(nc_model* m, const int32_t* tokens, const int32_t* targets
   for (int64_t c0 = 0; c0 < N; c0 += m->chunk_rows) {
     const int nc = (int)std::min<int64_t>(m->chunk_rows, N - c0);
     const void* xfc = (const uint8_t*)m->xf + (size_t)c0 * C * m->act;
-    NC_TRY(gemm(m, nc, V, C, xfc, C, 1, Wlm, C, 1, NC_EP_STORE, m->logits, V, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_LM, nc, V, C, xfc, C, 1, Wlm, C, 1, NC_EP_STORE, m->logits, V, nullptr, 0, st));
     PROF(NC_PROF_CE, 0, (double)nc * (2.0 * V * m->act + 8),
          launch_cross_entropy(m->dtype, nc, V, m->logits, V, targets + c0, m->rowloss + c0, scale, m->err, st));
-    NC_TRY(gemm(m, nc, C, V, m->logits, V, 1, Wlm, C, 0, NC_EP_STORE_F32, m->dxn + c0 * C, C, nullptr, 0, st));
-    NC_TRY(gemm(m, V, C, nc, m->logits, V, 0, xfc, C, 0, c0 == 0 ? NC_EP_STORE_F32 : NC_EP_ACCUM_F32,
+    NC_TRY(gemm(m, NC_PROF_GEMM_LM, nc, C, V, m->logits, V, 1, Wlm, C, 0, NC_EP_STORE_F32, m->dxn + c0 * C, C, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_LM, V, C, nc, m->logits, V, 0, xfc, C, 0, c0 == 0 ? NC_EP_STORE_F32 : NC_EP_ACCUM_F32,
                 grads + tl.off, C, nullptr, 0, st));
     m->launches += 1;
   }
@@ -551,7 +560,7 @@ extern "C" nc_status nc_forward_logits(nc_model* m, const int32_t* tokens, int32
   m->launches = 0;
   NC_TRY(forward_trunk(m, tokens, B, T, st));
   const int64_t N = (int64_t)B * T;
-  NC_TRY(gemm(m, (int)N, m->V, m->C, m->xf, m->C, 1, wptr(m, m->layout.back()), m->C, 1, NC_EP_STORE_F32, logits,
+  NC_TRY(gemm(m, NC_PROF_GEMM_LM, (int)N, m->V, m->C, m->xf, m->C, 1, wptr(m, m->layout.back()), m->C, 1, NC_EP_STORE_F32, logits,
               m->V, nullptr, 0, st));
   return NC_OK;
 }
@@ -567,7 +576,7 @@ extern "C" nc_status nc_forward_row_losses(nc_model* m, const int32_t* tokens, c
   for (int64_t c0 = 0; c0 < N; c0 += m->chunk_rows) {
     const int nc = (int)std::min<int64_t>(m->chunk_rows, N - c0);
     const void* xfc = (const uint8_t*)m->xf + (size_t)c0 * m->C * m->act;
-    NC_TRY(gemm(m, nc, m->V, m->C, xfc, m->C, 1, wptr(m, m->layout.back()), m->C, 1, NC_EP_STORE, m->logits, m->V,
+    NC_TRY(gemm(m, NC_PROF_GEMM_LM, nc, m->V, m->C, xfc, m->C, 1, wptr(m, m->layout.back()), m->C, 1, NC_EP_STORE, m->logits, m->V,
                 nullptr, 0, st));
     NC_TRY(launch_cross_entropy(m->dtype, nc, m->V, m->logits, m->V, targets + c0, losses + c0, 1.f, m->err, st));
   }
@@ -578,14 +587,17 @@ extern "C" nc_status nc_forward_row_losses(nc_model* m, const int32_t* tokens, c
 
 static bool dtype_ok(int32_t d) { return d == NC_FP32 || d == NC_BF16; }
 
+extern "C" size_t nc_gemm_workspace_bytes(void) { return gemm_tc_workspace_bytes(); }
+
 extern "C" nc_status nc_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A, int64_t lda,
                                 int32_t a_kmajor, const void* B, int64_t ldb, int32_t b_kmajor, int32_t ep, void* D,
-                                int64_t ldd, void* aux, int64_t ldaux, void* stream) {
+                                int64_t ldd, void* aux, int64_t ldaux, void* workspace, size_t workspace_bytes,
+                                void* stream) {
   if (!dtype_ok(dtype) || !A || !B || !D || ep < 0 || ep > NC_EP_RELU2_BWD) return NC_ERR_ARG;
   if (M < 0 || N < 0 || K < 0) return NC_ERR_ARG;
   if (dtype == NC_BF16)
     return launch_gemm_tc(M, N, K, (const bf16*)A, lda, a_kmajor, (const bf16*)B, ldb, b_kmajor, ep, D, ldd, aux,
-                          ldaux, nullptr, as_stream(stream));
+                          ldaux, nullptr, workspace, workspace ? workspace_bytes : 0, as_stream(stream));
   return launch_gemm_simt(dtype, M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, ep, D, ldd, aux, ldaux,
                           as_stream(stream));
 }

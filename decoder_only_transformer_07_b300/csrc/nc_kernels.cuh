@@ -32,9 +32,12 @@ nc_status launch_gemm_simt(int dtype, int M, int N, int K, const void* A, int64_
                            const void* B, int64_t ldb, int b_kmajor, int ep, void* D, int64_t ldd,
                            void* aux, int64_t ldaux, cudaStream_t st);
 // tcgen05 tensor-core GEMM (bf16 operands, fp32 accumulation in TMEM).
+// ws (optional, 16-byte aligned): stream-K partial tiles for fp32-output GEMMs
+// with few output tiles; gemm_tc_workspace_bytes() is enough for any shape.
 nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_kmajor,
                          const bf16* B, int64_t ldb, int b_kmajor, int ep, void* D, int64_t ldd,
-                         void* aux, int64_t ldaux, int32_t* err, cudaStream_t st);
+                         void* aux, int64_t ldaux, int32_t* err, void* ws, size_t ws_bytes, cudaStream_t st);
+size_t gemm_tc_workspace_bytes();
 
 nc_status launch_attn_fwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv, void* o,
                                float* lse, cudaStream_t st);

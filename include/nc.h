@@ -161,14 +161,20 @@ int64_t nc_last_launch_count(const nc_model* m);
  *   NC_EP_RELU2_BWD D (dtype) = acc * 2 * aux   (aux holds relu(u))
  * ldd / ldaux are leading dimensions in elements.  NC_BF16 runs the tcgen05
  * tensor-core kernel (lda, ldb multiples of 8, 16-byte aligned bases);
- * NC_FP32 runs exact fp32 FMA. */
+ * NC_FP32 runs exact fp32 FMA.  workspace may be NULL (see below). */
 enum { NC_EP_STORE = 0, NC_EP_STORE_F32 = 1, NC_EP_ACCUM_F32 = 2,
        NC_EP_RELU2 = 3, NC_EP_RELU2_BWD = 4 };
 nc_status nc_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K,
                      const void* A, int64_t lda, int32_t a_kmajor,
                      const void* B, int64_t ldb, int32_t b_kmajor,
                      int32_t ep, void* D, int64_t ldd, void* aux, int64_t ldaux,
-                     void* stream);
+                     void* workspace, size_t workspace_bytes, void* stream);
+/* Device workspace (bytes) that lets an NC_BF16 GEMM with an fp32 epilogue
+ * and few output tiles run stream-K: each CTA takes an equal share of the
+ * (tile, k-block) work and tiles split between CTAs are summed afterwards in
+ * CTA order (deterministic).  With a NULL or smaller workspace the GEMM runs
+ * one CTA per output tile. */
+size_t nc_gemm_workspace_bytes(void);
 
 /* RMSNorm without gain over rows of x (float [rows, C]):
  * y (dtype) = x * rstd, rstd (float [rows]) = 1/sqrt(mean(x^2) + eps). */
@@ -239,7 +245,10 @@ nc_status nc_op_embed_bwd(int64_t n, int32_t C, int32_t V, const int32_t* tokens
  * ---------------------------------------------------------------------- */
 enum { NC_PROF_GEMM = 0, NC_PROF_ATTN_FWD = 1, NC_PROF_ATTN_BWD = 2, NC_PROF_NORM = 3,
        NC_PROF_ROPE = 4, NC_PROF_CE = 5, NC_PROF_EMBED = 6, NC_PROF_CAST = 7,
-       NC_PROF_OTHER = 8, NC_PROF_CLASSES = 9 };
+       NC_PROF_OTHER = 8,
+       /* sub-classes of NC_PROF_GEMM (each GEMM is counted in one of these too) */
+       NC_PROF_GEMM_FWD = 9, NC_PROF_GEMM_DX = 10, NC_PROF_GEMM_DW = 11, NC_PROF_GEMM_LM = 12,
+       NC_PROF_CLASSES = 13 };
 nc_status nc_profile_enable(nc_model* m, int32_t on);
 nc_status nc_profile_read(nc_model* m, int32_t cls, double* ms, int64_t* launches,
                           double* flops, double* bytes);

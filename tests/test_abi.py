@@ -61,4 +61,4 @@ def test_null_arguments_rejected():
     lib = nc.lib()
     assert lib.nc_model_create(None, 1, None) == 3
     assert lib.nc_forward_backward(None, None, None, 1, 1, None, None, None) == 3
-    assert lib.nc_op_gemm(1, 4, 4, 4, None, 4, 1, None, 4, 1, 0, None, 4, None, 0, None) == 3
+    assert lib.nc_op_gemm(1, 4, 4, 4, None, 4, 1, None, 4, 1, 0, None, 4, None, 0, None, 0, None) == 3
