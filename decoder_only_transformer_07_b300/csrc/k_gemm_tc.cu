@@ -10,7 +10,8 @@
 //               and tcgen05.commit to free ring slots / publish accumulators;
 //   warp 2      allocates / frees 2*BN TMEM columns (two accumulators, so the
 //               epilogue of tile i overlaps the main loop of tile i+1);
-//   warps 4..7  epilogue: tcgen05.ld of their 32-lane quarter, fused op,
+//   warps 4..11 epilogue: tcgen05.ld of their 32-lane quarter (warps w and
+//               w+4 share a quarter and split the tile's columns), fused op,
 //               vector stores to global memory.
 // Operands may be K-major ([rows][K]) or MN-major ([K][rows]); the forward
 // uses K-major A and B, dX = dY W uses an MN-major B, and dW = dY^T X uses
@@ -25,7 +26,8 @@
 
 #define TC_BM 128
 #define TC_BK 64
-#define TC_THREADS 256
+#define TC_EPI_WARPS 8                          // two per TMEM lane quarter
+#define TC_THREADS (128 + 32 * TC_EPI_WARPS)
 
 #ifndef NC_MN_SWAP_LBO_SBO
 #define NC_MN_SWAP_LBO_SBO 0
@@ -42,53 +44,35 @@ struct TcParams {
   int tiles_m, tiles_n, num_kb;
   int32_t* err;
   uint64_t wait_ns;
-  // stream-K: CTA c owns the flattened (tile, k-block) range [c*per, (c+1)*per);
-  // tiles it covers only in part go to ws[c][0 (first) or 1 (last)][128][BN] fp32
-  int streamk;
-  int64_t per;
+  // split-K: work unit u covers k-blocks [s*kps, (s+1)*kps) of tile t, with
+  // s = u / tiles and t = u % tiles, so CTAs running together stream the same
+  // K slice (L2 reuse).  With splits > 1 every unit writes its fp32 partial
+  // to ws[s][t][128][BN] and a fix-up kernel sums the slices in order.
+  int splits, kps;
   float* ws;
 };
 
-// One unit of work of a CTA: k-blocks [k0, k1) of output tile t.
+// One unit of work of a CTA: k-blocks [k0, k1) of output tile t (slice s).
 struct TcSeg {
-  int t, k0, k1;
-  bool full, first;
+  int t, s, k0, k1;
 };
 
-// Iterates the segments a CTA owns, identically in every role.
+// Iterates the units a CTA owns, identically in every role.
 struct TcSegIter {
-  int64_t g, end;       // stream-K cursor in the flattened k-block space
-  int t, stride, tiles; // plain mode
-  bool sk, started;
+  int u, stride, units, tiles;
   __device__ TcSegIter(const TcParams& p, int cta, int grid) {
-    sk = p.streamk != 0;
     tiles = p.tiles_m * p.tiles_n;
-    if (sk) {
-      const int64_t total = (int64_t)tiles * p.num_kb;
-      g = (int64_t)cta * p.per;
-      end = g + p.per < total ? g + p.per : total;
-    }
-    t = cta;
+    units = tiles * p.splits;
+    u = cta - grid;
     stride = grid;
-    started = false;
   }
-  __device__ bool next(const TcParams& p, TcSeg& s) {
-    if (!sk) {
-      if (started) t += stride;
-      started = true;
-      if (t >= tiles) return false;
-      s.t = t; s.k0 = 0; s.k1 = p.num_kb; s.full = true; s.first = true;
-      return true;
-    }
-    if (g >= end) return false;
-    s.first = !started;
-    started = true;
-    s.t = (int)(g / p.num_kb);
-    s.k0 = (int)(g % p.num_kb);
-    const int64_t rem = end - g;
-    s.k1 = (int)((p.num_kb - s.k0) < rem ? p.num_kb : s.k0 + rem);
-    s.full = (s.k0 == 0 && s.k1 == p.num_kb);
-    g += s.k1 - s.k0;
+  __device__ bool next(const TcParams& p, TcSeg& g) {
+    u += stride;
+    if (u >= units) return false;
+    g.s = u / tiles;
+    g.t = u - g.s * tiles;
+    g.k0 = g.s * p.kps;
+    g.k1 = min(p.num_kb, g.k0 + p.kps);
     return true;
   }
 };
@@ -230,7 +214,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 4); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], TC_EPI_WARPS); }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -327,6 +311,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp >= 4) {
     // ---------------- epilogue
     const int quarter = warp & 3;
+    const int c_lo = ((warp - 4) >> 2) * (BN / 2);   // this warp's half of the columns
     int local = 0;
     TcSegIter it(p, blockIdx.x, gridDim.x);
     TcSeg sg;
@@ -339,23 +324,41 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc_fence_after();
       const int64_t m = (int64_t)tm * TC_BM + quarter * 32 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      // a tile this CTA covers only in part: its fp32 partial goes to the workspace
-      float* part = sg.full ? nullptr
-                            : p.ws + ((size_t)blockIdx.x * 2 + (sg.first ? 0 : 1)) * TC_BM * BN +
-                                  (size_t)(quarter * 32 + lane) * BN;
+      // split-K: this unit's fp32 partial goes to the workspace
+      float* part = (p.splits > 1)
+                        ? p.ws + ((size_t)sg.s * (p.tiles_m * p.tiles_n) + sg.t) * TC_BM * BN +
+                              (size_t)(quarter * 32 + lane) * BN
+                        : nullptr;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
+      for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
+        const int n0 = tn * BN + c;
+        const bool row_ok = (m < p.M) && (n0 < p.N);
+        // residual / accumulate target loaded before the TMEM read so that
+        // the two latencies overlap
+        float4 prev[8];
+        const bool pre = !part && row_ok && p.ep == NC_EP_ACCUM_F32 && (n0 + 32 <= p.N) &&
+                         ((((uintptr_t)((float*)p.D + m * p.ldd + n0)) & 15) == 0);
+        if (pre) {
+          const float4* src = reinterpret_cast<const float4*>((float*)p.D + m * p.ldd + n0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) prev[i] = src[i];
+        }
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + c, r);
         tmem_ld_wait();
-        const int n0 = tn * BN + c;
         if (part) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4*>(part + c + i) =
                 make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
                             __uint_as_float(r[i + 3]));
-        } else if (m < p.M && n0 < p.N) {
+        } else if (pre) {
+          float4* dst = reinterpret_cast<float4*>((float*)p.D + m * p.ldd + n0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(prev[i].x + __uint_as_float(r[4 * i]), prev[i].y + __uint_as_float(r[4 * i + 1]),
+                                 prev[i].z + __uint_as_float(r[4 * i + 2]), prev[i].w + __uint_as_float(r[4 * i + 3]));
+        } else if (row_ok) {
           tc_epilogue_row(p, m, n0, r);
         }
       }
@@ -370,29 +373,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == 2) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
-// Stream-K fix-up: for every tile split across CTAs, add the partials in CTA
-// order (a fixed order, so results are bitwise reproducible) and apply the
-// fp32 epilogue (store or accumulate).  One block per tile.
+// Split-K fix-up: out (op)= sum over slices s = 0..splits-1, in that order
+// (bitwise reproducible), of the fp32 partial tiles.  One block per tile.
 template <int BN>
 __global__ void __launch_bounds__(256) k_gemm_tc_fixup(TcParams p) {
   const int t = blockIdx.x;
-  const int64_t lo = (int64_t)t * p.num_kb, hi = lo + p.num_kb - 1;
-  const int c0 = (int)(lo / p.per), c1 = (int)(hi / p.per);
-  if (c0 == c1) return;                     // written whole by one CTA
+  const int tiles = p.tiles_m * p.tiles_n;
   int tm, tn;
   tile_coords(p, t, tm, tn);
   for (int i = threadIdx.x; i < TC_BM * BN / 4; i += blockDim.x) {
     const int r = (i * 4) / BN, cc = (i * 4) % BN;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = c0; c <= c1; ++c) {
-      const int first_tile = (int)(((int64_t)c * p.per) / p.num_kb);
-      const int slot = (t == first_tile) ? 0 : 1;
-      const float4 v = *reinterpret_cast<const float4*>(p.ws + ((size_t)c * 2 + slot) * TC_BM * BN + (size_t)r * BN + cc);
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-    }
     const int64_t m = (int64_t)tm * TC_BM + r;
     const int n = tn * BN + cc;
-    if (m >= p.M) continue;
+    if (m >= p.M || n >= p.N) continue;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sl = 0; sl < p.splits; ++sl) {
+      const float4 v = *reinterpret_cast<const float4*>(p.ws + ((size_t)sl * tiles + t) * TC_BM * BN +
+                                                        (size_t)r * BN + cc);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
     float* d = (float*)p.D + m * p.ldd + n;
     const float a[4] = {acc.x, acc.y, acc.z, acc.w};
     for (int j = 0; j < 4 && n + j < p.N; ++j) d[j] = (p.ep == NC_EP_ACCUM_F32) ? d[j] + a[j] : a[j];
@@ -441,39 +440,38 @@ static nc_status launch_tc_bn(TcParams p, const CUtensorMap& ta, const CUtensorM
     attr_set = true;
   }
   const int tiles = p.tiles_m * p.tiles_n;
-  int grid = std::min(tiles, g_num_sms);
-  // Stream-K when whole tiles would leave the last wave badly filled (fp32
-  // outputs only: the weight gradients, whose K is the token count).
-  p.streamk = 0;
+  // Split K when whole tiles would leave the last wave badly filled (fp32
+  // outputs only: the weight gradients and the lm_head input gradient, whose
+  // K is the token count or the vocabulary).  Cost model per split count S:
+  // waves(S) * (k-blocks per slice) * t_kb + partial-tile traffic.
+  p.splits = 1;
+  p.kps = p.num_kb;
   const bool f32_out = (p.ep == NC_EP_STORE_F32 || p.ep == NC_EP_ACCUM_F32);
-  if (f32_out && p.ws && tiles < 8 * g_num_sms && p.num_kb >= 8) {
-    const int waves = (tiles + g_num_sms - 1) / g_num_sms;
-    const double fill = (double)tiles / ((double)waves * g_num_sms);
-    if (fill < 0.9 && ws_bytes >= (size_t)g_num_sms * 2 * TC_BM * BN * sizeof(float)) {
-      const int64_t total = (int64_t)tiles * p.num_kb;
-      grid = g_num_sms;
-      p.per = (total + grid - 1) / grid;
-      p.streamk = 1;
+  if (f32_out && p.ws && tiles < 4 * g_num_sms) {
+    const double t_kb = 0.35e-6;                                   // s per 128 x BN x 64 block, one SM
+    const double tile_bytes = 2.0 * TC_BM * BN * sizeof(float);    // write + read of one partial
+    double best = 1e30;
+    for (int S = 1; S <= 16; ++S) {
+      const int kps = (p.num_kb + S - 1) / S;
+      if (S > 1 && (kps < 16 || (size_t)S * tiles * TC_BM * BN * sizeof(float) > ws_bytes)) break;
+      const int waves = (tiles * S + g_num_sms - 1) / g_num_sms;
+      const double cost = waves * kps * t_kb + (S > 1 ? S * tiles * tile_bytes / 6.0e12 : 0.0);
+      if (cost < best * 0.98) { best = cost; p.splits = S; p.kps = kps; }
     }
+    p.splits = (p.num_kb + p.kps - 1) / p.kps;
   }
+  const int grid = std::min(tiles * p.splits, g_num_sms);
   kern<<<grid, TC_THREADS, TcCfg<BN>::SMEM, st>>>(ta, tb, p);
   NC_CUDA_TRY(cudaGetLastError());
-  if (p.streamk) {
+  if (p.splits > 1) {
     k_gemm_tc_fixup<BN><<<tiles, 256, 0, st>>>(p);
     NC_CUDA_TRY(cudaGetLastError());
   }
   return NC_OK;
 }
 
-size_t gemm_tc_workspace_bytes() {
-  if (!g_num_sms) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return (size_t)160 * 2 * TC_BM * 256 * sizeof(float);
-  }
-  return (size_t)g_num_sms * 2 * TC_BM * 256 * sizeof(float);
-}
+// Split-K partials: up to 4 waves of 128 x 256 fp32 tiles per slice set.
+size_t gemm_tc_workspace_bytes() { return (size_t)256 << 20; }
 
 nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_kmajor, const bf16* B,
                          int64_t ldb, int b_kmajor, int ep, void* D, int64_t ldd, void* aux, int64_t ldaux,
@@ -499,8 +497,8 @@ nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_
   p.err = err;
   p.wait_ns = g_tc_wait_ns;
   p.ws = (float*)ws;
-  p.streamk = 0;
-  p.per = 0;
+  p.splits = 1;
+  p.kps = 0;
   if (ws && (((uintptr_t)ws) & 15)) return NC_ERR_ARG;
   CUtensorMap ta, tb;
   bool ok;

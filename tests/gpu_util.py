@@ -29,7 +29,8 @@ def rel_close(got, want, rtol, floor_frac=0.1):
     """
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
-    rms = float(np.sqrt(np.mean(want * want))) if want.size else 0.0
+    nz = want[want != 0]            # rms over the entries that carry a value (the
+    rms = float(np.sqrt(np.mean(nz * nz))) if nz.size else 0.0   # zero rows of dwte are not a scale)
     bound = rtol * np.maximum(np.abs(want), floor_frac * rms)
     err = np.abs(got - want)
     bad = err > bound

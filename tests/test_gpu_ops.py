@@ -238,11 +238,12 @@ def test_attention_fwd_bwd(hd, H, Hkv, T, dt):
         ok, worst = rel_close(to64(O), o_ref, 1e-4, 1e-2)
     else:
         # bf16 path: P is rounded to bf16 (2^-9 relative) before P V, so the
-        # error of an output element scales with rms(o), not with |o|: bound
-        # 2^-7 |o| + 2^-6 rms(o), about 3x the largest error bf16 rounding of
-        # P and of the stored o gives on these shapes.
+        # error of an output element scales with rms(o), not with |o|
+        # (sigma ~ 2^-9 rms(o) per element, 2^-9 relative for the bf16 store):
+        # per element 2^-7 |o| + 2^-5 rms(o) (about 6 sigma over ~5e5
+        # elements), and the aggregate cosine >= 0.99999.
         from tests.gpu_util import cosine
-        ok, worst = rel_close(to64(O), o_ref, 2.0 ** -7, 2.0)
+        ok, worst = rel_close(to64(O), o_ref, 2.0 ** -7, 4.0)
         assert cosine(to64(O), o_ref) > 0.99999
     assert ok, worst
     assert np.allclose(to64(L), lse_ref, rtol=1e-5, atol=1e-5)
