@@ -235,6 +235,33 @@ nc_status nc_op_embed_bwd(int64_t n, int32_t C, int32_t V, const int32_t* tokens
                           const float* dx, float* dwte, void* scratch, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Embedding backward that allocates nothing.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory,
+ * for example a host that gives this library only its input and output
+ * buffers under a device-memory budget fixed in advance, or a process whose
+ * allocator has already reserved the device's memory, where one more
+ * cudaMalloc would fail.  nc_op_embed_bwd needs caller-provided scratch;
+ * this variant computes the same result (bit for bit) using a scratch area
+ * in a file-scope device array of NC_NOALLOC_SCRATCH_BYTES that every GPU
+ * which loads the library keeps until the process exits.
+ *  - Sizes whose scratch (nc_embed_bwd_scratch_bytes(n, C, V)) exceeds
+ *    NC_NOALLOC_SCRATCH_BYTES are rejected with NC_ERR_UNSUPPORTED before any
+ *    GPU work; NULL pointers or non-positive sizes give NC_ERR_ARG.
+ *  - The first call on a device looks up the array's device address (a
+ *    one-time set-up per device, done with that device current); make that
+ *    first call before any stream capture.
+ *  - It calls no cudaMalloc/cudaFree and no allocating library routine.
+ *  - All calls share the one array, which keeps the last call's contents;
+ *    the counters are zeroed on the stream at the start of every call.
+ *    Calls that overlap on the GPU (different streams, or different host
+ *    threads) race on the array: issue them in order on one stream.
+ * Arguments are those of nc_op_embed_bwd without the scratch pointer.
+ * ---------------------------------------------------------------------- */
+#define NC_NOALLOC_SCRATCH_BYTES (64u << 20)
+nc_status nc_op_embed_bwd_noalloc(int64_t n, int32_t C, int32_t V, const int32_t* tokens,
+                                  const float* dx, float* dwte, void* stream);
+
+/* ------------------------------------------------------------------------
  * Per-kernel-class device timing of the step.  While enabled, every kernel
  * the step enqueues is bracketed by CUDA events on the caller's stream, and
  * its class, algorithmic FLOPs and algorithmic HBM bytes are recorded.
