@@ -1,0 +1,877 @@
+// Causal grouped-query flash attention on the 5th-generation tensor cores:
+// tcgen05.mma with fp32 accumulators in tensor memory (TMEM), operand tiles
+// staged by TMA into 128-byte-swizzled shared memory, bf16 in and out,
+// head_dim 64 or 128.  Query head h reads kv head h / (H / Hkv) (cosmicrealm
+// "noao-chat-0-项目总体介绍" §2.1 item 6); scores are q.k / sqrt(hd) under a
+// causal mask; the forward saves the natural-log logsumexp of every row.
+//
+// Layout: q, k, v are column blocks of the fused projection output
+// qkv[B*T, (H + 2 Hkv) * hd]; o and do are [B*T, H * hd]; lse and the
+// backward's D = rowsum(do * o) are fp32 [B, H, T].
+//
+// Every kernel is warp-specialised, 12 warps, one CTA per SM:
+//   warp 0      TMA producer (one elected thread)
+//   warp 1      MMA issuer (one thread issues tcgen05.mma / tcgen05.commit)
+//   warp 2      allocates and frees the 512 TMEM columns
+//   warp 3      (dK/dV kernel only) stages lse and D of each query tile
+//   warps 4-11  "softmax" warps: each thread owns one TMEM lane = one row of
+//               the score tile, so row reductions need no shuffles.
+//
+// Forward: a CTA takes 256 queries (two 128-row tiles i = 0, 1) of one
+//   (b, h) and streams the 128-key K and V tiles through a 3-slot ring.  Per
+//   key tile j the tensor core computes S_i = Q_i K_j^T into TMEM; warpgroup
+//   i turns its row of S_i into P = exp2(S * log2e/sqrt(hd) - m), writes P as
+//   bf16 into shared memory and the tensor core accumulates O_i += P V_j in
+//   TMEM.  The two tiles ping-pong: the tensor core works on one tile's
+//   matrix products while the other's warpgroup does its softmax.  The
+//   running max m is raised only when a row's new maximum exceeds it by more
+//   than 8 (log2 units), in which case the warp rescales its rows of O in
+//   TMEM; otherwise P <= 2^8, which bf16 and fp32 hold exactly enough.
+// Backward (deterministic, no atomics), with P recomputed from lse:
+//   dQ kernel    per 128-query tile, over key tiles 0..diagonal:
+//                S = Q K^T, dP = dO V^T (TMEM), dS = P (dP - D) (bf16, smem),
+//                dQ += dS K (TMEM);
+//   dK/dV kernel per 128-key tile, over the group's query heads and the
+//                64-query tiles from the diagonal on: S^T = K Q^T,
+//                dP^T = V dO^T (double-buffered in TMEM), P^T and dS^T (bf16,
+//                smem), dV += P^T dO, dK += dS^T Q (TMEM).
+// The 1/sqrt(hd) of dQ and dK is applied to the fp32 accumulators on output.
+//
+// Every mbarrier wait is bounded in time (the GEMM's limit): on expiry the
+// kernel raises the timeout bit of the error flag, stops issuing work, drains
+// its own TMA loads and MMAs (bounded again) and frees its TMEM.
+#include <cuda.h>
+
+#include "nc_kernels.cuh"
+#include "nc_ptx.cuh"
+
+extern uint64_t g_tc_wait_ns;
+
+namespace {
+
+constexpr int AT_THREADS = 384;
+constexpr uint32_t CHUNK128 = 128 * 128;   // one [128 rows][64 bf16] swizzled chunk
+constexpr uint32_t CHUNK64 = 64 * 128;     // one [64 rows][64 bf16] swizzled chunk
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.69314718055994531f;
+
+struct AtShape {
+  int B, T, H, Hkv, G;
+  int64_t ld_qkv, ld_o;
+  float scale_log2;   // log2(e) / sqrt(hd)
+  float scale;        // 1 / sqrt(hd)
+  int32_t* err;
+  uint64_t wait_ns;
+};
+
+// tcgen05.mma kind::f16 instruction descriptor: fp32 accumulator, bf16 A and
+// B, A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), M = 128, N = n.
+__device__ __forceinline__ uint32_t at_idesc(int n, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(n >> 3) << 17) | (8u << 24);
+}
+// K-major operand: rows of 64 elements (128 B) per chunk, chunks of `chunk`
+// bytes along K; the kk-th 16-deep slice starts 32 B further in its chunk.
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk, uint32_t chunk) {
+  return smem_desc(base + (uint32_t)(kk >> 2) * chunk + (uint32_t)(kk & 3) * 32u, 16u, 1024u);
+}
+// MN-major operand read from a [K rows][64-element MN chunks] tile: MN chunks
+// `chunk` bytes apart, 8-row K groups 1 KB apart, slice kk 16 rows further.
+__device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk, uint32_t chunk) {
+  return smem_desc(base + (uint32_t)kk * 2048u, chunk, 1024u);
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ bool at_wait(uint64_t* bar, uint32_t parity, const AtShape& sh, volatile int* abort_flag) {
+  if (mbar_wait_bounded(bar, parity, sh.wait_ns)) return true;
+  if (sh.err) atomicOr(sh.err, NC_DEVERR_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+// Every lane waits; the warp proceeds only if all lanes saw the phase.
+__device__ __forceinline__ bool at_wait_warp(uint64_t* bar, uint32_t parity, const AtShape& sh,
+                                             volatile int* abort_flag) {
+  const bool ok = at_wait(bar, parity, sh, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+
+// ======================================================================= forward
+template <int HD>
+struct FwdSmem {
+  static constexpr uint32_t TILE = 128 * HD * 2;          // one [128][HD] bf16 tile
+  static constexpr uint32_t P_BYTES = 2 * CHUNK128;       // [128 queries][128 keys] bf16
+  static constexpr uint32_t OFF_Q = 0;                    // Q0, Q1
+  static constexpr uint32_t OFF_KV = 2 * TILE;            // 3-slot ring: K0 V0 K1 V1 ...
+  static constexpr uint32_t OFF_P = OFF_KV + 3 * TILE;    // P0, P1
+  static constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    k_attn_fwd_tc(const __grid_constant__ CUtensorMap tm_qkv, AtShape sh, bf16* __restrict__ o,
+                  float* __restrict__ lse) {
+  using L = FwdSmem<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bar = (uint64_t*)(smem + L::OFF_BAR);
+  uint64_t* q_full = bar;          // [1]
+  uint64_t* kv_full = bar + 1;     // [3]
+  uint64_t* kv_empty = bar + 4;    // [3]
+  uint64_t* s_full = bar + 7;      // [2] S_i in TMEM
+  uint64_t* s_free = bar + 9;      // [2] S_i read into registers (4 warps)
+  uint64_t* p_full = bar + 11;     // [2] P_i in smem, O_i rescaled (4 warps)
+  uint64_t* pv_done = bar + 13;    // [2] O_i += P_i V complete
+  uint64_t* drain = bar + 15;
+  uint32_t* tmem_slot = (uint32_t*)(bar + 16);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = sh.B * sh.H;
+  const int nqb = (sh.T + 255) >> 8;
+  const int qb = nqb - 1 - (int)(blockIdx.x / BH);    // longest causal rows first
+  const int bh = blockIdx.x % BH, b = bh / sh.H, h = bh - b * sh.H, g = h / sh.G;
+  const int nt = (sh.T + 127) >> 7;
+  const int n0 = 2 * qb + 1;                           // key tiles of query tile 0
+  const int n1 = (2 * qb + 1 < nt) ? 2 * qb + 2 : 0;   // of query tile 1 (0: past the end)
+  const int nmax = n1 > 0 ? n1 : n0;
+  const int row0 = b * sh.T;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 3; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1); mbar_init(&s_free[i], 4); mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_qkv);
+  }
+  if (warp == 2) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;   // S0 cols 0-127, S1 128-255, O0 256.., O1 256+HD..
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    mbar_arrive_expect_tx(q_full, 2 * L::TILE);
+    for (int i = 0; i < 2; ++i)
+      for (int c = 0; c < HD / 64; ++c)
+        tma_load_2d(smem + L::OFF_Q + i * L::TILE + c * CHUNK128, &tm_qkv, q_full, h * HD + 64 * c,
+                    row0 + (2 * qb + i) * 128);
+    int issued = 0;
+    for (int c = 0; c < 2 * nmax && !*abort_flag; ++c) {
+      const int s = c % 3;
+      if (!at_wait(&kv_empty[s], ((c / 3) & 1) ^ 1, sh, abort_flag)) break;
+      const int col = ((c & 1) ? (sh.H + sh.Hkv + g) : (sh.H + g)) * HD;
+      mbar_arrive_expect_tx(&kv_full[s], L::TILE);
+      for (int cc = 0; cc < HD / 64; ++cc)
+        tma_load_2d(smem + L::OFF_KV + s * L::TILE + cc * CHUNK128, &tm_qkv, &kv_full[s], col + 64 * cc,
+                    row0 + (c >> 1) * 128);
+      ++issued;
+    }
+    // every load lands before the CTA exits (already so unless aborted)
+    mbar_wait_bounded(q_full, 0, sh.wait_ns);
+    for (int s = 0; s < 3; ++s) {
+      const int uses = issued / 3 + ((issued % 3) > s ? 1 : 0);
+      if (uses > 0) mbar_wait_bounded(&kv_full[s], (uses - 1) & 1, sh.wait_ns);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    const uint32_t id_s = at_idesc(128, 0), id_pv = at_idesc(HD, 1);
+    const uint32_t sq = smem_u32(smem + L::OFF_Q), skv = smem_u32(smem + L::OFF_KV);
+    const uint32_t sp = smem_u32(smem + L::OFF_P);
+    auto kv_ready = [&](int c) { return at_wait(&kv_full[c % 3], (c / 3) & 1, sh, abort_flag); };
+    auto issue_s = [&](int i, int j) -> bool {   // S_i = Q_i K_j^T
+      if (j > 0 && !at_wait(&s_free[i], (j - 1) & 1, sh, abort_flag)) return false;
+      tc_fence_after();
+      const uint32_t a = sq + i * L::TILE, kb = skv + ((2 * j) % 3) * L::TILE;
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        tc_mma_f16(tbase + i * 128, kdesc(a, kk, CHUNK128), kdesc(kb, kk, CHUNK128), id_s, kk > 0 ? 1u : 0u);
+      tc_commit(&s_full[i]);
+      return true;
+    };
+    auto issue_pv = [&](int i, int j) -> bool {  // O_i += P_i V_j
+      if (!at_wait(&p_full[i], j & 1, sh, abort_flag)) return false;
+      tc_fence_after();
+      const uint32_t a = sp + i * L::P_BYTES, vb = skv + ((2 * j + 1) % 3) * L::TILE;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        tc_mma_f16(tbase + 256 + i * HD, kdesc(a, kk, CHUNK128), mndesc(vb, kk, CHUNK128), id_pv,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(&pv_done[i]);
+      return true;
+    };
+    bool ok = at_wait(q_full, 0, sh, abort_flag) && kv_ready(0);
+    if (ok) ok = issue_s(0, 0);
+    if (ok && n1 > 0) ok = issue_s(1, 0);
+    if (ok) tc_commit(&kv_empty[0]);
+    for (int j = 0; ok && j < nmax; ++j) {
+      const bool more = j + 1 < nmax;
+      ok = kv_ready(2 * j + 1);
+      if (ok && j < n0) ok = issue_pv(0, j);
+      if (ok && more) ok = kv_ready(2 * j + 2);
+      if (ok && j + 1 < n0) ok = issue_s(0, j + 1);
+      if (ok && j < n1) ok = issue_pv(1, j);
+      if (ok) tc_commit(&kv_empty[(2 * j + 1) % 3]);
+      if (ok && j + 1 < n1) ok = issue_s(1, j + 1);
+      if (ok && more) tc_commit(&kv_empty[(2 * j + 2) % 3]);
+      if (*abort_flag) ok = false;
+    }
+    tc_commit(drain);
+    mbar_wait_bounded(drain, 0, sh.wait_ns);
+  } else if (warp >= 4) {
+    // ---------------- softmax warpgroups: warps 4-7 own query tile 0, 8-11 tile 1
+    const int i = (warp - 4) >> 2, quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int qt = 2 * qb + i;
+    const int qpos = qt * 128 + r;
+    const int n = i ? n1 : n0;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tbase + lane_off + i * 128;
+    const uint32_t tO = tbase + lane_off + 256 + i * HD;
+    const uint32_t sP = smem_u32(smem + L::OFF_P + i * L::P_BYTES) + r * 128;
+    const uint32_t swz = r & 7;
+    float m = 0.f, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!(ok = at_wait_warp(&s_full[i], j & 1, sh, abort_flag))) break;
+      tc_fence_after();
+      uint32_t x[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS + 32 * c, x + 32 * c);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[i]);
+      const int k0 = j * 128;
+      const bool diag = (j == qt) || (k0 + 128 > sh.T);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        float v = __uint_as_float(x[c]) * sh.scale_log2;
+        if (diag && (k0 + c > qpos || k0 + c >= sh.T)) v = -INFINITY;
+        x[c] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      // P_i's buffer and O_i are free once the previous O_i += P V completed
+      if (j > 0) {
+        if (!(ok = at_wait_warp(&pv_done[i], (j - 1) & 1, sh, abort_flag))) break;
+        tc_fence_after();
+      }
+      if (j == 0) {
+        m = (mx == -INFINITY) ? 0.f : mx;
+      } else {
+        const bool need = mx > m + 8.f;
+        if (__any_sync(0xffffffffu, need)) {
+          const float mn = need ? mx : m;
+          const float alpha = ex2_approx(m - mn);
+          l *= alpha;
+          m = mn;
+#pragma unroll 1
+          for (int c = 0; c < HD / 16; ++c) {
+            uint32_t ov[16];
+            tmem_ld_32x32b_x16(tO + 16 * c, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st_32x32b_x16(tO + 16 * c, ov);
+          }
+          tmem_st_wait();
+        }
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = ex2_approx(__uint_as_float(x[8 * u + 2 * e]) - m);
+          const float p1 = ex2_approx(__uint_as_float(x[8 * u + 2 * e + 1]) - m);
+          sum += p0 + p1;
+          w[e] = pack2(p0, p1);
+        }
+        st_shared_v4(sP + (u >> 3) * CHUNK128 + ((((uint32_t)u & 7u) ^ swz) << 4), w[0], w[1], w[2], w[3]);
+      }
+      l += sum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[i]);
+    }
+    if (ok && n > 0 && at_wait_warp(&pv_done[i], (n - 1) & 1, sh, abort_flag)) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      bf16* orow = o + (int64_t)(row0 + qpos) * sh.ld_o + (int64_t)h * HD;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld_32x32b_x32(tO + 32 * c, ov);
+        tmem_ld_wait();
+        if (qpos < sh.T) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 w;
+            w.x = pack2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
+            w.y = pack2(__uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+            w.z = pack2(__uint_as_float(ov[e + 4]) * inv, __uint_as_float(ov[e + 5]) * inv);
+            w.w = pack2(__uint_as_float(ov[e + 6]) * inv, __uint_as_float(ov[e + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + 32 * c + e) = w;
+          }
+        }
+      }
+      if (qpos < sh.T) lse[(int64_t)bh * sh.T + qpos] = (m + log2f(l)) * LN2;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tbase, 512);
+}
+
+// ======================================================================= backward: dQ
+template <int HD>
+struct DqSmem {
+  static constexpr uint32_t TILE = 128 * HD * 2;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_DO = TILE;
+  static constexpr uint32_t OFF_K = 2 * TILE;      // 2 slots
+  static constexpr uint32_t OFF_V = 4 * TILE;      // 2 slots
+  static constexpr uint32_t OFF_DS = 6 * TILE;     // [128 queries][128 keys] bf16
+  static constexpr uint32_t OFF_BAR = OFF_DS + 2 * CHUNK128;
+  static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
+                     AtShape sh, const float* __restrict__ lse, const float* __restrict__ Dv,
+                     bf16* __restrict__ dqkv) {
+  using L = DqSmem<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bar = (uint64_t*)(smem + L::OFF_BAR);
+  uint64_t* qd_full = bar;         // [1]
+  uint64_t* k_full = bar + 1;      // [2]
+  uint64_t* k_empty = bar + 3;     // [2]
+  uint64_t* v_full = bar + 5;      // [2]
+  uint64_t* v_empty = bar + 7;     // [2]
+  uint64_t* sdp_full = bar + 9;    // S and dP in TMEM
+  uint64_t* sdp_free = bar + 10;   // S and dP read (8 warps)
+  uint64_t* ds_full = bar + 11;    // dS in smem (8 warps)
+  uint64_t* ds_free = bar + 12;    // dQ += dS K complete
+  uint64_t* dq_done = bar + 13;
+  uint64_t* drain = bar + 14;
+  uint32_t* tmem_slot = (uint32_t*)(bar + 15);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = sh.B * sh.H;
+  const int nt = (sh.T + 127) >> 7;
+  const int qt = nt - 1 - (int)(blockIdx.x / BH);
+  const int bh = blockIdx.x % BH, b = bh / sh.H, h = bh - b * sh.H, g = h / sh.G;
+  const int n = qt + 1;
+  const int row0 = b * sh.T;
+
+  if (threadIdx.x == 0) {
+    mbar_init(qd_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1);
+    }
+    mbar_init(sdp_full, 1); mbar_init(sdp_free, 8); mbar_init(ds_full, 8); mbar_init(ds_free, 1);
+    mbar_init(dq_done, 1); mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_qkv);
+    prefetch_tmap(&tm_do);
+  }
+  if (warp == 2) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;   // S cols 0-127, dP 128-255, dQ 256..
+
+  if (warp == 0 && lane == 0) {
+    mbar_arrive_expect_tx(qd_full, 2 * L::TILE);
+    for (int c = 0; c < HD / 64; ++c) {
+      tma_load_2d(smem + L::OFF_Q + c * CHUNK128, &tm_qkv, qd_full, h * HD + 64 * c, row0 + qt * 128);
+      tma_load_2d(smem + L::OFF_DO + c * CHUNK128, &tm_do, qd_full, h * HD + 64 * c, row0 + qt * 128);
+    }
+    int k_issued = 0, v_issued = 0;
+    for (int j = 0; j < n && !*abort_flag; ++j) {
+      const int s = j & 1;
+      const uint32_t par = ((j >> 1) & 1) ^ 1;
+      if (!at_wait(&k_empty[s], par, sh, abort_flag)) break;
+      mbar_arrive_expect_tx(&k_full[s], L::TILE);
+      for (int c = 0; c < HD / 64; ++c)
+        tma_load_2d(smem + L::OFF_K + s * L::TILE + c * CHUNK128, &tm_qkv, &k_full[s], (sh.H + g) * HD + 64 * c,
+                    row0 + j * 128);
+      ++k_issued;
+      if (!at_wait(&v_empty[s], par, sh, abort_flag)) break;
+      mbar_arrive_expect_tx(&v_full[s], L::TILE);
+      for (int c = 0; c < HD / 64; ++c)
+        tma_load_2d(smem + L::OFF_V + s * L::TILE + c * CHUNK128, &tm_qkv, &v_full[s],
+                    (sh.H + sh.Hkv + g) * HD + 64 * c, row0 + j * 128);
+      ++v_issued;
+    }
+    mbar_wait_bounded(qd_full, 0, sh.wait_ns);
+    for (int s = 0; s < 2; ++s) {
+      const int ku = k_issued / 2 + ((k_issued % 2) > s ? 1 : 0);
+      const int vu = v_issued / 2 + ((v_issued % 2) > s ? 1 : 0);
+      if (ku > 0) mbar_wait_bounded(&k_full[s], (ku - 1) & 1, sh.wait_ns);
+      if (vu > 0) mbar_wait_bounded(&v_full[s], (vu - 1) & 1, sh.wait_ns);
+    }
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t id_s = at_idesc(128, 0), id_q = at_idesc(HD, 1);
+    const uint32_t sq = smem_u32(smem + L::OFF_Q), sdo = smem_u32(smem + L::OFF_DO);
+    const uint32_t sk = smem_u32(smem + L::OFF_K), sv = smem_u32(smem + L::OFF_V);
+    const uint32_t sds = smem_u32(smem + L::OFF_DS);
+    auto issue_sdp = [&](int j) -> bool {
+      const int s = j & 1;
+      const uint32_t par = (j >> 1) & 1;
+      if (!at_wait(&k_full[s], par, sh, abort_flag) || !at_wait(&v_full[s], par, sh, abort_flag)) return false;
+      if (j > 0 && !at_wait(sdp_free, (j - 1) & 1, sh, abort_flag)) return false;
+      tc_fence_after();
+      const uint32_t kb = sk + s * L::TILE, vb = sv + s * L::TILE;
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        tc_mma_f16(tbase, kdesc(sq, kk, CHUNK128), kdesc(kb, kk, CHUNK128), id_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        tc_mma_f16(tbase + 128, kdesc(sdo, kk, CHUNK128), kdesc(vb, kk, CHUNK128), id_s, kk > 0 ? 1u : 0u);
+      tc_commit(sdp_full);
+      tc_commit(&v_empty[s]);
+      return true;
+    };
+    bool ok = at_wait(qd_full, 0, sh, abort_flag) && issue_sdp(0);
+    for (int j = 0; ok && j < n; ++j) {
+      if (j + 1 < n) ok = issue_sdp(j + 1);
+      if (ok) ok = at_wait(ds_full, j & 1, sh, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t kb = sk + (j & 1) * L::TILE;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        tc_mma_f16(tbase + 256, kdesc(sds, kk, CHUNK128), mndesc(kb, kk, CHUNK128), id_q,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(ds_free);
+      tc_commit(&k_empty[j & 1]);
+      if (*abort_flag) ok = false;
+    }
+    if (ok) tc_commit(dq_done);
+    tc_commit(drain);
+    mbar_wait_bounded(drain, 0, sh.wait_ns);
+  } else if (warp >= 4) {
+    const int quarter = warp & 3, hf = (warp - 4) >> 2;   // hf: key columns [64 hf, 64 hf + 64)
+    const int r = quarter * 32 + lane;
+    const int qpos = qt * 128 + r;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tbase + lane_off + 64 * hf, tP = tS + 128;
+    const uint32_t sDS = smem_u32(smem + L::OFF_DS) + hf * CHUNK128 + r * 128;
+    const uint32_t swz = r & 7;
+    const bool valid = qpos < sh.T;
+    const float lse2 = valid ? lse[(int64_t)bh * sh.T + qpos] * LOG2E : INFINITY;
+    const float Dr = valid ? Dv[(int64_t)bh * sh.T + qpos] : 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!(ok = at_wait_warp(sdp_full, j & 1, sh, abort_flag))) break;
+      tc_fence_after();
+      uint32_t s[64], dp[64];
+      tmem_ld_32x32b_x32(tS, s);
+      tmem_ld_32x32b_x32(tS + 32, s + 32);
+      tmem_ld_32x32b_x32(tP, dp);
+      tmem_ld_32x32b_x32(tP + 32, dp + 32);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sdp_free);
+      const int k0 = j * 128 + 64 * hf;
+      const bool diag = (j == qt) || (j * 128 + 128 > sh.T);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float p = ex2_approx(__uint_as_float(s[c]) * sh.scale_log2 - lse2);
+        if (diag && (k0 + c > qpos || k0 + c >= sh.T)) p = 0.f;
+        s[c] = __float_as_uint(p * (__uint_as_float(dp[c]) - Dr));
+      }
+      if (j > 0) {
+        if (!(ok = at_wait_warp(ds_free, (j - 1) & 1, sh, abort_flag))) break;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float* f = reinterpret_cast<const float*>(s + 8 * u);
+        st_shared_v4(sDS + ((((uint32_t)u) ^ swz) << 4), pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]),
+                     pack2(f[6], f[7]));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+    }
+    if (ok && at_wait_warp(dq_done, 0, sh, abort_flag)) {
+      tc_fence_after();
+      bf16* dst = dqkv + (int64_t)(row0 + qpos) * sh.ld_qkv + (int64_t)h * HD + hf * (HD / 2);
+#pragma unroll 1
+      for (int c = 0; c < HD / 64; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tbase + lane_off + 256 + hf * (HD / 2) + 32 * c, v);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 w;
+            w.x = pack2(__uint_as_float(v[e]) * sh.scale, __uint_as_float(v[e + 1]) * sh.scale);
+            w.y = pack2(__uint_as_float(v[e + 2]) * sh.scale, __uint_as_float(v[e + 3]) * sh.scale);
+            w.z = pack2(__uint_as_float(v[e + 4]) * sh.scale, __uint_as_float(v[e + 5]) * sh.scale);
+            w.w = pack2(__uint_as_float(v[e + 6]) * sh.scale, __uint_as_float(v[e + 7]) * sh.scale);
+            *reinterpret_cast<uint4*>(dst + 32 * c + e) = w;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tbase, 512);
+}
+
+// ======================================================================= backward: dK, dV
+template <int HD>
+struct DkvSmem {
+  static constexpr uint32_t KT = 128 * HD * 2;       // one [128][HD] tile
+  static constexpr uint32_t QT = 64 * HD * 2;        // one [64][HD] tile
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = KT;
+  static constexpr uint32_t OFF_QS = 2 * KT;         // 3 stages of {Q, dO}
+  static constexpr uint32_t OFF_PT = OFF_QS + 3 * 2 * QT;   // [128 keys][64 queries] bf16
+  static constexpr uint32_t OFF_DST = OFF_PT + CHUNK128;
+  static constexpr uint32_t OFF_LD = OFF_DST + CHUNK128;    // 3 stages of {lse*log2e[64], D[64]}
+  static constexpr uint32_t OFF_BAR = OFF_LD + 3 * 128 * 4;
+  static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    k_attn_bwd_dkv_tc(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_do, AtShape sh, const float* __restrict__ lse,
+                      const float* __restrict__ Dv, bf16* __restrict__ dqkv) {
+  using L = DkvSmem<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bar = (uint64_t*)(smem + L::OFF_BAR);
+  uint64_t* kv_full = bar;          // [1]
+  uint64_t* q_full = bar + 1;       // [3] TMA bytes + 32 loader lanes
+  uint64_t* q_empty = bar + 4;      // [3]
+  uint64_t* st_full = bar + 7;      // [2] S^T, dP^T in TMEM buffer
+  uint64_t* st_free = bar + 9;      // [2] buffer read (8 warps)
+  uint64_t* pt_full = bar + 11;     // P^T, dS^T in smem (8 warps)
+  uint64_t* pt_free = bar + 12;     // dV, dK products complete
+  uint64_t* dkv_done = bar + 13;
+  uint64_t* drain = bar + 14;
+  uint32_t* tmem_slot = (uint32_t*)(bar + 15);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  float* LD = (float*)(smem + L::OFF_LD);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BG = sh.B * sh.Hkv;
+  const int kt = (int)(blockIdx.x / BG);              // key tile 0 sees the most queries: first
+  const int bg = blockIdx.x % BG, b = bg / sh.Hkv, g = bg - b * sh.Hkv;
+  const int nq = (sh.T + 63) >> 6;
+  const int per = nq - 2 * kt;                        // 64-query tiles from the diagonal on
+  const int n = sh.G * per;
+  const int row0 = b * sh.T;
+  auto step_q0 = [&](int i) { return (2 * kt + i % per) * 64; };
+  auto step_h = [&](int i) { return g * sh.G + i / per; };
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < 3; ++s) { mbar_init(&q_full[s], 33); mbar_init(&q_empty[s], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&st_full[i], 1); mbar_init(&st_free[i], 8); }
+    mbar_init(pt_full, 8); mbar_init(pt_free, 1); mbar_init(dkv_done, 1); mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_kv);
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_do);
+  }
+  if (warp == 2) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;   // S^T[2] cols 0,64; dP^T[2] 128,192; dV 256..; dK 256+HD..
+
+  if (warp == 0 && lane == 0) {
+    mbar_arrive_expect_tx(kv_full, 2 * L::KT);
+    for (int c = 0; c < HD / 64; ++c) {
+      tma_load_2d(smem + L::OFF_K + c * CHUNK128, &tm_kv, kv_full, (sh.H + g) * HD + 64 * c, row0 + kt * 128);
+      tma_load_2d(smem + L::OFF_V + c * CHUNK128, &tm_kv, kv_full, (sh.H + sh.Hkv + g) * HD + 64 * c,
+                  row0 + kt * 128);
+    }
+    int issued = 0;
+    for (int i = 0; i < n && !*abort_flag; ++i) {
+      const int s = i % 3;
+      if (!at_wait(&q_empty[s], ((i / 3) & 1) ^ 1, sh, abort_flag)) break;
+      const int h = step_h(i), q0 = step_q0(i);
+      uint8_t* dst = smem + L::OFF_QS + s * 2 * L::QT;
+      mbar_arrive_expect_tx(&q_full[s], 2 * L::QT);
+      for (int c = 0; c < HD / 64; ++c) {
+        tma_load_2d(dst + c * CHUNK64, &tm_q, &q_full[s], h * HD + 64 * c, row0 + q0);
+        tma_load_2d(dst + L::QT + c * CHUNK64, &tm_do, &q_full[s], h * HD + 64 * c, row0 + q0);
+      }
+      ++issued;
+    }
+    mbar_wait_bounded(kv_full, 0, sh.wait_ns);
+    for (int s = 0; s < 3; ++s) {
+      const int uses = issued / 3 + ((issued % 3) > s ? 1 : 0);
+      if (uses > 0) mbar_wait_bounded(&q_full[s], (uses - 1) & 1, sh.wait_ns);
+    }
+  } else if (warp == 3) {
+    // ---------------- lse / D of each query tile into the stage (every lane arrives)
+    for (int i = 0; i < n && !*abort_flag; ++i) {
+      const int s = i % 3;
+      if (!at_wait_warp(&q_empty[s], ((i / 3) & 1) ^ 1, sh, abort_flag)) break;
+      const int h = step_h(i), q0 = step_q0(i);
+      float* ld = LD + s * 128;
+      const int64_t base = ((int64_t)b * sh.H + h) * sh.T;
+#pragma unroll
+      for (int e = lane; e < 64; e += 32) {
+        const int q = q0 + e;
+        ld[e] = q < sh.T ? lse[base + q] * LOG2E : INFINITY;   // rows past the end get P = 0
+        ld[64 + e] = q < sh.T ? Dv[base + q] : 0.f;
+      }
+      mbar_arrive(&q_full[s]);
+    }
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t id_s = at_idesc(64, 0), id_kv = at_idesc(HD, 1);
+    const uint32_t sk = smem_u32(smem + L::OFF_K), sv = smem_u32(smem + L::OFF_V);
+    const uint32_t sqs = smem_u32(smem + L::OFF_QS);
+    const uint32_t spt = smem_u32(smem + L::OFF_PT), sdst = smem_u32(smem + L::OFF_DST);
+    auto issue_st = [&](int i) -> bool {
+      const int s = i % 3, buf = i & 1;
+      if (!at_wait(&q_full[s], (i / 3) & 1, sh, abort_flag)) return false;
+      if (i >= 2 && !at_wait(&st_free[buf], ((i - 2) >> 1) & 1, sh, abort_flag)) return false;
+      tc_fence_after();
+      const uint32_t qb = sqs + s * 2 * L::QT, db = qb + L::QT;
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        tc_mma_f16(tbase + buf * 64, kdesc(sk, kk, CHUNK128), kdesc(qb, kk, CHUNK64), id_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        tc_mma_f16(tbase + 128 + buf * 64, kdesc(sv, kk, CHUNK128), kdesc(db, kk, CHUNK64), id_s,
+                   kk > 0 ? 1u : 0u);
+      tc_commit(&st_full[buf]);
+      return true;
+    };
+    bool ok = at_wait(kv_full, 0, sh, abort_flag) && issue_st(0);
+    for (int i = 0; ok && i < n; ++i) {
+      if (i + 1 < n) ok = issue_st(i + 1);
+      if (ok) ok = at_wait(pt_full, i & 1, sh, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const int s = i % 3;
+      const uint32_t qb = sqs + s * 2 * L::QT, db = qb + L::QT;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_f16(tbase + 256, kdesc(spt, kk, CHUNK128), mndesc(db, kk, CHUNK64), id_kv,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_f16(tbase + 256 + HD, kdesc(sdst, kk, CHUNK128), mndesc(qb, kk, CHUNK64), id_kv,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(pt_free);
+      tc_commit(&q_empty[s]);
+      if (*abort_flag) ok = false;
+    }
+    if (ok) tc_commit(dkv_done);
+    tc_commit(drain);
+    mbar_wait_bounded(drain, 0, sh.wait_ns);
+  } else if (warp >= 4) {
+    const int quarter = warp & 3, hf = (warp - 4) >> 2;   // hf: query columns [32 hf, 32 hf + 32)
+    const int r = quarter * 32 + lane;
+    const int key = kt * 128 + r;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t swz = r & 7;
+    const uint32_t sPT = smem_u32(smem + L::OFF_PT) + r * 128, sDST = smem_u32(smem + L::OFF_DST) + r * 128;
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const int buf = i & 1, s = i % 3;
+      if (!(ok = at_wait_warp(&st_full[buf], (i >> 1) & 1, sh, abort_flag))) break;
+      tc_fence_after();
+      uint32_t st[32], dp[32];
+      tmem_ld_32x32b_x32(tbase + lane_off + buf * 64 + 32 * hf, st);
+      tmem_ld_32x32b_x32(tbase + lane_off + 128 + buf * 64 + 32 * hf, dp);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&st_free[buf]);
+      const int q0 = step_q0(i) + 32 * hf;
+      const bool diag = step_q0(i) < kt * 128 + 128;
+      const float4* ld4 = reinterpret_cast<const float4*>(LD + s * 128 + 32 * hf);
+      const float4* dd4 = reinterpret_cast<const float4*>(LD + s * 128 + 64 + 32 * hf);
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 l4 = ld4[c4], d4 = dd4[c4];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 4 * c4 + e;
+          float p = ex2_approx(__uint_as_float(st[c]) * sh.scale_log2 - lv[e]);
+          if (diag && q0 + c < key) p = 0.f;
+          st[c] = __float_as_uint(p);
+          dp[c] = __float_as_uint(p * (__uint_as_float(dp[c]) - dv[e]));
+        }
+      }
+      if (i > 0) {
+        if (!(ok = at_wait_warp(pt_free, (i - 1) & 1, sh, abort_flag))) break;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t off = ((((uint32_t)(4 * hf + u)) ^ swz) << 4);
+        const float* f = reinterpret_cast<const float*>(st + 8 * u);
+        st_shared_v4(sPT + off, pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+        const float* d = reinterpret_cast<const float*>(dp + 8 * u);
+        st_shared_v4(sDST + off, pack2(d[0], d[1]), pack2(d[2], d[3]), pack2(d[4], d[5]), pack2(d[6], d[7]));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pt_full);
+    }
+    if (ok && at_wait_warp(dkv_done, 0, sh, abort_flag)) {
+      tc_fence_after();
+      const bool valid = key < sh.T;
+      bf16* dk = dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + g) * HD + hf * (HD / 2);
+      bf16* dv = dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + sh.Hkv + g) * HD + hf * (HD / 2);
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const float sc = which ? sh.scale : 1.f;    // which = 1: dK (carries 1/sqrt(hd))
+        bf16* dst = which ? dk : dv;
+#pragma unroll 1
+        for (int c = 0; c < HD / 64; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + lane_off + 256 + which * HD + hf * (HD / 2) + 32 * c, v);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              uint4 w;
+              w.x = pack2(__uint_as_float(v[e]) * sc, __uint_as_float(v[e + 1]) * sc);
+              w.y = pack2(__uint_as_float(v[e + 2]) * sc, __uint_as_float(v[e + 3]) * sc);
+              w.z = pack2(__uint_as_float(v[e + 4]) * sc, __uint_as_float(v[e + 5]) * sc);
+              w.w = pack2(__uint_as_float(v[e + 6]) * sc, __uint_as_float(v[e + 7]) * sc);
+              *reinterpret_cast<uint4*>(dst + 32 * c + e) = w;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tbase, 512);
+}
+
+// D = rowsum(dO * O) per (row, head), fp32 [B, H, T]; one warp per (row, head).
+template <typename T>
+__global__ void k_attn_rowdot(int64_t rows, int H, int hd, int T_, int64_t ld_o, const T* __restrict__ o,
+                              const T* __restrict__ dout, float* __restrict__ Dv) {
+  int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int lane = threadIdx.x & 31;
+  if (w >= rows * H) return;
+  int64_t row = w / H;
+  int h = (int)(w % H);
+  const T* a = o + row * ld_o + (int64_t)h * hd;
+  const T* c = dout + row * ld_o + (int64_t)h * hd;
+  float s = 0.f;
+  for (int i = lane; i < hd; i += 32) s += to_f32(a[i]) * to_f32(c[i]);
+  s = warp_sum(s);
+  int b = (int)(row / T_), t = (int)(row % T_);
+  if (lane == 0) Dv[((int64_t)b * H + h) * T_ + t] = s;
+}
+
+bool at_shape(int B, int T, int H, int Hkv, int hd, int32_t* err, AtShape* sh) {
+  if (B <= 0 || T <= 0 || H <= 0 || Hkv <= 0 || H % Hkv || (hd != 64 && hd != 128)) return false;
+  if ((int64_t)B * T >= (1ll << 31) || (int64_t)B * H * ((T + 127) / 128) >= (1ll << 31)) return false;
+  sh->B = B; sh->T = T; sh->H = H; sh->Hkv = Hkv; sh->G = H / Hkv;
+  sh->ld_qkv = (int64_t)(H + 2 * Hkv) * hd;
+  sh->ld_o = (int64_t)H * hd;
+  sh->scale = 1.f / sqrtf((float)hd);
+  sh->scale_log2 = LOG2E * sh->scale;
+  sh->err = err;
+  sh->wait_ns = g_tc_wait_ns;
+  return true;
+}
+
+bool aligned16(const void* p) { return (((uintptr_t)p) & 15) == 0; }
+
+template <int HD>
+nc_status attn_fwd_tc(const AtShape& sh, const bf16* qkv, bf16* o, float* lse, cudaStream_t st) {
+  CUtensorMap tm;
+  if (!make_tmap_bf16_2d(&tm, qkv, sh.ld_qkv, (uint64_t)sh.B * sh.T, sh.ld_qkv, 64, 128)) return NC_ERR_CUDA;
+  static bool attr = false;
+  if (!attr) {
+    NC_CUDA_TRY(cudaFuncSetAttribute(k_attn_fwd_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)FwdSmem<HD>::BYTES));
+    attr = true;
+  }
+  const unsigned grid = (unsigned)((sh.T + 255) / 256) * (unsigned)(sh.B * sh.H);
+  k_attn_fwd_tc<HD><<<grid, AT_THREADS, FwdSmem<HD>::BYTES, st>>>(tm, sh, o, lse);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+template <int HD>
+nc_status attn_bwd_tc(const AtShape& sh, const bf16* qkv, const bf16* o, const float* lse, const bf16* dout,
+                      bf16* dqkv, float* Dv, cudaStream_t st) {
+  const int64_t rows = (int64_t)sh.B * sh.T;
+  k_attn_rowdot<bf16><<<cdiv(rows * sh.H, 8), 256, 0, st>>>(rows, sh.H, HD, sh.T, sh.ld_o, o, dout, Dv);
+  NC_CUDA_TRY(cudaGetLastError());
+  CUtensorMap tm_qkv128, tm_qkv64, tm_do128, tm_do64;
+  if (!make_tmap_bf16_2d(&tm_qkv128, qkv, sh.ld_qkv, rows, sh.ld_qkv, 64, 128) ||
+      !make_tmap_bf16_2d(&tm_qkv64, qkv, sh.ld_qkv, rows, sh.ld_qkv, 64, 64) ||
+      !make_tmap_bf16_2d(&tm_do128, dout, sh.ld_o, rows, sh.ld_o, 64, 128) ||
+      !make_tmap_bf16_2d(&tm_do64, dout, sh.ld_o, rows, sh.ld_o, 64, 64))
+    return NC_ERR_CUDA;
+  static bool attr = false;
+  if (!attr) {
+    NC_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd_dq_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)DqSmem<HD>::BYTES));
+    NC_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd_dkv_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)DkvSmem<HD>::BYTES));
+    attr = true;
+  }
+  const unsigned nt = (unsigned)((sh.T + 127) / 128);
+  k_attn_bwd_dq_tc<HD><<<nt * (unsigned)(sh.B * sh.H), AT_THREADS, DqSmem<HD>::BYTES, st>>>(
+      tm_qkv128, tm_do128, sh, lse, Dv, dqkv);
+  NC_CUDA_TRY(cudaGetLastError());
+  k_attn_bwd_dkv_tc<HD><<<nt * (unsigned)(sh.B * sh.Hkv), AT_THREADS, DkvSmem<HD>::BYTES, st>>>(
+      tm_qkv128, tm_qkv64, tm_do64, sh, lse, Dv, dqkv);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+}  // namespace
+
+nc_status launch_attn_fwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, bf16* o, float* lse,
+                             int32_t* err, cudaStream_t st) {
+  AtShape sh;
+  if (!at_shape(B, T, H, Hkv, hd, err, &sh)) return NC_ERR_ARG;
+  if (!aligned16(qkv) || !aligned16(o)) return NC_ERR_ARG;
+  return hd == 128 ? attn_fwd_tc<128>(sh, qkv, o, lse, st) : attn_fwd_tc<64>(sh, qkv, o, lse, st);
+}
+
+nc_status launch_attn_bwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, const bf16* o, const float* lse,
+                             const bf16* dout, bf16* dqkv, float* Dv, int32_t* err, cudaStream_t st) {
+  AtShape sh;
+  if (!at_shape(B, T, H, Hkv, hd, err, &sh)) return NC_ERR_ARG;
+  if (!aligned16(qkv) || !aligned16(dout) || !aligned16(dqkv)) return NC_ERR_ARG;
+  return hd == 128 ? attn_bwd_tc<128>(sh, qkv, o, lse, dout, dqkv, Dv, st)
+                   : attn_bwd_tc<64>(sh, qkv, o, lse, dout, dqkv, Dv, st);
+}

@@ -413,7 +413,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 // 2D bf16 tensor map over a row-major [outer][inner] matrix with leading
 // dimension ld (elements), box {box_inner, box_outer}, 128-byte swizzle.
-static bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, int64_t ld,
+bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, int64_t ld,
                       uint32_t box_inner, uint32_t box_outer) {
   auto enc = get_encode();
   if (!enc) return false;
@@ -427,7 +427,7 @@ static bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_
   return r == CUDA_SUCCESS;
 }
 
-static int g_num_sms = 0;
+int g_num_sms = 0;
 uint64_t g_tc_wait_ns = 4000000000ull;   // bounded-wait limit of the tensor-core kernels
 
 template <int BN>
@@ -502,11 +502,11 @@ nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_
   if (ws && (((uintptr_t)ws) & 15)) return NC_ERR_ARG;
   CUtensorMap ta, tb;
   bool ok;
-  if (a_kmajor) ok = make_tmap(&ta, A, K, M, lda, TC_BK, TC_BM);
-  else ok = make_tmap(&ta, A, M, K, lda, 64, TC_BK);
+  if (a_kmajor) ok = make_tmap_bf16_2d(&ta, A, K, M, lda, TC_BK, TC_BM);
+  else ok = make_tmap_bf16_2d(&ta, A, M, K, lda, 64, TC_BK);
   if (!ok) return NC_ERR_CUDA;
-  if (b_kmajor) ok = make_tmap(&tb, B, K, N, ldb, TC_BK, BN);
-  else ok = make_tmap(&tb, B, N, K, ldb, 64, TC_BK);
+  if (b_kmajor) ok = make_tmap_bf16_2d(&tb, B, K, N, ldb, TC_BK, BN);
+  else ok = make_tmap_bf16_2d(&tb, B, N, K, ldb, 64, TC_BK);
   if (!ok) return NC_ERR_CUDA;
   if (BN == 256) return launch_tc_bn<256>(p, ta, tb, ws_bytes, st);
   return launch_tc_bn<128>(p, ta, tb, ws_bytes, st);

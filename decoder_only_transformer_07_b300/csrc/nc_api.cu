@@ -172,15 +172,15 @@ static nc_status gemm(nc_model* m, int role, int M, int N, int K, const void* A,
 
 // Attention: bf16 runs on the tensor cores, fp32 on CUDA cores in fp32.
 static nc_status attn_fwd(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv, void* o, float* lse,
-                          cudaStream_t st) {
-  if (dtype == NC_BF16) return launch_attn_fwd_tc(B, T, H, Hkv, hd, (const bf16*)qkv, (bf16*)o, lse, st);
+                          int32_t* err, cudaStream_t st) {
+  if (dtype == NC_BF16) return launch_attn_fwd_tc(B, T, H, Hkv, hd, (const bf16*)qkv, (bf16*)o, lse, err, st);
   return launch_attn_fwd_simt(dtype, B, T, H, Hkv, hd, qkv, o, lse, st);
 }
 static nc_status attn_bwd(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv, const void* o,
-                          const float* lse, const void* dout, void* dqkv, float* Dv, cudaStream_t st) {
+                          const float* lse, const void* dout, void* dqkv, float* Dv, int32_t* err, cudaStream_t st) {
   if (dtype == NC_BF16)
     return launch_attn_bwd_tc(B, T, H, Hkv, hd, (const bf16*)qkv, (const bf16*)o, lse, (const bf16*)dout,
-                              (bf16*)dqkv, Dv, st);
+                              (bf16*)dqkv, Dv, err, st);
   return launch_attn_bwd_simt(dtype, B, T, H, Hkv, hd, qkv, o, lse, dout, dqkv, Dv, st);
 }
 
@@ -436,7 +436,7 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
     PROF(NC_PROF_ROPE, 0, (double)N * nh * (2.0 * a * m->hd + 4),
          launch_rope_qknorm_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, rstdqk, m->rope_tab, eps, st));
     PROF(NC_PROF_ATTN_FWD, attn_fl, (double)N * (W + Hd) * a + 4.0 * N * m->H,
-         attn_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, st));
+         attn_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->err, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_FWD, (int)N, C, Hd, o, Hd, 1, wptr(m, tensor(m, l, 3)), Hd, 1, NC_EP_ACCUM_F32, m->x, C, nullptr, 0,
                 st));
     PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn2, rstd2, eps, st));
@@ -482,7 +482,7 @@ static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int 
     NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, Hd, n, m->dx_act, C, 0, o, Hd, 0, NC_EP_STORE_F32, grads + to.off, Hd, nullptr, 0, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, Hd, C, m->dx_act, C, 1, wptr(m, to), Hd, 0, NC_EP_STORE, m->dout, Hd, nullptr, 0, st));
     PROF(NC_PROF_ATTN_BWD, attn_fl, (double)N * (2.0 * W + 2.0 * Hd) * a + 8.0 * N * m->H,
-         attn_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, st));
+         attn_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, m->err, st));
     PROF(NC_PROF_ROPE, 0, (double)N * nh * (3.0 * a * m->hd + 4),
          launch_rope_qknorm_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, m->dqkv, qkv, rstdqk, m->rope_tab, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_DW, W, C, n, m->dqkv, W, 0, xn1, C, 0, NC_EP_STORE_F32, grads + tq.off, C, nullptr, 0, st));
@@ -635,14 +635,14 @@ extern "C" nc_status nc_op_rope_qknorm_bwd(int32_t dtype, int32_t B, int32_t T, 
 extern "C" nc_status nc_op_attention_fwd(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
                                          const void* qkv, void* o, float* lse, void* stream) {
   if (!dtype_ok(dtype) || !qkv || !o || !lse) return NC_ERR_ARG;
-  return attn_fwd(dtype, B, T, H, Hkv, hd, qkv, o, lse, as_stream(stream));
+  return attn_fwd(dtype, B, T, H, Hkv, hd, qkv, o, lse, nullptr, as_stream(stream));
 }
 
 extern "C" nc_status nc_op_attention_bwd(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
                                          const void* qkv, const void* o, const float* lse, const void* do_,
                                          void* dqkv, float* workspace, void* stream) {
   if (!dtype_ok(dtype) || !qkv || !o || !lse || !do_ || !dqkv || !workspace) return NC_ERR_ARG;
-  return attn_bwd(dtype, B, T, H, Hkv, hd, qkv, o, lse, do_, dqkv, workspace, as_stream(stream));
+  return attn_bwd(dtype, B, T, H, Hkv, hd, qkv, o, lse, do_, dqkv, workspace, nullptr, as_stream(stream));
 }
 
 extern "C" nc_status nc_op_cross_entropy(int32_t dtype, int64_t rows, int32_t V, void* z, const int32_t* targets,

@@ -2,6 +2,7 @@
 #pragma once
 #include <algorithm>
 #include "nc_common.cuh"
+#include <cuda.h>
 
 nc_status launch_init_normal(float* out, int64_t count, uint64_t seed, int tensor_index, float std,
                              cudaStream_t st);
@@ -44,8 +45,14 @@ nc_status launch_attn_fwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, 
 nc_status launch_attn_bwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv,
                                const void* o, const float* lse, const void* dout, void* dqkv, float* Dv,
                                cudaStream_t st);
-// bf16 flash attention on tensor cores (head_dim 64 or 128).
+// bf16 causal GQA flash attention on tcgen05 tensor cores (head_dim 64 or 128).
+// err (device int32, may be NULL) receives NC_DEVERR_TIMEOUT if a bounded wait expires.
 nc_status launch_attn_fwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, bf16* o, float* lse,
-                             cudaStream_t st);
+                             int32_t* err, cudaStream_t st);
 nc_status launch_attn_bwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, const bf16* o, const float* lse,
-                             const bf16* dout, bf16* dqkv, float* Dv, cudaStream_t st);
+                             const bf16* dout, bf16* dqkv, float* Dv, int32_t* err, cudaStream_t st);
+
+// 2D bf16 TMA descriptor over a row-major [outer][inner] matrix with leading
+// dimension ld (elements), box {box_inner, box_outer}, 128-byte swizzle.
+bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, int64_t ld,
+                       uint32_t box_inner, uint32_t box_outer);
