@@ -21,7 +21,7 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 NC_FP32, NC_BF16 = 0, 1
-EP_STORE, EP_STORE_F32, EP_ACCUM_F32, EP_RELU2, EP_RELU2_BWD = range(5)
+EP_STORE, EP_STORE_F32, EP_ACCUM_F32, EP_RELU2, EP_RELU2_BWD, EP_RELU2_SQ, EP_RELU2_SQ_BWD = range(7)
 STATUS = {0: "NC_OK", 1: "NC_ERR_CONFIG", 2: "NC_ERR_ALLOC", 3: "NC_ERR_ARG",
           4: "NC_ERR_TOKEN_RANGE", 5: "NC_ERR_CUDA", 6: "NC_ERR_TIMEOUT", 7: "NC_ERR_UNSUPPORTED"}
 
@@ -67,6 +67,7 @@ _SIGS = {
     "nc_op_rmsnorm_bwd": (_i32, [_i32, _i64, _i32, _p, _p, _p, _p, _p, _p]),
     "nc_op_rope_table": (_i32, [_i32, _i32, _f32, _p, _p]),
     "nc_op_rope_qknorm_fwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _f32, _p]),
+    "nc_op_gemm_qkv_rope": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _i64, _p, _p, _i64, _p, _p, _f32, _p]),
     "nc_op_rope_qknorm_bwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_op_attention_fwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p]),
     "nc_op_attention_bwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p, _p, _p]),
@@ -260,6 +261,13 @@ class ops:
     def rope_qknorm_fwd(qkv, B, T, H, Hkv, hd, rstd, table, eps):
         _check(_lib.nc_op_rope_qknorm_fwd(_dtype_code(qkv), B, T, H, Hkv, hd, _ptr(qkv), _ptr(rstd), _ptr(table),
                                           eps, _stream()), "nc_op_rope_qknorm_fwd")
+
+    @staticmethod
+    def gemm_qkv_rope(x, wqkv, qkv, T, H, Hkv, hd, rstd, table, eps):
+        M, K = x.shape
+        _check(_lib.nc_op_gemm_qkv_rope(M, K, T, H, Hkv, hd, _ptr(x), x.stride(0), _ptr(wqkv), _ptr(qkv),
+                                        qkv.stride(0), _ptr(rstd), _ptr(table), eps, _stream()),
+               "nc_op_gemm_qkv_rope")
 
     @staticmethod
     def rope_qknorm_bwd(dqkv, qkv, B, T, H, Hkv, hd, rstd, table):

@@ -242,7 +242,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const uint32_t tO = tbase + lane_off + 256 + i * HD;
     const uint32_t sP = smem_u32(smem + L::OFF_P + i * L::P_BYTES) + r * 128;
     const uint32_t swz = r & 7;
-    float m = 0.f, l = 0.f;
+    float m = 0.f, l = 0.f;                        // running max (raw score units), row sum
+    const float thresh = 8.f / sh.scale_log2;      // raise m only when it grows by > 2^8 in P
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       if (!(ok = at_wait_warp(&s_full[i], j & 1, sh, abort_flag))) break;
@@ -255,15 +256,20 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[i]);
       const int k0 = j * 128;
-      const bool diag = (j == qt) || (k0 + 128 > sh.T);
-      float mx = -INFINITY;
+      if ((j == qt) || (k0 + 128 > sh.T)) {   // diagonal / ragged tile: mask in raw units
+        const int lim = min(qpos - k0, sh.T - 1 - k0);   // last visible column
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        float v = __uint_as_float(x[c]) * sh.scale_log2;
-        if (diag && (k0 + c > qpos || k0 + c >= sh.T)) v = -INFINITY;
-        x[c] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) x[c] = __float_as_uint(-INFINITY);
       }
+      // row max with 8 independent chains (raw score units)
+      float m8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(x[e]);
+#pragma unroll
+      for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(x[c]));
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       // P_i's buffer and O_i are free once the previous O_i += P V completed
       if (j > 0) {
         if (!(ok = at_wait_warp(&pv_done[i], (j - 1) & 1, sh, abort_flag))) break;
@@ -272,10 +278,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       if (j == 0) {
         m = (mx == -INFINITY) ? 0.f : mx;
       } else {
-        const bool need = mx > m + 8.f;
+        const bool need = mx > m + thresh;
         if (__any_sync(0xffffffffu, need)) {
           const float mn = need ? mx : m;
-          const float alpha = ex2_approx(m - mn);
+          const float alpha = ex2_approx((m - mn) * sh.scale_log2);
           l *= alpha;
           m = mn;
 #pragma unroll 1
@@ -290,19 +296,21 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           tmem_st_wait();
         }
       }
-      float sum = 0.f;
+      // p = 2^(s c - m c): one FFMA and one ex2 per score; 8 partial row sums
+      const float mc = m * sh.scale_log2;
+      float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
-        uint32_t w[4];
+        float pv[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = ex2_approx(__uint_as_float(x[8 * u + 2 * e]) - m);
-          const float p1 = ex2_approx(__uint_as_float(x[8 * u + 2 * e + 1]) - m);
-          sum += p0 + p1;
-          w[e] = pack2(p0, p1);
+        for (int e = 0; e < 8; ++e) {
+          pv[e] = ex2_approx(fmaf(__uint_as_float(x[8 * u + e]), sh.scale_log2, -mc));
+          s8[e] += pv[e];
         }
-        st_shared_v4(sP + (u >> 3) * CHUNK128 + ((((uint32_t)u & 7u) ^ swz) << 4), w[0], w[1], w[2], w[3]);
+        st_shared_v4(sP + (u >> 3) * CHUNK128 + ((((uint32_t)u & 7u) ^ swz) << 4), pack2(pv[0], pv[1]),
+                     pack2(pv[2], pv[3]), pack2(pv[4], pv[5]), pack2(pv[6], pv[7]));
       }
+      const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
       l += sum;
       fence_proxy_async_smem();
       tc_fence_before();
@@ -330,7 +338,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           }
         }
       }
-      if (qpos < sh.T) lse[(int64_t)bh * sh.T + qpos] = (m + log2f(l)) * LN2;
+      if (qpos < sh.T) lse[(int64_t)bh * sh.T + qpos] = (m * sh.scale_log2 + log2f(l)) * LN2;
     }
   }
   tc_fence_before();

@@ -25,6 +25,16 @@ __device__ __forceinline__ void ep_apply(int ep, int64_t m, int64_t n, float acc
       ((T*)D)[m * ldd + n] = from_f32<T>(acc * 2.f * r);
       break;
     }
+    case NC_EP_RELU2_SQ: {
+      float r = fmaxf(acc, 0.f);
+      ((T*)D)[m * ldd + n] = from_f32<T>(r * r);
+      break;
+    }
+    case NC_EP_RELU2_SQ_BWD: {
+      float r = sqrtf(to_f32(((const T*)aux)[m * ldaux + n]));
+      ((T*)D)[m * ldd + n] = from_f32<T>(acc * 2.f * r);
+      break;
+    }
   }
 }
 

@@ -50,6 +50,13 @@ struct TcParams {
   // to ws[s][t][128][BN] and a fix-up kernel sums the slices in order.
   int splits, kps;
   float* ws;
+  // NC_EP_QKV_ROPE (the fused q/k/v projection): heads < rope_nh are rotated
+  // (RoPE, cos/sin table [T][hd/2][2]) and RMS-normalised per head, their
+  // rstd stored to rstd_qk[row * rope_nh + head]; the other heads are stored as is.
+  const float* rope_tab;
+  float* rstd_qk;
+  int rope_T, rope_nh, rope_hd;
+  float rope_eps;
 };
 
 // One unit of work of a CTA: k-blocks [k0, k1) of output tile t (slice s).
@@ -153,7 +160,12 @@ __device__ __forceinline__ void tc_epilogue_row(const TcParams& p, int64_t m, in
   if (p.ep == NC_EP_RELU2) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.f);
-  } else if (p.ep == NC_EP_RELU2_BWD) {
+  } else if (p.ep == NC_EP_RELU2_SQ) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.f) * fmaxf(v[i], 0.f);
+  } else if (p.ep == NC_EP_RELU2_BWD || p.ep == NC_EP_RELU2_SQ_BWD) {
+    // aux holds relu(u) (RELU2_BWD) or relu(u)^2 (RELU2_SQ_BWD, whose root is relu(u))
+    const bool sq = p.ep == NC_EP_RELU2_SQ_BWD;
     const bf16* a = (const bf16*)p.aux + m * p.ldaux + n0;
     if (full && ((((uintptr_t)a) & 15) == 0)) {
 #pragma unroll
@@ -161,10 +173,16 @@ __device__ __forceinline__ void tc_epilogue_row(const TcParams& p, int64_t m, in
         uint4 u = *reinterpret_cast<const uint4*>(a + i);
         const bf16* h = reinterpret_cast<const bf16*>(&u);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[i + j] *= 2.f * __bfloat162float(h[j]);
+        for (int j = 0; j < 8; ++j) {
+          const float x = __bfloat162float(h[j]);
+          v[i + j] *= 2.f * (sq ? sqrtf(x) : x);
+        }
       }
     } else {
-      for (int i = 0; i < 32; ++i) v[i] = (n0 + i < p.N) ? v[i] * 2.f * __bfloat162float(a[i]) : 0.f;
+      for (int i = 0; i < 32; ++i) {
+        const float x = (n0 + i < p.N) ? __bfloat162float(a[i]) : 0.f;
+        v[i] = (n0 + i < p.N) ? v[i] * 2.f * (sq ? sqrtf(x) : x) : 0.f;
+      }
     }
   }
   bf16* d = (bf16*)p.D + m * p.ldd + n0;
@@ -192,6 +210,92 @@ __device__ __forceinline__ void tc_epilogue_row(const TcParams& p, int64_t m, in
       d[i] = __float2bfloat16_rn(v[i]);
       if (h) h[i] = __float2bfloat16_rn(v[i] * v[i]);
     }
+  }
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  uint4 o;
+  o.x = pack_bf16x2(v[0], v[1]);
+  o.y = pack_bf16x2(v[2], v[3]);
+  o.z = pack_bf16x2(v[4], v[5]);
+  o.w = pack_bf16x2(v[6], v[7]);
+  return o;
+}
+
+// NC_EP_QKV_ROPE epilogue of one row over `ncols` accumulator columns (whole
+// heads) starting at output column n_base / TMEM column tcol0.  For a q or k
+// head: rstd = 1/sqrt(mean(u^2) + eps) from the fp32 accumulator u (the
+// rotation preserves the sum of squares, so this is the RMS of rope(u)), then
+// y_i = (u_i cos + u_{i+d} sin) rstd, y_{i+d} = (-u_i sin + u_{i+d} cos) rstd
+// with d = hd/2 and the angle of the row's position (cosmicrealm
+// "noao-chat-0-项目总体介绍" §2.1 items 1-2: rotary embedding, then QK norm).
+__device__ __forceinline__ void tc_epilogue_qkv_rope(const TcParams& p, int64_t m, int n_base, int ncols,
+                                                     uint32_t tcol0) {
+  const int hd = p.rope_hd, d = hd >> 1;
+  const bool row_ok = m < p.M;
+  const int t = (int)(m % p.rope_T);
+#pragma unroll 1
+  for (int hc = 0; hc < ncols; hc += hd) {
+    const int n0 = n_base + hc;
+    if (n0 >= p.N) break;
+    const int head = n0 / hd;
+    const uint32_t tc = tcol0 + hc;
+    bf16* dst = (bf16*)p.D + m * p.ldd + n0;
+    if (head >= p.rope_nh) {   // v head
+#pragma unroll 1
+      for (int c = 0; c < hd; c += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tc + c, r);
+        tmem_ld_wait();
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(r[e + k]);
+            *reinterpret_cast<uint4*>(dst + c + e) = pack8_bf16(v);
+          }
+        }
+      }
+      continue;
+    }
+    float ss = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < hd; c += 32) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tc + c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) ss += __uint_as_float(r[e]) * __uint_as_float(r[e]);
+    }
+    const float rs = rsqrtf(ss / (float)hd + p.rope_eps);
+    const float4* cs = reinterpret_cast<const float4*>(p.rope_tab + (size_t)t * hd);
+#pragma unroll 1
+    for (int c = 0; c < d; c += 32) {
+      uint32_t a[32], b[32];
+      tmem_ld_32x32b_x32(tc + c, a);
+      tmem_ld_32x32b_x32(tc + d + c, b);
+      tmem_ld_wait();
+      if (row_ok) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          float y1[8], y2[8];
+#pragma unroll
+          for (int k = 0; k < 8; k += 2) {
+            const float4 q = __ldg(cs + ((c + e + k) >> 1));   // cos_i, sin_i, cos_i+1, sin_i+1
+            const float a0 = __uint_as_float(a[e + k]), a1 = __uint_as_float(a[e + k + 1]);
+            const float b0 = __uint_as_float(b[e + k]), b1 = __uint_as_float(b[e + k + 1]);
+            y1[k] = (a0 * q.x + b0 * q.y) * rs;
+            y2[k] = (-a0 * q.y + b0 * q.x) * rs;
+            y1[k + 1] = (a1 * q.z + b1 * q.w) * rs;
+            y2[k + 1] = (-a1 * q.w + b1 * q.z) * rs;
+          }
+          *reinterpret_cast<uint4*>(dst + c + e) = pack8_bf16(y1);
+          *reinterpret_cast<uint4*>(dst + d + c + e) = pack8_bf16(y2);
+        }
+      }
+    }
+    if (row_ok) p.rstd_qk[m * p.rope_nh + head] = rs;
   }
 }
 
@@ -329,6 +433,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         ? p.ws + ((size_t)sg.s * (p.tiles_m * p.tiles_n) + sg.t) * TC_BM * BN +
                               (size_t)(quarter * 32 + lane) * BN
                         : nullptr;
+      if (p.ep == NC_EP_QKV_ROPE) {
+        tc_epilogue_qkv_rope(p, m, tn * BN + c_lo, BN / 2, taddr + c_lo);
+      } else
 #pragma unroll 1
       for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
         const int n0 = tn * BN + c;
@@ -473,13 +580,21 @@ static nc_status launch_tc_bn(TcParams p, const CUtensorMap& ta, const CUtensorM
 // Split-K partials: up to 4 waves of 128 x 256 fp32 tiles per slice set.
 size_t gemm_tc_workspace_bytes() { return (size_t)256 << 20; }
 
-nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_kmajor, const bf16* B,
-                         int64_t ldb, int b_kmajor, int ep, void* D, int64_t ldd, void* aux, int64_t ldaux,
-                         int32_t* err, void* ws, size_t ws_bytes, cudaStream_t st) {
+struct TcRope {
+  const float* tab;
+  float* rstd;
+  int T, nh, hd;
+  float eps;
+};
+
+static nc_status gemm_tc_impl(int M, int N, int K, const bf16* A, int64_t lda, int a_kmajor, const bf16* B,
+                              int64_t ldb, int b_kmajor, int ep, void* D, int64_t ldd, void* aux, int64_t ldaux,
+                              const TcRope* rope, int32_t* err, void* ws, size_t ws_bytes, cudaStream_t st) {
   if (M <= 0 || N <= 0) return NC_OK;
   if (K <= 0) return NC_ERR_ARG;
   if ((lda % 8) || (ldb % 8) || (((uintptr_t)A) & 15) || (((uintptr_t)B) & 15)) return NC_ERR_ARG;
-  if (!D || ((ep == NC_EP_RELU2 || ep == NC_EP_RELU2_BWD) && !aux)) return NC_ERR_ARG;
+  if (!D || ((ep == NC_EP_RELU2 || ep == NC_EP_RELU2_BWD || ep == NC_EP_RELU2_SQ_BWD) && !aux))
+    return NC_ERR_ARG;
   if (!g_num_sms) {
     int dev = 0;
     NC_CUDA_TRY(cudaGetDevice(&dev));
@@ -499,6 +614,18 @@ nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_
   p.ws = (float*)ws;
   p.splits = 1;
   p.kps = 0;
+  p.rope_tab = nullptr; p.rstd_qk = nullptr; p.rope_T = 1; p.rope_nh = 0; p.rope_hd = 0; p.rope_eps = 0.f;
+  if (rope) {
+    // whole heads in each epilogue warp's 128 columns, 16-byte row segments
+    if (ep != NC_EP_QKV_ROPE || BN != 256 || (rope->hd != 64 && rope->hd != 128) || (N % rope->hd) ||
+        rope->nh * rope->hd > N || rope->T <= 0 || (ldd % 8) || (((uintptr_t)D) & 15) ||
+        (((uintptr_t)rope->tab) & 15) || !rope->rstd)
+      return NC_ERR_ARG;
+    p.rope_tab = rope->tab; p.rstd_qk = rope->rstd; p.rope_T = rope->T; p.rope_nh = rope->nh;
+    p.rope_hd = rope->hd; p.rope_eps = rope->eps;
+  } else if (ep == NC_EP_QKV_ROPE) {
+    return NC_ERR_ARG;
+  }
   if (ws && (((uintptr_t)ws) & 15)) return NC_ERR_ARG;
   CUtensorMap ta, tb;
   bool ok;
@@ -510,4 +637,21 @@ nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_
   if (!ok) return NC_ERR_CUDA;
   if (BN == 256) return launch_tc_bn<256>(p, ta, tb, ws_bytes, st);
   return launch_tc_bn<128>(p, ta, tb, ws_bytes, st);
+}
+
+nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_kmajor, const bf16* B,
+                         int64_t ldb, int b_kmajor, int ep, void* D, int64_t ldd, void* aux, int64_t ldaux,
+                         int32_t* err, void* ws, size_t ws_bytes, cudaStream_t st) {
+  if (ep == NC_EP_QKV_ROPE) return NC_ERR_ARG;
+  return gemm_tc_impl(M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, ep, D, ldd, aux, ldaux, nullptr, err, ws,
+                      ws_bytes, st);
+}
+
+nc_status launch_gemm_tc_qkv_rope(int M, int N, int K, const bf16* A, int64_t lda, const bf16* Wqkv, int64_t ldb,
+                                  bf16* qkv, int64_t ldd, int T, int nh, int hd, const float* tab, float* rstd,
+                                  float eps, int32_t* err, cudaStream_t st) {
+  TcRope r{tab, rstd, T, nh, hd, eps};
+  if (N <= 128) return NC_ERR_UNSUPPORTED;
+  return gemm_tc_impl(M, N, K, A, lda, 1, Wqkv, ldb, 1, NC_EP_QKV_ROPE, qkv, ldd, nullptr, 0, &r, err, nullptr, 0,
+                      st);
 }

@@ -39,7 +39,7 @@ struct nc_model {
   float* result_host = nullptr;      // pinned host copy
   // forward activations (per layer, strides sized for Nmax tokens)
   float* x = nullptr;                // residual stream [N, C]
-  uint8_t *xn1, *xn2, *qkv, *o, *r, *h;
+  uint8_t *xn1, *xn2, *qkv, *o, *h;      // h = relu(u)^2 (relu(u) = sqrt(h) in the backward)
   float *rstd1, *rstd2, *rstdqk, *lse;
   void* xf = nullptr;
   float* rstd_f = nullptr;
@@ -157,7 +157,7 @@ static nc_status gemm(nc_model* m, int role, int M, int N, int K, const void* A,
   m->launches += 1;
   const double a = (double)m->act;
   const double out = (ep == NC_EP_STORE_F32) ? 4.0 : (ep == NC_EP_ACCUM_F32) ? 8.0
-                   : (ep == NC_EP_STORE) ? a : 2.0 * a;
+                   : (ep == NC_EP_STORE || ep == NC_EP_RELU2_SQ) ? a : 2.0 * a;
   const double bytes = ((double)M * K + (double)N * K) * a + (double)M * N * out;
   const double flops = 2.0 * M * N * K;
   if (m->dtype == NC_BF16)
@@ -248,7 +248,6 @@ static nc_status allocate(nc_model* m) {
   NC_TRY(dalloc(m, (size_t)L * N * m->C * a, (void**)&m->xn2));
   NC_TRY(dalloc(m, (size_t)L * N * m->qkvw * a, (void**)&m->qkv));
   NC_TRY(dalloc(m, (size_t)L * N * m->H * m->hd * a, (void**)&m->o));
-  NC_TRY(dalloc(m, (size_t)L * N * m->F * a, (void**)&m->r));
   NC_TRY(dalloc(m, (size_t)L * N * m->F * a, (void**)&m->h));
   NC_TRY(dalloc_t(m, (size_t)L * N, &m->rstd1));
   NC_TRY(dalloc_t(m, (size_t)L * N, &m->rstd2));
@@ -425,22 +424,30 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
     uint8_t* xn2 = layer_act(m, m->xn2, l, C);
     uint8_t* qkv = layer_act(m, m->qkv, l, W);
     uint8_t* o = layer_act(m, m->o, l, Hd);
-    uint8_t* r = layer_act(m, m->r, l, F);
     uint8_t* h = layer_act(m, m->h, l, F);
     float* rstd1 = m->rstd1 + (size_t)l * m->Nmax;
     float* rstd2 = m->rstd2 + (size_t)l * m->Nmax;
     float* rstdqk = m->rstdqk + (size_t)l * m->Nmax * (m->H + m->Hkv);
     float* lse = m->lse + (size_t)l * m->Nmax * m->H;
     PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn1, rstd1, eps, st));
-    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, (int)N, W, C, xn1, C, 1, wptr(m, tensor(m, l, 0)), C, 1, NC_EP_STORE, qkv, W, nullptr, 0, st));
-    PROF(NC_PROF_ROPE, 0, (double)N * nh * (2.0 * a * m->hd + 4),
-         launch_rope_qknorm_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, rstdqk, m->rope_tab, eps, st));
+    if (m->dtype == NC_BF16) {
+      // q/k/v projection with RoPE and the q/k RMSNorm in the GEMM epilogue
+      PROF_SUB(NC_PROF_GEMM, NC_PROF_GEMM_FWD, 2.0 * N * W * C, ((double)N * C + (double)W * C + (double)N * W) * a,
+               launch_gemm_tc_qkv_rope((int)N, W, C, (const bf16*)xn1, C, (const bf16*)wptr(m, tensor(m, l, 0)), C,
+                                       (bf16*)qkv, W, T, nh, m->hd, m->rope_tab, rstdqk, eps, m->err, st));
+      m->launches += 1;
+    } else {
+      NC_TRY(gemm(m, NC_PROF_GEMM_FWD, (int)N, W, C, xn1, C, 1, wptr(m, tensor(m, l, 0)), C, 1, NC_EP_STORE, qkv, W,
+                  nullptr, 0, st));
+      PROF(NC_PROF_ROPE, 0, (double)N * nh * (2.0 * a * m->hd + 4),
+           launch_rope_qknorm_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, rstdqk, m->rope_tab, eps, st));
+    }
     PROF(NC_PROF_ATTN_FWD, attn_fl, (double)N * (W + Hd) * a + 4.0 * N * m->H,
          attn_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->err, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_FWD, (int)N, C, Hd, o, Hd, 1, wptr(m, tensor(m, l, 3)), Hd, 1, NC_EP_ACCUM_F32, m->x, C, nullptr, 0,
                 st));
     PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn2, rstd2, eps, st));
-    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, (int)N, F, C, xn2, C, 1, wptr(m, tensor(m, l, 4)), C, 1, NC_EP_RELU2, r, F, h, F, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, (int)N, F, C, xn2, C, 1, wptr(m, tensor(m, l, 4)), C, 1, NC_EP_RELU2_SQ, h, F, nullptr, 0, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_FWD, (int)N, C, F, h, F, 1, wptr(m, tensor(m, l, 5)), F, 1, NC_EP_ACCUM_F32, m->x, C, nullptr, 0, st));
     m->launches += 4;
   }
@@ -462,7 +469,6 @@ static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int 
     uint8_t* xn2 = layer_act(m, m->xn2, l, C);
     uint8_t* qkv = layer_act(m, m->qkv, l, W);
     uint8_t* o = layer_act(m, m->o, l, Hd);
-    uint8_t* r = layer_act(m, m->r, l, F);
     uint8_t* h = layer_act(m, m->h, l, F);
     float* rstd1 = m->rstd1 + (size_t)l * m->Nmax;
     float* rstd2 = m->rstd2 + (size_t)l * m->Nmax;
@@ -472,7 +478,7 @@ static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int 
                       &tpj = tensor(m, l, 5);
     // MLP: x2 = x1 + relu(xn2 Wfc^T)^2 Wproj^T
     NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, F, n, m->dx_act, C, 0, h, F, 0, NC_EP_STORE_F32, grads + tpj.off, F, nullptr, 0, st));
-    NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, F, C, m->dx_act, C, 1, wptr(m, tpj), F, 0, NC_EP_RELU2_BWD, m->du, F, r, F, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, F, C, m->dx_act, C, 1, wptr(m, tpj), F, 0, NC_EP_RELU2_SQ_BWD, m->du, F, h, F, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_DW, F, C, n, m->du, F, 0, xn2, C, 0, NC_EP_STORE_F32, grads + tfc.off, C, nullptr, 0, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, C, F, m->du, F, 1, wptr(m, tfc), C, 0, NC_EP_STORE_F32, m->dxn, C, nullptr, 0, st));
     PROF(NC_PROF_NORM, 0, nb_by,
@@ -593,7 +599,7 @@ extern "C" nc_status nc_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, 
                                 int32_t a_kmajor, const void* B, int64_t ldb, int32_t b_kmajor, int32_t ep, void* D,
                                 int64_t ldd, void* aux, int64_t ldaux, void* workspace, size_t workspace_bytes,
                                 void* stream) {
-  if (!dtype_ok(dtype) || !A || !B || !D || ep < 0 || ep > NC_EP_RELU2_BWD) return NC_ERR_ARG;
+  if (!dtype_ok(dtype) || !A || !B || !D || ep < 0 || ep > NC_EP_RELU2_SQ_BWD) return NC_ERR_ARG;
   if (M < 0 || N < 0 || K < 0) return NC_ERR_ARG;
   if (dtype == NC_BF16)
     return launch_gemm_tc(M, N, K, (const bf16*)A, lda, a_kmajor, (const bf16*)B, ldb, b_kmajor, ep, D, ldd, aux,
@@ -622,6 +628,16 @@ extern "C" nc_status nc_op_rope_qknorm_fwd(int32_t dtype, int32_t B, int32_t T, 
                                            void* qkv, float* rstd, const float* cos_sin, float eps, void* stream) {
   if (!dtype_ok(dtype) || !qkv || !rstd || !cos_sin || B <= 0 || T <= 0 || H <= 0 || Hkv <= 0) return NC_ERR_ARG;
   return launch_rope_qknorm_fwd(dtype, B, T, H, Hkv, hd, qkv, rstd, cos_sin, eps, as_stream(stream));
+}
+
+extern "C" nc_status nc_op_gemm_qkv_rope(int32_t M, int32_t K, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
+                                         const void* x, int64_t ldx, const void* wqkv, void* qkv, int64_t ldqkv,
+                                         float* rstd, const float* cos_sin, float eps, void* stream) {
+  if (!x || !wqkv || !qkv || !rstd || !cos_sin || M < 0 || K <= 0 || T <= 0 || H <= 0 || Hkv <= 0 || H % Hkv)
+    return NC_ERR_ARG;
+  const int N = (H + 2 * Hkv) * hd;
+  return launch_gemm_tc_qkv_rope(M, N, K, (const bf16*)x, ldx, (const bf16*)wqkv, K, (bf16*)qkv, ldqkv, T, H + Hkv,
+                                 hd, cos_sin, rstd, eps, nullptr, as_stream(stream));
 }
 
 extern "C" nc_status nc_op_rope_qknorm_bwd(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t hd,

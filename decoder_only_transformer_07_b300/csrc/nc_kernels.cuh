@@ -39,6 +39,15 @@ nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_
                          const bf16* B, int64_t ldb, int b_kmajor, int ep, void* D, int64_t ldd,
                          void* aux, int64_t ldaux, int32_t* err, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t gemm_tc_workspace_bytes();
+// Internal epilogue of the fused q/k/v projection (not part of the public enum).
+#define NC_EP_QKV_ROPE 100
+// qkv[M, N] = A[M, K] Wqkv[N, K]^T in bf16 with RoPE and the per-head RMSNorm
+// of the first nh heads (q and k) applied in the epilogue (rstd [M, nh] fp32);
+// the remaining heads (v) are stored as computed.  Rows are positions m % T.
+// NC_ERR_UNSUPPORTED for N <= 128; hd 64 or 128.
+nc_status launch_gemm_tc_qkv_rope(int M, int N, int K, const bf16* A, int64_t lda, const bf16* Wqkv, int64_t ldb,
+                                  bf16* qkv, int64_t ldd, int T, int nh, int hd, const float* tab, float* rstd,
+                                  float eps, int32_t* err, cudaStream_t st);
 
 nc_status launch_attn_fwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv, void* o,
                                float* lse, cudaStream_t st);

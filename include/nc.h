@@ -159,11 +159,14 @@ int64_t nc_last_launch_count(const nc_model* m);
  *   NC_EP_ACCUM_F32 D (float) += acc          (residual add, dW accumulate)
  *   NC_EP_RELU2     D (dtype) = relu(acc), aux (dtype) = relu(acc)^2
  *   NC_EP_RELU2_BWD D (dtype) = acc * 2 * aux   (aux holds relu(u))
+ *   NC_EP_RELU2_SQ  D (dtype) = relu(acc)^2      (aux unused)
+ *   NC_EP_RELU2_SQ_BWD D (dtype) = acc * 2 * sqrt(aux)   (aux holds relu(u)^2;
+ *                   sqrt(relu(u)^2) = relu(u), so the forward need not keep relu(u))
  * ldd / ldaux are leading dimensions in elements.  NC_BF16 runs the tcgen05
  * tensor-core kernel (lda, ldb multiples of 8, 16-byte aligned bases);
  * NC_FP32 runs exact fp32 FMA.  workspace may be NULL (see below). */
 enum { NC_EP_STORE = 0, NC_EP_STORE_F32 = 1, NC_EP_ACCUM_F32 = 2,
-       NC_EP_RELU2 = 3, NC_EP_RELU2_BWD = 4 };
+       NC_EP_RELU2 = 3, NC_EP_RELU2_BWD = 4, NC_EP_RELU2_SQ = 5, NC_EP_RELU2_SQ_BWD = 6 };
 nc_status nc_op_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K,
                      const void* A, int64_t lda, int32_t a_kmajor,
                      const void* B, int64_t ldb, int32_t b_kmajor,
@@ -197,6 +200,19 @@ nc_status nc_op_rope_table(int32_t T, int32_t hd, float rope_base, float* cos_si
 nc_status nc_op_rope_qknorm_fwd(int32_t dtype, int32_t B, int32_t T, int32_t H,
                                 int32_t Hkv, int32_t hd, void* qkv, float* rstd,
                                 const float* cos_sin, float eps, void* stream);
+/* The q/k/v projection with the above fused into its epilogue (bf16 only):
+ * qkv (bf16 [M, (H+2*Hkv)*hd], leading dimension ldqkv) = x (bf16 [M, K],
+ * leading dimension ldx) times Wqkv^T (bf16 [(H+2*Hkv)*hd, K]), then for the
+ * first H+Hkv heads of every row the rotary embedding at position row % T
+ * followed by the per-head RMSNorm, computed from the fp32 accumulator; v is
+ * stored as computed.  rstd (float [M, H+Hkv]).  The rotation preserves the
+ * sum of squares, so rstd is taken before rotating (cosmicrealm
+ * "noao-chat-0-项目总体介绍" §2.1 items 1-2).  hd 64 or 128, (H+2*Hkv)*hd > 128,
+ * 16-byte aligned buffers; NC_ERR_ARG / NC_ERR_UNSUPPORTED otherwise. */
+nc_status nc_op_gemm_qkv_rope(int32_t M, int32_t K, int32_t T, int32_t H, int32_t Hkv,
+                              int32_t hd, const void* x, int64_t ldx, const void* wqkv,
+                              void* qkv, int64_t ldqkv, float* rstd, const float* cos_sin,
+                              float eps, void* stream);
 /* In place on dqkv: the backward of the above, given the saved (normalised)
  * qkv and rstd. */
 nc_status nc_op_rope_qknorm_bwd(int32_t dtype, int32_t B, int32_t T, int32_t H,

@@ -23,6 +23,11 @@ def relu2_bwd(dh, r):
     return np.asarray(dh, dtype=np.float64) * 2.0 * np.asarray(r, dtype=np.float64)
 
 
+def relu2_bwd_from_square(dh, h):
+    """The same derivative written with h = relu(u)^2: relu(u) = sqrt(h), since relu(u) >= 0."""
+    return np.asarray(dh, dtype=np.float64) * 2.0 * np.sqrt(np.asarray(h, dtype=np.float64))
+
+
 def embed(wte, tokens):
     return np.asarray(wte)[np.asarray(tokens)]
 

@@ -43,7 +43,7 @@ def _gemm_case(M, N, K, a_kmajor, b_kmajor, ep, dt, seed=0, ws=False):
         ref = ref + base
     if ep == nc.EP_RELU2:
         aux = torch.zeros((M, N), dtype=dt, device="cuda")
-    if ep == nc.EP_RELU2_BWD:
+    if ep in (nc.EP_RELU2_BWD, nc.EP_RELU2_SQ_BWD):
         aux = dev_tensor(np.abs(rnd(seed + 3, (M, N))), dt)
     W = torch.empty(nc.ops.gemm_workspace_bytes(), dtype=torch.uint8, device="cuda") if ws else None
     nc.ops.gemm(A, a_kmajor, B, b_kmajor, M, N, K, D, ep=ep, aux=aux,
@@ -54,6 +54,10 @@ def _gemm_case(M, N, K, a_kmajor, b_kmajor, ep, dt, seed=0, ws=False):
         return [(to64(D), r_ref), (to64(aux), h_ref)]
     if ep == nc.EP_RELU2_BWD:
         return [(to64(D), OO.relu2_bwd(ref, to64(aux)))]
+    if ep == nc.EP_RELU2_SQ:
+        return [(to64(D), OO.relu2(ref)[0])]
+    if ep == nc.EP_RELU2_SQ_BWD:
+        return [(to64(D), OO.relu2_bwd_from_square(ref, to64(aux)))]
     return [(to64(D), ref)]
 
 
@@ -85,7 +89,8 @@ def test_gemm_layouts_ragged(a_kmajor, b_kmajor, dt):
     _assert_gemm(_gemm_case(M, N, K, a_kmajor, b_kmajor, nc.EP_STORE_F32, dt), dt, K, nc.EP_STORE_F32)
 
 
-@pytest.mark.parametrize("ep", [nc.EP_STORE, nc.EP_STORE_F32, nc.EP_ACCUM_F32, nc.EP_RELU2, nc.EP_RELU2_BWD])
+@pytest.mark.parametrize("ep", [nc.EP_STORE, nc.EP_STORE_F32, nc.EP_ACCUM_F32, nc.EP_RELU2, nc.EP_RELU2_BWD,
+                                nc.EP_RELU2_SQ, nc.EP_RELU2_SQ_BWD])
 @pytest.mark.parametrize("dt", [BF16, F32])
 def test_gemm_epilogues(ep, dt):
     M, N, K = 256, 384, 192
@@ -197,6 +202,33 @@ def test_rope_qknorm_fwd_bwd(hd, dt):
     rtol = 1e-4 if dt == F32 else 2e-2
     ok, worst = rel_close(got_g[:, :, :H + Hkv].transpose(0, 2, 1, 3), want, rtol, 1e-2)
     assert ok, worst
+
+
+@pytest.mark.parametrize("hd,H,Hkv", [(64, 4, 2), (128, 3, 1), (128, 2, 2)])
+def test_gemm_qkv_rope_fused(hd, H, Hkv):
+    """The q/k/v projection with RoPE + per-head RMSNorm in its epilogue, against
+    gemm -> rope -> rms_norm of the oracle on the same bf16 inputs."""
+    B, T, K, eps, base = 2, 100, 192, 1.1920929e-07, 10000.0
+    M, W = B * T, (H + 2 * Hkv) * hd
+    X = dev_tensor(rnd(50, (M, K)), BF16)
+    Wq = dev_tensor(rnd(51, (W, K), 0.1), BF16)
+    tab = torch.empty((T, hd // 2, 2), dtype=F32, device="cuda")
+    nc.ops.rope_table(T, hd, base, tab)
+    QKV = torch.full((M, W), float("nan"), dtype=BF16, device="cuda")
+    R = torch.empty((M, H + Hkv), dtype=F32, device="cuda")
+    nc.ops.gemm_qkv_rope(X, Wq, QKV, T, H, Hkv, hd, R, tab, eps)
+    torch.cuda.synchronize()
+    u = OO.gemm(to64(X), to64(Wq)).reshape(B, T, H + 2 * Hkv, hd)
+    cos, sin = OM.rope_tables(T, hd, base)
+    heads = u[:, :, :H + Hkv].transpose(0, 2, 1, 3)
+    y_ref, r_ref = OM.rms_norm(OM.rope(heads, cos, sin), eps)
+    got = to64(QKV).reshape(B, T, H + 2 * Hkv, hd)
+    # one bf16 rounding of a value computed in fp32 from exact products
+    ok, worst = rel_close(got[:, :, :H + Hkv].transpose(0, 2, 1, 3), y_ref, 2.0 ** -8, 1e-2)
+    assert ok, worst
+    ok, worst = rel_close(got[:, :, H + Hkv:], u[:, :, H + Hkv:], 2.0 ** -8, 1e-2)
+    assert ok, worst
+    assert np.allclose(to64(R).reshape(B, T, H + Hkv).transpose(0, 2, 1), r_ref[..., 0], rtol=1e-4)
 
 
 # ---------------------------------------------------------------- attention

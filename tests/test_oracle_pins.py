@@ -242,6 +242,23 @@ def test_relu_squared_mlp_properties():
     assert np.allclose(d2, 9.0 * d_pos, rtol=1e-12, atol=1e-13)
 
 
+def test_relu_squared_derivative_single_ops():
+    """The single-op definitions the GEMM epilogues are checked against: relu2
+    returns (relu(u)^2, relu(u)); both backward forms equal the central
+    difference of relu(u)^2 (away from the kink at 0)."""
+    from oracle import ops as O
+    u = np.random.default_rng(14).normal(size=200)
+    u = u[np.abs(u) > 1e-3]
+    dh = np.random.default_rng(15).normal(size=u.size)
+    h, r = O.relu2(u)
+    assert np.array_equal(r, np.where(u > 0, u, 0.0)) and np.array_equal(h, r * r)
+    eps = 1e-6
+    fd = dh * ((np.maximum(u + eps, 0) ** 2 - np.maximum(u - eps, 0) ** 2) / (2 * eps))
+    assert np.allclose(O.relu2_bwd(dh, r), fd, rtol=1e-7, atol=1e-9)
+    assert np.allclose(O.relu2_bwd_from_square(dh, h), fd, rtol=1e-7, atol=1e-9)
+    assert np.all(O.relu2_bwd_from_square(dh, h)[u < 0] == 0.0)
+
+
 # ---------------------------------------------------------------- whole step
 
 @pytest.mark.parametrize("kv", [2, 1])
