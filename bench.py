@@ -182,7 +182,7 @@ def run_op(args):
         A = torch.randn((M, K) if args.a_major == "k" else (K, M), device="cuda", generator=g).to(torch.bfloat16)
         B = torch.randn((N, K) if args.b_major == "k" else (K, N), device="cuda", generator=g).to(torch.bfloat16)
         D = torch.empty((M, N), dtype=torch.float32 if args.ep in (1, 2) else torch.bfloat16, device="cuda")
-        aux = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda") if args.ep in (3, 4) else None
+        aux = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda") if args.ep in (3, 4, 6) else None
         W = torch.empty(nc.ops.gemm_workspace_bytes(), dtype=torch.uint8, device="cuda")
         flops = 2.0 * M * N * K
 

@@ -71,11 +71,13 @@ _SIGS = {
     "nc_op_rope_qknorm_bwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_op_attention_fwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p]),
     "nc_op_attention_bwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p, _p, _p]),
+    "nc_op_attention_bwd_rope": (_i32, [_i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p, _p, _p, _p, _p]),
     "nc_op_cross_entropy": (_i32, [_i32, _i64, _i32, _p, _p, _p, _f32, _p, _p]),
     "nc_op_embed_fwd": (_i32, [_i32, _i64, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_embed_bwd_scratch_bytes": (_sz, [_i64, _i32, _i32]),
     "nc_op_embed_bwd": (_i32, [_i64, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_debug_set_wait_limit_ns": (None, [_u64]),
+    "nc_debug_set_gemm_pair": (None, [_i32]),
     "nc_profile_enable": (_i32, [_p, _i32]),
     "nc_profile_read": (_i32, [_p, _i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64),
                                 ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
@@ -283,6 +285,12 @@ class ops:
     def attention_bwd(qkv, o, lse, do, B, T, H, Hkv, hd, dqkv, ws):
         _check(_lib.nc_op_attention_bwd(_dtype_code(qkv), B, T, H, Hkv, hd, _ptr(qkv), _ptr(o), _ptr(lse),
                                         _ptr(do), _ptr(dqkv), _ptr(ws), _stream()), "nc_op_attention_bwd")
+
+    @staticmethod
+    def attention_bwd_rope(qkv, o, lse, do, B, T, H, Hkv, hd, dqkv, workspace, rstd, table):
+        _check(_lib.nc_op_attention_bwd_rope(B, T, H, Hkv, hd, _ptr(qkv), _ptr(o), _ptr(lse), _ptr(do), _ptr(dqkv),
+                                             _ptr(workspace), _ptr(rstd), _ptr(table), _stream()),
+               "nc_op_attention_bwd_rope")
 
     @staticmethod
     def cross_entropy(z, targets, row_loss, scale, err=None):

@@ -62,6 +62,11 @@ struct AtShape {
   float scale;        // 1 / sqrt(hd)
   int32_t* err;
   uint64_t wait_ns;
+  // Backward only: with rope_tab set, dq and dk leave through the per-head
+  // RMSNorm backward and the transposed rotation (rstd_qk [B*T, H+Hkv],
+  // cos/sin table [T][hd/2][2]), i.e. as gradients of the projection output.
+  const float* rope_tab;
+  const float* rstd_qk;
 };
 
 // tcgen05.mma kind::f16 instruction descriptor: fp32 accumulator, bf16 A and
@@ -347,6 +352,99 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (warp == 2) tmem_dealloc(tbase, 512);
 }
 
+// Output of a dQ or dK tile (128 rows x HD in TMEM, fp32) by the 8 epilogue
+// warps (quarter = TMEM lane group, hf = half).  Plain: dst = scale * acc in
+// bf16, each half-warp group writing HD/2 columns.  With rope_tab: g = scale *
+// acc is the gradient of the normalised, rotated head y (the bf16 tile in
+// shared memory, [128][HD] as 64-column 128B-swizzled chunks); the thread
+// forms dot = mean(g * y) over the whole row, dr = rstd * (g - y * dot)
+// (RMSNorm backward), and for its half of the rotation pairs (i, i + HD/2)
+// writes dx_i = dr_i cos - dr_{i+d} sin, dx_{i+d} = dr_i sin + dr_{i+d} cos
+// (the transpose of the forward rotation at the row's position).
+template <int HD>
+__device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, const uint8_t* ytile, int r, int hf,
+                                            bool valid, int pos, int64_t token, int head, bf16* dst) {
+  if (!sh.rope_tab) {
+#pragma unroll 1
+    for (int c = 0; c < HD / 64; ++c) {
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(tacc + hf * (HD / 2) + 32 * c, v);
+      tmem_ld_wait();
+      if (valid) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 w;
+          w.x = pack2(__uint_as_float(v[e]) * sh.scale, __uint_as_float(v[e + 1]) * sh.scale);
+          w.y = pack2(__uint_as_float(v[e + 2]) * sh.scale, __uint_as_float(v[e + 3]) * sh.scale);
+          w.z = pack2(__uint_as_float(v[e + 4]) * sh.scale, __uint_as_float(v[e + 5]) * sh.scale);
+          w.w = pack2(__uint_as_float(v[e + 6]) * sh.scale, __uint_as_float(v[e + 7]) * sh.scale);
+          *reinterpret_cast<uint4*>(dst + hf * (HD / 2) + 32 * c + e) = w;
+        }
+      }
+    }
+    return;
+  }
+  constexpr int D = HD / 2, PW = D / 2;   // pairs per thread
+  const uint32_t ybase = smem_u32(ytile) + r * 128;
+  auto y8 = [&](int col, float* f) {      // 8 bf16 of row r from column col (multiple of 8)
+    const uint4 u = ld_shared_v4(ybase + (col >> 6) * CHUNK128 + (((((uint32_t)col >> 3) & 7u) ^ (r & 7)) << 4));
+    const bf16* b = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(b[e]);
+  };
+  float dot = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < HD; c += 32) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tacc + c, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < 32; q += 8) {
+      float y[8];
+      y8(c + q, y);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dot += __uint_as_float(v[q + e]) * y[e];
+    }
+  }
+  dot *= sh.scale / (float)HD;
+  const float rr = valid ? sh.rstd_qk[token * (sh.H + sh.Hkv) + head] : 0.f;
+  const int i0 = hf * PW;
+  uint32_t g1[PW], g2[PW];
+  if constexpr (PW == 32) {
+    tmem_ld_32x32b_x32(tacc + i0, g1);
+    tmem_ld_32x32b_x32(tacc + D + i0, g2);
+  } else {
+    tmem_ld_32x32b_x16(tacc + i0, g1);
+    tmem_ld_32x32b_x16(tacc + D + i0, g2);
+  }
+  tmem_ld_wait();
+  if (!valid) return;
+  const float4* cs = reinterpret_cast<const float4*>(sh.rope_tab + (size_t)pos * HD) + (i0 >> 1);
+#pragma unroll
+  for (int q = 0; q < PW; q += 8) {
+    float y1[8], y2[8], o1[8], o2[8];
+    y8(i0 + q, y1);
+    y8(D + i0 + q, y2);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const float4 t = __ldg(cs + ((q + e) >> 1));   // cos_i, sin_i, cos_i+1, sin_i+1
+      const float a0 = rr * (__uint_as_float(g1[q + e]) * sh.scale - y1[e] * dot);
+      const float a1 = rr * (__uint_as_float(g1[q + e + 1]) * sh.scale - y1[e + 1] * dot);
+      const float b0 = rr * (__uint_as_float(g2[q + e]) * sh.scale - y2[e] * dot);
+      const float b1 = rr * (__uint_as_float(g2[q + e + 1]) * sh.scale - y2[e + 1] * dot);
+      o1[e] = a0 * t.x - b0 * t.y;
+      o2[e] = a0 * t.y + b0 * t.x;
+      o1[e + 1] = a1 * t.z - b1 * t.w;
+      o2[e + 1] = a1 * t.w + b1 * t.z;
+    }
+    uint4 w1, w2;
+    w1.x = pack2(o1[0], o1[1]); w1.y = pack2(o1[2], o1[3]); w1.z = pack2(o1[4], o1[5]); w1.w = pack2(o1[6], o1[7]);
+    w2.x = pack2(o2[0], o2[1]); w2.y = pack2(o2[2], o2[3]); w2.z = pack2(o2[4], o2[5]); w2.w = pack2(o2[6], o2[7]);
+    *reinterpret_cast<uint4*>(dst + i0 + q) = w1;
+    *reinterpret_cast<uint4*>(dst + D + i0 + q) = w2;
+  }
+}
+
 // ======================================================================= backward: dQ
 template <int HD>
 struct DqSmem {
@@ -526,24 +624,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
     if (ok && at_wait_warp(dq_done, 0, sh, abort_flag)) {
       tc_fence_after();
-      bf16* dst = dqkv + (int64_t)(row0 + qpos) * sh.ld_qkv + (int64_t)h * HD + hf * (HD / 2);
-#pragma unroll 1
-      for (int c = 0; c < HD / 64; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tbase + lane_off + 256 + hf * (HD / 2) + 32 * c, v);
-        tmem_ld_wait();
-        if (valid) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 w;
-            w.x = pack2(__uint_as_float(v[e]) * sh.scale, __uint_as_float(v[e + 1]) * sh.scale);
-            w.y = pack2(__uint_as_float(v[e + 2]) * sh.scale, __uint_as_float(v[e + 3]) * sh.scale);
-            w.z = pack2(__uint_as_float(v[e + 4]) * sh.scale, __uint_as_float(v[e + 5]) * sh.scale);
-            w.w = pack2(__uint_as_float(v[e + 6]) * sh.scale, __uint_as_float(v[e + 7]) * sh.scale);
-            *reinterpret_cast<uint4*>(dst + 32 * c + e) = w;
-          }
-        }
-      }
+      at_out_tile<HD>(sh, tbase + lane_off + 256, smem + L::OFF_Q, r, hf, valid, qpos, (int64_t)row0 + qpos, h,
+                      dqkv + (int64_t)(row0 + qpos) * sh.ld_qkv + (int64_t)h * HD);
     }
   }
   tc_fence_before();
@@ -756,30 +838,27 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (ok && at_wait_warp(dkv_done, 0, sh, abort_flag)) {
       tc_fence_after();
       const bool valid = key < sh.T;
-      bf16* dk = dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + g) * HD + hf * (HD / 2);
       bf16* dv = dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + sh.Hkv + g) * HD + hf * (HD / 2);
 #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        const float sc = which ? sh.scale : 1.f;    // which = 1: dK (carries 1/sqrt(hd))
-        bf16* dst = which ? dk : dv;
-#pragma unroll 1
-        for (int c = 0; c < HD / 64; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + lane_off + 256 + which * HD + hf * (HD / 2) + 32 * c, v);
-          tmem_ld_wait();
-          if (valid) {
+      for (int c = 0; c < HD / 64; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tbase + lane_off + 256 + hf * (HD / 2) + 32 * c, v);
+        tmem_ld_wait();
+        if (valid) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint4 w;
-              w.x = pack2(__uint_as_float(v[e]) * sc, __uint_as_float(v[e + 1]) * sc);
-              w.y = pack2(__uint_as_float(v[e + 2]) * sc, __uint_as_float(v[e + 3]) * sc);
-              w.z = pack2(__uint_as_float(v[e + 4]) * sc, __uint_as_float(v[e + 5]) * sc);
-              w.w = pack2(__uint_as_float(v[e + 6]) * sc, __uint_as_float(v[e + 7]) * sc);
-              *reinterpret_cast<uint4*>(dst + 32 * c + e) = w;
-            }
+          for (int e = 0; e < 32; e += 8) {
+            uint4 w;
+            w.x = pack2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+            w.y = pack2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            w.z = pack2(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
+            w.w = pack2(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+            *reinterpret_cast<uint4*>(dv + 32 * c + e) = w;
           }
         }
       }
+      // dK (carries 1/sqrt(hd)), through the k-norm and rotation backward when fused
+      at_out_tile<HD>(sh, tbase + lane_off + 256 + HD, smem + L::OFF_K, r, hf, valid, key, (int64_t)row0 + key,
+                      sh.H + g, dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + g) * HD);
     }
   }
   tc_fence_before();
@@ -816,6 +895,8 @@ bool at_shape(int B, int T, int H, int Hkv, int hd, int32_t* err, AtShape* sh) {
   sh->scale_log2 = LOG2E * sh->scale;
   sh->err = err;
   sh->wait_ns = g_tc_wait_ns;
+  sh->rope_tab = nullptr;
+  sh->rstd_qk = nullptr;
   return true;
 }
 
@@ -876,9 +957,13 @@ nc_status launch_attn_fwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* q
 }
 
 nc_status launch_attn_bwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, const bf16* o, const float* lse,
-                             const bf16* dout, bf16* dqkv, float* Dv, int32_t* err, cudaStream_t st) {
+                             const bf16* dout, bf16* dqkv, float* Dv, const float* rstd_qk, const float* rope_tab,
+                             int32_t* err, cudaStream_t st) {
   AtShape sh;
   if (!at_shape(B, T, H, Hkv, hd, err, &sh)) return NC_ERR_ARG;
+  if ((rstd_qk == nullptr) != (rope_tab == nullptr) || (rope_tab && !aligned16(rope_tab))) return NC_ERR_ARG;
+  sh.rstd_qk = rstd_qk;
+  sh.rope_tab = rope_tab;
   if (!aligned16(qkv) || !aligned16(dout) || !aligned16(dqkv)) return NC_ERR_ARG;
   return hd == 128 ? attn_bwd_tc<128>(sh, qkv, o, lse, dout, dqkv, Dv, st)
                    : attn_bwd_tc<64>(sh, qkv, o, lse, dout, dqkv, Dv, st);

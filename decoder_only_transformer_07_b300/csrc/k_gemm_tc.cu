@@ -20,6 +20,7 @@
 // and MMAs (again bounded) and frees its TMEM before returning.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <string.h>
 
 #include "nc_kernels.cuh"
 #include "nc_ptx.cuh"
@@ -53,6 +54,7 @@ struct TcParams {
   // NC_EP_QKV_ROPE (the fused q/k/v projection): heads < rope_nh are rotated
   // (RoPE, cos/sin table [T][hd/2][2]) and RMS-normalised per head, their
   // rstd stored to rstd_qk[row * rope_nh + head]; the other heads are stored as is.
+  int tma_epi;             // 1: epilogue staged in smem and written by TMA (tmD / tmAux valid)
   const float* rope_tab;
   float* rstd_qk;
   int rope_T, rope_nh, rope_hd;
@@ -91,7 +93,11 @@ struct TcCfg {
   static constexpr int B_BYTES = BN * TC_BK * 2;            // 32 KB or 16 KB
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+  // epilogue staging: one [32 rows][128 B] 128B-swizzled box per epilogue warp
+  static constexpr int STG_OFF = STAGES * STAGE_BYTES;
+  static constexpr int STG_BYTES = TC_EPI_WARPS * 4096;
+  static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
+  static constexpr size_t SMEM = 1024 + (size_t)BAR_OFF + 256;
 };
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A and
@@ -222,96 +228,213 @@ __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
   return o;
 }
 
-// NC_EP_QKV_ROPE epilogue of one row over `ncols` accumulator columns (whole
-// heads) starting at output column n_base / TMEM column tcol0.  For a q or k
-// head: rstd = 1/sqrt(mean(u^2) + eps) from the fp32 accumulator u (the
-// rotation preserves the sum of squares, so this is the RMS of rope(u)), then
-// y_i = (u_i cos + u_{i+d} sin) rstd, y_{i+d} = (-u_i sin + u_{i+d} cos) rstd
-// with d = hd/2 and the angle of the row's position (cosmicrealm
-// "noao-chat-0-项目总体介绍" §2.1 items 1-2: rotary embedding, then QK norm).
-__device__ __forceinline__ void tc_epilogue_qkv_rope(const TcParams& p, int64_t m, int n_base, int ncols,
-                                                     uint32_t tcol0) {
+// Byte offset of 16-byte unit u of row r in a [32 rows][128 B] box stored
+// with the TMA 128-byte swizzle (unit index XOR row mod 8): the 32 lanes of a
+// warp, one row each, write a unit column in 4 conflict-free wavefronts.
+__device__ __forceinline__ uint32_t stg_off(int r, int u) {
+  return (uint32_t)(r * 128 + ((((u ^ r) & 7)) << 4));
+}
+
+// Staged epilogue of one warp: its 32 rows x (BN/2) accumulator columns pass
+// through the warp's [32][128 B] shared-memory box, 128 bytes of output per
+// row at a time (32 fp32 or 64 bf16 columns), and leave by TMA store - or
+// TMA reduce-add for the fp32 accumulate - as whole lines.  The relu^2
+// backward's aux input arrives in the same box by TMA load and is replaced in
+// place by the result.  Returns false if a bounded wait expired.
+template <int BN>
+__device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, const CUtensorMap* tmD, const CUtensorMap* tmAux,
+                                                   uint8_t* stg, uint64_t* aux_bar, uint32_t& aux_phase,
+                                                   uint32_t taddr, int n_base, int m0, int lane) {
+  const bool f32o = (p.ep == NC_EP_STORE_F32 || p.ep == NC_EP_ACCUM_F32);
+  const bool aux_in = (p.ep == NC_EP_RELU2_BWD || p.ep == NC_EP_RELU2_SQ_BWD);
+  const bool sq_bwd = (p.ep == NC_EP_RELU2_SQ_BWD);
+  const int cc = f32o ? 32 : 64;
+  const uint32_t sa = smem_u32(stg);
+  const int r = lane;
+#pragma unroll 1
+  for (int oc = 0; oc < BN / 2; oc += cc) {
+    const int n_out = n_base + oc;
+    if (n_out >= p.N) break;
+    // first accumulator piece into registers before the wait: the TMEM read
+    // overlaps the previous store still reading the box
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(taddr + oc, v);
+    tmem_ld_wait();
+    if (lane == 0) bulk_wait_read();   // the previous store has read the box
+    __syncwarp();
+    if (aux_in) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(aux_bar, 4096);
+        tma_load_2d(stg, tmAux, aux_bar, n_out, m0);
+      }
+      const bool ok = mbar_wait_bounded(aux_bar, aux_phase, p.wait_ns);
+      aux_phase ^= 1;
+      if (!__all_sync(0xffffffffu, ok)) return false;
+    }
+#pragma unroll 1
+    for (int pc = 0; pc < cc; pc += 32) {
+      if (pc > 0) {
+        tmem_ld_32x32b_x32(taddr + oc + pc, v);
+        tmem_ld_wait();
+      }
+      if (f32o) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) st_shared_v4(sa + stg_off(r, u), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int u = (pc >> 3) + k;
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[8 * k + e]);
+          if (p.ep == NC_EP_RELU2 || p.ep == NC_EP_RELU2_SQ) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = fmaxf(f[e], 0.f);
+            if (p.ep == NC_EP_RELU2_SQ) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] *= f[e];
+            }
+          } else if (aux_in) {
+            const uint4 a = ld_shared_v4(sa + stg_off(r, u));
+            const bf16* h = reinterpret_cast<const bf16*>(&a);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float x = __bfloat162float(h[e]);
+              f[e] *= 2.f * (sq_bwd ? sqrtf(x) : x);
+            }
+          }
+          const uint4 o = pack8_bf16(f);
+          st_shared_v4(sa + stg_off(r, u), o.x, o.y, o.z, o.w);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (p.ep == NC_EP_ACCUM_F32) tma_reduce_add_2d(tmD, stg, n_out, m0);
+      else tma_store_2d(tmD, stg, n_out, m0);
+      bulk_commit();
+    }
+    if (p.ep == NC_EP_RELU2) {   // second output: aux = relu(acc)^2
+      if (lane == 0) bulk_wait_read();
+      __syncwarp();
+#pragma unroll 1
+      for (int pc = 0; pc < cc; pc += 32) {
+        tmem_ld_32x32b_x32(taddr + oc + pc, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = fmaxf(__uint_as_float(v[8 * k + e]), 0.f) * fmaxf(__uint_as_float(v[8 * k + e]), 0.f);
+          const uint4 o = pack8_bf16(f);
+          st_shared_v4(sa + stg_off(r, (pc >> 3) + k), o.x, o.y, o.z, o.w);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tmAux, stg, n_out, m0);
+        bulk_commit();
+      }
+    }
+  }
+  return true;
+}
+
+// NC_EP_QKV_ROPE through the staging box: per head of the warp's columns,
+// q/k heads get rstd from the fp32 accumulator (the rotation keeps the sum of
+// squares) and the rotated, scaled values; v heads are stored as computed.
+__device__ __forceinline__ void tc_epilogue_qkv_rope_staged(const TcParams& p, const CUtensorMap* tmD, uint8_t* stg,
+                                                            uint32_t tcol0, int n_base, int ncols, int m0,
+                                                            int64_t m, int lane) {
   const int hd = p.rope_hd, d = hd >> 1;
+  const uint32_t sa = smem_u32(stg);
+  const int r = lane;
   const bool row_ok = m < p.M;
-  const int t = (int)(m % p.rope_T);
+  const float4* cs = reinterpret_cast<const float4*>(p.rope_tab + (size_t)(m % p.rope_T) * hd);
 #pragma unroll 1
   for (int hc = 0; hc < ncols; hc += hd) {
     const int n0 = n_base + hc;
     if (n0 >= p.N) break;
     const int head = n0 / hd;
     const uint32_t tc = tcol0 + hc;
-    bf16* dst = (bf16*)p.D + m * p.ldd + n0;
-    if (head >= p.rope_nh) {   // v head
+    const bool qk = head < p.rope_nh;
+    float rs = 1.f;
+    if (qk) {
+      float ss = 0.f;
 #pragma unroll 1
       for (int c = 0; c < hd; c += 32) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tc + c, r);
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tc + c, v);
         tmem_ld_wait();
-        if (row_ok) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            float v[8];
+        for (int e = 0; e < 32; ++e) ss += __uint_as_float(v[e]) * __uint_as_float(v[e]);
+      }
+      rs = rsqrtf(ss / (float)hd + p.rope_eps);
+    }
+#pragma unroll 1
+    for (int oc = 0; oc < hd; oc += 64) {
+      if (lane == 0) bulk_wait_read();
+      __syncwarp();
+#pragma unroll 1
+      for (int pc = oc; pc < oc + 64; pc += 32) {
+        float y[32];
+        if (!qk) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tc + pc, v);
+          tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(r[e + k]);
-            *reinterpret_cast<uint4*>(dst + c + e) = pack8_bf16(v);
+          for (int e = 0; e < 32; ++e) y[e] = __uint_as_float(v[e]);
+        } else {
+          // first half: y_i = (u_i cos + u_{i+d} sin) rs; second: y_{i+d} = (-u_i sin + u_{i+d} cos) rs
+          const bool first = pc < d;
+          const int i0 = first ? pc : pc - d;
+          uint32_t a[32], b[32];
+          tmem_ld_32x32b_x32(tc + i0, a);
+          tmem_ld_32x32b_x32(tc + i0 + d, b);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float4 q = __ldg(cs + ((i0 + e) >> 1));   // cos_i, sin_i, cos_i+1, sin_i+1
+            const float a0 = __uint_as_float(a[e]), a1 = __uint_as_float(a[e + 1]);
+            const float b0 = __uint_as_float(b[e]), b1 = __uint_as_float(b[e + 1]);
+            y[e] = (first ? (a0 * q.x + b0 * q.y) : (-a0 * q.y + b0 * q.x)) * rs;
+            y[e + 1] = (first ? (a1 * q.z + b1 * q.w) : (-a1 * q.w + b1 * q.z)) * rs;
           }
         }
-      }
-      continue;
-    }
-    float ss = 0.f;
-#pragma unroll 1
-    for (int c = 0; c < hd; c += 32) {
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(tc + c, r);
-      tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 32; ++e) ss += __uint_as_float(r[e]) * __uint_as_float(r[e]);
-    }
-    const float rs = rsqrtf(ss / (float)hd + p.rope_eps);
-    const float4* cs = reinterpret_cast<const float4*>(p.rope_tab + (size_t)t * hd);
-#pragma unroll 1
-    for (int c = 0; c < d; c += 32) {
-      uint32_t a[32], b[32];
-      tmem_ld_32x32b_x32(tc + c, a);
-      tmem_ld_32x32b_x32(tc + d + c, b);
-      tmem_ld_wait();
-      if (row_ok) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          float y1[8], y2[8];
-#pragma unroll
-          for (int k = 0; k < 8; k += 2) {
-            const float4 q = __ldg(cs + ((c + e + k) >> 1));   // cos_i, sin_i, cos_i+1, sin_i+1
-            const float a0 = __uint_as_float(a[e + k]), a1 = __uint_as_float(a[e + k + 1]);
-            const float b0 = __uint_as_float(b[e + k]), b1 = __uint_as_float(b[e + k + 1]);
-            y1[k] = (a0 * q.x + b0 * q.y) * rs;
-            y2[k] = (-a0 * q.y + b0 * q.x) * rs;
-            y1[k + 1] = (a1 * q.z + b1 * q.w) * rs;
-            y2[k + 1] = (-a1 * q.w + b1 * q.z) * rs;
-          }
-          *reinterpret_cast<uint4*>(dst + c + e) = pack8_bf16(y1);
-          *reinterpret_cast<uint4*>(dst + d + c + e) = pack8_bf16(y2);
+        for (int k = 0; k < 4; ++k) {
+          const uint4 o = pack8_bf16(y + 8 * k);
+          st_shared_v4(sa + stg_off(r, ((pc - oc) >> 3) + k), o.x, o.y, o.z, o.w);
         }
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tmD, stg, n0 + oc, m0);
+        bulk_commit();
+      }
     }
-    if (row_ok) p.rstd_qk[m * p.rope_nh + head] = rs;
+    if (qk && row_ok) p.rstd_qk[m * p.rope_nh + head] = rs;
   }
 }
 
 template <int BN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmAux, TcParams p) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* full_bar = (uint64_t*)(smem + S * Cfg::STAGE_BYTES);
+  uint64_t* full_bar = (uint64_t*)(smem + Cfg::BAR_OFF);
   uint64_t* empty_bar = full_bar + S;
   uint64_t* acc_full = empty_bar + S;      // [2]
   uint64_t* acc_empty = acc_full + 2;      // [2]
   uint64_t* drain_bar = acc_empty + 2;     // [1]
-  uint32_t* tmem_slot = (uint32_t*)(drain_bar + 1);
+  uint64_t* aux_bar = drain_bar + 1;       // [TC_EPI_WARPS] TMA loads of the epilogue's aux input
+  uint32_t* tmem_slot = (uint32_t*)(aux_bar + TC_EPI_WARPS);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -320,10 +443,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (int s = 0; s < S; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], TC_EPI_WARPS); }
     mbar_init(drain_bar, 1);
+    for (int w = 0; w < TC_EPI_WARPS; ++w) mbar_init(&aux_bar[w], 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (p.tma_epi) prefetch_tmap(&tmD);
   }
   if (warp == 2) {
     tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -416,6 +541,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ---------------- epilogue
     const int quarter = warp & 3;
     const int c_lo = ((warp - 4) >> 2) * (BN / 2);   // this warp's half of the columns
+    uint8_t* stg = smem + Cfg::STG_OFF + (warp - 4) * 4096;
+    uint32_t aux_phase = 0;
     int local = 0;
     TcSegIter it(p, blockIdx.x, gridDim.x);
     TcSeg sg;
@@ -433,8 +560,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         ? p.ws + ((size_t)sg.s * (p.tiles_m * p.tiles_n) + sg.t) * TC_BM * BN +
                               (size_t)(quarter * 32 + lane) * BN
                         : nullptr;
-      if (p.ep == NC_EP_QKV_ROPE) {
-        tc_epilogue_qkv_rope(p, m, tn * BN + c_lo, BN / 2, taddr + c_lo);
+      const int m0 = tm * TC_BM + quarter * 32;
+      if (m0 >= p.M && (p.ep == NC_EP_QKV_ROPE || (p.tma_epi && !part))) {
+        // all 32 rows of this warp are past the end: nothing to store
+      } else if (p.ep == NC_EP_QKV_ROPE) {
+        tc_epilogue_qkv_rope_staged(p, &tmD, stg, taddr + c_lo, tn * BN + c_lo, BN / 2, m0, m, lane);
+      } else if (p.tma_epi && !part) {
+        if (!tc_epilogue_staged<BN>(p, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
+                                    tn * BN + c_lo, m0, lane)) {
+          fail();
+          break;
+        }
       } else
 #pragma unroll 1
       for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
@@ -473,11 +609,199 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
     }
+    if (lane == 0) bulk_wait_all();   // TMA stores of this warp complete before the CTA exits
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- CTA-pair kernel
+// The same GEMM over 256 x 256 output tiles computed by a pair of CTAs (a
+// cluster of 2) with tcgen05 cta_group::2: CTA rank r stages rows
+// [128 r, 128 r + 128) of the A tile and rows [128 r, 128 r + 128) of the B
+// tile; one thread of rank 0 issues M = 256, N = 256 MMAs that read both
+// CTAs' shared memory, and each CTA's tensor memory holds its 128 rows of the
+// accumulator.  Per SM this stages 32 KB per 64-deep k-block instead of 48 KB
+// for the same multiply-adds as the single-CTA 128 x 256 tile.  Ring slots are
+// released (and accumulators published) to both CTAs by multicast commits;
+// both CTAs' epilogue warps release an accumulator on rank 0's barrier.
+struct Tc2Cfg {
+  static constexpr int STAGES = 6;
+  static constexpr int A_BYTES = TC_BM * TC_BK * 2;         // 16 KB: this CTA's 128 rows of A
+  static constexpr int B_BYTES = 128 * TC_BK * 2;           // 16 KB: this CTA's half of B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 512;                     // two 256-column accumulators
+  static constexpr int STG_OFF = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = STG_OFF + TC_EPI_WARPS * 4096;
+  static constexpr size_t SMEM = 1024 + (size_t)BAR_OFF + 256;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
+    k_gemm_tc2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmAux, TcParams p) {
+  using Cfg = Tc2Cfg;
+  constexpr int S = Cfg::STAGES;
+  constexpr int BN = 256;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* full_bar = (uint64_t*)(smem + Cfg::BAR_OFF);   // rank 0: both CTAs' loads land here
+  uint64_t* empty_bar = full_bar + S;                       // each CTA: its slot is free again
+  uint64_t* acc_full = empty_bar + S;                       // [2] each CTA: accumulator ready
+  uint64_t* acc_empty = acc_full + 2;                       // [2] rank 0: both epilogues done
+  uint64_t* drain_bar = acc_empty + 2;
+  uint64_t* aux_bar = drain_bar + 1;                        // [TC_EPI_WARPS]
+  uint32_t* tmem_slot = (uint32_t*)(aux_bar + TC_EPI_WARPS);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 2 * TC_EPI_WARPS); }
+    mbar_init(drain_bar, 1);
+    for (int w = 0; w < TC_EPI_WARPS; ++w) mbar_init(&aux_bar[w], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    if (p.tma_epi) prefetch_tmap(&tmD);
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();    // barriers of both CTAs initialised before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t full_rank0 = mapa_shared(smem_u32(full_bar), 0);
+  const uint32_t acc_empty_rank0 = mapa_shared(smem_u32(acc_empty), 0);
+
+  auto fail = [&]() {
+    if (p.err) atomicOr(p.err, NC_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer (both CTAs): own A rows and own half of B
+    int stage = 0;
+    uint32_t phase = 0;
+    TcSegIter it(p, cluster, nclusters);
+    TcSeg sg;
+    while (!*abort_flag && it.next(p, sg)) {
+      int tm, tn;
+      tile_coords(p, sg.t, tm, tn);
+      const int arow = tm * 256 + (int)rank * 128, brow = tn * BN + (int)rank * 128;
+      for (int kb = sg.k0; kb < sg.k1; ++kb) {
+        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, p.wait_ns)) { fail(); break; }
+        if (*abort_flag) break;
+        uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
+        uint8_t* sb = sa + Cfg::A_BYTES;
+        const uint32_t fb = full_rank0 + stage * 8;
+        if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * Cfg::STAGE_BYTES);
+        const int k0 = kb * TC_BK;
+        if (!p.a_mn) {
+          tma_load_2d_pair(sa, &tmA, fb, k0, arow);
+        } else {
+          tma_load_2d_pair(sa, &tmA, fb, arow, k0);
+          tma_load_2d_pair(sa + 8192, &tmA, fb, arow + 64, k0);
+        }
+        if (!p.b_mn) {
+          tma_load_2d_pair(sb, &tmB, fb, k0, brow);
+        } else {
+          tma_load_2d_pair(sb, &tmB, fb, brow, k0);
+          tma_load_2d_pair(sb + 8192, &tmB, fb, brow + 64, k0);
+        }
+        if (++stage == S) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ---------------- MMA issuer (rank 0 only): M = 256, N = 256
+    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)p.a_mn << 15) | ((uint32_t)p.b_mn << 16) |
+                           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+    int stage = 0;
+    uint32_t phase = 0;
+    int local = 0;
+    TcSegIter it(p, cluster, nclusters);
+    TcSeg sg;
+    for (; !*abort_flag && it.next(p, sg); ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1, p.wait_ns)) { fail(); break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = sg.k0; kb < sg.k1; ++kb) {
+        if (!mbar_wait_bounded(&full_bar[stage], phase, p.wait_ns)) { fail(); break; }
+        if (*abort_flag) break;
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+        const uint32_t sb = sa + Cfg::A_BYTES;
+#pragma unroll
+        for (int k = 0; k < TC_BK / 16; ++k)
+          tc_mma_f16_pair(d_tmem, operand_desc(sa, p.a_mn, k), operand_desc(sb, p.b_mn, k), idesc,
+                          (kb > sg.k0 || k > 0) ? 1u : 0u);
+        tc_commit_pair(&empty_bar[stage], 0x3);
+        if (++stage == S) { stage = 0; phase ^= 1; }
+      }
+      if (*abort_flag) break;
+      tc_commit_pair(&acc_full[acc], 0x3);
+    }
+    tc_commit_pair(drain_bar, 0x1);
+    mbar_wait_bounded(drain_bar, 0, p.wait_ns);
+  } else if (warp >= 4) {
+    // ---------------- epilogue (both CTAs): this CTA's 128 rows of the tile
+    const int quarter = warp & 3;
+    const int c_lo = ((warp - 4) >> 2) * (BN / 2);
+    uint8_t* stg = smem + Cfg::STG_OFF + (warp - 4) * 4096;
+    uint32_t aux_phase = 0;
+    int local = 0;
+    TcSegIter it(p, cluster, nclusters);
+    TcSeg sg;
+    for (; !*abort_flag && it.next(p, sg); ++local) {
+      int tm, tn;
+      tile_coords(p, sg.t, tm, tn);
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!mbar_wait_bounded(&acc_full[acc], acc_phase, p.wait_ns)) { fail(); break; }
+      tc_fence_after();
+      const int m0 = tm * 256 + (int)rank * 128 + quarter * 32;
+      const int64_t m = (int64_t)m0 + lane;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      if (m0 >= p.M) {
+        // all 32 rows of this warp are past the end: nothing to store
+      } else if (p.ep == NC_EP_QKV_ROPE) {
+        tc_epilogue_qkv_rope_staged(p, &tmD, stg, taddr + c_lo, tn * BN + c_lo, BN / 2, m0, m, lane);
+      } else if (p.tma_epi) {
+        if (!tc_epilogue_staged<BN>(p, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
+                                    tn * BN + c_lo, m0, lane)) {
+          fail();
+          break;
+        }
+      } else {
+#pragma unroll 1
+        for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c, r);
+          tmem_ld_wait();
+          if (m < p.M && tn * BN + c < p.N) tc_epilogue_row(p, m, tn * BN + c, r);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_rank0 + acc * 8);
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();    // the peer's shared memory and barriers stay alive until both CTAs are done
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
 }
 
 // Split-K fix-up: out (op)= sum over slices s = 0..splits-1, in that order
@@ -518,28 +842,34 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 2D bf16 tensor map over a row-major [outer][inner] matrix with leading
-// dimension ld (elements), box {box_inner, box_outer}, 128-byte swizzle.
-bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, int64_t ld,
-                      uint32_t box_inner, uint32_t box_outer) {
+// 2D tensor map over a row-major [outer][inner] matrix of 2- or 4-byte
+// elements with leading dimension ld (elements), box {box_inner, box_outer},
+// 128-byte swizzle.
+static bool make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
+                         uint64_t outer, int64_t ld, uint32_t box_inner, uint32_t box_outer) {
   auto enc = get_encode();
   if (!enc) return false;
+  if ((((uintptr_t)base) & 15) || ((ld * esize) % 16)) return false;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * esize};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, int64_t ld,
+                       uint32_t box_inner, uint32_t box_outer) {
+  return make_tmap_2d(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, outer, ld, box_inner, box_outer);
 }
 
 int g_num_sms = 0;
 uint64_t g_tc_wait_ns = 4000000000ull;   // bounded-wait limit of the tensor-core kernels
 
 template <int BN>
-static nc_status launch_tc_bn(TcParams p, const CUtensorMap& ta, const CUtensorMap& tb, size_t ws_bytes,
-                              cudaStream_t st) {
+static nc_status launch_tc_bn(TcParams p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
+                              const CUtensorMap& tx, size_t ws_bytes, cudaStream_t st) {
   static bool attr_set = false;
   auto kern = k_gemm_tc<BN>;
   if (!attr_set) {
@@ -568,13 +898,47 @@ static nc_status launch_tc_bn(TcParams p, const CUtensorMap& ta, const CUtensorM
     p.splits = (p.num_kb + p.kps - 1) / p.kps;
   }
   const int grid = std::min(tiles * p.splits, g_num_sms);
-  kern<<<grid, TC_THREADS, TcCfg<BN>::SMEM, st>>>(ta, tb, p);
+  kern<<<grid, TC_THREADS, TcCfg<BN>::SMEM, st>>>(ta, tb, td, tx, p);
   NC_CUDA_TRY(cudaGetLastError());
   if (p.splits > 1) {
     k_gemm_tc_fixup<BN><<<tiles, 256, 0, st>>>(p);
     NC_CUDA_TRY(cudaGetLastError());
   }
   return NC_OK;
+}
+
+int g_gemm_pair = 1;       // CTA-pair kernel for eligible shapes (test hook can turn it off)
+
+// 256 x 256 tiles on CTA pairs: persistent grid of co-resident clusters.
+static nc_status launch_tc_pair(TcParams p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
+                                const CUtensorMap& tx, cudaStream_t st) {
+  static int max_clusters = 0;
+  if (!max_clusters) {
+    NC_CUDA_TRY(cudaFuncSetAttribute(k_gemm_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Tc2Cfg::SMEM));
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (g_num_sms / 2));
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = Tc2Cfg::SMEM;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void*)k_gemm_tc2, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = g_num_sms / 2;
+    }
+    max_clusters = std::min(n, g_num_sms / 2);
+  }
+  p.splits = 1;
+  p.kps = p.num_kb;
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int grid = 2 * std::min(tiles, max_clusters);
+  k_gemm_tc2<<<grid, TC_THREADS, Tc2Cfg::SMEM, st>>>(ta, tb, td, tx, p);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
 // Split-K partials: up to 4 waves of 128 x 256 fp32 tiles per slice set.
@@ -627,16 +991,33 @@ static nc_status gemm_tc_impl(int M, int N, int K, const bf16* A, int64_t lda, i
     return NC_ERR_ARG;
   }
   if (ws && (((uintptr_t)ws) & 15)) return NC_ERR_ARG;
+  // CTA pairs (256 x 256 tiles) unless the single-CTA kernel would split K
+  // (few output tiles with an fp32 output: the weight gradients)
+  const bool f32_out = (ep == NC_EP_STORE_F32 || ep == NC_EP_ACCUM_F32);
+  const bool would_split = f32_out && ws && p.tiles_m * p.tiles_n < 4 * g_num_sms;
+  const bool pair = g_gemm_pair && BN == 256 && M >= 256 && !would_split;
+  if (pair) p.tiles_m = (M + 255) / 256;
   CUtensorMap ta, tb;
   bool ok;
   if (a_kmajor) ok = make_tmap_bf16_2d(&ta, A, K, M, lda, TC_BK, TC_BM);
   else ok = make_tmap_bf16_2d(&ta, A, M, K, lda, 64, TC_BK);
   if (!ok) return NC_ERR_CUDA;
-  if (b_kmajor) ok = make_tmap_bf16_2d(&tb, B, K, N, ldb, TC_BK, BN);
+  if (b_kmajor) ok = make_tmap_bf16_2d(&tb, B, K, N, ldb, TC_BK, pair ? 128 : BN);
   else ok = make_tmap_bf16_2d(&tb, B, N, K, ldb, 64, TC_BK);
   if (!ok) return NC_ERR_CUDA;
-  if (BN == 256) return launch_tc_bn<256>(p, ta, tb, ws_bytes, st);
-  return launch_tc_bn<128>(p, ta, tb, ws_bytes, st);
+  // Epilogue tensor maps: D (and aux for the relu^2 modes) in boxes of 32 rows
+  // x 128 bytes; without them (unaligned D) the epilogue stores per thread.
+  CUtensorMap td, tx;
+  memset(&td, 0, sizeof(td));
+  memset(&tx, 0, sizeof(tx));
+  p.tma_epi = f32_out ? make_tmap_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, N, M, ldd, 32, 32)
+                      : make_tmap_bf16_2d(&td, D, N, M, ldd, 64, 32);
+  if (p.tma_epi && (ep == NC_EP_RELU2 || ep == NC_EP_RELU2_BWD || ep == NC_EP_RELU2_SQ_BWD))
+    p.tma_epi = make_tmap_bf16_2d(&tx, aux, N, M, ldaux, 64, 32);
+  if (ep == NC_EP_QKV_ROPE && !p.tma_epi) return NC_ERR_ARG;
+  if (pair) return launch_tc_pair(p, ta, tb, td, tx, st);
+  if (BN == 256) return launch_tc_bn<256>(p, ta, tb, td, tx, ws_bytes, st);
+  return launch_tc_bn<128>(p, ta, tb, td, tx, ws_bytes, st);
 }
 
 nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_kmajor, const bf16* B,

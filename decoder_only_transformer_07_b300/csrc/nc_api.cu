@@ -176,11 +176,14 @@ static nc_status attn_fwd(int dtype, int B, int T, int H, int Hkv, int hd, const
   if (dtype == NC_BF16) return launch_attn_fwd_tc(B, T, H, Hkv, hd, (const bf16*)qkv, (bf16*)o, lse, err, st);
   return launch_attn_fwd_simt(dtype, B, T, H, Hkv, hd, qkv, o, lse, st);
 }
+// rstd_qk / rope_tab (bf16 only): fold the RoPE + QK-norm backward into the output.
 static nc_status attn_bwd(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv, const void* o,
-                          const float* lse, const void* dout, void* dqkv, float* Dv, int32_t* err, cudaStream_t st) {
+                          const float* lse, const void* dout, void* dqkv, float* Dv, const float* rstd_qk,
+                          const float* rope_tab, int32_t* err, cudaStream_t st) {
   if (dtype == NC_BF16)
     return launch_attn_bwd_tc(B, T, H, Hkv, hd, (const bf16*)qkv, (const bf16*)o, lse, (const bf16*)dout,
-                              (bf16*)dqkv, Dv, err, st);
+                              (bf16*)dqkv, Dv, rstd_qk, rope_tab, err, st);
+  if (rstd_qk || rope_tab) return NC_ERR_UNSUPPORTED;
   return launch_attn_bwd_simt(dtype, B, T, H, Hkv, hd, qkv, o, lse, dout, dqkv, Dv, st);
 }
 
@@ -487,10 +490,18 @@ static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int 
     // attention: x1 = x + o Wo^T
     NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, Hd, n, m->dx_act, C, 0, o, Hd, 0, NC_EP_STORE_F32, grads + to.off, Hd, nullptr, 0, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, Hd, C, m->dx_act, C, 1, wptr(m, to), Hd, 0, NC_EP_STORE, m->dout, Hd, nullptr, 0, st));
-    PROF(NC_PROF_ATTN_BWD, attn_fl, (double)N * (2.0 * W + 2.0 * Hd) * a + 8.0 * N * m->H,
-         attn_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, m->err, st));
-    PROF(NC_PROF_ROPE, 0, (double)N * nh * (3.0 * a * m->hd + 4),
-         launch_rope_qknorm_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, m->dqkv, qkv, rstdqk, m->rope_tab, st));
+    if (m->dtype == NC_BF16) {
+      // attention backward with the q/k RMSNorm + RoPE backward in its output epilogue
+      PROF(NC_PROF_ATTN_BWD, attn_fl, (double)N * (2.0 * W + 2.0 * Hd) * a + 8.0 * N * m->H,
+           attn_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, rstdqk, m->rope_tab,
+                    m->err, st));
+    } else {
+      PROF(NC_PROF_ATTN_BWD, attn_fl, (double)N * (2.0 * W + 2.0 * Hd) * a + 8.0 * N * m->H,
+           attn_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, nullptr, nullptr,
+                    m->err, st));
+      PROF(NC_PROF_ROPE, 0, (double)N * nh * (3.0 * a * m->hd + 4),
+           launch_rope_qknorm_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, m->dqkv, qkv, rstdqk, m->rope_tab, st));
+    }
     NC_TRY(gemm(m, NC_PROF_GEMM_DW, W, C, n, m->dqkv, W, 0, xn1, C, 0, NC_EP_STORE_F32, grads + tq.off, C, nullptr, 0, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, C, W, m->dqkv, W, 1, wptr(m, tq), C, 0, NC_EP_STORE_F32, m->dxn, C, nullptr, 0, st));
     PROF(NC_PROF_NORM, 0, nb_by,
@@ -658,7 +669,17 @@ extern "C" nc_status nc_op_attention_bwd(int32_t dtype, int32_t B, int32_t T, in
                                          const void* qkv, const void* o, const float* lse, const void* do_,
                                          void* dqkv, float* workspace, void* stream) {
   if (!dtype_ok(dtype) || !qkv || !o || !lse || !do_ || !dqkv || !workspace) return NC_ERR_ARG;
-  return attn_bwd(dtype, B, T, H, Hkv, hd, qkv, o, lse, do_, dqkv, workspace, nullptr, as_stream(stream));
+  return attn_bwd(dtype, B, T, H, Hkv, hd, qkv, o, lse, do_, dqkv, workspace, nullptr, nullptr, nullptr,
+                  as_stream(stream));
+}
+
+extern "C" nc_status nc_op_attention_bwd_rope(int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
+                                              const void* qkv, const void* o, const float* lse, const void* do_,
+                                              void* dqkv, float* workspace, const float* rstd, const float* cos_sin,
+                                              void* stream) {
+  if (!qkv || !o || !lse || !do_ || !dqkv || !workspace || !rstd || !cos_sin) return NC_ERR_ARG;
+  return attn_bwd(NC_BF16, B, T, H, Hkv, hd, qkv, o, lse, do_, dqkv, workspace, rstd, cos_sin, nullptr,
+                  as_stream(stream));
 }
 
 extern "C" nc_status nc_op_cross_entropy(int32_t dtype, int64_t rows, int32_t V, void* z, const int32_t* targets,
@@ -707,3 +728,6 @@ extern "C" nc_status nc_profile_read(nc_model* m, int32_t cls, double* ms, int64
 
 // Test hook: the time limit (ns) of every bounded wait in the tensor-core kernels.
 extern "C" void nc_debug_set_wait_limit_ns(uint64_t ns) { g_tc_wait_ns = ns; }
+
+extern int g_gemm_pair;
+extern "C" void nc_debug_set_gemm_pair(int32_t on) { g_gemm_pair = on != 0; }

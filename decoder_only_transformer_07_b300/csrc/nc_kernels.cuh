@@ -58,8 +58,12 @@ nc_status launch_attn_bwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, 
 // err (device int32, may be NULL) receives NC_DEVERR_TIMEOUT if a bounded wait expires.
 nc_status launch_attn_fwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, bf16* o, float* lse,
                              int32_t* err, cudaStream_t st);
+// With rstd_qk and rope_tab (both or neither), dq and dk are returned through the
+// per-head RMSNorm backward and the transposed rotation (the RoPE + QK-norm
+// backward fused into the output epilogue).
 nc_status launch_attn_bwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, const bf16* o, const float* lse,
-                             const bf16* dout, bf16* dqkv, float* Dv, int32_t* err, cudaStream_t st);
+                             const bf16* dout, bf16* dqkv, float* Dv, const float* rstd_qk, const float* rope_tab,
+                             int32_t* err, cudaStream_t st);
 
 // 2D bf16 TMA descriptor over a row-major [outer][inner] matrix with leading
 // dimension ld (elements), box {box_inner, box_outer}, 128-byte swizzle.

@@ -230,6 +230,16 @@ nc_status nc_op_attention_bwd(int32_t dtype, int32_t B, int32_t T, int32_t H,
                               int32_t Hkv, int32_t hd, const void* qkv, const void* o,
                               const float* lse, const void* do_, void* dqkv,
                               float* workspace, void* stream);
+/* The bf16 attention backward with the backward of nc_op_rope_qknorm_fwd
+ * folded into its output: the q and k blocks of dqkv receive the gradient with
+ * respect to the projection output (before RoPE and the per-head RMSNorm),
+ * given the saved normalised qkv, rstd (float [B*T, H+Hkv]) and the cos/sin
+ * table; the v block is as from nc_op_attention_bwd.  Equivalent to
+ * nc_op_attention_bwd followed by nc_op_rope_qknorm_bwd.  hd 64 or 128. */
+nc_status nc_op_attention_bwd_rope(int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
+                                   const void* qkv, const void* o, const float* lse,
+                                   const void* do_, void* dqkv, float* workspace,
+                                   const float* rstd, const float* cos_sin, void* stream);
 
 /* Cross-entropy on logits z (dtype [rows, V]) against targets (int32 [rows]):
  * row_loss (float [rows]) = logsumexp(z) - z[target]; z is overwritten in
@@ -304,6 +314,12 @@ nc_status nc_profile_read(nc_model* m, int32_t cls, double* ms, int64_t* launche
  * MMAs (again bounded), frees its tensor memory and returns.
  * ---------------------------------------------------------------------- */
 void nc_debug_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook.  on = 0 makes every bf16 GEMM use the single-CTA kernel (128 x
+ * 256 tiles); on = 1 (default) lets shapes with M >= 256 and N > 128 that do
+ * not split K run on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2).  Both
+ * compute the same sums; the switch exists to test and time either path. */
+void nc_debug_set_gemm_pair(int32_t on);
 
 #ifdef __cplusplus
 }

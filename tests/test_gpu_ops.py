@@ -296,6 +296,42 @@ def test_attention_fwd_bwd(hd, H, Hkv, T, dt):
             assert cosine(got[:, :, sl], ref[:, :, sl]) > 0.9999, name
 
 
+@pytest.mark.parametrize("hd,H,Hkv,T", [(128, 4, 2, 300), (64, 2, 1, 200), (128, 2, 2, 128)])
+def test_attention_bwd_with_fused_rope_qknorm_bwd(hd, H, Hkv, T):
+    """Attention backward whose dq / dk leave through the QK-norm and RoPE
+    backward, against the oracle's attention backward followed by its RMSNorm
+    and rotation backward on the same normalised bf16 q, k, v."""
+    B, eps, base = 2, 1.1920929e-07, 10000.0
+    W = (H + 2 * Hkv) * hd
+    QKV = dev_tensor(rnd(60, (B * T, W)), BF16)
+    tab = torch.empty((T, hd // 2, 2), dtype=F32, device="cuda")
+    nc.ops.rope_table(T, hd, base, tab)
+    R = torch.empty((B * T, H + Hkv), dtype=F32, device="cuda")
+    nc.ops.rope_qknorm_fwd(QKV, B, T, H, Hkv, hd, R, tab, eps)      # q, k now rotated and normalised
+    O = torch.empty((B * T, H * hd), dtype=BF16, device="cuda")
+    L = torch.empty((B, H, T), dtype=F32, device="cuda")
+    nc.ops.attention_fwd(QKV, B, T, H, Hkv, hd, O, L)
+    DO = dev_tensor(rnd(61, (B * T, H * hd)), BF16)
+    DQKV = torch.zeros((B * T, W), dtype=BF16, device="cuda")
+    ws = torch.empty(B * H * T, dtype=F32, device="cuda")
+    nc.ops.attention_bwd_rope(QKV, O, L, DO, B, T, H, Hkv, hd, DQKV, ws, R, tab)
+    torch.cuda.synchronize()
+    qkv = to64(QKV)
+    _, _, d_ref = _attn_ref(qkv, B, T, H, Hkv, hd, to64(DO))
+    cos, sin = OM.rope_tables(T, hd, base)
+    g = d_ref.reshape(B, T, H + 2 * Hkv, hd)[:, :, :H + Hkv].transpose(0, 2, 1, 3)
+    y = qkv.reshape(B, T, H + 2 * Hkv, hd)[:, :, :H + Hkv].transpose(0, 2, 1, 3)
+    rr = to64(R).reshape(B, T, H + Hkv).transpose(0, 2, 1)[..., None]
+    want_qk = OM.rope_bwd(OM.rms_norm_bwd(g, y, rr), cos, sin)
+    got = to64(DQKV).reshape(B, T, H + 2 * Hkv, hd)
+    from tests.gpu_util import cosine
+    got_qk = got[:, :, :H + Hkv].transpose(0, 2, 1, 3)
+    assert cosine(got_qk[:, :H], want_qk[:, :H]) > 0.9999, "dq"
+    assert cosine(got_qk[:, H:], want_qk[:, H:]) > 0.9999, "dk"
+    want_v = d_ref.reshape(B, T, H + 2 * Hkv, hd)[:, :, H + Hkv:]
+    assert cosine(got[:, :, H + Hkv:], want_v) > 0.9999, "dv"
+
+
 # ---------------------------------------------------------------- cross-entropy
 
 @pytest.mark.parametrize("dt", [F32, BF16])
