@@ -44,6 +44,10 @@ DESCR = {
     "d26": "d26 GPT L26 C1664 H13/13 hd128 F6656 V65536 T2048 B16 (bf16)",
     "d24gqa": "d24 GQA GPT L24 C1536 H12/4 hd128 F6144 V65536 T4096 B8 (bf16)",
 }
+# DRAM traffic per GEMM call (main kernel + split-K fix-up), from the ncu capture of a
+# full step summarised in profiles/launches_d20_step.md; set to None when the GEMM
+# kernels change and the capture is not repeated.
+GEMM_DRAM_BYTES_PER_CALL = {"d20": 1190e6}
 # CPU-oracle sample (tokens of one sequence) per workload: ~10-30 s of fp64 work
 CPU_SAMPLE_T = {"tiny": 64, "d12": 128, "d20": 64, "d26": 48, "d24gqa": 48}
 
@@ -227,6 +231,8 @@ def main():
     ap.add_argument("--config", default="d20", choices=sorted(S.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step-batch", type=int, default=0,
+                    help="profiling only: run the step at this batch size instead of the workload's")
     # single-op mode (profiling)
     ap.add_argument("--op", choices=["gemm", "attn", "attn_fwd"])
     ap.add_argument("--m", type=int, default=65536)
@@ -244,7 +250,7 @@ def main():
     args = ap.parse_args()
     if args.op:
         return run_op(args)
-    w = S.workload(args.config)
+    w = S.workload(args.config, **({"batch": args.step_batch} if args.step_batch else {}))
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -338,9 +344,11 @@ def main():
 
     g = prof["gemm"]
     gemm_tflops = g["flops"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else None
-    roofline = {"kernel": "k_gemm_tc (tcgen05 bf16 GEMM, all 5 linear layers fwd + dX + dW)",
+    roofline = {"kernel": "k_gemm_tc2 / k_gemm_tc (tcgen05 bf16 GEMM, all 5 linear layers fwd + dX + dW)",
                 "bound": "tensor", "achieved": gemm_tflops, "peak": peak_sust, "unit": "TFLOP/s",
-                "frac": (gemm_tflops / peak_sust) if gemm_tflops else None, "traffic": None,
+                "frac": (gemm_tflops / peak_sust) if gemm_tflops else None,
+                "traffic": GEMM_DRAM_BYTES_PER_CALL.get(args.config) if not args.step_batch else None,
+                "traffic_unit": "DRAM bytes per GEMM call (ncu dram__bytes_read.sum + write.sum)",
                 "peak_kind": f"bf16 dense, sustained ({peak_src})"}
     total_prof_ms = sum(v["ms"] for k, v in prof.items() if not k.startswith("gemm_"))
     kernels = {k: {"ms_per_step": v["ms"] / args.steps, "share": (v["ms"] / total_prof_ms) if total_prof_ms else None,

@@ -13,7 +13,7 @@
 //   warp 0      TMA producer (one elected thread)
 //   warp 1      MMA issuer (one thread issues tcgen05.mma / tcgen05.commit)
 //   warp 2      allocates and frees the 512 TMEM columns
-//   warp 3      (dK/dV kernel only) stages lse and D of each query tile
+//   warp 3      forward: second MMA issuer; dK/dV kernel: stages lse and D
 //   warps 4-11  "softmax" warps: each thread owns one TMEM lane = one row of
 //               the score tile, so row reductions need no shuffles.
 //
@@ -107,15 +107,28 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
 
+// CTA order: heads in chunks of 16, and within a chunk the most expensive
+// tile of every head first.  The chunk's K / V stays in L2 while its CTAs run,
+// and the cheap tiles of one chunk overlap the expensive tiles of the next, so
+// only the last chunk ends on short work.  Returns (rank, head): rank 0 is the
+// most expensive tile.
+__device__ __forceinline__ void at_cta_order(int idx, int heads, int ntiles, int& rank, int& head) {
+  constexpr int HG = 16;
+  const int chunk = idx / (HG * ntiles);
+  const int hg = min(HG, heads - chunk * HG);
+  const int within = idx - chunk * HG * ntiles;
+  rank = within / hg;
+  head = chunk * HG + within % hg;
+}
+
 // ======================================================================= forward
 template <int HD>
 struct FwdSmem {
   static constexpr uint32_t TILE = 128 * HD * 2;          // one [128][HD] bf16 tile
-  static constexpr uint32_t P_BYTES = 2 * CHUNK128;       // [128 queries][128 keys] bf16
+  static constexpr int NSLOT = 4;
   static constexpr uint32_t OFF_Q = 0;                    // Q0, Q1
-  static constexpr uint32_t OFF_KV = 2 * TILE;            // 3-slot ring: K0 V0 K1 V1 ...
-  static constexpr uint32_t OFF_P = OFF_KV + 3 * TILE;    // P0, P1
-  static constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr uint32_t OFF_KV = 2 * TILE;            // 4-slot ring: K0 V0 K1 V1 ...
+  static constexpr uint32_t OFF_BAR = OFF_KV + NSLOT * TILE;
   static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
 };
 
@@ -127,22 +140,23 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bar = (uint64_t*)(smem + L::OFF_BAR);
+  constexpr int NS = L::NSLOT;
   uint64_t* q_full = bar;          // [1]
-  uint64_t* kv_full = bar + 1;     // [3]
-  uint64_t* kv_empty = bar + 4;    // [3]
-  uint64_t* s_full = bar + 7;      // [2] S_i in TMEM
-  uint64_t* s_free = bar + 9;      // [2] S_i read into registers (4 warps)
-  uint64_t* p_full = bar + 11;     // [2] P_i in smem, O_i rescaled (4 warps)
-  uint64_t* pv_done = bar + 13;    // [2] O_i += P_i V complete
-  uint64_t* drain = bar + 15;
-  uint32_t* tmem_slot = (uint32_t*)(bar + 16);
+  uint64_t* kv_full = bar + 1;     // [NS]
+  uint64_t* kv_empty = kv_full + NS;
+  uint64_t* s_full = kv_empty + NS;   // [2] S_i in TMEM (and every earlier MMA of the CTA done)
+  uint64_t* p_full = s_full + 2;      // [2] P_i in TMEM, O_i rescaled (4 warps)
+  uint64_t* pv_done = p_full + 2;     // [2] O_i += P_i V complete
+  uint64_t* drain = pv_done + 2;      // [2] one per issuer
+  uint32_t* tmem_slot = (uint32_t*)(drain + 2);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int BH = sh.B * sh.H;
   const int nqb = (sh.T + 255) >> 8;
-  const int qb = nqb - 1 - (int)(blockIdx.x / BH);    // longest causal rows first
-  const int bh = blockIdx.x % BH, b = bh / sh.H, h = bh - b * sh.H, g = h / sh.G;
+  int rank, bh;
+  at_cta_order((int)blockIdx.x, sh.B * sh.H, nqb, rank, bh);
+  const int qb = nqb - 1 - rank;                       // longest causal rows first
+  const int b = bh / sh.H, h = bh - b * sh.H, g = h / sh.G;
   const int nt = (sh.T + 127) >> 7;
   const int n0 = 2 * qb + 1;                           // key tiles of query tile 0
   const int n1 = (2 * qb + 1 < nt) ? 2 * qb + 2 : 0;   // of query tile 1 (0: past the end)
@@ -151,11 +165,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 3; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
+    // every K / V slot is released by both issuers when query tile 1 exists
+    for (int s = 0; s < NS; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], n1 > 0 ? 2 : 1); }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1); mbar_init(&s_free[i], 4); mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1);
+      mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1); mbar_init(&drain[i], 1);
     }
-    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_qkv);
@@ -164,7 +178,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tbase = *tmem_slot;   // S0 cols 0-127, S1 128-255, O0 256.., O1 256+HD..
+  // S0 cols 0-127, S1 128-255 (P_i overwrites the first 64 columns of S_i), O0 256.., O1 256+HD..
+  const uint32_t tbase = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
@@ -175,8 +190,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     row0 + (2 * qb + i) * 128);
     int issued = 0;
     for (int c = 0; c < 2 * nmax && !*abort_flag; ++c) {
-      const int s = c % 3;
-      if (!at_wait(&kv_empty[s], ((c / 3) & 1) ^ 1, sh, abort_flag)) break;
+      const int s = c % NS;
+      if (!at_wait(&kv_empty[s], ((c / NS) & 1) ^ 1, sh, abort_flag)) break;
       const int col = ((c & 1) ? (sh.H + sh.Hkv + g) : (sh.H + g)) * HD;
       mbar_arrive_expect_tx(&kv_full[s], L::TILE);
       for (int cc = 0; cc < HD / 64; ++cc)
@@ -186,55 +201,53 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
     // every load lands before the CTA exits (already so unless aborted)
     mbar_wait_bounded(q_full, 0, sh.wait_ns);
-    for (int s = 0; s < 3; ++s) {
-      const int uses = issued / 3 + ((issued % 3) > s ? 1 : 0);
+    for (int s = 0; s < NS; ++s) {
+      const int uses = issued / NS + ((issued % NS) > s ? 1 : 0);
       if (uses > 0) mbar_wait_bounded(&kv_full[s], (uses - 1) & 1, sh.wait_ns);
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
+  } else if ((warp == 1 || warp == 3) && lane == 0) {
+    // ---------------- MMA issuers: warp 1 for query tile 0, warp 3 for tile 1.
+    // A single thread issues at most about one MMA per ~100 cycles, less than
+    // an M = 128, N = 128 product takes, so each tile has its own issuer and
+    // the tensor pipe interleaves two independent chains
+    //   S_i = Q_i K_j^T  ->  (softmax writes P_i over S_i)  ->  O_i += P_i V_j
+    // In-order execution per issuer keeps S_i of tile j+1 behind O_i += P_i V_j.
+    const int i = warp == 1 ? 0 : 1;
+    const int n = i ? n1 : n0;
     const uint32_t id_s = at_idesc(128, 0), id_pv = at_idesc(HD, 1);
-    const uint32_t sq = smem_u32(smem + L::OFF_Q), skv = smem_u32(smem + L::OFF_KV);
-    const uint32_t sp = smem_u32(smem + L::OFF_P);
-    auto kv_ready = [&](int c) { return at_wait(&kv_full[c % 3], (c / 3) & 1, sh, abort_flag); };
-    auto issue_s = [&](int i, int j) -> bool {   // S_i = Q_i K_j^T
-      if (j > 0 && !at_wait(&s_free[i], (j - 1) & 1, sh, abort_flag)) return false;
+    const uint32_t sq = smem_u32(smem + L::OFF_Q) + i * L::TILE, skv = smem_u32(smem + L::OFF_KV);
+    auto kv_ready = [&](int c) { return at_wait(&kv_full[c % NS], (c / NS) & 1, sh, abort_flag); };
+    // (an inactive tile 1, n1 = 0, takes no part: the slots then count one release)
+    bool ok = (n > 0) && at_wait(q_full, 0, sh, abort_flag);
+    for (int j = 0; ok && j < nmax; ++j) {
+      const int cK = 2 * j, cV = 2 * j + 1;
+      if (j >= n) {
+        // key tile only the other query tile uses: release its slots once filled
+        if (kv_ready(cK)) mbar_arrive(&kv_empty[cK % NS]);
+        if (kv_ready(cV)) mbar_arrive(&kv_empty[cV % NS]);
+        continue;
+      }
+      if (!(ok = kv_ready(cK))) break;
       tc_fence_after();
-      const uint32_t a = sq + i * L::TILE, kb = skv + ((2 * j) % 3) * L::TILE;
+      const uint32_t kb = skv + (cK % NS) * L::TILE;
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk)
-        tc_mma_f16(tbase + i * 128, kdesc(a, kk, CHUNK128), kdesc(kb, kk, CHUNK128), id_s, kk > 0 ? 1u : 0u);
+        tc_mma_f16(tbase + i * 128, kdesc(sq, kk, CHUNK128), kdesc(kb, kk, CHUNK128), id_s, kk > 0 ? 1u : 0u);
       tc_commit(&s_full[i]);
-      return true;
-    };
-    auto issue_pv = [&](int i, int j) -> bool {  // O_i += P_i V_j
-      if (!at_wait(&p_full[i], j & 1, sh, abort_flag)) return false;
+      tc_commit(&kv_empty[cK % NS]);
+      if (!(ok = kv_ready(cV)) || !(ok = at_wait(&p_full[i], j & 1, sh, abort_flag))) break;
       tc_fence_after();
-      const uint32_t a = sp + i * L::P_BYTES, vb = skv + ((2 * j + 1) % 3) * L::TILE;
+      const uint32_t vb = skv + (cV % NS) * L::TILE;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        tc_mma_f16(tbase + 256 + i * HD, kdesc(a, kk, CHUNK128), mndesc(vb, kk, CHUNK128), id_pv,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < 8; ++kk)   // O_i += P_i V_j, P_i from tensor memory
+        tc_mma_f16_ts(tbase + 256 + i * HD, tbase + i * 128 + 8 * kk, mndesc(vb, kk, CHUNK128), id_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
       tc_commit(&pv_done[i]);
-      return true;
-    };
-    bool ok = at_wait(q_full, 0, sh, abort_flag) && kv_ready(0);
-    if (ok) ok = issue_s(0, 0);
-    if (ok && n1 > 0) ok = issue_s(1, 0);
-    if (ok) tc_commit(&kv_empty[0]);
-    for (int j = 0; ok && j < nmax; ++j) {
-      const bool more = j + 1 < nmax;
-      ok = kv_ready(2 * j + 1);
-      if (ok && j < n0) ok = issue_pv(0, j);
-      if (ok && more) ok = kv_ready(2 * j + 2);
-      if (ok && j + 1 < n0) ok = issue_s(0, j + 1);
-      if (ok && j < n1) ok = issue_pv(1, j);
-      if (ok) tc_commit(&kv_empty[(2 * j + 1) % 3]);
-      if (ok && j + 1 < n1) ok = issue_s(1, j + 1);
-      if (ok && more) tc_commit(&kv_empty[(2 * j + 2) % 3]);
+      tc_commit(&kv_empty[cV % NS]);
       if (*abort_flag) ok = false;
     }
-    tc_commit(drain);
-    mbar_wait_bounded(drain, 0, sh.wait_ns);
+    tc_commit(&drain[i]);
+    mbar_wait_bounded(&drain[i], 0, sh.wait_ns);
   } else if (warp >= 4) {
     // ---------------- softmax warpgroups: warps 4-7 own query tile 0, 8-11 tile 1
     const int i = (warp - 4) >> 2, quarter = warp & 3;
@@ -245,8 +258,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tS = tbase + lane_off + i * 128;
     const uint32_t tO = tbase + lane_off + 256 + i * HD;
-    const uint32_t sP = smem_u32(smem + L::OFF_P + i * L::P_BYTES) + r * 128;
-    const uint32_t swz = r & 7;
     float m = 0.f, l = 0.f;                        // running max (raw score units), row sum
     const float thresh = 8.f / sh.scale_log2;      // raise m only when it grows by > 2^8 in P
     bool ok = true;
@@ -257,9 +268,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS + 32 * c, x + 32 * c);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[i]);
       const int k0 = j * 128;
       if ((j == qt) || (k0 + 128 > sh.T)) {   // diagonal / ragged tile: mask in raw units
         const int lim = min(qpos - k0, sh.T - 1 - k0);   // last visible column
@@ -275,11 +283,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(x[c]));
       const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                              fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      // P_i's buffer and O_i are free once the previous O_i += P V completed
-      if (j > 0) {
-        if (!(ok = at_wait_warp(&pv_done[i], (j - 1) & 1, sh, abort_flag))) break;
-        tc_fence_after();
-      }
+      // O_i += P_i V_{j-1} was issued before S_i of this tile, so it completed
+      // with it: O_i is stable and may be rescaled here.
       if (j == 0) {
         m = (mx == -INFINITY) ? 0.f : mx;
       } else {
@@ -305,19 +310,19 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       const float mc = m * sh.scale_log2;
       float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        float pv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          pv[e] = ex2_approx(fmaf(__uint_as_float(x[8 * u + e]), sh.scale_log2, -mc));
-          s8[e] += pv[e];
-        }
-        st_shared_v4(sP + (u >> 3) * CHUNK128 + ((((uint32_t)u & 7u) ^ swz) << 4), pack2(pv[0], pv[1]),
-                     pack2(pv[2], pv[3]), pack2(pv[4], pv[5]), pack2(pv[6], pv[7]));
+      for (int c = 0; c < 64; ++c) {   // packed in place: x[c] <- bf16x2(p[2c], p[2c+1])
+        const float p0 = ex2_approx(fmaf(__uint_as_float(x[2 * c]), sh.scale_log2, -mc));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(x[2 * c + 1]), sh.scale_log2, -mc));
+        s8[(2 * c) & 7] += p0;
+        s8[(2 * c + 1) & 7] += p1;
+        x[c] = pack2(p0, p1);
       }
       const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+      // P_i into the first 64 columns of S_i (this warp's lanes, already read)
+      tmem_st_32x32b_x32(tS, x);
+      tmem_st_32x32b_x32(tS + 32, x + 32);
+      tmem_st_wait();
       l += sum;
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[i]);
@@ -453,8 +458,7 @@ struct DqSmem {
   static constexpr uint32_t OFF_DO = TILE;
   static constexpr uint32_t OFF_K = 2 * TILE;      // 2 slots
   static constexpr uint32_t OFF_V = 4 * TILE;      // 2 slots
-  static constexpr uint32_t OFF_DS = 6 * TILE;     // [128 queries][128 keys] bf16
-  static constexpr uint32_t OFF_BAR = OFF_DS + 2 * CHUNK128;
+  static constexpr uint32_t OFF_BAR = 6 * TILE;
   static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
 };
 
@@ -474,7 +478,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint64_t* v_empty = bar + 7;     // [2]
   uint64_t* sdp_full = bar + 9;    // S and dP in TMEM
   uint64_t* sdp_free = bar + 10;   // S and dP read (8 warps)
-  uint64_t* ds_full = bar + 11;    // dS in smem (8 warps)
+  uint64_t* ds_full = bar + 11;    // dS in tensor memory (8 warps)
   uint64_t* ds_free = bar + 12;    // dQ += dS K complete
   uint64_t* dq_done = bar + 13;
   uint64_t* drain = bar + 14;
@@ -482,10 +486,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int BH = sh.B * sh.H;
   const int nt = (sh.T + 127) >> 7;
-  const int qt = nt - 1 - (int)(blockIdx.x / BH);
-  const int bh = blockIdx.x % BH, b = bh / sh.H, h = bh - b * sh.H, g = h / sh.G;
+  int rank, bh;
+  at_cta_order((int)blockIdx.x, sh.B * sh.H, nt, rank, bh);
+  const int qt = nt - 1 - rank;                        // longest causal rows first
+  const int b = bh / sh.H, h = bh - b * sh.H, g = h / sh.G;
   const int n = qt + 1;
   const int row0 = b * sh.T;
 
@@ -505,7 +510,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tbase = *tmem_slot;   // S cols 0-127, dP 128-255, dQ 256..
+  const uint32_t tbase = *tmem_slot;   // S cols 0-127, dP 128-255, dQ 256.., dS (bf16 pairs) 384-447
 
   if (warp == 0 && lane == 0) {
     mbar_arrive_expect_tx(qd_full, 2 * L::TILE);
@@ -541,7 +546,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const uint32_t id_s = at_idesc(128, 0), id_q = at_idesc(HD, 1);
     const uint32_t sq = smem_u32(smem + L::OFF_Q), sdo = smem_u32(smem + L::OFF_DO);
     const uint32_t sk = smem_u32(smem + L::OFF_K), sv = smem_u32(smem + L::OFF_V);
-    const uint32_t sds = smem_u32(smem + L::OFF_DS);
     auto issue_sdp = [&](int j) -> bool {
       const int s = j & 1;
       const uint32_t par = (j >> 1) & 1;
@@ -567,9 +571,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       tc_fence_after();
       const uint32_t kb = sk + (j & 1) * L::TILE;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        tc_mma_f16(tbase + 256, kdesc(sds, kk, CHUNK128), mndesc(kb, kk, CHUNK128), id_q,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < 8; ++kk)   // dQ += dS K_j, dS from tensor memory
+        tc_mma_f16_ts(tbase + 256, tbase + 384 + 8 * kk, mndesc(kb, kk, CHUNK128), id_q,
+                      (j > 0 || kk > 0) ? 1u : 0u);
       tc_commit(ds_free);
       tc_commit(&k_empty[j & 1]);
       if (*abort_flag) ok = false;
@@ -583,8 +587,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int qpos = qt * 128 + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tS = tbase + lane_off + 64 * hf, tP = tS + 128;
-    const uint32_t sDS = smem_u32(smem + L::OFF_DS) + hf * CHUNK128 + r * 128;
-    const uint32_t swz = r & 7;
+    const uint32_t tDS = tbase + lane_off + 384 + 32 * hf;   // this half's 64 keys as 32 bf16 pairs
     const bool valid = qpos < sh.T;
     const float lse2 = valid ? lse[(int64_t)bh * sh.T + qpos] * LOG2E : INFINITY;
     const float Dr = valid ? Dv[(int64_t)bh * sh.T + qpos] : 0.f;
@@ -613,12 +616,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         if (!(ok = at_wait_warp(ds_free, (j - 1) & 1, sh, abort_flag))) break;
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float* f = reinterpret_cast<const float*>(s + 8 * u);
-        st_shared_v4(sDS + ((((uint32_t)u) ^ swz) << 4), pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]),
-                     pack2(f[6], f[7]));
-      }
-      fence_proxy_async_smem();
+      for (int c = 0; c < 32; ++c) s[c] = pack2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
+      tmem_st_32x32b_x32(tDS, s);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
     }
@@ -641,11 +642,10 @@ struct DkvSmem {
   static constexpr uint32_t QT = 64 * HD * 2;        // one [64][HD] tile
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = KT;
-  static constexpr uint32_t OFF_QS = 2 * KT;         // 3 stages of {Q, dO}
-  static constexpr uint32_t OFF_PT = OFF_QS + 3 * 2 * QT;   // [128 keys][64 queries] bf16
-  static constexpr uint32_t OFF_DST = OFF_PT + CHUNK128;
-  static constexpr uint32_t OFF_LD = OFF_DST + CHUNK128;    // 3 stages of {lse*log2e[64], D[64]}
-  static constexpr uint32_t OFF_BAR = OFF_LD + 3 * 128 * 4;
+  static constexpr int NS = 4;
+  static constexpr uint32_t OFF_QS = 2 * KT;                // NS stages of {Q, dO}
+  static constexpr uint32_t OFF_LD = OFF_QS + NS * 2 * QT;  // NS stages of {lse*log2e[64], D[64]}
+  static constexpr uint32_t OFF_BAR = OFF_LD + NS * 128 * 4;
   static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
 };
 
@@ -658,23 +658,24 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bar = (uint64_t*)(smem + L::OFF_BAR);
-  uint64_t* kv_full = bar;          // [1]
-  uint64_t* q_full = bar + 1;       // [3] TMA bytes + 32 loader lanes
-  uint64_t* q_empty = bar + 4;      // [3]
-  uint64_t* st_full = bar + 7;      // [2] S^T, dP^T in TMEM buffer
-  uint64_t* st_free = bar + 9;      // [2] buffer read (8 warps)
-  uint64_t* pt_full = bar + 11;     // P^T, dS^T in smem (8 warps)
-  uint64_t* pt_free = bar + 12;     // dV, dK products complete
-  uint64_t* dkv_done = bar + 13;
-  uint64_t* drain = bar + 14;
-  uint32_t* tmem_slot = (uint32_t*)(bar + 15);
+  constexpr int NS = L::NS;
+  uint64_t* kv_full = bar;              // [1]
+  uint64_t* q_full = bar + 1;           // [NS] TMA bytes + 32 loader lanes
+  uint64_t* q_empty = q_full + NS;      // [NS]
+  uint64_t* st_full = q_empty + NS;     // [2] S^T, dP^T in TMEM buffer
+  uint64_t* st_free = st_full + 2;      // [2] buffer read (8 warps)
+  uint64_t* pt_full = st_free + 2;      // P^T, dS^T in TMEM (8 warps)
+  uint64_t* dkv_done = pt_full + 1;
+  uint64_t* drain = dkv_done + 1;
+  uint32_t* tmem_slot = (uint32_t*)(drain + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   float* LD = (float*)(smem + L::OFF_LD);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int BG = sh.B * sh.Hkv;
-  const int kt = (int)(blockIdx.x / BG);              // key tile 0 sees the most queries: first
-  const int bg = blockIdx.x % BG, b = bg / sh.Hkv, g = bg - b * sh.Hkv;
+  const int ntk = (sh.T + 127) >> 7;
+  int kt, bg;
+  at_cta_order((int)blockIdx.x, sh.B * sh.Hkv, ntk, kt, bg);   // key tile 0 sees the most queries: first
+  const int b = bg / sh.Hkv, g = bg - b * sh.Hkv;
   const int nq = (sh.T + 63) >> 6;
   const int per = nq - 2 * kt;                        // 64-query tiles from the diagonal on
   const int n = sh.G * per;
@@ -684,9 +685,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < 3; ++s) { mbar_init(&q_full[s], 33); mbar_init(&q_empty[s], 1); }
+    for (int s = 0; s < NS; ++s) { mbar_init(&q_full[s], 33); mbar_init(&q_empty[s], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&st_full[i], 1); mbar_init(&st_free[i], 8); }
-    mbar_init(pt_full, 8); mbar_init(pt_free, 1); mbar_init(dkv_done, 1); mbar_init(drain, 1);
+    mbar_init(pt_full, 8); mbar_init(dkv_done, 1); mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_kv);
@@ -697,7 +698,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tbase = *tmem_slot;   // S^T[2] cols 0,64; dP^T[2] 128,192; dV 256..; dK 256+HD..
+  // S^T[2] cols 0,64; dP^T[2] 128,192; dV 256..; dK 256+HD.  Warp half hf reads
+  // columns [32 hf, 32 hf + 32) of S^T[buf] and overwrites them with P^T (first
+  // 16) and dS^T (next 16), bf16 pairs of its 32 queries.
+  const uint32_t tbase = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
     mbar_arrive_expect_tx(kv_full, 2 * L::KT);
@@ -708,8 +712,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
     int issued = 0;
     for (int i = 0; i < n && !*abort_flag; ++i) {
-      const int s = i % 3;
-      if (!at_wait(&q_empty[s], ((i / 3) & 1) ^ 1, sh, abort_flag)) break;
+      const int s = i % NS;
+      if (!at_wait(&q_empty[s], ((i / NS) & 1) ^ 1, sh, abort_flag)) break;
       const int h = step_h(i), q0 = step_q0(i);
       uint8_t* dst = smem + L::OFF_QS + s * 2 * L::QT;
       mbar_arrive_expect_tx(&q_full[s], 2 * L::QT);
@@ -720,15 +724,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       ++issued;
     }
     mbar_wait_bounded(kv_full, 0, sh.wait_ns);
-    for (int s = 0; s < 3; ++s) {
-      const int uses = issued / 3 + ((issued % 3) > s ? 1 : 0);
+    for (int s = 0; s < NS; ++s) {
+      const int uses = issued / NS + ((issued % NS) > s ? 1 : 0);
       if (uses > 0) mbar_wait_bounded(&q_full[s], (uses - 1) & 1, sh.wait_ns);
     }
   } else if (warp == 3) {
     // ---------------- lse / D of each query tile into the stage (every lane arrives)
     for (int i = 0; i < n && !*abort_flag; ++i) {
-      const int s = i % 3;
-      if (!at_wait_warp(&q_empty[s], ((i / 3) & 1) ^ 1, sh, abort_flag)) break;
+      const int s = i % NS;
+      if (!at_wait_warp(&q_empty[s], ((i / NS) & 1) ^ 1, sh, abort_flag)) break;
       const int h = step_h(i), q0 = step_q0(i);
       float* ld = LD + s * 128;
       const int64_t base = ((int64_t)b * sh.H + h) * sh.T;
@@ -744,10 +748,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const uint32_t id_s = at_idesc(64, 0), id_kv = at_idesc(HD, 1);
     const uint32_t sk = smem_u32(smem + L::OFF_K), sv = smem_u32(smem + L::OFF_V);
     const uint32_t sqs = smem_u32(smem + L::OFF_QS);
-    const uint32_t spt = smem_u32(smem + L::OFF_PT), sdst = smem_u32(smem + L::OFF_DST);
+    // S^T / dP^T of step i+2 reuse buffer i & 1, issued after dV_i and dK_i
+    // (which read P^T_i and dS^T_i from it): in-order execution keeps them apart.
     auto issue_st = [&](int i) -> bool {
-      const int s = i % 3, buf = i & 1;
-      if (!at_wait(&q_full[s], (i / 3) & 1, sh, abort_flag)) return false;
+      const int s = i % NS, buf = i & 1;
+      if (!at_wait(&q_full[s], (i / NS) & 1, sh, abort_flag)) return false;
       if (i >= 2 && !at_wait(&st_free[buf], ((i - 2) >> 1) & 1, sh, abort_flag)) return false;
       tc_fence_after();
       const uint32_t qb = sqs + s * 2 * L::QT, db = qb + L::QT;
@@ -767,17 +772,17 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       if (ok) ok = at_wait(pt_full, i & 1, sh, abort_flag);
       if (!ok) break;
       tc_fence_after();
-      const int s = i % 3;
+      const int s = i % NS;
       const uint32_t qb = sqs + s * 2 * L::QT, db = qb + L::QT;
+      const uint32_t pt = tbase + (i & 1) * 64;   // query slice kk: half kk/2, 8 columns per 16 queries
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc_mma_f16(tbase + 256, kdesc(spt, kk, CHUNK128), mndesc(db, kk, CHUNK64), id_kv,
-                   (i > 0 || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO
+        tc_mma_f16_ts(tbase + 256, pt + 32 * (kk >> 1) + 8 * (kk & 1), mndesc(db, kk, CHUNK64), id_kv,
+                      (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc_mma_f16(tbase + 256 + HD, kdesc(sdst, kk, CHUNK128), mndesc(qb, kk, CHUNK64), id_kv,
-                   (i > 0 || kk > 0) ? 1u : 0u);
-      tc_commit(pt_free);
+      for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
+        tc_mma_f16_ts(tbase + 256 + HD, pt + 32 * (kk >> 1) + 16 + 8 * (kk & 1), mndesc(qb, kk, CHUNK64), id_kv,
+                      (i > 0 || kk > 0) ? 1u : 0u);
       tc_commit(&q_empty[s]);
       if (*abort_flag) ok = false;
     }
@@ -789,11 +794,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int r = quarter * 32 + lane;
     const int key = kt * 128 + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t swz = r & 7;
-    const uint32_t sPT = smem_u32(smem + L::OFF_PT) + r * 128, sDST = smem_u32(smem + L::OFF_DST) + r * 128;
     bool ok = true;
     for (int i = 0; i < n; ++i) {
-      const int buf = i & 1, s = i % 3;
+      const int buf = i & 1, s = i % NS;
       if (!(ok = at_wait_warp(&st_full[buf], (i >> 1) & 1, sh, abort_flag))) break;
       tc_fence_after();
       uint32_t st[32], dp[32];
@@ -820,18 +823,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           dp[c] = __float_as_uint(p * (__uint_as_float(dp[c]) - dv[e]));
         }
       }
-      if (i > 0) {
-        if (!(ok = at_wait_warp(pt_free, (i - 1) & 1, sh, abort_flag))) break;
-      }
+      // P^T and dS^T as bf16 pairs into the columns this warp just read
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t off = ((((uint32_t)(4 * hf + u)) ^ swz) << 4);
-        const float* f = reinterpret_cast<const float*>(st + 8 * u);
-        st_shared_v4(sPT + off, pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
-        const float* d = reinterpret_cast<const float*>(dp + 8 * u);
-        st_shared_v4(sDST + off, pack2(d[0], d[1]), pack2(d[2], d[3]), pack2(d[4], d[5]), pack2(d[6], d[7]));
-      }
-      fence_proxy_async_smem();
+      for (int c = 0; c < 16; ++c) st[c] = pack2(__uint_as_float(st[2 * c]), __uint_as_float(st[2 * c + 1]));
+#pragma unroll
+      for (int c = 0; c < 16; ++c) st[16 + c] = pack2(__uint_as_float(dp[2 * c]), __uint_as_float(dp[2 * c + 1]));
+      tmem_st_32x32b_x32(tbase + lane_off + buf * 64 + 32 * hf, st);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(pt_full);
     }

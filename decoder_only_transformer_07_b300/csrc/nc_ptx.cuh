@@ -257,3 +257,16 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tma
       "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster_addr)
       : "memory");
 }
+
+// D(tmem) (+)= A(tmem) * B(smem desc), kind::f16.  A (M = 128) sits in tensor
+// memory with row m in lane m and elements k, k+1 packed in column k/2 (k
+// even in the low half); the K-slice kk of 16 starts 8 columns further.
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
