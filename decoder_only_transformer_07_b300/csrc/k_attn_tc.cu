@@ -12,7 +12,7 @@
 // Every kernel is warp-specialised, 12 warps, one CTA per SM:
 //   warp 0      TMA producer (one elected thread)
 //   warp 1      MMA issuer (one thread issues tcgen05.mma / tcgen05.commit)
-//   warp 2      allocates and frees the 512 TMEM columns
+//   warp 2      allocates and frees the 512 TMEM columns; backward: second MMA issuer
 //   warp 3      forward: second MMA issuer; dK/dV kernel: stages lse and D
 //   warps 4-11  "softmax" warps: each thread owns one TMEM lane = one row of
 //               the score tile, so row reductions need no shuffles.
@@ -456,9 +456,12 @@ struct DqSmem {
   static constexpr uint32_t TILE = 128 * HD * 2;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_DO = TILE;
-  static constexpr uint32_t OFF_K = 2 * TILE;      // 2 slots
-  static constexpr uint32_t OFF_V = 4 * TILE;      // 2 slots
-  static constexpr uint32_t OFF_BAR = 6 * TILE;
+  // K_j is held until dQ += dS K_j completes, late in step j, so its ring is one
+  // slot deeper than V's (V_j is released right after dP = dO V_j^T).
+  static constexpr int NK = 3, NV = 2;
+  static constexpr uint32_t OFF_K = 2 * TILE;               // NK slots
+  static constexpr uint32_t OFF_V = OFF_K + NK * TILE;      // NV slots
+  static constexpr uint32_t OFF_BAR = OFF_V + NV * TILE;
   static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
 };
 
@@ -471,18 +474,19 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bar = (uint64_t*)(smem + L::OFF_BAR);
-  uint64_t* qd_full = bar;         // [1]
-  uint64_t* k_full = bar + 1;      // [2]
-  uint64_t* k_empty = bar + 3;     // [2]
-  uint64_t* v_full = bar + 5;      // [2]
-  uint64_t* v_empty = bar + 7;     // [2]
-  uint64_t* sdp_full = bar + 9;    // S and dP in TMEM
-  uint64_t* sdp_free = bar + 10;   // S and dP read (8 warps)
-  uint64_t* ds_full = bar + 11;    // dS in tensor memory (8 warps)
-  uint64_t* ds_free = bar + 12;    // dQ += dS K complete
-  uint64_t* dq_done = bar + 13;
-  uint64_t* drain = bar + 14;
-  uint32_t* tmem_slot = (uint32_t*)(bar + 15);
+  constexpr int NK = L::NK, NV = L::NV;
+  uint64_t* qd_full = bar;            // [1]
+  uint64_t* k_full = qd_full + 1;     // [NK]
+  uint64_t* k_empty = k_full + NK;    // [NK]
+  uint64_t* v_full = k_empty + NK;    // [NV]
+  uint64_t* v_empty = v_full + NV;    // [NV]
+  uint64_t* sdp_full = v_empty + NV;  // S and dP in TMEM
+  uint64_t* sdp_free = sdp_full + 1;  // S and dP read (8 warps)
+  uint64_t* ds_full = sdp_free + 1;   // dS in tensor memory (8 warps)
+  uint64_t* ds_free = ds_full + 1;    // dQ += dS K complete
+  uint64_t* dq_done = ds_free + 1;
+  uint64_t* drain = dq_done + 1;      // [2] one per issuer
+  uint32_t* tmem_slot = (uint32_t*)(drain + 2);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -496,11 +500,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(qd_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1);
-    }
-    mbar_init(sdp_full, 1); mbar_init(sdp_free, 8); mbar_init(ds_full, 8); mbar_init(ds_free, 1);
-    mbar_init(dq_done, 1); mbar_init(drain, 1);
+    for (int s = 0; s < NK; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+    for (int s = 0; s < NV; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
+    mbar_init(sdp_full, 2); mbar_init(sdp_free, 8); mbar_init(ds_full, 8); mbar_init(ds_free, 1);   // S, dP: 2 issuers
+    mbar_init(dq_done, 1); mbar_init(&drain[0], 1); mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_qkv);
@@ -520,67 +523,69 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
     int k_issued = 0, v_issued = 0;
     for (int j = 0; j < n && !*abort_flag; ++j) {
-      const int s = j & 1;
-      const uint32_t par = ((j >> 1) & 1) ^ 1;
-      if (!at_wait(&k_empty[s], par, sh, abort_flag)) break;
-      mbar_arrive_expect_tx(&k_full[s], L::TILE);
+      const int sk_ = j % NK, sv_ = j % NV;
+      if (!at_wait(&k_empty[sk_], ((j / NK) & 1) ^ 1, sh, abort_flag)) break;
+      mbar_arrive_expect_tx(&k_full[sk_], L::TILE);
       for (int c = 0; c < HD / 64; ++c)
-        tma_load_2d(smem + L::OFF_K + s * L::TILE + c * CHUNK128, &tm_qkv, &k_full[s], (sh.H + g) * HD + 64 * c,
-                    row0 + j * 128);
+        tma_load_2d(smem + L::OFF_K + sk_ * L::TILE + c * CHUNK128, &tm_qkv, &k_full[sk_],
+                    (sh.H + g) * HD + 64 * c, row0 + j * 128);
       ++k_issued;
-      if (!at_wait(&v_empty[s], par, sh, abort_flag)) break;
-      mbar_arrive_expect_tx(&v_full[s], L::TILE);
+      if (!at_wait(&v_empty[sv_], ((j / NV) & 1) ^ 1, sh, abort_flag)) break;
+      mbar_arrive_expect_tx(&v_full[sv_], L::TILE);
       for (int c = 0; c < HD / 64; ++c)
-        tma_load_2d(smem + L::OFF_V + s * L::TILE + c * CHUNK128, &tm_qkv, &v_full[s],
+        tma_load_2d(smem + L::OFF_V + sv_ * L::TILE + c * CHUNK128, &tm_qkv, &v_full[sv_],
                     (sh.H + sh.Hkv + g) * HD + 64 * c, row0 + j * 128);
       ++v_issued;
     }
     mbar_wait_bounded(qd_full, 0, sh.wait_ns);
-    for (int s = 0; s < 2; ++s) {
-      const int ku = k_issued / 2 + ((k_issued % 2) > s ? 1 : 0);
-      const int vu = v_issued / 2 + ((v_issued % 2) > s ? 1 : 0);
+    for (int s = 0; s < NK; ++s) {
+      const int ku = k_issued / NK + ((k_issued % NK) > s ? 1 : 0);
       if (ku > 0) mbar_wait_bounded(&k_full[s], (ku - 1) & 1, sh.wait_ns);
+    }
+    for (int s = 0; s < NV; ++s) {
+      const int vu = v_issued / NV + ((v_issued % NV) > s ? 1 : 0);
       if (vu > 0) mbar_wait_bounded(&v_full[s], (vu - 1) & 1, sh.wait_ns);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if ((warp == 1 || warp == 2) && lane == 0) {
+    // ---------------- two MMA issuers: warp 1 issues S = Q K^T and dQ += dS K
+    // (one accumulator, one issuer); warp 2 issues dP = dO V^T.
+    const int role = warp - 1;
     const uint32_t id_s = at_idesc(128, 0), id_q = at_idesc(HD, 1);
     const uint32_t sq = smem_u32(smem + L::OFF_Q), sdo = smem_u32(smem + L::OFF_DO);
     const uint32_t sk = smem_u32(smem + L::OFF_K), sv = smem_u32(smem + L::OFF_V);
-    auto issue_sdp = [&](int j) -> bool {
-      const int s = j & 1;
-      const uint32_t par = (j >> 1) & 1;
-      if (!at_wait(&k_full[s], par, sh, abort_flag) || !at_wait(&v_full[s], par, sh, abort_flag)) return false;
+    auto issue_sdp = [&](int j) -> bool {   // role 0: S_j; role 1: dP_j
+      if (role == 0 ? !at_wait(&k_full[j % NK], (j / NK) & 1, sh, abort_flag)
+                    : !at_wait(&v_full[j % NV], (j / NV) & 1, sh, abort_flag))
+        return false;
       if (j > 0 && !at_wait(sdp_free, (j - 1) & 1, sh, abort_flag)) return false;
       tc_fence_after();
-      const uint32_t kb = sk + s * L::TILE, vb = sv + s * L::TILE;
+      const uint32_t a = role ? sdo : sq;
+      const uint32_t b = role ? sv + (j % NV) * L::TILE : sk + (j % NK) * L::TILE;
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk)
-        tc_mma_f16(tbase, kdesc(sq, kk, CHUNK128), kdesc(kb, kk, CHUNK128), id_s, kk > 0 ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
-        tc_mma_f16(tbase + 128, kdesc(sdo, kk, CHUNK128), kdesc(vb, kk, CHUNK128), id_s, kk > 0 ? 1u : 0u);
+        tc_mma_f16(tbase + role * 128, kdesc(a, kk, CHUNK128), kdesc(b, kk, CHUNK128), id_s, kk > 0 ? 1u : 0u);
       tc_commit(sdp_full);
-      tc_commit(&v_empty[s]);
+      if (role) tc_commit(&v_empty[j % NV]);
       return true;
     };
     bool ok = at_wait(qd_full, 0, sh, abort_flag) && issue_sdp(0);
     for (int j = 0; ok && j < n; ++j) {
       if (j + 1 < n) ok = issue_sdp(j + 1);
-      if (ok) ok = at_wait(ds_full, j & 1, sh, abort_flag);
-      if (!ok) break;
+      if (!ok || role) continue;
+      if (!(ok = at_wait(ds_full, j & 1, sh, abort_flag))) break;
       tc_fence_after();
-      const uint32_t kb = sk + (j & 1) * L::TILE;
+      const uint32_t kb = sk + (j % NK) * L::TILE;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)   // dQ += dS K_j, dS from tensor memory
         tc_mma_f16_ts(tbase + 256, tbase + 384 + 8 * kk, mndesc(kb, kk, CHUNK128), id_q,
                       (j > 0 || kk > 0) ? 1u : 0u);
       tc_commit(ds_free);
-      tc_commit(&k_empty[j & 1]);
+      tc_commit(&k_empty[j % NK]);
       if (*abort_flag) ok = false;
     }
-    if (ok) tc_commit(dq_done);
-    tc_commit(drain);
-    mbar_wait_bounded(drain, 0, sh.wait_ns);
+    if (ok && role == 0) tc_commit(dq_done);
+    tc_commit(&drain[role]);
+    mbar_wait_bounded(&drain[role], 0, sh.wait_ns);
   } else if (warp >= 4) {
     const int quarter = warp & 3, hf = (warp - 4) >> 2;   // hf: key columns [64 hf, 64 hf + 64)
     const int r = quarter * 32 + lane;
@@ -665,9 +670,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint64_t* st_full = q_empty + NS;     // [2] S^T, dP^T in TMEM buffer
   uint64_t* st_free = st_full + 2;      // [2] buffer read (8 warps)
   uint64_t* pt_full = st_free + 2;      // P^T, dS^T in TMEM (8 warps)
-  uint64_t* dkv_done = pt_full + 1;
-  uint64_t* drain = dkv_done + 1;
-  uint32_t* tmem_slot = (uint32_t*)(drain + 1);
+  uint64_t* dkv_done = pt_full + 1;     // both issuers' products complete
+  uint64_t* drain = dkv_done + 1;       // [2] one per issuer
+  uint32_t* tmem_slot = (uint32_t*)(drain + 2);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   float* LD = (float*)(smem + L::OFF_LD);
 
@@ -685,9 +690,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < NS; ++s) { mbar_init(&q_full[s], 33); mbar_init(&q_empty[s], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&st_full[i], 1); mbar_init(&st_free[i], 8); }
-    mbar_init(pt_full, 8); mbar_init(dkv_done, 1); mbar_init(drain, 1);
+    // stages are released, buffers filled and the step finished by both issuers
+    for (int s = 0; s < NS; ++s) { mbar_init(&q_full[s], 33); mbar_init(&q_empty[s], 2); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&st_full[i], 2); mbar_init(&st_free[i], 8); mbar_init(&drain[i], 1); }
+    mbar_init(pt_full, 8); mbar_init(dkv_done, 2);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_kv);
@@ -744,24 +750,26 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       }
       mbar_arrive(&q_full[s]);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if ((warp == 1 || warp == 2) && lane == 0) {
+    // ---------------- two MMA issuers (a single thread issues about one MMA per
+    // ~100 cycles, more than these N <= 128 products take):
+    //   warp 1: S^T = K Q^T  and  dV += P^T dO
+    //   warp 2: dP^T = V dO^T and dK += dS^T Q
+    // S^T / dP^T of step i+2 reuse buffer i & 1; each issuer issues them after
+    // its own dV_i / dK_i, which read P^T_i / dS^T_i from that buffer.
+    const int role = warp - 1;
     const uint32_t id_s = at_idesc(64, 0), id_kv = at_idesc(HD, 1);
-    const uint32_t sk = smem_u32(smem + L::OFF_K), sv = smem_u32(smem + L::OFF_V);
+    const uint32_t a_op = smem_u32(smem + (role ? L::OFF_V : L::OFF_K));
     const uint32_t sqs = smem_u32(smem + L::OFF_QS);
-    // S^T / dP^T of step i+2 reuse buffer i & 1, issued after dV_i and dK_i
-    // (which read P^T_i and dS^T_i from it): in-order execution keeps them apart.
     auto issue_st = [&](int i) -> bool {
       const int s = i % NS, buf = i & 1;
       if (!at_wait(&q_full[s], (i / NS) & 1, sh, abort_flag)) return false;
       if (i >= 2 && !at_wait(&st_free[buf], ((i - 2) >> 1) & 1, sh, abort_flag)) return false;
       tc_fence_after();
-      const uint32_t qb = sqs + s * 2 * L::QT, db = qb + L::QT;
+      const uint32_t bop = sqs + s * 2 * L::QT + (role ? L::QT : 0u);   // Q (S^T) or dO (dP^T)
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk)
-        tc_mma_f16(tbase + buf * 64, kdesc(sk, kk, CHUNK128), kdesc(qb, kk, CHUNK64), id_s, kk > 0 ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
-        tc_mma_f16(tbase + 128 + buf * 64, kdesc(sv, kk, CHUNK128), kdesc(db, kk, CHUNK64), id_s,
+        tc_mma_f16(tbase + role * 128 + buf * 64, kdesc(a_op, kk, CHUNK128), kdesc(bop, kk, CHUNK64), id_s,
                    kk > 0 ? 1u : 0u);
       tc_commit(&st_full[buf]);
       return true;
@@ -773,22 +781,18 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const int s = i % NS;
-      const uint32_t qb = sqs + s * 2 * L::QT, db = qb + L::QT;
-      const uint32_t pt = tbase + (i & 1) * 64;   // query slice kk: half kk/2, 8 columns per 16 queries
+      const uint32_t bop = sqs + s * 2 * L::QT + (role ? 0u : L::QT);    // dO (dV) or Q (dK)
+      const uint32_t pt = tbase + (i & 1) * 64 + role * 16;   // P^T or dS^T; query slice kk at 32 (kk/2) + 8 (kk%2)
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO
-        tc_mma_f16_ts(tbase + 256, pt + 32 * (kk >> 1) + 8 * (kk & 1), mndesc(db, kk, CHUNK64), id_kv,
-                      (i > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
-        tc_mma_f16_ts(tbase + 256 + HD, pt + 32 * (kk >> 1) + 16 + 8 * (kk & 1), mndesc(qb, kk, CHUNK64), id_kv,
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_f16_ts(tbase + 256 + role * HD, pt + 32 * (kk >> 1) + 8 * (kk & 1), mndesc(bop, kk, CHUNK64), id_kv,
                       (i > 0 || kk > 0) ? 1u : 0u);
       tc_commit(&q_empty[s]);
       if (*abort_flag) ok = false;
     }
     if (ok) tc_commit(dkv_done);
-    tc_commit(drain);
-    mbar_wait_bounded(drain, 0, sh.wait_ns);
+    tc_commit(&drain[role]);
+    mbar_wait_bounded(&drain[role], 0, sh.wait_ns);
   } else if (warp >= 4) {
     const int quarter = warp & 3, hf = (warp - 4) >> 2;   // hf: query columns [32 hf, 32 hf + 32)
     const int r = quarter * 32 + lane;
