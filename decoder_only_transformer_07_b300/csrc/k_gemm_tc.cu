@@ -623,14 +623,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // [128 r, 128 r + 128) of the A tile and rows [128 r, 128 r + 128) of the B
 // tile; one thread of rank 0 issues M = 256, N = 256 MMAs that read both
 // CTAs' shared memory, and each CTA's tensor memory holds its 128 rows of the
-// accumulator.  Per SM this stages 32 KB per 64-deep k-block instead of 48 KB
-// for the same multiply-adds as the single-CTA 128 x 256 tile.  Ring slots are
+// accumulator.  Per SM this stages 32 KB per 64 of depth instead of 48 KB for
+// the same multiply-adds as the single-CTA 128 x 256 tile.  A ring slot holds
+// two 64-column (128 B) swizzled chunks along K: K-major [2][128 rows][128 B],
+// MN-major [2][2 mn-chunks][64 k-rows][128 B].  Ring slots are
 // released (and accumulators published) to both CTAs by multicast commits;
 // both CTAs' epilogue warps release an accumulator on rank 0's barrier.
 struct Tc2Cfg {
-  static constexpr int STAGES = 6;
-  static constexpr int A_BYTES = TC_BM * TC_BK * 2;         // 16 KB: this CTA's 128 rows of A
-  static constexpr int B_BYTES = 128 * TC_BK * 2;           // 16 KB: this CTA's half of B
+  // 128-deep k-blocks: eight MMAs per ring slot, so the issuing thread's per-slot
+  // wait / commit / loop overhead is spread over twice the work of a 64-deep slot.
+  static constexpr int BK = 128;
+  static constexpr int STAGES = 3;
+  static constexpr int A_BYTES = TC_BM * BK * 2;            // 32 KB: this CTA's 128 rows of A
+  static constexpr int B_BYTES = 128 * BK * 2;              // 32 KB: this CTA's half of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = 512;                     // two 256-column accumulators
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
@@ -704,18 +709,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         uint8_t* sb = sa + Cfg::A_BYTES;
         const uint32_t fb = full_rank0 + stage * 8;
         if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * Cfg::STAGE_BYTES);
-        const int k0 = kb * TC_BK;
-        if (!p.a_mn) {
-          tma_load_2d_pair(sa, &tmA, fb, k0, arow);
-        } else {
-          tma_load_2d_pair(sa, &tmA, fb, arow, k0);
-          tma_load_2d_pair(sa + 8192, &tmA, fb, arow + 64, k0);
-        }
-        if (!p.b_mn) {
-          tma_load_2d_pair(sb, &tmB, fb, k0, brow);
-        } else {
-          tma_load_2d_pair(sb, &tmB, fb, brow, k0);
-          tma_load_2d_pair(sb + 8192, &tmB, fb, brow + 64, k0);
+        const int k0 = kb * Cfg::BK;
+#pragma unroll
+        for (int kc = 0; kc < 2; ++kc) {
+          if (!p.a_mn) {
+            tma_load_2d_pair(sa + kc * 16384, &tmA, fb, k0 + 64 * kc, arow);
+          } else {
+            tma_load_2d_pair(sa + kc * 16384, &tmA, fb, arow, k0 + 64 * kc);
+            tma_load_2d_pair(sa + kc * 16384 + 8192, &tmA, fb, arow + 64, k0 + 64 * kc);
+          }
+          if (!p.b_mn) {
+            tma_load_2d_pair(sb + kc * 16384, &tmB, fb, k0 + 64 * kc, brow);
+          } else {
+            tma_load_2d_pair(sb + kc * 16384, &tmB, fb, brow, k0 + 64 * kc);
+            tma_load_2d_pair(sb + kc * 16384 + 8192, &tmB, fb, brow + 64, k0 + 64 * kc);
+          }
         }
         if (++stage == S) { stage = 0; phase ^= 1; }
       }
@@ -742,9 +750,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         const uint32_t sa = smem_u32(smem + stage * Cfg::STAGE_BYTES);
         const uint32_t sb = sa + Cfg::A_BYTES;
 #pragma unroll
-        for (int k = 0; k < TC_BK / 16; ++k)
-          tc_mma_f16_pair(d_tmem, operand_desc(sa, p.a_mn, k), operand_desc(sb, p.b_mn, k), idesc,
-                          (kb > sg.k0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < Cfg::BK / 16; ++k)   // k-chunk k/4 sits 16 KB further
+          tc_mma_f16_pair(d_tmem, operand_desc(sa + (k >> 2) * 16384, p.a_mn, k & 3),
+                          operand_desc(sb + (k >> 2) * 16384, p.b_mn, k & 3), idesc, (kb > sg.k0 || k > 0) ? 1u : 0u);
         tc_commit_pair(&empty_bar[stage], 0x3);
         if (++stage == S) { stage = 0; phase ^= 1; }
       }
@@ -933,6 +941,7 @@ static nc_status launch_tc_pair(TcParams p, const CUtensorMap& ta, const CUtenso
     }
     max_clusters = std::min(n, g_num_sms / 2);
   }
+  p.num_kb = (p.K + Tc2Cfg::BK - 1) / Tc2Cfg::BK;
   p.splits = 1;
   p.kps = p.num_kb;
   const int tiles = p.tiles_m * p.tiles_n;
