@@ -241,20 +241,23 @@ __device__ __forceinline__ uint32_t stg_off(int r, int u) {
 // TMA reduce-add for the fp32 accumulate - as whole lines.  The relu^2
 // backward's aux input arrives in the same box by TMA load and is replaced in
 // place by the result.  Returns false if a bounded wait expired.
+// `ep` is the epilogue kind (p.ep, or NC_EP_STORE_F32 for a split-K partial);
+// columns n_base.. of the box row m0 in tmD's coordinates, clipped at n_lim.
 template <int BN>
-__device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, const CUtensorMap* tmD, const CUtensorMap* tmAux,
-                                                   uint8_t* stg, uint64_t* aux_bar, uint32_t& aux_phase,
-                                                   uint32_t taddr, int n_base, int m0, int lane) {
-  const bool f32o = (p.ep == NC_EP_STORE_F32 || p.ep == NC_EP_ACCUM_F32);
-  const bool aux_in = (p.ep == NC_EP_RELU2_BWD || p.ep == NC_EP_RELU2_SQ_BWD);
-  const bool sq_bwd = (p.ep == NC_EP_RELU2_SQ_BWD);
+__device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, int ep, const CUtensorMap* tmD,
+                                                   const CUtensorMap* tmAux, uint8_t* stg, uint64_t* aux_bar,
+                                                   uint32_t& aux_phase, uint32_t taddr, int n_base, int n_lim, int m0,
+                                                   int lane) {
+  const bool f32o = (ep == NC_EP_STORE_F32 || ep == NC_EP_ACCUM_F32);
+  const bool aux_in = (ep == NC_EP_RELU2_BWD || ep == NC_EP_RELU2_SQ_BWD);
+  const bool sq_bwd = (ep == NC_EP_RELU2_SQ_BWD);
   const int cc = f32o ? 32 : 64;
   const uint32_t sa = smem_u32(stg);
   const int r = lane;
 #pragma unroll 1
   for (int oc = 0; oc < BN / 2; oc += cc) {
     const int n_out = n_base + oc;
-    if (n_out >= p.N) break;
+    if (n_out >= n_lim) break;
     // first accumulator piece into registers before the wait: the TMEM read
     // overlaps the previous store still reading the box
     uint32_t v[32];
@@ -287,10 +290,10 @@ __device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, const CUte
           float f[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[8 * k + e]);
-          if (p.ep == NC_EP_RELU2 || p.ep == NC_EP_RELU2_SQ) {
+          if (ep == NC_EP_RELU2 || ep == NC_EP_RELU2_SQ) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = fmaxf(f[e], 0.f);
-            if (p.ep == NC_EP_RELU2_SQ) {
+            if (ep == NC_EP_RELU2_SQ) {
 #pragma unroll
               for (int e = 0; e < 8; ++e) f[e] *= f[e];
             }
@@ -311,11 +314,11 @@ __device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, const CUte
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      if (p.ep == NC_EP_ACCUM_F32) tma_reduce_add_2d(tmD, stg, n_out, m0);
+      if (ep == NC_EP_ACCUM_F32) tma_reduce_add_2d(tmD, stg, n_out, m0);
       else tma_store_2d(tmD, stg, n_out, m0);
       bulk_commit();
     }
-    if (p.ep == NC_EP_RELU2) {   // second output: aux = relu(acc)^2
+    if (ep == NC_EP_RELU2) {   // second output: aux = relu(acc)^2
       if (lane == 0) bulk_wait_read();
       __syncwarp();
 #pragma unroll 1
@@ -566,8 +569,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       } else if (p.ep == NC_EP_QKV_ROPE) {
         tc_epilogue_qkv_rope_staged(p, &tmD, stg, taddr + c_lo, tn * BN + c_lo, BN / 2, m0, m, lane);
       } else if (p.tma_epi && !part) {
-        if (!tc_epilogue_staged<BN>(p, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
-                                    tn * BN + c_lo, m0, lane)) {
+        if (!tc_epilogue_staged<BN>(p, p.ep, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
+                                    tn * BN + c_lo, p.N, m0, lane)) {
           fail();
           break;
         }
@@ -782,11 +785,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
       if (m0 >= p.M) {
         // all 32 rows of this warp are past the end: nothing to store
+      } else if (p.splits > 1) {
+        // split-K slice: this CTA's 128 x 256 fp32 partial into the workspace
+        // ws[s][t][256][256] (tensor map tmAux), summed in slice order afterwards
+        const int wrow = (sg.s * (p.tiles_m * p.tiles_n) + sg.t) * 256 + (int)rank * 128 + quarter * 32;
+        if (!tc_epilogue_staged<BN>(p, NC_EP_STORE_F32, &tmAux, &tmAux, stg, &aux_bar[warp - 4], aux_phase,
+                                    taddr + c_lo, c_lo, BN, wrow, lane)) {
+          fail();
+          break;
+        }
       } else if (p.ep == NC_EP_QKV_ROPE) {
         tc_epilogue_qkv_rope_staged(p, &tmD, stg, taddr + c_lo, tn * BN + c_lo, BN / 2, m0, m, lane);
       } else if (p.tma_epi) {
-        if (!tc_epilogue_staged<BN>(p, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
-                                    tn * BN + c_lo, m0, lane)) {
+        if (!tc_epilogue_staged<BN>(p, p.ep, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
+                                    tn * BN + c_lo, p.N, m0, lane)) {
           fail();
           break;
         }
@@ -814,20 +826,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 
 // Split-K fix-up: out (op)= sum over slices s = 0..splits-1, in that order
 // (bitwise reproducible), of the fp32 partial tiles.  One block per tile.
-template <int BN>
+template <int BM, int BN>
 __global__ void __launch_bounds__(256) k_gemm_tc_fixup(TcParams p) {
   const int t = blockIdx.x;
   const int tiles = p.tiles_m * p.tiles_n;
   int tm, tn;
   tile_coords(p, t, tm, tn);
-  for (int i = threadIdx.x; i < TC_BM * BN / 4; i += blockDim.x) {
+  for (int i = threadIdx.x; i < BM * BN / 4; i += blockDim.x) {
     const int r = (i * 4) / BN, cc = (i * 4) % BN;
-    const int64_t m = (int64_t)tm * TC_BM + r;
+    const int64_t m = (int64_t)tm * BM + r;
     const int n = tn * BN + cc;
     if (m >= p.M || n >= p.N) continue;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int sl = 0; sl < p.splits; ++sl) {
-      const float4 v = *reinterpret_cast<const float4*>(p.ws + ((size_t)sl * tiles + t) * TC_BM * BN +
+      const float4 v = *reinterpret_cast<const float4*>(p.ws + ((size_t)sl * tiles + t) * BM * BN +
                                                         (size_t)r * BN + cc);
       acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
@@ -909,7 +921,7 @@ static nc_status launch_tc_bn(TcParams p, const CUtensorMap& ta, const CUtensorM
   kern<<<grid, TC_THREADS, TcCfg<BN>::SMEM, st>>>(ta, tb, td, tx, p);
   NC_CUDA_TRY(cudaGetLastError());
   if (p.splits > 1) {
-    k_gemm_tc_fixup<BN><<<tiles, 256, 0, st>>>(p);
+    k_gemm_tc_fixup<TC_BM, BN><<<tiles, 256, 0, st>>>(p);
     NC_CUDA_TRY(cudaGetLastError());
   }
   return NC_OK;
@@ -919,7 +931,7 @@ int g_gemm_pair = 1;       // CTA-pair kernel for eligible shapes (test hook can
 
 // 256 x 256 tiles on CTA pairs: persistent grid of co-resident clusters.
 static nc_status launch_tc_pair(TcParams p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
-                                const CUtensorMap& tx, cudaStream_t st) {
+                                const CUtensorMap& tx, size_t ws_bytes, cudaStream_t st) {
   static int max_clusters = 0;
   if (!max_clusters) {
     NC_CUDA_TRY(cudaFuncSetAttribute(k_gemm_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Tc2Cfg::SMEM));
@@ -945,9 +957,41 @@ static nc_status launch_tc_pair(TcParams p, const CUtensorMap& ta, const CUtenso
   p.splits = 1;
   p.kps = p.num_kb;
   const int tiles = p.tiles_m * p.tiles_n;
-  const int grid = 2 * std::min(tiles, max_clusters);
-  k_gemm_tc2<<<grid, TC_THREADS, Tc2Cfg::SMEM, st>>>(ta, tb, td, tx, p);
-  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+  // Split K when whole 256 x 256 tiles would leave the last wave of clusters
+  // badly filled (fp32 outputs only: the weight gradients, whose K is the token
+  // count).  Cost per split count S: waves(S) * (k-blocks per slice) * t_kb plus
+  // the partial tiles' write and read.
+  const bool f32_out = (p.ep == NC_EP_STORE_F32 || p.ep == NC_EP_ACCUM_F32);
+  if (f32_out && p.ws && tiles < 4 * max_clusters) {
+    const double t_kb = 0.9e-6;                                 // s per 256 x 256 x 128 block, one pair
+    const double tile_bytes = 2.0 * 256 * 256 * sizeof(float);  // write + read of one partial
+    double best = 1e30;
+    int kps_best = p.num_kb;
+    for (int S = 1; S <= 16; ++S) {
+      const int kps = (p.num_kb + S - 1) / S;
+      if (S > 1 && (kps < 8 || (size_t)S * tiles * 256 * 256 * sizeof(float) > ws_bytes)) break;
+      const int waves = (tiles * S + max_clusters - 1) / max_clusters;
+      const double cost = waves * kps * t_kb + (S > 1 ? S * tiles * tile_bytes / 6.0e12 : 0.0);
+      if (cost < best * 0.98) { best = cost; kps_best = kps; }
+    }
+    p.kps = kps_best;
+    p.splits = (p.num_kb + p.kps - 1) / p.kps;
+  }
+  CUtensorMap tw = tx;
+  if (p.splits > 1) {
+    // partial tiles ws[s][t][256][256] as one fp32 matrix of 256 columns
+    if (!make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.ws, 256, (uint64_t)p.splits * tiles * 256, 256, 32,
+                      32))
+      return NC_ERR_CUDA;
+  }
+  const int grid = 2 * std::min(tiles * p.splits, max_clusters);
+  k_gemm_tc2<<<grid, TC_THREADS, Tc2Cfg::SMEM, st>>>(ta, tb, td, tw, p);
+  NC_CUDA_TRY(cudaGetLastError());
+  if (p.splits > 1) {
+    k_gemm_tc_fixup<256, 256><<<tiles, 256, 0, st>>>(p);
+    NC_CUDA_TRY(cudaGetLastError());
+  }
+  return NC_OK;
 }
 
 // Split-K partials: up to 4 waves of 128 x 256 fp32 tiles per slice set.
@@ -1000,11 +1044,10 @@ static nc_status gemm_tc_impl(int M, int N, int K, const bf16* A, int64_t lda, i
     return NC_ERR_ARG;
   }
   if (ws && (((uintptr_t)ws) & 15)) return NC_ERR_ARG;
-  // CTA pairs (256 x 256 tiles) unless the single-CTA kernel would split K
-  // (few output tiles with an fp32 output: the weight gradients)
+  // CTA pairs (256 x 256 tiles, split-K for few-tile fp32 outputs) whenever N > 128
+  // and M >= 256; the single-CTA kernel otherwise
   const bool f32_out = (ep == NC_EP_STORE_F32 || ep == NC_EP_ACCUM_F32);
-  const bool would_split = f32_out && ws && p.tiles_m * p.tiles_n < 4 * g_num_sms;
-  const bool pair = g_gemm_pair && BN == 256 && M >= 256 && !would_split;
+  const bool pair = g_gemm_pair && BN == 256 && M >= 256;
   if (pair) p.tiles_m = (M + 255) / 256;
   CUtensorMap ta, tb;
   bool ok;
@@ -1024,7 +1067,7 @@ static nc_status gemm_tc_impl(int M, int N, int K, const bf16* A, int64_t lda, i
   if (p.tma_epi && (ep == NC_EP_RELU2 || ep == NC_EP_RELU2_BWD || ep == NC_EP_RELU2_SQ_BWD))
     p.tma_epi = make_tmap_bf16_2d(&tx, aux, N, M, ldaux, 64, 32);
   if (ep == NC_EP_QKV_ROPE && !p.tma_epi) return NC_ERR_ARG;
-  if (pair) return launch_tc_pair(p, ta, tb, td, tx, st);
+  if (pair) return launch_tc_pair(p, ta, tb, td, tx, ws_bytes, st);
   if (BN == 256) return launch_tc_bn<256>(p, ta, tb, td, tx, ws_bytes, st);
   return launch_tc_bn<128>(p, ta, tb, td, tx, ws_bytes, st);
 }
