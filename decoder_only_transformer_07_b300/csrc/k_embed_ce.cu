@@ -5,6 +5,7 @@
 // (cosmicrealm "noao-chat-0-项目总体介绍" §2.1 item 3); the loss is next-token
 // cross-entropy (devpress "用不到100美元，亲手训练一个属于你的GPT-2" §2.2 item 2).
 #include "nc_kernels.cuh"
+#include "nc_ptx.cuh"
 
 // ---------------------------------------------------------------- gather
 // One warp per token row: x[i] = float(round_act(wte[tokens[i]])).  An id
@@ -273,8 +274,8 @@ __global__ void __launch_bounds__(512) k_cross_entropy(int V, T* __restrict__ z,
 
 // bf16 rows with V % 8 == 0 and V <= 512 * 8 * CE_VEC: the row is read once
 // into registers (16-byte loads), reduced, and dz written from registers.
-#define CE_THREADS 512
-#define CE_VEC 16
+#define CE_THREADS 1024
+#define CE_VEC 8
 __global__ void __launch_bounds__(CE_THREADS) k_cross_entropy_bf16(int V, bf16* __restrict__ z, int64_t ldz,
                                                                    const int32_t* __restrict__ targets,
                                                                    float* __restrict__ row_loss, float scale,
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(CE_THREADS) k_cross_entropy_bf16(int V, bf16* 
     if (i < nv) {
       const bf16* e = reinterpret_cast<const bf16*>(&v[k]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) sum += exp2f(__bfloat162float(e[j]) * L2E - mb);
+      for (int j = 0; j < 8; ++j) sum += ex2_approx(fmaf(__bfloat162float(e[j]), L2E, -mb));
     }
   }
   sum = block_sum(sum, sh);
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(CE_THREADS) k_cross_entropy_bf16(int V, bf16* 
       float p[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        p[j] = exp2f(__bfloat162float(e[j]) * L2E - mb) * inv;
+        p[j] = ex2_approx(fmaf(__bfloat162float(e[j]), L2E, -mb)) * inv;
         if (i * 8 + j == tgt) p[j] -= scale;
       }
       uint4 o;
