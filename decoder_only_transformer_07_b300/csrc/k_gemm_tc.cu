@@ -181,13 +181,13 @@ __device__ __forceinline__ void tc_epilogue_row(const TcParams& p, int64_t m, in
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float x = __bfloat162float(h[j]);
-          v[i + j] *= 2.f * (sq ? sqrtf(x) : x);
+          v[i + j] *= 2.f * (sq ? sqrt_approx(x) : x);
         }
       }
     } else {
       for (int i = 0; i < 32; ++i) {
         const float x = (n0 + i < p.N) ? __bfloat162float(a[i]) : 0.f;
-        v[i] = (n0 + i < p.N) ? v[i] * 2.f * (sq ? sqrtf(x) : x) : 0.f;
+        v[i] = (n0 + i < p.N) ? v[i] * 2.f * (sq ? sqrt_approx(x) : x) : 0.f;
       }
     }
   }
@@ -303,7 +303,7 @@ __device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, int ep, co
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const float x = __bfloat162float(h[e]);
-              f[e] *= 2.f * (sq_bwd ? sqrtf(x) : x);
+              f[e] *= 2.f * (sq_bwd ? sqrt_approx(x) : x);
             }
           }
           const uint4 o = pack8_bf16(f);
