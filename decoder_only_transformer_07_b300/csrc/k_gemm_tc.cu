@@ -826,14 +826,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 
 // Split-K fix-up: out (op)= sum over slices s = 0..splits-1, in that order
 // (bitwise reproducible), of the fp32 partial tiles.  One block per tile.
+// One block per 32-row slab of a tile (BM / 32 blocks per tile), so that
+// the few tiles of a weight-gradient GEMM still spread over every SM.
 template <int BM, int BN>
 __global__ void __launch_bounds__(256) k_gemm_tc_fixup(TcParams p) {
-  const int t = blockIdx.x;
+  constexpr int RB = 32;
+  const int t = blockIdx.x / (BM / RB), rb = blockIdx.x % (BM / RB);
   const int tiles = p.tiles_m * p.tiles_n;
   int tm, tn;
   tile_coords(p, t, tm, tn);
-  for (int i = threadIdx.x; i < BM * BN / 4; i += blockDim.x) {
-    const int r = (i * 4) / BN, cc = (i * 4) % BN;
+  for (int i = threadIdx.x; i < RB * BN / 4; i += blockDim.x) {
+    const int r = rb * RB + (i * 4) / BN, cc = (i * 4) % BN;
     const int64_t m = (int64_t)tm * BM + r;
     const int n = tn * BN + cc;
     if (m >= p.M || n >= p.N) continue;
@@ -921,7 +924,7 @@ static nc_status launch_tc_bn(TcParams p, const CUtensorMap& ta, const CUtensorM
   kern<<<grid, TC_THREADS, TcCfg<BN>::SMEM, st>>>(ta, tb, td, tx, p);
   NC_CUDA_TRY(cudaGetLastError());
   if (p.splits > 1) {
-    k_gemm_tc_fixup<TC_BM, BN><<<tiles, 256, 0, st>>>(p);
+    k_gemm_tc_fixup<TC_BM, BN><<<tiles * (TC_BM / 32), 256, 0, st>>>(p);
     NC_CUDA_TRY(cudaGetLastError());
   }
   return NC_OK;
@@ -988,7 +991,7 @@ static nc_status launch_tc_pair(TcParams p, const CUtensorMap& ta, const CUtenso
   k_gemm_tc2<<<grid, TC_THREADS, Tc2Cfg::SMEM, st>>>(ta, tb, td, tw, p);
   NC_CUDA_TRY(cudaGetLastError());
   if (p.splits > 1) {
-    k_gemm_tc_fixup<256, 256><<<tiles, 256, 0, st>>>(p);
+    k_gemm_tc_fixup<256, 256><<<tiles * (256 / 32), 256, 0, st>>>(p);
     NC_CUDA_TRY(cudaGetLastError());
   }
   return NC_OK;
