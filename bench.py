@@ -47,7 +47,7 @@ DESCR = {
 # DRAM traffic per GEMM call (main kernel + split-K fix-up), from the ncu capture of a
 # full step summarised in profiles/launches_d20_step.md; set to None when the GEMM
 # kernels change and the capture is not repeated.
-GEMM_DRAM_BYTES_PER_CALL = {"d20": 1190e6}
+GEMM_DRAM_BYTES_PER_CALL = {"d20": 1258e6}
 # CPU-oracle sample (tokens of one sequence) per workload: ~10-30 s of fp64 work
 CPU_SAMPLE_T = {"tiny": 64, "d12": 128, "d20": 64, "d26": 48, "d24gqa": 48}
 
