@@ -67,7 +67,9 @@ _SIGS = {
     "nc_op_rmsnorm_bwd": (_i32, [_i32, _i64, _i32, _p, _p, _p, _p, _p, _p]),
     "nc_op_rope_table": (_i32, [_i32, _i32, _f32, _p, _p]),
     "nc_op_rope_qknorm_fwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _f32, _p]),
-    "nc_op_gemm_qkv_rope": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _i64, _p, _p, _i64, _p, _p, _f32, _p]),
+    "nc_op_gemm_qkv_rope": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _i64, _p, _p, _i64, _p, _p, _i32, _f32,
+                                   _p]),
+    "nc_op_rope_table_pairs": (_i32, [_i32, _i32, _f32, _p, _p]),
     "nc_op_rope_qknorm_bwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_op_attention_fwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p]),
     "nc_op_attention_bwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p, _p, _p]),
@@ -265,11 +267,15 @@ class ops:
                                           eps, _stream()), "nc_op_rope_qknorm_fwd")
 
     @staticmethod
-    def gemm_qkv_rope(x, wqkv, qkv, T, H, Hkv, hd, rstd, table, eps):
+    def gemm_qkv_rope(x, wqkv, qkv, T, H, Hkv, hd, rstd, table, eps, pair_rows=0):
         M, K = x.shape
         _check(_lib.nc_op_gemm_qkv_rope(M, K, T, H, Hkv, hd, _ptr(x), x.stride(0), _ptr(wqkv), _ptr(qkv),
-                                        qkv.stride(0), _ptr(rstd), _ptr(table), eps, _stream()),
+                                        qkv.stride(0), _ptr(rstd), _ptr(table), pair_rows, eps, _stream()),
                "nc_op_gemm_qkv_rope")
+
+    @staticmethod
+    def rope_table_pairs(T, hd, base, pairs):
+        _check(_lib.nc_op_rope_table_pairs(T, hd, base, _ptr(pairs), _stream()), "nc_op_rope_table_pairs")
 
     @staticmethod
     def rope_qknorm_bwd(dqkv, qkv, B, T, H, Hkv, hd, rstd, table):

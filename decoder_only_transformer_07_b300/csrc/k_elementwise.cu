@@ -67,21 +67,33 @@ nc_status launch_cast_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t 
 }
 
 // ---------------------------------------------------------------- RoPE table
-__global__ void k_rope_table(float* __restrict__ tab, int T, int hd, double base) {
+// cos / sin of t * base^(-2i/hd) in fp64, rounded to float.  `tab` is
+// [T][hd/2][2]; `pairs` (optional, hd % 4 == 0) holds the same numbers
+// pair-major, [hd/4][T][4] = (cos_i, sin_i, cos_i+1, sin_i+1) for even i, so
+// that 32 threads handling 32 consecutive positions read 512 contiguous bytes.
+__global__ void k_rope_table(float* __restrict__ tab, float* __restrict__ pairs, int T, int hd, double base) {
   const int d = hd / 2;
   int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= T * d) return;
   int t = idx / d, i = idx % d;
   double omega = pow(base, -2.0 * (double)i / (double)hd);
   double th = (double)t * omega;
-  tab[2 * idx] = (float)cos(th);
-  tab[2 * idx + 1] = (float)sin(th);
+  const float c = (float)cos(th), sn = (float)sin(th);
+  if (tab) {
+    tab[2 * idx] = c;
+    tab[2 * idx + 1] = sn;
+  }
+  if (pairs) {
+    float* q = pairs + ((size_t)(i >> 1) * T + t) * 4 + (i & 1) * 2;
+    q[0] = c;
+    q[1] = sn;
+  }
 }
 
-nc_status launch_rope_table(int T, int hd, float base, float* tab, cudaStream_t st) {
-  if (T <= 0 || hd <= 0 || (hd & 1) || !tab) return NC_ERR_ARG;
+nc_status launch_rope_table(int T, int hd, float base, float* tab, float* pairs, cudaStream_t st) {
+  if (T <= 0 || hd <= 0 || (hd & 1) || (!tab && !pairs) || (pairs && (hd & 3))) return NC_ERR_ARG;
   int n = T * (hd / 2);
-  k_rope_table<<<cdiv(n, 256), 256, 0, st>>>(tab, T, hd, (double)base);
+  k_rope_table<<<cdiv(n, 256), 256, 0, st>>>(tab, pairs, T, hd, (double)base);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 

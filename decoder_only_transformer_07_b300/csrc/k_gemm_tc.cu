@@ -58,6 +58,7 @@ struct TcParams {
   const float* rope_tab;
   float* rstd_qk;
   int rope_T, rope_nh, rope_hd;
+  int rope_pair_rows;      // 0: table [T][hd/2][2]; > 0: pair-major [hd/4][rope_pair_rows][4]
   float rope_eps;
 };
 
@@ -355,7 +356,12 @@ __device__ __forceinline__ void tc_epilogue_qkv_rope_staged(const TcParams& p, c
   const uint32_t sa = smem_u32(stg);
   const int r = lane;
   const bool row_ok = m < p.M;
-  const float4* cs = reinterpret_cast<const float4*>(p.rope_tab + (size_t)(m % p.rope_T) * hd);
+  // float4 (cos_i, sin_i, cos_i+1, sin_i+1) of pair i (even) at this row's position: element
+  // (i / 2) * cs_step of cs (pair-major table: consecutive rows are consecutive in memory)
+  const int pos = (int)(m % p.rope_T);
+  const float4* cs = reinterpret_cast<const float4*>(p.rope_tab) +
+                     (p.rope_pair_rows ? (size_t)pos : (size_t)pos * (hd / 4));
+  const size_t cs_step = p.rope_pair_rows ? (size_t)p.rope_pair_rows : 1;
 #pragma unroll 1
   for (int hc = 0; hc < ncols; hc += hd) {
     const int n0 = n_base + hc;
@@ -399,7 +405,7 @@ __device__ __forceinline__ void tc_epilogue_qkv_rope_staged(const TcParams& p, c
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float4 q = __ldg(cs + ((i0 + e) >> 1));   // cos_i, sin_i, cos_i+1, sin_i+1
+            const float4 q = __ldg(cs + ((i0 + e) >> 1) * cs_step);   // cos_i, sin_i, cos_i+1, sin_i+1
             const float a0 = __uint_as_float(a[e]), a1 = __uint_as_float(a[e + 1]);
             const float b0 = __uint_as_float(b[e]), b1 = __uint_as_float(b[e + 1]);
             y[e] = (first ? (a0 * q.x + b0 * q.y) : (-a0 * q.y + b0 * q.x)) * rs;
@@ -1003,7 +1009,7 @@ size_t gemm_tc_workspace_bytes() { return (size_t)256 << 20; }
 struct TcRope {
   const float* tab;
   float* rstd;
-  int T, nh, hd;
+  int T, nh, hd, pair_rows;
   float eps;
 };
 
@@ -1034,15 +1040,17 @@ static nc_status gemm_tc_impl(int M, int N, int K, const bf16* A, int64_t lda, i
   p.ws = (float*)ws;
   p.splits = 1;
   p.kps = 0;
-  p.rope_tab = nullptr; p.rstd_qk = nullptr; p.rope_T = 1; p.rope_nh = 0; p.rope_hd = 0; p.rope_eps = 0.f;
+  p.rope_tab = nullptr; p.rstd_qk = nullptr; p.rope_T = 1; p.rope_nh = 0; p.rope_hd = 0; p.rope_pair_rows = 0;
+  p.rope_eps = 0.f;
   if (rope) {
     // whole heads in each epilogue warp's 128 columns, 16-byte row segments
     if (ep != NC_EP_QKV_ROPE || BN != 256 || (rope->hd != 64 && rope->hd != 128) || (N % rope->hd) ||
         rope->nh * rope->hd > N || rope->T <= 0 || (ldd % 8) || (((uintptr_t)D) & 15) ||
         (((uintptr_t)rope->tab) & 15) || !rope->rstd)
       return NC_ERR_ARG;
+    if (rope->pair_rows < 0 || (rope->pair_rows > 0 && rope->pair_rows < rope->T)) return NC_ERR_ARG;
     p.rope_tab = rope->tab; p.rstd_qk = rope->rstd; p.rope_T = rope->T; p.rope_nh = rope->nh;
-    p.rope_hd = rope->hd; p.rope_eps = rope->eps;
+    p.rope_hd = rope->hd; p.rope_pair_rows = rope->pair_rows; p.rope_eps = rope->eps;
   } else if (ep == NC_EP_QKV_ROPE) {
     return NC_ERR_ARG;
   }
@@ -1084,9 +1092,9 @@ nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_
 }
 
 nc_status launch_gemm_tc_qkv_rope(int M, int N, int K, const bf16* A, int64_t lda, const bf16* Wqkv, int64_t ldb,
-                                  bf16* qkv, int64_t ldd, int T, int nh, int hd, const float* tab, float* rstd,
-                                  float eps, int32_t* err, cudaStream_t st) {
-  TcRope r{tab, rstd, T, nh, hd, eps};
+                                  bf16* qkv, int64_t ldd, int T, int nh, int hd, const float* tab, int pair_rows,
+                                  float* rstd, float eps, int32_t* err, cudaStream_t st) {
+  TcRope r{tab, rstd, T, nh, hd, pair_rows, eps};
   if (N <= 128) return NC_ERR_UNSUPPORTED;
   return gemm_tc_impl(M, N, K, A, lda, 1, Wqkv, ldb, 1, NC_EP_QKV_ROPE, qkv, ldd, nullptr, 0, &r, err, nullptr, 0,
                       st);

@@ -34,6 +34,7 @@ struct nc_model {
   float* master = nullptr;           // fp32 [P]
   void* wact = nullptr;              // compute-dtype weights [P] (== master in fp32 mode)
   float* rope_tab = nullptr;         // [Tmax, hd/2, 2]
+  float* rope_pairs = nullptr;       // the same, pair-major [hd/4, Tmax, 4] (bf16 QKV GEMM epilogue)
   int32_t* err = nullptr;            // device error flag
   float* result = nullptr;           // device: [0] loss, [1] error flag copy
   float* result_host = nullptr;      // pinned host copy
@@ -243,6 +244,7 @@ static nc_status allocate(nc_model* m) {
   if (m->dtype == NC_BF16) NC_TRY(dalloc(m, (size_t)m->P * 2, &m->wact));
   else m->wact = m->master;
   NC_TRY(dalloc_t(m, (size_t)m->Tmax * m->hd, &m->rope_tab));
+  if (m->hd % 4 == 0) NC_TRY(dalloc_t(m, (size_t)m->Tmax * m->hd, &m->rope_pairs));
   NC_TRY(dalloc_t(m, 4, &m->err));
   NC_TRY(dalloc_t(m, 4, &m->result));
   if (cudaMallocHost((void**)&m->result_host, 16) != cudaSuccess) { cudaGetLastError(); return NC_ERR_ALLOC; }
@@ -331,7 +333,7 @@ extern "C" nc_status nc_model_create(const nc_config* cfg, uint64_t seed, nc_mod
       s = launch_init_normal(m->master + t.off, t.rows * t.cols, seed, (int)j, c.init_std, st);
     }
   }
-  if (s == NC_OK) s = launch_rope_table(m->Tmax, m->hd, c.rope_base, m->rope_tab, st);
+  if (s == NC_OK) s = launch_rope_table(m->Tmax, m->hd, c.rope_base, m->rope_tab, m->rope_pairs, st);
   if (s == NC_OK && cudaMemsetAsync(m->err, 0, sizeof(int32_t), st) != cudaSuccess) s = NC_ERR_CUDA;
   if (s == NC_OK && cudaStreamSynchronize(st) != cudaSuccess) s = NC_ERR_CUDA;
   if (s != NC_OK) {
@@ -437,7 +439,8 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
       // q/k/v projection with RoPE and the q/k RMSNorm in the GEMM epilogue
       PROF_SUB(NC_PROF_GEMM, NC_PROF_GEMM_FWD, 2.0 * N * W * C, ((double)N * C + (double)W * C + (double)N * W) * a,
                launch_gemm_tc_qkv_rope((int)N, W, C, (const bf16*)xn1, C, (const bf16*)wptr(m, tensor(m, l, 0)), C,
-                                       (bf16*)qkv, W, T, nh, m->hd, m->rope_tab, rstdqk, eps, m->err, st));
+                                       (bf16*)qkv, W, T, nh, m->hd, m->rope_pairs ? m->rope_pairs : m->rope_tab,
+                                       m->rope_pairs ? m->Tmax : 0, rstdqk, eps, m->err, st));
       m->launches += 1;
     } else {
       NC_TRY(gemm(m, NC_PROF_GEMM_FWD, (int)N, W, C, xn1, C, 1, wptr(m, tensor(m, l, 0)), C, 1, NC_EP_STORE, qkv, W,
@@ -632,7 +635,11 @@ extern "C" nc_status nc_op_rmsnorm_bwd(int32_t dtype, int64_t rows, int32_t C, c
 }
 
 extern "C" nc_status nc_op_rope_table(int32_t T, int32_t hd, float rope_base, float* cos_sin, void* stream) {
-  return launch_rope_table(T, hd, rope_base, cos_sin, as_stream(stream));
+  return launch_rope_table(T, hd, rope_base, cos_sin, nullptr, as_stream(stream));
+}
+
+extern "C" nc_status nc_op_rope_table_pairs(int32_t T, int32_t hd, float rope_base, float* pairs, void* stream) {
+  return launch_rope_table(T, hd, rope_base, nullptr, pairs, as_stream(stream));
 }
 
 extern "C" nc_status nc_op_rope_qknorm_fwd(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
@@ -643,12 +650,13 @@ extern "C" nc_status nc_op_rope_qknorm_fwd(int32_t dtype, int32_t B, int32_t T, 
 
 extern "C" nc_status nc_op_gemm_qkv_rope(int32_t M, int32_t K, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
                                          const void* x, int64_t ldx, const void* wqkv, void* qkv, int64_t ldqkv,
-                                         float* rstd, const float* cos_sin, float eps, void* stream) {
+                                         float* rstd, const float* cos_sin, int32_t pair_rows, float eps,
+                                         void* stream) {
   if (!x || !wqkv || !qkv || !rstd || !cos_sin || M < 0 || K <= 0 || T <= 0 || H <= 0 || Hkv <= 0 || H % Hkv)
     return NC_ERR_ARG;
   const int N = (H + 2 * Hkv) * hd;
   return launch_gemm_tc_qkv_rope(M, N, K, (const bf16*)x, ldx, (const bf16*)wqkv, K, (bf16*)qkv, ldqkv, T, H + Hkv,
-                                 hd, cos_sin, rstd, eps, nullptr, as_stream(stream));
+                                 hd, cos_sin, pair_rows, rstd, eps, nullptr, as_stream(stream));
 }
 
 extern "C" nc_status nc_op_rope_qknorm_bwd(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t hd,

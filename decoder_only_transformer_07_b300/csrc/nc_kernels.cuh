@@ -7,7 +7,8 @@
 nc_status launch_init_normal(float* out, int64_t count, uint64_t seed, int tensor_index, float std,
                              cudaStream_t st);
 nc_status launch_cast_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t st);
-nc_status launch_rope_table(int T, int hd, float base, float* tab, cudaStream_t st);
+// tab [T][hd/2][2] and/or pairs [hd/4][T][4] (pair-major copy); either may be NULL.
+nc_status launch_rope_table(int T, int hd, float base, float* tab, float* pairs, cudaStream_t st);
 
 nc_status launch_rmsnorm_fwd(int dtype, int64_t rows, int C, const float* x, void* y, float* rstd,
                              float eps, cudaStream_t st);
@@ -45,9 +46,11 @@ size_t gemm_tc_workspace_bytes();
 // of the first nh heads (q and k) applied in the epilogue (rstd [M, nh] fp32);
 // the remaining heads (v) are stored as computed.  Rows are positions m % T.
 // NC_ERR_UNSUPPORTED for N <= 128; hd 64 or 128.
+// tab: [T][hd/2][2] (pair_rows = 0) or pair-major [hd/4][pair_rows][4] with
+// pair_rows >= T (the coalesced layout the epilogue prefers).
 nc_status launch_gemm_tc_qkv_rope(int M, int N, int K, const bf16* A, int64_t lda, const bf16* Wqkv, int64_t ldb,
-                                  bf16* qkv, int64_t ldd, int T, int nh, int hd, const float* tab, float* rstd,
-                                  float eps, int32_t* err, cudaStream_t st);
+                                  bf16* qkv, int64_t ldd, int T, int nh, int hd, const float* tab, int pair_rows,
+                                  float* rstd, float eps, int32_t* err, cudaStream_t st);
 
 nc_status launch_attn_fwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv, void* o,
                                float* lse, cudaStream_t st);

@@ -197,6 +197,9 @@ nc_status nc_op_rope_table(int32_t T, int32_t hd, float rope_base, float* cos_si
 /* In place on qkv (dtype [B*T, (H+2*Hkv)*hd]): RoPE on the H query and Hkv key
  * heads at position t = row % T, then RMSNorm of each of those head vectors;
  * rstd (float [B*T, H+Hkv]).  cos_sin from nc_op_rope_table with >= T rows. */
+/* The same numbers as nc_op_rope_table, pair-major: pairs (float [hd/4, T, 4])
+ * holds (cos_i, sin_i, cos_i+1, sin_i+1) for even i at each position.  hd % 4 == 0. */
+nc_status nc_op_rope_table_pairs(int32_t T, int32_t hd, float rope_base, float* pairs, void* stream);
 nc_status nc_op_rope_qknorm_fwd(int32_t dtype, int32_t B, int32_t T, int32_t H,
                                 int32_t Hkv, int32_t hd, void* qkv, float* rstd,
                                 const float* cos_sin, float eps, void* stream);
@@ -205,14 +208,16 @@ nc_status nc_op_rope_qknorm_fwd(int32_t dtype, int32_t B, int32_t T, int32_t H,
  * leading dimension ldx) times Wqkv^T (bf16 [(H+2*Hkv)*hd, K]), then for the
  * first H+Hkv heads of every row the rotary embedding at position row % T
  * followed by the per-head RMSNorm, computed from the fp32 accumulator; v is
- * stored as computed.  rstd (float [M, H+Hkv]).  The rotation preserves the
+ * stored as computed.  rstd (float [M, H+Hkv]).  cos_sin is the table of
+ * nc_op_rope_table (pair_rows = 0) or of nc_op_rope_table_pairs built for
+ * pair_rows >= T positions (faster: the epilogue's reads coalesce).  The rotation preserves the
  * sum of squares, so rstd is taken before rotating (cosmicrealm
  * "noao-chat-0-项目总体介绍" §2.1 items 1-2).  hd 64 or 128, (H+2*Hkv)*hd > 128,
  * 16-byte aligned buffers; NC_ERR_ARG / NC_ERR_UNSUPPORTED otherwise. */
 nc_status nc_op_gemm_qkv_rope(int32_t M, int32_t K, int32_t T, int32_t H, int32_t Hkv,
                               int32_t hd, const void* x, int64_t ldx, const void* wqkv,
                               void* qkv, int64_t ldqkv, float* rstd, const float* cos_sin,
-                              float eps, void* stream);
+                              int32_t pair_rows, float eps, void* stream);
 /* In place on dqkv: the backward of the above, given the saved (normalised)
  * qkv and rstd. */
 nc_status nc_op_rope_qknorm_bwd(int32_t dtype, int32_t B, int32_t T, int32_t H,

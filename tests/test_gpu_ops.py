@@ -204,8 +204,9 @@ def test_rope_qknorm_fwd_bwd(hd, dt):
     assert ok, worst
 
 
+@pytest.mark.parametrize("pairs", [False, True])
 @pytest.mark.parametrize("hd,H,Hkv", [(64, 4, 2), (128, 3, 1), (128, 2, 2)])
-def test_gemm_qkv_rope_fused(hd, H, Hkv):
+def test_gemm_qkv_rope_fused(hd, H, Hkv, pairs):
     """The q/k/v projection with RoPE + per-head RMSNorm in its epilogue, against
     gemm -> rope -> rms_norm of the oracle on the same bf16 inputs."""
     B, T, K, eps, base = 2, 100, 192, 1.1920929e-07, 10000.0
@@ -216,7 +217,14 @@ def test_gemm_qkv_rope_fused(hd, H, Hkv):
     nc.ops.rope_table(T, hd, base, tab)
     QKV = torch.full((M, W), float("nan"), dtype=BF16, device="cuda")
     R = torch.empty((M, H + Hkv), dtype=F32, device="cuda")
-    nc.ops.gemm_qkv_rope(X, Wq, QKV, T, H, Hkv, hd, R, tab, eps)
+    if pairs:   # pair-major table built for more positions than T (row stride 160)
+        tabp = torch.empty((hd // 4, 160, 4), dtype=F32, device="cuda")
+        nc.ops.rope_table_pairs(160, hd, base, tabp)
+        torch.cuda.synchronize()
+        assert torch.equal(tabp[:, :T].reshape(hd // 4, T, 2, 2).permute(1, 0, 2, 3).reshape(T, hd // 2, 2), tab)
+        nc.ops.gemm_qkv_rope(X, Wq, QKV, T, H, Hkv, hd, R, tabp, eps, pair_rows=160)
+    else:
+        nc.ops.gemm_qkv_rope(X, Wq, QKV, T, H, Hkv, hd, R, tab, eps)
     torch.cuda.synchronize()
     u = OO.gemm(to64(X), to64(Wq)).reshape(B, T, H + 2 * Hkv, hd)
     cos, sin = OM.rope_tables(T, hd, base)
