@@ -228,6 +228,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         continue;
       }
       if (!(ok = kv_ready(cK))) break;
+      // Tile 1 runs half a step behind tile 0: its S is issued once tile 0's S of
+      // the same key tile has completed, so the tensor core computes it while tile
+      // 0's softmax runs (and tile 0's O += P V and next S during tile 1's softmax)
+      // instead of both softmaxes running at once with the tensor core idle.
+      if (i == 1 && j < n0 && !(ok = at_wait(&s_full[0], j & 1, sh, abort_flag))) break;
       tc_fence_after();
       const uint32_t kb = skv + (cK % NS) * L::TILE;
 #pragma unroll
@@ -485,8 +490,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint64_t* ds_full = sdp_free + 1;   // dS in tensor memory (8 warps)
   uint64_t* ds_free = ds_full + 1;    // dQ += dS K complete
   uint64_t* dq_done = ds_free + 1;
-  uint64_t* drain = dq_done + 1;      // [2] one per issuer
-  uint32_t* tmem_slot = (uint32_t*)(drain + 2);
+  uint64_t* drain = dq_done + 1;      // [3] one per issuer
+  uint32_t* tmem_slot = (uint32_t*)(drain + 3);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -503,7 +508,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     for (int s = 0; s < NK; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
     for (int s = 0; s < NV; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
     mbar_init(sdp_full, 2); mbar_init(sdp_free, 8); mbar_init(ds_full, 8); mbar_init(ds_free, 1);   // S, dP: 2 issuers
-    mbar_init(dq_done, 1); mbar_init(&drain[0], 1); mbar_init(&drain[1], 1);
+    mbar_init(dq_done, 1);
+    for (int r = 0; r < 3; ++r) mbar_init(&drain[r], 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_qkv);
@@ -546,44 +552,47 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       const int vu = v_issued / NV + ((v_issued % NV) > s ? 1 : 0);
       if (vu > 0) mbar_wait_bounded(&v_full[s], (vu - 1) & 1, sh.wait_ns);
     }
-  } else if ((warp == 1 || warp == 2) && lane == 0) {
-    // ---------------- two MMA issuers: warp 1 issues S = Q K^T and dQ += dS K
-    // (one accumulator, one issuer); warp 2 issues dP = dO V^T.
+  } else if ((warp == 1 || warp == 2 || warp == 3) && lane == 0) {
+    // ---------------- three MMA issuers (one thread issues about one MMA per ~100
+    // cycles): warp 1 S = Q K^T, warp 2 dP = dO V^T, warp 3 dQ += dS K (one
+    // accumulator, one issuer).  S_{j+1} / dP_{j+1} overlap the softmax of step j
+    // and dQ_j overlaps S_{j+2} / dP_{j+2}.
     const int role = warp - 1;
     const uint32_t id_s = at_idesc(128, 0), id_q = at_idesc(HD, 1);
     const uint32_t sq = smem_u32(smem + L::OFF_Q), sdo = smem_u32(smem + L::OFF_DO);
     const uint32_t sk = smem_u32(smem + L::OFF_K), sv = smem_u32(smem + L::OFF_V);
-    auto issue_sdp = [&](int j) -> bool {   // role 0: S_j; role 1: dP_j
-      if (role == 0 ? !at_wait(&k_full[j % NK], (j / NK) & 1, sh, abort_flag)
-                    : !at_wait(&v_full[j % NV], (j / NV) & 1, sh, abort_flag))
-        return false;
-      if (j > 0 && !at_wait(sdp_free, (j - 1) & 1, sh, abort_flag)) return false;
-      tc_fence_after();
-      const uint32_t a = role ? sdo : sq;
-      const uint32_t b = role ? sv + (j % NV) * L::TILE : sk + (j % NK) * L::TILE;
+    bool ok = at_wait(qd_full, 0, sh, abort_flag);
+    if (role < 2) {
+      for (int j = 0; ok && j < n; ++j) {   // role 0: S_j; role 1: dP_j
+        if (role == 0 ? !(ok = at_wait(&k_full[j % NK], (j / NK) & 1, sh, abort_flag))
+                      : !(ok = at_wait(&v_full[j % NV], (j / NV) & 1, sh, abort_flag)))
+          break;
+        if (j > 0 && !(ok = at_wait(sdp_free, (j - 1) & 1, sh, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t a = role ? sdo : sq;
+        const uint32_t b = role ? sv + (j % NV) * L::TILE : sk + (j % NK) * L::TILE;
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
-        tc_mma_f16(tbase + role * 128, kdesc(a, kk, CHUNK128), kdesc(b, kk, CHUNK128), id_s, kk > 0 ? 1u : 0u);
-      tc_commit(sdp_full);
-      if (role) tc_commit(&v_empty[j % NV]);
-      return true;
-    };
-    bool ok = at_wait(qd_full, 0, sh, abort_flag) && issue_sdp(0);
-    for (int j = 0; ok && j < n; ++j) {
-      if (j + 1 < n) ok = issue_sdp(j + 1);
-      if (!ok || role) continue;
-      if (!(ok = at_wait(ds_full, j & 1, sh, abort_flag))) break;
-      tc_fence_after();
-      const uint32_t kb = sk + (j % NK) * L::TILE;
+        for (int kk = 0; kk < HD / 16; ++kk)
+          tc_mma_f16(tbase + role * 128, kdesc(a, kk, CHUNK128), kdesc(b, kk, CHUNK128), id_s, kk > 0 ? 1u : 0u);
+        tc_commit(sdp_full);
+        if (role) tc_commit(&v_empty[j % NV]);
+        if (*abort_flag) ok = false;
+      }
+    } else {
+      for (int j = 0; ok && j < n; ++j) {   // dQ += dS_j K_j, dS from tensor memory
+        if (!(ok = at_wait(ds_full, j & 1, sh, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t kb = sk + (j % NK) * L::TILE;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)   // dQ += dS K_j, dS from tensor memory
-        tc_mma_f16_ts(tbase + 256, tbase + 384 + 8 * kk, mndesc(kb, kk, CHUNK128), id_q,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-      tc_commit(ds_free);
-      tc_commit(&k_empty[j % NK]);
-      if (*abort_flag) ok = false;
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16_ts(tbase + 256, tbase + 384 + 8 * kk, mndesc(kb, kk, CHUNK128), id_q,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(ds_free);
+        tc_commit(&k_empty[j % NK]);
+        if (*abort_flag) ok = false;
+      }
+      if (ok) tc_commit(dq_done);
     }
-    if (ok && role == 0) tc_commit(dq_done);
     tc_commit(&drain[role]);
     mbar_wait_bounded(&drain[role], 0, sh.wait_ns);
   } else if (warp >= 4) {
