@@ -11,31 +11,36 @@
 //
 // Every kernel is warp-specialised, 12 warps, one CTA per SM:
 //   warp 0      TMA producer (one elected thread)
-//   warp 1      MMA issuer (one thread issues tcgen05.mma / tcgen05.commit)
-//   warp 2      allocates and frees the 512 TMEM columns; backward: second MMA issuer
-//   warp 3      forward: second MMA issuer; dK/dV kernel: stages lse and D
+//   warps 1-3   MMA issuers (one thread each issues tcgen05.mma / tcgen05.commit;
+//               a single thread issues only about one MMA per ~100 cycles, so
+//               independent product chains get their own issuer); warp 2 also
+//               allocates and frees the 512 TMEM columns; in the dK/dV kernel
+//               warp 3 stages lse and D instead
 //   warps 4-11  "softmax" warps: each thread owns one TMEM lane = one row of
 //               the score tile, so row reductions need no shuffles.
 //
-// Forward: a CTA takes 256 queries (two 128-row tiles i = 0, 1) of one
-//   (b, h) and streams the 128-key K and V tiles through a 3-slot ring.  Per
-//   key tile j the tensor core computes S_i = Q_i K_j^T into TMEM; warpgroup
-//   i turns its row of S_i into P = exp2(S * log2e/sqrt(hd) - m), writes P as
-//   bf16 into shared memory and the tensor core accumulates O_i += P V_j in
-//   TMEM.  The two tiles ping-pong: the tensor core works on one tile's
-//   matrix products while the other's warpgroup does its softmax.  The
+// Forward: a CTA takes 256 queries (two 128-row tiles i = 0, 1, issuers warps 1
+//   and 3) of one (b, h) and streams the 128-key K and V tiles through a 4-slot
+//   ring.  Per key tile j the tensor core computes S_i = Q_i K_j^T into TMEM;
+//   warpgroup i turns its row of S_i into P = exp2(S * log2e/sqrt(hd) - m),
+//   writes P as bf16 over the first 64 columns of S_i, and the tensor core
+//   accumulates O_i += P V_j with P read from TMEM.  Tile 1 runs half a step
+//   behind tile 0, so one tile's products overlap the other's softmax.  The
 //   running max m is raised only when a row's new maximum exceeds it by more
 //   than 8 (log2 units), in which case the warp rescales its rows of O in
 //   TMEM; otherwise P <= 2^8, which bf16 and fp32 hold exactly enough.
 // Backward (deterministic, no atomics), with P recomputed from lse:
 //   dQ kernel    per 128-query tile, over key tiles 0..diagonal:
-//                S = Q K^T, dP = dO V^T (TMEM), dS = P (dP - D) (bf16, smem),
-//                dQ += dS K (TMEM);
+//                S = Q K^T (warp 1), dP = dO V^T (warp 2) into TMEM,
+//                dS = P (dP - D) as bf16 into TMEM, dQ += dS K (warp 3);
 //   dK/dV kernel per 128-key tile, over the group's query heads and the
-//                64-query tiles from the diagonal on: S^T = K Q^T,
-//                dP^T = V dO^T (double-buffered in TMEM), P^T and dS^T (bf16,
-//                smem), dV += P^T dO, dK += dS^T Q (TMEM).
+//                64-query tiles from the diagonal on: S^T = K Q^T (warp 1),
+//                dP^T = V dO^T (warp 2), double-buffered in TMEM; P^T and dS^T
+//                as bf16 over their own product's columns; dV += P^T dO
+//                (warp 1), dK += dS^T Q (warp 2).
 // The 1/sqrt(hd) of dQ and dK is applied to the fp32 accumulators on output.
+// A TMEM region is only ever overwritten by the issuer whose earlier product
+// reads it, or by softmax warps after a barrier that follows that read.
 //
 // Every mbarrier wait is bounded in time (the GEMM's limit): on expiry the
 // kernel raises the timeout bit of the error flag, stops issuing work, drains
@@ -103,6 +108,23 @@ __device__ __forceinline__ bool at_wait_warp(uint64_t* bar, uint32_t parity, con
   return __all_sync(0xffffffffu, ok);
 }
 
+// Bounded wait for a shared-memory counter written by another warp to reach
+// `target` (counters only grow, so there is no phase to alias).
+__device__ __forceinline__ bool at_wait_count(volatile int* cnt, int target, const AtShape& sh,
+                                              volatile int* abort_flag) {
+  if (*cnt >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (*cnt >= target) return true;
+    if (*abort_flag) return false;
+    if ((it & 255u) == 0 && globaltimer_ns() - t0 > sh.wait_ns) {
+      if (sh.err) atomicOr(sh.err, NC_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
@@ -150,6 +172,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint64_t* drain = pv_done + 2;      // [2] one per issuer
   uint32_t* tmem_slot = (uint32_t*)(drain + 2);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  volatile int* s0_seen = abort_flag + 1;   // key tiles whose S_0 tile 0's softmax has seen
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = (sh.T + 255) >> 8;
@@ -171,6 +194,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1); mbar_init(&drain[i], 1);
     }
     *abort_flag = 0;
+    *s0_seen = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_qkv);
   }
@@ -231,8 +255,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       // Tile 1 runs half a step behind tile 0: its S is issued once tile 0's S of
       // the same key tile has completed, so the tensor core computes it while tile
       // 0's softmax runs (and tile 0's O += P V and next S during tile 1's softmax)
-      // instead of both softmaxes running at once with the tensor core idle.
-      if (i == 1 && j < n0 && !(ok = at_wait(&s_full[0], j & 1, sh, abort_flag))) break;
+      // instead of both softmaxes running at once with the tensor core idle.  The
+      // signal is a count, not s_full[0]'s phase parity, which would alias if
+      // tile 0 were ever two key tiles ahead.
+      if (i == 1 && j < n0 && !(ok = at_wait_count(s0_seen, j + 1, sh, abort_flag))) break;
       tc_fence_after();
       const uint32_t kb = skv + (cK % NS) * L::TILE;
 #pragma unroll
@@ -268,6 +294,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       if (!(ok = at_wait_warp(&s_full[i], j & 1, sh, abort_flag))) break;
+      if (i == 0 && quarter == 0 && lane == 0) *s0_seen = j + 1;
       tc_fence_after();
       uint32_t x[128];
 #pragma unroll
@@ -714,8 +741,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   // S^T[2] cols 0,64; dP^T[2] 128,192; dV 256..; dK 256+HD.  Warp half hf reads
-  // columns [32 hf, 32 hf + 32) of S^T[buf] and overwrites them with P^T (first
-  // 16) and dS^T (next 16), bf16 pairs of its 32 queries.
+  // columns [32 hf, 32 hf + 32) of S^T[buf] and of dP^T[buf] and overwrites the
+  // first 16 of them with P^T and dS^T respectively, bf16 pairs of its 32
+  // queries.  Each product buffer is thus only ever written by the issuer that
+  // reads it back (warp 1: S^T, then dV += P^T dO; warp 2: dP^T, then dK +=
+  // dS^T Q), and in-order execution per issuer orders that read before the
+  // buffer's next S^T / dP^T.  (Were dS^T kept in the S^T columns, warp 1's
+  // S^T of step i+2 could overwrite it before warp 2's dK of step i read it.)
   const uint32_t tbase = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
@@ -764,8 +796,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     // ~100 cycles, more than these N <= 128 products take):
     //   warp 1: S^T = K Q^T  and  dV += P^T dO
     //   warp 2: dP^T = V dO^T and dK += dS^T Q
-    // S^T / dP^T of step i+2 reuse buffer i & 1; each issuer issues them after
-    // its own dV_i / dK_i, which read P^T_i / dS^T_i from that buffer.
+    // S^T / dP^T of step i+2 reuse buffer i & 1; each issuer issues its product
+    // after its own dV_i / dK_i, which read P^T_i / dS^T_i from the columns that
+    // product overwrites.
     const int role = warp - 1;
     const uint32_t id_s = at_idesc(64, 0), id_kv = at_idesc(HD, 1);
     const uint32_t a_op = smem_u32(smem + (role ? L::OFF_V : L::OFF_K));
@@ -791,7 +824,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       tc_fence_after();
       const int s = i % NS;
       const uint32_t bop = sqs + s * 2 * L::QT + (role ? 0u : L::QT);    // dO (dV) or Q (dK)
-      const uint32_t pt = tbase + (i & 1) * 64 + role * 16;   // P^T or dS^T; query slice kk at 32 (kk/2) + 8 (kk%2)
+      // P^T (in S^T's columns) or dS^T (in dP^T's); query slice kk at 32 (kk/2) + 8 (kk%2)
+      const uint32_t pt = tbase + role * 128 + (i & 1) * 64;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         tc_mma_f16_ts(tbase + 256 + role * HD, pt + 32 * (kk >> 1) + 8 * (kk & 1), mndesc(bop, kk, CHUNK64), id_kv,
@@ -836,12 +870,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           dp[c] = __float_as_uint(p * (__uint_as_float(dp[c]) - dv[e]));
         }
       }
-      // P^T and dS^T as bf16 pairs into the columns this warp just read
+      // P^T and dS^T as bf16 pairs into the S^T and dP^T columns this warp just read
 #pragma unroll
       for (int c = 0; c < 16; ++c) st[c] = pack2(__uint_as_float(st[2 * c]), __uint_as_float(st[2 * c + 1]));
 #pragma unroll
-      for (int c = 0; c < 16; ++c) st[16 + c] = pack2(__uint_as_float(dp[2 * c]), __uint_as_float(dp[2 * c + 1]));
-      tmem_st_32x32b_x32(tbase + lane_off + buf * 64 + 32 * hf, st);
+      for (int c = 0; c < 16; ++c) dp[c] = pack2(__uint_as_float(dp[2 * c]), __uint_as_float(dp[2 * c + 1]));
+      tmem_st_32x32b_x16(tbase + lane_off + buf * 64 + 32 * hf, st);
+      tmem_st_32x32b_x16(tbase + lane_off + 128 + buf * 64 + 32 * hf, dp);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();

@@ -1,0 +1,157 @@
+"""Parity at the full sizes of the four bf16 workloads (d12, d20, d26, d24 GQA).
+
+The fp64 oracle cannot run a whole 65k-token step of these models, so the
+checks split as the sizes allow:
+
+* full size, in the launch configuration the benchmark times (batch x seq_len
+  of the workload): per-position losses of sampled sequences against the
+  oracle on those sequences' first positions (causal attention makes a
+  position's loss depend only on the tokens up to it), and properties that hold
+  at any size - a deterministic step, finite gradients, the embedding rows of
+  token ids absent from the batch exactly zero, the step's loss equal to the
+  mean of the per-position losses;
+* full widths, depth and vocabulary on one short sequence: the loss within
+  2e-2 and every gradient tensor at cosine >= 0.999 against the oracle.
+
+Weights are N(0, 0.02) float32 from NumPy's seeded generator, set on the GPU
+with nc_set_params; tokens are the workload's seeded Zipf stream.
+"""
+import numpy as np
+import pytest
+
+import synthetic as S
+from oracle import model as OM
+from tests.gpu_util import cosine
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import decoder_only_transformer_07_b300 as nc  # noqa: E402
+
+FULL = ["d12", "d20", "d26", "d24gqa"]
+SAMPLE_T = 64
+
+
+@pytest.fixture(scope="module", params=FULL)
+def full(request):
+    w = S.workload(request.param)
+    cfg = OM.Config.from_workload(w)
+    params = np.random.default_rng(1234).standard_normal(OM.n_params(cfg), dtype=np.float32)
+    params *= np.float32(cfg.init_std)
+    m = nc.Model(nc.config_from_workload(w), seed=S.WEIGHT_SEED)
+    m.set_params(torch.from_numpy(params))
+    yield w, cfg, params, m
+    m.close()
+
+
+def test_full_size_step(full):
+    w, cfg, params, m = full
+    tok, tgt = S.batch_tokens(w)                        # [batch, seq_len]: the benchmark's launch
+    T_, G_ = torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda()
+    rl = m.row_losses(T_, G_).cpu().numpy().astype(np.float64).reshape(w.batch, w.seq_len)
+    loss1, g1 = m.forward_backward(T_, G_)
+    g1 = g1.cpu()
+    loss2, g2 = m.forward_backward(T_, G_)
+    assert loss1 == loss2 and torch.equal(g1, g2.cpu()), "step not deterministic"
+    g = g1.numpy()
+    assert np.all(np.isfinite(g)) and np.isfinite(loss1)
+    assert abs(loss1 - rl.mean()) <= 1e-5 * abs(rl.mean()) + 1e-6
+    # rows of wte for ids absent from the batch receive exactly zero gradient
+    V, C = w.vocab, w.n_embd
+    dwte = g[:V * C].reshape(V, C)
+    present = np.zeros(V, dtype=bool)
+    present[tok.reshape(-1)] = True
+    assert np.all(dwte[~present] == 0.0) and np.all(np.abs(dwte[present]).max(axis=1) > 0)
+    # sampled outputs: the first SAMPLE_T positions of the first and last sequence
+    rows = [0, w.batch - 1]
+    want = OM.row_losses(cfg, params.astype(np.float64), tok[rows, :SAMPLE_T], tgt[rows, :SAMPLE_T])
+    for i, b in enumerate(rows):
+        got = rl[b, :SAMPLE_T]
+        assert abs(got.mean() - want[i].mean()) <= 2e-2, (b, got.mean(), want[i].mean())
+        assert np.max(np.abs(got - want[i])) <= 0.1, (b, np.max(np.abs(got - want[i])))
+
+
+def test_full_widths_short_sequence_gradients(full):
+    w, cfg, params, m = full
+    tok, tgt = S.batch_tokens(w, batch=1, seq_len=SAMPLE_T)
+    loss, g = m.forward_backward(torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda())
+    loss_ref, G = OM.forward_backward(cfg, params.astype(np.float64), tok, tgt)
+    assert abs(loss - loss_ref) <= 2e-2, (loss, loss_ref)
+    g = g.cpu().numpy().astype(np.float64)
+    g_ref = OM.pack(cfg, G)
+    for name, r, c, off in m.layout:
+        assert cosine(g[off:off + r * c], g_ref[off:off + r * c]) >= 0.999, name
+
+
+def _attn_oracle_group(y, do, rstd, b, g, T, H, Hkv, hd, cos, sin):
+    """Oracle outputs for batch row b, kv head g and its query heads, at the
+    full sequence length: o, lse per query head; dq, dk through the RMSNorm
+    and rotation backward; dv."""
+    G = H // Hkv
+    x = y[b].astype(np.float64)                       # [T, H + 2 Hkv, hd]
+    k, v = x[:, H + g], x[:, H + Hkv + g]
+    dk = np.zeros((T, hd))
+    dv = np.zeros((T, hd))
+    out = {}
+    for h in range(g * G, (g + 1) * G):
+        q = x[:, h]
+        o, lse = OM.attention(q, k, v)
+        dq, dk_h, dv_h = OM.attention_bwd(q, k, v, do[b, :, h].astype(np.float64))
+        dk += dk_h
+        dv += dv_h
+        out[h] = (o, lse, OM.rope_bwd(OM.rms_norm_bwd(dq, q, rstd[b, :, h, None]), cos, sin))
+    dk = OM.rope_bwd(OM.rms_norm_bwd(dk, k, rstd[b, :, H + g, None]), cos, sin)
+    return out, dk, dv
+
+
+@pytest.mark.parametrize("name", ["d20", "d24gqa"])
+def test_attention_full_size_repeatable_and_sampled(name):
+    """The step's attention at the workload's full batch and length: forward
+    and fused backward bitwise repeatable over many launches and finite; one
+    (batch row, kv head) group against the oracle at the full length."""
+    w = S.workload(name)
+    B, T, H, Hkv, hd = w.batch, w.seq_len, w.n_head, w.n_kv_head, w.head_dim
+    rng = np.random.default_rng(77)
+    # q, k as the normalised and rotated heads the attention reads, v, dO, and
+    # the per-head rstd of the unnormalised projection
+    y = rng.standard_normal((B, T, H + 2 * Hkv, hd), dtype=np.float32)
+    y = torch.from_numpy(y).to(torch.bfloat16)
+    do = torch.from_numpy(rng.standard_normal((B, T, H, hd), dtype=np.float32)).to(torch.bfloat16)
+    rstd = rng.uniform(0.5, 2.0, size=(B, T, H + Hkv)).astype(np.float32)
+    QKV = y.reshape(B * T, -1).cuda()
+    DO = do.reshape(B * T, -1).cuda()
+    R = torch.from_numpy(rstd).reshape(B * T, -1).cuda()
+    tab = torch.empty((T, hd // 2, 2), dtype=torch.float32, device="cuda")
+    nc.ops.rope_table(T, hd, 10000.0, tab)
+    O = torch.empty((B * T, H * hd), dtype=torch.bfloat16, device="cuda")
+    L = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+    nc.ops.attention_fwd(QKV, B, T, H, Hkv, hd, O, L)
+    O1, L1 = O.clone(), L.clone()
+    for _ in range(2):
+        nc.ops.attention_fwd(QKV, B, T, H, Hkv, hd, O, L)
+        assert torch.equal(O, O1) and torch.equal(L, L1), "forward not repeatable"
+    ws = torch.empty(B * H * T, dtype=torch.float32, device="cuda")
+    D = torch.empty((B * T, (H + 2 * Hkv) * hd), dtype=torch.bfloat16, device="cuda")
+    nc.ops.attention_bwd_rope(QKV, O, L, DO, B, T, H, Hkv, hd, D, ws, R, tab)
+    D1 = D.clone()
+    assert bool(torch.isfinite(D1.float()).all()), "non-finite attention gradient"
+    for it in range(10):
+        nc.ops.attention_bwd_rope(QKV, O, L, DO, B, T, H, Hkv, hd, D, ws, R, tab)
+        assert torch.equal(D, D1), f"backward not repeatable (launch {it + 2})"
+    # sampled: last batch row, last kv group, against the oracle at full length
+    b, g, G = B - 1, Hkv - 1, H // Hkv
+    cos, sin = OM.rope_tables(T, hd, 10000.0)
+    want, dk_ref, dv_ref = _attn_oracle_group(y.float().numpy(), do.float().numpy(), rstd, b, g, T, H, Hkv,
+                                              hd, cos, sin)
+    o_got = O.float().cpu().numpy().reshape(B, T, H, hd)[b]
+    l_got = L.cpu().numpy()[b]
+    d_got = D1.float().cpu().numpy().reshape(B, T, H + 2 * Hkv, hd)[b]
+    for h, (o_ref, lse_ref, dq_ref) in want.items():
+        assert cosine(o_got[:, h], o_ref) > 0.9999, ("o", h)
+        assert np.max(np.abs(l_got[h] - lse_ref)) < 2e-2, ("lse", h)
+        assert cosine(d_got[:, h], dq_ref) > 0.9999, ("dq", h)
+    assert cosine(d_got[:, H + g], dk_ref) > 0.9999, "dk"
+    assert cosine(d_got[:, H + Hkv + g], dv_ref) > 0.9999, "dv"
