@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(512) k_cross_entropy(int V, T* __restrict__ z,
   }
 }
 
-// bf16 rows with V % 8 == 0 and V <= 512 * 8 * CE_VEC: the row is read once
+// bf16 rows with V % 8 == 0 and V <= 8 * CE_THREADS * CE_VEC: the row is read once
 // into registers (16-byte loads), reduced, and dz written from registers.
 #define CE_THREADS 1024
 #define CE_VEC 8
