@@ -203,15 +203,15 @@ def run_op(args):
         dqkv = torch.empty_like(qkv)
         ws = torch.empty(Bsz * H * T, dtype=torch.float32, device="cuda")
         # the training step's backward: dq, dk leave through the QK-norm and RoPE backward
-        tab = torch.empty((T, hd // 2, 2), dtype=torch.float32, device="cuda")
-        nc.ops.rope_table(T, hd, 10000.0, tab)
+        tab = torch.empty((hd // 4, T, 4), dtype=torch.float32, device="cuda")   # pair-major, as the step uses
+        nc.ops.rope_table_pairs(T, hd, 10000.0, tab)
         rstd = torch.ones((Bsz * T, H + Hkv), dtype=torch.float32, device="cuda")
         flops = 4.0 * Bsz * H * hd * T * (T + 1) / 2 * (3 if args.op == "attn" else 1)
 
         def once():
             nc.ops.attention_fwd(qkv, Bsz, T, H, Hkv, hd, o, lse)
             if args.op == "attn":
-                nc.ops.attention_bwd_rope(qkv, o, lse, do, Bsz, T, H, Hkv, hd, dqkv, ws, rstd, tab)
+                nc.ops.attention_bwd_rope(qkv, o, lse, do, Bsz, T, H, Hkv, hd, dqkv, ws, rstd, tab, pair_rows=T)
     for _ in range(args.warmup):
         once()
     torch.cuda.synchronize()

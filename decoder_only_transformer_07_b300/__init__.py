@@ -73,7 +73,7 @@ _SIGS = {
     "nc_op_rope_qknorm_bwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_op_attention_fwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p]),
     "nc_op_attention_bwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p, _p, _p]),
-    "nc_op_attention_bwd_rope": (_i32, [_i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p, _p, _p, _p, _p]),
+    "nc_op_attention_bwd_rope": (_i32, [_i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p, _p, _p, _p, _i32, _p]),
     "nc_op_cross_entropy": (_i32, [_i32, _i64, _i32, _p, _p, _p, _f32, _p, _p]),
     "nc_op_embed_fwd": (_i32, [_i32, _i64, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_embed_bwd_scratch_bytes": (_sz, [_i64, _i32, _i32]),
@@ -293,9 +293,9 @@ class ops:
                                         _ptr(do), _ptr(dqkv), _ptr(ws), _stream()), "nc_op_attention_bwd")
 
     @staticmethod
-    def attention_bwd_rope(qkv, o, lse, do, B, T, H, Hkv, hd, dqkv, workspace, rstd, table):
+    def attention_bwd_rope(qkv, o, lse, do, B, T, H, Hkv, hd, dqkv, workspace, rstd, table, pair_rows=0):
         _check(_lib.nc_op_attention_bwd_rope(B, T, H, Hkv, hd, _ptr(qkv), _ptr(o), _ptr(lse), _ptr(do), _ptr(dqkv),
-                                             _ptr(workspace), _ptr(rstd), _ptr(table), _stream()),
+                                             _ptr(workspace), _ptr(rstd), _ptr(table), pair_rows, _stream()),
                "nc_op_attention_bwd_rope")
 
     @staticmethod

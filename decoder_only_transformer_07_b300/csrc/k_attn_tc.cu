@@ -72,6 +72,7 @@ struct AtShape {
   // cos/sin table [T][hd/2][2]), i.e. as gradients of the projection output.
   const float* rope_tab;
   const float* rstd_qk;
+  int rope_pair_rows;   // 0: rope_tab is [T][hd/2][2]; else pair-major [hd/4][rope_pair_rows][4]
 };
 
 // tcgen05.mma kind::f16 instruction descriptor: fp32 accumulator, bf16 A and
@@ -156,8 +157,8 @@ struct FwdSmem {
 
 template <int HD>
 __global__ void __launch_bounds__(AT_THREADS, 1)
-    k_attn_fwd_tc(const __grid_constant__ CUtensorMap tm_qkv, AtShape sh, bf16* __restrict__ o,
-                  float* __restrict__ lse) {
+    k_attn_fwd_tc(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_o, AtShape sh,
+                  bf16* __restrict__ o, float* __restrict__ lse) {
   using L = FwdSmem<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -362,6 +363,38 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (ok && n > 0 && at_wait_warp(&pv_done[i], (n - 1) & 1, sh, abort_flag)) {
       tc_fence_after();
       const float inv = 1.f / l;
+      if constexpr (HD == 128) {
+        // two 32 x 64 boxes per warp, staged in this tile's Q buffer (its last
+        // S has completed) and stored by TMA
+        const uint32_t sbox = smem_u32(smem + L::OFF_Q + i * L::TILE + quarter * 8192) + (uint32_t)lane * 128u;
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll 1
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t ov[32];
+            tmem_ld_32x32b_x32(tO + 64 * c + 32 * cc, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              const uint32_t chunk = (uint32_t)(4 * cc + e / 8);
+              st_shared_v4(sbox + c * 4096u + (((chunk ^ (uint32_t)lane) & 7u) << 4),
+                           pack2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv),
+                           pack2(__uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv),
+                           pack2(__uint_as_float(ov[e + 4]) * inv, __uint_as_float(ov[e + 5]) * inv),
+                           pack2(__uint_as_float(ov[e + 6]) * inv, __uint_as_float(ov[e + 7]) * inv));
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && qt * 128 + quarter * 32 < sh.T) {
+          for (int c = 0; c < 2; ++c)
+            tma_store_3d(&tm_o, smem + L::OFF_Q + i * L::TILE + quarter * 8192 + c * 4096, h * HD + 64 * c,
+                         qt * 128 + quarter * 32, b);
+          bulk_commit();
+          bulk_wait_all();
+        }
+      } else {
       bf16* orow = o + (int64_t)(row0 + qpos) * sh.ld_o + (int64_t)h * HD;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
@@ -379,6 +412,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             *reinterpret_cast<uint4*>(orow + 32 * c + e) = w;
           }
         }
+      }
       }
       if (qpos < sh.T) lse[(int64_t)bh * sh.T + qpos] = (m * sh.scale_log2 + log2f(l)) * LN2;
     }
@@ -444,7 +478,12 @@ __device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, co
     }
   }
   dot *= sh.scale / (float)HD;
-  const float rr = valid ? sh.rstd_qk[token * (sh.H + sh.Hkv) + head] : 0.f;
+  // in range for every row (rows past the end are skipped below); the warp
+  // reconverges before the aligned TMEM loads
+  const int64_t ri = (valid ? token : 0) * (sh.H + sh.Hkv) + head;
+  float rr = 0.f;
+  if (valid) rr = sh.rstd_qk[ri];
+  __syncwarp();
   const int i0 = hf * PW;
   uint32_t g1[PW], g2[PW];
   if constexpr (PW == 32) {
@@ -456,7 +495,9 @@ __device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, co
   }
   tmem_ld_wait();
   if (!valid) return;
-  const float4* cs = reinterpret_cast<const float4*>(sh.rope_tab + (size_t)pos * HD) + (i0 >> 1);
+  const size_t cstep = sh.rope_pair_rows ? (size_t)sh.rope_pair_rows : 1;
+  const float4* cs = reinterpret_cast<const float4*>(sh.rope_tab) +
+                     (sh.rope_pair_rows ? (size_t)pos : (size_t)pos * (HD / 4)) + (size_t)(i0 >> 1) * cstep;
 #pragma unroll
   for (int q = 0; q < PW; q += 8) {
     float y1[8], y2[8], o1[8], o2[8];
@@ -464,7 +505,7 @@ __device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, co
     y8(D + i0 + q, y2);
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
-      const float4 t = __ldg(cs + ((q + e) >> 1));   // cos_i, sin_i, cos_i+1, sin_i+1
+      const float4 t = __ldg(cs + (size_t)((q + e) >> 1) * cstep);   // cos_i, sin_i, cos_i+1, sin_i+1
       const float a0 = rr * (__uint_as_float(g1[q + e]) * sh.scale - y1[e] * dot);
       const float a1 = rr * (__uint_as_float(g1[q + e + 1]) * sh.scale - y1[e + 1] * dot);
       const float b0 = rr * (__uint_as_float(g2[q + e]) * sh.scale - y2[e] * dot);
@@ -480,6 +521,38 @@ __device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, co
     *reinterpret_cast<uint4*>(dst + i0 + q) = w1;
     *reinterpret_cast<uint4*>(dst + D + i0 + q) = w2;
   }
+}
+
+// Plain output (mul * acc) of a 128 x 128 tile through shared memory and TMA.
+// Warp (quarter, hf) writes columns [64 hf, 64 hf + 64) of its 32 rows as bf16
+// into `box` (4 KB, 1024-aligned, 128-byte swizzled rows); one lane stores it
+// by TMA at {x, y, bz} of a [B][T][cols] tensor map, which drops rows at or
+// past T.  Every lane of the warp takes part, and the warp is converged again
+// on return (the caller may issue aligned tcgen05 instructions next).
+__device__ __forceinline__ void at_out_box128(uint32_t tacc, int hf, float mul, uint8_t* box, const CUtensorMap* tm,
+                                              int x, int y, int bz, int T) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t srow = smem_u32(box) + (uint32_t)lane * 128u;
+#pragma unroll 1
+  for (int c = 0; c < 2; ++c) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tacc + hf * 64 + 32 * c, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 32; e += 8)
+      st_shared_v4(srow + ((((uint32_t)(4 * c + e / 8) ^ (uint32_t)lane) & 7u) << 4),
+                   pack2(__uint_as_float(v[e]) * mul, __uint_as_float(v[e + 1]) * mul),
+                   pack2(__uint_as_float(v[e + 2]) * mul, __uint_as_float(v[e + 3]) * mul),
+                   pack2(__uint_as_float(v[e + 4]) * mul, __uint_as_float(v[e + 5]) * mul),
+                   pack2(__uint_as_float(v[e + 6]) * mul, __uint_as_float(v[e + 7]) * mul));
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && y < T) {
+    tma_store_3d(tm, box, x, y, bz);
+    bulk_commit();
+  }
+  __syncwarp();
 }
 
 // ======================================================================= backward: dQ
@@ -500,8 +573,8 @@ struct DqSmem {
 template <int HD>
 __global__ void __launch_bounds__(AT_THREADS, 1)
     k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
-                     AtShape sh, const float* __restrict__ lse, const float* __restrict__ Dv,
-                     bf16* __restrict__ dqkv) {
+                     const __grid_constant__ CUtensorMap tm_out, AtShape sh, const float* __restrict__ lse,
+                     const float* __restrict__ Dv, bf16* __restrict__ dqkv) {
   using L = DqSmem<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -666,8 +739,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
     if (ok && at_wait_warp(dq_done, 0, sh, abort_flag)) {
       tc_fence_after();
-      at_out_tile<HD>(sh, tbase + lane_off + 256, smem + L::OFF_Q, r, hf, valid, qpos, (int64_t)row0 + qpos, h,
-                      dqkv + (int64_t)(row0 + qpos) * sh.ld_qkv + (int64_t)h * HD);
+      if (HD == 128 && !sh.rope_tab) {
+        // staged in the K ring, free once every dQ product has completed
+        at_out_box128(tbase + lane_off + 256, hf, sh.scale, smem + L::OFF_K + (hf * 4 + quarter) * 4096, &tm_out,
+                      h * HD + hf * 64, qt * 128 + quarter * 32, b, sh.T);
+        if (lane == 0) bulk_wait_all();
+      } else {
+        at_out_tile<HD>(sh, tbase + lane_off + 256, smem + L::OFF_Q, r, hf, valid, qpos, (int64_t)row0 + qpos, h,
+                        dqkv + (int64_t)(row0 + qpos) * sh.ld_qkv + (int64_t)h * HD);
+      }
     }
   }
   tc_fence_before();
@@ -693,8 +773,9 @@ struct DkvSmem {
 template <int HD>
 __global__ void __launch_bounds__(AT_THREADS, 1)
     k_attn_bwd_dkv_tc(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_do, AtShape sh, const float* __restrict__ lse,
-                      const float* __restrict__ Dv, bf16* __restrict__ dqkv) {
+                      const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_out,
+                      AtShape sh, const float* __restrict__ lse, const float* __restrict__ Dv,
+                      bf16* __restrict__ dqkv) {
   using L = DkvSmem<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -885,6 +966,21 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (ok && at_wait_warp(dkv_done, 0, sh, abort_flag)) {
       tc_fence_after();
       const bool valid = key < sh.T;
+      if constexpr (HD == 128) {
+        // dV, then dK (carries 1/sqrt(hd)), staged in the Q / dO stages, free
+        // once every product has completed; a fused dK leaves through the k-norm
+        // and rotation backward with per-thread stores
+        const int w8 = hf * 4 + quarter;
+        at_out_box128(tbase + lane_off + 256, hf, 1.f, smem + L::OFF_QS + w8 * 4096, &tm_out,
+                      (sh.H + sh.Hkv + g) * HD + hf * 64, kt * 128 + quarter * 32, b, sh.T);
+        if (!sh.rope_tab)
+          at_out_box128(tbase + lane_off + 256 + HD, hf, sh.scale, smem + L::OFF_QS + 32768 + w8 * 4096, &tm_out,
+                        (sh.H + g) * HD + hf * 64, kt * 128 + quarter * 32, b, sh.T);
+        else
+          at_out_tile<HD>(sh, tbase + lane_off + 256 + HD, smem + L::OFF_K, r, hf, valid, key, (int64_t)row0 + key,
+                          sh.H + g, dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + g) * HD);
+        if (lane == 0) bulk_wait_all();
+      } else {
       bf16* dv = dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + sh.Hkv + g) * HD + hf * (HD / 2);
 #pragma unroll 1
       for (int c = 0; c < HD / 64; ++c) {
@@ -906,6 +1002,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       // dK (carries 1/sqrt(hd)), through the k-norm and rotation backward when fused
       at_out_tile<HD>(sh, tbase + lane_off + 256 + HD, smem + L::OFF_K, r, hf, valid, key, (int64_t)row0 + key,
                       sh.H + g, dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + g) * HD);
+      }
     }
   }
   tc_fence_before();
@@ -944,6 +1041,7 @@ bool at_shape(int B, int T, int H, int Hkv, int hd, int32_t* err, AtShape* sh) {
   sh->wait_ns = g_tc_wait_ns;
   sh->rope_tab = nullptr;
   sh->rstd_qk = nullptr;
+  sh->rope_pair_rows = 0;
   return true;
 }
 
@@ -951,8 +1049,10 @@ bool aligned16(const void* p) { return (((uintptr_t)p) & 15) == 0; }
 
 template <int HD>
 nc_status attn_fwd_tc(const AtShape& sh, const bf16* qkv, bf16* o, float* lse, cudaStream_t st) {
-  CUtensorMap tm;
-  if (!make_tmap_bf16_2d(&tm, qkv, sh.ld_qkv, (uint64_t)sh.B * sh.T, sh.ld_qkv, 64, 128)) return NC_ERR_CUDA;
+  CUtensorMap tm, tm_o;
+  if (!make_tmap_bf16_2d(&tm, qkv, sh.ld_qkv, (uint64_t)sh.B * sh.T, sh.ld_qkv, 64, 128) ||
+      !make_tmap_bf16_3d(&tm_o, o, sh.ld_o, sh.T, sh.B, sh.ld_o, 64, 32))
+    return NC_ERR_CUDA;
   static bool attr = false;
   if (!attr) {
     NC_CUDA_TRY(cudaFuncSetAttribute(k_attn_fwd_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -960,7 +1060,7 @@ nc_status attn_fwd_tc(const AtShape& sh, const bf16* qkv, bf16* o, float* lse, c
     attr = true;
   }
   const unsigned grid = (unsigned)((sh.T + 255) / 256) * (unsigned)(sh.B * sh.H);
-  k_attn_fwd_tc<HD><<<grid, AT_THREADS, FwdSmem<HD>::BYTES, st>>>(tm, sh, o, lse);
+  k_attn_fwd_tc<HD><<<grid, AT_THREADS, FwdSmem<HD>::BYTES, st>>>(tm, tm_o, sh, o, lse);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
@@ -970,8 +1070,9 @@ nc_status attn_bwd_tc(const AtShape& sh, const bf16* qkv, const bf16* o, const f
   const int64_t rows = (int64_t)sh.B * sh.T;
   k_attn_rowdot<bf16><<<cdiv(rows * sh.H, 8), 256, 0, st>>>(rows, sh.H, HD, sh.T, sh.ld_o, o, dout, Dv);
   NC_CUDA_TRY(cudaGetLastError());
-  CUtensorMap tm_qkv128, tm_qkv64, tm_do128, tm_do64;
-  if (!make_tmap_bf16_2d(&tm_qkv128, qkv, sh.ld_qkv, rows, sh.ld_qkv, 64, 128) ||
+  CUtensorMap tm_qkv128, tm_qkv64, tm_do128, tm_do64, tm_out;
+  if (!make_tmap_bf16_3d(&tm_out, dqkv, sh.ld_qkv, sh.T, sh.B, sh.ld_qkv, 64, 32) ||
+      !make_tmap_bf16_2d(&tm_qkv128, qkv, sh.ld_qkv, rows, sh.ld_qkv, 64, 128) ||
       !make_tmap_bf16_2d(&tm_qkv64, qkv, sh.ld_qkv, rows, sh.ld_qkv, 64, 64) ||
       !make_tmap_bf16_2d(&tm_do128, dout, sh.ld_o, rows, sh.ld_o, 64, 128) ||
       !make_tmap_bf16_2d(&tm_do64, dout, sh.ld_o, rows, sh.ld_o, 64, 64))
@@ -986,10 +1087,10 @@ nc_status attn_bwd_tc(const AtShape& sh, const bf16* qkv, const bf16* o, const f
   }
   const unsigned nt = (unsigned)((sh.T + 127) / 128);
   k_attn_bwd_dq_tc<HD><<<nt * (unsigned)(sh.B * sh.H), AT_THREADS, DqSmem<HD>::BYTES, st>>>(
-      tm_qkv128, tm_do128, sh, lse, Dv, dqkv);
+      tm_qkv128, tm_do128, tm_out, sh, lse, Dv, dqkv);
   NC_CUDA_TRY(cudaGetLastError());
   k_attn_bwd_dkv_tc<HD><<<nt * (unsigned)(sh.B * sh.Hkv), AT_THREADS, DkvSmem<HD>::BYTES, st>>>(
-      tm_qkv128, tm_qkv64, tm_do64, sh, lse, Dv, dqkv);
+      tm_qkv128, tm_qkv64, tm_do64, tm_out, sh, lse, Dv, dqkv);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
@@ -1005,12 +1106,14 @@ nc_status launch_attn_fwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* q
 
 nc_status launch_attn_bwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, const bf16* o, const float* lse,
                              const bf16* dout, bf16* dqkv, float* Dv, const float* rstd_qk, const float* rope_tab,
-                             int32_t* err, cudaStream_t st) {
+                             int rope_pair_rows, int32_t* err, cudaStream_t st) {
   AtShape sh;
   if (!at_shape(B, T, H, Hkv, hd, err, &sh)) return NC_ERR_ARG;
   if ((rstd_qk == nullptr) != (rope_tab == nullptr) || (rope_tab && !aligned16(rope_tab))) return NC_ERR_ARG;
+  if (rope_pair_rows < 0 || (rope_pair_rows > 0 && (rope_pair_rows < T || hd % 4))) return NC_ERR_ARG;
   sh.rstd_qk = rstd_qk;
   sh.rope_tab = rope_tab;
+  sh.rope_pair_rows = rope_pair_rows;
   if (!aligned16(qkv) || !aligned16(dout) || !aligned16(dqkv)) return NC_ERR_ARG;
   return hd == 128 ? attn_bwd_tc<128>(sh, qkv, o, lse, dout, dqkv, Dv, st)
                    : attn_bwd_tc<64>(sh, qkv, o, lse, dout, dqkv, Dv, st);

@@ -893,6 +893,25 @@ bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64
   return make_tmap_2d(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, outer, ld, box_inner, box_outer);
 }
 
+// 3-D bf16 tensor map over [d2][d1][inner] with row pitch ld elements and
+// d1 rows per d2 slice (a [B][T][cols] view of a [B*T, ld] matrix), box
+// {box_inner, box_mid, 1}, 128-byte swizzle.  Boxes are clipped at d1, so a
+// tile that runs past the end of one sequence never touches the next.
+bool make_tmap_bf16_3d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t d1, uint64_t d2, int64_t ld,
+                       uint32_t box_inner, uint32_t box_mid) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  if ((((uintptr_t)base) & 15) || ((ld * 2) % 16)) return false;
+  cuuint64_t dims[3] = {inner, d1, d2};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)ld * 2 * d1};
+  cuuint32_t box[3] = {box_inner, box_mid, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int g_num_sms = 0;
 uint64_t g_tc_wait_ns = 4000000000ull;   // bounded-wait limit of the tensor-core kernels
 

@@ -177,13 +177,14 @@ static nc_status attn_fwd(int dtype, int B, int T, int H, int Hkv, int hd, const
   if (dtype == NC_BF16) return launch_attn_fwd_tc(B, T, H, Hkv, hd, (const bf16*)qkv, (bf16*)o, lse, err, st);
   return launch_attn_fwd_simt(dtype, B, T, H, Hkv, hd, qkv, o, lse, st);
 }
-// rstd_qk / rope_tab (bf16 only): fold the RoPE + QK-norm backward into the output.
+// rstd_qk / rope_tab (bf16 only): fold the RoPE + QK-norm backward into the output;
+// pair_rows > 0 selects the pair-major table layout.
 static nc_status attn_bwd(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv, const void* o,
                           const float* lse, const void* dout, void* dqkv, float* Dv, const float* rstd_qk,
-                          const float* rope_tab, int32_t* err, cudaStream_t st) {
+                          const float* rope_tab, int pair_rows, int32_t* err, cudaStream_t st) {
   if (dtype == NC_BF16)
     return launch_attn_bwd_tc(B, T, H, Hkv, hd, (const bf16*)qkv, (const bf16*)o, lse, (const bf16*)dout,
-                              (bf16*)dqkv, Dv, rstd_qk, rope_tab, err, st);
+                              (bf16*)dqkv, Dv, rstd_qk, rope_tab, pair_rows, err, st);
   if (rstd_qk || rope_tab) return NC_ERR_UNSUPPORTED;
   return launch_attn_bwd_simt(dtype, B, T, H, Hkv, hd, qkv, o, lse, dout, dqkv, Dv, st);
 }
@@ -496,11 +497,11 @@ static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int 
     if (m->dtype == NC_BF16) {
       // attention backward with the q/k RMSNorm + RoPE backward in its output epilogue
       PROF(NC_PROF_ATTN_BWD, attn_fl, (double)N * (2.0 * W + 2.0 * Hd) * a + 8.0 * N * m->H,
-           attn_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, rstdqk, m->rope_tab,
-                    m->err, st));
+           attn_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, rstdqk,
+                    m->rope_pairs ? m->rope_pairs : m->rope_tab, m->rope_pairs ? m->Tmax : 0, m->err, st));
     } else {
       PROF(NC_PROF_ATTN_BWD, attn_fl, (double)N * (2.0 * W + 2.0 * Hd) * a + 8.0 * N * m->H,
-           attn_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, nullptr, nullptr,
+           attn_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, nullptr, nullptr, 0,
                     m->err, st));
       PROF(NC_PROF_ROPE, 0, (double)N * nh * (3.0 * a * m->hd + 4),
            launch_rope_qknorm_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, m->dqkv, qkv, rstdqk, m->rope_tab, st));
@@ -677,16 +678,17 @@ extern "C" nc_status nc_op_attention_bwd(int32_t dtype, int32_t B, int32_t T, in
                                          const void* qkv, const void* o, const float* lse, const void* do_,
                                          void* dqkv, float* workspace, void* stream) {
   if (!dtype_ok(dtype) || !qkv || !o || !lse || !do_ || !dqkv || !workspace) return NC_ERR_ARG;
-  return attn_bwd(dtype, B, T, H, Hkv, hd, qkv, o, lse, do_, dqkv, workspace, nullptr, nullptr, nullptr,
+  return attn_bwd(dtype, B, T, H, Hkv, hd, qkv, o, lse, do_, dqkv, workspace, nullptr, nullptr, 0, nullptr,
                   as_stream(stream));
 }
 
 extern "C" nc_status nc_op_attention_bwd_rope(int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
                                               const void* qkv, const void* o, const float* lse, const void* do_,
                                               void* dqkv, float* workspace, const float* rstd, const float* cos_sin,
-                                              void* stream) {
+                                              int32_t pair_rows, void* stream) {
   if (!qkv || !o || !lse || !do_ || !dqkv || !workspace || !rstd || !cos_sin) return NC_ERR_ARG;
-  return attn_bwd(NC_BF16, B, T, H, Hkv, hd, qkv, o, lse, do_, dqkv, workspace, rstd, cos_sin, nullptr,
+  if (pair_rows < 0 || (pair_rows > 0 && pair_rows < T)) return NC_ERR_ARG;
+  return attn_bwd(NC_BF16, B, T, H, Hkv, hd, qkv, o, lse, do_, dqkv, workspace, rstd, cos_sin, pair_rows, nullptr,
                   as_stream(stream));
 }
 

@@ -63,12 +63,17 @@ nc_status launch_attn_fwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* q
                              int32_t* err, cudaStream_t st);
 // With rstd_qk and rope_tab (both or neither), dq and dk are returned through the
 // per-head RMSNorm backward and the transposed rotation (the RoPE + QK-norm
-// backward fused into the output epilogue).
+// backward fused into the output epilogue).  rope_tab is [T][hd/2][2]
+// (rope_pair_rows = 0) or pair-major [hd/4][rope_pair_rows][4] (rope_pair_rows >= T).
 nc_status launch_attn_bwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, const bf16* o, const float* lse,
                              const bf16* dout, bf16* dqkv, float* Dv, const float* rstd_qk, const float* rope_tab,
-                             int32_t* err, cudaStream_t st);
+                             int rope_pair_rows, int32_t* err, cudaStream_t st);
 
 // 2D bf16 TMA descriptor over a row-major [outer][inner] matrix with leading
 // dimension ld (elements), box {box_inner, box_outer}, 128-byte swizzle.
 bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, int64_t ld,
                        uint32_t box_inner, uint32_t box_outer);
+// 3D bf16 TMA descriptor viewing a [d2*d1, ld] matrix as [d2][d1][inner], box
+// {box_inner, box_mid, 1}, 128-byte swizzle; stores are clipped at d1.
+bool make_tmap_bf16_3d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t d1, uint64_t d2, int64_t ld,
+                       uint32_t box_inner, uint32_t box_mid);

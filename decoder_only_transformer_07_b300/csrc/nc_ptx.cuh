@@ -181,6 +181,12 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, const void* smem_
                "r"(y), "r"(smem_u32(smem_src))
                : "memory");
 }
+// Same over a 3-D tensor map {x, y, z}; elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* smem_src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap), "r"(x),
+               "r"(y), "r"(z), "r"(smem_u32(smem_src))
+               : "memory");
+}
 // Element-wise global += shared over one box (fp32 add at L2; each element is
 // updated exactly once per call, so the result is the single rounded sum).
 __device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, const void* smem_src, int x, int y) {

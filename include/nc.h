@@ -240,11 +240,15 @@ nc_status nc_op_attention_bwd(int32_t dtype, int32_t B, int32_t T, int32_t H,
  * respect to the projection output (before RoPE and the per-head RMSNorm),
  * given the saved normalised qkv, rstd (float [B*T, H+Hkv]) and the cos/sin
  * table; the v block is as from nc_op_attention_bwd.  Equivalent to
- * nc_op_attention_bwd followed by nc_op_rope_qknorm_bwd.  hd 64 or 128. */
+ * nc_op_attention_bwd followed by nc_op_rope_qknorm_bwd.  cos_sin is the table
+ * of nc_op_rope_table (pair_rows = 0) or of nc_op_rope_table_pairs built for
+ * pair_rows >= T positions (faster: a warp's reads of it coalesce).  hd 64 or
+ * 128; NC_ERR_ARG for a NULL buffer or 0 < pair_rows < T. */
 nc_status nc_op_attention_bwd_rope(int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
                                    const void* qkv, const void* o, const float* lse,
                                    const void* do_, void* dqkv, float* workspace,
-                                   const float* rstd, const float* cos_sin, void* stream);
+                                   const float* rstd, const float* cos_sin, int32_t pair_rows,
+                                   void* stream);
 
 /* Cross-entropy on logits z (dtype [rows, V]) against targets (int32 [rows]):
  * row_loss (float [rows]) = logsumexp(z) - z[target]; z is overwritten in

@@ -124,8 +124,8 @@ def test_attention_full_size_repeatable_and_sampled(name):
     QKV = y.reshape(B * T, -1).cuda()
     DO = do.reshape(B * T, -1).cuda()
     R = torch.from_numpy(rstd).reshape(B * T, -1).cuda()
-    tab = torch.empty((T, hd // 2, 2), dtype=torch.float32, device="cuda")
-    nc.ops.rope_table(T, hd, 10000.0, tab)
+    tab = torch.empty((hd // 4, T, 4), dtype=torch.float32, device="cuda")   # pair-major, as the step uses
+    nc.ops.rope_table_pairs(T, hd, 10000.0, tab)
     O = torch.empty((B * T, H * hd), dtype=torch.bfloat16, device="cuda")
     L = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
     nc.ops.attention_fwd(QKV, B, T, H, Hkv, hd, O, L)
@@ -135,11 +135,11 @@ def test_attention_full_size_repeatable_and_sampled(name):
         assert torch.equal(O, O1) and torch.equal(L, L1), "forward not repeatable"
     ws = torch.empty(B * H * T, dtype=torch.float32, device="cuda")
     D = torch.empty((B * T, (H + 2 * Hkv) * hd), dtype=torch.bfloat16, device="cuda")
-    nc.ops.attention_bwd_rope(QKV, O, L, DO, B, T, H, Hkv, hd, D, ws, R, tab)
+    nc.ops.attention_bwd_rope(QKV, O, L, DO, B, T, H, Hkv, hd, D, ws, R, tab, pair_rows=T)
     D1 = D.clone()
     assert bool(torch.isfinite(D1.float()).all()), "non-finite attention gradient"
     for it in range(10):
-        nc.ops.attention_bwd_rope(QKV, O, L, DO, B, T, H, Hkv, hd, D, ws, R, tab)
+        nc.ops.attention_bwd_rope(QKV, O, L, DO, B, T, H, Hkv, hd, D, ws, R, tab, pair_rows=T)
         assert torch.equal(D, D1), f"backward not repeatable (launch {it + 2})"
     # sampled: last batch row, last kv group, against the oracle at full length
     b, g, G = B - 1, Hkv - 1, H // Hkv

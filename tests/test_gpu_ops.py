@@ -304,8 +304,9 @@ def test_attention_fwd_bwd(hd, H, Hkv, T, dt):
             assert cosine(got[:, :, sl], ref[:, :, sl]) > 0.9999, name
 
 
-@pytest.mark.parametrize("hd,H,Hkv,T", [(128, 4, 2, 300), (64, 2, 1, 200), (128, 2, 2, 128)])
-def test_attention_bwd_with_fused_rope_qknorm_bwd(hd, H, Hkv, T):
+@pytest.mark.parametrize("pairs", [False, True])
+@pytest.mark.parametrize("hd,H,Hkv,T", [(128, 4, 2, 300), (64, 2, 1, 200), (128, 2, 2, 128), (128, 3, 1, 257)])
+def test_attention_bwd_with_fused_rope_qknorm_bwd(hd, H, Hkv, T, pairs):
     """Attention backward whose dq / dk leave through the QK-norm and RoPE
     backward, against the oracle's attention backward followed by its RMSNorm
     and rotation backward on the same normalised bf16 q, k, v."""
@@ -322,7 +323,12 @@ def test_attention_bwd_with_fused_rope_qknorm_bwd(hd, H, Hkv, T):
     DO = dev_tensor(rnd(61, (B * T, H * hd)), BF16)
     DQKV = torch.zeros((B * T, W), dtype=BF16, device="cuda")
     ws = torch.empty(B * H * T, dtype=F32, device="cuda")
-    nc.ops.attention_bwd_rope(QKV, O, L, DO, B, T, H, Hkv, hd, DQKV, ws, R, tab)
+    if pairs:   # the pair-major table, built for more positions than T
+        ptab = torch.empty((hd // 4, T + 5, 4), dtype=F32, device="cuda")
+        nc.ops.rope_table_pairs(T + 5, hd, base, ptab)
+        nc.ops.attention_bwd_rope(QKV, O, L, DO, B, T, H, Hkv, hd, DQKV, ws, R, ptab, pair_rows=T + 5)
+    else:
+        nc.ops.attention_bwd_rope(QKV, O, L, DO, B, T, H, Hkv, hd, DQKV, ws, R, tab)
     torch.cuda.synchronize()
     qkv = to64(QKV)
     _, _, d_ref = _attn_ref(qkv, B, T, H, Hkv, hd, to64(DO))
