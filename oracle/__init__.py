@@ -14,6 +14,10 @@ The model it computes is the one the nanochat pages describe:
   master weights cast to the compute dtype in the forward;
 * woshipm nanochat analysis §五.1: a 4x feed-forward layer.
 
+``optim.py`` restates the optimizer step that follows the gradients (Muon for
+the weight matrices, AdamW for the embedding and the output head;
+cosmicrealm §2.2 and §4.2).
+
 Readings taken where the pages are silent are listed in each function's
 docstring.  Parity of the whole step is pinned by finite differences and by the
 invariants in ``tests/test_oracle_*.py``.
