@@ -173,6 +173,55 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_optim(args):
+    """Optimizer mode: times nc_optimizer_step (Muon for every weight matrix,
+    AdamW for wte and lm_head) on the --config model with seeded synthetic
+    gradients, then splits one profiled step into its Newton-Schulz products
+    (tensor cores) and its elementwise kernels (HBM)."""
+    import ctypes
+    import statistics
+    import torch
+    import decoder_only_transformer_07_b300 as nc
+    torch.cuda.set_device(0)
+    w = S.workload(args.config)
+    model = nc.Model(nc.config_from_workload(w), seed=S.WEIGHT_SEED)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    grads = torch.randn(model.n_params, device="cuda", generator=g) * 1e-3
+    oc = nc.optim_config()
+    for _ in range(args.warmup):
+        model.optimizer_step(grads, oc)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.iters):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        model.optimizer_step(grads, oc)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    lib = nc.lib()
+    lib.nc_profile_enable(model.handle, 1)
+    model.optimizer_step(grads, oc)
+    torch.cuda.synchronize()
+    phases = {}
+    for cls, name in ((13, "newton_schulz"), (14, "elementwise")):
+        t, n, fl, by = ctypes.c_double(), ctypes.c_int64(), ctypes.c_double(), ctypes.c_double()
+        lib.nc_profile_read(model.handle, cls, ctypes.byref(t), ctypes.byref(n), ctypes.byref(fl), ctypes.byref(by))
+        phases[name] = {"ms": t.value, "launches": n.value, "tflops": fl.value / t.value / 1e9 if t.value else None,
+                        "gbs": by.value / t.value / 1e6 if t.value else None}
+    lib.nc_profile_enable(model.handle, 0)
+    _, sustained, hbm, kind = load_peaks()
+    ns, ew = phases["newton_schulz"], phases["elementwise"]
+    print(json.dumps({"op": "optim", "config": args.config, "ms": statistics.median(times), "iters": args.iters,
+                      "phases": phases,
+                      "roofline": {"bound": "tensor", "achieved": ns["tflops"], "peak": sustained, "unit": "TFLOP/s",
+                                   "frac": ns["tflops"] / sustained, "peak_kind": f"bf16 dense, sustained ({kind})",
+                                   "kernel": "Newton-Schulz products (tcgen05 GEMM)"},
+                      "elementwise_hbm_frac": ew["gbs"] / hbm if ew["gbs"] else None,
+                      "optimizer_steps": model.optimizer_steps()}), flush=True)
+    model.close()
+
+
 def run_op(args):
     """Single-kernel mode (for ncu captures of one kernel on a small case):
     times --iters launches of one GEMM or one attention forward+backward."""
@@ -238,7 +287,7 @@ def main():
     ap.add_argument("--step-batch", type=int, default=0,
                     help="profiling only: run the step at this batch size instead of the workload's")
     # single-op mode (profiling)
-    ap.add_argument("--op", choices=["gemm", "attn", "attn_fwd"])
+    ap.add_argument("--op", choices=["gemm", "attn", "attn_fwd", "optim"])
     ap.add_argument("--m", type=int, default=65536)
     ap.add_argument("--n", type=int, default=3840)
     ap.add_argument("--k", type=int, default=1280)
@@ -252,6 +301,8 @@ def main():
     ap.add_argument("--head-dim", type=int, default=128)
     ap.add_argument("--iters", type=int, default=5)
     args = ap.parse_args()
+    if args.op == "optim":
+        return run_optim(args)
     if args.op:
         return run_op(args)
     w = S.workload(args.config, **({"batch": args.step_batch} if args.step_batch else {}))

@@ -41,6 +41,13 @@ class nc_config(ctypes.Structure):
                 ("norm_eps", ctypes.c_float), ("init_std", ctypes.c_float)]
 
 
+class nc_optim_config(ctypes.Structure):
+    _fields_ = [("matrix_lr", ctypes.c_float), ("embedding_lr", ctypes.c_float),
+                ("unembedding_lr", ctypes.c_float), ("momentum", ctypes.c_float), ("nesterov", ctypes.c_int32),
+                ("ns_steps", ctypes.c_int32), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("adam_eps", ctypes.c_float), ("weight_decay", ctypes.c_float)]
+
+
 _p, _i32, _i64, _f32, _u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_uint64
 _sz = ctypes.c_size_t
 _SIGS = {
@@ -77,6 +84,12 @@ _SIGS = {
     "nc_op_cross_entropy": (_i32, [_i32, _i64, _i32, _p, _p, _p, _f32, _p, _p]),
     "nc_op_embed_fwd": (_i32, [_i32, _i64, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_embed_bwd_scratch_bytes": (_sz, [_i64, _i32, _i32]),
+    "nc_optim_config_default": (None, [ctypes.POINTER(nc_optim_config)]),
+    "nc_optimizer_step": (_i32, [_p, ctypes.POINTER(nc_optim_config), _p, _f32, _p]),
+    "nc_optimizer_reset": (_i32, [_p, _p]),
+    "nc_optimizer_steps": (_i64, [_p]),
+    "nc_newton_schulz_workspace_bytes": (_sz, [_i32, _i32, _i32]),
+    "nc_op_newton_schulz": (_i32, [_i32, _i32, _i32, _i32, _p, _p, _p, _p]),
     "nc_op_embed_bwd": (_i32, [_i64, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_debug_set_wait_limit_ns": (None, [_u64]),
     "nc_debug_set_gemm_pair": (None, [_i32]),
@@ -124,6 +137,15 @@ def make_config(depth, n_embd, n_head, n_kv_head, head_dim, mlp_hidden, vocab, s
     d = NC_BF16 if dtype in ("bf16", NC_BF16) else NC_FP32
     return nc_config(depth, n_embd, n_head, n_kv_head, head_dim, mlp_hidden, vocab, seq_len, batch, d,
                      rope_base, norm_eps, init_std)
+
+
+def optim_config(**kw):
+    """nc_optim_config with the library defaults, fields overridden by keyword."""
+    oc = nc_optim_config()
+    _lib.nc_optim_config_default(ctypes.byref(oc))
+    for k, v in kw.items():
+        setattr(oc, k, v)
+    return oc
 
 
 def config_from_workload(w, **kw):
@@ -218,6 +240,18 @@ class Model:
     def check(self):
         _check(_lib.nc_last_error(self._h, _stream()), "device error flag")
 
+    def optimizer_step(self, grads, config=None, lr_mult=1.0):
+        """One Muon (matrices) + AdamW (wte, lm_head) step on the fp32 master weights."""
+        oc = config if config is not None else optim_config()
+        _check(_lib.nc_optimizer_step(self._h, ctypes.byref(oc), _ptr(grads), lr_mult, _stream()),
+               "nc_optimizer_step")
+
+    def optimizer_reset(self):
+        _check(_lib.nc_optimizer_reset(self._h, _stream()), "nc_optimizer_reset")
+
+    def optimizer_steps(self):
+        return int(_lib.nc_optimizer_steps(self._h))
+
     def last_launch_count(self):
         return int(_lib.nc_last_launch_count(self._h))
 
@@ -309,6 +343,18 @@ class ops:
         V, C = wte.shape
         _check(_lib.nc_op_embed_fwd(dtype, tokens.numel(), C, V, _ptr(tokens), _ptr(wte), _ptr(x), _ptr(err),
                                     _stream()), "nc_op_embed_fwd")
+
+    @staticmethod
+    def newton_schulz(u, x, steps=5, dtype=None, workspace=None):
+        """x (float [rows, cols]) = Newton-Schulz orthogonalisation of u in `dtype`."""
+        import torch
+        rows, cols = u.shape
+        d = NC_BF16 if dtype in (None, "bf16", NC_BF16) else NC_FP32
+        if workspace is None:
+            nb = int(_lib.nc_newton_schulz_workspace_bytes(d, rows, cols))
+            workspace = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        _check(_lib.nc_op_newton_schulz(d, rows, cols, steps, _ptr(u), _ptr(x), _ptr(workspace), _stream()),
+               "nc_op_newton_schulz")
 
     @staticmethod
     def embed_bwd_scratch_bytes(n, C, V):

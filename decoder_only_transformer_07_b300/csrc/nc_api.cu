@@ -8,6 +8,7 @@
 // and backward per chunk), then per layer in reverse the matching backward
 // kernels, and the embedding scatter.  The only synchronisation is the final
 // read of the loss and the device error flag.
+#include <algorithm>
 #include <cfloat>
 #include <cstdio>
 #include <cstring>
@@ -60,6 +61,13 @@ struct nc_model {
   size_t gemm_ws_bytes = 0;
   int32_t *tok_dev = nullptr, *tgt_dev = nullptr;
   int64_t launches = 0;
+  // optimizer state, allocated and zeroed by the first nc_optimizer_step
+  bool opt_ready = false;
+  int64_t opt_t = 0;                 // optimizer steps taken
+  OptTensors* opt_tl = nullptr;      // the Muon matrices (host copy of the kernel parameter)
+  float *opt_mom = nullptr, *opt_u = nullptr, *opt_partial = nullptr, *opt_norm = nullptr;
+  void *opt_x0 = nullptr, *opt_ping0 = nullptr, *opt_ping1 = nullptr, *opt_a = nullptr, *opt_a2 = nullptr;
+  float *adam_m = nullptr, *adam_v = nullptr;   // [wte | lm_head] moments
   // profiling (nc_profile_enable)
   struct Rec { int cls, sub; int ev; double flops, bytes; };
   bool prof_on = false;
@@ -301,13 +309,16 @@ extern "C" const char* nc_status_string(nc_status s) {
   return "unknown status";
 }
 
-extern "C" const char* nc_version(void) { return "libnc 0.2 sm_103a (tcgen05 GEMM, mma.sync flash attention)"; }
+extern "C" const char* nc_version(void) {
+  return "libnc 0.3 sm_103a (tcgen05 GEMM and flash attention, Muon + AdamW optimizer)";
+}
 
 extern "C" void nc_model_destroy(nc_model* m) {
   if (!m) return;
   for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
   for (void* p : m->allocs) cudaFree(p);
   if (m->result_host) cudaFreeHost(m->result_host);
+  delete m->opt_tl;
   delete m;
 }
 
@@ -741,3 +752,178 @@ extern "C" void nc_debug_set_wait_limit_ns(uint64_t ns) { g_tc_wait_ns = ns; }
 
 extern int g_gemm_pair;
 extern "C" void nc_debug_set_gemm_pair(int32_t on) { g_gemm_pair = on != 0; }
+
+// ------------------------------------------------------------------ optimizer
+// Muon for every weight matrix, AdamW for wte and lm_head (cosmicrealm
+// "noao-chat-0-项目总体介绍" §2.2, §4.2).
+
+extern "C" void nc_optim_config_default(nc_optim_config* oc) {
+  if (!oc) return;
+  oc->matrix_lr = 0.02f;
+  oc->embedding_lr = 0.2f;
+  oc->unembedding_lr = 0.004f;
+  oc->momentum = 0.95f;
+  oc->nesterov = 1;
+  oc->ns_steps = 5;
+  oc->beta1 = 0.9f;
+  oc->beta2 = 0.999f;
+  oc->adam_eps = 1e-8f;
+  oc->weight_decay = 0.f;
+}
+
+static void opt_fill(OptTensors* tl, const int64_t* off, const int64_t* len, int n) {
+  memset(tl, 0, sizeof(*tl));
+  tl->n = n;
+  int32_t c = 0;
+  int64_t so = 0;
+  for (int i = 0; i < n; ++i) {
+    tl->chunk0[i] = c;
+    tl->off[i] = off[i];
+    tl->soff[i] = so;
+    tl->len[i] = len[i];
+    c += (int32_t)((len[i] + OPT_CHUNK - 1) / OPT_CHUNK);
+    so += len[i];
+  }
+  tl->chunk0[n] = c;
+}
+
+static nc_status opt_alloc(nc_model* m) {
+  const int nm = 6 * m->L;
+  if (nm > NC_OPT_MAXT) return NC_ERR_UNSUPPORTED;
+  std::vector<int64_t> off(nm), len(nm);
+  int64_t total = 0, maxrc = 0, maxn = 0;
+  for (int i = 0; i < nm; ++i) {
+    const ParamTensor& t = m->layout[1 + i];
+    off[i] = t.off;
+    len[i] = t.rows * t.cols;
+    total += len[i];
+    maxrc = std::max(maxrc, len[i]);
+    maxn = std::max(maxn, std::min(t.rows, t.cols));
+  }
+  m->opt_tl = new OptTensors;
+  opt_fill(m->opt_tl, off.data(), len.data(), nm);
+  const int64_t nchunks = m->opt_tl->chunk0[nm];
+  const ParamTensor& te = m->layout.front();
+  const ParamTensor& tl = m->layout.back();
+  const int64_t na = te.rows * te.cols + tl.rows * tl.cols;
+  NC_TRY(dalloc_t(m, (size_t)total, &m->opt_mom));
+  NC_TRY(dalloc_t(m, (size_t)total, &m->opt_u));
+  NC_TRY(dalloc_t(m, (size_t)std::max<int64_t>(nchunks, 1), &m->opt_partial));
+  NC_TRY(dalloc_t(m, (size_t)nm, &m->opt_norm));
+  NC_TRY(dalloc(m, (size_t)total * m->act, &m->opt_x0));
+  NC_TRY(dalloc(m, (size_t)maxrc * m->act, &m->opt_ping0));
+  NC_TRY(dalloc(m, (size_t)maxrc * m->act, &m->opt_ping1));
+  NC_TRY(dalloc(m, (size_t)(maxn * maxn) * m->act, &m->opt_a));
+  NC_TRY(dalloc(m, (size_t)(maxn * maxn) * m->act, &m->opt_a2));
+  NC_TRY(dalloc_t(m, (size_t)na, &m->adam_m));
+  NC_TRY(dalloc_t(m, (size_t)na, &m->adam_v));
+  m->opt_tl->norm = m->opt_norm;
+  m->opt_ready = true;
+  return NC_OK;
+}
+
+extern "C" nc_status nc_optimizer_reset(nc_model* m, void* stream) {
+  if (!m) return NC_ERR_ARG;
+  m->opt_t = 0;
+  if (!m->opt_ready) return NC_OK;
+  cudaStream_t st = as_stream(stream);
+  const int64_t total = m->opt_tl->soff[m->opt_tl->n - 1] + m->opt_tl->len[m->opt_tl->n - 1];
+  const ParamTensor& te = m->layout.front();
+  const ParamTensor& tl = m->layout.back();
+  const int64_t na = te.rows * te.cols + tl.rows * tl.cols;
+  NC_CUDA_TRY(cudaMemsetAsync(m->opt_mom, 0, (size_t)total * sizeof(float), st));
+  NC_CUDA_TRY(cudaMemsetAsync(m->adam_m, 0, (size_t)na * sizeof(float), st));
+  NC_CUDA_TRY(cudaMemsetAsync(m->adam_v, 0, (size_t)na * sizeof(float), st));
+  return NC_OK;
+}
+
+extern "C" int64_t nc_optimizer_steps(const nc_model* m) { return m ? m->opt_t : -1; }
+
+extern "C" nc_status nc_optimizer_step(nc_model* m, const nc_optim_config* oc, const float* grads, float lr_mult,
+                                       void* stream) {
+  if (!m || !oc || !grads) return NC_ERR_ARG;
+  if (oc->ns_steps < 0 || oc->ns_steps > 64 || !(oc->momentum >= 0.f && oc->momentum < 1.f) ||
+      !(oc->beta1 >= 0.f && oc->beta1 < 1.f) || !(oc->beta2 >= 0.f && oc->beta2 < 1.f) || !(oc->adam_eps > 0.f))
+    return NC_ERR_ARG;
+  cudaStream_t st = as_stream(stream);
+  if (!m->opt_ready) {
+    NC_TRY(opt_alloc(m));
+    NC_TRY(nc_optimizer_reset(m, stream));
+  }
+  prof_flush(m);
+  m->opt_t += 1;
+  const OptTensors& tl = *m->opt_tl;
+  const int64_t total = tl.soff[tl.n - 1] + tl.len[tl.n - 1];
+  const double act = (double)m->act;
+  // Muon: momentum, Nesterov update and its norm for every matrix at once
+  PROF(NC_PROF_OPT_EW, 0, 16.0 * total,
+       launch_muon_momentum(tl, grads, m->opt_mom, m->opt_u, oc->momentum, oc->nesterov, m->opt_partial, st));
+  PROF(NC_PROF_OPT_EW, 0, (4.0 + act) * total, launch_ns_init(m->dtype, tl, m->opt_u, 1e-7f, m->opt_x0, st));
+  for (int i = 0; i < tl.n; ++i) {
+    const ParamTensor& t = m->layout[1 + i];
+    const void* x = (const uint8_t*)m->opt_x0 + tl.soff[i] * m->act;
+    const double n = (double)std::min(t.rows, t.cols), k = (double)std::max(t.rows, t.cols);
+    if (oc->ns_steps > 0)
+      PROF(NC_PROF_OPT_NS, oc->ns_steps * (4.0 * n * n * k + 2.0 * n * n * n),
+           oc->ns_steps * (4.0 * n * k + 4.0 * n * n) * act,
+           newton_schulz_run(m->dtype, (int)t.rows, (int)t.cols, oc->ns_steps, x, m->opt_ping0, m->opt_ping1,
+                             m->opt_a, m->opt_a2, &x, m->err, m->gemm_ws, m->gemm_ws_bytes, st));
+    const float scale = sqrtf(std::max(1.f, (float)t.rows / (float)t.cols));
+    PROF(NC_PROF_OPT_EW, 0, (8.0 + act) * t.rows * t.cols,
+         launch_muon_apply(m->dtype, t.rows * t.cols, m->master + t.off, x, oc->matrix_lr * lr_mult * scale, st));
+  }
+  // AdamW on the embedding and the output head
+  const ParamTensor& te = m->layout.front();
+  const ParamTensor& th = m->layout.back();
+  const int64_t ne = te.rows * te.cols, nh = th.rows * th.cols;
+  PROF(NC_PROF_OPT_EW, 0, 28.0 * ne,
+       launch_adamw(ne, m->master + te.off, grads + te.off, m->adam_m, m->adam_v, oc->embedding_lr * lr_mult,
+                    oc->beta1, oc->beta2, oc->adam_eps, oc->weight_decay, m->opt_t, st));
+  PROF(NC_PROF_OPT_EW, 0, 28.0 * nh,
+       launch_adamw(nh, m->master + th.off, grads + th.off, m->adam_m + ne, m->adam_v + ne,
+                    oc->unembedding_lr * lr_mult, oc->beta1, oc->beta2, oc->adam_eps, oc->weight_decay, m->opt_t,
+                    st));
+  return NC_OK;
+}
+
+static int64_t align_up(int64_t b) { return (b + 255) & ~(int64_t)255; }
+
+extern "C" size_t nc_newton_schulz_workspace_bytes(int32_t dtype, int32_t rows, int32_t cols) {
+  if (!dtype_ok(dtype) || rows <= 0 || cols <= 0) return 0;
+  const int64_t rc = (int64_t)rows * cols, n = std::min(rows, cols);
+  const int64_t act = dtype == NC_BF16 ? 2 : 4;
+  const int64_t nchunks = (rc + OPT_CHUNK - 1) / OPT_CHUNK;
+  return (size_t)(align_up(nchunks * 4) + align_up(4) + 2 * align_up(rc * 4) + 3 * align_up(rc * act) +
+                  2 * align_up(n * n * act));
+}
+
+extern "C" nc_status nc_op_newton_schulz(int32_t dtype, int32_t rows, int32_t cols, int32_t steps, const float* u,
+                                         float* x, void* workspace, void* stream) {
+  if (!dtype_ok(dtype) || rows <= 0 || cols <= 0 || steps < 0 || steps > 64 || !u || !x || !workspace)
+    return NC_ERR_ARG;
+  if ((((uintptr_t)workspace) & 255)) return NC_ERR_ARG;
+  cudaStream_t st = as_stream(stream);
+  const int64_t rc = (int64_t)rows * cols, n = std::min(rows, cols);
+  const int64_t act = dtype == NC_BF16 ? 2 : 4;
+  uint8_t* p = (uint8_t*)workspace;
+  OptTensors tl;
+  const int64_t off0 = 0;
+  opt_fill(&tl, &off0, &rc, 1);
+  float* partial = (float*)p; p += align_up((int64_t)tl.chunk0[1] * 4);
+  tl.norm = (float*)p; p += align_up(4);
+  float* mom = (float*)p; p += align_up(rc * 4);
+  float* uu = (float*)p; p += align_up(rc * 4);
+  void* x0 = p; p += align_up(rc * act);
+  void* ping0 = p; p += align_up(rc * act);
+  void* ping1 = p; p += align_up(rc * act);
+  void* A = p; p += align_up(n * n * act);
+  void* A2 = p;
+  // momentum 0 from a zero buffer gives U = u; this also forms ||u||_F
+  NC_CUDA_TRY(cudaMemsetAsync(mom, 0, (size_t)rc * 4, st));
+  NC_TRY(launch_muon_momentum(tl, u, mom, uu, 0.f, 0, partial, st));
+  NC_TRY(launch_ns_init(dtype, tl, uu, 1e-7f, x0, st));
+  const void* out = x0;
+  if (steps > 0)
+    NC_TRY(newton_schulz_run(dtype, rows, cols, steps, x0, ping0, ping1, A, A2, &out, nullptr, nullptr, 0, st));
+  return launch_cast_out(dtype, rc, out, x, st);
+}

@@ -77,3 +77,36 @@ bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64
 // {box_inner, box_mid, 1}, 128-byte swizzle; stores are clipped at d1.
 bool make_tmap_bf16_3d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t d1, uint64_t d2, int64_t ld,
                        uint32_t box_inner, uint32_t box_mid);
+
+// ---------------------------------------------------------------- optimizer (k_optim.cu)
+extern int g_num_sms;
+// The weight matrices one Muon launch covers, passed by value as a kernel
+// parameter.  Block b works on chunk b - chunk0[t] of tensor t, where
+// chunk0[t] <= b < chunk0[t + 1]; each chunk is OPT_CHUNK elements.
+#define NC_OPT_MAXT 384
+#define OPT_CHUNK 16384
+struct OptTensors {
+  int32_t n;
+  int32_t chunk0[NC_OPT_MAXT + 1];
+  int64_t off[NC_OPT_MAXT];    // element offset in the packed parameter / gradient vectors
+  int64_t soff[NC_OPT_MAXT];   // element offset in the optimizer's state buffers
+  int64_t len[NC_OPT_MAXT];    // elements
+  float* norm;                 // device [n]: ||U||_F per tensor (written by launch_muon_momentum)
+};
+// M <- mu M + G; U = nesterov ? G + mu M : M; then tl.norm[t] = ||U_t||_F.
+// partial: one float per chunk.
+nc_status launch_muon_momentum(const OptTensors& tl, const float* G, float* M, float* U, float mu, int nesterov,
+                               float* partial, cudaStream_t st);
+// X = U / (norm + eps) in the compute dtype.
+nc_status launch_ns_init(int dtype, const OptTensors& tl, const float* U, float eps, void* X, cudaStream_t st);
+// `steps` Newton-Schulz iterations on X0[rows, cols]; the result is left in ping0
+// or ping1 (*out).  A and A2 hold min(rows, cols)^2 elements.
+nc_status newton_schulz_run(int dtype, int rows, int cols, int steps, const void* x0, void* ping0, void* ping1,
+                            void* A, void* A2, const void** out, int32_t* err, void* gemm_ws, size_t gemm_ws_bytes,
+                            cudaStream_t st);
+// W <- W - lr X (n elements, X in the compute dtype).
+nc_status launch_muon_apply(int dtype, int64_t n, float* W, const void* X, float lr, cudaStream_t st);
+nc_status launch_cast_out(int dtype, int64_t n, const void* X, float* out, cudaStream_t st);
+// One bias-corrected AdamW step (t >= 1) with decoupled weight decay.
+nc_status launch_adamw(int64_t n, float* W, const float* G, float* m, float* v, float lr, float b1, float b2,
+                       float eps, float wd, int64_t t, cudaStream_t st);

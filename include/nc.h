@@ -310,7 +310,10 @@ enum { NC_PROF_GEMM = 0, NC_PROF_ATTN_FWD = 1, NC_PROF_ATTN_BWD = 2, NC_PROF_NOR
        NC_PROF_OTHER = 8,
        /* sub-classes of NC_PROF_GEMM (each GEMM is counted in one of these too) */
        NC_PROF_GEMM_FWD = 9, NC_PROF_GEMM_DX = 10, NC_PROF_GEMM_DW = 11, NC_PROF_GEMM_LM = 12,
-       NC_PROF_CLASSES = 13 };
+       /* nc_optimizer_step: the Newton-Schulz products of each matrix, and the
+          elementwise kernels (momentum and norms, scaling, Muon apply, AdamW) */
+       NC_PROF_OPT_NS = 13, NC_PROF_OPT_EW = 14,
+       NC_PROF_CLASSES = 15 };
 nc_status nc_profile_enable(nc_model* m, int32_t on);
 nc_status nc_profile_read(nc_model* m, int32_t cls, double* ms, int64_t* launches,
                           double* flops, double* bytes);
@@ -329,6 +332,62 @@ void nc_debug_set_wait_limit_ns(uint64_t ns);
  * not split K run on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2).  Both
  * compute the same sums; the switch exists to test and time either path. */
 void nc_debug_set_gemm_pair(int32_t on);
+
+/* ------------------------------------------------------------------------
+ * Optimizer step (cosmicrealm "noao-chat-0-项目总体介绍" §2.2 and §4.2;
+ * woshipm nanochat analysis §六.1): the weight matrices (every Wq, Wk, Wv,
+ * Wo, Wfc, Wproj) are updated by Muon, wte and lm_head by AdamW.  The pages
+ * name the method and the learning rates; the constants below are those of the
+ * published methods (Muon: Jordan et al. 2024; AdamW: Loshchilov & Hutter).
+ *
+ * Muon, per matrix W[rows, cols] with gradient G and momentum buffer M:
+ *   M <- momentum M + G;  U = G + momentum M (nesterov) or M;
+ *   X = U / (||U||_F + 1e-7), then ns_steps times X <- a X + (b A + c A^2) X
+ *   with A = X X^T ((a, b, c) = (3.4445, -4.7750, 2.0315); a tall matrix is
+ *   iterated as X <- a X + X (b A + c A^2) with A = X^T X, the same map);
+ *   W <- W - lr_mult * matrix_lr * sqrt(max(1, rows/cols)) * X.
+ *   The iteration runs in the model's compute dtype (bf16 products with fp32
+ *   accumulation in NC_BF16 mode).
+ * AdamW, per element of wte (lr = embedding_lr) and lm_head (unembedding_lr):
+ *   m <- b1 m + (1-b1) g;  v <- b2 v + (1-b2) g^2;
+ *   W <- W - lr_mult * lr * (m/(1-b1^t) / (sqrt(v/(1-b2^t)) + eps) + wd W),
+ *   t = the number of steps taken, counting this one.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  float matrix_lr;       /* Muon learning rate (0.02)                          */
+  float embedding_lr;    /* AdamW learning rate of wte (0.2)                   */
+  float unembedding_lr;  /* AdamW learning rate of lm_head (0.004)             */
+  float momentum;        /* Muon momentum in [0, 1) (0.95)                     */
+  int32_t nesterov;      /* nonzero: the Nesterov form above (1)               */
+  int32_t ns_steps;      /* Newton-Schulz iterations, 0..64 (5)                */
+  float beta1, beta2;    /* AdamW moment decay rates in [0, 1) (0.9, 0.999)    */
+  float adam_eps;        /* > 0 (1e-8)                                         */
+  float weight_decay;    /* AdamW decoupled weight decay (0)                   */
+} nc_optim_config;
+/* Fill *oc with the defaults in parentheses above. */
+void nc_optim_config_default(nc_optim_config* oc);
+/* Apply one optimizer step to the model's fp32 master weights, given the
+ * packed fp32 gradient `grads` (device, the layout of nc_forward_backward's
+ * output); lr_mult (the caller's schedule value, e.g. warmup + cosine) scales
+ * every learning rate.  The first call allocates the optimizer state on the
+ * device and zeroes it; the state lives with the model.  Enqueued on `stream`
+ * without synchronising; a bounded-wait timeout in a GEMM is reported by the
+ * next call that reads the device error flag.  NC_ERR_ARG for NULL pointers or
+ * out-of-range settings, NC_ERR_ALLOC if the state does not fit, and
+ * NC_ERR_UNSUPPORTED for more than 384 weight matrices. */
+nc_status nc_optimizer_step(nc_model* m, const nc_optim_config* oc, const float* grads,
+                            float lr_mult, void* stream);
+/* Zero the momentum and Adam moments and the step count. */
+nc_status nc_optimizer_reset(nc_model* m, void* stream);
+/* Optimizer steps taken since creation or the last reset (-1 for NULL). */
+int64_t nc_optimizer_steps(const nc_model* m);
+/* The orthogonalisation above on its own: x (float [rows, cols]) = `steps`
+ * Newton-Schulz iterations from u / (||u||_F + 1e-7), computed in `dtype`.
+ * workspace: nc_newton_schulz_workspace_bytes(dtype, rows, cols) bytes,
+ * 256-byte aligned.  NC_BF16 needs rows, cols multiples of 8. */
+size_t nc_newton_schulz_workspace_bytes(int32_t dtype, int32_t rows, int32_t cols);
+nc_status nc_op_newton_schulz(int32_t dtype, int32_t rows, int32_t cols, int32_t steps,
+                              const float* u, float* x, void* workspace, void* stream);
 
 #ifdef __cplusplus
 }
