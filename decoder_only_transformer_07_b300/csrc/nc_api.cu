@@ -66,8 +66,18 @@ struct nc_model {
   int64_t opt_t = 0;                 // optimizer steps taken
   OptTensors* opt_tl = nullptr;      // the Muon matrices (host copy of the kernel parameter)
   float *opt_mom = nullptr, *opt_u = nullptr, *opt_partial = nullptr, *opt_norm = nullptr;
-  void *opt_x0 = nullptr, *opt_ping0 = nullptr, *opt_ping1 = nullptr, *opt_a = nullptr, *opt_a2 = nullptr;
+  void* opt_x0 = nullptr;
   float *adam_m = nullptr, *adam_v = nullptr;   // [wte | lm_head] moments
+  // The matrices' Newton-Schulz iterations are independent: they run on
+  // NC_OPT_STREAMS side streams (fork / join through events on the caller's
+  // stream), each with its own ping-pong and A buffers; matrices are assigned
+  // largest first to the least-loaded stream.
+  static constexpr int NC_OPT_STREAMS = 4;
+  cudaStream_t opt_st[NC_OPT_STREAMS] = {};
+  cudaEvent_t opt_fork = nullptr, opt_join[NC_OPT_STREAMS] = {};
+  void *opt_ping0[NC_OPT_STREAMS] = {}, *opt_ping1[NC_OPT_STREAMS] = {};
+  void *opt_a[NC_OPT_STREAMS] = {}, *opt_a2[NC_OPT_STREAMS] = {};
+  std::vector<int> opt_order, opt_lane;    // matrices by decreasing work, and each one's stream
   // profiling (nc_profile_enable)
   struct Rec { int cls, sub; int ev; double flops, bytes; };
   bool prof_on = false;
@@ -319,6 +329,11 @@ extern "C" void nc_model_destroy(nc_model* m) {
   for (void* p : m->allocs) cudaFree(p);
   if (m->result_host) cudaFreeHost(m->result_host);
   delete m->opt_tl;
+  for (int k = 0; k < nc_model::NC_OPT_STREAMS; ++k) {
+    if (m->opt_st[k]) cudaStreamDestroy(m->opt_st[k]);
+    if (m->opt_join[k]) cudaEventDestroy(m->opt_join[k]);
+  }
+  if (m->opt_fork) cudaEventDestroy(m->opt_fork);
   delete m;
 }
 
@@ -811,12 +826,36 @@ static nc_status opt_alloc(nc_model* m) {
   NC_TRY(dalloc_t(m, (size_t)std::max<int64_t>(nchunks, 1), &m->opt_partial));
   NC_TRY(dalloc_t(m, (size_t)nm, &m->opt_norm));
   NC_TRY(dalloc(m, (size_t)total * m->act, &m->opt_x0));
-  NC_TRY(dalloc(m, (size_t)maxrc * m->act, &m->opt_ping0));
-  NC_TRY(dalloc(m, (size_t)maxrc * m->act, &m->opt_ping1));
-  NC_TRY(dalloc(m, (size_t)(maxn * maxn) * m->act, &m->opt_a));
-  NC_TRY(dalloc(m, (size_t)(maxn * maxn) * m->act, &m->opt_a2));
+  for (int k = 0; k < nc_model::NC_OPT_STREAMS; ++k) {
+    NC_TRY(dalloc(m, (size_t)maxrc * m->act, &m->opt_ping0[k]));
+    NC_TRY(dalloc(m, (size_t)maxrc * m->act, &m->opt_ping1[k]));
+    NC_TRY(dalloc(m, (size_t)(maxn * maxn) * m->act, &m->opt_a[k]));
+    NC_TRY(dalloc(m, (size_t)(maxn * maxn) * m->act, &m->opt_a2[k]));
+    NC_CUDA_TRY(cudaStreamCreateWithFlags(&m->opt_st[k], cudaStreamNonBlocking));
+    NC_CUDA_TRY(cudaEventCreateWithFlags(&m->opt_join[k], cudaEventDisableTiming));
+  }
+  NC_CUDA_TRY(cudaEventCreateWithFlags(&m->opt_fork, cudaEventDisableTiming));
   NC_TRY(dalloc_t(m, (size_t)na, &m->adam_m));
   NC_TRY(dalloc_t(m, (size_t)na, &m->adam_v));
+  // longest-processing-time-first assignment of matrices to the side streams
+  std::vector<double> work(nm);
+  for (int i = 0; i < nm; ++i) {
+    const ParamTensor& t = m->layout[1 + i];
+    const double n = (double)std::min(t.rows, t.cols), k = (double)std::max(t.rows, t.cols);
+    work[i] = 4.0 * n * n * k + 2.0 * n * n * n;
+  }
+  m->opt_order.resize(nm);
+  m->opt_lane.assign(nm, 0);
+  for (int i = 0; i < nm; ++i) m->opt_order[i] = i;
+  std::stable_sort(m->opt_order.begin(), m->opt_order.end(), [&](int a, int b) { return work[a] > work[b]; });
+  double load[nc_model::NC_OPT_STREAMS] = {};
+  for (int i : m->opt_order) {
+    int best = 0;
+    for (int k = 1; k < nc_model::NC_OPT_STREAMS; ++k)
+      if (load[k] < load[best]) best = k;
+    m->opt_lane[i] = best;
+    load[best] += work[i];
+  }
   m->opt_tl->norm = m->opt_norm;
   m->opt_ready = true;
   return NC_OK;
@@ -839,6 +878,36 @@ extern "C" nc_status nc_optimizer_reset(nc_model* m, void* stream) {
 
 extern "C" int64_t nc_optimizer_steps(const nc_model* m) { return m ? m->opt_t : -1; }
 
+// Newton-Schulz + apply for every matrix, forked onto the side streams and
+// joined back into `st`.  No split-K workspace: the side streams run
+// concurrently and must not share one.
+static nc_status opt_matrices(nc_model* m, const nc_optim_config* oc, float lr_mult, cudaStream_t st) {
+  const OptTensors& tl = *m->opt_tl;
+  NC_CUDA_TRY(cudaEventRecord(m->opt_fork, st));
+  for (int k = 0; k < nc_model::NC_OPT_STREAMS; ++k) NC_CUDA_TRY(cudaStreamWaitEvent(m->opt_st[k], m->opt_fork, 0));
+  nc_status s = NC_OK;
+  for (int i : m->opt_order) {
+    const ParamTensor& t = m->layout[1 + i];
+    const int k = m->opt_lane[i];
+    cudaStream_t sk = m->opt_st[k];
+    const void* x = (const uint8_t*)m->opt_x0 + tl.soff[i] * m->act;
+    if (oc->ns_steps > 0)
+      s = newton_schulz_run(m->dtype, (int)t.rows, (int)t.cols, oc->ns_steps, x, m->opt_ping0[k], m->opt_ping1[k],
+                            m->opt_a[k], m->opt_a2[k], &x, m->err, nullptr, 0, sk);
+    if (s != NC_OK) break;
+    const float scale = sqrtf(std::max(1.f, (float)t.rows / (float)t.cols));
+    s = launch_muon_apply(m->dtype, t.rows * t.cols, m->master + t.off, x, oc->matrix_lr * lr_mult * scale, sk);
+    if (s != NC_OK) break;
+  }
+  // always join, so that `st` orders after everything already enqueued on the side streams
+  for (int k = 0; k < nc_model::NC_OPT_STREAMS; ++k) {
+    if (cudaEventRecord(m->opt_join[k], m->opt_st[k]) != cudaSuccess ||
+        cudaStreamWaitEvent(st, m->opt_join[k], 0) != cudaSuccess)
+      s = NC_ERR_CUDA;
+  }
+  return s;
+}
+
 extern "C" nc_status nc_optimizer_step(nc_model* m, const nc_optim_config* oc, const float* grads, float lr_mult,
                                        void* stream) {
   if (!m || !oc || !grads) return NC_ERR_ARG;
@@ -859,19 +928,15 @@ extern "C" nc_status nc_optimizer_step(nc_model* m, const nc_optim_config* oc, c
   PROF(NC_PROF_OPT_EW, 0, 16.0 * total,
        launch_muon_momentum(tl, grads, m->opt_mom, m->opt_u, oc->momentum, oc->nesterov, m->opt_partial, st));
   PROF(NC_PROF_OPT_EW, 0, (4.0 + act) * total, launch_ns_init(m->dtype, tl, m->opt_u, 1e-7f, m->opt_x0, st));
+  // per matrix: Newton-Schulz and the apply, on the side streams (profiled as one phase)
+  double ns_flops = 0.0, ns_bytes = 0.0;
   for (int i = 0; i < tl.n; ++i) {
     const ParamTensor& t = m->layout[1 + i];
-    const void* x = (const uint8_t*)m->opt_x0 + tl.soff[i] * m->act;
     const double n = (double)std::min(t.rows, t.cols), k = (double)std::max(t.rows, t.cols);
-    if (oc->ns_steps > 0)
-      PROF(NC_PROF_OPT_NS, oc->ns_steps * (4.0 * n * n * k + 2.0 * n * n * n),
-           oc->ns_steps * (4.0 * n * k + 4.0 * n * n) * act,
-           newton_schulz_run(m->dtype, (int)t.rows, (int)t.cols, oc->ns_steps, x, m->opt_ping0, m->opt_ping1,
-                             m->opt_a, m->opt_a2, &x, m->err, m->gemm_ws, m->gemm_ws_bytes, st));
-    const float scale = sqrtf(std::max(1.f, (float)t.rows / (float)t.cols));
-    PROF(NC_PROF_OPT_EW, 0, (8.0 + act) * t.rows * t.cols,
-         launch_muon_apply(m->dtype, t.rows * t.cols, m->master + t.off, x, oc->matrix_lr * lr_mult * scale, st));
+    ns_flops += oc->ns_steps * (4.0 * n * n * k + 2.0 * n * n * n);
+    ns_bytes += oc->ns_steps * (4.0 * n * k + 4.0 * n * n) * act + (8.0 + act) * n * k;
   }
+  PROF(NC_PROF_OPT_NS, ns_flops, ns_bytes, opt_matrices(m, oc, lr_mult, st));
   // AdamW on the embedding and the output head
   const ParamTensor& te = m->layout.front();
   const ParamTensor& th = m->layout.back();

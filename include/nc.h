@@ -310,8 +310,9 @@ enum { NC_PROF_GEMM = 0, NC_PROF_ATTN_FWD = 1, NC_PROF_ATTN_BWD = 2, NC_PROF_NOR
        NC_PROF_OTHER = 8,
        /* sub-classes of NC_PROF_GEMM (each GEMM is counted in one of these too) */
        NC_PROF_GEMM_FWD = 9, NC_PROF_GEMM_DX = 10, NC_PROF_GEMM_DW = 11, NC_PROF_GEMM_LM = 12,
-       /* nc_optimizer_step: the Newton-Schulz products of each matrix, and the
-          elementwise kernels (momentum and norms, scaling, Muon apply, AdamW) */
+       /* nc_optimizer_step: the matrices' Newton-Schulz iterations and Muon
+          applies (concurrent on side streams, timed as one phase), and the
+          elementwise kernels (momentum and norms, scaling, AdamW) */
        NC_PROF_OPT_NS = 13, NC_PROF_OPT_EW = 14,
        NC_PROF_CLASSES = 15 };
 nc_status nc_profile_enable(nc_model* m, int32_t on);
