@@ -63,6 +63,7 @@ _SIGS = {
     "nc_set_params": (_i32, [_p, _p, _p]),
     "nc_forward_backward": (_i32, [_p, _p, _p, _i32, _i32, ctypes.POINTER(_f32), _p, _p]),
     "nc_forward_backward_host": (_i32, [_p, _p, _p, _i32, _i32, ctypes.POINTER(_f32), _p, _p]),
+    "nc_forward_backward_accumulate": (_i32, [_p, _p, _p, _i32, _i32, _f32, _i32, ctypes.POINTER(_f32), _p, _p]),
     "nc_forward_logits": (_i32, [_p, _p, _i32, _i32, _p, _p]),
     "nc_forward_row_losses": (_i32, [_p, _p, _p, _i32, _i32, _p, _p]),
     "nc_last_error": (_i32, [_p, _p]),
@@ -209,6 +210,15 @@ class Model:
         _check(_lib.nc_forward_backward(self._h, _ptr(tokens), _ptr(targets), B, T, ctypes.byref(loss),
                                         _ptr(grads), _stream()), "nc_forward_backward")
         return loss.value, grads
+
+    def forward_backward_accumulate(self, tokens, targets, grads, grad_scale=1.0, accumulate=True):
+        """grads (+)= grad_scale * d(mean CE of this micro-batch)/d(params).  Returns the loss."""
+        B, T = tokens.shape
+        loss = _f32()
+        _check(_lib.nc_forward_backward_accumulate(self._h, _ptr(tokens), _ptr(targets), B, T, grad_scale,
+                                                   1 if accumulate else 0, ctypes.byref(loss), _ptr(grads),
+                                                   _stream()), "nc_forward_backward_accumulate")
+        return loss.value
 
     def forward_backward_host(self, tokens, targets, grads):
         """tokens, targets: int32 host (pinned) tensors [B, T]."""

@@ -185,20 +185,29 @@ __global__ void k_emb_bwd_list(EmbScratch s) {
   s.list[s.offs[v] + pos] = (int)(base + r);
 }
 
-__global__ void __launch_bounds__(256) k_emb_bwd_rows(int V, int C, EmbScratch s, float* __restrict__ dwte) {
+__global__ void __launch_bounds__(256) k_emb_bwd_rows(int V, int C, EmbScratch s, float* __restrict__ dwte,
+                                                      int accumulate) {
   __shared__ int slots[EMB_MAX_CHUNKS];
   const int v = blockIdx.x;
   const int cnt = s.count[v];
   float4* dst = reinterpret_cast<float4*>(dwte + (int64_t)v * C);
   const int C4 = C / 4;
   if (cnt == 0) {
-    for (int c = threadIdx.x; c < C4; c += blockDim.x) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!accumulate)
+      for (int c = threadIdx.x; c < C4; c += blockDim.x) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
+  auto put = [&](int c, float4 v4) {
+    if (accumulate) {
+      const float4 d = dst[c];
+      v4.x += d.x; v4.y += d.y; v4.z += d.z; v4.w += d.w;
+    }
+    dst[c] = v4;
+  };
   const int o = s.offs[v];
   if (cnt == 1) {
     const float4* src = reinterpret_cast<const float4*>(s.partial + (int64_t)s.list[o] * C);
-    for (int c = threadIdx.x; c < C4; c += blockDim.x) dst[c] = src[c];
+    for (int c = threadIdx.x; c < C4; c += blockDim.x) put(c, src[c]);
     return;
   }
   int len = 1;
@@ -211,12 +220,12 @@ __global__ void __launch_bounds__(256) k_emb_bwd_rows(int V, int C, EmbScratch s
       float4 p = reinterpret_cast<const float4*>(s.partial + (int64_t)slots[k] * C)[c];
       acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
     }
-    dst[c] = acc;
+    put(c, acc);
   }
 }
 
 nc_status launch_embed_bwd(int64_t n, int C, int V, const int32_t* tokens, const float* dx,
-                           float* dwte, void* scratch, cudaStream_t st) {
+                           float* dwte, void* scratch, cudaStream_t st, int accumulate) {
   if (C % 4 || C > 4 * EMB_MAXV4 * EMB_CH || V <= 0) return NC_ERR_ARG;
   int64_t nchunks = (n + EMB_CH - 1) / EMB_CH;
   if (nchunks > EMB_MAX_CHUNKS) return NC_ERR_UNSUPPORTED;
@@ -234,7 +243,7 @@ nc_status launch_embed_bwd(int64_t n, int C, int V, const int32_t* tokens, const
     k_emb_bwd_list<<<(unsigned)nchunks, EMB_CH, 0, st>>>(s);
     NC_CUDA_TRY(cudaGetLastError());
   }
-  k_emb_bwd_rows<<<V, 256, 0, st>>>(V, C, s, dwte);
+  k_emb_bwd_rows<<<V, 256, 0, st>>>(V, C, s, dwte, accumulate);
   NC_CUDA_TRY(cudaGetLastError());
   return NC_OK;
 }

@@ -9,6 +9,7 @@
 // kernels, and the embedding scatter.  The only synchronisation is the final
 // read of the loss and the device error flag.
 #include <algorithm>
+#include <cmath>
 #include <cfloat>
 #include <cstdio>
 #include <cstring>
@@ -489,7 +490,10 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
   return NC_OK;
 }
 
-static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int T, float* grads, cudaStream_t st) {
+// accumulate: the weight gradients are added to `grads` instead of stored.
+static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int T, float* grads, bool accumulate,
+                                 cudaStream_t st) {
+  const int gw = accumulate ? NC_EP_ACCUM_F32 : NC_EP_STORE_F32;
   const int64_t N = (int64_t)B * T;
   const int C = m->C, F = m->F, Hd = m->H * m->hd, W = m->qkvw;
   const int n = (int)N;
@@ -510,15 +514,15 @@ static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int 
     const ParamTensor &tq = tensor(m, l, 0), &to = tensor(m, l, 3), &tfc = tensor(m, l, 4),
                       &tpj = tensor(m, l, 5);
     // MLP: x2 = x1 + relu(xn2 Wfc^T)^2 Wproj^T
-    NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, F, n, m->dx_act, C, 0, h, F, 0, NC_EP_STORE_F32, grads + tpj.off, F, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, F, n, m->dx_act, C, 0, h, F, 0, gw, grads + tpj.off, F, nullptr, 0, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, F, C, m->dx_act, C, 1, wptr(m, tpj), F, 0, NC_EP_RELU2_SQ_BWD, m->du, F, h, F, st));
-    NC_TRY(gemm(m, NC_PROF_GEMM_DW, F, C, n, m->du, F, 0, xn2, C, 0, NC_EP_STORE_F32, grads + tfc.off, C, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_DW, F, C, n, m->du, F, 0, xn2, C, 0, gw, grads + tfc.off, C, nullptr, 0, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, C, F, m->du, F, 1, wptr(m, tfc), C, 0, NC_EP_STORE_F32, m->dxn, C, nullptr, 0, st));
     PROF(NC_PROF_NORM, 0, nb_by,
          launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, xn2, rstd2, m->dx, m->dtype == NC_BF16 ? m->dx_act : nullptr,
                             st));
     // attention: x1 = x + o Wo^T
-    NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, Hd, n, m->dx_act, C, 0, o, Hd, 0, NC_EP_STORE_F32, grads + to.off, Hd, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, Hd, n, m->dx_act, C, 0, o, Hd, 0, gw, grads + to.off, Hd, nullptr, 0, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, Hd, C, m->dx_act, C, 1, wptr(m, to), Hd, 0, NC_EP_STORE, m->dout, Hd, nullptr, 0, st));
     if (m->dtype == NC_BF16) {
       // attention backward with the q/k RMSNorm + RoPE backward in its output epilogue
@@ -532,7 +536,7 @@ static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int 
       PROF(NC_PROF_ROPE, 0, (double)N * nh * (3.0 * a * m->hd + 4),
            launch_rope_qknorm_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, m->dqkv, qkv, rstdqk, m->rope_tab, st));
     }
-    NC_TRY(gemm(m, NC_PROF_GEMM_DW, W, C, n, m->dqkv, W, 0, xn1, C, 0, NC_EP_STORE_F32, grads + tq.off, C, nullptr, 0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_DW, W, C, n, m->dqkv, W, 0, xn1, C, 0, gw, grads + tq.off, C, nullptr, 0, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, C, W, m->dqkv, W, 1, wptr(m, tq), C, 0, NC_EP_STORE_F32, m->dxn, C, nullptr, 0, st));
     PROF(NC_PROF_NORM, 0, nb_by,
          launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, xn1, rstd1, m->dx, m->dtype == NC_BF16 ? m->dx_act : nullptr,
@@ -541,13 +545,15 @@ static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int 
   }
   const ParamTensor& te = m->layout[0];
   PROF(NC_PROF_EMBED, 0, 4.0 * N * C + 4.0 * m->V * C,
-       launch_embed_bwd(N, C, m->V, tokens, m->dx, grads + te.off, m->emb_scratch, st));
+       launch_embed_bwd(N, C, m->V, tokens, m->dx, grads + te.off, m->emb_scratch, st, accumulate ? 1 : 0));
   m->launches += 4;
   return NC_OK;
 }
 
+// grads = (accumulate ? grads : 0) + gscale * d(mean CE)/d(params); the scale
+// enters through the cross-entropy gradient, which every gradient is linear in.
 static nc_status step(nc_model* m, const int32_t* tokens, const int32_t* targets, int B, int T, float* loss_host,
-                      float* grads, cudaStream_t st) {
+                      float* grads, float gscale, bool accumulate, cudaStream_t st) {
   const int64_t N = (int64_t)B * T;
   const int C = m->C, V = m->V;
   m->launches = 0;
@@ -556,7 +562,7 @@ static nc_status step(nc_model* m, const int32_t* tokens, const int32_t* targets
   const ParamTensor& tl = m->layout.back();
   const void* Wlm = wptr(m, tl);
   NC_CUDA_TRY(cudaMemsetAsync(m->dx, 0, (size_t)N * C * sizeof(float), st));
-  const float scale = 1.f / (float)N;
+  const float scale = gscale / (float)N;
   for (int64_t c0 = 0; c0 < N; c0 += m->chunk_rows) {
     const int nc = (int)std::min<int64_t>(m->chunk_rows, N - c0);
     const void* xfc = (const uint8_t*)m->xf + (size_t)c0 * C * m->act;
@@ -564,7 +570,8 @@ static nc_status step(nc_model* m, const int32_t* tokens, const int32_t* targets
     PROF(NC_PROF_CE, 0, (double)nc * (2.0 * V * m->act + 8),
          launch_cross_entropy(m->dtype, nc, V, m->logits, V, targets + c0, m->rowloss + c0, scale, m->err, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_LM, nc, C, V, m->logits, V, 1, Wlm, C, 0, NC_EP_STORE_F32, m->dxn + c0 * C, C, nullptr, 0, st));
-    NC_TRY(gemm(m, NC_PROF_GEMM_LM, V, C, nc, m->logits, V, 0, xfc, C, 0, c0 == 0 ? NC_EP_STORE_F32 : NC_EP_ACCUM_F32,
+    NC_TRY(gemm(m, NC_PROF_GEMM_LM, V, C, nc, m->logits, V, 0, xfc, C, 0,
+                (c0 == 0 && !accumulate) ? NC_EP_STORE_F32 : NC_EP_ACCUM_F32,
                 grads + tl.off, C, nullptr, 0, st));
     m->launches += 1;
   }
@@ -572,7 +579,7 @@ static nc_status step(nc_model* m, const int32_t* tokens, const int32_t* targets
        launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, m->xf, m->rstd_f, m->dx, m->dtype == NC_BF16 ? m->dx_act : nullptr,
                           st));
   m->launches += 1;
-  NC_TRY(backward_layers(m, tokens, B, T, grads, st));
+  NC_TRY(backward_layers(m, tokens, B, T, grads, accumulate, st));
   PROF(NC_PROF_OTHER, 0, 4.0 * N, launch_mean(N, m->rowloss, m->result, st));
   m->launches += 1;
   NC_CUDA_TRY(cudaMemcpyAsync(m->result_host, m->result, 4, cudaMemcpyDeviceToHost, st));
@@ -585,7 +592,15 @@ extern "C" nc_status nc_forward_backward(nc_model* m, const int32_t* tokens, con
                                          int32_t T, float* loss_host, float* grads, void* stream) {
   if (!m || !tokens || !targets || !loss_host || !grads) return NC_ERR_ARG;
   NC_TRY(check_bt(m, B, T));
-  return step(m, tokens, targets, B, T, loss_host, grads, as_stream(stream));
+  return step(m, tokens, targets, B, T, loss_host, grads, 1.f, false, as_stream(stream));
+}
+
+extern "C" nc_status nc_forward_backward_accumulate(nc_model* m, const int32_t* tokens, const int32_t* targets,
+                                                    int32_t B, int32_t T, float grad_scale, int32_t accumulate,
+                                                    float* loss_host, float* grads, void* stream) {
+  if (!m || !tokens || !targets || !loss_host || !grads || !std::isfinite(grad_scale)) return NC_ERR_ARG;
+  NC_TRY(check_bt(m, B, T));
+  return step(m, tokens, targets, B, T, loss_host, grads, grad_scale, accumulate != 0, as_stream(stream));
 }
 
 extern "C" nc_status nc_forward_backward_host(nc_model* m, const int32_t* tokens_host, const int32_t* targets_host,
@@ -596,7 +611,7 @@ extern "C" nc_status nc_forward_backward_host(nc_model* m, const int32_t* tokens
   size_t bytes = (size_t)B * T * sizeof(int32_t);
   NC_CUDA_TRY(cudaMemcpyAsync(m->tok_dev, tokens_host, bytes, cudaMemcpyHostToDevice, st));
   NC_CUDA_TRY(cudaMemcpyAsync(m->tgt_dev, targets_host, bytes, cudaMemcpyHostToDevice, st));
-  return step(m, m->tok_dev, m->tgt_dev, B, T, loss_host, grads, st);
+  return step(m, m->tok_dev, m->tgt_dev, B, T, loss_host, grads, 1.f, false, st);
 }
 
 extern "C" nc_status nc_forward_logits(nc_model* m, const int32_t* tokens, int32_t B, int32_t T, float* logits,

@@ -119,6 +119,19 @@ nc_status nc_forward_backward(nc_model* m, const int32_t* tokens_dev,
                               const int32_t* targets_dev, int32_t B, int32_t T,
                               float* loss_host, float* grads_dev, void* stream);
 
+/* The step for gradient accumulation over micro-batches (cosmicrealm
+ * "noao-chat-0-项目总体介绍" §4.3: several forward + backward passes, then
+ * one optimizer step): grads_dev = (accumulate ? grads_dev : 0) +
+ * grad_scale * d(loss)/d(weights), loss being this call's mean cross-entropy
+ * (written to loss_host unscaled).  With grad_scale = 1/k and accumulate set
+ * on all but the first of k equal micro-batches, grads_dev ends as the
+ * gradient of the mean loss over all of them.  grad_scale must be finite.
+ * nc_forward_backward is this call with grad_scale = 1, accumulate = 0. */
+nc_status nc_forward_backward_accumulate(nc_model* m, const int32_t* tokens_dev,
+                                         const int32_t* targets_dev, int32_t B, int32_t T,
+                                         float grad_scale, int32_t accumulate, float* loss_host,
+                                         float* grads_dev, void* stream);
+
 /* The same step with tokens and targets in (preferably pinned) host memory:
  * they are copied to the model's device buffers on `stream` first. */
 nc_status nc_forward_backward_host(nc_model* m, const int32_t* tokens_host,

@@ -8,6 +8,11 @@ Tolerances come from the arithmetic.
 * bf16 mode: every product is rounded to bf16 (fp32 accumulation).  A bf16
   emulation lands 0.8-1.3e-2 from fp64 with cosine >= 0.9999, so the bounds
   are 3e-2 and cosine >= 0.999.
+* A real model gradient is ill-conditioned (singular values spanning up to
+  ~1e11 at initialisation) and the iteration magnifies its small directions,
+  where the bf16 rounding lands: the same emulation on the oracle gradient of a
+  small model reaches cosine 0.9977-0.9995 per matrix, so that case is bounded
+  at 0.99.
 * AdamW is fp32 elementwise: 1e-5 of the step.
 Inputs are seeded host draws (weights N(0, 0.02), gradients standard normal);
 nothing the GPU computes feeds the oracle.
@@ -145,4 +150,27 @@ def test_optimizer_rejects_bad_settings():
     for bad in (dict(momentum=1.0), dict(beta2=1.5), dict(adam_eps=0.0), dict(ns_steps=-1)):
         with pytest.raises(nc.NcError):
             m.optimizer_step(g, nc.optim_config(**bad))
+    m.close()
+
+
+def test_optimizer_step_from_a_real_gradient_bf16():
+    """Muon on the ill-conditioned gradient of an actual batch (the oracle's)."""
+    from oracle import rng as OR
+    w = S.Workload("realgrad", 2, 256, 4, 2, 64, 1024, 1024, 128, 2, "bf16", "zipf")
+    cfg = OM.Config.from_workload(w)
+    params = OR.init_params(cfg, S.WEIGHT_SEED)
+    tok, tgt = S.batch_tokens(w)
+    _, G = OM.forward_backward(cfg, params.astype(np.float64), tok, tgt)
+    g32 = OM.pack(cfg, G).astype(np.float32)
+    m = nc.Model(nc.config_from_workload(w), seed=S.WEIGHT_SEED)
+    m.set_params(torch.from_numpy(params))
+    m.optimizer_step(torch.from_numpy(g32).cuda())
+    d_got = m.get_params().cpu().numpy().astype(np.float64) - params
+    d_ref = OO.optimizer_step(cfg, params.astype(np.float64), g32.astype(np.float64), OO.new_state(cfg)) - params
+    for name, r, c, off in m.layout:
+        a, b = d_got[off:off + r * c], d_ref[off:off + r * c]
+        if name in ("wte", "lm_head"):
+            assert np.max(np.abs(a - b)) <= 1e-5 * np.max(np.abs(b)), name
+        else:
+            assert _cos(a, b) > 0.99, (name, _cos(a, b))
     m.close()
