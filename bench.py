@@ -222,6 +222,50 @@ def run_optim(args):
     model.close()
 
 
+def run_decode(args):
+    """Decode mode: prefill --batch prompts of --seq tokens of the --config
+    model, then time --iters decode steps (one token per sequence each).
+    Decoding is memory-bound: every step reads each weight once (all but the
+    embedding table) and the whole key/value cache, which is the algorithmic
+    byte count the HBM roofline uses."""
+    import statistics
+    import numpy as np
+    import torch
+    import decoder_only_transformer_07_b300 as nc
+    torch.cuda.set_device(0)
+    w = S.workload(args.config)
+    B, T0, K = args.batch, args.seq, args.iters
+    model = nc.Model(nc.config_from_workload(w), seed=S.WEIGHT_SEED)
+    model.kv_cache_create(B, T0 + K + args.warmup + 1)
+    tok, _ = S.batch_tokens(w, batch=B, seq_len=T0 + K + args.warmup + 1)
+    dev = torch.from_numpy(tok).cuda()
+    model.prefill(dev[:, :T0].contiguous())
+    steps = [dev[:, T0 + j].contiguous() for j in range(K + args.warmup)]
+    for j in range(args.warmup):
+        model.decode_step(steps[j])
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for j in range(K):
+        model.decode_step(steps[args.warmup + j])
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    act = 2 if w.dtype == "bf16" else 4
+    n_w = model.n_params - w.vocab * w.n_embd
+    avg_len = T0 + args.warmup + (K + 1) / 2.0
+    kv_bytes = w.depth * B * w.n_kv_head * avg_len * w.head_dim * 2 * act
+    step_bytes = n_w * act + kv_bytes
+    _, _, hbm, kind = load_peaks()
+    gbs = step_bytes / (ms / 1e3) / 1e9
+    print(json.dumps({"op": "decode", "config": args.config, "batch": B, "prompt": T0, "steps": K,
+                      "ms_per_step": ms, "tokens_per_s": B / (ms / 1e3),
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                                   "peak_kind": kind, "bytes_per_step": step_bytes,
+                                   "kernel": "whole decode step (weights + KV cache read once)"}}), flush=True)
+    model.close()
+
+
 def run_op(args):
     """Single-kernel mode (for ncu captures of one kernel on a small case):
     times --iters launches of one GEMM or one attention forward+backward."""
@@ -287,7 +331,7 @@ def main():
     ap.add_argument("--step-batch", type=int, default=0,
                     help="profiling only: run the step at this batch size instead of the workload's")
     # single-op mode (profiling)
-    ap.add_argument("--op", choices=["gemm", "attn", "attn_fwd", "optim"])
+    ap.add_argument("--op", choices=["gemm", "attn", "attn_fwd", "optim", "decode"])
     ap.add_argument("--m", type=int, default=65536)
     ap.add_argument("--n", type=int, default=3840)
     ap.add_argument("--k", type=int, default=1280)
@@ -303,6 +347,8 @@ def main():
     args = ap.parse_args()
     if args.op == "optim":
         return run_optim(args)
+    if args.op == "decode":
+        return run_decode(args)
     if args.op:
         return run_op(args)
     w = S.workload(args.config, **({"batch": args.step_batch} if args.step_batch else {}))

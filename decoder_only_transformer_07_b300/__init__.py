@@ -86,6 +86,10 @@ _SIGS = {
     "nc_op_embed_fwd": (_i32, [_i32, _i64, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_embed_bwd_scratch_bytes": (_sz, [_i64, _i32, _i32]),
     "nc_optim_config_default": (None, [ctypes.POINTER(nc_optim_config)]),
+    "nc_kv_cache_create": (_i32, [_p, _i32, _i32]),
+    "nc_prefill": (_i32, [_p, _p, _i32, _i32, _p, _p]),
+    "nc_decode_step": (_i32, [_p, _p, _i32, _p, _p]),
+    "nc_kv_cache_length": (_i32, [_p]),
     "nc_optimizer_step": (_i32, [_p, ctypes.POINTER(nc_optim_config), _p, _f32, _p]),
     "nc_optimizer_reset": (_i32, [_p, _p]),
     "nc_optimizer_steps": (_i64, [_p]),
@@ -261,6 +265,30 @@ class Model:
 
     def optimizer_steps(self):
         return int(_lib.nc_optimizer_steps(self._h))
+
+    def kv_cache_create(self, max_batch, max_len):
+        _check(_lib.nc_kv_cache_create(self._h, max_batch, max_len), "nc_kv_cache_create")
+
+    def prefill(self, tokens, out=None):
+        """tokens: int32 CUDA [B, T].  Returns fp32 logits [B, V] of the last positions."""
+        import torch
+        B, T = tokens.shape
+        if out is None:
+            out = torch.empty((B, self.cfg.vocab), dtype=torch.float32, device="cuda")
+        _check(_lib.nc_prefill(self._h, _ptr(tokens), B, T, _ptr(out), _stream()), "nc_prefill")
+        return out
+
+    def decode_step(self, tokens, out=None):
+        """tokens: int32 CUDA [B] at the next position.  Returns fp32 logits [B, V]."""
+        import torch
+        B = tokens.shape[0]
+        if out is None:
+            out = torch.empty((B, self.cfg.vocab), dtype=torch.float32, device="cuda")
+        _check(_lib.nc_decode_step(self._h, _ptr(tokens), B, _ptr(out), _stream()), "nc_decode_step")
+        return out
+
+    def kv_cache_length(self):
+        return int(_lib.nc_kv_cache_length(self._h))
 
     def last_launch_count(self):
         return int(_lib.nc_last_launch_count(self._h))

@@ -79,6 +79,11 @@ struct nc_model {
   void *opt_ping0[NC_OPT_STREAMS] = {}, *opt_ping1[NC_OPT_STREAMS] = {};
   void *opt_a[NC_OPT_STREAMS] = {}, *opt_a2[NC_OPT_STREAMS] = {};
   std::vector<int> opt_order, opt_lane;    // matrices by decreasing work, and each one's stream
+  // key/value cache for incremental decoding (nc_kv_cache_create)
+  void *kcache = nullptr, *vcache = nullptr;   // per layer [kv_b][Hkv][kv_max][hd], compute dtype
+  float* dec_part = nullptr;                   // decode-attention partials
+  int kv_b = 0, kv_max = 0;                    // capacity
+  int kv_batch = 0, kv_len = 0;                // sequences and positions held
   // profiling (nc_profile_enable)
   struct Rec { int cls, sub; int ev; double flops, bytes; };
   bool prof_on = false;
@@ -1006,4 +1011,96 @@ extern "C" nc_status nc_op_newton_schulz(int32_t dtype, int32_t rows, int32_t co
   if (steps > 0)
     NC_TRY(newton_schulz_run(dtype, rows, cols, steps, x0, ping0, ping1, A, A2, &out, nullptr, nullptr, 0, st));
   return launch_cast_out(dtype, rc, out, x, st);
+}
+
+// ------------------------------------------------------------------ KV-cache decoding
+// Prefill runs the forward over B prompts and keeps every layer's (rotated,
+// normalised) keys and values; each decode step then feeds one token per
+// sequence at the next position: one row of every projection and one
+// attention row over the cache (woshipm nanochat analysis §三 item 4).
+
+static size_t kv_layer_elems(const nc_model* m) { return (size_t)m->kv_b * m->Hkv * m->kv_max * m->hd; }
+
+extern "C" nc_status nc_kv_cache_create(nc_model* m, int32_t max_batch, int32_t max_len) {
+  if (!m || max_batch < 1 || max_batch > m->Bmax || max_len < 1 || max_len > m->Tmax) return NC_ERR_ARG;
+  if ((m->hd != 64 && m->hd != 128) || (m->H / m->Hkv != 1 && m->H / m->Hkv != 2 && m->H / m->Hkv != 3 &&
+                                        m->H / m->Hkv != 4 && m->H / m->Hkv != 8))
+    return NC_ERR_UNSUPPORTED;
+  if (m->kcache && max_batch <= m->kv_b && max_len <= m->kv_max) {
+    m->kv_batch = m->kv_len = 0;
+    return NC_OK;
+  }
+  m->kv_b = max_batch;
+  m->kv_max = max_len;
+  const size_t n = kv_layer_elems(m) * m->L;
+  NC_TRY(dalloc(m, n * m->act, &m->kcache));
+  NC_TRY(dalloc(m, n * m->act, &m->vcache));
+  NC_TRY(dalloc_t(m, decode_part_floats(max_batch, m->H, m->hd, max_len), &m->dec_part));
+  m->kv_batch = m->kv_len = 0;
+  return NC_OK;
+}
+
+extern "C" int32_t nc_kv_cache_length(const nc_model* m) { return m ? m->kv_len : -1; }
+
+static void* kv_layer(const nc_model* m, void* base, int l) {
+  return (uint8_t*)base + kv_layer_elems(m) * l * m->act;
+}
+
+extern "C" nc_status nc_prefill(nc_model* m, const int32_t* tokens, int32_t B, int32_t T, float* logits,
+                                void* stream) {
+  if (!m || !tokens || !logits) return NC_ERR_ARG;
+  if (!m->kcache) return NC_ERR_ARG;
+  if (B < 1 || B > m->kv_b || T < 1 || T > m->kv_max) return NC_ERR_ARG;
+  cudaStream_t st = as_stream(stream);
+  m->launches = 0;
+  NC_TRY(forward_trunk(m, tokens, B, T, st));
+  for (int l = 0; l < m->L; ++l)
+    NC_TRY(launch_kv_store(m->dtype, (int64_t)B * T, T, 0, m->H, m->Hkv, m->hd, layer_act(m, m->qkv, l, m->qkvw),
+                           m->qkvw, kv_layer(m, m->kcache, l), kv_layer(m, m->vcache, l), m->kv_max, st));
+  // logits of each prompt's last position: rows b*T + T-1 of xf
+  const void* last = (const uint8_t*)m->xf + (size_t)(T - 1) * m->C * m->act;
+  NC_TRY(gemm(m, NC_PROF_GEMM_LM, B, m->V, m->C, last, (int64_t)T * m->C, 1, wptr(m, m->layout.back()), m->C, 1,
+              NC_EP_STORE_F32, logits, m->V, nullptr, 0, st));
+  m->kv_batch = B;
+  m->kv_len = T;
+  return NC_OK;
+}
+
+extern "C" nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, float* logits, void* stream) {
+  if (!m || !tokens || !logits) return NC_ERR_ARG;
+  if (!m->kcache || m->kv_len < 1 || B != m->kv_batch || m->kv_len >= m->kv_max) return NC_ERR_ARG;
+  cudaStream_t st = as_stream(stream);
+  const int C = m->C, F = m->F, Hd = m->H * m->hd, W = m->qkvw, p = m->kv_len;
+  const float eps = m->cfg.norm_eps;
+  // the weights' compute-dtype copy is the one the prefill cast
+  NC_TRY(launch_embed_fwd(m->dtype, B, C, m->V, tokens, m->master, m->x, m->err, st));
+  uint8_t* xn1 = layer_act(m, m->xn1, 0, C);
+  uint8_t* xn2 = layer_act(m, m->xn2, 0, C);
+  uint8_t* qkv = layer_act(m, m->qkv, 0, W);
+  uint8_t* o = layer_act(m, m->o, 0, Hd);
+  uint8_t* h = layer_act(m, m->h, 0, F);
+  // RoPE at position p: the table from row p with T = 1 (every row at offset 0)
+  const float* tab_p = m->rope_tab + (size_t)p * m->hd;
+  for (int l = 0; l < m->L; ++l) {
+    NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, xn1, m->rstd1, eps, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, B, W, C, xn1, C, 1, wptr(m, tensor(m, l, 0)), C, 1, NC_EP_STORE, qkv, W, nullptr,
+                0, st));
+    NC_TRY(launch_rope_qknorm_fwd(m->dtype, B, 1, m->H, m->Hkv, m->hd, qkv, m->rstdqk, tab_p, eps, st));
+    NC_TRY(launch_kv_store(m->dtype, B, 1, p, m->H, m->Hkv, m->hd, qkv, W, kv_layer(m, m->kcache, l),
+                           kv_layer(m, m->vcache, l), m->kv_max, st));
+    NC_TRY(launch_decode_attn(m->dtype, B, m->H, m->Hkv, m->hd, p + 1, qkv, W, kv_layer(m, m->kcache, l),
+                              kv_layer(m, m->vcache, l), m->kv_max, m->dec_part, o, Hd, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, B, C, Hd, o, Hd, 1, wptr(m, tensor(m, l, 3)), Hd, 1, NC_EP_ACCUM_F32, m->x, C,
+                nullptr, 0, st));
+    NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, xn2, m->rstd2, eps, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, B, F, C, xn2, C, 1, wptr(m, tensor(m, l, 4)), C, 1, NC_EP_RELU2_SQ, h, F, nullptr,
+                0, st));
+    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, B, C, F, h, F, 1, wptr(m, tensor(m, l, 5)), F, 1, NC_EP_ACCUM_F32, m->x, C,
+                nullptr, 0, st));
+  }
+  NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, m->xf, m->rstd_f, eps, st));
+  NC_TRY(gemm(m, NC_PROF_GEMM_LM, B, m->V, C, m->xf, C, 1, wptr(m, m->layout.back()), C, 1, NC_EP_STORE_F32, logits,
+              m->V, nullptr, 0, st));
+  m->kv_len = p + 1;
+  return NC_OK;
 }

@@ -111,3 +111,16 @@ nc_status launch_cast_out(int dtype, int64_t n, const void* X, float* out, cudaS
 // One bias-corrected AdamW step (t >= 1) with decoupled weight decay.
 nc_status launch_adamw(int64_t n, float* W, const float* G, float* m, float* v, float lr, float b1, float b2,
                        float eps, float wd, int64_t t, cudaStream_t st);
+
+// ---------------------------------------------------------------- KV-cache decoding (k_decode.cu)
+// Row r of qkv[rows, ld] = sequence r / T, position t0 + r % T: its k and v heads
+// go to kc / vc ([B][Hkv][max_len][hd], compute dtype).
+nc_status launch_kv_store(int dtype, int64_t rows, int T, int t0, int H, int Hkv, int hd, const void* qkv, int64_t ld,
+                          void* kc, void* vc, int max_len, cudaStream_t st);
+// o[b, h*hd..] = softmax(q_bh . K[b, h/G, 0..len) / sqrt(hd)) V for the single
+// query row b of qkv (ld), H/Hkv in {1, 2, 3, 4, 8}, hd 64 or 128.  part holds
+// decode_part_floats(B, H, hd, max_len) floats.
+nc_status launch_decode_attn(int dtype, int B, int H, int Hkv, int hd, int len, const void* qkv, int64_t ld,
+                             const void* kc, const void* vc, int max_len, float* part, void* o, int64_t ldo,
+                             cudaStream_t st);
+size_t decode_part_floats(int B, int H, int hd, int max_len);

@@ -403,6 +403,33 @@ size_t nc_newton_schulz_workspace_bytes(int32_t dtype, int32_t rows, int32_t col
 nc_status nc_op_newton_schulz(int32_t dtype, int32_t rows, int32_t cols, int32_t steps,
                               const float* u, float* x, void* workspace, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Incremental decoding with a key/value cache (woshipm nanochat analysis §三
+ * item 4).  nc_prefill runs the forward over B prompts of T tokens
+ * (positions 0..T-1), keeps every layer's keys (after RoPE and the QK norm)
+ * and values, and writes the logits of each prompt's last position; every
+ * nc_decode_step then feeds one token per sequence at the next position and
+ * writes that position's logits.  The logits of prompt b at position t equal
+ * row (b, t) of nc_forward_logits on the whole sequence (up to rounding).
+ * The weights used are those cast by the last nc_prefill: after
+ * nc_set_params or nc_optimizer_step, prefill again.
+ * ---------------------------------------------------------------------- */
+/* Allocate (or reuse, if large enough) the cache for max_batch sequences of
+ * max_len positions and empty it.  1 <= max_batch <= cfg.batch,
+ * 1 <= max_len <= cfg.seq_len; NC_ERR_UNSUPPORTED unless hd is 64 or 128 and
+ * n_head / n_kv_head is 1, 2, 3, 4 or 8. */
+nc_status nc_kv_cache_create(nc_model* m, int32_t max_batch, int32_t max_len);
+/* tokens_dev: int32 [B, T]; logits_dev: fp32 [B, V] (device).  Replaces the
+ * cache contents; B <= max_batch, T <= max_len.  Does not synchronise. */
+nc_status nc_prefill(nc_model* m, const int32_t* tokens_dev, int32_t B, int32_t T,
+                     float* logits_dev, void* stream);
+/* tokens_dev: int32 [B], B = the prefill's B; logits_dev: fp32 [B, V].
+ * NC_ERR_ARG when the cache is empty or full.  Does not synchronise. */
+nc_status nc_decode_step(nc_model* m, const int32_t* tokens_dev, int32_t B, float* logits_dev,
+                         void* stream);
+/* Positions held per sequence (-1 for NULL). */
+int32_t nc_kv_cache_length(const nc_model* m);
+
 #ifdef __cplusplus
 }
 #endif

@@ -130,6 +130,14 @@ def test_gemm_bf16_streamk_is_deterministic():
     assert torch.equal(outs[0], outs[1])
 
 
+@pytest.mark.parametrize("M", [1, 2, 5, 33])
+@pytest.mark.parametrize("dt", [BF16, F32])
+def test_gemm_few_rows(M, dt):
+    # the decode step's projections: one row per sequence
+    _assert_gemm(_gemm_case(M, 640, 256, 1, 1, nc.EP_STORE_F32, dt, seed=40 + M), dt, 256, nc.EP_STORE_F32)
+    _assert_gemm(_gemm_case(M, 384, 256, 1, 1, nc.EP_ACCUM_F32, dt, seed=50 + M), dt, 256, nc.EP_ACCUM_F32)
+
+
 def test_gemm_bf16_narrow_n():
     _assert_gemm(_gemm_case(384, 64, 256, 1, 1, nc.EP_STORE_F32, BF16, seed=3), BF16, 256, nc.EP_STORE_F32)
     _assert_gemm(_gemm_case(136, 128, 72, 0, 0, nc.EP_STORE_F32, BF16, seed=4), BF16, 72, nc.EP_STORE_F32)
