@@ -98,6 +98,8 @@ _SIGS = {
     "nc_op_embed_bwd": (_i32, [_i64, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_debug_set_wait_limit_ns": (None, [_u64]),
     "nc_debug_set_gemm_pair": (None, [_i32]),
+    "nc_debug_set_decode_graph": (None, [_i32]),
+    "nc_op_gemm_rows": (_i32, [_i32, _i32, _i32, _i32, _p, _i64, _p, _i64, _i32, _p, _i64, _p]),
     "nc_profile_enable": (_i32, [_p, _i32]),
     "nc_profile_read": (_i32, [_p, _i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64),
                                 ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
@@ -381,6 +383,14 @@ class ops:
         V, C = wte.shape
         _check(_lib.nc_op_embed_fwd(dtype, tokens.numel(), C, V, _ptr(tokens), _ptr(wte), _ptr(x), _ptr(err),
                                     _stream()), "nc_op_embed_fwd")
+
+    @staticmethod
+    def gemm_rows(A, W, D, ep=EP_STORE_F32):
+        """D[m, n] (op)= sum_k A[m, k] W[n, k] for at most 32 rows (CUDA-core skinny GEMM)."""
+        M, K = A.shape
+        N = W.shape[0]
+        _check(_lib.nc_op_gemm_rows(_dtype_code(A), M, N, K, _ptr(A), A.stride(0), _ptr(W), W.stride(0), ep, _ptr(D),
+                                    D.stride(0), _stream()), "nc_op_gemm_rows")
 
     @staticmethod
     def newton_schulz(u, x, steps=5, dtype=None, workspace=None):

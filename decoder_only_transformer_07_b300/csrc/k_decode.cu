@@ -25,8 +25,9 @@ __device__ __forceinline__ void st_f(bf16* p, float v) { *p = __float2bfloat16_r
 // Row r of qkv[rows, ld] is (sequence r / T, position t0 + r % T): its k and v
 // heads go to the cache at that position.  One thread per element.
 template <typename E>
-__global__ void k_kv_store(int64_t rows, int T, int t0, int H, int Hkv, int hd, const E* __restrict__ qkv, int64_t ld,
-                           E* __restrict__ kc, E* __restrict__ vc, int max_len) {
+__global__ void k_kv_store(int64_t rows, int T, int t0, const int32_t* __restrict__ t0_dev, int H, int Hkv, int hd,
+                           const E* __restrict__ qkv, int64_t ld, E* __restrict__ kc, E* __restrict__ vc,
+                           int max_len) {
   const int64_t per_row = (int64_t)Hkv * hd;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= rows * per_row) return;
@@ -34,7 +35,7 @@ __global__ void k_kv_store(int64_t rows, int T, int t0, int H, int Hkv, int hd, 
   const int rem = (int)(i % per_row);
   const int g = rem / hd, d = rem % hd;
   const int64_t b = r / T;
-  const int t = t0 + (int)(r % T);
+  const int t = (t0_dev ? *t0_dev : t0) + (int)(r % T);
   const int64_t dst = ((b * Hkv + g) * max_len + t) * hd + d;
   kc[dst] = qkv[r * ld + (int64_t)(H + g) * hd + d];
   vc[dst] = qkv[r * ld + (int64_t)(H + Hkv + g) * hd + d];
@@ -44,12 +45,15 @@ constexpr int DEC_CHUNK = 256;
 constexpr int DEC_WARPS = 4;
 
 // Partials: part[((b * H + h) * nsplit + s) * (HD + 2) + {0: max (log2 units), 1: sum, 2..: output}]
+// len_dev (device, may be NULL): the key count is *len_dev + 1 (the position of
+// the token just appended, plus one); chunks past it leave empty partials.
 template <typename E, int HD, int G>
 __global__ void __launch_bounds__(DEC_WARPS * 32)
-    k_decode_attn(int H, int Hkv, int len, int nsplit, const E* __restrict__ qkv, int64_t ld,
-                  const E* __restrict__ kc, const E* __restrict__ vc, int max_len, float scale_log2,
-                  float* __restrict__ part) {
+    k_decode_attn(int H, int Hkv, int len, const int32_t* __restrict__ len_dev, int nsplit,
+                  const E* __restrict__ qkv, int64_t ld, const E* __restrict__ kc, const E* __restrict__ vc,
+                  int max_len, float scale_log2, float* __restrict__ part) {
   constexpr int DPL = HD / 32;
+  if (len_dev) len = *len_dev + 1;
   const int bg = blockIdx.x, s = blockIdx.y;
   const int b = bg / Hkv, g = bg % Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -159,12 +163,13 @@ __global__ void k_decode_combine(int64_t rows, int nsplit, const float* __restri
 }
 
 template <typename E, int HD, int G>
-nc_status decode_attn_t(int B, int H, int Hkv, int len, const E* qkv, int64_t ld, const E* kc, const E* vc,
-                        int max_len, float* part, E* o, int64_t ldo, cudaStream_t st) {
-  const int nsplit = (len + DEC_CHUNK - 1) / DEC_CHUNK;
+nc_status decode_attn_t(int B, int H, int Hkv, int len, const int32_t* len_dev, const E* qkv, int64_t ld,
+                        const E* kc, const E* vc, int max_len, float* part, E* o, int64_t ldo, cudaStream_t st) {
+  // with the length on the device the grid covers the whole capacity
+  const int nsplit = ((len_dev ? max_len : len) + DEC_CHUNK - 1) / DEC_CHUNK;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   k_decode_attn<E, HD, G><<<dim3((unsigned)(B * Hkv), (unsigned)nsplit), DEC_WARPS * 32, 0, st>>>(
-      H, Hkv, len, nsplit, qkv, ld, kc, vc, max_len, scale_log2, part);
+      H, Hkv, len, len_dev, nsplit, qkv, ld, kc, vc, max_len, scale_log2, part);
   NC_CUDA_TRY(cudaGetLastError());
   const int64_t rows = (int64_t)B * H;
   k_decode_combine<E, HD><<<cdiv(rows, 8), 256, 0, st>>>(rows, nsplit, part, o, ldo, H);
@@ -172,14 +177,14 @@ nc_status decode_attn_t(int B, int H, int Hkv, int len, const E* qkv, int64_t ld
 }
 
 template <typename E, int HD>
-nc_status decode_attn_g(int G, int B, int H, int Hkv, int len, const E* qkv, int64_t ld, const E* kc, const E* vc,
-                        int max_len, float* part, E* o, int64_t ldo, cudaStream_t st) {
+nc_status decode_attn_g(int G, int B, int H, int Hkv, int len, const int32_t* len_dev, const E* qkv, int64_t ld,
+                        const E* kc, const E* vc, int max_len, float* part, E* o, int64_t ldo, cudaStream_t st) {
   switch (G) {
-    case 1: return decode_attn_t<E, HD, 1>(B, H, Hkv, len, qkv, ld, kc, vc, max_len, part, o, ldo, st);
-    case 2: return decode_attn_t<E, HD, 2>(B, H, Hkv, len, qkv, ld, kc, vc, max_len, part, o, ldo, st);
-    case 3: return decode_attn_t<E, HD, 3>(B, H, Hkv, len, qkv, ld, kc, vc, max_len, part, o, ldo, st);
-    case 4: return decode_attn_t<E, HD, 4>(B, H, Hkv, len, qkv, ld, kc, vc, max_len, part, o, ldo, st);
-    case 8: return decode_attn_t<E, HD, 8>(B, H, Hkv, len, qkv, ld, kc, vc, max_len, part, o, ldo, st);
+    case 1: return decode_attn_t<E, HD, 1>(B, H, Hkv, len, len_dev, qkv, ld, kc, vc, max_len, part, o, ldo, st);
+    case 2: return decode_attn_t<E, HD, 2>(B, H, Hkv, len, len_dev, qkv, ld, kc, vc, max_len, part, o, ldo, st);
+    case 3: return decode_attn_t<E, HD, 3>(B, H, Hkv, len, len_dev, qkv, ld, kc, vc, max_len, part, o, ldo, st);
+    case 4: return decode_attn_t<E, HD, 4>(B, H, Hkv, len, len_dev, qkv, ld, kc, vc, max_len, part, o, ldo, st);
+    case 8: return decode_attn_t<E, HD, 8>(B, H, Hkv, len, len_dev, qkv, ld, kc, vc, max_len, part, o, ldo, st);
     default: return NC_ERR_UNSUPPORTED;
   }
 }
@@ -191,30 +196,160 @@ size_t decode_part_floats(int B, int H, int hd, int max_len) {
 }
 
 nc_status launch_kv_store(int dtype, int64_t rows, int T, int t0, int H, int Hkv, int hd, const void* qkv, int64_t ld,
-                          void* kc, void* vc, int max_len, cudaStream_t st) {
+                          void* kc, void* vc, int max_len, cudaStream_t st, const int32_t* t0_dev) {
   const int64_t n = rows * Hkv * hd;
   if (n <= 0) return NC_OK;
   if (dtype == NC_BF16)
-    k_kv_store<bf16><<<cdiv(n, 256), 256, 0, st>>>(rows, T, t0, H, Hkv, hd, (const bf16*)qkv, ld, (bf16*)kc,
+    k_kv_store<bf16><<<cdiv(n, 256), 256, 0, st>>>(rows, T, t0, t0_dev, H, Hkv, hd, (const bf16*)qkv, ld, (bf16*)kc,
                                                     (bf16*)vc, max_len);
   else
-    k_kv_store<float><<<cdiv(n, 256), 256, 0, st>>>(rows, T, t0, H, Hkv, hd, (const float*)qkv, ld, (float*)kc,
+    k_kv_store<float><<<cdiv(n, 256), 256, 0, st>>>(rows, T, t0, t0_dev, H, Hkv, hd, (const float*)qkv, ld, (float*)kc,
                                                      (float*)vc, max_len);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
 nc_status launch_decode_attn(int dtype, int B, int H, int Hkv, int hd, int len, const void* qkv, int64_t ld,
                              const void* kc, const void* vc, int max_len, float* part, void* o, int64_t ldo,
-                             cudaStream_t st) {
-  if (B <= 0 || len <= 0 || len > max_len || H % Hkv || (hd != 64 && hd != 128)) return NC_ERR_ARG;
+                             cudaStream_t st, const int32_t* len_dev) {
+  if (B <= 0 || (!len_dev && (len <= 0 || len > max_len)) || H % Hkv || (hd != 64 && hd != 128)) return NC_ERR_ARG;
   const int G = H / Hkv;
   if (dtype == NC_BF16)
-    return hd == 128 ? decode_attn_g<bf16, 128>(G, B, H, Hkv, len, (const bf16*)qkv, ld, (const bf16*)kc,
+    return hd == 128 ? decode_attn_g<bf16, 128>(G, B, H, Hkv, len, len_dev, (const bf16*)qkv, ld, (const bf16*)kc,
                                                 (const bf16*)vc, max_len, part, (bf16*)o, ldo, st)
-                     : decode_attn_g<bf16, 64>(G, B, H, Hkv, len, (const bf16*)qkv, ld, (const bf16*)kc,
+                     : decode_attn_g<bf16, 64>(G, B, H, Hkv, len, len_dev, (const bf16*)qkv, ld, (const bf16*)kc,
                                                (const bf16*)vc, max_len, part, (bf16*)o, ldo, st);
-  return hd == 128 ? decode_attn_g<float, 128>(G, B, H, Hkv, len, (const float*)qkv, ld, (const float*)kc,
+  return hd == 128 ? decode_attn_g<float, 128>(G, B, H, Hkv, len, len_dev, (const float*)qkv, ld, (const float*)kc,
                                                (const float*)vc, max_len, part, (float*)o, ldo, st)
-                   : decode_attn_g<float, 64>(G, B, H, Hkv, len, (const float*)qkv, ld, (const float*)kc,
+                   : decode_attn_g<float, 64>(G, B, H, Hkv, len, len_dev, (const float*)qkv, ld, (const float*)kc,
                                               (const float*)vc, max_len, part, (float*)o, ldo, st);
+}
+
+namespace {
+__global__ void k_set_i32(int32_t* p, int32_t v, int32_t add) { *p = add ? *p + v : v; }
+}  // namespace
+
+nc_status launch_set_i32(int32_t* p, int32_t v, bool add, cudaStream_t st) {
+  k_set_i32<<<1, 1, 0, st>>>(p, v, add ? 1 : 0);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- skinny GEMM
+// D[m, n] (op)= sum_k A[m, k] W[n, k] for M <= 32 rows (the decode step's
+// projections: one row per sequence).  With so few rows every weight is used
+// M times at most, so the product is bound by reading W once; it runs on the
+// CUDA cores with one warp per output column n streaming W's row n in 16-byte
+// pieces, and A staged in shared memory in K chunks that all 8 warps of the
+// CTA share.  Accumulation is fp32 in a fixed order.
+namespace {
+
+constexpr int SK_WARPS = 8;
+// K chunk staged per round: 1024, or less so that the chunk of A stays within 32 KB
+template <typename E, int MB>
+__host__ __device__ constexpr int sk_kc() { return MB * (int)sizeof(E) * 1024 <= 32768 ? 1024 : 32768 / (MB * (int)sizeof(E)); }
+
+__device__ __forceinline__ void ld8(const float* p, float* f) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void ld8(const bf16* p, float* f) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const bf16* h = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(h[e]);
+}
+
+template <typename E, int MB>
+__global__ void __launch_bounds__(SK_WARPS * 32)
+    k_gemm_skinny(int M, int N, int K, const E* __restrict__ A, int64_t lda, const E* __restrict__ W, int64_t ldw,
+                  int ep, void* __restrict__ D, int64_t ldd) {
+  constexpr int SK_KC = sk_kc<E, MB>();
+  __shared__ __align__(16) E xs[MB][SK_KC];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * SK_WARPS + warp;
+  float acc[MB];
+#pragma unroll
+  for (int m = 0; m < MB; ++m) acc[m] = 0.f;
+  for (int k0 = 0; k0 < K; k0 += SK_KC) {
+    const int kc = min(SK_KC, K - k0);
+    __syncthreads();
+    for (int i = threadIdx.x * 8; i < MB * SK_KC; i += SK_WARPS * 32 * 8) {
+      const int m = i / SK_KC, k = i % SK_KC;
+      if (m < M && k < kc) {
+        *reinterpret_cast<uint4*>(&xs[m][k]) = *reinterpret_cast<const uint4*>(A + (int64_t)m * lda + k0 + k);
+        if (sizeof(E) == 4) *reinterpret_cast<uint4*>(&xs[m][k + 4]) =
+            *reinterpret_cast<const uint4*>(A + (int64_t)m * lda + k0 + k + 4);
+      }
+    }
+    __syncthreads();
+    if (n < N) {
+      const E* wr = W + (int64_t)n * ldw + k0;
+      // four 16-byte pieces of the row in flight per lane before any is used
+      for (int kb = lane * 8; kb < kc; kb += 1024) {
+        float w[4][8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (kb + 256 * u < kc) ld8(wr + kb + 256 * u, w[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int k = kb + 256 * u;
+          if (k >= kc) break;
+#pragma unroll
+          for (int m = 0; m < MB; ++m) {
+            if (m < M) {
+              float x[8];
+              ld8(&xs[m][k], x);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[m] = fmaf(x[e], w[u][e], acc[m]);
+            }
+          }
+        }
+      }
+    }
+  }
+  if (n >= N) return;
+#pragma unroll
+  for (int m = 0; m < MB; ++m) {
+    float v = acc[m];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0 && m < M) {
+      if (ep == NC_EP_STORE_F32) reinterpret_cast<float*>(D)[(int64_t)m * ldd + n] = v;
+      else if (ep == NC_EP_ACCUM_F32) reinterpret_cast<float*>(D)[(int64_t)m * ldd + n] += v;
+      else {
+        if (ep == NC_EP_RELU2_SQ) { v = fmaxf(v, 0.f); v *= v; }
+        st_f(reinterpret_cast<E*>(D) + (int64_t)m * ldd + n, v);
+      }
+    }
+  }
+}
+
+template <typename E, int MB>
+nc_status skinny_t(int M, int N, int K, const E* A, int64_t lda, const E* W, int64_t ldw, int ep, void* D, int64_t ldd,
+                   cudaStream_t st) {
+  k_gemm_skinny<E, MB><<<cdiv(N, SK_WARPS), SK_WARPS * 32, 0, st>>>(M, N, K, A, lda, W, ldw, ep, D, ldd);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+template <typename E>
+nc_status skinny_e(int M, int N, int K, const E* A, int64_t lda, const E* W, int64_t ldw, int ep, void* D, int64_t ldd,
+                   cudaStream_t st) {
+  if (M <= 1) return skinny_t<E, 1>(M, N, K, A, lda, W, ldw, ep, D, ldd, st);
+  if (M <= 2) return skinny_t<E, 2>(M, N, K, A, lda, W, ldw, ep, D, ldd, st);
+  if (M <= 4) return skinny_t<E, 4>(M, N, K, A, lda, W, ldw, ep, D, ldd, st);
+  if (M <= 8) return skinny_t<E, 8>(M, N, K, A, lda, W, ldw, ep, D, ldd, st);
+  if (M <= 16) return skinny_t<E, 16>(M, N, K, A, lda, W, ldw, ep, D, ldd, st);
+  return skinny_t<E, 32>(M, N, K, A, lda, W, ldw, ep, D, ldd, st);
+}
+
+}  // namespace
+
+nc_status launch_gemm_skinny(int dtype, int M, int N, int K, const void* A, int64_t lda, const void* W, int64_t ldw,
+                             int ep, void* D, int64_t ldd, cudaStream_t st) {
+  if (M < 1 || M > SKINNY_MAX_M || N < 1 || K < 8 || K % 8 || lda % 8 || ldw % 8 ||
+      (ep != NC_EP_STORE && ep != NC_EP_STORE_F32 && ep != NC_EP_ACCUM_F32 && ep != NC_EP_RELU2_SQ))
+    return NC_ERR_ARG;
+  if ((((uintptr_t)A) & 15) || (((uintptr_t)W) & 15)) return NC_ERR_ARG;
+  if (dtype == NC_BF16)
+    return skinny_e<bf16>(M, N, K, (const bf16*)A, lda, (const bf16*)W, ldw, ep, D, ldd, st);
+  return skinny_e<float>(M, N, K, (const float*)A, lda, (const float*)W, ldw, ep, D, ldd, st);
 }

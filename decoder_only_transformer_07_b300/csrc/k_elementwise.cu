@@ -213,13 +213,13 @@ __device__ __forceinline__ void st2(bf16* p, float a, float b) {
 template <typename T>
 __global__ void k_rope_qknorm_fwd(int64_t rows, int T_, int nh, int hd, int64_t ld,
                                   T* __restrict__ qkv, float* __restrict__ rstd,
-                                  const float2* __restrict__ tab, float eps) {
+                                  const float2* __restrict__ tab, float eps, const int32_t* __restrict__ pos0) {
   int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   int lane = threadIdx.x & 31;
   if (w >= rows * nh) return;
   int64_t row = w / nh;
   int j = (int)(w % nh);
-  int t = (int)(row % T_);
+  int t = (int)(row % T_) + (pos0 ? *pos0 : 0);
   const int d = hd / 2;
   T* p = qkv + row * ld + (int64_t)j * hd;
   const float2* cs = tab + (int64_t)t * d;
@@ -299,7 +299,7 @@ __global__ void k_rope_qknorm_bwd(int64_t rows, int T_, int nh, int hd, int64_t 
 }
 
 nc_status launch_rope_qknorm_fwd(int dtype, int B, int T, int H, int Hkv, int hd, void* qkv,
-                                 float* rstd, const float* tab, float eps, cudaStream_t st) {
+                                 float* rstd, const float* tab, float eps, cudaStream_t st, const int32_t* pos0) {
   if (hd > 256 || (hd & 3) || (((uintptr_t)qkv) & 7) || (((uintptr_t)tab) & 15)) return NC_ERR_ARG;
   int64_t rows = (int64_t)B * T;
   int nh = H + Hkv;
@@ -308,10 +308,10 @@ nc_status launch_rope_qknorm_fwd(int dtype, int B, int T, int H, int Hkv, int hd
   if (warps == 0) return NC_OK;
   if (dtype == NC_BF16)
     k_rope_qknorm_fwd<bf16><<<cdiv(warps, 8), 256, 0, st>>>(rows, T, nh, hd, ld, (bf16*)qkv, rstd,
-                                                             (const float2*)tab, eps);
+                                                             (const float2*)tab, eps, pos0);
   else
     k_rope_qknorm_fwd<float><<<cdiv(warps, 8), 256, 0, st>>>(rows, T, nh, hd, ld, (float*)qkv, rstd,
-                                                              (const float2*)tab, eps);
+                                                              (const float2*)tab, eps, pos0);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 

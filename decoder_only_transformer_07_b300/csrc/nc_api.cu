@@ -84,6 +84,15 @@ struct nc_model {
   float* dec_part = nullptr;                   // decode-attention partials
   int kv_b = 0, kv_max = 0;                    // capacity
   int kv_batch = 0, kv_len = 0;                // sequences and positions held
+  // A decode step reads its position from dec_pos (device) and its tokens /
+  // writes its logits through fixed buffers, so the same CUDA graph replays
+  // every step; it is captured on dec_st once per batch size.
+  int32_t *dec_pos = nullptr, *dec_tok = nullptr;
+  float* dec_logits = nullptr;
+  cudaStream_t dec_st = nullptr;
+  cudaEvent_t dec_ev0 = nullptr, dec_ev1 = nullptr;
+  cudaGraphExec_t dec_exec = nullptr;
+  int dec_graph_b = 0;                         // batch of dec_exec (0: none, -1: capture failed)
   // profiling (nc_profile_enable)
   struct Rec { int cls, sub; int ev; double flops, bytes; };
   bool prof_on = false;
@@ -340,6 +349,10 @@ extern "C" void nc_model_destroy(nc_model* m) {
     if (m->opt_join[k]) cudaEventDestroy(m->opt_join[k]);
   }
   if (m->opt_fork) cudaEventDestroy(m->opt_fork);
+  if (m->dec_exec) cudaGraphExecDestroy(m->dec_exec);
+  if (m->dec_st) cudaStreamDestroy(m->dec_st);
+  if (m->dec_ev0) cudaEventDestroy(m->dec_ev0);
+  if (m->dec_ev1) cudaEventDestroy(m->dec_ev1);
   delete m;
 }
 
@@ -1036,6 +1049,17 @@ extern "C" nc_status nc_kv_cache_create(nc_model* m, int32_t max_batch, int32_t 
   NC_TRY(dalloc(m, n * m->act, &m->kcache));
   NC_TRY(dalloc(m, n * m->act, &m->vcache));
   NC_TRY(dalloc_t(m, decode_part_floats(max_batch, m->H, m->hd, max_len), &m->dec_part));
+  NC_TRY(dalloc_t(m, (size_t)max_batch, &m->dec_tok));
+  NC_TRY(dalloc_t(m, (size_t)max_batch * m->V, &m->dec_logits));
+  if (!m->dec_pos) NC_TRY(dalloc_t(m, 1, &m->dec_pos));
+  if (!m->dec_st) {
+    NC_CUDA_TRY(cudaStreamCreateWithFlags(&m->dec_st, cudaStreamNonBlocking));
+    NC_CUDA_TRY(cudaEventCreateWithFlags(&m->dec_ev0, cudaEventDisableTiming));
+    NC_CUDA_TRY(cudaEventCreateWithFlags(&m->dec_ev1, cudaEventDisableTiming));
+  }
+  if (m->dec_exec) cudaGraphExecDestroy(m->dec_exec);   // it baked in the old buffers
+  m->dec_exec = nullptr;
+  m->dec_graph_b = 0;
   m->kv_batch = m->kv_len = 0;
   return NC_OK;
 }
@@ -1061,8 +1085,65 @@ extern "C" nc_status nc_prefill(nc_model* m, const int32_t* tokens, int32_t B, i
   const void* last = (const uint8_t*)m->xf + (size_t)(T - 1) * m->C * m->act;
   NC_TRY(gemm(m, NC_PROF_GEMM_LM, B, m->V, m->C, last, (int64_t)T * m->C, 1, wptr(m, m->layout.back()), m->C, 1,
               NC_EP_STORE_F32, logits, m->V, nullptr, 0, st));
+  NC_TRY(launch_set_i32(m->dec_pos, T, false, st));
   m->kv_batch = B;
   m->kv_len = T;
+  return NC_OK;
+}
+
+// One decode step for B sequences at position *dec_pos: tokens from dec_tok,
+// logits to dec_logits; ends by advancing *dec_pos.  Every argument is fixed
+// for a given B, so the enqueued work can be captured once and replayed.
+static nc_status decode_body(nc_model* m, int B, cudaStream_t st) {
+  const int C = m->C, F = m->F, Hd = m->H * m->hd, W = m->qkvw;
+  // the projections of B <= 8 rows are bound by reading the weights once:
+  // CUDA-core skinny GEMM; beyond that the tensor-core GEMM is faster
+  auto proj = [&](int role, int N, int K, const void* a, const void* w, int ep, void* d, int64_t ldd) -> nc_status {
+    if (B <= 8) return launch_gemm_skinny(m->dtype, B, N, K, a, K, w, K, ep, d, ldd, st);
+    return gemm(m, role, B, N, K, a, K, 1, w, K, 1, ep, d, ldd, nullptr, 0, st);
+  };
+  const float eps = m->cfg.norm_eps;
+  NC_TRY(launch_embed_fwd(m->dtype, B, C, m->V, m->dec_tok, m->master, m->x, m->err, st));
+  uint8_t* xn1 = layer_act(m, m->xn1, 0, C);
+  uint8_t* xn2 = layer_act(m, m->xn2, 0, C);
+  uint8_t* qkv = layer_act(m, m->qkv, 0, W);
+  uint8_t* o = layer_act(m, m->o, 0, Hd);
+  uint8_t* h = layer_act(m, m->h, 0, F);
+  for (int l = 0; l < m->L; ++l) {
+    NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, xn1, m->rstd1, eps, st));
+    NC_TRY(proj(NC_PROF_GEMM_FWD, W, C, xn1, wptr(m, tensor(m, l, 0)), NC_EP_STORE, qkv, W));
+    // RoPE + QK norm at position *dec_pos (T = 1)
+    NC_TRY(launch_rope_qknorm_fwd(m->dtype, B, 1, m->H, m->Hkv, m->hd, qkv, m->rstdqk, m->rope_tab, eps, st,
+                                  m->dec_pos));
+    NC_TRY(launch_kv_store(m->dtype, B, 1, 0, m->H, m->Hkv, m->hd, qkv, W, kv_layer(m, m->kcache, l),
+                           kv_layer(m, m->vcache, l), m->kv_max, st, m->dec_pos));
+    NC_TRY(launch_decode_attn(m->dtype, B, m->H, m->Hkv, m->hd, 0, qkv, W, kv_layer(m, m->kcache, l),
+                              kv_layer(m, m->vcache, l), m->kv_max, m->dec_part, o, Hd, st, m->dec_pos));
+    NC_TRY(proj(NC_PROF_GEMM_FWD, C, Hd, o, wptr(m, tensor(m, l, 3)), NC_EP_ACCUM_F32, m->x, C));
+    NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, xn2, m->rstd2, eps, st));
+    NC_TRY(proj(NC_PROF_GEMM_FWD, F, C, xn2, wptr(m, tensor(m, l, 4)), NC_EP_RELU2_SQ, h, F));
+    NC_TRY(proj(NC_PROF_GEMM_FWD, C, F, h, wptr(m, tensor(m, l, 5)), NC_EP_ACCUM_F32, m->x, C));
+  }
+  NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, m->xf, m->rstd_f, eps, st));
+  NC_TRY(proj(NC_PROF_GEMM_LM, m->V, C, m->xf, wptr(m, m->layout.back()), NC_EP_STORE_F32, m->dec_logits, m->V));
+  return launch_set_i32(m->dec_pos, 1, true, st);
+}
+
+int g_decode_graph = 1;   // test hook: 0 runs decode steps eagerly
+
+static nc_status decode_capture(nc_model* m, int B) {
+  cudaGraph_t g = nullptr;
+  NC_CUDA_TRY(cudaStreamBeginCapture(m->dec_st, cudaStreamCaptureModeRelaxed));
+  nc_status s = decode_body(m, B, m->dec_st);
+  cudaError_t e = cudaStreamEndCapture(m->dec_st, &g);
+  if (s == NC_OK && e == cudaSuccess) e = cudaGraphInstantiate(&m->dec_exec, g, 0);
+  if (g) cudaGraphDestroy(g);
+  if (s != NC_OK || e != cudaSuccess) {
+    cudaGetLastError();
+    m->dec_exec = nullptr;
+    return s != NC_OK ? s : NC_ERR_CUDA;
+  }
+  m->dec_graph_b = B;
   return NC_OK;
 }
 
@@ -1070,37 +1151,32 @@ extern "C" nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t 
   if (!m || !tokens || !logits) return NC_ERR_ARG;
   if (!m->kcache || m->kv_len < 1 || B != m->kv_batch || m->kv_len >= m->kv_max) return NC_ERR_ARG;
   cudaStream_t st = as_stream(stream);
-  const int C = m->C, F = m->F, Hd = m->H * m->hd, W = m->qkvw, p = m->kv_len;
-  const float eps = m->cfg.norm_eps;
-  // the weights' compute-dtype copy is the one the prefill cast
-  NC_TRY(launch_embed_fwd(m->dtype, B, C, m->V, tokens, m->master, m->x, m->err, st));
-  uint8_t* xn1 = layer_act(m, m->xn1, 0, C);
-  uint8_t* xn2 = layer_act(m, m->xn2, 0, C);
-  uint8_t* qkv = layer_act(m, m->qkv, 0, W);
-  uint8_t* o = layer_act(m, m->o, 0, Hd);
-  uint8_t* h = layer_act(m, m->h, 0, F);
-  // RoPE at position p: the table from row p with T = 1 (every row at offset 0)
-  const float* tab_p = m->rope_tab + (size_t)p * m->hd;
-  for (int l = 0; l < m->L; ++l) {
-    NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, xn1, m->rstd1, eps, st));
-    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, B, W, C, xn1, C, 1, wptr(m, tensor(m, l, 0)), C, 1, NC_EP_STORE, qkv, W, nullptr,
-                0, st));
-    NC_TRY(launch_rope_qknorm_fwd(m->dtype, B, 1, m->H, m->Hkv, m->hd, qkv, m->rstdqk, tab_p, eps, st));
-    NC_TRY(launch_kv_store(m->dtype, B, 1, p, m->H, m->Hkv, m->hd, qkv, W, kv_layer(m, m->kcache, l),
-                           kv_layer(m, m->vcache, l), m->kv_max, st));
-    NC_TRY(launch_decode_attn(m->dtype, B, m->H, m->Hkv, m->hd, p + 1, qkv, W, kv_layer(m, m->kcache, l),
-                              kv_layer(m, m->vcache, l), m->kv_max, m->dec_part, o, Hd, st));
-    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, B, C, Hd, o, Hd, 1, wptr(m, tensor(m, l, 3)), Hd, 1, NC_EP_ACCUM_F32, m->x, C,
-                nullptr, 0, st));
-    NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, xn2, m->rstd2, eps, st));
-    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, B, F, C, xn2, C, 1, wptr(m, tensor(m, l, 4)), C, 1, NC_EP_RELU2_SQ, h, F, nullptr,
-                0, st));
-    NC_TRY(gemm(m, NC_PROF_GEMM_FWD, B, C, F, h, F, 1, wptr(m, tensor(m, l, 5)), F, 1, NC_EP_ACCUM_F32, m->x, C,
-                nullptr, 0, st));
+  NC_CUDA_TRY(cudaMemcpyAsync(m->dec_tok, tokens, (size_t)B * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+  const bool graph = g_decode_graph && !m->prof_on && m->dec_graph_b >= 0;
+  if (graph && m->dec_graph_b != B) {
+    if (m->dec_exec) cudaGraphExecDestroy(m->dec_exec);
+    m->dec_exec = nullptr;
+    if (decode_capture(m, B) != NC_OK) m->dec_graph_b = -1;   // run eagerly from now on
   }
-  NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, m->xf, m->rstd_f, eps, st));
-  NC_TRY(gemm(m, NC_PROF_GEMM_LM, B, m->V, C, m->xf, C, 1, wptr(m, m->layout.back()), C, 1, NC_EP_STORE_F32, logits,
-              m->V, nullptr, 0, st));
-  m->kv_len = p + 1;
+  if (graph && m->dec_exec) {
+    NC_CUDA_TRY(cudaEventRecord(m->dec_ev0, st));
+    NC_CUDA_TRY(cudaStreamWaitEvent(m->dec_st, m->dec_ev0, 0));
+    NC_CUDA_TRY(cudaGraphLaunch(m->dec_exec, m->dec_st));
+    NC_CUDA_TRY(cudaEventRecord(m->dec_ev1, m->dec_st));
+    NC_CUDA_TRY(cudaStreamWaitEvent(st, m->dec_ev1, 0));
+  } else {
+    NC_TRY(decode_body(m, B, st));
+  }
+  NC_CUDA_TRY(cudaMemcpyAsync(logits, m->dec_logits, (size_t)B * m->V * sizeof(float), cudaMemcpyDeviceToDevice, st));
+  m->kv_len += 1;
   return NC_OK;
+}
+
+// Test hook: 0 makes decode steps run eagerly instead of through the captured graph.
+extern "C" void nc_debug_set_decode_graph(int32_t on) { g_decode_graph = on != 0; }
+
+extern "C" nc_status nc_op_gemm_rows(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A, int64_t lda,
+                                     const void* W, int64_t ldw, int32_t ep, void* D, int64_t ldd, void* stream) {
+  if (!dtype_ok(dtype) || !A || !W || !D) return NC_ERR_ARG;
+  return launch_gemm_skinny(dtype, M, N, K, A, lda, W, ldw, ep, D, ldd, as_stream(stream));
 }

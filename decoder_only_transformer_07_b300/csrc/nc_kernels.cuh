@@ -14,8 +14,10 @@ nc_status launch_rmsnorm_fwd(int dtype, int64_t rows, int C, const float* x, voi
                              float eps, cudaStream_t st);
 nc_status launch_rmsnorm_bwd(int dtype, int64_t rows, int C, const float* dy, const void* y,
                              const float* rstd, float* dx, void* dx_act, cudaStream_t st);
+// pos0 (device, may be NULL): positions are *pos0 + row % T instead of row % T.
 nc_status launch_rope_qknorm_fwd(int dtype, int B, int T, int H, int Hkv, int hd, void* qkv,
-                                 float* rstd, const float* tab, float eps, cudaStream_t st);
+                                 float* rstd, const float* tab, float eps, cudaStream_t st,
+                                 const int32_t* pos0 = nullptr);
 nc_status launch_rope_qknorm_bwd(int dtype, int B, int T, int H, int Hkv, int hd, void* dqkv,
                                  const void* qkv, const float* rstd, const float* tab,
                                  cudaStream_t st);
@@ -115,12 +117,23 @@ nc_status launch_adamw(int64_t n, float* W, const float* G, float* m, float* v, 
 // ---------------------------------------------------------------- KV-cache decoding (k_decode.cu)
 // Row r of qkv[rows, ld] = sequence r / T, position t0 + r % T: its k and v heads
 // go to kc / vc ([B][Hkv][max_len][hd], compute dtype).
+// t0_dev (device, may be NULL) replaces t0.
 nc_status launch_kv_store(int dtype, int64_t rows, int T, int t0, int H, int Hkv, int hd, const void* qkv, int64_t ld,
-                          void* kc, void* vc, int max_len, cudaStream_t st);
+                          void* kc, void* vc, int max_len, cudaStream_t st, const int32_t* t0_dev = nullptr);
 // o[b, h*hd..] = softmax(q_bh . K[b, h/G, 0..len) / sqrt(hd)) V for the single
 // query row b of qkv (ld), H/Hkv in {1, 2, 3, 4, 8}, hd 64 or 128.  part holds
 // decode_part_floats(B, H, hd, max_len) floats.
+// len_dev (device, may be NULL): the keys are 0..*len_dev (inclusive) and the
+// grid covers max_len (for a graph that replays at growing lengths).
 nc_status launch_decode_attn(int dtype, int B, int H, int Hkv, int hd, int len, const void* qkv, int64_t ld,
                              const void* kc, const void* vc, int max_len, float* part, void* o, int64_t ldo,
-                             cudaStream_t st);
+                             cudaStream_t st, const int32_t* len_dev = nullptr);
+// *p = v (add = false) or *p += v, on the device.
+nc_status launch_set_i32(int32_t* p, int32_t v, bool add, cudaStream_t st);
 size_t decode_part_floats(int B, int H, int hd, int max_len);
+// D[m, n] (op)= sum_k A[m, k] W[n, k] for 1 <= M <= SKINNY_MAX_M rows on the
+// CUDA cores (memory-bound on W); K, lda, ldw multiples of 8, 16-byte aligned
+// A and W; ep one of NC_EP_STORE, NC_EP_STORE_F32, NC_EP_ACCUM_F32, NC_EP_RELU2_SQ.
+#define SKINNY_MAX_M 32
+nc_status launch_gemm_skinny(int dtype, int M, int N, int K, const void* A, int64_t lda, const void* W, int64_t ldw,
+                             int ep, void* D, int64_t ldd, cudaStream_t st);

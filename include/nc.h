@@ -347,6 +347,12 @@ void nc_debug_set_wait_limit_ns(uint64_t ns);
  * compute the same sums; the switch exists to test and time either path. */
 void nc_debug_set_gemm_pair(int32_t on);
 
+/* Test hook.  on = 1 (default): a decode step replays a CUDA graph of the
+ * step, captured once per batch size on an internal stream (its position
+ * lives on the device, its tokens and logits pass through fixed buffers);
+ * on = 0 enqueues the same kernels directly.  Both compute the same values. */
+void nc_debug_set_decode_graph(int32_t on);
+
 /* ------------------------------------------------------------------------
  * Optimizer step (cosmicrealm "noao-chat-0-项目总体介绍" §2.2 and §4.2;
  * woshipm nanochat analysis §六.1): the weight matrices (every Wq, Wk, Wv,
@@ -400,6 +406,14 @@ int64_t nc_optimizer_steps(const nc_model* m);
  * workspace: nc_newton_schulz_workspace_bytes(dtype, rows, cols) bytes,
  * 256-byte aligned.  NC_BF16 needs rows, cols multiples of 8. */
 size_t nc_newton_schulz_workspace_bytes(int32_t dtype, int32_t rows, int32_t cols);
+/* D[m, n] (op)= sum_k A[m, k] W[n, k] for 1 <= M <= 32 rows (A [M][K], W
+ * [N][K], both K-major), the decode step's projections: CUDA cores, one pass
+ * over W, fp32 accumulation.  ep: NC_EP_STORE, NC_EP_STORE_F32,
+ * NC_EP_ACCUM_F32 or NC_EP_RELU2_SQ.  K, lda, ldw multiples of 8, 16-byte
+ * aligned A and W; NC_ERR_ARG otherwise. */
+nc_status nc_op_gemm_rows(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A,
+                          int64_t lda, const void* W, int64_t ldw, int32_t ep, void* D,
+                          int64_t ldd, void* stream);
 nc_status nc_op_newton_schulz(int32_t dtype, int32_t rows, int32_t cols, int32_t steps,
                               const float* u, float* x, void* workspace, void* stream);
 
@@ -412,7 +426,8 @@ nc_status nc_op_newton_schulz(int32_t dtype, int32_t rows, int32_t cols, int32_t
  * writes that position's logits.  The logits of prompt b at position t equal
  * row (b, t) of nc_forward_logits on the whole sequence (up to rounding).
  * The weights used are those cast by the last nc_prefill: after
- * nc_set_params or nc_optimizer_step, prefill again.
+ * nc_set_params or nc_optimizer_step, prefill again.  A decode step replays a
+ * CUDA graph of the whole step (see nc_debug_set_decode_graph).
  * ---------------------------------------------------------------------- */
 /* Allocate (or reuse, if large enough) the cache for max_batch sequences of
  * max_len positions and empty it.  1 <= max_batch <= cfg.batch,

@@ -94,3 +94,23 @@ def test_decode_errors_and_cache_reuse():
     ok, worst = rel_close(z1, z_ref, 1e-4)
     assert ok, worst
     m.close()
+
+
+def test_decode_graph_replay_equals_eager():
+    """The captured step and the eagerly enqueued one give bitwise the same logits."""
+    w = S.Workload(name="dec", dtype="bf16", tokens="zipf", depth=2, n_embd=256, n_head=4, n_kv_head=2, head_dim=64,
+                   mlp_hidden=1024, vocab=1024, seq_len=320, batch=2)
+    cfg, m, params = _model(w)
+    tok, _ = S.batch_tokens(w, seq_len=270)
+    dev = torch.from_numpy(tok).cuda()
+    outs = []
+    for graph in (1, 0):
+        nc.lib().nc_debug_set_decode_graph(graph)
+        m.kv_cache_create(2, 270)
+        z = [m.prefill(dev[:, :250].contiguous()).cpu()]
+        for j in range(19):
+            z.append(m.decode_step(dev[:, 250 + j].contiguous()).cpu())
+        outs.append(torch.stack(z))
+    nc.lib().nc_debug_set_decode_graph(1)
+    assert torch.equal(outs[0], outs[1])
+    m.close()

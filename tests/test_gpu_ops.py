@@ -138,6 +138,29 @@ def test_gemm_few_rows(M, dt):
     _assert_gemm(_gemm_case(M, 384, 256, 1, 1, nc.EP_ACCUM_F32, dt, seed=50 + M), dt, 256, nc.EP_ACCUM_F32)
 
 
+@pytest.mark.parametrize("M", [1, 5, 17, 32])
+@pytest.mark.parametrize("dt", [BF16, F32])
+@pytest.mark.parametrize("ep", [nc.EP_STORE, nc.EP_STORE_F32, nc.EP_ACCUM_F32, nc.EP_RELU2_SQ])
+def test_gemm_rows_skinny(M, dt, ep):
+    # the decode step's CUDA-core projections: at most 32 rows, ragged N
+    N, K = 333, 1096
+    a, w = rnd(70 + M, (M, K)), rnd(71 + M, (N, K))
+    A, W = dev_tensor(a, dt), dev_tensor(w, dt)
+    out_f32 = ep in (nc.EP_STORE_F32, nc.EP_ACCUM_F32)
+    d0 = rnd(72, (M, N)) if ep == nc.EP_ACCUM_F32 else np.zeros((M, N), np.float32)
+    D = dev_tensor(d0, F32 if out_f32 else dt)
+    nc.ops.gemm_rows(A, W, D, ep)
+    acc = OO.gemm(to64(A), to64(W))
+    want = {nc.EP_STORE: acc, nc.EP_STORE_F32: acc, nc.EP_ACCUM_F32: d0.astype(np.float64) + acc,
+            nc.EP_RELU2_SQ: np.maximum(acc, 0.0) ** 2}[ep]
+    got = to64(D)
+    scale = np.abs(want).max()
+    if dt == F32 or out_f32:   # fp32 accumulation of exact products of the inputs
+        assert np.max(np.abs(got - want)) <= 1e-5 * scale, float(np.max(np.abs(got - want)) / scale)
+    else:                      # one bf16 rounding of a correct fp32 value
+        assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 1e-4 * scale)
+
+
 def test_gemm_bf16_narrow_n():
     _assert_gemm(_gemm_case(384, 64, 256, 1, 1, nc.EP_STORE_F32, BF16, seed=3), BF16, 256, nc.EP_STORE_F32)
     _assert_gemm(_gemm_case(136, 128, 72, 0, 0, nc.EP_STORE_F32, BF16, seed=4), BF16, 72, nc.EP_STORE_F32)
