@@ -156,6 +156,24 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(x, world, device):
+    """The maximum of x over all ranks (every rank gets it); x itself when
+    world == 1.  device: "cuda" under NCCL, "cpu" under gloo."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, tokens_per_step, steps, ms):
+    """Whole-job tokens/s of `world` independent replicas that each ran `steps`
+    steps of `tokens_per_step` tokens, timed by the slowest rank (ms)."""
+    return world * tokens_per_step * steps / (ms / 1e3)
+
+
 def run_reference(args, w):
     world, rank, _ = dist_setup()
     if rank != 0:
@@ -409,13 +427,10 @@ def main():
                                    ctypes.byref(by))
         prof[name] = {"ms": t.value, "launches": n.value, "flops": fl.value, "bytes": by.value}
     model_prof.nc_profile_enable(model.handle, 0)
-    if world > 1:
-        tt = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, "cuda")
 
     tokens_per_step = w.batch * w.seq_len
-    value = world * tokens_per_step * args.steps / (ms / 1e3)
+    value = replica_throughput(world, tokens_per_step, args.steps, ms)
     ms_step = ms / args.steps
 
     # ---- end-to-end through the host-buffer entry point
@@ -429,12 +444,8 @@ def main():
     for _ in range(args.steps):
         model.forward_backward_host(tok_h, tgt_h, grads)
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if world > 1:
-        tt = torch.tensor([e2e_s], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(tt.item())
-    e2e = {"value": world * tokens_per_step * args.steps / e2e_s, "unit": UNIT,
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, "cuda")
+    e2e = {"value": replica_throughput(world, tokens_per_step, args.steps, 1e3 * e2e_s), "unit": UNIT,
            "h2d_bytes_per_step": int(tok_np.nbytes + tgt_np.nbytes), "d2h_bytes_per_step": 8}
 
     peak_burst, peak_sust, hbm, peak_src = load_peaks()
