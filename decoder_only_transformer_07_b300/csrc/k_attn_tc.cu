@@ -1011,22 +1011,35 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (warp == 2) tmem_dealloc(tbase, 512);
 }
 
-// D = rowsum(dO * O) per (row, head), fp32 [B, H, T]; one warp per (row, head).
-template <typename T>
-__global__ void k_attn_rowdot(int64_t rows, int H, int hd, int T_, int64_t ld_o, const T* __restrict__ o,
-                              const T* __restrict__ dout, float* __restrict__ Dv) {
-  int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  int lane = threadIdx.x & 31;
-  if (w >= rows * H) return;
-  int64_t row = w / H;
-  int h = (int)(w % H);
-  const T* a = o + row * ld_o + (int64_t)h * hd;
-  const T* c = dout + row * ld_o + (int64_t)h * hd;
-  float s = 0.f;
-  for (int i = lane; i < hd; i += 32) s += to_f32(a[i]) * to_f32(c[i]);
-  s = warp_sum(s);
-  int b = (int)(row / T_), t = (int)(row % T_);
-  if (lane == 0) Dv[((int64_t)b * H + h) * T_ + t] = s;
+// D = rowsum(dO * O) per (row, head), fp32 [B, H, T].  One warp per row reads
+// O and dO in 16-byte pieces (HD / 8 per head, held by a group of as many
+// consecutive lanes), and each group reduces its head's sum.
+template <int HD>
+__global__ void k_attn_rowdot(int64_t rows, int H, int T_, int64_t ld_o, const bf16* __restrict__ o,
+                              const bf16* __restrict__ dout, float* __restrict__ Dv) {
+  constexpr int CPH = HD / 8;   // 16-byte pieces per head (divides 32)
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int nchunk = H * CPH;
+  const uint4* a = reinterpret_cast<const uint4*>(o + row * ld_o);
+  const uint4* c = reinterpret_cast<const uint4*>(dout + row * ld_o);
+  const int64_t b = row / T_;
+  const int t = (int)(row % T_);
+  for (int c0 = 0; c0 < nchunk; c0 += 32) {
+    const int ci = c0 + lane;
+    float s = 0.f;
+    if (ci < nchunk) {
+      const uint4 x = a[ci], y = c[ci];
+      const bf16* xe = reinterpret_cast<const bf16*>(&x);
+      const bf16* ye = reinterpret_cast<const bf16*>(&y);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s = fmaf(__bfloat162float(xe[e]), __bfloat162float(ye[e]), s);
+    }
+#pragma unroll
+    for (int off = CPH / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (ci < nchunk && (lane % CPH) == 0) Dv[(b * H + ci / CPH) * T_ + t] = s;
+  }
 }
 
 bool at_shape(int B, int T, int H, int Hkv, int hd, int32_t* err, AtShape* sh) {
@@ -1068,7 +1081,7 @@ template <int HD>
 nc_status attn_bwd_tc(const AtShape& sh, const bf16* qkv, const bf16* o, const float* lse, const bf16* dout,
                       bf16* dqkv, float* Dv, cudaStream_t st) {
   const int64_t rows = (int64_t)sh.B * sh.T;
-  k_attn_rowdot<bf16><<<cdiv(rows * sh.H, 8), 256, 0, st>>>(rows, sh.H, HD, sh.T, sh.ld_o, o, dout, Dv);
+  k_attn_rowdot<HD><<<cdiv(rows, 8), 256, 0, st>>>(rows, sh.H, sh.T, sh.ld_o, o, dout, Dv);
   NC_CUDA_TRY(cudaGetLastError());
   CUtensorMap tm_qkv128, tm_qkv64, tm_do128, tm_do64, tm_out;
   if (!make_tmap_bf16_3d(&tm_out, dqkv, sh.ld_qkv, sh.T, sh.B, sh.ld_qkv, 64, 32) ||
@@ -1114,7 +1127,7 @@ nc_status launch_attn_bwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* q
   sh.rstd_qk = rstd_qk;
   sh.rope_tab = rope_tab;
   sh.rope_pair_rows = rope_pair_rows;
-  if (!aligned16(qkv) || !aligned16(dout) || !aligned16(dqkv)) return NC_ERR_ARG;
+  if (!aligned16(qkv) || !aligned16(o) || !aligned16(dout) || !aligned16(dqkv)) return NC_ERR_ARG;
   return hd == 128 ? attn_bwd_tc<128>(sh, qkv, o, lse, dout, dqkv, Dv, st)
                    : attn_bwd_tc<64>(sh, qkv, o, lse, dout, dqkv, Dv, st);
 }

@@ -352,13 +352,112 @@ __global__ void __launch_bounds__(CE_THREADS) k_cross_entropy_bf16(int V, bf16* 
   }
 }
 
+// Wide bf16 rows (V >= 16384): 256 threads per row and up to four rows per SM,
+// so that one row's reductions overlap other rows' memory traffic.  Pass 1
+// streams the row once for its maximum and sum of exponentials (online: the
+// sum is rescaled when the maximum grows); pass 2 reads the row again, while
+// it is still in L2, and writes dz in place.
+#define CE2_THREADS 256
+__global__ void __launch_bounds__(CE2_THREADS, 4) k_cross_entropy_bf16_stream(int V, bf16* __restrict__ z, int64_t ldz,
+                                                                             const int32_t* __restrict__ targets,
+                                                                             float* __restrict__ row_loss, float scale,
+                                                                             int32_t* __restrict__ err) {
+  __shared__ float shm[CE2_THREADS / 32], shs[CE2_THREADS / 32];
+  const int64_t row = blockIdx.x;
+  bf16* zr = z + row * ldz;
+  const uint4* zv = reinterpret_cast<const uint4*>(zr);
+  const int nv = V / 8;
+  const float L2E = 1.4426950408889634f;
+  float m = -INFINITY, sum = 0.f;   // m in log2 units
+  for (int i0 = threadIdx.x; i0 < nv; i0 += 4 * CE2_THREADS) {
+    uint4 u[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (i0 + q * CE2_THREADS < nv) u[q] = zv[i0 + q * CE2_THREADS];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (i0 + q * CE2_THREADS >= nv) break;
+      const bf16* e = reinterpret_cast<const bf16*>(&u[q]);
+      float x[8], cm = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        x[j] = __bfloat162float(e[j]) * L2E;
+        cm = fmaxf(cm, x[j]);
+      }
+      if (cm > m) {
+        sum *= ex2_approx(m - cm);
+        m = cm;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sum += ex2_approx(x[j] - m);
+    }
+  }
+  // (m, sum) over the block: warps by shuffles, then warp 0 over the warps
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, off), os = __shfl_xor_sync(0xffffffffu, sum, off);
+    const float nm = fmaxf(m, om);
+    sum = (m == -INFINITY ? 0.f : sum * ex2_approx(m - nm)) + (om == -INFINITY ? 0.f : os * ex2_approx(om - nm));
+    m = nm;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) { shm[warp] = m; shs[warp] = sum; }
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < CE2_THREADS / 32 ? shm[lane] : -INFINITY;
+    sum = lane < CE2_THREADS / 32 ? shs[lane] : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, m, off), os = __shfl_xor_sync(0xffffffffu, sum, off);
+      const float nm = fmaxf(m, om);
+      sum = (m == -INFINITY ? 0.f : sum * ex2_approx(m - nm)) + (om == -INFINITY ? 0.f : os * ex2_approx(om - nm));
+      m = nm;
+    }
+    if (lane == 0) { shm[0] = m; shs[0] = sum; }
+  }
+  __syncthreads();
+  m = shm[0];
+  sum = shs[0];
+  const int tgt = targets[row];
+  const bool ok = tgt >= 0 && tgt < V;
+  if (threadIdx.x == 0) {
+    const float ztgt = ok ? __bfloat162float(zr[tgt]) : 0.f;
+    if (!ok && err) atomicOr(err, NC_DEVERR_TOKEN);
+    row_loss[row] = ok ? (m + log2f(sum)) * 0.69314718055994531f - ztgt : 0.f;
+  }
+  __syncthreads();   // zr[tgt] is read before pass 2 overwrites it
+  const float inv = scale / sum;
+  uint4* zw = reinterpret_cast<uint4*>(zr);
+  for (int i = threadIdx.x; i < nv; i += CE2_THREADS) {
+    const uint4 u = zv[i];
+    const bf16* e = reinterpret_cast<const bf16*>(&u);
+    float p[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      p[j] = ex2_approx(fmaf(__bfloat162float(e[j]), L2E, -m)) * inv;
+      if (i * 8 + j == tgt) p[j] -= scale;
+    }
+    uint4 o;
+    __nv_bfloat162 q0 = __floats2bfloat162_rn(p[0], p[1]), q1 = __floats2bfloat162_rn(p[2], p[3]);
+    __nv_bfloat162 q2 = __floats2bfloat162_rn(p[4], p[5]), q3 = __floats2bfloat162_rn(p[6], p[7]);
+    o.x = *reinterpret_cast<uint32_t*>(&q0);
+    o.y = *reinterpret_cast<uint32_t*>(&q1);
+    o.z = *reinterpret_cast<uint32_t*>(&q2);
+    o.w = *reinterpret_cast<uint32_t*>(&q3);
+    zw[i] = o;
+  }
+}
+
 nc_status launch_cross_entropy(int dtype, int64_t rows, int V, void* z, int64_t ldz,
                                const int32_t* targets, float* row_loss, float scale, int32_t* err,
                                cudaStream_t st) {
   if (rows <= 0) return NC_OK;
   if (rows > 0x7fffffff) return NC_ERR_ARG;
-  if (dtype == NC_BF16 && V % 8 == 0 && ldz % 8 == 0 && V <= 8 * CE_THREADS * CE_VEC &&
-      (((uintptr_t)z) & 15) == 0)
+  const bool vec = dtype == NC_BF16 && V % 8 == 0 && ldz % 8 == 0 && (((uintptr_t)z) & 15) == 0;
+  if (vec && V >= 16384)
+    k_cross_entropy_bf16_stream<<<(unsigned)rows, CE2_THREADS, 0, st>>>(V, (bf16*)z, ldz, targets, row_loss, scale,
+                                                                        err);
+  else if (vec && V <= 8 * CE_THREADS * CE_VEC)
     k_cross_entropy_bf16<<<(unsigned)rows, CE_THREADS, 0, st>>>(V, (bf16*)z, ldz, targets, row_loss, scale, err);
   else if (dtype == NC_BF16)
     k_cross_entropy<bf16><<<(unsigned)rows, 512, 0, st>>>(V, (bf16*)z, ldz, targets, row_loss, scale, err);

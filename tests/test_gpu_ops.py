@@ -396,6 +396,23 @@ def test_cross_entropy(dt):
     assert ok, worst
 
 
+@pytest.mark.parametrize("V", [16384, 65536])
+def test_cross_entropy_wide_rows_bf16(V):
+    # the vocabulary-sized rows of the step (two-pass streaming kernel)
+    rows = 24
+    Z = dev_tensor(rnd(52, (rows, V), 3.0), BF16)
+    z = to64(Z)
+    tgt = np.random.default_rng(53).integers(0, V, size=rows).astype(np.int32)
+    TG = torch.from_numpy(tgt).cuda()
+    RL = torch.empty(rows, dtype=F32, device="cuda")
+    nc.ops.cross_entropy(Z, TG, RL, 0.25)
+    loss_ref, dz_ref = OM.cross_entropy(z, tgt)
+    torch.cuda.synchronize()
+    assert np.allclose(to64(RL), loss_ref, rtol=1e-5, atol=1e-5)
+    ok, worst = rel_close(to64(Z), 0.25 * dz_ref, 2.0 ** -8, 1e-3)
+    assert ok, worst
+
+
 def test_cross_entropy_flags_bad_target():
     Z = torch.zeros((4, 64), dtype=F32, device="cuda")
     TG = torch.tensor([0, 64, 3, -1], dtype=torch.int32, device="cuda")
