@@ -258,14 +258,32 @@ __device__ __forceinline__ void ld8(const bf16* p, float* f) {
   for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(h[e]);
 }
 
-template <typename E, int MB>
+// NORM: the rows come from the fp32 residual stream and are normalised on the
+// way in, A = act(x * rstd(x)) with rstd = 1/sqrt(mean(x^2) + eps) formed as the
+// RMSNorm kernel forms it (so the staged values are the ones it would write);
+// M <= SK_WARPS then, one warp per row's statistics.
+template <typename E, int MB, bool NORM>
 __global__ void __launch_bounds__(SK_WARPS * 32)
-    k_gemm_skinny(int M, int N, int K, const E* __restrict__ A, int64_t lda, const E* __restrict__ W, int64_t ldw,
-                  int ep, void* __restrict__ D, int64_t ldd) {
+    k_gemm_skinny(int M, int N, int K, const void* __restrict__ Ain, int64_t lda, const E* __restrict__ W,
+                  int64_t ldw, int ep, void* __restrict__ D, int64_t ldd, float eps) {
   constexpr int SK_KC = sk_kc<E, MB>();
   __shared__ __align__(16) E xs[MB][SK_KC];
+  __shared__ float rs[MB];
+  const E* A = reinterpret_cast<const E*>(Ain);
+  const float* X = reinterpret_cast<const float*>(Ain);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * SK_WARPS + warp;
+  if (NORM && warp < M) {
+    const float4* xr = reinterpret_cast<const float4*>(X + (int64_t)warp * lda);
+    float ss = 0.f;
+    for (int c = lane; c < K / 4; c += 32) {
+      const float4 v = xr[c];
+      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) rs[warp] = rsqrtf(ss / (float)K + eps);
+  }
   float acc[MB];
 #pragma unroll
   for (int m = 0; m < MB; ++m) acc[m] = 0.f;
@@ -275,9 +293,15 @@ __global__ void __launch_bounds__(SK_WARPS * 32)
     for (int i = threadIdx.x * 8; i < MB * SK_KC; i += SK_WARPS * 32 * 8) {
       const int m = i / SK_KC, k = i % SK_KC;
       if (m < M && k < kc) {
-        *reinterpret_cast<uint4*>(&xs[m][k]) = *reinterpret_cast<const uint4*>(A + (int64_t)m * lda + k0 + k);
-        if (sizeof(E) == 4) *reinterpret_cast<uint4*>(&xs[m][k + 4]) =
-            *reinterpret_cast<const uint4*>(A + (int64_t)m * lda + k0 + k + 4);
+        if (NORM) {
+          const float r = rs[m];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) st_f(&xs[m][k + e], X[(int64_t)m * lda + k0 + k + e] * r);
+        } else {
+          *reinterpret_cast<uint4*>(&xs[m][k]) = *reinterpret_cast<const uint4*>(A + (int64_t)m * lda + k0 + k);
+          if (sizeof(E) == 4) *reinterpret_cast<uint4*>(&xs[m][k + 4]) =
+              *reinterpret_cast<const uint4*>(A + (int64_t)m * lda + k0 + k + 4);
+        }
       }
     }
     __syncthreads();
@@ -323,22 +347,22 @@ __global__ void __launch_bounds__(SK_WARPS * 32)
   }
 }
 
-template <typename E, int MB>
-nc_status skinny_t(int M, int N, int K, const E* A, int64_t lda, const E* W, int64_t ldw, int ep, void* D, int64_t ldd,
-                   cudaStream_t st) {
-  k_gemm_skinny<E, MB><<<cdiv(N, SK_WARPS), SK_WARPS * 32, 0, st>>>(M, N, K, A, lda, W, ldw, ep, D, ldd);
+template <typename E, int MB, bool NORM>
+nc_status skinny_t(int M, int N, int K, const void* A, int64_t lda, const E* W, int64_t ldw, int ep, void* D,
+                   int64_t ldd, float eps, cudaStream_t st) {
+  k_gemm_skinny<E, MB, NORM><<<cdiv(N, SK_WARPS), SK_WARPS * 32, 0, st>>>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
-template <typename E>
-nc_status skinny_e(int M, int N, int K, const E* A, int64_t lda, const E* W, int64_t ldw, int ep, void* D, int64_t ldd,
-                   cudaStream_t st) {
-  if (M <= 1) return skinny_t<E, 1>(M, N, K, A, lda, W, ldw, ep, D, ldd, st);
-  if (M <= 2) return skinny_t<E, 2>(M, N, K, A, lda, W, ldw, ep, D, ldd, st);
-  if (M <= 4) return skinny_t<E, 4>(M, N, K, A, lda, W, ldw, ep, D, ldd, st);
-  if (M <= 8) return skinny_t<E, 8>(M, N, K, A, lda, W, ldw, ep, D, ldd, st);
-  if (M <= 16) return skinny_t<E, 16>(M, N, K, A, lda, W, ldw, ep, D, ldd, st);
-  return skinny_t<E, 32>(M, N, K, A, lda, W, ldw, ep, D, ldd, st);
+template <typename E, bool NORM>
+nc_status skinny_e(int M, int N, int K, const void* A, int64_t lda, const E* W, int64_t ldw, int ep, void* D,
+                   int64_t ldd, float eps, cudaStream_t st) {
+  if (M <= 1) return skinny_t<E, 1, NORM>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
+  if (M <= 2) return skinny_t<E, 2, NORM>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
+  if (M <= 4) return skinny_t<E, 4, NORM>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
+  if (M <= 8 || NORM) return skinny_t<E, 8, NORM>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
+  if (M <= 16) return skinny_t<E, 16, false>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
+  return skinny_t<E, 32, false>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
 }
 
 }  // namespace
@@ -349,7 +373,16 @@ nc_status launch_gemm_skinny(int dtype, int M, int N, int K, const void* A, int6
       (ep != NC_EP_STORE && ep != NC_EP_STORE_F32 && ep != NC_EP_ACCUM_F32 && ep != NC_EP_RELU2_SQ))
     return NC_ERR_ARG;
   if ((((uintptr_t)A) & 15) || (((uintptr_t)W) & 15)) return NC_ERR_ARG;
-  if (dtype == NC_BF16)
-    return skinny_e<bf16>(M, N, K, (const bf16*)A, lda, (const bf16*)W, ldw, ep, D, ldd, st);
-  return skinny_e<float>(M, N, K, (const float*)A, lda, (const float*)W, ldw, ep, D, ldd, st);
+  if (dtype == NC_BF16) return skinny_e<bf16, false>(M, N, K, A, lda, (const bf16*)W, ldw, ep, D, ldd, 0.f, st);
+  return skinny_e<float, false>(M, N, K, A, lda, (const float*)W, ldw, ep, D, ldd, 0.f, st);
+}
+
+nc_status launch_gemm_skinny_norm(int dtype, int M, int N, int K, const float* x, int64_t ldx, const void* W,
+                                  int64_t ldw, int ep, void* D, int64_t ldd, float eps, cudaStream_t st) {
+  if (M < 1 || M > SK_WARPS || N < 1 || K < 8 || K % 8 || ldx % 4 || ldw % 8 ||
+      (ep != NC_EP_STORE && ep != NC_EP_STORE_F32 && ep != NC_EP_ACCUM_F32 && ep != NC_EP_RELU2_SQ))
+    return NC_ERR_ARG;
+  if ((((uintptr_t)x) & 15) || (((uintptr_t)W) & 15)) return NC_ERR_ARG;
+  if (dtype == NC_BF16) return skinny_e<bf16, true>(M, N, K, x, ldx, (const bf16*)W, ldw, ep, D, ldd, eps, st);
+  return skinny_e<float, true>(M, N, K, x, ldx, (const float*)W, ldw, ep, D, ldd, eps, st);
 }

@@ -213,13 +213,24 @@ __device__ __forceinline__ void st2(bf16* p, float a, float b) {
 template <typename T>
 __global__ void k_rope_qknorm_fwd(int64_t rows, int T_, int nh, int hd, int64_t ld,
                                   T* __restrict__ qkv, float* __restrict__ rstd,
-                                  const float2* __restrict__ tab, float eps, const int32_t* __restrict__ pos0) {
+                                  const float2* __restrict__ tab, float eps, const int32_t* __restrict__ pos0,
+                                  T* __restrict__ kc, T* __restrict__ vc, int hq, int max_len) {
+  // with a cache, Hkv more warps per row copy the v heads into it
+  const int hkv = nh - hq;
+  const int nw = kc ? nh + hkv : nh;
   int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   int lane = threadIdx.x & 31;
-  if (w >= rows * nh) return;
-  int64_t row = w / nh;
-  int j = (int)(w % nh);
+  if (w >= rows * nw) return;
+  int64_t row = w / nw;
+  int j = (int)(w % nw);
   int t = (int)(row % T_) + (pos0 ? *pos0 : 0);
+  const int64_t cache_row = kc ? ((row / T_) * hkv + (j - hq - (j >= nh ? hkv : 0))) * max_len + t : 0;
+  if (j >= nh) {   // v head j - nh: copied as computed
+    const T* src = qkv + row * ld + (int64_t)j * hd;
+    T* dst = vc + cache_row * hd;
+    for (int i = lane; i < hd; i += 32) dst[i] = src[i];
+    return;
+  }
   const int d = hd / 2;
   T* p = qkv + row * ld + (int64_t)j * hd;
   const float2* cs = tab + (int64_t)t * d;
@@ -247,6 +258,11 @@ __global__ void k_rope_qknorm_fwd(int64_t rows, int T_, int nh, int hd, int64_t 
     if (i < d) {
       st2(p + i, y[k][0] * r, y[k][1] * r);
       st2(p + i + d, y[k][2] * r, y[k][3] * r);
+      if (kc && j >= hq) {   // k head j - hq: also into the cache
+        T* q = kc + cache_row * hd;
+        st2(q + i, y[k][0] * r, y[k][1] * r);
+        st2(q + i + d, y[k][2] * r, y[k][3] * r);
+      }
     }
   }
   if (lane == 0) rstd[row * nh + j] = r;
@@ -299,19 +315,23 @@ __global__ void k_rope_qknorm_bwd(int64_t rows, int T_, int nh, int hd, int64_t 
 }
 
 nc_status launch_rope_qknorm_fwd(int dtype, int B, int T, int H, int Hkv, int hd, void* qkv,
-                                 float* rstd, const float* tab, float eps, cudaStream_t st, const int32_t* pos0) {
+                                 float* rstd, const float* tab, float eps, cudaStream_t st, const int32_t* pos0,
+                                 void* kc, void* vc, int max_len) {
   if (hd > 256 || (hd & 3) || (((uintptr_t)qkv) & 7) || (((uintptr_t)tab) & 15)) return NC_ERR_ARG;
   int64_t rows = (int64_t)B * T;
   int nh = H + Hkv;
   int64_t ld = (int64_t)(H + 2 * Hkv) * hd;
-  int64_t warps = rows * nh;
+  if ((kc == nullptr) != (vc == nullptr) || (kc && max_len < 1)) return NC_ERR_ARG;
+  int64_t warps = rows * (nh + (kc ? Hkv : 0));
   if (warps == 0) return NC_OK;
   if (dtype == NC_BF16)
     k_rope_qknorm_fwd<bf16><<<cdiv(warps, 8), 256, 0, st>>>(rows, T, nh, hd, ld, (bf16*)qkv, rstd,
-                                                             (const float2*)tab, eps, pos0);
+                                                             (const float2*)tab, eps, pos0, (bf16*)kc, (bf16*)vc, H,
+                                                             max_len);
   else
     k_rope_qknorm_fwd<float><<<cdiv(warps, 8), 256, 0, st>>>(rows, T, nh, hd, ld, (float*)qkv, rstd,
-                                                              (const float2*)tab, eps, pos0);
+                                                              (const float2*)tab, eps, pos0, (float*)kc, (float*)vc,
+                                                              H, max_len);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 

@@ -1096,13 +1096,22 @@ extern "C" nc_status nc_prefill(nc_model* m, const int32_t* tokens, int32_t B, i
 // for a given B, so the enqueued work can be captured once and replayed.
 static nc_status decode_body(nc_model* m, int B, cudaStream_t st) {
   const int C = m->C, F = m->F, Hd = m->H * m->hd, W = m->qkvw;
-  // the projections of B <= 8 rows are bound by reading the weights once:
-  // CUDA-core skinny GEMM; beyond that the tensor-core GEMM is faster
+  const float eps = m->cfg.norm_eps;
+  // Projections of B <= 8 rows are bound by reading the weights once: CUDA-core
+  // skinny GEMM, with the RMSNorm of its input rows done inside it when the
+  // input is the residual stream.  Beyond that, the tensor-core GEMM after a
+  // separate RMSNorm.
+  const bool skinny = B <= 8;
   auto proj = [&](int role, int N, int K, const void* a, const void* w, int ep, void* d, int64_t ldd) -> nc_status {
-    if (B <= 8) return launch_gemm_skinny(m->dtype, B, N, K, a, K, w, K, ep, d, ldd, st);
+    if (skinny) return launch_gemm_skinny(m->dtype, B, N, K, a, K, w, K, ep, d, ldd, st);
     return gemm(m, role, B, N, K, a, K, 1, w, K, 1, ep, d, ldd, nullptr, 0, st);
   };
-  const float eps = m->cfg.norm_eps;
+  auto norm_proj = [&](int role, int N, const void* w, int ep, void* d, int64_t ldd, void* xn,
+                       float* rstd) -> nc_status {   // d = op(norm(x) W^T)
+    if (skinny) return launch_gemm_skinny_norm(m->dtype, B, N, C, m->x, C, w, C, ep, d, ldd, eps, st);
+    NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, xn, rstd, eps, st));
+    return proj(role, N, C, xn, w, ep, d, ldd);
+  };
   NC_TRY(launch_embed_fwd(m->dtype, B, C, m->V, m->dec_tok, m->master, m->x, m->err, st));
   uint8_t* xn1 = layer_act(m, m->xn1, 0, C);
   uint8_t* xn2 = layer_act(m, m->xn2, 0, C);
@@ -1110,22 +1119,18 @@ static nc_status decode_body(nc_model* m, int B, cudaStream_t st) {
   uint8_t* o = layer_act(m, m->o, 0, Hd);
   uint8_t* h = layer_act(m, m->h, 0, F);
   for (int l = 0; l < m->L; ++l) {
-    NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, xn1, m->rstd1, eps, st));
-    NC_TRY(proj(NC_PROF_GEMM_FWD, W, C, xn1, wptr(m, tensor(m, l, 0)), NC_EP_STORE, qkv, W));
-    // RoPE + QK norm at position *dec_pos (T = 1)
+    NC_TRY(norm_proj(NC_PROF_GEMM_FWD, W, wptr(m, tensor(m, l, 0)), NC_EP_STORE, qkv, W, xn1, m->rstd1));
+    // RoPE + QK norm at position *dec_pos (T = 1); k and v also go into the cache
     NC_TRY(launch_rope_qknorm_fwd(m->dtype, B, 1, m->H, m->Hkv, m->hd, qkv, m->rstdqk, m->rope_tab, eps, st,
-                                  m->dec_pos));
-    NC_TRY(launch_kv_store(m->dtype, B, 1, 0, m->H, m->Hkv, m->hd, qkv, W, kv_layer(m, m->kcache, l),
-                           kv_layer(m, m->vcache, l), m->kv_max, st, m->dec_pos));
+                                  m->dec_pos, kv_layer(m, m->kcache, l), kv_layer(m, m->vcache, l), m->kv_max));
     NC_TRY(launch_decode_attn(m->dtype, B, m->H, m->Hkv, m->hd, 0, qkv, W, kv_layer(m, m->kcache, l),
                               kv_layer(m, m->vcache, l), m->kv_max, m->dec_part, o, Hd, st, m->dec_pos));
     NC_TRY(proj(NC_PROF_GEMM_FWD, C, Hd, o, wptr(m, tensor(m, l, 3)), NC_EP_ACCUM_F32, m->x, C));
-    NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, xn2, m->rstd2, eps, st));
-    NC_TRY(proj(NC_PROF_GEMM_FWD, F, C, xn2, wptr(m, tensor(m, l, 4)), NC_EP_RELU2_SQ, h, F));
+    NC_TRY(norm_proj(NC_PROF_GEMM_FWD, F, wptr(m, tensor(m, l, 4)), NC_EP_RELU2_SQ, h, F, xn2, m->rstd2));
     NC_TRY(proj(NC_PROF_GEMM_FWD, C, F, h, wptr(m, tensor(m, l, 5)), NC_EP_ACCUM_F32, m->x, C));
   }
-  NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, m->xf, m->rstd_f, eps, st));
-  NC_TRY(proj(NC_PROF_GEMM_LM, m->V, C, m->xf, wptr(m, m->layout.back()), NC_EP_STORE_F32, m->dec_logits, m->V));
+  NC_TRY(norm_proj(NC_PROF_GEMM_LM, m->V, wptr(m, m->layout.back()), NC_EP_STORE_F32, m->dec_logits, m->V, m->xf,
+                   m->rstd_f));
   return launch_set_i32(m->dec_pos, 1, true, st);
 }
 

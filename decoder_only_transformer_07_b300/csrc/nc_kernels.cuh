@@ -15,9 +15,12 @@ nc_status launch_rmsnorm_fwd(int dtype, int64_t rows, int C, const float* x, voi
 nc_status launch_rmsnorm_bwd(int dtype, int64_t rows, int C, const float* dy, const void* y,
                              const float* rstd, float* dx, void* dx_act, cudaStream_t st);
 // pos0 (device, may be NULL): positions are *pos0 + row % T instead of row % T.
+// kc, vc (both or neither): also write every row's rotated, normalised k heads
+// and its v heads into a [B][Hkv][max_len][hd] cache at the row's position.
 nc_status launch_rope_qknorm_fwd(int dtype, int B, int T, int H, int Hkv, int hd, void* qkv,
                                  float* rstd, const float* tab, float eps, cudaStream_t st,
-                                 const int32_t* pos0 = nullptr);
+                                 const int32_t* pos0 = nullptr, void* kc = nullptr, void* vc = nullptr,
+                                 int max_len = 0);
 nc_status launch_rope_qknorm_bwd(int dtype, int B, int T, int H, int Hkv, int hd, void* dqkv,
                                  const void* qkv, const float* rstd, const float* tab,
                                  cudaStream_t st);
@@ -137,3 +140,7 @@ size_t decode_part_floats(int B, int H, int hd, int max_len);
 #define SKINNY_MAX_M 32
 nc_status launch_gemm_skinny(int dtype, int M, int N, int K, const void* A, int64_t lda, const void* W, int64_t ldw,
                              int ep, void* D, int64_t ldd, cudaStream_t st);
+// The same with A = act(rmsnorm(x)) of the fp32 rows x (ldx a multiple of 4),
+// the normalisation done in the kernel; 1 <= M <= 8.
+nc_status launch_gemm_skinny_norm(int dtype, int M, int N, int K, const float* x, int64_t ldx, const void* W,
+                                  int64_t ldw, int ep, void* D, int64_t ldd, float eps, cudaStream_t st);
