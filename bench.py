@@ -284,6 +284,59 @@ def run_decode(args):
     model.close()
 
 
+def run_gemm8(args):
+    """The 8-bit GEMM against the bf16 GEMM on the same shape (default: the d20
+    MLP up-projection, 65536 x 5120 x 1280, bf16 output), and the per-tensor
+    quantisation of the bf16 A operand.  The 8-bit tensor-core peak is taken
+    as twice the measured bf16 peak (the nominal fp8 : bf16 dense ratio)."""
+    import torch
+    import decoder_only_transformer_07_b300 as nc
+    torch.cuda.set_device(0)
+    bf16_peak, bf16_sus, hbm, kind = load_peaks()
+    g = torch.Generator(device="cuda").manual_seed(0)
+    M, N, K = args.m, args.n, args.k
+    a8 = torch.randint(0x20, 0x60, (M, K), dtype=torch.uint8, device="cuda", generator=g)
+    b8 = torch.randint(0x20, 0x60, (N, K), dtype=torch.uint8, device="cuda", generator=g)
+    a8 |= torch.randint(0, 2, (M, K), dtype=torch.uint8, device="cuda", generator=g) << 7
+    b8 |= torch.randint(0, 2, (N, K), dtype=torch.uint8, device="cuda", generator=g) << 7
+    sc = torch.tensor([2.0 ** -6, 2.0 ** -7], dtype=torch.float32, device="cuda")
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    A16 = torch.randn((M, K), device="cuda", generator=g).to(torch.bfloat16)
+    B16 = torch.randn((N, K), device="cuda", generator=g).to(torch.bfloat16)
+    W = torch.empty(nc.ops.gemm_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    codes = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    stats = torch.empty(3, dtype=torch.float32, device="cuda")
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.iters):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    flops = 2.0 * M * N * K
+    ms8 = timed(lambda: nc.ops.gemm_fp8(a8, b8, sc[0:1], sc[1:2], D))
+    ms16 = timed(lambda: nc.ops.gemm(A16, True, B16, True, M, N, K, D, ep=0, workspace=W))
+    msq = timed(lambda: nc.ops.quantize_fp8(A16, codes, stats))
+    tf8, tf16 = flops / (ms8 / 1e3) / 1e12, flops / (ms16 / 1e3) / 1e12
+    qbytes = 5.0 * M * K          # two passes: read 2 B per value twice, write 1 B
+    qgbs = qbytes / (msq / 1e3) / 1e9
+    print(json.dumps({"op": "gemm8", "shape": [M, N, K], "iters": args.iters,
+                      "fp8": {"ms": ms8, "tflops": tf8, "peak": 2 * bf16_peak, "frac": tf8 / (2 * bf16_peak),
+                              "frac_of_sustained": tf8 / (2 * bf16_sus)},
+                      "bf16": {"ms": ms16, "tflops": tf16, "frac": tf16 / bf16_peak},
+                      "speedup": ms16 / ms8,
+                      "quantize_bf16": {"ms": msq, "gbs": qgbs, "frac_of_hbm": qgbs / hbm, "bytes": qbytes},
+                      "peak_kind": kind + " (fp8 = 2 x bf16)"}), flush=True)
+
+
 def run_op(args):
     """Single-kernel mode (for ncu captures of one kernel on a small case):
     times --iters launches of one GEMM or one attention forward+backward."""
@@ -349,9 +402,9 @@ def main():
     ap.add_argument("--step-batch", type=int, default=0,
                     help="profiling only: run the step at this batch size instead of the workload's")
     # single-op mode (profiling)
-    ap.add_argument("--op", choices=["gemm", "attn", "attn_fwd", "optim", "decode"])
+    ap.add_argument("--op", choices=["gemm", "gemm8", "attn", "attn_fwd", "optim", "decode"])
     ap.add_argument("--m", type=int, default=65536)
-    ap.add_argument("--n", type=int, default=3840)
+    ap.add_argument("--n", type=int, default=None, help="default 3840 (--op gemm), 5120 (--op gemm8)")
     ap.add_argument("--k", type=int, default=1280)
     ap.add_argument("--a-major", choices=["k", "mn"], default="k")
     ap.add_argument("--b-major", choices=["k", "mn"], default="k")
@@ -363,10 +416,14 @@ def main():
     ap.add_argument("--head-dim", type=int, default=128)
     ap.add_argument("--iters", type=int, default=5)
     args = ap.parse_args()
+    if args.n is None:
+        args.n = 5120 if args.op == "gemm8" else 3840
     if args.op == "optim":
         return run_optim(args)
     if args.op == "decode":
         return run_decode(args)
+    if args.op == "gemm8":
+        return run_gemm8(args)
     if args.op:
         return run_op(args)
     w = S.workload(args.config, **({"batch": args.step_batch} if args.step_batch else {}))

@@ -100,6 +100,8 @@ _SIGS = {
     "nc_debug_set_gemm_pair": (None, [_i32]),
     "nc_debug_set_decode_graph": (None, [_i32]),
     "nc_op_gemm_rows": (_i32, [_i32, _i32, _i32, _i32, _p, _i64, _p, _i64, _i32, _p, _i64, _p]),
+    "nc_op_quantize_fp8": (_i32, [_i32, _p, _i64, _p, _p, _p]),
+    "nc_op_gemm_fp8": (_i32, [_i32, _i32, _i32, _p, _i64, _p, _i64, _p, _p, _i32, _p, _i64, _p]),
     "nc_profile_enable": (_i32, [_p, _i32]),
     "nc_profile_read": (_i32, [_p, _i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64),
                                 ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
@@ -391,6 +393,29 @@ class ops:
         N = W.shape[0]
         _check(_lib.nc_op_gemm_rows(_dtype_code(A), M, N, K, _ptr(A), A.stride(0), _ptr(W), W.stride(0), ep, _ptr(D),
                                     D.stride(0), _stream()), "nc_op_gemm_rows")
+
+    @staticmethod
+    def quantize_fp8(x, codes=None, stats=None):
+        """Per-tensor E4M3 codes of x (fp32 / bf16, contiguous): returns (codes uint8, stats fp32[3] =
+        amax, scale, scale_inv), both on x's device."""
+        import torch
+        if codes is None:
+            codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+        if stats is None:
+            stats = torch.empty(3, dtype=torch.float32, device=x.device)
+        _check(_lib.nc_op_quantize_fp8(_dtype_code(x), _ptr(x), x.numel(), _ptr(codes), _ptr(stats), _stream()),
+               "nc_op_quantize_fp8")
+        return codes, stats
+
+    @staticmethod
+    def gemm_fp8(a8, b8, a_scale_inv, b_scale_inv, D):
+        """D[m, n] = a_scale_inv b_scale_inv sum_k a8[m, k] b8[n, k]; a8, b8 uint8 E4M3 codes (row-major, K
+        innermost); the scales are one-element fp32 device tensors (views); D bf16 or fp32."""
+        M, K = a8.shape
+        N = b8.shape[0]
+        _check(_lib.nc_op_gemm_fp8(M, N, K, _ptr(a8), a8.stride(0), _ptr(b8), b8.stride(0), _ptr(a_scale_inv),
+                                   _ptr(b_scale_inv), _dtype_code(D), _ptr(D), D.stride(0), _stream()),
+               "nc_op_gemm_fp8")
 
     @staticmethod
     def newton_schulz(u, x, steps=5, dtype=None, workspace=None):

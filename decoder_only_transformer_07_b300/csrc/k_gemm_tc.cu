@@ -15,7 +15,11 @@
 //               vector stores to global memory.
 // Operands may be K-major ([rows][K]) or MN-major ([K][rows]); the forward
 // uses K-major A and B, dX = dY W uses an MN-major B, and dW = dY^T X uses
-// MN-major A and B.  Every mbarrier wait is bounded in time: on expiry the
+// MN-major A and B.  The F8 instantiations take E4M3 operands (K-major only)
+// through tcgen05.mma kind::f8f6f4: a 128-byte swizzled row then holds 128
+// elements instead of 64, so every shared-memory offset and descriptor is the
+// same as for bf16 and only the K coordinates double; the epilogue multiplies
+// the fp32 accumulator by the two operands' dequantisation factors.  Every mbarrier wait is bounded in time: on expiry the
 // kernel raises the timeout bit of the error flag, drains its own TMA loads
 // and MMAs (again bounded) and frees its TMEM before returning.
 #include <cuda.h>
@@ -60,6 +64,9 @@ struct TcParams {
   int rope_T, rope_nh, rope_hd;
   int rope_pair_rows;      // 0: table [T][hd/2][2]; > 0: pair-major [hd/4][rope_pair_rows][4]
   float rope_eps;
+  // F8 kernels: D = (*scale_a) (*scale_b) sum_k A8(m,k) B8(n,k)
+  const float* scale_a;
+  const float* scale_b;
 };
 
 // One unit of work of a CTA: k-blocks [k0, k1) of output tile t (slice s).
@@ -101,10 +108,11 @@ struct TcCfg {
   static constexpr size_t SMEM = 1024 + (size_t)BAR_OFF + 256;
 };
 
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A and
-// B, operand majorness, N/8 and M/16.
-__device__ __forceinline__ uint32_t tc_idesc(int bn, int a_mn, int b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+// Instruction descriptor of tcgen05.mma: fp32 accumulator (bits 4-5 = 1); A and
+// B formats (bits 7-9, 10-12) bf16 = 1 for kind::f16, E4M3 = 0 for
+// kind::f8f6f4; operand majorness, N/8 and M/16.
+__device__ __forceinline__ uint32_t tc_idesc(int bn, int a_mn, int b_mn, bool f8 = false) {
+  return (1u << 4) | (f8 ? 0u : ((1u << 7) | (1u << 10))) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
          ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(TC_BM >> 4) << 24);
 }
 
@@ -244,7 +252,7 @@ __device__ __forceinline__ uint32_t stg_off(int r, int u) {
 // place by the result.  Returns false if a bounded wait expired.
 // `ep` is the epilogue kind (p.ep, or NC_EP_STORE_F32 for a split-K partial);
 // columns n_base.. of the box row m0 in tmD's coordinates, clipped at n_lim.
-template <int BN>
+template <int BN, bool F8 = false>
 __device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, int ep, const CUtensorMap* tmD,
                                                    const CUtensorMap* tmAux, uint8_t* stg, uint64_t* aux_bar,
                                                    uint32_t& aux_phase, uint32_t taddr, int n_base, int n_lim, int m0,
@@ -255,6 +263,7 @@ __device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, int ep, co
   const int cc = f32o ? 32 : 64;
   const uint32_t sa = smem_u32(stg);
   const int r = lane;
+  const float alpha = F8 ? __ldg(p.scale_a) * __ldg(p.scale_b) : 1.f;
 #pragma unroll 1
   for (int oc = 0; oc < BN / 2; oc += cc) {
     const int n_out = n_base + oc;
@@ -280,6 +289,10 @@ __device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, int ep, co
       if (pc > 0) {
         tmem_ld_32x32b_x32(taddr + oc + pc, v);
         tmem_ld_wait();
+      }
+      if (F8) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
       }
       if (f32o) {
 #pragma unroll
@@ -429,7 +442,7 @@ __device__ __forceinline__ void tc_epilogue_qkv_rope_staged(const TcParams& p, c
   }
 }
 
-template <int BN>
+template <int BN, bool F8>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmAux, TcParams p) {
@@ -489,7 +502,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
         uint8_t* sb = sa + Cfg::A_BYTES;
         mbar_arrive_expect_tx(&full_bar[stage], Cfg::STAGE_BYTES);
-        const int k0 = kb * TC_BK;
+        const int k0 = kb * (F8 ? 2 * TC_BK : TC_BK);   // elements: 128 bytes of K per slot
         if (!p.a_mn) {
           tma_load_2d(sa, &tmA, &full_bar[stage], k0, tm * TC_BM);
         } else {
@@ -514,7 +527,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
-    const uint32_t idesc = tc_idesc(BN, p.a_mn, p.b_mn);
+    const uint32_t idesc = tc_idesc(BN, p.a_mn, p.b_mn, F8);
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
@@ -534,8 +547,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t sb = sa + Cfg::A_BYTES;
 #pragma unroll
         for (int k = 0; k < TC_BK / 16; ++k) {
-          tc_mma_f16(d_tmem, operand_desc(sa, p.a_mn, k), operand_desc(sb, p.b_mn, k), idesc,
-                     (kb > sg.k0 || k > 0) ? 1u : 0u);
+          if constexpr (F8)
+            tc_mma_f8(d_tmem, operand_desc(sa, 0, k), operand_desc(sb, 0, k), idesc, (kb > sg.k0 || k > 0) ? 1u : 0u);
+          else
+            tc_mma_f16(d_tmem, operand_desc(sa, p.a_mn, k), operand_desc(sb, p.b_mn, k), idesc,
+                       (kb > sg.k0 || k > 0) ? 1u : 0u);
         }
         tc_commit(&empty_bar[stage]);
         if (++stage == S) { stage = 0; phase ^= 1; }
@@ -575,8 +591,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       } else if (p.ep == NC_EP_QKV_ROPE) {
         tc_epilogue_qkv_rope_staged(p, &tmD, stg, taddr + c_lo, tn * BN + c_lo, BN / 2, m0, m, lane);
       } else if (p.tma_epi && !part) {
-        if (!tc_epilogue_staged<BN>(p, p.ep, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
-                                    tn * BN + c_lo, p.N, m0, lane)) {
+        if (!tc_epilogue_staged<BN, F8>(p, p.ep, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
+                                        tn * BN + c_lo, p.N, m0, lane)) {
           fail();
           break;
         }
@@ -652,6 +668,7 @@ struct Tc2Cfg {
   static constexpr size_t SMEM = 1024 + (size_t)BAR_OFF + 256;
 };
 
+template <bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     k_gemm_tc2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmAux, TcParams p) {
@@ -718,17 +735,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         uint8_t* sb = sa + Cfg::A_BYTES;
         const uint32_t fb = full_rank0 + stage * 8;
         if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * Cfg::STAGE_BYTES);
-        const int k0 = kb * Cfg::BK;
+        constexpr int KE = F8 ? 2 : 1;            // a 128-byte chunk holds 64 bf16 or 128 E4M3 values
+        const int k0 = kb * Cfg::BK * KE;
 #pragma unroll
         for (int kc = 0; kc < 2; ++kc) {
           if (!p.a_mn) {
-            tma_load_2d_pair(sa + kc * 16384, &tmA, fb, k0 + 64 * kc, arow);
+            tma_load_2d_pair(sa + kc * 16384, &tmA, fb, k0 + 64 * KE * kc, arow);
           } else {
             tma_load_2d_pair(sa + kc * 16384, &tmA, fb, arow, k0 + 64 * kc);
             tma_load_2d_pair(sa + kc * 16384 + 8192, &tmA, fb, arow + 64, k0 + 64 * kc);
           }
           if (!p.b_mn) {
-            tma_load_2d_pair(sb + kc * 16384, &tmB, fb, k0 + 64 * kc, brow);
+            tma_load_2d_pair(sb + kc * 16384, &tmB, fb, k0 + 64 * KE * kc, brow);
           } else {
             tma_load_2d_pair(sb + kc * 16384, &tmB, fb, brow, k0 + 64 * kc);
             tma_load_2d_pair(sb + kc * 16384 + 8192, &tmB, fb, brow + 64, k0 + 64 * kc);
@@ -739,8 +757,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     }
   } else if (warp == 1 && lane == 0 && leader) {
     // ---------------- MMA issuer (rank 0 only): M = 256, N = 256
-    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)p.a_mn << 15) | ((uint32_t)p.b_mn << 16) |
-                           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+    const uint32_t idesc = (1u << 4) | (F8 ? 0u : ((1u << 7) | (1u << 10))) | ((uint32_t)p.a_mn << 15) |
+                           ((uint32_t)p.b_mn << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
@@ -759,9 +777,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         const uint32_t sa = smem_u32(smem + stage * Cfg::STAGE_BYTES);
         const uint32_t sb = sa + Cfg::A_BYTES;
 #pragma unroll
-        for (int k = 0; k < Cfg::BK / 16; ++k)   // k-chunk k/4 sits 16 KB further
-          tc_mma_f16_pair(d_tmem, operand_desc(sa + (k >> 2) * 16384, p.a_mn, k & 3),
-                          operand_desc(sb + (k >> 2) * 16384, p.b_mn, k & 3), idesc, (kb > sg.k0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < Cfg::BK / 16; ++k) {  // k-chunk k/4 sits 16 KB further
+          if constexpr (F8)
+            tc_mma_f8_pair(d_tmem, operand_desc(sa + (k >> 2) * 16384, 0, k & 3),
+                           operand_desc(sb + (k >> 2) * 16384, 0, k & 3), idesc, (kb > sg.k0 || k > 0) ? 1u : 0u);
+          else
+            tc_mma_f16_pair(d_tmem, operand_desc(sa + (k >> 2) * 16384, p.a_mn, k & 3),
+                            operand_desc(sb + (k >> 2) * 16384, p.b_mn, k & 3), idesc,
+                            (kb > sg.k0 || k > 0) ? 1u : 0u);
+        }
         tc_commit_pair(&empty_bar[stage], 0x3);
         if (++stage == S) { stage = 0; phase ^= 1; }
       }
@@ -803,8 +827,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       } else if (p.ep == NC_EP_QKV_ROPE) {
         tc_epilogue_qkv_rope_staged(p, &tmD, stg, taddr + c_lo, tn * BN + c_lo, BN / 2, m0, m, lane);
       } else if (p.tma_epi) {
-        if (!tc_epilogue_staged<BN>(p, p.ep, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
-                                    tn * BN + c_lo, p.N, m0, lane)) {
+        if (!tc_epilogue_staged<BN, F8>(p, p.ep, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
+                                        tn * BN + c_lo, p.N, m0, lane)) {
           fail();
           break;
         }
@@ -915,11 +939,11 @@ bool make_tmap_bf16_3d(CUtensorMap* tm, const void* base, uint64_t inner, uint64
 int g_num_sms = 0;
 uint64_t g_tc_wait_ns = 4000000000ull;   // bounded-wait limit of the tensor-core kernels
 
-template <int BN>
+template <int BN, bool F8 = false>
 static nc_status launch_tc_bn(TcParams p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
                               const CUtensorMap& tx, size_t ws_bytes, cudaStream_t st) {
   static bool attr_set = false;
-  auto kern = k_gemm_tc<BN>;
+  auto kern = k_gemm_tc<BN, F8>;
   if (!attr_set) {
     NC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<BN>::SMEM));
     attr_set = true;
@@ -958,11 +982,13 @@ static nc_status launch_tc_bn(TcParams p, const CUtensorMap& ta, const CUtensorM
 int g_gemm_pair = 1;       // CTA-pair kernel for eligible shapes (test hook can turn it off)
 
 // 256 x 256 tiles on CTA pairs: persistent grid of co-resident clusters.
+template <bool F8 = false>
 static nc_status launch_tc_pair(TcParams p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
                                 const CUtensorMap& tx, size_t ws_bytes, cudaStream_t st) {
   static int max_clusters = 0;
+  auto kern = k_gemm_tc2<F8>;
   if (!max_clusters) {
-    NC_CUDA_TRY(cudaFuncSetAttribute(k_gemm_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Tc2Cfg::SMEM));
+    NC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Tc2Cfg::SMEM));
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -975,13 +1001,14 @@ static nc_status launch_tc_pair(TcParams p, const CUtensorMap& ta, const CUtenso
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (void*)k_gemm_tc2, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = g_num_sms / 2;
     }
     max_clusters = std::min(n, g_num_sms / 2);
   }
-  p.num_kb = (p.K + Tc2Cfg::BK - 1) / Tc2Cfg::BK;
+  const int bk = Tc2Cfg::BK * (F8 ? 2 : 1);                   // K elements per ring slot
+  p.num_kb = (p.K + bk - 1) / bk;
   p.splits = 1;
   p.kps = p.num_kb;
   const int tiles = p.tiles_m * p.tiles_n;
@@ -1013,7 +1040,7 @@ static nc_status launch_tc_pair(TcParams p, const CUtensorMap& ta, const CUtenso
       return NC_ERR_CUDA;
   }
   const int grid = 2 * std::min(tiles * p.splits, max_clusters);
-  k_gemm_tc2<<<grid, TC_THREADS, Tc2Cfg::SMEM, st>>>(ta, tb, td, tw, p);
+  kern<<<grid, TC_THREADS, Tc2Cfg::SMEM, st>>>(ta, tb, td, tw, p);
   NC_CUDA_TRY(cudaGetLastError());
   if (p.splits > 1) {
     k_gemm_tc_fixup<256, 256><<<tiles * (256 / 32), 256, 0, st>>>(p);
@@ -1061,6 +1088,7 @@ static nc_status gemm_tc_impl(int M, int N, int K, const bf16* A, int64_t lda, i
   p.kps = 0;
   p.rope_tab = nullptr; p.rstd_qk = nullptr; p.rope_T = 1; p.rope_nh = 0; p.rope_hd = 0; p.rope_pair_rows = 0;
   p.rope_eps = 0.f;
+  p.scale_a = nullptr; p.scale_b = nullptr;
   if (rope) {
     // whole heads in each epilogue warp's 128 columns, 16-byte row segments
     if (ep != NC_EP_QKV_ROPE || BN != 256 || (rope->hd != 64 && rope->hd != 128) || (N % rope->hd) ||
@@ -1108,6 +1136,53 @@ nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_
   if (ep == NC_EP_QKV_ROPE) return NC_ERR_ARG;
   return gemm_tc_impl(M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, ep, D, ldd, aux, ldaux, nullptr, err, ws,
                       ws_bytes, st);
+}
+
+// E4M3 GEMM: D[M,N] = (*scale_a) (*scale_b) A8 B8^T, both operands K-major
+// bytes ([M][lda], [N][ldb]), fp32 accumulation; D bf16 or fp32 (row pitch ldd)
+// through the TMA-staged epilogue.  CTA pairs (256 x 256 tiles) when N > 128
+// and M >= 256, the single-CTA kernel otherwise; no split-K.
+nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
+                          const float* scale_a, const float* scale_b, int out_f32, void* D, int64_t ldd,
+                          int32_t* err, cudaStream_t st) {
+  if (M <= 0 || N <= 0) return NC_OK;
+  if (K <= 0 || !A || !B || !D || !scale_a || !scale_b) return NC_ERR_ARG;
+  if ((lda % 16) || (ldb % 16) || lda < K || ldb < K || (((uintptr_t)A) & 15) || (((uintptr_t)B) & 15))
+    return NC_ERR_ARG;
+  if (ldd < N || ((ldd * (out_f32 ? 4 : 2)) % 16) || (((uintptr_t)D) & 15)) return NC_ERR_ARG;
+  if (!g_num_sms) {
+    int dev = 0;
+    NC_CUDA_TRY(cudaGetDevice(&dev));
+    NC_CUDA_TRY(cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev));
+  }
+  const int BN = (N > 128) ? 256 : 128;
+  const bool pair = g_gemm_pair && BN == 256 && M >= 256;
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  p.M = M; p.N = N; p.K = K;
+  p.a_mn = 0; p.b_mn = 0;
+  p.ep = out_f32 ? NC_EP_STORE_F32 : NC_EP_STORE;
+  p.D = D; p.ldd = ldd;
+  p.tiles_m = pair ? (M + 255) / 256 : (M + TC_BM - 1) / TC_BM;
+  p.tiles_n = (N + BN - 1) / BN;
+  p.num_kb = (K + 2 * TC_BK - 1) / (2 * TC_BK);
+  p.err = err;
+  p.wait_ns = g_tc_wait_ns;
+  p.ws = nullptr;
+  p.splits = 1;
+  p.rope_T = 1;
+  p.scale_a = scale_a; p.scale_b = scale_b;
+  // 128-byte (128-element) K boxes; rows 128 (A), BN or 128 per CTA of a pair (B)
+  CUtensorMap ta, tb, td, tx;
+  memset(&tx, 0, sizeof(tx));
+  if (!make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, lda, 128, TC_BM)) return NC_ERR_CUDA;
+  if (!make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, ldb, 128, pair ? 128 : BN)) return NC_ERR_CUDA;
+  p.tma_epi = out_f32 ? make_tmap_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, N, M, ldd, 32, 32)
+                      : make_tmap_bf16_2d(&td, D, N, M, ldd, 64, 32);
+  if (!p.tma_epi) return NC_ERR_CUDA;
+  if (pair) return launch_tc_pair<true>(p, ta, tb, td, tx, 0, st);
+  if (BN == 256) return launch_tc_bn<256, true>(p, ta, tb, td, tx, 0, st);
+  return launch_tc_bn<128, true>(p, ta, tb, td, tx, 0, st);
 }
 
 nc_status launch_gemm_tc_qkv_rope(int M, int N, int K, const bf16* A, int64_t lda, const bf16* Wqkv, int64_t ldb,

@@ -1185,3 +1185,17 @@ extern "C" nc_status nc_op_gemm_rows(int32_t dtype, int32_t M, int32_t N, int32_
   if (!dtype_ok(dtype) || !A || !W || !D) return NC_ERR_ARG;
   return launch_gemm_skinny(dtype, M, N, K, A, lda, W, ldw, ep, D, ldd, as_stream(stream));
 }
+
+extern "C" nc_status nc_op_quantize_fp8(int32_t dtype, const void* x_dev, int64_t n, uint8_t* codes_dev,
+                                        float* stats_dev, void* stream) {
+  return launch_quantize_fp8(dtype, x_dev, n, codes_dev, stats_dev, as_stream(stream));
+}
+
+extern "C" nc_status nc_op_gemm_fp8(int32_t M, int32_t N, int32_t K, const uint8_t* a_dev, int64_t lda,
+                                    const uint8_t* b_dev, int64_t ldb, const float* a_scale_inv_dev,
+                                    const float* b_scale_inv_dev, int32_t out_dtype, void* d_dev, int64_t ldd,
+                                    void* stream) {
+  if (M < 0 || N < 0 || K < 0 || (out_dtype != NC_BF16 && out_dtype != NC_FP32)) return NC_ERR_ARG;
+  return launch_gemm_fp8(M, N, K, a_dev, lda, b_dev, ldb, a_scale_inv_dev, b_scale_inv_dev, out_dtype == NC_FP32,
+                         d_dev, ldd, nullptr, as_stream(stream));
+}

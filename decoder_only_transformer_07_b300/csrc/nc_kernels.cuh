@@ -58,6 +58,16 @@ nc_status launch_gemm_tc_qkv_rope(int M, int N, int K, const bf16* A, int64_t ld
                                   bf16* qkv, int64_t ldd, int T, int nh, int hd, const float* tab, int pair_rows,
                                   float* rstd, float eps, int32_t* err, cudaStream_t st);
 
+// E4M3 GEMM on the tensor cores (kind::f8f6f4): D[M, N] = (*scale_a) (*scale_b)
+// A[M, K] B[N, K]^T, operands K-major bytes (lda, ldb multiples of 16, bases
+// 16-byte aligned), fp32 accumulation, D bf16 (out_f32 = 0) or fp32.
+nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
+                          const float* scale_a, const float* scale_b, int out_f32, void* D, int64_t ldd,
+                          int32_t* err, cudaStream_t st);
+// Per-tensor E4M3 quantisation of n fp32 / bf16 values: stats (device, 3
+// floats) gets {amax, scale, scale_inv}; y the codes.
+nc_status launch_quantize_fp8(int dtype, const void* x, int64_t n, uint8_t* y, float* stats, cudaStream_t st);
+
 nc_status launch_attn_fwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv, void* o,
                                float* lse, cudaStream_t st);
 nc_status launch_attn_bwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv,

@@ -445,6 +445,35 @@ nc_status nc_decode_step(nc_model* m, const int32_t* tokens_dev, int32_t B, floa
 /* Positions held per sequence (-1 for NULL). */
 int32_t nc_kv_cache_length(const nc_model* m);
 
+/* ------------------------------------------------------------------------
+ * 8-bit floating-point GEMM (woshipm nanochat analysis §一.2 and §六.2: FP8
+ * as a training speed lever; the pages fix no recipe).  Values are OCP FP8
+ * E4M3 codes (1 sign, 4 exponent bits of bias 7, 3 mantissa bits; largest
+ * finite 448, no infinities, 0x7f / 0xff NaN) with one fp32 scale per tensor.
+ * ---------------------------------------------------------------------- */
+/* Quantise n values of x_dev (dtype NC_FP32 or NC_BF16, device, 16-byte
+ * aligned) to E4M3 codes in codes_dev (device, n bytes, 8-byte aligned):
+ *   amax = max |x|;  scale = fl32(448 / amax), or 1 if that is not finite
+ *   and positive;  code_i = E4M3(fl32(x_i * scale)), round to nearest even,
+ *   saturating at +-448;  scale_inv = fl32(1 / scale).
+ * stats_dev (device, 3 floats, 4-byte aligned) receives {amax, scale,
+ * scale_inv}; element 0 is also the running maximum while the call runs.
+ * Inputs must be finite.  n = 0 writes stats {0, 1, 1} only.  Does not
+ * synchronise. */
+nc_status nc_op_quantize_fp8(int32_t dtype, const void* x_dev, int64_t n, uint8_t* codes_dev,
+                             float* stats_dev, void* stream);
+/* D[M, N] = (*a_scale_inv) (*b_scale_inv) sum_k A(m, k) B(n, k) with A, B
+ * E4M3 codes, both K-major: A[M][lda], B[N][ldb] bytes (lda, ldb >= K and
+ * multiples of 16, bases 16-byte aligned).  The scales are device pointers
+ * (e.g. element 2 of nc_op_quantize_fp8's stats).  fp32 accumulation on the
+ * tensor cores; out_dtype NC_BF16 or NC_FP32 gives D's type, row pitch ldd
+ * elements (16-byte aligned base and rows).  NC_ERR_ARG on a violated
+ * precondition.  Does not synchronise. */
+nc_status nc_op_gemm_fp8(int32_t M, int32_t N, int32_t K, const uint8_t* a_dev, int64_t lda,
+                         const uint8_t* b_dev, int64_t ldb, const float* a_scale_inv_dev,
+                         const float* b_scale_inv_dev, int32_t out_dtype, void* d_dev, int64_t ldd,
+                         void* stream);
+
 #ifdef __cplusplus
 }
 #endif

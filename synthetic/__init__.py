@@ -94,3 +94,17 @@ def batch_tokens(w, seed=TOKEN_SEED, batch=None, seq_len=None):
     T = w.seq_len if seq_len is None else seq_len
     s = token_stream(w.vocab, B, T, w.tokens, seed)
     return np.ascontiguousarray(s[:, :T]), np.ascontiguousarray(s[:, 1:])
+
+
+FP8_SEED = 3
+
+
+def fp8_codes(rows, cols, seed=FP8_SEED):
+    """Random E4M3 byte codes for the 8-bit GEMM's operands: exponent fields
+    4..11 (magnitudes 2^-3 .. 30, the range a per-tensor scale maps a
+    normal-like activation's bulk into), any mantissa, random sign.  No NaN
+    code (0x7f / 0xff) can occur."""
+    rng = np.random.default_rng(seed)
+    mag = rng.integers(0x20, 0x60, size=(rows, cols), dtype=np.uint8)
+    sign = rng.integers(0, 2, size=(rows, cols), dtype=np.uint8) << 7
+    return mag | sign
