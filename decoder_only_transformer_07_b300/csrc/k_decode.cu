@@ -8,12 +8,16 @@
 // (sequence, kv head) is contiguous and read once for the whole query group.
 //
 // Decode attention is split over the key positions (flash decoding): CTA
-// (b, g, s) takes keys [256 s, 256 s + 256) of kv head g for every query head
-// of its group, each warp an interleaved quarter of them with an online
-// softmax, and leaves a partial (max, sum, unnormalised output) per head; a
-// second kernel merges the partials of a row.  Scores are q.k / sqrt(hd) in
-// fp32 (exp2 form), as in the training attention.
+// (b, g, s) takes the CK keys [CK s, CK s + CK) of kv head g for every query
+// head of its group.  It stages their K and V rows in shared memory with
+// 16-byte asynchronous copies (rows padded by 16 bytes, so that lanes reading
+// different rows hit different banks), computes every (head, key) score at
+// once, one per thread, then the chunk's softmax statistics per head, then the
+// unnormalised output with one output column per thread, and leaves a partial
+// (max, sum, output) per head; a second kernel merges the partials of a row.
+// Scores are q.k / sqrt(hd) in fp32 (exp2 form), as in the training attention.
 #include "nc_kernels.cuh"
+#include "nc_ptx.cuh"
 
 namespace {
 
@@ -41,138 +45,181 @@ __global__ void k_kv_store(int64_t rows, int T, int t0, const int32_t* __restric
   vc[dst] = qkv[r * ld + (int64_t)(H + Hkv + g) * hd + d];
 }
 
-constexpr int DEC_CHUNK = 256;
-constexpr int DEC_WARPS = 4;
+constexpr int DEC_THREADS = 128;
+// Keys per CTA: 64 rows of bf16, 32 of fp32, so that K and V stay within the
+// static shared-memory limit; the partial buffer is sized for the smaller.
+template <typename E>
+__host__ __device__ constexpr int dec_chunk() { return sizeof(E) == 2 ? 64 : 32; }
+constexpr int DEC_CHUNK_MIN = 32;
+
+__device__ __forceinline__ void ld_unit(const uint8_t* p, const float*, float* f) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+}
+__device__ __forceinline__ void ld_unit(const uint8_t* p, const bf16*, float* f) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const bf16* h = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(h[e]);
+}
 
 // Partials: part[((b * H + h) * nsplit + s) * (HD + 2) + {0: max (log2 units), 1: sum, 2..: output}]
 // len_dev (device, may be NULL): the key count is *len_dev + 1 (the position of
 // the token just appended, plus one); chunks past it leave empty partials.
 template <typename E, int HD, int G>
-__global__ void __launch_bounds__(DEC_WARPS * 32)
+__global__ void __launch_bounds__(DEC_THREADS)
     k_decode_attn(int H, int Hkv, int len, const int32_t* __restrict__ len_dev, int nsplit,
                   const E* __restrict__ qkv, int64_t ld, const E* __restrict__ kc, const E* __restrict__ vc,
                   int max_len, float scale_log2, float* __restrict__ part) {
-  constexpr int DPL = HD / 32;
+  constexpr int CK = dec_chunk<E>();
+  constexpr int EPU = 16 / (int)sizeof(E);              // elements per 16-byte unit
+  constexpr int UPR = HD / EPU;                         // units per row
+  constexpr int RB = HD * (int)sizeof(E) + 16;          // padded row bytes in shared memory
+  static_assert(HD <= DEC_THREADS && DEC_THREADS % HD == 0, "one output column per thread");
+  __shared__ __align__(16) uint8_t ks[CK * RB];
+  __shared__ __align__(16) uint8_t vs[CK * RB];
+  __shared__ float qs[G][HD];
+  __shared__ float ps[G][CK];
+  __shared__ float mh[G], sh[G];
   if (len_dev) len = *len_dev + 1;
   const int bg = blockIdx.x, s = blockIdx.y;
   const int b = bg / Hkv, g = bg % Hkv;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int k0 = s * DEC_CHUNK, k1 = min(len, k0 + DEC_CHUNK);
-  float q[G][DPL], mx[G], sm[G], o[G][DPL];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const E* qp = qkv + (int64_t)b * ld + (int64_t)(g * G + h) * HD + lane * DPL;
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) {
-      q[h][i] = ld_f(qp + i) * scale_log2;
-      o[h][i] = 0.f;
+  const int tid = threadIdx.x;
+  const int k0 = s * CK;
+  const int nk = min(len - k0, CK);
+  // head g * G + h of row b: partial at pbase + h * nsplit * (HD + 2)
+  float* pbase = part + ((int64_t)(b * H + g * G) * nsplit + s) * (HD + 2);
+  if (nk <= 0) {
+    if (tid < G) {
+      pbase[(int64_t)tid * nsplit * (HD + 2)] = -INFINITY;
+      pbase[(int64_t)tid * nsplit * (HD + 2) + 1] = 0.f;
     }
-    mx[h] = -INFINITY;
-    sm[h] = 0.f;
+    return;
   }
-  const E* kb = kc + ((int64_t)(b * Hkv + g) * max_len) * HD + lane * DPL;
-  const E* vb = vc + ((int64_t)(b * Hkv + g) * max_len) * HD + lane * DPL;
-  for (int t = k0 + warp; t < k1; t += DEC_WARPS) {
-    float kv[DPL], vv[DPL];
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) {
-      kv[i] = ld_f(kb + (int64_t)t * HD + i);
-      vv[i] = ld_f(vb + (int64_t)t * HD + i);
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float sc = 0.f;
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) sc = fmaf(q[h][i], kv[i], sc);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
-      const float mn = fmaxf(mx[h], sc);
-      const float alpha = exp2f(mx[h] - mn), p = exp2f(sc - mn);
-      sm[h] = fmaf(sm[h], alpha, p);
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) o[h][i] = fmaf(o[h][i], alpha, p * vv[i]);
-      mx[h] = mn;
-    }
+  const int64_t row0 = ((int64_t)(b * Hkv + g) * max_len + k0) * HD;
+  const uint8_t* kg = reinterpret_cast<const uint8_t*>(kc + row0);
+  const uint8_t* vg = reinterpret_cast<const uint8_t*>(vc + row0);
+  for (int i = tid; i < nk * UPR; i += DEC_THREADS) {
+    const int r = i / UPR, u = i - r * UPR;
+    cp_async16(ks + r * RB + u * 16, kg + (int64_t)i * 16);
+    cp_async16(vs + r * RB + u * 16, vg + (int64_t)i * 16);
   }
-  // merge the warps' partials through shared memory; warp 0 writes the CTA's
-  __shared__ float sm_mx[DEC_WARPS][G], sm_sum[DEC_WARPS][G], sm_o[DEC_WARPS][G][HD];
+  cp_async_commit();
+  for (int i = tid; i < G * HD; i += DEC_THREADS) {
+    const int h = i / HD, d = i - h * HD;
+    qs[h][d] = ld_f(qkv + (int64_t)b * ld + (int64_t)(g * G + h) * HD + d) * scale_log2;
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  // scores, one (head, key) per thread
+  for (int i = tid; i < G * CK; i += DEC_THREADS) {
+    const int h = i / CK, key = i - h * CK;
+    if (key < nk) {
+      const uint8_t* kr = ks + key * RB;
+      float acc = 0.f;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    if (lane == 0) {
-      sm_mx[warp][h] = mx[h];
-      sm_sum[warp][h] = sm[h];
+      for (int u = 0; u < UPR; ++u) {
+        float kf[EPU];
+        ld_unit(kr + u * 16, (const E*)nullptr, kf);
+#pragma unroll
+        for (int e = 0; e < EPU; ++e) acc = fmaf(qs[h][u * EPU + e], kf[e], acc);
+      }
+      ps[h][key] = acc;
     }
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) sm_o[warp][h][lane * DPL + i] = o[h][i];
   }
   __syncthreads();
-  if (warp != 0) return;
+  // per head: the chunk's maximum, p = 2^(s - max) in place, and their sum
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int h = warp; h < G; h += DEC_THREADS / 32) {
+    float m = -INFINITY;
+    for (int key = lane; key < nk; key += 32) m = fmaxf(m, ps[h][key]);
+    m = warp_max(m);
+    float sum = 0.f;
+    for (int key = lane; key < nk; key += 32) {
+      const float p = exp2f(ps[h][key] - m);
+      ps[h][key] = p;
+      sum += p;
+    }
+    sum = warp_sum(sum);
+    if (lane == 0) {
+      mh[h] = m;
+      sh[h] = sum;
+    }
+  }
+  __syncthreads();
+  // output column d of heads h0, h0 + STEP, ... (STEP = threads / HD)
+  constexpr int STEP = DEC_THREADS / HD;
+  constexpr int NJ = (G + STEP - 1) / STEP;
+  const int d = tid % HD, h0 = tid / HD;
+  float acc[NJ];
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float M = -INFINITY;
-    for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, sm_mx[w][h]);
-    float S = 0.f, acc[DPL];
+  for (int j = 0; j < NJ; ++j) acc[j] = 0.f;
+  for (int key = 0; key < nk; ++key) {
+    const float v = ld_f(reinterpret_cast<const E*>(vs + key * RB) + d);
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-    if (M != -INFINITY) {
-      for (int w = 0; w < DEC_WARPS; ++w) {
-        const float f = exp2f(sm_mx[w][h] - M);   // 0 for a warp that saw no key
-        S = fmaf(sm_sum[w][h], f, S);
+    for (int j = 0; j < NJ; ++j) {
+      const int h = h0 + STEP * j;
+      if (h < G) acc[j] = fmaf(ps[h][key], v, acc[j]);
+    }
+  }
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) acc[i] = fmaf(sm_o[w][h][lane * DPL + i], f, acc[i]);
+  for (int j = 0; j < NJ; ++j) {
+    const int h = h0 + STEP * j;
+    if (h < G) {
+      float* pp = pbase + (int64_t)h * nsplit * (HD + 2);
+      pp[2 + d] = acc[j];
+      if (d == 0) {
+        pp[0] = mh[h];
+        pp[1] = sh[h];
       }
     }
-    float* pp = part + ((int64_t)(b * H + g * G + h) * nsplit + s) * (HD + 2);
-    if (lane == 0) {
-      pp[0] = M;
-      pp[1] = S;
-    }
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) pp[2 + lane * DPL + i] = acc[i];
   }
 }
 
-// o[b, h*HD + d] = merged output of row (b, h); one warp per row.
+// o[b, h*HD + d] = merged output of row (b, h); one block of HD threads per
+// row: the splits' weights 2^(max_s - max) and the total sum in parallel, then
+// output column d per thread over all splits (independent loads).  Dynamic
+// shared memory: nsplit floats.
 template <typename E, int HD>
-__global__ void k_decode_combine(int64_t rows, int nsplit, const float* __restrict__ part, E* __restrict__ out,
-                                 int64_t ldo, int H) {
-  constexpr int DPL = HD / 32;
-  const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
+__global__ void __launch_bounds__(HD) k_decode_combine(int nsplit, const float* __restrict__ part,
+                                                       E* __restrict__ out, int64_t ldo, int H) {
+  extern __shared__ float fw[];
+  __shared__ float red[32];
+  const int64_t r = blockIdx.x;
+  const int tid = threadIdx.x;
   const float* pr = part + r * nsplit * (HD + 2);
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pr[s * (HD + 2)]);
-  float S = 0.f, acc[DPL];
-#pragma unroll
-  for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-  for (int s = 0; s < nsplit; ++s) {
-    const float* ps = pr + s * (HD + 2);
-    if (ps[0] == -INFINITY) continue;
-    const float f = exp2f(ps[0] - M);
-    S = fmaf(ps[1], f, S);
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) acc[i] = fmaf(ps[2 + lane * DPL + i], f, acc[i]);
+  float m = -INFINITY;
+  for (int s = tid; s < nsplit; s += HD) m = fmaxf(m, pr[(int64_t)s * (HD + 2)]);
+  m = block_max(m, red);
+  float S = 0.f;
+  for (int s = tid; s < nsplit; s += HD) {
+    const float ms = pr[(int64_t)s * (HD + 2)];
+    const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - m);   // an empty split weighs nothing
+    fw[s] = f;
+    S = fmaf(pr[(int64_t)s * (HD + 2) + 1], f, S);
   }
-  const float inv = S > 0.f ? 1.f / S : 0.f;
+  S = block_sum(S, red);
+  __syncthreads();
+  float acc = 0.f;
+#pragma unroll 8
+  for (int s = 0; s < nsplit; ++s) acc = fmaf(fw[s], pr[(int64_t)s * (HD + 2) + 2 + tid], acc);
   const int64_t b = r / H;
   const int h = (int)(r % H);
-  E* op = out + b * ldo + (int64_t)h * HD + lane * DPL;
-#pragma unroll
-  for (int i = 0; i < DPL; ++i) st_f(op + i, acc[i] * inv);
+  st_f(out + b * ldo + (int64_t)h * HD + tid, S > 0.f ? acc / S : 0.f);
 }
 
 template <typename E, int HD, int G>
 nc_status decode_attn_t(int B, int H, int Hkv, int len, const int32_t* len_dev, const E* qkv, int64_t ld,
                         const E* kc, const E* vc, int max_len, float* part, E* o, int64_t ldo, cudaStream_t st) {
   // with the length on the device the grid covers the whole capacity
-  const int nsplit = ((len_dev ? max_len : len) + DEC_CHUNK - 1) / DEC_CHUNK;
+  constexpr int CK = dec_chunk<E>();
+  const int nsplit = ((len_dev ? max_len : len) + CK - 1) / CK;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
-  k_decode_attn<E, HD, G><<<dim3((unsigned)(B * Hkv), (unsigned)nsplit), DEC_WARPS * 32, 0, st>>>(
+  k_decode_attn<E, HD, G><<<dim3((unsigned)(B * Hkv), (unsigned)nsplit), DEC_THREADS, 0, st>>>(
       H, Hkv, len, len_dev, nsplit, qkv, ld, kc, vc, max_len, scale_log2, part);
   NC_CUDA_TRY(cudaGetLastError());
-  const int64_t rows = (int64_t)B * H;
-  k_decode_combine<E, HD><<<cdiv(rows, 8), 256, 0, st>>>(rows, nsplit, part, o, ldo, H);
+  if ((size_t)nsplit * sizeof(float) > 48 * 1024) return NC_ERR_UNSUPPORTED;
+  k_decode_combine<E, HD><<<(unsigned)(B * H), HD, nsplit * sizeof(float), st>>>(nsplit, part, o, ldo, H);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
@@ -192,7 +239,7 @@ nc_status decode_attn_g(int G, int B, int H, int Hkv, int len, const int32_t* le
 }  // namespace
 
 size_t decode_part_floats(int B, int H, int hd, int max_len) {
-  return (size_t)B * H * ((max_len + DEC_CHUNK - 1) / DEC_CHUNK) * (hd + 2);
+  return (size_t)B * H * ((max_len + DEC_CHUNK_MIN - 1) / DEC_CHUNK_MIN) * (hd + 2);
 }
 
 nc_status launch_kv_store(int dtype, int64_t rows, int T, int t0, int H, int Hkv, int hd, const void* qkv, int64_t ld,
@@ -238,99 +285,78 @@ nc_status launch_set_i32(int32_t* p, int32_t v, bool add, cudaStream_t st) {
 // projections: one row per sequence).  With so few rows every weight is used
 // M times at most, so the product is bound by reading W once; it runs on the
 // CUDA cores with one warp per output column n streaming W's row n in 16-byte
-// pieces, and A staged in shared memory in K chunks that all 8 warps of the
-// CTA share.  Accumulation is fp32 in a fixed order.
+// pieces, eight in flight per lane.  The grid is persistent (two CTAs per SM):
+// a CTA stages A in shared memory once (all of K when it fits in the dynamic
+// shared-memory budget, else chunk by chunk for every column group) and walks
+// column groups of 8, each warp issuing the next batch of pieces - of this
+// column or of its next column - before it uses the current one.
+// Accumulation is fp32 in a fixed order.
 namespace {
 
 constexpr int SK_WARPS = 8;
-// K chunk staged per round: 1024, or less so that the chunk of A stays within 32 KB
-template <typename E, int MB>
-__host__ __device__ constexpr int sk_kc() { return MB * (int)sizeof(E) * 1024 <= 32768 ? 1024 : 32768 / (MB * (int)sizeof(E)); }
+constexpr int SK_PIECES = 8;                 // 16-byte pieces of W in flight per lane
+constexpr int SK_SMEM_MAX = 100 * 1024;      // dynamic shared memory of a CTA: two CTAs per SM
 
-__device__ __forceinline__ void ld8(const float* p, float* f) {
-  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-}
 __device__ __forceinline__ void ld8(const bf16* p, float* f) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
   const bf16* h = reinterpret_cast<const bf16*>(&u);
 #pragma unroll
   for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(h[e]);
 }
+__device__ __forceinline__ void unpack(const uint4& u, const float*, float* f) {
+  f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y); f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ void unpack(const uint4& u, const bf16*, float* f) {
+  const bf16* h = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(h[e]);
+}
 
-// NORM: the rows come from the fp32 residual stream and are normalised on the
-// way in, A = act(x * rstd(x)) with rstd = 1/sqrt(mean(x^2) + eps) formed as the
-// RMSNorm kernel forms it (so the staged values are the ones it would write);
-// M <= SK_WARPS then, one warp per row's statistics.
-template <typename E, int MB, bool NORM>
-__global__ void __launch_bounds__(SK_WARPS * 32)
-    k_gemm_skinny(int M, int N, int K, const void* __restrict__ Ain, int64_t lda, const E* __restrict__ W,
-                  int64_t ldw, int ep, void* __restrict__ D, int64_t ldd, float eps) {
-  constexpr int SK_KC = sk_kc<E, MB>();
-  __shared__ __align__(16) E xs[MB][SK_KC];
-  __shared__ float rs[MB];
-  const E* A = reinterpret_cast<const E*>(Ain);
-  const float* X = reinterpret_cast<const float*>(Ain);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = blockIdx.x * SK_WARPS + warp;
-  if (NORM && warp < M) {
-    const float4* xr = reinterpret_cast<const float4*>(X + (int64_t)warp * lda);
-    float ss = 0.f;
-    for (int c = lane; c < K / 4; c += 32) {
-      const float4 v = xr[c];
-      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-    }
+// Pieces u < SK_PIECES of the batch at column kb: lane l's piece u covers
+// columns kb + (32 u + l) EPU ..+EPU (32 lanes read 512 contiguous bytes);
+// pieces at or past kc are not loaded.
+template <typename E>
+__device__ __forceinline__ void sk_load(const E* wr, int kb, int kc, int lane, uint4* w) {
+  constexpr int EPU = 16 / (int)sizeof(E);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) rs[warp] = rsqrtf(ss / (float)K + eps);
+  for (int u = 0; u < SK_PIECES; ++u) {
+    const int k = kb + (32 * u + lane) * EPU;
+    if (k < kc) w[u] = __ldg(reinterpret_cast<const uint4*>(wr + k));
   }
-  float acc[MB];
+}
+
+// acc[m] += the batch at column kb (pieces below kc) times rows m of xs (row pitch ldx)
+template <typename E, int MB>
+__device__ __forceinline__ void sk_fma(const E* xs, int ldx, int M, int kb, int kc, int lane, const uint4* w,
+                                       float* acc) {
+  constexpr int EPU = 16 / (int)sizeof(E);
 #pragma unroll
-  for (int m = 0; m < MB; ++m) acc[m] = 0.f;
-  for (int k0 = 0; k0 < K; k0 += SK_KC) {
-    const int kc = min(SK_KC, K - k0);
-    __syncthreads();
-    for (int i = threadIdx.x * 8; i < MB * SK_KC; i += SK_WARPS * 32 * 8) {
-      const int m = i / SK_KC, k = i % SK_KC;
-      if (m < M && k < kc) {
-        if (NORM) {
-          const float r = rs[m];
+  for (int u = 0; u < SK_PIECES; ++u) {
+    const int k = kb + (32 * u + lane) * EPU;
+    if (k < kc) {
+      float wf[EPU];
+      unpack(w[u], (const E*)nullptr, wf);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) st_f(&xs[m][k + e], X[(int64_t)m * lda + k0 + k + e] * r);
-        } else {
-          *reinterpret_cast<uint4*>(&xs[m][k]) = *reinterpret_cast<const uint4*>(A + (int64_t)m * lda + k0 + k);
-          if (sizeof(E) == 4) *reinterpret_cast<uint4*>(&xs[m][k + 4]) =
-              *reinterpret_cast<const uint4*>(A + (int64_t)m * lda + k0 + k + 4);
-        }
-      }
-    }
-    __syncthreads();
-    if (n < N) {
-      const E* wr = W + (int64_t)n * ldw + k0;
-      // four 16-byte pieces of the row in flight per lane before any is used
-      for (int kb = lane * 8; kb < kc; kb += 1024) {
-        float w[4][8];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (kb + 256 * u < kc) ld8(wr + kb + 256 * u, w[u]);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int k = kb + 256 * u;
-          if (k >= kc) break;
-#pragma unroll
-          for (int m = 0; m < MB; ++m) {
-            if (m < M) {
-              float x[8];
-              ld8(&xs[m][k], x);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) acc[m] = fmaf(x[e], w[u][e], acc[m]);
-            }
+      for (int m = 0; m < MB; ++m) {
+        if (m < M) {
+          float x[EPU];
+          if constexpr (EPU == 8) {
+            ld8(xs + (int64_t)m * ldx + k, x);
+          } else {
+            const float4 a = *reinterpret_cast<const float4*>(xs + (int64_t)m * ldx + k);
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
           }
+#pragma unroll
+          for (int e = 0; e < EPU; ++e) acc[m] = fmaf(x[e], wf[e], acc[m]);
         }
       }
     }
   }
-  if (n >= N) return;
+}
+
+// Warp-wide sums of acc[m] and the epilogue of column n.
+template <typename E, int MB>
+__device__ __forceinline__ void sk_store(const float* acc, int M, int n, int lane, int ep, void* D, int64_t ldd) {
 #pragma unroll
   for (int m = 0; m < MB; ++m) {
     float v = acc[m];
@@ -347,11 +373,162 @@ __global__ void __launch_bounds__(SK_WARPS * 32)
   }
 }
 
+// NORM: the rows come from the fp32 residual stream and are normalised on the
+// way in, A = act(x * rstd(x)), rstd = 1/sqrt(mean(x^2) + eps) in fp32 (the
+// RMSNorm kernel's formula; the sum of squares is taken in another order, so
+// rstd may differ from that kernel's in the last bit); M <= SK_WARPS then.
+// Dynamic shared memory: xs [MB][KC] then rs [MB] and red [SK_WARPS][MB].
+template <typename E, int MB, bool NORM>
+__global__ void __launch_bounds__(SK_WARPS * 32)
+    k_gemm_skinny(int M, int N, int K, int KC, const void* __restrict__ Ain, int64_t lda, const E* __restrict__ W,
+                  int64_t ldw, int ep, void* __restrict__ D, int64_t ldd, float eps) {
+  constexpr int EPU = 16 / (int)sizeof(E);
+  constexpr int BATCH = 32 * SK_PIECES * EPU;          // K columns per batch of pieces
+  extern __shared__ __align__(16) uint8_t sk_smem[];
+  E* xs = reinterpret_cast<E*>(sk_smem);
+  float* rs = reinterpret_cast<float*>(sk_smem + (size_t)MB * KC * sizeof(E));
+  float* red = rs + MB;
+  const E* A = reinterpret_cast<const E*>(Ain);
+  const float* X = reinterpret_cast<const float*>(Ain);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ngroups = (N + SK_WARPS - 1) / SK_WARPS;
+  const int nchunks = (K + KC - 1) / KC;
+
+  // columns [k0, k0 + kc) of the M rows of A into xs
+  auto stage = [&](int k0, int kc) {
+    for (int i = threadIdx.x * 8; i < MB * KC; i += SK_WARPS * 32 * 8) {
+      const int m = i / KC, k = i - m * KC;
+      if (m < M && k < kc) {
+        if (NORM) {
+          const float r = rs[m];
+          const float4 a = *reinterpret_cast<const float4*>(X + (int64_t)m * lda + k0 + k);
+          const float4 b = *reinterpret_cast<const float4*>(X + (int64_t)m * lda + k0 + k + 4);
+          const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) st_f(&xs[m * KC + k + e], v[e] * r);
+        } else {
+          *reinterpret_cast<uint4*>(&xs[m * KC + k]) = *reinterpret_cast<const uint4*>(A + (int64_t)m * lda + k0 + k);
+          if (sizeof(E) == 4) *reinterpret_cast<uint4*>(&xs[m * KC + k + 4]) =
+              *reinterpret_cast<const uint4*>(A + (int64_t)m * lda + k0 + k + 4);
+        }
+      }
+    }
+  };
+
+  uint4 w[SK_PIECES], wn[SK_PIECES];
+  int g = blockIdx.x;
+  // the first pieces of W are in flight while A is prepared
+  if (g * SK_WARPS + warp < N) sk_load(W + (int64_t)(g * SK_WARPS + warp) * ldw, 0, min(KC, K), lane, w);
+  if (NORM) {
+    // sum of squares of each row: every thread a strided share, then the warps' partials in order
+    float ss[MB];
+#pragma unroll
+    for (int m = 0; m < MB; ++m) ss[m] = 0.f;
+    for (int c = threadIdx.x; c < K / 4; c += SK_WARPS * 32) {
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        if (m < M) {
+          const float4 v = *reinterpret_cast<const float4*>(X + (int64_t)m * lda + 4 * c);
+          ss[m] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MB; ++m) {
+      float v = ss[m];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) red[warp * MB + m] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < M) {
+      float t = 0.f;
+      for (int q = 0; q < SK_WARPS; ++q) t += red[q * MB + threadIdx.x];
+      rs[threadIdx.x] = rsqrtf(t / (float)K + eps);
+    }
+  }
+  float acc[MB];
+#pragma unroll
+  for (int m = 0; m < MB; ++m) acc[m] = 0.f;
+  if (nchunks == 1) {
+    __syncthreads();
+    stage(0, K);
+    __syncthreads();
+    // this warp's sequence of (column group, batch), the next one's pieces always in flight
+    const int nb = (K + BATCH - 1) / BATCH;
+    int b = 0;
+    while (g < ngroups) {
+      const int n = g * SK_WARPS + warp;
+      int g2 = g, b2 = b + 1;
+      if (b2 == nb) {
+        b2 = 0;
+        g2 = g + gridDim.x;
+      }
+      const int n2 = g2 * SK_WARPS + warp;
+      if (g2 < ngroups && n2 < N) sk_load(W + (int64_t)n2 * ldw, b2 * BATCH, K, lane, wn);
+      if (n < N) sk_fma<E, MB>(xs, KC, M, b * BATCH, K, lane, w, acc);
+      if (b == nb - 1) {
+        if (n < N) sk_store<E, MB>(acc, M, n, lane, ep, D, ldd);
+#pragma unroll
+        for (int m = 0; m < MB; ++m) acc[m] = 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < SK_PIECES; ++u) w[u] = wn[u];
+      g = g2;
+      b = b2;
+    }
+    return;
+  }
+  // A larger than the budget: every column group walks the K chunks, restaging A
+  for (; g < ngroups; g += gridDim.x) {
+    const int n = g * SK_WARPS + warp;
+    const bool has_n = n < N;
+    const E* wrow = W + (int64_t)(has_n ? n : 0) * ldw;
+    for (int k0 = 0; k0 < K; k0 += KC) {
+      const int kc = min(KC, K - k0);
+      if ((k0 > 0 || g != (int)blockIdx.x) && has_n) sk_load(wrow + k0, 0, kc, lane, w);
+      __syncthreads();
+      stage(k0, kc);
+      __syncthreads();
+      if (has_n) {
+        for (int kb = 0; kb < kc; kb += BATCH) {
+          const bool more = kb + BATCH < kc;
+          if (more) sk_load(wrow + k0, kb + BATCH, kc, lane, wn);
+          sk_fma<E, MB>(xs, KC, M, kb, kc, lane, w, acc);
+          if (more) {
+#pragma unroll
+            for (int u = 0; u < SK_PIECES; ++u) w[u] = wn[u];
+          }
+        }
+      }
+    }
+    if (has_n) sk_store<E, MB>(acc, M, n, lane, ep, D, ldd);
+#pragma unroll
+    for (int m = 0; m < MB; ++m) acc[m] = 0.f;
+  }
+}
+
+template <typename E, int MB>
+size_t sk_smem_bytes(int KC) {
+  return (size_t)MB * KC * sizeof(E) + (size_t)(MB + SK_WARPS * MB) * sizeof(float);
+}
+
 template <typename E, int MB, bool NORM>
 nc_status skinny_t(int M, int N, int K, const void* A, int64_t lda, const E* W, int64_t ldw, int ep, void* D,
                    int64_t ldd, float eps, cudaStream_t st) {
-  k_gemm_skinny<E, MB, NORM><<<cdiv(N, SK_WARPS), SK_WARPS * 32, 0, st>>>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps);
+  // K chunk: all of K (rounded up to 8) if it fits the budget, else the largest multiple of 8 that does
+  const int64_t fit = (int64_t)((SK_SMEM_MAX - sk_smem_bytes<E, MB>(0)) / (MB * sizeof(E))) / 8 * 8;
+  const int KC = (int)std::min<int64_t>((K + 7) / 8 * 8, fit);
+  const int ngroups = (N + SK_WARPS - 1) / SK_WARPS;
+  const int grid = std::min(ngroups, 2 * g_num_sms);
+  k_gemm_skinny<E, MB, NORM><<<grid, SK_WARPS * 32, sk_smem_bytes<E, MB>(KC), st>>>(M, N, K, KC, A, lda, W, ldw,
+                                                                                     ep, D, ldd, eps);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+template <typename E, int MB, bool NORM>
+cudaError_t sk_attr() {
+  return cudaFuncSetAttribute(k_gemm_skinny<E, MB, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM_MAX);
 }
 
 template <typename E, bool NORM>
@@ -365,7 +542,32 @@ nc_status skinny_e(int M, int N, int K, const void* A, int64_t lda, const E* W, 
   return skinny_t<E, 32, false>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
 }
 
+// Raise the dynamic shared-memory limit of every skinny instantiation once
+// (outside any stream capture: the decode graph is captured later).
+nc_status skinny_prepare() {
+  static bool done = false;
+  if (done) return NC_OK;
+  if (!g_num_sms) {
+    int dev = 0;
+    NC_CUDA_TRY(cudaGetDevice(&dev));
+    NC_CUDA_TRY(cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev));
+  }
+  const cudaError_t e[] = {
+      sk_attr<bf16, 1, false>(), sk_attr<bf16, 2, false>(), sk_attr<bf16, 4, false>(), sk_attr<bf16, 8, false>(),
+      sk_attr<bf16, 16, false>(), sk_attr<bf16, 32, false>(), sk_attr<bf16, 1, true>(), sk_attr<bf16, 2, true>(),
+      sk_attr<bf16, 4, true>(), sk_attr<bf16, 8, true>(), sk_attr<float, 1, false>(), sk_attr<float, 2, false>(),
+      sk_attr<float, 4, false>(), sk_attr<float, 8, false>(), sk_attr<float, 16, false>(),
+      sk_attr<float, 32, false>(), sk_attr<float, 1, true>(), sk_attr<float, 2, true>(), sk_attr<float, 4, true>(),
+      sk_attr<float, 8, true>()};
+  for (cudaError_t x : e)
+    if (x != cudaSuccess) return NC_ERR_CUDA;
+  done = true;
+  return NC_OK;
+}
+
 }  // namespace
+
+nc_status decode_kernels_prepare() { return skinny_prepare(); }
 
 nc_status launch_gemm_skinny(int dtype, int M, int N, int K, const void* A, int64_t lda, const void* W, int64_t ldw,
                              int ep, void* D, int64_t ldd, cudaStream_t st) {
@@ -373,6 +575,7 @@ nc_status launch_gemm_skinny(int dtype, int M, int N, int K, const void* A, int6
       (ep != NC_EP_STORE && ep != NC_EP_STORE_F32 && ep != NC_EP_ACCUM_F32 && ep != NC_EP_RELU2_SQ))
     return NC_ERR_ARG;
   if ((((uintptr_t)A) & 15) || (((uintptr_t)W) & 15)) return NC_ERR_ARG;
+  NC_TRY(skinny_prepare());
   if (dtype == NC_BF16) return skinny_e<bf16, false>(M, N, K, A, lda, (const bf16*)W, ldw, ep, D, ldd, 0.f, st);
   return skinny_e<float, false>(M, N, K, A, lda, (const float*)W, ldw, ep, D, ldd, 0.f, st);
 }
@@ -383,6 +586,7 @@ nc_status launch_gemm_skinny_norm(int dtype, int M, int N, int K, const float* x
       (ep != NC_EP_STORE && ep != NC_EP_STORE_F32 && ep != NC_EP_ACCUM_F32 && ep != NC_EP_RELU2_SQ))
     return NC_ERR_ARG;
   if ((((uintptr_t)x) & 15) || (((uintptr_t)W) & 15)) return NC_ERR_ARG;
+  NC_TRY(skinny_prepare());
   if (dtype == NC_BF16) return skinny_e<bf16, true>(M, N, K, x, ldx, (const bf16*)W, ldw, ep, D, ldd, eps, st);
   return skinny_e<float, true>(M, N, K, x, ldx, (const float*)W, ldw, ep, D, ldd, eps, st);
 }

@@ -1039,6 +1039,7 @@ extern "C" nc_status nc_kv_cache_create(nc_model* m, int32_t max_batch, int32_t 
   if ((m->hd != 64 && m->hd != 128) || (m->H / m->Hkv != 1 && m->H / m->Hkv != 2 && m->H / m->Hkv != 3 &&
                                         m->H / m->Hkv != 4 && m->H / m->Hkv != 8))
     return NC_ERR_UNSUPPORTED;
+  NC_TRY(decode_kernels_prepare());
   if (m->kcache && max_batch <= m->kv_b && max_len <= m->kv_max) {
     m->kv_batch = m->kv_len = 0;
     return NC_OK;

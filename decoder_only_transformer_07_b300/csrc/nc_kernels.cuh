@@ -144,6 +144,8 @@ nc_status launch_decode_attn(int dtype, int B, int H, int Hkv, int hd, int len, 
 // *p = v (add = false) or *p += v, on the device.
 nc_status launch_set_i32(int32_t* p, int32_t v, bool add, cudaStream_t st);
 size_t decode_part_floats(int B, int H, int hd, int max_len);
+// One-time launch attributes of the decode kernels (call outside stream capture).
+nc_status decode_kernels_prepare();
 // D[m, n] (op)= sum_k A[m, k] W[n, k] for 1 <= M <= SKINNY_MAX_M rows on the
 // CUDA cores (memory-bound on W); K, lda, ldw multiples of 8, 16-byte aligned
 // A and W; ep one of NC_EP_STORE, NC_EP_STORE_F32, NC_EP_ACCUM_F32, NC_EP_RELU2_SQ.

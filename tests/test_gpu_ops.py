@@ -141,9 +141,11 @@ def test_gemm_few_rows(M, dt):
 @pytest.mark.parametrize("M", [1, 5, 17, 32])
 @pytest.mark.parametrize("dt", [BF16, F32])
 @pytest.mark.parametrize("ep", [nc.EP_STORE, nc.EP_STORE_F32, nc.EP_ACCUM_F32, nc.EP_RELU2_SQ])
-def test_gemm_rows_skinny(M, dt, ep):
-    # the decode step's CUDA-core projections: at most 32 rows, ragged N
-    N, K = 333, 1096
+@pytest.mark.parametrize("K", [1096, 4104])
+def test_gemm_rows_skinny(M, dt, ep, K):
+    # the decode step's CUDA-core projections: at most 32 rows, ragged N; K = 4104 spans
+    # several batches of in-flight weight pieces and several staged chunks of A
+    N = 333
     a, w = rnd(70 + M, (M, K)), rnd(71 + M, (N, K))
     A, W = dev_tensor(a, dt), dev_tensor(w, dt)
     out_f32 = ep in (nc.EP_STORE_F32, nc.EP_ACCUM_F32)
