@@ -62,3 +62,18 @@ def test_null_arguments_rejected():
     assert lib.nc_model_create(None, 1, None) == 3
     assert lib.nc_forward_backward(None, None, None, 1, 1, None, None, None) == 3
     assert lib.nc_op_gemm(1, 4, 4, 4, None, 4, 1, None, 4, 1, 0, None, 4, None, 0, None, 0, None) == 3
+
+
+def test_fp8_and_row_gemm_arguments_rejected_without_gpu():
+    lib = nc.lib()
+    # E4M3 GEMM: null operands, a row pitch that is not a multiple of 16 bytes, an unknown output type
+    assert lib.nc_op_gemm_fp8(64, 64, 64, None, 64, None, 64, None, None, 1, None, 64, None) == 3
+    buf = ctypes.create_string_buffer(64 * 64 + 16)
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    assert lib.nc_op_gemm_fp8(64, 64, 40, p, 40, p, 40, p, p, 1, p, 64, None) == 3
+    assert lib.nc_op_gemm_fp8(64, 64, 64, p, 64, p, 64, p, p, 9, p, 64, None) == 3
+    # quantiser: missing stats, an unknown input type
+    assert lib.nc_op_quantize_fp8(1, p, 16, p, None, None) == 3
+    assert lib.nc_op_quantize_fp8(7, p, 16, p, p, None) == 3
+    # skinny row GEMM: more than 32 rows
+    assert lib.nc_op_gemm_rows(1, 33, 64, 64, p, 64, p, 64, 1, p, 64, None) == 3
