@@ -16,6 +16,11 @@
 // unnormalised output with one output column per thread, and leaves a partial
 // (max, sum, output) per head; a second kernel merges the partials of a row.
 // Scores are q.k / sqrt(hd) in fp32 (exp2 form), as in the training attention.
+// With a RoPE table the kernel also does the decode step's RoPE + QK norm: each
+// CTA rotates and normalises the G query heads of its group from the raw
+// projection, and the CTA whose chunk holds the new position does the same for
+// its key head and appends key and value to the cache (and to its staged rows)
+// - with the RoPE/QK-norm kernel's arithmetic, so the values are the same.
 #include "nc_kernels.cuh"
 #include "nc_ptx.cuh"
 
@@ -66,11 +71,14 @@ __device__ __forceinline__ void ld_unit(const uint8_t* p, const bf16*, float* f)
 // Partials: part[((b * H + h) * nsplit + s) * (HD + 2) + {0: max (log2 units), 1: sum, 2..: output}]
 // len_dev (device, may be NULL): the key count is *len_dev + 1 (the position of
 // the token just appended, plus one); chunks past it leave empty partials.
+// tab (may be NULL): RoPE table [T][HD/2] of (cos, sin); then qkv holds the raw
+// projection of the new position len - 1 and its k, v are not yet cached.
 template <typename E, int HD, int G>
 __global__ void __launch_bounds__(DEC_THREADS)
     k_decode_attn(int H, int Hkv, int len, const int32_t* __restrict__ len_dev, int nsplit,
-                  const E* __restrict__ qkv, int64_t ld, const E* __restrict__ kc, const E* __restrict__ vc,
-                  int max_len, float scale_log2, float* __restrict__ part) {
+                  const E* __restrict__ qkv, int64_t ld, E* __restrict__ kc, E* __restrict__ vc,
+                  int max_len, float scale_log2, float* __restrict__ part, const float2* __restrict__ tab,
+                  float eps) {
   constexpr int CK = dec_chunk<E>();
   constexpr int EPU = 16 / (int)sizeof(E);              // elements per 16-byte unit
   constexpr int UPR = HD / EPU;                         // units per row
@@ -96,18 +104,82 @@ __global__ void __launch_bounds__(DEC_THREADS)
     }
     return;
   }
+  const int pos = len - 1;                             // the position just appended
+  const int rp = tab ? pos - k0 : -1;                  // its row in this chunk (fused RoPE), if < nk
+  const bool owner = rp >= 0 && rp < nk;
   const int64_t row0 = ((int64_t)(b * Hkv + g) * max_len + k0) * HD;
   const uint8_t* kg = reinterpret_cast<const uint8_t*>(kc + row0);
   const uint8_t* vg = reinterpret_cast<const uint8_t*>(vc + row0);
   for (int i = tid; i < nk * UPR; i += DEC_THREADS) {
     const int r = i / UPR, u = i - r * UPR;
+    if (r == rp) continue;                             // computed below
     cp_async16(ks + r * RB + u * 16, kg + (int64_t)i * 16);
     cp_async16(vs + r * RB + u * 16, vg + (int64_t)i * 16);
   }
   cp_async_commit();
-  for (int i = tid; i < G * HD; i += DEC_THREADS) {
-    const int h = i / HD, d = i - h * HD;
-    qs[h][d] = ld_f(qkv + (int64_t)b * ld + (int64_t)(g * G + h) * HD + d) * scale_log2;
+  if (tab) {
+    // item j < G: query head g*G + j; j == G: key head g; j == G + 1: value head g (the last two in the owner only)
+    const int warp = tid >> 5, lane = tid & 31;
+    const int64_t crow = ((int64_t)(b * Hkv + g) * max_len + pos) * HD;   // the new position in the cache
+    for (int j = warp; j < G + (owner ? 2 : 0); j += DEC_THREADS / 32) {
+      if (j == G + 1) {
+        const E* src = qkv + (int64_t)b * ld + (int64_t)(H + Hkv + g) * HD;
+        E* sv = reinterpret_cast<E*>(vs + rp * RB);
+        for (int i = lane; i < HD; i += 32) {
+          const E v = src[i];
+          vc[crow + i] = v;
+          sv[i] = v;
+        }
+        continue;
+      }
+      const E* src = qkv + (int64_t)b * ld + (int64_t)(j < G ? g * G + j : H + g) * HD;
+      constexpr int D2 = HD / 2;
+      const float2* cs = tab + (int64_t)pos * D2;
+      float y[2][4];
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int i = 2 * lane + 64 * k;
+        y[k][0] = y[k][1] = y[k][2] = y[k][3] = 0.f;
+        if (i < D2) {
+          const float ax = ld_f(src + i), ay = ld_f(src + i + 1);
+          const float bx = ld_f(src + i + D2), by = ld_f(src + i + D2 + 1);
+          const float4 c = *reinterpret_cast<const float4*>(cs + i);   // cos_i, sin_i, cos_i+1, sin_i+1
+          y[k][0] = ax * c.x + bx * c.y;
+          y[k][2] = -ax * c.y + bx * c.x;
+          y[k][1] = ay * c.z + by * c.w;
+          y[k][3] = -ay * c.w + by * c.z;
+          ss += y[k][0] * y[k][0] + y[k][1] * y[k][1] + y[k][2] * y[k][2] + y[k][3] * y[k][3];
+        }
+      }
+      ss = warp_sum(ss);
+      const float r = rsqrtf(ss / (float)HD + eps);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int i = 2 * lane + 64 * k;
+        if (i < D2) {
+          const E e[4] = {from_f32<E>(y[k][0] * r), from_f32<E>(y[k][1] * r), from_f32<E>(y[k][2] * r),
+                          from_f32<E>(y[k][3] * r)};
+          const int at[4] = {i, i + 1, i + D2, i + D2 + 1};
+          if (j < G) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) qs[j][at[t]] = to_f32(e[t]) * scale_log2;
+          } else {
+            E* sk = reinterpret_cast<E*>(ks + rp * RB);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              kc[crow + at[t]] = e[t];
+              sk[at[t]] = e[t];
+            }
+          }
+        }
+      }
+    }
+  } else {
+    for (int i = tid; i < G * HD; i += DEC_THREADS) {
+      const int h = i / HD, d = i - h * HD;
+      qs[h][d] = ld_f(qkv + (int64_t)b * ld + (int64_t)(g * G + h) * HD + d) * scale_log2;
+    }
   }
   cp_async_wait_all();
   __syncthreads();
@@ -209,14 +281,15 @@ __global__ void __launch_bounds__(HD) k_decode_combine(int nsplit, const float* 
 }
 
 template <typename E, int HD, int G>
-nc_status decode_attn_t(int B, int H, int Hkv, int len, const int32_t* len_dev, const E* qkv, int64_t ld,
-                        const E* kc, const E* vc, int max_len, float* part, E* o, int64_t ldo, cudaStream_t st) {
+nc_status decode_attn_t(int B, int H, int Hkv, int len, const int32_t* len_dev, const E* qkv, int64_t ld, E* kc,
+                        E* vc, int max_len, float* part, E* o, int64_t ldo, const float2* tab, float eps,
+                        cudaStream_t st) {
   // with the length on the device the grid covers the whole capacity
   constexpr int CK = dec_chunk<E>();
   const int nsplit = ((len_dev ? max_len : len) + CK - 1) / CK;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   k_decode_attn<E, HD, G><<<dim3((unsigned)(B * Hkv), (unsigned)nsplit), DEC_THREADS, 0, st>>>(
-      H, Hkv, len, len_dev, nsplit, qkv, ld, kc, vc, max_len, scale_log2, part);
+      H, Hkv, len, len_dev, nsplit, qkv, ld, kc, vc, max_len, scale_log2, part, tab, eps);
   NC_CUDA_TRY(cudaGetLastError());
   if ((size_t)nsplit * sizeof(float) > 48 * 1024) return NC_ERR_UNSUPPORTED;
   k_decode_combine<E, HD><<<(unsigned)(B * H), HD, nsplit * sizeof(float), st>>>(nsplit, part, o, ldo, H);
@@ -225,13 +298,16 @@ nc_status decode_attn_t(int B, int H, int Hkv, int len, const int32_t* len_dev, 
 
 template <typename E, int HD>
 nc_status decode_attn_g(int G, int B, int H, int Hkv, int len, const int32_t* len_dev, const E* qkv, int64_t ld,
-                        const E* kc, const E* vc, int max_len, float* part, E* o, int64_t ldo, cudaStream_t st) {
+                        E* kc, E* vc, int max_len, float* part, E* o, int64_t ldo, const float2* tab, float eps,
+                        cudaStream_t st) {
+#define NC_DEC_ARGS B, H, Hkv, len, len_dev, qkv, ld, kc, vc, max_len, part, o, ldo, tab, eps, st
   switch (G) {
-    case 1: return decode_attn_t<E, HD, 1>(B, H, Hkv, len, len_dev, qkv, ld, kc, vc, max_len, part, o, ldo, st);
-    case 2: return decode_attn_t<E, HD, 2>(B, H, Hkv, len, len_dev, qkv, ld, kc, vc, max_len, part, o, ldo, st);
-    case 3: return decode_attn_t<E, HD, 3>(B, H, Hkv, len, len_dev, qkv, ld, kc, vc, max_len, part, o, ldo, st);
-    case 4: return decode_attn_t<E, HD, 4>(B, H, Hkv, len, len_dev, qkv, ld, kc, vc, max_len, part, o, ldo, st);
-    case 8: return decode_attn_t<E, HD, 8>(B, H, Hkv, len, len_dev, qkv, ld, kc, vc, max_len, part, o, ldo, st);
+    case 1: return decode_attn_t<E, HD, 1>(NC_DEC_ARGS);
+    case 2: return decode_attn_t<E, HD, 2>(NC_DEC_ARGS);
+    case 3: return decode_attn_t<E, HD, 3>(NC_DEC_ARGS);
+    case 4: return decode_attn_t<E, HD, 4>(NC_DEC_ARGS);
+    case 8: return decode_attn_t<E, HD, 8>(NC_DEC_ARGS);
+#undef NC_DEC_ARGS
     default: return NC_ERR_UNSUPPORTED;
   }
 }
@@ -256,19 +332,21 @@ nc_status launch_kv_store(int dtype, int64_t rows, int T, int t0, int H, int Hkv
 }
 
 nc_status launch_decode_attn(int dtype, int B, int H, int Hkv, int hd, int len, const void* qkv, int64_t ld,
-                             const void* kc, const void* vc, int max_len, float* part, void* o, int64_t ldo,
-                             cudaStream_t st, const int32_t* len_dev) {
+                             void* kc, void* vc, int max_len, float* part, void* o, int64_t ldo, cudaStream_t st,
+                             const int32_t* len_dev, const float* rope_tab, float eps) {
   if (B <= 0 || (!len_dev && (len <= 0 || len > max_len)) || H % Hkv || (hd != 64 && hd != 128)) return NC_ERR_ARG;
+  if (rope_tab && (((uintptr_t)rope_tab) & 15)) return NC_ERR_ARG;
   const int G = H / Hkv;
+  const float2* tab = reinterpret_cast<const float2*>(rope_tab);
   if (dtype == NC_BF16)
-    return hd == 128 ? decode_attn_g<bf16, 128>(G, B, H, Hkv, len, len_dev, (const bf16*)qkv, ld, (const bf16*)kc,
-                                                (const bf16*)vc, max_len, part, (bf16*)o, ldo, st)
-                     : decode_attn_g<bf16, 64>(G, B, H, Hkv, len, len_dev, (const bf16*)qkv, ld, (const bf16*)kc,
-                                               (const bf16*)vc, max_len, part, (bf16*)o, ldo, st);
-  return hd == 128 ? decode_attn_g<float, 128>(G, B, H, Hkv, len, len_dev, (const float*)qkv, ld, (const float*)kc,
-                                               (const float*)vc, max_len, part, (float*)o, ldo, st)
-                   : decode_attn_g<float, 64>(G, B, H, Hkv, len, len_dev, (const float*)qkv, ld, (const float*)kc,
-                                              (const float*)vc, max_len, part, (float*)o, ldo, st);
+    return hd == 128 ? decode_attn_g<bf16, 128>(G, B, H, Hkv, len, len_dev, (const bf16*)qkv, ld, (bf16*)kc,
+                                                (bf16*)vc, max_len, part, (bf16*)o, ldo, tab, eps, st)
+                     : decode_attn_g<bf16, 64>(G, B, H, Hkv, len, len_dev, (const bf16*)qkv, ld, (bf16*)kc,
+                                               (bf16*)vc, max_len, part, (bf16*)o, ldo, tab, eps, st);
+  return hd == 128 ? decode_attn_g<float, 128>(G, B, H, Hkv, len, len_dev, (const float*)qkv, ld, (float*)kc,
+                                               (float*)vc, max_len, part, (float*)o, ldo, tab, eps, st)
+                   : decode_attn_g<float, 64>(G, B, H, Hkv, len, len_dev, (const float*)qkv, ld, (float*)kc,
+                                              (float*)vc, max_len, part, (float*)o, ldo, tab, eps, st);
 }
 
 namespace {

@@ -1121,11 +1121,10 @@ static nc_status decode_body(nc_model* m, int B, cudaStream_t st) {
   uint8_t* h = layer_act(m, m->h, 0, F);
   for (int l = 0; l < m->L; ++l) {
     NC_TRY(norm_proj(NC_PROF_GEMM_FWD, W, wptr(m, tensor(m, l, 0)), NC_EP_STORE, qkv, W, xn1, m->rstd1));
-    // RoPE + QK norm at position *dec_pos (T = 1); k and v also go into the cache
-    NC_TRY(launch_rope_qknorm_fwd(m->dtype, B, 1, m->H, m->Hkv, m->hd, qkv, m->rstdqk, m->rope_tab, eps, st,
-                                  m->dec_pos, kv_layer(m, m->kcache, l), kv_layer(m, m->vcache, l), m->kv_max));
+    // RoPE + QK norm at position *dec_pos, the cache append of k and v, and attention in one kernel
     NC_TRY(launch_decode_attn(m->dtype, B, m->H, m->Hkv, m->hd, 0, qkv, W, kv_layer(m, m->kcache, l),
-                              kv_layer(m, m->vcache, l), m->kv_max, m->dec_part, o, Hd, st, m->dec_pos));
+                              kv_layer(m, m->vcache, l), m->kv_max, m->dec_part, o, Hd, st, m->dec_pos,
+                              m->rope_tab, eps));
     NC_TRY(proj(NC_PROF_GEMM_FWD, C, Hd, o, wptr(m, tensor(m, l, 3)), NC_EP_ACCUM_F32, m->x, C));
     NC_TRY(norm_proj(NC_PROF_GEMM_FWD, F, wptr(m, tensor(m, l, 4)), NC_EP_RELU2_SQ, h, F, xn2, m->rstd2));
     NC_TRY(proj(NC_PROF_GEMM_FWD, C, F, h, wptr(m, tensor(m, l, 5)), NC_EP_ACCUM_F32, m->x, C));

@@ -138,9 +138,12 @@ nc_status launch_kv_store(int dtype, int64_t rows, int T, int t0, int H, int Hkv
 // decode_part_floats(B, H, hd, max_len) floats.
 // len_dev (device, may be NULL): the keys are 0..*len_dev (inclusive) and the
 // grid covers max_len (for a graph that replays at growing lengths).
+// rope_tab (may be NULL; [T][hd/2][2] cos/sin, 16-byte aligned): qkv holds the
+// raw projection of position len - 1; the kernel applies RoPE + the per-head
+// RMSNorm (eps) to q and k itself and appends k and v to the cache.
 nc_status launch_decode_attn(int dtype, int B, int H, int Hkv, int hd, int len, const void* qkv, int64_t ld,
-                             const void* kc, const void* vc, int max_len, float* part, void* o, int64_t ldo,
-                             cudaStream_t st, const int32_t* len_dev = nullptr);
+                             void* kc, void* vc, int max_len, float* part, void* o, int64_t ldo, cudaStream_t st,
+                             const int32_t* len_dev = nullptr, const float* rope_tab = nullptr, float eps = 0.f);
 // *p = v (add = false) or *p += v, on the device.
 nc_status launch_set_i32(int32_t* p, int32_t v, bool add, cudaStream_t st);
 size_t decode_part_floats(int B, int H, int hd, int max_len);
