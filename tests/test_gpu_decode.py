@@ -69,6 +69,18 @@ def test_decode_bf16_matches_full_forward(shape):
         assert np.all(np.abs(g - z) <= 0.02 + 0.02 * np.abs(z)), (j, float(np.max(np.abs(g - z))))
 
 
+def test_decode_bf16_wide_batch_tensor_core_projections():
+    """12 sequences: beyond 8 rows the projections run on the tensor-core GEMM after a separate RMSNorm."""
+    w = S.Workload(name="dec", dtype="bf16", tokens="zipf", depth=2, n_embd=256, n_head=4, n_kv_head=2, head_dim=64,
+                   mlp_hidden=1024, vocab=1024, seq_len=128, batch=12)
+    got, want = _decode_run(w, 100, 3)
+    for j, (g, z) in enumerate(zip(got, want)):
+        for b in range(g.shape[0]):
+            cos = float(g[b] @ z[b] / (np.linalg.norm(g[b]) * np.linalg.norm(z[b])))
+            assert cos >= 0.999, (j, b, cos)
+        assert np.all(np.abs(g - z) <= 0.02 + 0.02 * np.abs(z)), (j, float(np.max(np.abs(g - z))))
+
+
 def test_decode_errors_and_cache_reuse():
     w = S.workload("tiny")
     cfg, m, params = _model(w)
