@@ -288,10 +288,10 @@ nc_status decode_attn_t(int B, int H, int Hkv, int len, const int32_t* len_dev, 
   constexpr int CK = dec_chunk<E>();
   const int nsplit = ((len_dev ? max_len : len) + CK - 1) / CK;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+  if ((size_t)nsplit * sizeof(float) > 48 * 1024) return NC_ERR_UNSUPPORTED;   // the combine's split weights
   k_decode_attn<E, HD, G><<<dim3((unsigned)(B * Hkv), (unsigned)nsplit), DEC_THREADS, 0, st>>>(
       H, Hkv, len, len_dev, nsplit, qkv, ld, kc, vc, max_len, scale_log2, part, tab, eps);
   NC_CUDA_TRY(cudaGetLastError());
-  if ((size_t)nsplit * sizeof(float) > 48 * 1024) return NC_ERR_UNSUPPORTED;
   k_decode_combine<E, HD><<<(unsigned)(B * H), HD, nsplit * sizeof(float), st>>>(nsplit, part, o, ldo, H);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
