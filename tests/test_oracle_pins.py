@@ -261,9 +261,12 @@ def test_relu_squared_derivative_single_ops():
 
 # ---------------------------------------------------------------- whole step
 
-@pytest.mark.parametrize("kv", [2, 1])
-def test_whole_step_central_finite_differences(kv):
-    cfg = small_cfg(n_kv_head=kv)
+@pytest.mark.parametrize("shape", [dict(n_kv_head=2), dict(n_kv_head=1),
+                                   # three query heads per kv head, as in the d24 GQA workload
+                                   dict(depth=1, n_embd=12, n_head=3, n_kv_head=1, mlp_hidden=48)],
+                         ids=["mha", "gqa2", "gqa3"])
+def test_whole_step_central_finite_differences(shape):
+    cfg = small_cfg(**shape)
     params = rand_params(cfg, 12)
     tok, tgt = rand_tokens(cfg, 2, 5, 13)
     loss, G = M.forward_backward(cfg, params, tok, tgt)
@@ -303,6 +306,30 @@ def test_gqa_equals_mha_with_repeated_kv_heads():
     for k in Gg:
         if k.endswith(".wk") or k.endswith(".wv"):
             summed = Gm[k].reshape(2, 2, hd, -1).sum(axis=1).reshape(2 * hd, -1)
+            assert np.allclose(Gg[k], summed, rtol=1e-10, atol=1e-13), k
+        else:
+            assert np.allclose(Gg[k], Gm[k], rtol=1e-10, atol=1e-13), k
+
+
+def test_gqa_three_groups_equals_mha_with_repeated_kv_heads():
+    """Three query heads per kv head (the d24 GQA grouping): kv head g serves q heads 3g .. 3g+2."""
+    g_cfg = small_cfg(n_head=6, n_kv_head=2, n_embd=24, mlp_hidden=96, depth=1)
+    m_cfg = small_cfg(n_head=6, n_kv_head=6, n_embd=24, mlp_hidden=96, depth=1)
+    Wg = M.unpack(g_cfg, rand_params(g_cfg, 18))
+    hd = g_cfg.head_dim
+    Wm = {}
+    for k, v in Wg.items():
+        if k.endswith(".wk") or k.endswith(".wv"):
+            Wm[k] = np.repeat(v.reshape(2, hd, -1), 3, axis=0).reshape(6 * hd, -1)
+        else:
+            Wm[k] = v.copy()
+    tok, tgt = rand_tokens(g_cfg, 2, 7, 19)
+    lg, Gg = M.forward_backward(g_cfg, Wg, tok, tgt)
+    lm, Gm = M.forward_backward(m_cfg, Wm, tok, tgt)
+    assert lg == pytest.approx(lm, rel=1e-13)
+    for k in Gg:
+        if k.endswith(".wk") or k.endswith(".wv"):
+            summed = Gm[k].reshape(2, 3, hd, -1).sum(axis=1).reshape(2 * hd, -1)
             assert np.allclose(Gg[k], summed, rtol=1e-10, atol=1e-13), k
         else:
             assert np.allclose(Gg[k], Gm[k], rtol=1e-10, atol=1e-13), k
