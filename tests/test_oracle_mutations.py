@@ -69,7 +69,7 @@ PINS = [
     P.test_attention_bwd_matches_fd,
     P.test_cross_entropy_zero_logits_and_row_sums,
     P.test_gqa_equals_mha_with_repeated_kv_heads,
-    lambda: P.test_whole_step_central_finite_differences(1),
+    lambda: P.test_whole_step_central_finite_differences(dict(n_kv_head=1)),
 ]
 
 
