@@ -56,6 +56,7 @@ _SIGS = {
     "nc_model_create": (_i32, [ctypes.POINTER(nc_config), _u64, ctypes.POINTER(_p)]),
     "nc_model_destroy": (None, [_p]),
     "nc_model_config": (_i32, [_p, ctypes.POINTER(nc_config)]),
+    "nc_param_layout": (_i32, [_p, ctypes.POINTER(_i32), ctypes.POINTER(_i64)]),
     "nc_param_count": (_i32, [_p, ctypes.POINTER(_i32), ctypes.POINTER(_i64)]),
     "nc_param_info": (_i32, [_p, _i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(_i64),
                              ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
@@ -98,6 +99,7 @@ _SIGS = {
     "nc_op_embed_bwd": (_i32, [_i64, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_debug_set_wait_limit_ns": (None, [_u64]),
     "nc_debug_set_gemm_pair": (None, [_i32]),
+    "nc_debug_stall_next_gemm": (None, [_i32]),
     "nc_debug_set_decode_graph": (None, [_i32]),
     "nc_op_gemm_rows": (_i32, [_i32, _i32, _i32, _i32, _p, _i64, _p, _i64, _i32, _p, _i64, _p]),
     "nc_op_quantize_fp8": (_i32, [_i32, _p, _i64, _p, _p, _p]),
@@ -171,7 +173,7 @@ class Model:
         _check(_lib.nc_model_create(ctypes.byref(cfg), ctypes.c_uint64(seed), ctypes.byref(self._h)),
                "nc_model_create")
         nt, ne = _i32(), _i64()
-        _check(_lib.nc_param_count(self._h, ctypes.byref(nt), ctypes.byref(ne)), "nc_param_count")
+        _check(_lib.nc_param_layout(self._h, ctypes.byref(nt), ctypes.byref(ne)), "nc_param_layout")
         self.n_tensors, self.n_params = nt.value, ne.value
         self.layout = []
         for i in range(self.n_tensors):

@@ -225,10 +225,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       ++issued;
     }
     // every load lands before the CTA exits (already so unless aborted)
-    mbar_wait_bounded(q_full, 0, sh.wait_ns);
+    mbar_wait_bounded(q_full, 0, NC_DRAIN_NS);
     for (int s = 0; s < NS; ++s) {
       const int uses = issued / NS + ((issued % NS) > s ? 1 : 0);
-      if (uses > 0) mbar_wait_bounded(&kv_full[s], (uses - 1) & 1, sh.wait_ns);
+      if (uses > 0) mbar_wait_bounded(&kv_full[s], (uses - 1) & 1, NC_DRAIN_NS);
     }
   } else if ((warp == 1 || warp == 3) && lane == 0) {
     // ---------------- MMA issuers: warp 1 for query tile 0, warp 3 for tile 1.
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       if (*abort_flag) ok = false;
     }
     tc_commit(&drain[i]);
-    mbar_wait_bounded(&drain[i], 0, sh.wait_ns);
+    mbar_wait_bounded(&drain[i], 0, NC_DRAIN_NS);
   } else if (warp >= 4) {
     // ---------------- softmax warpgroups: warps 4-7 own query tile 0, 8-11 tile 1
     const int i = (warp - 4) >> 2, quarter = warp & 3;
@@ -643,14 +643,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     (sh.H + sh.Hkv + g) * HD + 64 * c, row0 + j * 128);
       ++v_issued;
     }
-    mbar_wait_bounded(qd_full, 0, sh.wait_ns);
+    mbar_wait_bounded(qd_full, 0, NC_DRAIN_NS);
     for (int s = 0; s < NK; ++s) {
       const int ku = k_issued / NK + ((k_issued % NK) > s ? 1 : 0);
-      if (ku > 0) mbar_wait_bounded(&k_full[s], (ku - 1) & 1, sh.wait_ns);
+      if (ku > 0) mbar_wait_bounded(&k_full[s], (ku - 1) & 1, NC_DRAIN_NS);
     }
     for (int s = 0; s < NV; ++s) {
       const int vu = v_issued / NV + ((v_issued % NV) > s ? 1 : 0);
-      if (vu > 0) mbar_wait_bounded(&v_full[s], (vu - 1) & 1, sh.wait_ns);
+      if (vu > 0) mbar_wait_bounded(&v_full[s], (vu - 1) & 1, NC_DRAIN_NS);
     }
   } else if ((warp == 1 || warp == 2 || warp == 3) && lane == 0) {
     // ---------------- three MMA issuers (one thread issues about one MMA per ~100
@@ -694,7 +694,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       if (ok) tc_commit(dq_done);
     }
     tc_commit(&drain[role]);
-    mbar_wait_bounded(&drain[role], 0, sh.wait_ns);
+    mbar_wait_bounded(&drain[role], 0, NC_DRAIN_NS);
   } else if (warp >= 4) {
     const int quarter = warp & 3, hf = (warp - 4) >> 2;   // hf: key columns [64 hf, 64 hf + 64)
     const int r = quarter * 32 + lane;
@@ -851,10 +851,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       }
       ++issued;
     }
-    mbar_wait_bounded(kv_full, 0, sh.wait_ns);
+    mbar_wait_bounded(kv_full, 0, NC_DRAIN_NS);
     for (int s = 0; s < NS; ++s) {
       const int uses = issued / NS + ((issued % NS) > s ? 1 : 0);
-      if (uses > 0) mbar_wait_bounded(&q_full[s], (uses - 1) & 1, sh.wait_ns);
+      if (uses > 0) mbar_wait_bounded(&q_full[s], (uses - 1) & 1, NC_DRAIN_NS);
     }
   } else if (warp == 3) {
     // ---------------- lse / D of each query tile into the stage (every lane arrives)
@@ -916,7 +916,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
     if (ok) tc_commit(dkv_done);
     tc_commit(&drain[role]);
-    mbar_wait_bounded(&drain[role], 0, sh.wait_ns);
+    mbar_wait_bounded(&drain[role], 0, NC_DRAIN_NS);
   } else if (warp >= 4) {
     const int quarter = warp & 3, hf = (warp - 4) >> 2;   // hf: query columns [32 hf, 32 hf + 32)
     const int r = quarter * 32 + lane;

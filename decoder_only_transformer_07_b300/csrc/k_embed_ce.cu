@@ -106,16 +106,30 @@ __device__ void block_bitonic_sort(K* keys, int len) {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(EMB_CH) k_emb_bwd_runs(int64_t n, int C, const int32_t* __restrict__ tokens,
-                                                          const float* __restrict__ dx, EmbScratch s) {
+// A position whose id lies outside [0, V) sets the token error bit and takes
+// part in no run: its key is the sentinel ~0 (which sorts last and which no
+// valid id can produce, since V < 2^31), so no count, offset or list slot is
+// ever formed from it.
+__global__ void __launch_bounds__(EMB_CH) k_emb_bwd_runs(int64_t n, int C, int V, const int32_t* __restrict__ tokens,
+                                                          const float* __restrict__ dx, EmbScratch s,
+                                                          int32_t* __restrict__ err) {
   __shared__ unsigned long long keys[EMB_CH];
   __shared__ int run_of[EMB_CH];
   const int64_t base = (int64_t)blockIdx.x * EMB_CH;
   const int tid = threadIdx.x;
   int64_t i = base + tid;
-  keys[tid] = (i < n) ? (((unsigned long long)(unsigned)tokens[i] << 32) | (unsigned)tid) : ~0ull;
+  bool in_range = false;
+  unsigned long long key = ~0ull;
+  if (i < n) {
+    const int tok = tokens[i];
+    in_range = (unsigned)tok < (unsigned)V;
+    if (in_range) key = ((unsigned long long)(unsigned)tok << 32) | (unsigned)tid;
+    else if (err) atomicOr(err, NC_DEVERR_TOKEN);
+  }
+  keys[tid] = key;
+  // the in-range positions, which the sort places first
+  const int valid = __syncthreads_count(in_range);
   block_bitonic_sort(keys, EMB_CH);
-  const int valid = (int)((n - base < (int64_t)EMB_CH) ? (n - base) : (int64_t)EMB_CH);
   // run index of each sorted position (inclusive scan of run starts; EMB_CH is small)
   if (tid == 0) {
     int r = -1;
@@ -225,7 +239,7 @@ __global__ void __launch_bounds__(256) k_emb_bwd_rows(int V, int C, EmbScratch s
 }
 
 nc_status launch_embed_bwd(int64_t n, int C, int V, const int32_t* tokens, const float* dx,
-                           float* dwte, void* scratch, cudaStream_t st, int accumulate) {
+                           float* dwte, void* scratch, cudaStream_t st, int accumulate, int32_t* err) {
   if (C % 4 || C > 4 * EMB_MAXV4 * EMB_CH || V <= 0) return NC_ERR_ARG;
   int64_t nchunks = (n + EMB_CH - 1) / EMB_CH;
   if (nchunks > EMB_MAX_CHUNKS) return NC_ERR_UNSUPPORTED;
@@ -234,7 +248,7 @@ nc_status launch_embed_bwd(int64_t n, int C, int V, const int32_t* tokens, const
   NC_CUDA_TRY(cudaMemsetAsync(s.count, 0, sizeof(int) * (size_t)V, st));
   NC_CUDA_TRY(cudaMemsetAsync(s.cursor, 0, sizeof(int) * (size_t)V, st));
   if (nchunks > 0) {
-    k_emb_bwd_runs<<<(unsigned)nchunks, EMB_CH, 0, st>>>(n, C, tokens, dx, s);
+    k_emb_bwd_runs<<<(unsigned)nchunks, EMB_CH, 0, st>>>(n, C, V, tokens, dx, s, err);
     NC_CUDA_TRY(cudaGetLastError());
   }
   k_emb_bwd_scan<<<1, 1024, 0, st>>>(V, s.count, s.offs);

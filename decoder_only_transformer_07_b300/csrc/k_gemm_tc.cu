@@ -49,6 +49,7 @@ struct TcParams {
   int tiles_m, tiles_n, num_kb;
   int32_t* err;
   uint64_t wait_ns;
+  int stall;               // test hook: the MMA issuer waits on a barrier nothing completes (single-CTA kernel)
   // split-K: work unit u covers k-blocks [s*kps, (s+1)*kps) of tile t, with
   // s = u / tiles and t = u % tiles, so CTAs running together stream the same
   // K slice (L2 reuse).  With splits > 1 every unit writes its fp32 partial
@@ -280,9 +281,15 @@ __device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, int ep, co
         mbar_arrive_expect_tx(aux_bar, 4096);
         tma_load_2d(stg, tmAux, aux_bar, n_out, m0);
       }
-      const bool ok = mbar_wait_bounded(aux_bar, aux_phase, p.wait_ns);
+      const uint32_t ph = aux_phase;
+      const bool ok = mbar_wait_bounded(aux_bar, ph, p.wait_ns);
       aux_phase ^= 1;
-      if (!__all_sync(0xffffffffu, ok)) return false;
+      if (!__all_sync(0xffffffffu, ok)) {
+        // the load was issued: it lands in the box before this warp gives up
+        if (lane == 0) mbar_wait_bounded(aux_bar, ph, NC_DRAIN_NS);
+        __syncwarp();
+        return false;
+      }
     }
 #pragma unroll 1
     for (int pc = 0; pc < cc; pc += 32) {
@@ -523,7 +530,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // (already true on the normal path, where the MMA issuer consumed them all).
     for (int s = 0; s < S; ++s) {
       long long n_s = issued / S + ((issued % S) > s ? 1 : 0);
-      if (n_s > 0) mbar_wait_bounded(&full_bar[s], (uint32_t)((n_s - 1) & 1), p.wait_ns);
+      if (n_s > 0) mbar_wait_bounded(&full_bar[s], (uint32_t)((n_s - 1) & 1), NC_DRAIN_NS);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
@@ -533,6 +540,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int local = 0;
     TcSegIter it(p, blockIdx.x, gridDim.x);
     TcSeg sg;
+    // Test hook (p.stall): first wait for drain_bar, which nothing completes
+    // before this thread's own drain commit below, so the wait runs out after
+    // the wait limit and the kernel takes its timeout path.
+    if (p.stall && !mbar_wait_bounded(drain_bar, 0, p.wait_ns)) fail();
     for (; !*abort_flag && it.next(p, sg); ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
@@ -561,7 +572,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     // Drain: all MMAs issued by this thread complete before TMEM is freed.
     tc_commit(drain_bar);
-    mbar_wait_bounded(drain_bar, 0, p.wait_ns);
+    mbar_wait_bounded(drain_bar, 0, NC_DRAIN_NS);
   } else if (warp >= 4) {
     // ---------------- epilogue
     const int quarter = warp & 3;
@@ -793,7 +804,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       tc_commit_pair(&acc_full[acc], 0x3);
     }
     tc_commit_pair(drain_bar, 0x1);
-    mbar_wait_bounded(drain_bar, 0, p.wait_ns);
+    mbar_wait_bounded(drain_bar, 0, NC_DRAIN_NS);
   } else if (warp >= 4) {
     // ---------------- epilogue (both CTAs): this CTA's 128 rows of the tile
     const int quarter = warp & 3;
@@ -888,7 +899,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   if (!fn) {
     cudaDriverEntryPointQueryResult q;
     void* f = nullptr;
-    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &f, cudaEnableDefault, &q) == cudaSuccess &&
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
   }
@@ -938,6 +949,7 @@ bool make_tmap_bf16_3d(CUtensorMap* tm, const void* base, uint64_t inner, uint64
 
 int g_num_sms = 0;
 uint64_t g_tc_wait_ns = 4000000000ull;   // bounded-wait limit of the tensor-core kernels
+int g_tc_stall_next = 0;                 // test hook: the next single-CTA GEMM launch times out
 
 template <int BN, bool F8 = false>
 static nc_status launch_tc_bn(TcParams p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
@@ -970,6 +982,8 @@ static nc_status launch_tc_bn(TcParams p, const CUtensorMap& ta, const CUtensorM
     p.splits = (p.num_kb + p.kps - 1) / p.kps;
   }
   const int grid = std::min(tiles * p.splits, g_num_sms);
+  p.stall = g_tc_stall_next;
+  g_tc_stall_next = 0;
   kern<<<grid, TC_THREADS, TcCfg<BN>::SMEM, st>>>(ta, tb, td, tx, p);
   NC_CUDA_TRY(cudaGetLastError());
   if (p.splits > 1) {
@@ -1083,6 +1097,7 @@ static nc_status gemm_tc_impl(int M, int N, int K, const bf16* A, int64_t lda, i
   p.num_kb = (K + TC_BK - 1) / TC_BK;
   p.err = err;
   p.wait_ns = g_tc_wait_ns;
+  p.stall = 0;
   p.ws = (float*)ws;
   p.splits = 1;
   p.kps = 0;

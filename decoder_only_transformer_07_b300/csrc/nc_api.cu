@@ -396,11 +396,15 @@ extern "C" nc_status nc_model_config(const nc_model* m, nc_config* out) {
   return NC_OK;
 }
 
-extern "C" nc_status nc_param_count(const nc_model* m, int32_t* n_tensors, int64_t* n_elems) {
+extern "C" nc_status nc_param_layout(const nc_model* m, int32_t* n_tensors, int64_t* n_elems) {
   if (!m) return NC_ERR_ARG;
   if (n_tensors) *n_tensors = (int32_t)m->layout.size();
   if (n_elems) *n_elems = m->P;
   return NC_OK;
+}
+
+extern "C" nc_status nc_param_count(const nc_model* m, int32_t* n_tensors, int64_t* n_elems) {
+  return nc_param_layout(m, n_tensors, n_elems);
 }
 
 extern "C" nc_status nc_param_info(const nc_model* m, int32_t i, const char** name, int64_t* rows, int64_t* cols,
@@ -563,7 +567,8 @@ static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int 
   }
   const ParamTensor& te = m->layout[0];
   PROF(NC_PROF_EMBED, 0, 4.0 * N * C + 4.0 * m->V * C,
-       launch_embed_bwd(N, C, m->V, tokens, m->dx, grads + te.off, m->emb_scratch, st, accumulate ? 1 : 0));
+       launch_embed_bwd(N, C, m->V, tokens, m->dx, grads + te.off, m->emb_scratch, st, accumulate ? 1 : 0,
+                        m->err));
   m->launches += 4;
   return NC_OK;
 }
@@ -800,6 +805,9 @@ extern "C" void nc_debug_set_wait_limit_ns(uint64_t ns) { g_tc_wait_ns = ns; }
 
 extern int g_gemm_pair;
 extern "C" void nc_debug_set_gemm_pair(int32_t on) { g_gemm_pair = on != 0; }
+
+extern int g_tc_stall_next;
+extern "C" void nc_debug_stall_next_gemm(int32_t on) { g_tc_stall_next = on != 0; }
 
 // ------------------------------------------------------------------ optimizer
 // Muon for every weight matrix, AdamW for wte and lm_head (cosmicrealm

@@ -29,8 +29,11 @@ nc_status launch_embed_fwd(int dtype, int64_t n, int C, int V, const int32_t* to
                            const float* wte, float* x, int32_t* err, cudaStream_t st);
 size_t embed_bwd_scratch_bytes(int64_t n, int C, int V);
 // accumulate != 0: dwte += the scatter (rows of absent ids untouched); else dwte = it.
+// Positions whose id lies outside [0, V) add to no row and set the token bit of
+// *err (when err is not NULL).
 nc_status launch_embed_bwd(int64_t n, int C, int V, const int32_t* tokens, const float* dx,
-                           float* dwte, void* scratch, cudaStream_t st, int accumulate = 0);
+                           float* dwte, void* scratch, cudaStream_t st, int accumulate = 0,
+                           int32_t* err = nullptr);
 nc_status launch_cross_entropy(int dtype, int64_t rows, int V, void* z, int64_t ldz,
                                const int32_t* targets, float* row_loss, float scale, int32_t* err,
                                cudaStream_t st);

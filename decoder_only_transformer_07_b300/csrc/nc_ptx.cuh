@@ -38,6 +38,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+// Time limit of the drain that follows a timeout: a kernel that gave up waits
+// this long for the copies and MMAs it has already issued (they finish within
+// microseconds unless the hardware has stopped).  It is a constant, not the
+// adjustable wait limit, so that lowering that limit in a test never lets a
+// copy or an MMA outlive its CTA.
+#define NC_DRAIN_NS 2000000000ull
+
 // Wait for the phase of `bar` with the given parity to complete, giving up
 // after `limit_ns` nanoseconds.  Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {

@@ -92,9 +92,15 @@ nc_status nc_model_create(const nc_config* cfg, uint64_t seed, nc_model** out);
 void nc_model_destroy(nc_model* m);
 nc_status nc_model_config(const nc_model* m, nc_config* cfg_out);
 
-/* Packed parameter layout: wte[V,C]; per layer l: Wq[H*hd,C], Wk[Hkv*hd,C],
- * Wv[Hkv*hd,C], Wo[C,H*hd], Wfc[F,C], Wproj[C,F]; lm_head[V,C].  Wq/Wk/Wv are
- * adjacent, so together they form one [(H+2Hkv)*hd, C] matrix. */
+/* Packed parameter layout (cosmicrealm "noao-chat-0-项目总体介绍" §2.1: the
+ * untied embedding and output head, bias-free linears): wte[V,C]; per layer l:
+ * Wq[H*hd,C], Wk[Hkv*hd,C], Wv[Hkv*hd,C], Wo[C,H*hd], Wfc[F,C], Wproj[C,F];
+ * lm_head[V,C].  Wq/Wk/Wv are adjacent, so together they form one
+ * [(H+2Hkv)*hd, C] matrix.  *n_tensors receives the number of tensors (2 + 6L)
+ * and *n_elems the length of the packed vector (either may be NULL);
+ * NC_ERR_ARG for a NULL model.  nc_param_info describes each tensor. */
+nc_status nc_param_layout(const nc_model* m, int32_t* n_tensors, int64_t* n_elems);
+/* The same call under its earlier name. */
 nc_status nc_param_count(const nc_model* m, int32_t* n_tensors, int64_t* n_elems);
 /* Tensor i: its name ("wte", "h3.wfc", "lm_head", ...), shape and element
  * offset in the packed vector.  `name` points to storage owned by the model. */
@@ -277,6 +283,8 @@ nc_status nc_op_embed_fwd(int32_t dtype, int64_t n, int32_t C, int32_t V,
                           int32_t* err_dev, void* stream);
 /* dwte (float [V, C]) = sum over i with tokens[i] == v of dx[i] (float [n, C]),
  * summed in increasing i; rows of ids not present are +0.0.  Deterministic.
+ * A position whose id lies outside [0, V) adds to no row (this call does not
+ * report it; the training step reports it as NC_ERR_TOKEN_RANGE).
  * scratch: at least nc_embed_bwd_scratch_bytes(n, C, V) bytes of device memory. */
 size_t nc_embed_bwd_scratch_bytes(int64_t n, int32_t C, int32_t V);
 nc_status nc_op_embed_bwd(int64_t n, int32_t C, int32_t V, const int32_t* tokens,
@@ -294,10 +302,12 @@ nc_status nc_op_embed_bwd(int64_t n, int32_t C, int32_t V, const int32_t* tokens
  * which loads the library keeps until the process exits.
  *  - Sizes whose scratch (nc_embed_bwd_scratch_bytes(n, C, V)) exceeds
  *    NC_NOALLOC_SCRATCH_BYTES are rejected with NC_ERR_UNSUPPORTED before any
- *    GPU work; NULL pointers or non-positive sizes give NC_ERR_ARG.
+ *    GPU work; NULL pointers, negative n or non-positive C or V give
+ *    NC_ERR_ARG; n == 0 writes zeros to dwte.
  *  - The first call on a device looks up the array's device address (a
  *    one-time set-up per device, done with that device current); make that
- *    first call before any stream capture.
+ *    first call before any stream capture.  After cudaDeviceReset the array
+ *    lives in a new context, and the next call looks its address up again.
  *  - It calls no cudaMalloc/cudaFree and no allocating library routine.
  *  - All calls share the one array, which keeps the last call's contents;
  *    the counters are zeroed on the stream at the start of every call.
@@ -340,6 +350,16 @@ nc_status nc_profile_read(nc_model* m, int32_t cls, double* ms, int64_t* launche
  * MMAs (again bounded), frees its tensor memory and returns.
  * ---------------------------------------------------------------------- */
 void nc_debug_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook for the timeout path.  on = 1 arms the next launch of the
+ * single-CTA tensor-core GEMM kernel (see nc_debug_set_gemm_pair): its
+ * MMA-issuing thread first waits on a barrier that nothing completes, so that
+ * wait runs out after the limit above; the kernel then takes its timeout path
+ * (error bit, drain of its own copies and MMAs under a fixed 2 s bound, TMEM
+ * freed) and the call that reads the flag returns NC_ERR_TIMEOUT.  The
+ * outputs of that GEMM are left unwritten.  The hook disarms itself at that
+ * launch; on = 0 disarms it. */
+void nc_debug_stall_next_gemm(int32_t on);
 
 /* Test hook.  on = 0 makes every bf16 GEMM use the single-CTA kernel (128 x
  * 256 tiles); on = 1 (default) lets shapes with M >= 256 and N > 128 that do

@@ -62,6 +62,8 @@ def test_null_arguments_rejected():
     assert lib.nc_model_create(None, 1, None) == 3
     assert lib.nc_forward_backward(None, None, None, 1, 1, None, None, None) == 3
     assert lib.nc_op_gemm(1, 4, 4, 4, None, 4, 1, None, 4, 1, 0, None, 4, None, 0, None, 0, None) == 3
+    assert lib.nc_param_layout(None, None, None) == 3
+    assert lib.nc_param_count(None, None, None) == 3
 
 
 def test_fp8_and_row_gemm_arguments_rejected_without_gpu():

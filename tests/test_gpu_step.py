@@ -47,6 +47,21 @@ def test_init_matches_oracle_rng():
     m.close()
 
 
+def test_param_layout_matches_oracle():
+    """nc_param_layout / nc_param_info give the oracle's packed order, shapes and offsets."""
+    import ctypes
+    w = S.Workload(name="gqa", dtype="bf16", tokens="zipf", depth=3, n_embd=256, n_head=4, n_kv_head=2,
+                   head_dim=64, mlp_hidden=1024, vocab=1024, seq_len=64, batch=1)
+    m = make(w)
+    nt, ne = ctypes.c_int32(), ctypes.c_int64()
+    assert nc.lib().nc_param_layout(m.handle, ctypes.byref(nt), ctypes.byref(ne)) == 0
+    want = OM.param_layout(oracle_cfg(w))
+    assert nt.value == len(want) == 2 + 6 * w.depth
+    assert ne.value == OM.n_params(oracle_cfg(w))
+    assert [tuple(t) for t in m.layout] == [tuple(t) for t in want]
+    m.close()
+
+
 def test_tiny_fp32_step_matches_oracle():
     w = S.workload("tiny")
     cfg = oracle_cfg(w)
