@@ -1,9 +1,12 @@
 """Benchmark: training tokens/s and MFU of one forward+backward GPT step on B300.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--config d20] [--impl ours|reference]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config d26] [--impl ours|reference]
 
-Prints ONE JSON line (rank 0).  A step is one nc_forward_backward call over a
-full batch of the workload: weight cast, forward, chunked lm_head +
+Prints ONE JSON line (rank 0).  The default workload is d26, the largest
+single-GPU configuration; on one GPU the d20, d24-GQA and d12 workloads are
+measured in the same run and reported under "other_configs" with the same
+fields.  A step is one nc_forward_backward call over a full batch of the
+workload: weight cast, forward, chunked lm_head +
 cross-entropy, backward, fp32 gradient write, loss read-back.  `value` is
 timed with CUDA events on the launching stream with inputs already resident
 in HBM; `e2e` times the same step through nc_forward_backward_host from
@@ -44,10 +47,12 @@ DESCR = {
     "d26": "d26 GPT L26 C1664 H13/13 hd128 F6656 V65536 T2048 B16 (bf16)",
     "d24gqa": "d24 GQA GPT L24 C1536 H12/4 hd128 F6144 V65536 T4096 B8 (bf16)",
 }
-# DRAM traffic per GEMM call (main kernel + split-K fix-up), from the ncu capture of a
-# full step summarised in profiles/launches_d20_step.md; set to None when the GEMM
-# kernels change and the capture is not repeated.
-GEMM_DRAM_BYTES_PER_CALL = {"d20": 1258e6}
+# DRAM traffic per GEMM call (main kernel + split-K fix-up) per workload: ncu
+# dram__bytes_read.sum + dram__bytes_write.sum of every distinct GEMM launch of
+# one step (`bench.py --op gemmset --config <w>`, each launch at full size),
+# weighted by the step's call counts.  A workload is left out (null traffic)
+# whenever the GEMM kernels change and the capture is not repeated.
+GEMM_DRAM_BYTES_PER_CALL = {}
 # CPU-oracle sample (tokens of one sequence) per workload: ~10-30 s of fp64 work
 CPU_SAMPLE_T = {"tiny": 64, "d12": 128, "d20": 64, "d26": 48, "d24gqa": 48}
 
@@ -149,6 +154,28 @@ def oracle_sample(w, t_sample, steps, warmup):
     return t_sample / statistics.median(times), threads, times
 
 
+def sample_flops_per_token(w, t_sample):
+    """Algorithmic FLOPs per token of the oracle's sample (one sequence of
+    t_sample tokens): the matrix term plus causal attention at that length."""
+    f = flops_per_token(w)
+    return f["causal"] - 6 * w.depth * w.n_head * w.head_dim * (w.seq_len - t_sample)
+
+
+def cpu_baseline(w, name):
+    """The oracle on the host cores: one sequence of CPU_SAMPLE_T tokens.  At
+    that length attention costs far less per token than at the workload's T,
+    so the line also gives the sample's FLOPs per token and the rate scaled to
+    the workload's FLOPs per token (the oracle's matrix products run at a
+    roughly constant FLOP rate)."""
+    t_sample = CPU_SAMPLE_T.get(name, 64)
+    tps, threads, _ = oracle_sample(w, t_sample, 1, 0)
+    fs, fw = sample_flops_per_token(w, t_sample), flops_per_token(w)["causal"]
+    return {"value": tps, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"one sequence of {t_sample} tokens of the {name} workload, fp64 NumPy fwd+bwd",
+            "sample_flops_per_token": fs, "workload_flops_per_token": fw,
+            "value_at_workload_flops_per_token": tps * fs / fw}
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -180,13 +207,16 @@ def run_reference(args, w):
         return
     t_sample = CPU_SAMPLE_T.get(args.config, 64)
     tps, threads, times = oracle_sample(w, t_sample, args.steps, args.warmup)
+    fs, fw = sample_flops_per_token(w, t_sample), flops_per_token(w)["causal"]
     line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": DESCR[args.config], "sample": f"1 x {t_sample} tokens"},
             "cpu_baseline": {"value": tps, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": f"one sequence of {t_sample} tokens of the {args.config} workload, "
-                                       f"fp64 NumPy forward+backward"},
+                                       f"fp64 NumPy forward+backward",
+                             "sample_flops_per_token": fs, "workload_flops_per_token": fw,
+                             "value_at_workload_flops_per_token": tps * fs / fw},
             "e2e": {"value": tps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -391,18 +421,180 @@ def run_op(args):
                       "args": {k: v for k, v in vars(args).items() if k not in ("impl",)}}), flush=True)
 
 
+def gemm_set(w):
+    """The GEMM launches of one training step of workload w: (count, M, N, K,
+    a_kmajor, b_kmajor, epilogue, fp32 output) per distinct launch, in the
+    step's operand layouts (the forward, the chunked lm_head, then the
+    backward of each layer)."""
+    N = w.batch * w.seq_len
+    C, F, V, L = w.n_embd, w.mlp_hidden, w.vocab, w.depth
+    Hd, W = w.n_head * w.head_dim, (w.n_head + 2 * w.n_kv_head) * w.head_dim
+    chunk = max(128, ((1 << 30) // (V * 2)) // 128 * 128)
+    nchunks = -(-N // chunk)
+    nc_rows = min(chunk, N)
+    return [  # (tag, count, M, N, K, a_kmajor, b_kmajor, ep)
+        ("qkv_rope", L, N, W, C, 1, 1, "qkv"), ("proj", L, N, C, Hd, 1, 1, 2), ("fc", L, N, F, C, 1, 1, 5),
+        ("c_proj", L, N, C, F, 1, 1, 2),
+        ("lm_logits", nchunks, nc_rows, V, C, 1, 1, 0), ("lm_dx", nchunks, nc_rows, C, V, 1, 0, 1),
+        ("lm_dw", nchunks, V, C, nc_rows, 0, 0, 2),
+        ("dw_proj", L, C, F, N, 0, 0, 1), ("du", L, N, F, C, 1, 0, 6), ("dw_fc", L, F, C, N, 0, 0, 1),
+        ("dx_fc", L, N, C, F, 1, 0, 1), ("dw_o", L, C, Hd, N, 0, 0, 1), ("do", L, N, Hd, C, 1, 0, 0),
+        ("dw_qkv", L, W, C, N, 0, 0, 1), ("dx_qkv", L, N, C, W, 1, 0, 1)]
+
+
+def run_gemmset(args):
+    """Launch every distinct GEMM of one --config training step once, at the
+    step's full shapes (for a per-kernel DRAM capture of the GEMM kernels;
+    a few GB on the device).  Prints the launch table with call counts."""
+    import torch
+    import decoder_only_transformer_07_b300 as nc
+    torch.cuda.set_device(0)
+    w = S.workload(args.config)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    ws = torch.empty(nc.ops.gemm_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    rows = []
+    for tag, count, M, N, K, ak, bk, ep in gemm_set(w):
+        A = (torch.randn((M, K) if ak else (K, M), device="cuda", generator=g) * 0.1).to(torch.bfloat16)
+        B = (torch.randn((N, K) if bk else (K, N), device="cuda", generator=g) * 0.1).to(torch.bfloat16)
+        if ep == "qkv":
+            T, H, Hkv, hd = w.seq_len, w.n_head, w.n_kv_head, w.head_dim
+            D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            tab = torch.empty((hd // 4, T, 4), dtype=torch.float32, device="cuda")
+            nc.ops.rope_table_pairs(T, hd, 10000.0, tab)
+            rstd = torch.empty((M, H + Hkv), dtype=torch.float32, device="cuda")
+            fn = (lambda A=A, B=B, D=D, tab=tab, rstd=rstd, T=T, H=H, Hkv=Hkv, hd=hd:
+                  nc.ops.gemm_qkv_rope(A, B, D, T, H, Hkv, hd, rstd, tab, 1.1920929e-07, pair_rows=T))
+        else:
+            D = torch.zeros((M, N), dtype=torch.float32 if ep in (1, 2) else torch.bfloat16, device="cuda")
+            aux = torch.rand((M, N), device="cuda", generator=g).to(torch.bfloat16) if ep == 6 else None
+            fn = (lambda A=A, B=B, D=D, aux=aux, M=M, N=N, K=K, ak=ak, bk=bk, ep=ep:
+                  nc.ops.gemm(A, ak, B, bk, M, N, K, D, ep=ep, aux=aux, workspace=ws))
+        fn()
+        torch.cuda.synchronize()
+        rows.append({"tag": tag, "count": count, "M": M, "N": N, "K": K, "flops": 2.0 * M * N * K})
+        del A, B, D
+        torch.cuda.empty_cache()
+    print(json.dumps({"op": "gemmset", "config": args.config, "launches": rows}), flush=True)
+
+
+def measure(w, name, args, world, rank, dev, gpu_traffic=True):
+    """Time `args.steps` training steps of workload w (device-resident inputs),
+    then the same through the host-buffer entry point; returns the fields of
+    the bench line for this workload."""
+    import ctypes
+    import torch
+    import decoder_only_transformer_07_b300 as nc
+
+    model = nc.Model(nc.config_from_workload(w), seed=S.WEIGHT_SEED)
+    tok_np, tgt_np = S.batch_tokens(w)
+    tok = torch.from_numpy(tok_np).cuda()
+    tgt = torch.from_numpy(tgt_np).cuda()
+    grads = torch.empty(model.n_params, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        model.forward_backward(tok, tgt, grads)
+    launches_per_step = model.last_launch_count()
+
+    # ---- device-resident timing
+    clocks = ClockSampler(dev)
+    lib = nc.lib()
+    lib.nc_profile_enable(model.handle, 1)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    losses = []
+    for _ in range(args.steps):
+        loss, _ = model.forward_backward(tok, tgt, grads)
+        losses.append(loss)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    prof = {}
+    for cls, pname in enumerate(["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "ce", "embed", "cast", "other",
+                                 "gemm_fwd", "gemm_dx", "gemm_dw", "gemm_lm_head"]):
+        t, n, fl, by = ctypes.c_double(), ctypes.c_int64(), ctypes.c_double(), ctypes.c_double()
+        lib.nc_profile_read(model.handle, cls, ctypes.byref(t), ctypes.byref(n), ctypes.byref(fl), ctypes.byref(by))
+        prof[pname] = {"ms": t.value, "launches": n.value, "flops": fl.value, "bytes": by.value}
+    lib.nc_profile_enable(model.handle, 0)
+    ms = max_over_ranks(ms, world, "cuda")
+
+    tokens_per_step = w.batch * w.seq_len
+    value = replica_throughput(world, tokens_per_step, args.steps, ms)
+    ms_step = ms / args.steps
+
+    # ---- end-to-end through the host-buffer entry point
+    tok_h = torch.from_numpy(tok_np).pin_memory()
+    tgt_h = torch.from_numpy(tgt_np).pin_memory()
+    for _ in range(2):
+        model.forward_backward_host(tok_h, tgt_h, grads)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        model.forward_backward_host(tok_h, tgt_h, grads)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, "cuda")
+    e2e = {"value": replica_throughput(world, tokens_per_step, args.steps, 1e3 * e2e_s), "unit": UNIT,
+           "h2d_bytes_per_step": int(tok_np.nbytes + tgt_np.nbytes), "d2h_bytes_per_step": 8}
+    model.close()
+    del grads, tok, tgt
+    torch.cuda.empty_cache()
+
+    peak_burst, peak_sust, hbm, peak_src = load_peaks()
+    fpt = flops_per_token(w)
+    per_gpu_tps = value / world
+    mfu = {k: per_gpu_tps * fpt[k] / (peak_burst * 1e12) for k in ("causal", "full_square", "six_n_total")}
+    mfu["causal_vs_sustained"] = per_gpu_tps * fpt["causal"] / (peak_sust * 1e12)
+
+    g = prof["gemm"]
+    gemm_tflops = g["flops"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else None
+    traffic = GEMM_DRAM_BYTES_PER_CALL.get(name) if gpu_traffic else None
+    roofline = {"kernel": "k_gemm_tc2 / k_gemm_tc (tcgen05 bf16 GEMM, all 5 linear layers fwd + dX + dW)",
+                "bound": "tensor", "achieved": gemm_tflops, "peak": peak_sust, "unit": "TFLOP/s",
+                "frac": (gemm_tflops / peak_sust) if gemm_tflops else None,
+                "traffic": traffic,
+                "traffic_unit": "DRAM bytes per GEMM call (ncu dram__bytes_read.sum + write.sum of the step's "
+                                "GEMM launches, each at full size, weighted by the step's call counts)",
+                "algorithmic_bytes_per_call": (g["bytes"] / g["launches"]) if g["launches"] else None,
+                "peak_kind": f"bf16 dense, sustained ({peak_src})"}
+    total_prof_ms = sum(v["ms"] for k, v in prof.items() if not k.startswith("gemm_"))
+    kernels = {k: {"ms_per_step": v["ms"] / args.steps, "share": (v["ms"] / total_prof_ms) if total_prof_ms else None,
+                   "launches_per_step": v["launches"] / args.steps,
+                   "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["ms"] > 0 and v["flops"] else None,
+                   "gbs": (v["bytes"] / (v["ms"] / 1e3) / 1e9) if v["ms"] > 0 and v["bytes"] else None}
+               for k, v in prof.items() if v["launches"]}
+    return {"value": value, "ms_per_step": ms_step, "mfu": mfu, "flops_per_token": fpt["causal"],
+            "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches_per_step * args.steps), "clocks": clk,
+            "kernels": kernels, "loss": losses[-1],
+            "config": {"workload": DESCR[name], "global_batch": world * w.batch, "seq_len": w.seq_len,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "working set >> L2 (no flush needed)"}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", default="d20", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--config", default="d26", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--extra-configs", default=None,
+                    help="comma-separated workloads measured after --config and reported under 'other_configs' "
+                         "(default: the other bf16 workloads when --config is d26 on one GPU; '' for none)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--step-batch", type=int, default=0,
                     help="profiling only: run the step at this batch size instead of the workload's")
     # single-op mode (profiling)
-    ap.add_argument("--op", choices=["gemm", "gemm8", "attn", "attn_fwd", "optim", "decode"])
+    ap.add_argument("--op", choices=["gemm", "gemm8", "gemmset", "attn", "attn_fwd", "optim", "decode"])
     ap.add_argument("--m", type=int, default=65536)
     ap.add_argument("--n", type=int, default=None, help="default 3840 (--op gemm), 5120 (--op gemm8)")
     ap.add_argument("--k", type=int, default=1280)
@@ -424,6 +616,8 @@ def main():
         return run_decode(args)
     if args.op == "gemm8":
         return run_gemm8(args)
+    if args.op == "gemmset":
+        return run_gemmset(args)
     if args.op:
         return run_op(args)
     w = S.workload(args.config, **({"batch": args.step_batch} if args.step_batch else {}))
@@ -431,7 +625,6 @@ def main():
         return run_reference(args, w)
 
     import torch
-    import decoder_only_transformer_07_b300 as nc
 
     world, rank, local = dist_setup()
     if world > 1:
@@ -442,110 +635,30 @@ def main():
         torch.cuda.set_device(0)
     dev = torch.cuda.current_device()
 
-    model = nc.Model(nc.config_from_workload(w), seed=S.WEIGHT_SEED)
-    tok_np, tgt_np = S.batch_tokens(w)
-    tok = torch.from_numpy(tok_np).cuda()
-    tgt = torch.from_numpy(tgt_np).cuda()
-    grads = torch.empty(model.n_params, dtype=torch.float32, device="cuda")
-    stream = torch.cuda.current_stream()
-
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
-
-    for _ in range(args.warmup):
-        model.forward_backward(tok, tgt, grads)
-    launches_per_step = model.last_launch_count()
-
-    # ---- device-resident timing
-    clocks = ClockSampler(dev)
-    model_prof = nc.lib()
-    model_prof.nc_profile_enable(model.handle, 1)
-    clocks.start()
-    barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    losses = []
-    for _ in range(args.steps):
-        loss, _ = model.forward_backward(tok, tgt, grads)
-        losses.append(loss)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    prof = {}
-    import ctypes
-    for cls, name in enumerate(["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "ce", "embed", "cast", "other",
-                                "gemm_fwd", "gemm_dx", "gemm_dw", "gemm_lm_head"]):
-        t, n, fl, by = ctypes.c_double(), ctypes.c_int64(), ctypes.c_double(), ctypes.c_double()
-        model_prof.nc_profile_read(model.handle, cls, ctypes.byref(t), ctypes.byref(n), ctypes.byref(fl),
-                                   ctypes.byref(by))
-        prof[name] = {"ms": t.value, "launches": n.value, "flops": fl.value, "bytes": by.value}
-    model_prof.nc_profile_enable(model.handle, 0)
-    ms = max_over_ranks(ms, world, "cuda")
-
-    tokens_per_step = w.batch * w.seq_len
-    value = replica_throughput(world, tokens_per_step, args.steps, ms)
-    ms_step = ms / args.steps
-
-    # ---- end-to-end through the host-buffer entry point
-    tok_h = torch.from_numpy(tok_np).pin_memory()
-    tgt_h = torch.from_numpy(tgt_np).pin_memory()
-    for _ in range(2):
-        model.forward_backward_host(tok_h, tgt_h, grads)
-    barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        model.forward_backward_host(tok_h, tgt_h, grads)
-    torch.cuda.synchronize()
-    e2e_s = max_over_ranks(time.perf_counter() - t0, world, "cuda")
-    e2e = {"value": replica_throughput(world, tokens_per_step, args.steps, 1e3 * e2e_s), "unit": UNIT,
-           "h2d_bytes_per_step": int(tok_np.nbytes + tgt_np.nbytes), "d2h_bytes_per_step": 8}
-
-    peak_burst, peak_sust, hbm, peak_src = load_peaks()
-    fpt = flops_per_token(w)
-    per_gpu_tps = value / world
-    mfu = {k: per_gpu_tps * fpt[k] / (peak_burst * 1e12) for k in ("causal", "full_square", "six_n_total")}
-    mfu["causal_vs_sustained"] = per_gpu_tps * fpt["causal"] / (peak_sust * 1e12)
-
-    g = prof["gemm"]
-    gemm_tflops = g["flops"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else None
-    roofline = {"kernel": "k_gemm_tc2 / k_gemm_tc (tcgen05 bf16 GEMM, all 5 linear layers fwd + dX + dW)",
-                "bound": "tensor", "achieved": gemm_tflops, "peak": peak_sust, "unit": "TFLOP/s",
-                "frac": (gemm_tflops / peak_sust) if gemm_tflops else None,
-                "traffic": GEMM_DRAM_BYTES_PER_CALL.get(args.config) if not args.step_batch else None,
-                "traffic_unit": "DRAM bytes per GEMM call (ncu dram__bytes_read.sum + write.sum)",
-                "peak_kind": f"bf16 dense, sustained ({peak_src})"}
-    total_prof_ms = sum(v["ms"] for k, v in prof.items() if not k.startswith("gemm_"))
-    kernels = {k: {"ms_per_step": v["ms"] / args.steps, "share": (v["ms"] / total_prof_ms) if total_prof_ms else None,
-                   "launches_per_step": v["launches"] / args.steps,
-                   "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["ms"] > 0 and v["flops"] else None,
-                   "gbs": (v["bytes"] / (v["ms"] / 1e3) / 1e9) if v["ms"] > 0 and v["bytes"] else None}
-               for k, v in prof.items() if v["launches"]}
+    res = measure(w, args.config, args, world, rank, dev, gpu_traffic=not args.step_batch)
+    extras = args.extra_configs
+    if extras is None:
+        extras = "d20,d24gqa,d12" if (args.config == "d26" and world == 1 and not args.step_batch) else ""
+    others = {}
+    for name in [e for e in extras.split(",") if e]:
+        others[name] = measure(S.workload(name), name, args, world, rank, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        t_sample = CPU_SAMPLE_T.get(args.config, 64)
-        tps, threads, _ = oracle_sample(w, t_sample, 1, 0)
-        cpu = {"value": tps, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"one sequence of {t_sample} tokens of the {args.config} workload, fp64 NumPy fwd+bwd"}
+        cpu = cpu_baseline(w, args.config)
 
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        line = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
                 "data": "synthetic: Zipf(1.1) token ids (seed 2), N(0,0.02) fp32 master weights (seed 1)",
-                "config": {"workload": DESCR[args.config], "global_batch": world * w.batch,
-                           "seq_len": w.seq_len, "parallelism": "replicas" if world > 1 else "single",
-                           "l2": "working set >> L2 (no flush needed)"},
-                "mfu": mfu, "flops_per_token": fpt["causal"], "roofline": roofline, "cpu_baseline": cpu,
-                "e2e": e2e, "gpu_launches": int(launches_per_step * args.steps), "clocks": clk,
-                "kernels": kernels, "loss": losses[-1]}
+                "config": res["config"], "mfu": res["mfu"], "flops_per_token": res["flops_per_token"],
+                "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
+                "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "kernels": res["kernels"],
+                "loss": res["loss"]}
+        if others:
+            line["other_configs"] = others
         print(json.dumps(line), flush=True)
-    model.close()
     if world > 1:
         torch.distributed.destroy_process_group()
 

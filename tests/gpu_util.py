@@ -21,11 +21,12 @@ def rel_close(got, want, rtol, floor_frac=0.1):
     """Per element |got - want| <= rtol * max(|want|, floor_frac * rms(want)).
 
     The floor keeps the bound meaningful for elements near zero, where any
-    finite-precision evaluation has an absolute (not relative) error: fp32
-    roundoff through the ~20 chained operations of a training step is about
-    1e-6 * rms(tensor), so with rtol = 1e-4 a floor of 0.1 * rms leaves 10x
-    margin on it while every element larger than 0.1 * rms is held to the
-    full relative bound.
+    finite-precision evaluation has an absolute (not relative) error.  On the
+    tiny fp32 step the largest error of any gradient or logit element
+    measures 1.0e-5 * rms(tensor) (fp32 roundoff through ~20 chained
+    operations), so the smallest floor every element meets is 0.059 * rms;
+    0.1 * rms keeps a 1.7x margin on it while every element larger than
+    0.1 * rms is held to the full relative bound.
     """
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)

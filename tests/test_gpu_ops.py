@@ -468,7 +468,7 @@ def test_embed_scatter_deterministic_and_exact_rows():
 
 def test_embed_scatter_skips_out_of_range_ids():
     """Ids outside [0, V) add to no row (no out-of-bounds write): every row
-    equals the scatter of the same positions with the bad ones left out."""
+    equals the oracle's scatter of the same positions with the bad ones left out."""
     import synthetic as S
     V, C = 2048, 256
     n = 1500                                     # 6 chunks, ragged tail
@@ -481,16 +481,12 @@ def test_embed_scatter_skips_out_of_range_ids():
     scratch = torch.empty(nc.ops.embed_bwd_scratch_bytes(n, C, V), dtype=torch.uint8, device="cuda")
     got = torch.full((V, C), float("nan"), dtype=F32, device="cuda")
     nc.ops.embed_bwd(torch.from_numpy(tok).cuda(), dev_tensor(dx, F32), got, scratch)
-    ref = torch.full((V, C), float("nan"), dtype=F32, device="cuda")
     tk = np.ascontiguousarray(tok[keep])
-    nk = int(keep.sum())
-    scratch2 = torch.empty(nc.ops.embed_bwd_scratch_bytes(nk, C, V), dtype=torch.uint8, device="cuda")
-    nc.ops.embed_bwd(torch.from_numpy(tk).cuda(), dev_tensor(np.ascontiguousarray(dx[keep]), F32), ref, scratch2)
     torch.cuda.synchronize()
     want = OO.embed_bwd(tk, dx[keep], V)
     g = to64(got)
     assert np.all(np.isfinite(g))
     assert np.allclose(g, want, rtol=1e-5, atol=1e-5 * np.sqrt(np.bincount(tk).max()))
-    # the same rows, by the same per-id order of positions, as the call without the bad positions
-    # (the chunk boundaries differ, so compare the values, not the bits)
-    assert np.allclose(g, to64(ref), rtol=1e-6, atol=1e-6)
+    present = np.zeros(V, dtype=bool)
+    present[tk] = True
+    assert np.all(g[~present] == 0.0)
