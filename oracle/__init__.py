@@ -25,5 +25,5 @@ invariants in ``tests/test_oracle_*.py``.
 from .rng import splitmix64_outputs, normal_init, init_params
 from .model import (Config, param_layout, n_params, rms_norm, rms_norm_bwd,
                     rope_tables, rope, rope_bwd, attention, attention_bwd,
-                    cross_entropy, forward_logits, forward_backward,
+                    cross_entropy, softcap, forward_logits, forward_backward,
                     row_losses, unpack, pack)

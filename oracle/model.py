@@ -17,8 +17,12 @@ Readings of the pages used here (each is repeated where it applies):
 * attention scale ``1/sqrt(hd)`` with a causal mask;
 * GQA query head ``h`` reads key/value head ``h // (H / Hkv)``;
 * RMSNorm ``eps`` is a config field, float32 machine epsilon by default;
-* cross-entropy is the mean over all B*T positions, no ignore index, no
-  logit soft-cap (the pages' "logit stabilisation" is left undefined).
+* cross-entropy is the mean over all B*T positions, no ignore index;
+* two variants, both off by default: the pages' "logit stabilisation"
+  (woshipm nanochat analysis §三.3 item 1) read as the tanh soft-cap
+  ``z <- c tanh(z / c)`` on the lm_head output (``logit_softcap = c > 0``),
+  and a parameter-free RMSNorm right after the embedding lookup
+  (``embed_norm``).
 """
 from dataclasses import dataclass
 
@@ -39,6 +43,8 @@ class Config:
     rope_base: float = 10000.0
     norm_eps: float = FLT_EPSILON
     init_std: float = 0.02
+    logit_softcap: float = 0.0      # c > 0: logits z <- c * tanh(z / c) before the loss
+    embed_norm: bool = False        # RMSNorm of the embedding rows before the first block
 
     @staticmethod
     def from_workload(w, **kw):
@@ -179,6 +185,18 @@ def cross_entropy(z, tgt):
     return loss, dz
 
 
+def softcap(z, c):
+    """Logit soft-cap: (c tanh(z / c), dzc/dz = 1 - tanh(z / c)^2); identity for c <= 0.
+
+    The reading of woshipm nanochat analysis §三.3 item 1 ("logit
+    stabilisation", not defined there): a smooth bound |z| < c on every logit.
+    """
+    if not c or c <= 0:
+        return z, None
+    t = np.tanh(z / c)
+    return c * t, 1.0 - t * t
+
+
 # --------------------------------------------------------------------------
 # One block.  cosmicrealm §2.1 items 2, 4, 6 and devpress §4.1.
 
@@ -267,10 +285,18 @@ def _embed(W, tokens):
     return W["wte"][tokens]
 
 
+def embed_norm_bwd(cfg, W, tokens, dx):
+    """Gradient with respect to the embedding rows e = wte[tok] of x0 = norm(e)."""
+    y0, r0 = rms_norm(_embed(W, tokens), cfg.norm_eps)
+    return rms_norm_bwd(dx, y0, r0)
+
+
 def _trunk(cfg, W, tokens, keep_inputs):
     B, T = tokens.shape
     cos, sin = rope_tables(T, cfg.head_dim, cfg.rope_base)
     x = _embed(W, tokens)
+    if cfg.embed_norm:
+        x, _ = rms_norm(x, cfg.norm_eps)
     xs = []
     for l in range(cfg.depth):
         if keep_inputs:
@@ -287,8 +313,8 @@ def forward_logits(cfg, params, tokens, rows=None):
     B, T, C = xf.shape
     xf = xf.reshape(B * T, C)
     if rows is not None:
-        return xf[np.asarray(rows)] @ W["lm_head"].T
-    return (xf @ W["lm_head"].T).reshape(B, T, -1)
+        return softcap(xf[np.asarray(rows)] @ W["lm_head"].T, cfg.logit_softcap)[0]
+    return softcap(xf @ W["lm_head"].T, cfg.logit_softcap)[0].reshape(B, T, -1)
 
 
 def row_losses(cfg, params, tokens, targets):
@@ -302,7 +328,7 @@ def row_losses(cfg, params, tokens, targets):
     t = targets.reshape(-1)
     out = np.empty(B * T)
     for a in range(0, B * T, 512):
-        z = xf[a:a + 512] @ W["lm_head"].T
+        z, _ = softcap(xf[a:a + 512] @ W["lm_head"].T, cfg.logit_softcap)
         out[a:a + 512], _ = cross_entropy(z, t[a:a + 512])
     return out.reshape(B, T)
 
@@ -327,14 +353,18 @@ def forward_backward(cfg, params, tokens, targets, chunk=512):
     total = 0.0
     dxf = np.empty((N, C))
     for a in range(0, N, chunk):
-        z = xf2[a:a + chunk] @ W["lm_head"].T
+        z, dcap = softcap(xf2[a:a + chunk] @ W["lm_head"].T, cfg.logit_softcap)
         l_rows, dz = cross_entropy(z, t[a:a + chunk])
         total += float(np.sum(l_rows))
         dz /= N                                   # the loss is a mean over B*T
+        if dcap is not None:
+            dz *= dcap                            # through the soft-cap
         G["lm_head"] += dz.T @ xf2[a:a + chunk]
         dxf[a:a + chunk] = dz @ W["lm_head"]
     dx = rms_norm_bwd(dxf.reshape(B, T, C), xf, rstd)
     for l in reversed(range(cfg.depth)):
         dx = block_backward(cfg, W, l, xs[l], dx, cos, sin, G)
+    if cfg.embed_norm:
+        dx = embed_norm_bwd(cfg, W, tokens, dx)
     np.add.at(G["wte"], tokens.reshape(-1), dx.reshape(N, C))
     return total / N, G
