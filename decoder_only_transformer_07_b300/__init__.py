@@ -38,7 +38,8 @@ class nc_config(ctypes.Structure):
                 ("n_kv_head", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("mlp_hidden", ctypes.c_int32), ("vocab", ctypes.c_int32), ("seq_len", ctypes.c_int32),
                 ("batch", ctypes.c_int32), ("dtype", ctypes.c_int32), ("rope_base", ctypes.c_float),
-                ("norm_eps", ctypes.c_float), ("init_std", ctypes.c_float)]
+                ("norm_eps", ctypes.c_float), ("init_std", ctypes.c_float), ("logit_softcap", ctypes.c_float),
+                ("embed_norm", ctypes.c_int32)]
 
 
 class nc_optim_config(ctypes.Structure):
@@ -84,6 +85,7 @@ _SIGS = {
     "nc_op_attention_bwd": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p, _p, _p]),
     "nc_op_attention_bwd_rope": (_i32, [_i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p, _p, _p, _p, _i32, _p]),
     "nc_op_cross_entropy": (_i32, [_i32, _i64, _i32, _p, _p, _p, _f32, _p, _p]),
+    "nc_op_cross_entropy_softcap": (_i32, [_i32, _i64, _i32, _p, _p, _p, _f32, _f32, _p, _p]),
     "nc_op_embed_fwd": (_i32, [_i32, _i64, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_embed_bwd_scratch_bytes": (_sz, [_i64, _i32, _i32]),
     "nc_optim_config_default": (None, [ctypes.POINTER(nc_optim_config)]),
@@ -144,10 +146,10 @@ def _dtype_code(t):
 
 
 def make_config(depth, n_embd, n_head, n_kv_head, head_dim, mlp_hidden, vocab, seq_len, batch,
-                dtype="bf16", rope_base=10000.0, norm_eps=-1.0, init_std=0.02):
+                dtype="bf16", rope_base=10000.0, norm_eps=-1.0, init_std=0.02, logit_softcap=0.0, embed_norm=False):
     d = NC_BF16 if dtype in ("bf16", NC_BF16) else NC_FP32
     return nc_config(depth, n_embd, n_head, n_kv_head, head_dim, mlp_hidden, vocab, seq_len, batch, d,
-                     rope_base, norm_eps, init_std)
+                     rope_base, norm_eps, init_std, logit_softcap, 1 if embed_norm else 0)
 
 
 def optim_config(**kw):
@@ -381,6 +383,12 @@ class ops:
         rows, V = z.shape
         _check(_lib.nc_op_cross_entropy(_dtype_code(z), rows, V, _ptr(z), _ptr(targets), _ptr(row_loss), scale,
                                         _ptr(err), _stream()), "nc_op_cross_entropy")
+
+    @staticmethod
+    def cross_entropy_softcap(z, targets, row_loss, scale, softcap, err=None):
+        rows, V = z.shape
+        _check(_lib.nc_op_cross_entropy_softcap(_dtype_code(z), rows, V, _ptr(z), _ptr(targets), _ptr(row_loss),
+                                                scale, softcap, _ptr(err), _stream()), "nc_op_cross_entropy_softcap")
 
     @staticmethod
     def embed_fwd(tokens, wte, x, dtype, err=None):

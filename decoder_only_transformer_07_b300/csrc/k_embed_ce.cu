@@ -4,16 +4,21 @@
 // The embedding `wte` is a separate (untied) table read by token id
 // (cosmicrealm "noao-chat-0-项目总体介绍" §2.1 item 3); the loss is next-token
 // cross-entropy (devpress "用不到100美元，亲手训练一个属于你的GPT-2" §2.2 item 2).
+#include <algorithm>
+
 #include "nc_kernels.cuh"
 #include "nc_ptx.cuh"
 
 // ---------------------------------------------------------------- gather
 // One warp per token row: x[i] = float(round_act(wte[tokens[i]])).  An id
-// outside [0, V) sets the token error bit and writes a zero row.
-template <typename T>
+// outside [0, V) sets the token error bit and writes a zero row.  With NORM
+// (the variant with a norm after the embedding) the row is then RMS-normalised
+// in fp32, x[i] = e * rstd with rstd = 1/sqrt(mean(e^2) + eps) saved per row,
+// the arithmetic of the step's RMSNorm kernel.
+template <typename T, bool NORM>
 __global__ void k_embed_fwd(int64_t n, int C, int V, const int32_t* __restrict__ tokens,
                             const float* __restrict__ wte, float* __restrict__ x,
-                            int32_t* __restrict__ err) {
+                            int32_t* __restrict__ err, float* __restrict__ rstd, float eps) {
   int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   int lane = threadIdx.x & 31;
   if (i >= n) return;
@@ -22,22 +27,83 @@ __global__ void k_embed_fwd(int64_t n, int C, int V, const int32_t* __restrict__
   if (!ok && lane == 0 && err) atomicOr(err, NC_DEVERR_TOKEN);
   const float4* src = reinterpret_cast<const float4*>(wte + (int64_t)(ok ? tok : 0) * C);
   float4* dst = reinterpret_cast<float4*>(x + i * C);
+  float r = 1.f;
+  if (NORM) {
+    float ss = 0.f;
+    for (int c = lane; c < C / 4; c += 32) {
+      float4 v = ok ? src[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+      v.x = round_act<T>(v.x); v.y = round_act<T>(v.y);
+      v.z = round_act<T>(v.z); v.w = round_act<T>(v.w);
+      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    ss = warp_sum(ss);
+    r = rsqrtf(ss / (float)C + eps);
+    if (lane == 0) rstd[i] = r;
+  }
   for (int c = lane; c < C / 4; c += 32) {
     float4 v = ok ? src[c] : make_float4(0.f, 0.f, 0.f, 0.f);
     v.x = round_act<T>(v.x); v.y = round_act<T>(v.y);
     v.z = round_act<T>(v.z); v.w = round_act<T>(v.w);
+    if (NORM) { v.x *= r; v.y *= r; v.z *= r; v.w *= r; }
     dst[c] = v;
   }
 }
 
 nc_status launch_embed_fwd(int dtype, int64_t n, int C, int V, const int32_t* tokens,
-                           const float* wte, float* x, int32_t* err, cudaStream_t st) {
+                           const float* wte, float* x, int32_t* err, cudaStream_t st, float* rstd, float eps) {
   if (n <= 0) return NC_OK;
   if (C % 4 || (((uintptr_t)wte) & 15) || (((uintptr_t)x) & 15)) return NC_ERR_ARG;
-  if (dtype == NC_BF16)
-    k_embed_fwd<bf16><<<cdiv(n, 8), 256, 0, st>>>(n, C, V, tokens, wte, x, err);
-  else
-    k_embed_fwd<float><<<cdiv(n, 8), 256, 0, st>>>(n, C, V, tokens, wte, x, err);
+  const unsigned g = (unsigned)cdiv(n, 8);
+  if (rstd) {
+    if (dtype == NC_BF16) k_embed_fwd<bf16, true><<<g, 256, 0, st>>>(n, C, V, tokens, wte, x, err, rstd, eps);
+    else k_embed_fwd<float, true><<<g, 256, 0, st>>>(n, C, V, tokens, wte, x, err, rstd, eps);
+  } else {
+    if (dtype == NC_BF16) k_embed_fwd<bf16, false><<<g, 256, 0, st>>>(n, C, V, tokens, wte, x, err, nullptr, 0.f);
+    else k_embed_fwd<float, false><<<g, 256, 0, st>>>(n, C, V, tokens, wte, x, err, nullptr, 0.f);
+  }
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+// Backward of the norm after the embedding, in place on dx (float [n, C]):
+// dx <- rstd * (dx - y * mean(dx * y)) with y = round_act(wte[tok]) * rstd
+// recomputed from the table (one warp per row).  Rows of out-of-range ids
+// (reported by the forward) are left as they are.
+template <typename T>
+__global__ void k_embed_norm_bwd(int64_t n, int C, int V, const int32_t* __restrict__ tokens,
+                                 const float* __restrict__ wte, const float* __restrict__ rstd,
+                                 float* __restrict__ dx) {
+  int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int lane = threadIdx.x & 31;
+  if (i >= n) return;
+  const int tok = tokens[i];
+  if (tok < 0 || tok >= V) return;
+  const float4* src = reinterpret_cast<const float4*>(wte + (int64_t)tok * C);
+  float4* d = reinterpret_cast<float4*>(dx + i * C);
+  const float r = rstd[i];
+  float dot = 0.f;
+  for (int c = lane; c < C / 4; c += 32) {
+    const float4 e = src[c], g = d[c];
+    dot += g.x * (round_act<T>(e.x) * r) + g.y * (round_act<T>(e.y) * r) + g.z * (round_act<T>(e.z) * r) +
+           g.w * (round_act<T>(e.w) * r);
+  }
+  dot = warp_sum(dot) / (float)C;
+  for (int c = lane; c < C / 4; c += 32) {
+    const float4 e = src[c];
+    float4 g = d[c];
+    g.x = r * (g.x - round_act<T>(e.x) * r * dot);
+    g.y = r * (g.y - round_act<T>(e.y) * r * dot);
+    g.z = r * (g.z - round_act<T>(e.z) * r * dot);
+    g.w = r * (g.w - round_act<T>(e.w) * r * dot);
+    d[c] = g;
+  }
+}
+
+nc_status launch_embed_norm_bwd(int dtype, int64_t n, int C, int V, const int32_t* tokens, const float* wte,
+                                const float* rstd, float* dx, cudaStream_t st) {
+  if (n <= 0) return NC_OK;
+  if (C % 4 || (((uintptr_t)wte) & 15) || (((uintptr_t)dx) & 15)) return NC_ERR_ARG;
+  if (dtype == NC_BF16) k_embed_norm_bwd<bf16><<<(unsigned)cdiv(n, 8), 256, 0, st>>>(n, C, V, tokens, wte, rstd, dx);
+  else k_embed_norm_bwd<float><<<(unsigned)cdiv(n, 8), 256, 0, st>>>(n, C, V, tokens, wte, rstd, dx);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
@@ -265,49 +331,77 @@ nc_status launch_embed_bwd(int64_t n, int C, int V, const int32_t* tokens, const
 // ---------------------------------------------------------------- cross-entropy
 // One block per row.  row_loss = logsumexp(z) - z[target];
 // z <- (softmax(z) - onehot(target)) * scale, in place.
-template <typename T>
+//
+// CAP (the logit soft-cap variant, cap = c > 0): every logit enters as
+// zc = c tanh(z / c), and the gradient written is the one with respect to the
+// raw z, (softmax(zc) - onehot) * (1 - tanh(z / c)^2) * scale.  The fp32
+// kernel evaluates tanhf; the bf16 kernels take tanh and its derivative from
+// one SFU exponential (tanh_sech2).
+template <typename T, bool CAP>
 __global__ void __launch_bounds__(512) k_cross_entropy(int V, T* __restrict__ z, int64_t ldz,
                                                        const int32_t* __restrict__ targets,
                                                        float* __restrict__ row_loss, float scale,
-                                                       int32_t* __restrict__ err) {
+                                                       int32_t* __restrict__ err, float cap) {
   __shared__ float sh[32];
   const int64_t row = blockIdx.x;
   T* zr = z + row * ldz;
+  const float icap = CAP ? 1.f / cap : 0.f;
+  auto capped = [&](float v) { return CAP ? cap * tanhf(v * icap) : v; };
   float m = -INFINITY;
-  for (int v = threadIdx.x; v < V; v += blockDim.x) m = fmaxf(m, to_f32(zr[v]));
+  for (int v = threadIdx.x; v < V; v += blockDim.x) m = fmaxf(m, capped(to_f32(zr[v])));
   m = block_max(m, sh);
   float s = 0.f;
-  for (int v = threadIdx.x; v < V; v += blockDim.x) s += expf(to_f32(zr[v]) - m);
+  for (int v = threadIdx.x; v < V; v += blockDim.x) s += expf(capped(to_f32(zr[v])) - m);
   s = block_sum(s, sh);
   const float lse = m + logf(s);
   const int tgt = targets[row];
   const bool ok = tgt >= 0 && tgt < V;
   if (threadIdx.x == 0) {
     if (!ok && err) atomicOr(err, NC_DEVERR_TOKEN);
-    row_loss[row] = ok ? lse - to_f32(zr[tgt]) : 0.f;
+    row_loss[row] = ok ? lse - capped(to_f32(zr[tgt])) : 0.f;
   }
   __syncthreads();   // z[tgt] is read above before any thread overwrites it
   const float inv = 1.f / s;
   for (int v = threadIdx.x; v < V; v += blockDim.x) {
-    float p = expf(to_f32(zr[v]) - m) * inv;
+    const float zv = to_f32(zr[v]);
+    const float t = CAP ? tanhf(zv * icap) : 0.f;
+    float p = expf((CAP ? cap * t : zv) - m) * inv;
     if (v == tgt) p -= 1.f;
+    if (CAP) p *= 1.f - t * t;
     zr[v] = from_f32<T>(p * scale);
   }
+}
+
+__device__ __forceinline__ uint4 pack8_bf16_rn(const float* p) {
+  uint4 o;
+  __nv_bfloat162 q0 = __floats2bfloat162_rn(p[0], p[1]), q1 = __floats2bfloat162_rn(p[2], p[3]);
+  __nv_bfloat162 q2 = __floats2bfloat162_rn(p[4], p[5]), q3 = __floats2bfloat162_rn(p[6], p[7]);
+  o.x = *reinterpret_cast<uint32_t*>(&q0);
+  o.y = *reinterpret_cast<uint32_t*>(&q1);
+  o.z = *reinterpret_cast<uint32_t*>(&q2);
+  o.w = *reinterpret_cast<uint32_t*>(&q3);
+  return o;
 }
 
 // bf16 rows with V % 8 == 0 and V <= 8 * CE_THREADS * CE_VEC: the row is read once
 // into registers (16-byte loads), reduced, and dz written from registers.
 #define CE_THREADS 1024
 #define CE_VEC 8
+template <bool CAP>
 __global__ void __launch_bounds__(CE_THREADS) k_cross_entropy_bf16(int V, bf16* __restrict__ z, int64_t ldz,
                                                                    const int32_t* __restrict__ targets,
                                                                    float* __restrict__ row_loss, float scale,
-                                                                   int32_t* __restrict__ err) {
+                                                                   int32_t* __restrict__ err, float cap) {
   __shared__ float sh[32];
   __shared__ float ztgt;
   const int64_t row = blockIdx.x;
   bf16* zr = z + row * ldz;
   const int nv = V / 8;
+  const float icap = CAP ? 1.f / cap : 0.f;
+  auto capped = [&](float v) {
+    float d;
+    return CAP ? cap * tanh_sech2(v * icap, &d) : v;
+  };
   uint4 v[CE_VEC];
   float m = -INFINITY;
 #pragma unroll
@@ -317,12 +411,12 @@ __global__ void __launch_bounds__(CE_THREADS) k_cross_entropy_bf16(int V, bf16* 
       v[k] = reinterpret_cast<const uint4*>(zr)[i];
       const bf16* e = reinterpret_cast<const bf16*>(&v[k]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) m = fmaxf(m, __bfloat162float(e[j]));
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, capped(__bfloat162float(e[j])));
     }
   }
   const int tgt = targets[row];
   const bool ok = tgt >= 0 && tgt < V;
-  if (threadIdx.x == 0) ztgt = ok ? __bfloat162float(zr[tgt]) : 0.f;
+  if (threadIdx.x == 0) ztgt = ok ? capped(__bfloat162float(zr[tgt])) : 0.f;
   m = block_max(m, sh);
   const float L2E = 1.4426950408889634f;
   const float mb = m * L2E;
@@ -333,7 +427,7 @@ __global__ void __launch_bounds__(CE_THREADS) k_cross_entropy_bf16(int V, bf16* 
     if (i < nv) {
       const bf16* e = reinterpret_cast<const bf16*>(&v[k]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) sum += ex2_approx(fmaf(__bfloat162float(e[j]), L2E, -mb));
+      for (int j = 0; j < 8; ++j) sum += ex2_approx(fmaf(capped(__bfloat162float(e[j])), L2E, -mb));
     }
   }
   sum = block_sum(sum, sh);
@@ -351,17 +445,14 @@ __global__ void __launch_bounds__(CE_THREADS) k_cross_entropy_bf16(int V, bf16* 
       float p[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        p[j] = ex2_approx(fmaf(__bfloat162float(e[j]), L2E, -mb)) * inv;
+        const float zv = __bfloat162float(e[j]);
+        float d = 1.f;
+        const float t = CAP ? tanh_sech2(zv * icap, &d) : 0.f;
+        p[j] = ex2_approx(fmaf(CAP ? cap * t : zv, L2E, -mb)) * inv;
         if (i * 8 + j == tgt) p[j] -= scale;
+        if (CAP) p[j] *= d;
       }
-      uint4 o;
-      __nv_bfloat162 q0 = __floats2bfloat162_rn(p[0], p[1]), q1 = __floats2bfloat162_rn(p[2], p[3]);
-      __nv_bfloat162 q2 = __floats2bfloat162_rn(p[4], p[5]), q3 = __floats2bfloat162_rn(p[6], p[7]);
-      o.x = *reinterpret_cast<uint32_t*>(&q0);
-      o.y = *reinterpret_cast<uint32_t*>(&q1);
-      o.z = *reinterpret_cast<uint32_t*>(&q2);
-      o.w = *reinterpret_cast<uint32_t*>(&q3);
-      reinterpret_cast<uint4*>(zr)[i] = o;
+      reinterpret_cast<uint4*>(zr)[i] = pack8_bf16_rn(p);
     }
   }
 }
@@ -372,16 +463,22 @@ __global__ void __launch_bounds__(CE_THREADS) k_cross_entropy_bf16(int V, bf16* 
 // sum is rescaled when the maximum grows); pass 2 reads the row again, while
 // it is still in L2, and writes dz in place.
 #define CE2_THREADS 256
+template <bool CAP>
 __global__ void __launch_bounds__(CE2_THREADS, 4) k_cross_entropy_bf16_stream(int V, bf16* __restrict__ z, int64_t ldz,
                                                                              const int32_t* __restrict__ targets,
                                                                              float* __restrict__ row_loss, float scale,
-                                                                             int32_t* __restrict__ err) {
+                                                                             int32_t* __restrict__ err, float cap) {
   __shared__ float shm[CE2_THREADS / 32], shs[CE2_THREADS / 32];
   const int64_t row = blockIdx.x;
   bf16* zr = z + row * ldz;
   const uint4* zv = reinterpret_cast<const uint4*>(zr);
   const int nv = V / 8;
   const float L2E = 1.4426950408889634f;
+  const float icap = CAP ? 1.f / cap : 0.f;
+  auto capped = [&](float v) {
+    float d;
+    return CAP ? cap * tanh_sech2(v * icap, &d) : v;
+  };
   float m = -INFINITY, sum = 0.f;   // m in log2 units
   for (int i0 = threadIdx.x; i0 < nv; i0 += 4 * CE2_THREADS) {
     uint4 u[4];
@@ -395,7 +492,7 @@ __global__ void __launch_bounds__(CE2_THREADS, 4) k_cross_entropy_bf16_stream(in
       float x[8], cm = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        x[j] = __bfloat162float(e[j]) * L2E;
+        x[j] = capped(__bfloat162float(e[j])) * L2E;
         cm = fmaxf(cm, x[j]);
       }
       if (cm > m) {
@@ -435,7 +532,7 @@ __global__ void __launch_bounds__(CE2_THREADS, 4) k_cross_entropy_bf16_stream(in
   const int tgt = targets[row];
   const bool ok = tgt >= 0 && tgt < V;
   if (threadIdx.x == 0) {
-    const float ztgt = ok ? __bfloat162float(zr[tgt]) : 0.f;
+    const float ztgt = ok ? capped(__bfloat162float(zr[tgt])) : 0.f;
     if (!ok && err) atomicOr(err, NC_DEVERR_TOKEN);
     row_loss[row] = ok ? (m + log2f(sum)) * 0.69314718055994531f - ztgt : 0.f;
   }
@@ -448,35 +545,55 @@ __global__ void __launch_bounds__(CE2_THREADS, 4) k_cross_entropy_bf16_stream(in
     float p[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      p[j] = ex2_approx(fmaf(__bfloat162float(e[j]), L2E, -m)) * inv;
+      const float zz = __bfloat162float(e[j]);
+      float d = 1.f;
+      const float t = CAP ? tanh_sech2(zz * icap, &d) : 0.f;
+      p[j] = ex2_approx(fmaf(CAP ? cap * t : zz, L2E, -m)) * inv;
       if (i * 8 + j == tgt) p[j] -= scale;
+      if (CAP) p[j] *= d;
     }
-    uint4 o;
-    __nv_bfloat162 q0 = __floats2bfloat162_rn(p[0], p[1]), q1 = __floats2bfloat162_rn(p[2], p[3]);
-    __nv_bfloat162 q2 = __floats2bfloat162_rn(p[4], p[5]), q3 = __floats2bfloat162_rn(p[6], p[7]);
-    o.x = *reinterpret_cast<uint32_t*>(&q0);
-    o.y = *reinterpret_cast<uint32_t*>(&q1);
-    o.z = *reinterpret_cast<uint32_t*>(&q2);
-    o.w = *reinterpret_cast<uint32_t*>(&q3);
-    zw[i] = o;
+    zw[i] = pack8_bf16_rn(p);
   }
+}
+
+template <bool CAP>
+static void launch_ce_t(int dtype, int64_t rows, int V, void* z, int64_t ldz, const int32_t* targets,
+                        float* row_loss, float scale, int32_t* err, float cap, cudaStream_t st) {
+  const bool vec = dtype == NC_BF16 && V % 8 == 0 && ldz % 8 == 0 && (((uintptr_t)z) & 15) == 0;
+  const unsigned g = (unsigned)rows;
+  if (vec && V >= 16384)
+    k_cross_entropy_bf16_stream<CAP><<<g, CE2_THREADS, 0, st>>>(V, (bf16*)z, ldz, targets, row_loss, scale, err, cap);
+  else if (vec && V <= 8 * CE_THREADS * CE_VEC)
+    k_cross_entropy_bf16<CAP><<<g, CE_THREADS, 0, st>>>(V, (bf16*)z, ldz, targets, row_loss, scale, err, cap);
+  else if (dtype == NC_BF16)
+    k_cross_entropy<bf16, CAP><<<g, 512, 0, st>>>(V, (bf16*)z, ldz, targets, row_loss, scale, err, cap);
+  else
+    k_cross_entropy<float, CAP><<<g, 512, 0, st>>>(V, (float*)z, ldz, targets, row_loss, scale, err, cap);
 }
 
 nc_status launch_cross_entropy(int dtype, int64_t rows, int V, void* z, int64_t ldz,
                                const int32_t* targets, float* row_loss, float scale, int32_t* err,
-                               cudaStream_t st) {
+                               cudaStream_t st, float softcap) {
   if (rows <= 0) return NC_OK;
   if (rows > 0x7fffffff) return NC_ERR_ARG;
-  const bool vec = dtype == NC_BF16 && V % 8 == 0 && ldz % 8 == 0 && (((uintptr_t)z) & 15) == 0;
-  if (vec && V >= 16384)
-    k_cross_entropy_bf16_stream<<<(unsigned)rows, CE2_THREADS, 0, st>>>(V, (bf16*)z, ldz, targets, row_loss, scale,
-                                                                        err);
-  else if (vec && V <= 8 * CE_THREADS * CE_VEC)
-    k_cross_entropy_bf16<<<(unsigned)rows, CE_THREADS, 0, st>>>(V, (bf16*)z, ldz, targets, row_loss, scale, err);
-  else if (dtype == NC_BF16)
-    k_cross_entropy<bf16><<<(unsigned)rows, 512, 0, st>>>(V, (bf16*)z, ldz, targets, row_loss, scale, err);
-  else
-    k_cross_entropy<float><<<(unsigned)rows, 512, 0, st>>>(V, (float*)z, ldz, targets, row_loss, scale, err);
+  if (!(softcap >= 0.f) || softcap == INFINITY) return NC_ERR_ARG;
+  if (softcap > 0.f) launch_ce_t<true>(dtype, rows, V, z, ldz, targets, row_loss, scale, err, softcap, st);
+  else launch_ce_t<false>(dtype, rows, V, z, ldz, targets, row_loss, scale, err, 0.f, st);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+// z <- c tanh(z / c) in place on n fp32 logits (the soft-cap variant's
+// logits, for the entry points that return them).  Grid-stride, tanhf.
+__global__ void k_softcap_f32(int64_t n, float* __restrict__ z, float cap) {
+  const float icap = 1.f / cap;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    z[i] = cap * tanhf(z[i] * icap);
+}
+
+nc_status launch_softcap_f32(int64_t n, float* z, float cap, cudaStream_t st) {
+  if (n <= 0 || cap <= 0.f) return NC_OK;
+  const int64_t blocks = std::min<int64_t>(cdiv(n, 256), 148 * 16);
+  k_softcap_f32<<<(unsigned)blocks, 256, 0, st>>>(n, z, cap);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 

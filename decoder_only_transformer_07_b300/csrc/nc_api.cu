@@ -37,6 +37,9 @@ struct nc_model {
   void* wact = nullptr;              // compute-dtype weights [P] (== master in fp32 mode)
   float* rope_tab = nullptr;         // [Tmax, hd/2, 2]
   float* rope_pairs = nullptr;       // the same, pair-major [hd/4, Tmax, 4] (bf16 QKV GEMM epilogue)
+  float softcap = 0.f;               // logit soft-cap c (0: off)
+  bool emb_norm = false;             // RMSNorm after the embedding lookup
+  float* rstd_e = nullptr;           // [Nmax] its per-row rstd (emb_norm only)
   int32_t* err = nullptr;            // device error flag
   float* result = nullptr;           // device: [0] loss, [1] error flag copy
   float* result_host = nullptr;      // pinned host copy
@@ -245,6 +248,8 @@ static nc_status validate(const nc_config* c, nc_config* out) {
   if (k.dtype == NC_BF16 && k.head_dim != 64 && k.head_dim != 128) return NC_ERR_CONFIG;
   if (k.n_embd % 8 || k.mlp_hidden % 8 || k.vocab % 8) return NC_ERR_CONFIG;
   if (k.n_embd > 8192) return NC_ERR_CONFIG;
+  if (!(k.logit_softcap >= 0.f) || k.logit_softcap == INFINITY) return NC_ERR_CONFIG;
+  if (k.embed_norm != 0 && k.embed_norm != 1) return NC_ERR_CONFIG;
   if ((int64_t)k.batch * k.seq_len > (1 << 20)) return NC_ERR_CONFIG;
   *out = k;
   return NC_OK;
@@ -293,6 +298,7 @@ static nc_status allocate(nc_model* m) {
   NC_TRY(dalloc_t(m, (size_t)L * N * (m->H + m->Hkv), &m->rstdqk));
   NC_TRY(dalloc_t(m, (size_t)L * N * m->H, &m->lse));
   NC_TRY(dalloc(m, (size_t)N * m->C * a, &m->xf));
+  if (m->emb_norm) NC_TRY(dalloc_t(m, (size_t)N, &m->rstd_e));
   NC_TRY(dalloc_t(m, (size_t)N, &m->rstd_f));
   // logits chunk: at most 1 GiB of compute-dtype logits per chunk, whole 128-row tiles
   int64_t rows = ((int64_t)1 << 30) / ((int64_t)m->V * (int64_t)a);
@@ -370,6 +376,8 @@ extern "C" nc_status nc_model_create(const nc_config* cfg, uint64_t seed, nc_mod
   m->dtype = c.dtype;
   m->act = (c.dtype == NC_BF16) ? 2 : 4;
   m->Nmax = (int64_t)c.batch * c.seq_len;
+  m->softcap = c.logit_softcap;
+  m->emb_norm = c.embed_norm != 0;
   build_layout(m);
   nc_status s = allocate(m);
   cudaStream_t st = 0;
@@ -468,7 +476,7 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
     m->launches += 1;
   }
   PROF(NC_PROF_EMBED, 0, (double)N * (8.0 * C + 4),
-       launch_embed_fwd(m->dtype, N, C, m->V, tokens, m->master, m->x, m->err, st));
+       launch_embed_fwd(m->dtype, N, C, m->V, tokens, m->master, m->x, m->err, st, m->rstd_e, eps));
   m->launches += 1;
   const double a = (double)m->act;
   const int nh = m->H + m->Hkv;
@@ -566,6 +574,11 @@ static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int 
     m->launches += 3 + 1 + 2;
   }
   const ParamTensor& te = m->layout[0];
+  if (m->emb_norm) {   // through the norm after the embedding, in place on dx
+    PROF(NC_PROF_EMBED, 0, (double)N * (12.0 * C + 8),
+         launch_embed_norm_bwd(m->dtype, N, C, m->V, tokens, m->master, m->rstd_e, m->dx, st));
+    m->launches += 1;
+  }
   PROF(NC_PROF_EMBED, 0, 4.0 * N * C + 4.0 * m->V * C,
        launch_embed_bwd(N, C, m->V, tokens, m->dx, grads + te.off, m->emb_scratch, st, accumulate ? 1 : 0,
                         m->err));
@@ -591,7 +604,8 @@ static nc_status step(nc_model* m, const int32_t* tokens, const int32_t* targets
     const void* xfc = (const uint8_t*)m->xf + (size_t)c0 * C * m->act;
     NC_TRY(gemm(m, NC_PROF_GEMM_LM, nc, V, C, xfc, C, 1, Wlm, C, 1, NC_EP_STORE, m->logits, V, nullptr, 0, st));
     PROF(NC_PROF_CE, 0, (double)nc * (2.0 * V * m->act + 8),
-         launch_cross_entropy(m->dtype, nc, V, m->logits, V, targets + c0, m->rowloss + c0, scale, m->err, st));
+         launch_cross_entropy(m->dtype, nc, V, m->logits, V, targets + c0, m->rowloss + c0, scale, m->err, st,
+                              m->softcap));
     NC_TRY(gemm(m, NC_PROF_GEMM_LM, nc, C, V, m->logits, V, 1, Wlm, C, 0, NC_EP_STORE_F32, m->dxn + c0 * C, C, nullptr, 0, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_LM, V, C, nc, m->logits, V, 0, xfc, C, 0,
                 (c0 == 0 && !accumulate) ? NC_EP_STORE_F32 : NC_EP_ACCUM_F32,
@@ -647,7 +661,7 @@ extern "C" nc_status nc_forward_logits(nc_model* m, const int32_t* tokens, int32
   const int64_t N = (int64_t)B * T;
   NC_TRY(gemm(m, NC_PROF_GEMM_LM, (int)N, m->V, m->C, m->xf, m->C, 1, wptr(m, m->layout.back()), m->C, 1, NC_EP_STORE_F32, logits,
               m->V, nullptr, 0, st));
-  return NC_OK;
+  return launch_softcap_f32(N * m->V, logits, m->softcap, st);
 }
 
 extern "C" nc_status nc_forward_row_losses(nc_model* m, const int32_t* tokens, const int32_t* targets, int32_t B,
@@ -663,7 +677,8 @@ extern "C" nc_status nc_forward_row_losses(nc_model* m, const int32_t* tokens, c
     const void* xfc = (const uint8_t*)m->xf + (size_t)c0 * m->C * m->act;
     NC_TRY(gemm(m, NC_PROF_GEMM_LM, nc, m->V, m->C, xfc, m->C, 1, wptr(m, m->layout.back()), m->C, 1, NC_EP_STORE, m->logits, m->V,
                 nullptr, 0, st));
-    NC_TRY(launch_cross_entropy(m->dtype, nc, m->V, m->logits, m->V, targets + c0, losses + c0, 1.f, m->err, st));
+    NC_TRY(launch_cross_entropy(m->dtype, nc, m->V, m->logits, m->V, targets + c0, losses + c0, 1.f, m->err, st,
+                                m->softcap));
   }
   return NC_OK;
 }
@@ -760,6 +775,15 @@ extern "C" nc_status nc_op_cross_entropy(int32_t dtype, int64_t rows, int32_t V,
                                          float* row_loss, float grad_scale, int32_t* err_dev, void* stream) {
   if (!dtype_ok(dtype) || !z || !targets || !row_loss || V <= 0) return NC_ERR_ARG;
   return launch_cross_entropy(dtype, rows, V, z, V, targets, row_loss, grad_scale, err_dev, as_stream(stream));
+}
+
+extern "C" nc_status nc_op_cross_entropy_softcap(int32_t dtype, int64_t rows, int32_t V, void* z,
+                                                 const int32_t* targets, float* row_loss, float grad_scale,
+                                                 float softcap, int32_t* err_dev, void* stream) {
+  if (!dtype_ok(dtype) || !z || !targets || !row_loss || V <= 0) return NC_ERR_ARG;
+  if (!(softcap >= 0.f) || softcap == INFINITY) return NC_ERR_ARG;
+  return launch_cross_entropy(dtype, rows, V, z, V, targets, row_loss, grad_scale, err_dev, as_stream(stream),
+                              softcap);
 }
 
 extern "C" nc_status nc_op_embed_fwd(int32_t dtype, int64_t n, int32_t C, int32_t V, const int32_t* tokens,
@@ -1094,6 +1118,7 @@ extern "C" nc_status nc_prefill(nc_model* m, const int32_t* tokens, int32_t B, i
   const void* last = (const uint8_t*)m->xf + (size_t)(T - 1) * m->C * m->act;
   NC_TRY(gemm(m, NC_PROF_GEMM_LM, B, m->V, m->C, last, (int64_t)T * m->C, 1, wptr(m, m->layout.back()), m->C, 1,
               NC_EP_STORE_F32, logits, m->V, nullptr, 0, st));
+  NC_TRY(launch_softcap_f32((int64_t)B * m->V, logits, m->softcap, st));
   NC_TRY(launch_set_i32(m->dec_pos, T, false, st));
   m->kv_batch = B;
   m->kv_len = T;
@@ -1121,7 +1146,7 @@ static nc_status decode_body(nc_model* m, int B, cudaStream_t st) {
     NC_TRY(launch_rmsnorm_fwd(m->dtype, B, C, m->x, xn, rstd, eps, st));
     return proj(role, N, C, xn, w, ep, d, ldd);
   };
-  NC_TRY(launch_embed_fwd(m->dtype, B, C, m->V, m->dec_tok, m->master, m->x, m->err, st));
+  NC_TRY(launch_embed_fwd(m->dtype, B, C, m->V, m->dec_tok, m->master, m->x, m->err, st, m->rstd_e, eps));
   uint8_t* xn1 = layer_act(m, m->xn1, 0, C);
   uint8_t* xn2 = layer_act(m, m->xn2, 0, C);
   uint8_t* qkv = layer_act(m, m->qkv, 0, W);
@@ -1139,6 +1164,7 @@ static nc_status decode_body(nc_model* m, int B, cudaStream_t st) {
   }
   NC_TRY(norm_proj(NC_PROF_GEMM_LM, m->V, wptr(m, m->layout.back()), NC_EP_STORE_F32, m->dec_logits, m->V, m->xf,
                    m->rstd_f));
+  NC_TRY(launch_softcap_f32((int64_t)B * m->V, m->dec_logits, m->softcap, st));
   return launch_set_i32(m->dec_pos, 1, true, st);
 }
 

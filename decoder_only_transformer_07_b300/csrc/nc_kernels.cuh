@@ -25,8 +25,13 @@ nc_status launch_rope_qknorm_bwd(int dtype, int B, int T, int H, int Hkv, int hd
                                  const void* qkv, const float* rstd, const float* tab,
                                  cudaStream_t st);
 
+// rstd != NULL: the variant with a norm after the embedding (x = e * rstd, rstd saved per row).
 nc_status launch_embed_fwd(int dtype, int64_t n, int C, int V, const int32_t* tokens,
-                           const float* wte, float* x, int32_t* err, cudaStream_t st);
+                           const float* wte, float* x, int32_t* err, cudaStream_t st, float* rstd = nullptr,
+                           float eps = 0.f);
+// In place on dx [n, C]: the backward of that norm, its output recomputed from wte.
+nc_status launch_embed_norm_bwd(int dtype, int64_t n, int C, int V, const int32_t* tokens, const float* wte,
+                                const float* rstd, float* dx, cudaStream_t st);
 size_t embed_bwd_scratch_bytes(int64_t n, int C, int V);
 // accumulate != 0: dwte += the scatter (rows of absent ids untouched); else dwte = it.
 // Positions whose id lies outside [0, V) add to no row and set the token bit of
@@ -34,9 +39,12 @@ size_t embed_bwd_scratch_bytes(int64_t n, int C, int V);
 nc_status launch_embed_bwd(int64_t n, int C, int V, const int32_t* tokens, const float* dx,
                            float* dwte, void* scratch, cudaStream_t st, int accumulate = 0,
                            int32_t* err = nullptr);
+// softcap > 0: the logits enter as softcap * tanh(z / softcap) (dz is taken with respect to z).
 nc_status launch_cross_entropy(int dtype, int64_t rows, int V, void* z, int64_t ldz,
                                const int32_t* targets, float* row_loss, float scale, int32_t* err,
-                               cudaStream_t st);
+                               cudaStream_t st, float softcap = 0.f);
+// z <- cap * tanh(z / cap) on n fp32 logits (no-op for cap <= 0).
+nc_status launch_softcap_f32(int64_t n, float* z, float cap, cudaStream_t st);
 nc_status launch_mean(int64_t n, const float* x, float* out, cudaStream_t st);
 
 nc_status launch_gemm_simt(int dtype, int M, int N, int K, const void* A, int64_t lda, int a_kmajor,

@@ -170,6 +170,19 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// tanh(x) and its derivative 1 - tanh(x)^2 from one exponential u = e^{2x}:
+// tanh = (u - 1)/(u + 1), 1 - tanh^2 = 4u/(u + 1)^2.  |x| is clamped to 15,
+// where tanh is 1 to within fp32 rounding, so u stays finite.  The absolute
+// error of tanh is a few fp32 ulps of 1, and the derivative keeps its
+// relative accuracy where tanh saturates (no 1 - t*t cancellation).
+__device__ __forceinline__ float tanh_sech2(float x, float* sech2) {
+  x = fminf(fmaxf(x, -15.f), 15.f);
+  const float u = ex2_approx(x * 2.8853900817779268f);   // 2 log2(e) x
+  const float r = __frcp_rn(u + 1.f);
+  *sech2 = 4.f * u * r * r;
+  return (u - 1.f) * r;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }

@@ -56,6 +56,13 @@ typedef struct {
   float rope_base;     /* RoPE base; 10000 when <= 0                          */
   float norm_eps;      /* RMSNorm eps; FLT_EPSILON when < 0                   */
   float init_std;      /* std of the N(0, std) init; 0.02 when <= 0           */
+  /* Variants, both off when 0 (woshipm nanochat analysis §三.3 item 1 names a
+   * "logit stabilisation" without defining it; read here as the soft-cap): */
+  float logit_softcap; /* c > 0: every logit z becomes c * tanh(z / c) before
+                          the softmax and in nc_forward_logits / decoding
+                          outputs; must be finite and >= 0                   */
+  int32_t embed_norm;  /* 1: RMSNorm (no gain, eps = norm_eps) of each
+                          embedding row before the first block; 0 or 1       */
 } nc_config;
 
 typedef struct nc_model nc_model;
@@ -276,6 +283,14 @@ nc_status nc_op_attention_bwd_rope(int32_t B, int32_t T, int32_t H, int32_t Hkv,
 nc_status nc_op_cross_entropy(int32_t dtype, int64_t rows, int32_t V, void* z,
                               const int32_t* targets, float* row_loss, float grad_scale,
                               int32_t* err_dev, void* stream);
+/* The same with the logit soft-cap: the loss is taken on c * tanh(z / c)
+ * (softcap = c > 0, finite) and z is overwritten with the gradient with
+ * respect to the raw logits, (softmax(zc) - onehot) * (1 - tanh(z / c)^2) *
+ * grad_scale; softcap = 0 is nc_op_cross_entropy.  NC_ERR_ARG for a negative
+ * or non-finite softcap. */
+nc_status nc_op_cross_entropy_softcap(int32_t dtype, int64_t rows, int32_t V, void* z,
+                                      const int32_t* targets, float* row_loss, float grad_scale,
+                                      float softcap, int32_t* err_dev, void* stream);
 
 /* x (float [n, C]) = float(round_dtype(wte[tokens[i]])) for wte float [V, C]. */
 nc_status nc_op_embed_fwd(int32_t dtype, int64_t n, int32_t C, int32_t V,

@@ -46,6 +46,9 @@ def test_status_strings_and_version():
     ("vocab", 0),
     ("seq_len", -1),
     ("dtype", 7),
+    ("logit_softcap", -1.0),  # the cap is c >= 0 (0: off)
+    ("logit_softcap", float("inf")),
+    ("embed_norm", 2),        # a 0/1 switch
 ])
 def test_invalid_config_rejected_without_gpu(field, value):
     kw = dict(depth=2, n_embd=256, n_head=2, n_kv_head=2, head_dim=128, mlp_hidden=1024, vocab=512,
