@@ -28,6 +28,8 @@ from dataclasses import dataclass
 
 import numpy as np
 
+from . import fp8 as _fp8
+
 FLT_EPSILON = float(np.finfo(np.float32).eps)
 
 
@@ -45,6 +47,7 @@ class Config:
     init_std: float = 0.02
     logit_softcap: float = 0.0      # c > 0: logits z <- c * tanh(z / c) before the loss
     embed_norm: bool = False        # RMSNorm of the embedding rows before the first block
+    fp8: bool = False               # the blocks' four linear layers multiply E4M3 operands (forward)
 
     @staticmethod
     def from_workload(w, **kw):
@@ -185,6 +188,42 @@ def cross_entropy(z, tgt):
     return loss, dz
 
 
+def bf16_round(x):
+    """Round to bfloat16 (round to nearest, ties to even) through float32,
+    returned as fp64: the top 16 bits of the float32 pattern after adding
+    0x7fff plus the lowest kept bit (finite inputs)."""
+    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def quantize_dequantize(x):
+    """Per-tensor E4M3 quantisation (of the float32 values of x, which are
+    exact for the bf16 activations and fp32 weights it receives) and the
+    values it stands for: decode(codes) * scale_inv (``oracle/fp8.py``)."""
+    codes, _, _, scale_inv = _fp8.quantize(x)
+    return _fp8.e4m3_decode(codes) * float(scale_inv)
+
+
+def linear(cfg, x, w):
+    """A bias-free linear layer y = x w^T (w stored [out, in]).
+
+    With cfg.fp8 (the 8-bit reading of woshipm nanochat analysis §一.2 / §六.2,
+    which name FP8 without a recipe): both operands are quantised per tensor
+    to E4M3 with current scaling, the activation from its bfloat16 value (the
+    tensor the layer reads) and the weight from its float32 master value, and
+    the product of the decoded values is taken exactly (fp32 accumulation on
+    the device).  The backward is unchanged: the gradient passes through each
+    quantiser as the identity, so dX = dY w and dW = dY^T x use the
+    unquantised operands.
+    """
+    if not cfg.fp8:
+        return x @ w.T
+    xq = quantize_dequantize(bf16_round(x))
+    wq = quantize_dequantize(w)
+    return xq @ wq.T
+
+
 def softcap(z, c):
     """Logit soft-cap: (c tanh(z / c), dzc/dz = 1 - tanh(z / c)^2); identity for c <= 0.
 
@@ -210,9 +249,15 @@ def block_forward(cfg, W, l, x, cos, sin, keep=False):
     H, Hkv, hd = cfg.n_head, cfg.n_kv_head, cfg.head_dim
     p = f"h{l}."
     a, rstd1 = rms_norm(x, cfg.norm_eps)
-    q = (a @ W[p + "wq"].T).reshape(B, T, H, hd).transpose(0, 2, 1, 3)
-    k = (a @ W[p + "wk"].T).reshape(B, T, Hkv, hd).transpose(0, 2, 1, 3)
-    v = (a @ W[p + "wv"].T).reshape(B, T, Hkv, hd).transpose(0, 2, 1, 3)
+    if cfg.fp8:
+        # one operand tensor [Wq; Wk; Wv] for the three projections, as multiplied together
+        qkv = linear(cfg, a, np.concatenate([W[p + "wq"], W[p + "wk"], W[p + "wv"]], axis=0))
+        q2, k2, v2 = np.split(qkv, [H * hd, (H + Hkv) * hd], axis=-1)
+    else:
+        q2, k2, v2 = a @ W[p + "wq"].T, a @ W[p + "wk"].T, a @ W[p + "wv"].T
+    q = q2.reshape(B, T, H, hd).transpose(0, 2, 1, 3)
+    k = k2.reshape(B, T, Hkv, hd).transpose(0, 2, 1, 3)
+    v = v2.reshape(B, T, Hkv, hd).transpose(0, 2, 1, 3)
     qr, kr = rope(q, cos, sin), rope(k, cos, sin)          # RoPE first ...
     qn, rq = rms_norm(qr, cfg.norm_eps)                     # ... then QK norm
     kn, rk = rms_norm(kr, cfg.norm_eps)
@@ -222,12 +267,12 @@ def block_forward(cfg, W, l, x, cos, sin, keep=False):
             g = _kv_head_of(cfg, h)
             o[b, h], _ = attention(qn[b, h], kn[b, g], v[b, g])
     o2 = o.transpose(0, 2, 1, 3).reshape(B, T, H * hd)
-    x1 = x + o2 @ W[p + "wo"].T
+    x1 = x + linear(cfg, o2, W[p + "wo"])
     bn, rstd2 = rms_norm(x1, cfg.norm_eps)
-    u = bn @ W[p + "wfc"].T
+    u = linear(cfg, bn, W[p + "wfc"])
     r = np.maximum(u, 0.0)
     hmid = r * r                                            # relu(u)^2
-    x2 = x1 + hmid @ W[p + "wproj"].T
+    x2 = x1 + linear(cfg, hmid, W[p + "wproj"])
     if not keep:
         return x2
     return x2, dict(a=a, rstd1=rstd1, qn=qn, kn=kn, rq=rq, rk=rk, v=v, o2=o2,
