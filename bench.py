@@ -477,15 +477,16 @@ def run_gemmset(args):
     print(json.dumps({"op": "gemmset", "config": args.config, "launches": rows}), flush=True)
 
 
-def measure(w, name, args, world, rank, dev, gpu_traffic=True):
+def measure(w, name, args, world, rank, dev, gpu_traffic=True, fp8=False):
     """Time `args.steps` training steps of workload w (device-resident inputs),
     then the same through the host-buffer entry point; returns the fields of
-    the bench line for this workload."""
+    the bench line for this workload.  fp8: the 8-bit step (the blocks'
+    forward linears on E4M3 operands)."""
     import ctypes
     import torch
     import decoder_only_transformer_07_b300 as nc
 
-    model = nc.Model(nc.config_from_workload(w), seed=S.WEIGHT_SEED)
+    model = nc.Model(nc.config_from_workload(w, fp8=fp8), seed=S.WEIGHT_SEED)
     tok_np, tgt_np = S.batch_tokens(w)
     tok = torch.from_numpy(tok_np).cuda()
     tgt = torch.from_numpy(tgt_np).cuda()
@@ -520,7 +521,7 @@ def measure(w, name, args, world, rank, dev, gpu_traffic=True):
     ms = e0.elapsed_time(e1)
     prof = {}
     for cls, pname in enumerate(["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "ce", "embed", "cast", "other",
-                                 "gemm_fwd", "gemm_dx", "gemm_dw", "gemm_lm_head"]):
+                                 "gemm_fwd", "gemm_dx", "gemm_dw", "gemm_lm_head", "opt_ns", "opt_ew", "quant"]):
         t, n, fl, by = ctypes.c_double(), ctypes.c_int64(), ctypes.c_double(), ctypes.c_double()
         lib.nc_profile_read(model.handle, cls, ctypes.byref(t), ctypes.byref(n), ctypes.byref(fl), ctypes.byref(by))
         prof[pname] = {"ms": t.value, "launches": n.value, "flops": fl.value, "bytes": by.value}
@@ -557,7 +558,7 @@ def measure(w, name, args, world, rank, dev, gpu_traffic=True):
 
     g = prof["gemm"]
     gemm_tflops = g["flops"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else None
-    traffic = GEMM_DRAM_BYTES_PER_CALL.get(name) if gpu_traffic else None
+    traffic = GEMM_DRAM_BYTES_PER_CALL.get(name) if (gpu_traffic and not fp8) else None
     roofline = {"kernel": "k_gemm_tc2 / k_gemm_tc (tcgen05 bf16 GEMM, all 5 linear layers fwd + dX + dW)",
                 "bound": "tensor", "achieved": gemm_tflops, "peak": peak_sust, "unit": "TFLOP/s",
                 "frac": (gemm_tflops / peak_sust) if gemm_tflops else None,
@@ -566,7 +567,7 @@ def measure(w, name, args, world, rank, dev, gpu_traffic=True):
                                 "GEMM launches, each at full size, weighted by the step's call counts)",
                 "algorithmic_bytes_per_call": (g["bytes"] / g["launches"]) if g["launches"] else None,
                 "peak_kind": f"bf16 dense, sustained ({peak_src})"}
-    total_prof_ms = sum(v["ms"] for k, v in prof.items() if not k.startswith("gemm_"))
+    total_prof_ms = sum(v["ms"] for k, v in prof.items() if not k.startswith(("gemm_", "opt_")))
     kernels = {k: {"ms_per_step": v["ms"] / args.steps, "share": (v["ms"] / total_prof_ms) if total_prof_ms else None,
                    "launches_per_step": v["launches"] / args.steps,
                    "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["ms"] > 0 and v["flops"] else None,
@@ -590,6 +591,8 @@ def main():
                     help="comma-separated workloads measured after --config and reported under 'other_configs' "
                          "(default: the other bf16 workloads when --config is d26 on one GPU; '' for none)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--fp8-step", type=int, default=None,
+                    help="1: also time the 8-bit step of --config (default: with the extra configs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--step-batch", type=int, default=0,
                     help="profiling only: run the step at this batch size instead of the workload's")
@@ -642,6 +645,12 @@ def main():
     others = {}
     for name in [e for e in extras.split(",") if e]:
         others[name] = measure(S.workload(name), name, args, world, rank, dev)
+    fp8_step = None
+    if (args.fp8_step if args.fp8_step is not None else (extras != "")) and w.dtype == "bf16":
+        fp8_step = measure(w, args.config, args, world, rank, dev, fp8=True)
+        fp8_step["dtype"] = "e4m3 operands in the blocks' forward linears, bf16 elsewhere"
+        fp8_step["note"] = ("the 8-bit training step (nc_config.fp8 = 1), same workload; MFU is quoted against the "
+                            "bf16 peak, and the GEMM roofline mixes 8-bit forward and bf16 backward products")
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -658,6 +667,8 @@ def main():
                 "loss": res["loss"]}
         if others:
             line["other_configs"] = others
+        if fp8_step:
+            line["fp8_step"] = fp8_step
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

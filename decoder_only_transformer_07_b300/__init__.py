@@ -39,7 +39,7 @@ class nc_config(ctypes.Structure):
                 ("mlp_hidden", ctypes.c_int32), ("vocab", ctypes.c_int32), ("seq_len", ctypes.c_int32),
                 ("batch", ctypes.c_int32), ("dtype", ctypes.c_int32), ("rope_base", ctypes.c_float),
                 ("norm_eps", ctypes.c_float), ("init_std", ctypes.c_float), ("logit_softcap", ctypes.c_float),
-                ("embed_norm", ctypes.c_int32)]
+                ("embed_norm", ctypes.c_int32), ("fp8", ctypes.c_int32)]
 
 
 class nc_optim_config(ctypes.Structure):
@@ -146,10 +146,11 @@ def _dtype_code(t):
 
 
 def make_config(depth, n_embd, n_head, n_kv_head, head_dim, mlp_hidden, vocab, seq_len, batch,
-                dtype="bf16", rope_base=10000.0, norm_eps=-1.0, init_std=0.02, logit_softcap=0.0, embed_norm=False):
+                dtype="bf16", rope_base=10000.0, norm_eps=-1.0, init_std=0.02, logit_softcap=0.0, embed_norm=False,
+                fp8=False):
     d = NC_BF16 if dtype in ("bf16", NC_BF16) else NC_FP32
     return nc_config(depth, n_embd, n_head, n_kv_head, head_dim, mlp_hidden, vocab, seq_len, batch, d,
-                     rope_base, norm_eps, init_std, logit_softcap, 1 if embed_norm else 0)
+                     rope_base, norm_eps, init_std, logit_softcap, 1 if embed_norm else 0, 1 if fp8 else 0)
 
 
 def optim_config(**kw):

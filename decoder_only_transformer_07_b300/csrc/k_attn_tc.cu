@@ -31,8 +31,10 @@
 //   TMEM; otherwise P <= 2^8, which bf16 and fp32 hold exactly enough.
 // Backward (deterministic, no atomics), with P recomputed from lse:
 //   dQ kernel    per 128-query tile, over key tiles 0..diagonal:
-//                S = Q K^T (warp 1), dP = dO V^T (warp 2) into TMEM,
-//                dS = P (dP - D) as bf16 into TMEM, dQ += dS K (warp 3);
+//                S = Q K^T (warp 1, double-buffered in TMEM, so S_{j+1} is
+//                computed while the softmax works on step j), dP = dO V^T
+//                (warp 2) into TMEM, dS = P (dP - D) as bf16 over S's
+//                columns, dQ += dS K (warp 3);
 //   dK/dV kernel per 128-key tile, over the group's query heads and the
 //                64-query tiles from the diagonal on: S^T = K Q^T (warp 1),
 //                dP^T = V dO^T (warp 2), double-buffered in TMEM; P^T and dS^T
@@ -339,7 +341,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           tmem_st_wait();
         }
       }
-      // p = 2^(s c - m c): one FFMA and one ex2 per score; 8 partial row sums
+      // p = 2^(s c - m c): one FFMA and one ex2 per score; 8 partial row sums.
+      // (Moving a quarter of the exponentials to an FMA-pipe polynomial measured
+      // 10 % slower: the softmax warps' issue slots, shared with the MMA-issuing
+      // threads, bound this loop rather than the SFU.)
       const float mc = m * sh.scale_log2;
       float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -585,11 +590,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint64_t* k_empty = k_full + NK;    // [NK]
   uint64_t* v_full = k_empty + NK;    // [NV]
   uint64_t* v_empty = v_full + NV;    // [NV]
-  uint64_t* sdp_full = v_empty + NV;  // S and dP in TMEM
-  uint64_t* sdp_free = sdp_full + 1;  // S and dP read (8 warps)
-  uint64_t* ds_full = sdp_free + 1;   // dS in tensor memory (8 warps)
-  uint64_t* ds_free = ds_full + 1;    // dQ += dS K complete
-  uint64_t* dq_done = ds_free + 1;
+  uint64_t* s_full = v_empty + NV;    // [2] S_j in TMEM buffer j & 1
+  uint64_t* dp_full = s_full + 2;     // dP_j in TMEM
+  uint64_t* sdp_free = dp_full + 1;   // S_j and dP_j read (8 warps)
+  uint64_t* ds_full = sdp_free + 1;   // [2] dS_j written over S_j's columns (8 warps)
+  uint64_t* buf_free = ds_full + 2;   // [2] dQ += dS_j K_j complete: buffer j & 1 may take S_{j+2}
+  uint64_t* dq_done = buf_free + 2;
   uint64_t* drain = dq_done + 1;      // [3] one per issuer
   uint32_t* tmem_slot = (uint32_t*)(drain + 3);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
@@ -607,7 +613,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     mbar_init(qd_full, 1);
     for (int s = 0; s < NK; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
     for (int s = 0; s < NV; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
-    mbar_init(sdp_full, 2); mbar_init(sdp_free, 8); mbar_init(ds_full, 8); mbar_init(ds_free, 1);   // S, dP: 2 issuers
+    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&ds_full[i], 8); mbar_init(&buf_free[i], 1); }
+    mbar_init(dp_full, 1); mbar_init(sdp_free, 8);
     mbar_init(dq_done, 1);
     for (int r = 0; r < 3; ++r) mbar_init(&drain[r], 1);
     *abort_flag = 0;
@@ -619,7 +626,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tbase = *tmem_slot;   // S cols 0-127, dP 128-255, dQ 256.., dS (bf16 pairs) 384-447
+  // S_j in buffer j & 1 (columns 0-127 or 128-255), dP 256-383, dQ 384.. .  The
+  // softmax warp of half hf reads S columns [64 hf, 64 hf + 64) of its buffer and
+  // writes dS_j there as 32 bf16-pair columns, [64 hf, 64 hf + 32); dQ += dS_j K_j
+  // reads them.  S_{j+2} overwrites the buffer only after buf_free signals that
+  // dQ_j completed (the S issuer waits for it), so a buffer is written by the
+  // tensor core only when no product reads it and by the softmax warps only
+  // between S_j's completion and S_{j+2}'s issue.
+  const uint32_t tbase = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
     mbar_arrive_expect_tx(qd_full, 2 * L::TILE);
@@ -654,40 +668,50 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
   } else if ((warp == 1 || warp == 2 || warp == 3) && lane == 0) {
     // ---------------- three MMA issuers (one thread issues about one MMA per ~100
-    // cycles): warp 1 S = Q K^T, warp 2 dP = dO V^T, warp 3 dQ += dS K (one
-    // accumulator, one issuer).  S_{j+1} / dP_{j+1} overlap the softmax of step j
-    // and dQ_j overlaps S_{j+2} / dP_{j+2}.
+    // cycles): warp 1 S_j = Q K_j^T into buffer j & 1, up to two steps ahead of the
+    // softmax; warp 2 dP_j = dO V_j^T, once the softmax has read dP_{j-1}; warp 3
+    // dQ += dS_j K_j.
     const int role = warp - 1;
     const uint32_t id_s = at_idesc(128, 0), id_q = at_idesc(HD, 1);
     const uint32_t sq = smem_u32(smem + L::OFF_Q), sdo = smem_u32(smem + L::OFF_DO);
     const uint32_t sk = smem_u32(smem + L::OFF_K), sv = smem_u32(smem + L::OFF_V);
     bool ok = at_wait(qd_full, 0, sh, abort_flag);
-    if (role < 2) {
-      for (int j = 0; ok && j < n; ++j) {   // role 0: S_j; role 1: dP_j
-        if (role == 0 ? !(ok = at_wait(&k_full[j % NK], (j / NK) & 1, sh, abort_flag))
-                      : !(ok = at_wait(&v_full[j % NV], (j / NV) & 1, sh, abort_flag)))
-          break;
-        if (j > 0 && !(ok = at_wait(sdp_free, (j - 1) & 1, sh, abort_flag))) break;
+    if (role == 0) {
+      for (int j = 0; ok && j < n; ++j) {
+        if (!(ok = at_wait(&k_full[j % NK], (j / NK) & 1, sh, abort_flag))) break;
+        if (j >= 2 && !(ok = at_wait(&buf_free[j & 1], ((j - 2) >> 1) & 1, sh, abort_flag))) break;
         tc_fence_after();
-        const uint32_t a = role ? sdo : sq;
-        const uint32_t b = role ? sv + (j % NV) * L::TILE : sk + (j % NK) * L::TILE;
+        const uint32_t kb = sk + (j % NK) * L::TILE;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          tc_mma_f16(tbase + role * 128, kdesc(a, kk, CHUNK128), kdesc(b, kk, CHUNK128), id_s, kk > 0 ? 1u : 0u);
-        tc_commit(sdp_full);
-        if (role) tc_commit(&v_empty[j % NV]);
+          tc_mma_f16(tbase + (j & 1) * 128, kdesc(sq, kk, CHUNK128), kdesc(kb, kk, CHUNK128), id_s, kk > 0 ? 1u : 0u);
+        tc_commit(&s_full[j & 1]);
+        if (*abort_flag) ok = false;
+      }
+    } else if (role == 1) {
+      for (int j = 0; ok && j < n; ++j) {
+        if (!(ok = at_wait(&v_full[j % NV], (j / NV) & 1, sh, abort_flag))) break;
+        if (j > 0 && !(ok = at_wait(sdp_free, (j - 1) & 1, sh, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t vb = sv + (j % NV) * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          tc_mma_f16(tbase + 256, kdesc(sdo, kk, CHUNK128), kdesc(vb, kk, CHUNK128), id_s, kk > 0 ? 1u : 0u);
+        tc_commit(dp_full);
+        tc_commit(&v_empty[j % NV]);
         if (*abort_flag) ok = false;
       }
     } else {
       for (int j = 0; ok && j < n; ++j) {   // dQ += dS_j K_j, dS from tensor memory
-        if (!(ok = at_wait(ds_full, j & 1, sh, abort_flag))) break;
+        if (!(ok = at_wait(&ds_full[j & 1], (j >> 1) & 1, sh, abort_flag))) break;
         tc_fence_after();
         const uint32_t kb = sk + (j % NK) * L::TILE;
+        const uint32_t ds = tbase + (j & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16_ts(tbase + 256, tbase + 384 + 8 * kk, mndesc(kb, kk, CHUNK128), id_q,
+        for (int kk = 0; kk < 8; ++kk)   // keys [16 kk, 16 kk + 16): half kk / 4, pair column 8 (kk % 4)
+          tc_mma_f16_ts(tbase + 384, ds + 64 * (kk >> 2) + 8 * (kk & 3), mndesc(kb, kk, CHUNK128), id_q,
                         (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(ds_free);
+        tc_commit(&buf_free[j & 1]);
         tc_commit(&k_empty[j % NK]);
         if (*abort_flag) ok = false;
       }
@@ -700,15 +724,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int r = quarter * 32 + lane;
     const int qpos = qt * 128 + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tbase + lane_off + 64 * hf, tP = tS + 128;
-    const uint32_t tDS = tbase + lane_off + 384 + 32 * hf;   // this half's 64 keys as 32 bf16 pairs
+    const uint32_t tP = tbase + lane_off + 256 + 64 * hf;
     const bool valid = qpos < sh.T;
     const float lse2 = valid ? lse[(int64_t)bh * sh.T + qpos] * LOG2E : INFINITY;
     const float Dr = valid ? Dv[(int64_t)bh * sh.T + qpos] : 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      if (!(ok = at_wait_warp(sdp_full, j & 1, sh, abort_flag))) break;
+      if (!(ok = at_wait_warp(&s_full[j & 1], (j >> 1) & 1, sh, abort_flag))) break;
+      if (!(ok = at_wait_warp(dp_full, j & 1, sh, abort_flag))) break;
       tc_fence_after();
+      const uint32_t tS = tbase + lane_off + (j & 1) * 128 + 64 * hf;
       uint32_t s[64], dp[64];
       tmem_ld_32x32b_x32(tS, s);
       tmem_ld_32x32b_x32(tS + 32, s + 32);
@@ -726,26 +751,23 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         if (diag && (k0 + c > qpos || k0 + c >= sh.T)) p = 0.f;
         s[c] = __float_as_uint(p * (__uint_as_float(dp[c]) - Dr));
       }
-      if (j > 0) {
-        if (!(ok = at_wait_warp(ds_free, (j - 1) & 1, sh, abort_flag))) break;
-      }
 #pragma unroll
       for (int c = 0; c < 32; ++c) s[c] = pack2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
-      tmem_st_32x32b_x32(tDS, s);
+      tmem_st_32x32b_x32(tS, s);            // dS_j over the S columns this warp read
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
+      if (lane == 0) mbar_arrive(&ds_full[j & 1]);
     }
     if (ok && at_wait_warp(dq_done, 0, sh, abort_flag)) {
       tc_fence_after();
       if (HD == 128 && !sh.rope_tab) {
         // staged in the K ring, free once every dQ product has completed
-        at_out_box128(tbase + lane_off + 256, hf, sh.scale, smem + L::OFF_K + (hf * 4 + quarter) * 4096, &tm_out,
+        at_out_box128(tbase + lane_off + 384, hf, sh.scale, smem + L::OFF_K + (hf * 4 + quarter) * 4096, &tm_out,
                       h * HD + hf * 64, qt * 128 + quarter * 32, b, sh.T);
         if (lane == 0) bulk_wait_all();
       } else {
-        at_out_tile<HD>(sh, tbase + lane_off + 256, smem + L::OFF_Q, r, hf, valid, qpos, (int64_t)row0 + qpos, h,
+        at_out_tile<HD>(sh, tbase + lane_off + 384, smem + L::OFF_Q, r, hf, valid, qpos, (int64_t)row0 + qpos, h,
                         dqkv + (int64_t)(row0 + qpos) * sh.ld_qkv + (int64_t)h * HD);
       }
     }

@@ -369,9 +369,11 @@ __device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, int ep, co
 // NC_EP_QKV_ROPE through the staging box: per head of the warp's columns,
 // q/k heads get rstd from the fp32 accumulator (the rotation keeps the sum of
 // squares) and the rotated, scaled values; v heads are stored as computed.
+// The projection output is alpha * accumulator (alpha = 1 for bf16 operands,
+// the two dequantisation factors for 8-bit ones; multiplying by 1 is exact).
 __device__ __forceinline__ void tc_epilogue_qkv_rope_staged(const TcParams& p, const CUtensorMap* tmD, uint8_t* stg,
                                                             uint32_t tcol0, int n_base, int ncols, int m0,
-                                                            int64_t m, int lane) {
+                                                            int64_t m, int lane, float alpha) {
   const int hd = p.rope_hd, d = hd >> 1;
   const uint32_t sa = smem_u32(stg);
   const int r = lane;
@@ -398,7 +400,10 @@ __device__ __forceinline__ void tc_epilogue_qkv_rope_staged(const TcParams& p, c
         tmem_ld_32x32b_x32(tc + c, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) ss += __uint_as_float(v[e]) * __uint_as_float(v[e]);
+        for (int e = 0; e < 32; ++e) {
+          const float u = __uint_as_float(v[e]) * alpha;
+          ss += u * u;
+        }
       }
       rs = rsqrtf(ss / (float)hd + p.rope_eps);
     }
@@ -414,7 +419,7 @@ __device__ __forceinline__ void tc_epilogue_qkv_rope_staged(const TcParams& p, c
           tmem_ld_32x32b_x32(tc + pc, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) y[e] = __uint_as_float(v[e]);
+          for (int e = 0; e < 32; ++e) y[e] = __uint_as_float(v[e]) * alpha;
         } else {
           // first half: y_i = (u_i cos + u_{i+d} sin) rs; second: y_{i+d} = (-u_i sin + u_{i+d} cos) rs
           const bool first = pc < d;
@@ -426,8 +431,8 @@ __device__ __forceinline__ void tc_epilogue_qkv_rope_staged(const TcParams& p, c
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float4 q = __ldg(cs + ((i0 + e) >> 1) * cs_step);   // cos_i, sin_i, cos_i+1, sin_i+1
-            const float a0 = __uint_as_float(a[e]), a1 = __uint_as_float(a[e + 1]);
-            const float b0 = __uint_as_float(b[e]), b1 = __uint_as_float(b[e + 1]);
+            const float a0 = __uint_as_float(a[e]) * alpha, a1 = __uint_as_float(a[e + 1]) * alpha;
+            const float b0 = __uint_as_float(b[e]) * alpha, b1 = __uint_as_float(b[e + 1]) * alpha;
             y[e] = (first ? (a0 * q.x + b0 * q.y) : (-a0 * q.y + b0 * q.x)) * rs;
             y[e + 1] = (first ? (a1 * q.z + b1 * q.w) : (-a1 * q.w + b1 * q.z)) * rs;
           }
@@ -600,7 +605,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (m0 >= p.M && (p.ep == NC_EP_QKV_ROPE || (p.tma_epi && !part))) {
         // all 32 rows of this warp are past the end: nothing to store
       } else if (p.ep == NC_EP_QKV_ROPE) {
-        tc_epilogue_qkv_rope_staged(p, &tmD, stg, taddr + c_lo, tn * BN + c_lo, BN / 2, m0, m, lane);
+        tc_epilogue_qkv_rope_staged(p, &tmD, stg, taddr + c_lo, tn * BN + c_lo, BN / 2, m0, m, lane,
+                                    F8 ? __ldg(p.scale_a) * __ldg(p.scale_b) : 1.f);
       } else if (p.tma_epi && !part) {
         if (!tc_epilogue_staged<BN, F8>(p, p.ep, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
                                         tn * BN + c_lo, p.N, m0, lane)) {
@@ -836,7 +842,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           break;
         }
       } else if (p.ep == NC_EP_QKV_ROPE) {
-        tc_epilogue_qkv_rope_staged(p, &tmD, stg, taddr + c_lo, tn * BN + c_lo, BN / 2, m0, m, lane);
+        tc_epilogue_qkv_rope_staged(p, &tmD, stg, taddr + c_lo, tn * BN + c_lo, BN / 2, m0, m, lane,
+                                    F8 ? __ldg(p.scale_a) * __ldg(p.scale_b) : 1.f);
       } else if (p.tma_epi) {
         if (!tc_epilogue_staged<BN, F8>(p, p.ep, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
                                         tn * BN + c_lo, p.N, m0, lane)) {
@@ -1154,16 +1161,23 @@ nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_
 }
 
 // E4M3 GEMM: D[M,N] = (*scale_a) (*scale_b) A8 B8^T, both operands K-major
-// bytes ([M][lda], [N][ldb]), fp32 accumulation; D bf16 or fp32 (row pitch ldd)
-// through the TMA-staged epilogue.  CTA pairs (256 x 256 tiles) when N > 128
-// and M >= 256, the single-CTA kernel otherwise; no split-K.
-nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
-                          const float* scale_a, const float* scale_b, int out_f32, void* D, int64_t ldd,
-                          int32_t* err, cudaStream_t st) {
+// bytes ([M][lda], [N][ldb]), fp32 accumulation, through the TMA-staged
+// epilogue `ep`: NC_EP_STORE (bf16 D), NC_EP_STORE_F32, NC_EP_ACCUM_F32 (fp32
+// D += ...), NC_EP_RELU2_SQ (bf16 relu(.)^2) or NC_EP_QKV_ROPE (with `rope`,
+// bf16 D).  CTA pairs (256 x 256 tiles) when N > 128 and M >= 256, the
+// single-CTA kernel otherwise; no split-K.
+static nc_status gemm_fp8_impl(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
+                               const float* scale_a, const float* scale_b, int ep, void* D, int64_t ldd,
+                               const TcRope* rope, int32_t* err, cudaStream_t st) {
   if (M <= 0 || N <= 0) return NC_OK;
   if (K <= 0 || !A || !B || !D || !scale_a || !scale_b) return NC_ERR_ARG;
   if ((lda % 16) || (ldb % 16) || lda < K || ldb < K || (((uintptr_t)A) & 15) || (((uintptr_t)B) & 15))
     return NC_ERR_ARG;
+  if (ep != NC_EP_STORE && ep != NC_EP_STORE_F32 && ep != NC_EP_ACCUM_F32 && ep != NC_EP_RELU2_SQ &&
+      ep != NC_EP_QKV_ROPE)
+    return NC_ERR_ARG;
+  if ((ep == NC_EP_QKV_ROPE) != (rope != nullptr)) return NC_ERR_ARG;
+  const bool out_f32 = (ep == NC_EP_STORE_F32 || ep == NC_EP_ACCUM_F32);
   if (ldd < N || ((ldd * (out_f32 ? 4 : 2)) % 16) || (((uintptr_t)D) & 15)) return NC_ERR_ARG;
   if (!g_num_sms) {
     int dev = 0;
@@ -1176,7 +1190,7 @@ nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, co
   memset(&p, 0, sizeof(p));
   p.M = M; p.N = N; p.K = K;
   p.a_mn = 0; p.b_mn = 0;
-  p.ep = out_f32 ? NC_EP_STORE_F32 : NC_EP_STORE;
+  p.ep = ep;
   p.D = D; p.ldd = ldd;
   p.tiles_m = pair ? (M + 255) / 256 : (M + TC_BM - 1) / TC_BM;
   p.tiles_n = (N + BN - 1) / BN;
@@ -1187,6 +1201,14 @@ nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, co
   p.splits = 1;
   p.rope_T = 1;
   p.scale_a = scale_a; p.scale_b = scale_b;
+  if (rope) {
+    if (BN != 256 || (rope->hd != 64 && rope->hd != 128) || (N % rope->hd) || rope->nh * rope->hd > N ||
+        rope->T <= 0 || (((uintptr_t)rope->tab) & 15) || !rope->rstd)
+      return NC_ERR_ARG;
+    if (rope->pair_rows < 0 || (rope->pair_rows > 0 && rope->pair_rows < rope->T)) return NC_ERR_ARG;
+    p.rope_tab = rope->tab; p.rstd_qk = rope->rstd; p.rope_T = rope->T; p.rope_nh = rope->nh;
+    p.rope_hd = rope->hd; p.rope_pair_rows = rope->pair_rows; p.rope_eps = rope->eps;
+  }
   // 128-byte (128-element) K boxes; rows 128 (A), BN or 128 per CTA of a pair (B)
   CUtensorMap ta, tb, td, tx;
   memset(&tx, 0, sizeof(tx));
@@ -1198,6 +1220,23 @@ nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, co
   if (pair) return launch_tc_pair<true>(p, ta, tb, td, tx, 0, st);
   if (BN == 256) return launch_tc_bn<256, true>(p, ta, tb, td, tx, 0, st);
   return launch_tc_bn<128, true>(p, ta, tb, td, tx, 0, st);
+}
+
+nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
+                          const float* scale_a, const float* scale_b, int out_f32, void* D, int64_t ldd,
+                          int32_t* err, cudaStream_t st) {
+  return gemm_fp8_impl(M, N, K, A, lda, B, ldb, scale_a, scale_b, out_f32 ? NC_EP_STORE_F32 : NC_EP_STORE, D, ldd,
+                       nullptr, err, st);
+}
+
+nc_status launch_gemm_fp8_ep(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
+                             const float* scale_a, const float* scale_b, int ep, void* D, int64_t ldd, int T, int nh,
+                             int hd, const float* tab, int pair_rows, float* rstd, float eps, int32_t* err,
+                             cudaStream_t st) {
+  if (ep != NC_EP_QKV_ROPE)
+    return gemm_fp8_impl(M, N, K, A, lda, B, ldb, scale_a, scale_b, ep, D, ldd, nullptr, err, st);
+  TcRope r{tab, rstd, T, nh, hd, pair_rows, eps};
+  return gemm_fp8_impl(M, N, K, A, lda, B, ldb, scale_a, scale_b, ep, D, ldd, &r, err, st);
 }
 
 nc_status launch_gemm_tc_qkv_rope(int M, int N, int K, const bf16* A, int64_t lda, const bf16* Wqkv, int64_t ldb,

@@ -40,6 +40,10 @@ struct nc_model {
   float softcap = 0.f;               // logit soft-cap c (0: off)
   bool emb_norm = false;             // RMSNorm after the embedding lookup
   float* rstd_e = nullptr;           // [Nmax] its per-row rstd (emb_norm only)
+  bool fp8 = false;                  // the blocks' forward linears on E4M3 operands
+  uint8_t* q8a = nullptr;            // E4M3 codes of a linear layer's input [Nmax, max(C, F)]
+  uint8_t* q8w = nullptr;            // E4M3 codes of its weight (the largest block weight)
+  float* q8s = nullptr;              // {amax, scale, scale_inv} of the activation [0..3), weight [4..7)
   int32_t* err = nullptr;            // device error flag
   float* result = nullptr;           // device: [0] loss, [1] error flag copy
   float* result_host = nullptr;      // pinned host copy
@@ -250,6 +254,8 @@ static nc_status validate(const nc_config* c, nc_config* out) {
   if (k.n_embd > 8192) return NC_ERR_CONFIG;
   if (!(k.logit_softcap >= 0.f) || k.logit_softcap == INFINITY) return NC_ERR_CONFIG;
   if (k.embed_norm != 0 && k.embed_norm != 1) return NC_ERR_CONFIG;
+  if (k.fp8 != 0 && k.fp8 != 1) return NC_ERR_CONFIG;
+  if (k.fp8 && (k.dtype != NC_BF16 || k.n_embd % 16 || k.mlp_hidden % 16)) return NC_ERR_CONFIG;
   if ((int64_t)k.batch * k.seq_len > (1 << 20)) return NC_ERR_CONFIG;
   *out = k;
   return NC_OK;
@@ -299,6 +305,13 @@ static nc_status allocate(nc_model* m) {
   NC_TRY(dalloc_t(m, (size_t)L * N * m->H, &m->lse));
   NC_TRY(dalloc(m, (size_t)N * m->C * a, &m->xf));
   if (m->emb_norm) NC_TRY(dalloc_t(m, (size_t)N, &m->rstd_e));
+  if (m->fp8) {
+    const int64_t kmax = std::max<int64_t>(m->C, m->F);
+    const int64_t wmax = std::max<int64_t>((int64_t)m->qkvw, 2 * (int64_t)m->F) * m->C;
+    NC_TRY(dalloc(m, (size_t)(N * kmax), (void**)&m->q8a));
+    NC_TRY(dalloc(m, (size_t)wmax, (void**)&m->q8w));
+    NC_TRY(dalloc_t(m, 8, &m->q8s));
+  }
   NC_TRY(dalloc_t(m, (size_t)N, &m->rstd_f));
   // logits chunk: at most 1 GiB of compute-dtype logits per chunk, whole 128-row tiles
   int64_t rows = ((int64_t)1 << 30) / ((int64_t)m->V * (int64_t)a);
@@ -378,6 +391,7 @@ extern "C" nc_status nc_model_create(const nc_config* cfg, uint64_t seed, nc_mod
   m->Nmax = (int64_t)c.batch * c.seq_len;
   m->softcap = c.logit_softcap;
   m->emb_norm = c.embed_norm != 0;
+  m->fp8 = c.fp8 != 0;
   build_layout(m);
   nc_status s = allocate(m);
   cudaStream_t st = 0;
@@ -482,6 +496,22 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
   const int nh = m->H + m->Hkv;
   const double attn_fl = 4.0 * B * m->H * m->hd * ((double)T * (T + 1) / 2.0);
   const double nrm_by = (double)N * (4.0 * C + a * C + 4);
+  // The 8-bit step's linear layer: quantise the bf16 input [N, K] and the fp32
+  // master weight [Nout, K] (per tensor, current scaling), then the E4M3 GEMM
+  // through the layer's epilogue (RoPE + QK-norm with rope, else `ep`).
+  auto lin8 = [&](const void* act_in, int K, const ParamTensor& w, int Nout, int ep, void* D, int64_t ldd,
+                  float* rstdqk) -> nc_status {
+    PROF(NC_PROF_QUANT, 0, 5.0 * N * K, launch_quantize_fp8(NC_BF16, act_in, N * K, m->q8a, m->q8s, st));
+    PROF(NC_PROF_QUANT, 0, 9.0 * Nout * K,
+         launch_quantize_fp8(NC_FP32, m->master + w.off, (int64_t)Nout * K, m->q8w, m->q8s + 4, st));
+    const double out = ep == NC_EP_ACCUM_F32 ? 8.0 : 2.0;
+    PROF_SUB(NC_PROF_GEMM, NC_PROF_GEMM_FWD, 2.0 * N * Nout * K, (double)N * K + (double)Nout * K + (double)N * Nout * out,
+             launch_gemm_fp8_ep((int)N, Nout, K, m->q8a, K, m->q8w, K, m->q8s + 2, m->q8s + 6, ep, D, ldd, T, nh,
+                                m->hd, m->rope_pairs ? m->rope_pairs : m->rope_tab, m->rope_pairs ? m->Tmax : 0,
+                                rstdqk, eps, m->err, st));
+    m->launches += 7;
+    return NC_OK;
+  };
   for (int l = 0; l < m->L; ++l) {
     uint8_t* xn1 = layer_act(m, m->xn1, l, C);
     uint8_t* xn2 = layer_act(m, m->xn2, l, C);
@@ -493,6 +523,17 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
     float* rstdqk = m->rstdqk + (size_t)l * m->Nmax * (m->H + m->Hkv);
     float* lse = m->lse + (size_t)l * m->Nmax * m->H;
     PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn1, rstd1, eps, st));
+    if (m->fp8) {
+      NC_TRY(lin8(xn1, C, tensor(m, l, 0), W, NC_EP_QKV_ROPE, qkv, W, rstdqk));
+      PROF(NC_PROF_ATTN_FWD, attn_fl, (double)N * (W + Hd) * a + 4.0 * N * m->H,
+           attn_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->err, st));
+      NC_TRY(lin8(o, Hd, tensor(m, l, 3), C, NC_EP_ACCUM_F32, m->x, C, nullptr));
+      PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn2, rstd2, eps, st));
+      NC_TRY(lin8(xn2, C, tensor(m, l, 4), F, NC_EP_RELU2_SQ, h, F, nullptr));
+      NC_TRY(lin8(h, F, tensor(m, l, 5), C, NC_EP_ACCUM_F32, m->x, C, nullptr));
+      m->launches += 3;
+      continue;
+    }
     if (m->dtype == NC_BF16) {
       // q/k/v projection with RoPE and the q/k RMSNorm in the GEMM epilogue
       PROF_SUB(NC_PROF_GEMM, NC_PROF_GEMM_FWD, 2.0 * N * W * C, ((double)N * C + (double)W * C + (double)N * W) * a,
@@ -1071,6 +1112,7 @@ extern "C" nc_status nc_kv_cache_create(nc_model* m, int32_t max_batch, int32_t 
   if ((m->hd != 64 && m->hd != 128) || (m->H / m->Hkv != 1 && m->H / m->Hkv != 2 && m->H / m->Hkv != 3 &&
                                         m->H / m->Hkv != 4 && m->H / m->Hkv != 8))
     return NC_ERR_UNSUPPORTED;
+  if (m->fp8) return NC_ERR_UNSUPPORTED;   // decode steps have no 8-bit projections
   NC_TRY(decode_kernels_prepare());
   if (m->kcache && max_batch <= m->kv_b && max_len <= m->kv_max) {
     m->kv_batch = m->kv_len = 0;

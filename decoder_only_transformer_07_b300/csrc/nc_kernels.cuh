@@ -75,6 +75,13 @@ nc_status launch_gemm_tc_qkv_rope(int M, int N, int K, const bf16* A, int64_t ld
 nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
                           const float* scale_a, const float* scale_b, int out_f32, void* D, int64_t ldd,
                           int32_t* err, cudaStream_t st);
+// The 8-bit GEMM through a step epilogue: NC_EP_STORE, NC_EP_STORE_F32,
+// NC_EP_ACCUM_F32, NC_EP_RELU2_SQ, or NC_EP_QKV_ROPE (then T, nh, hd, tab,
+// pair_rows, rstd and eps as for launch_gemm_tc_qkv_rope; ignored otherwise).
+nc_status launch_gemm_fp8_ep(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
+                             const float* scale_a, const float* scale_b, int ep, void* D, int64_t ldd, int T, int nh,
+                             int hd, const float* tab, int pair_rows, float* rstd, float eps, int32_t* err,
+                             cudaStream_t st);
 // Per-tensor E4M3 quantisation of n fp32 / bf16 values: stats (device, 3
 // floats) gets {amax, scale, scale_inv}; y the codes.
 nc_status launch_quantize_fp8(int dtype, const void* x, int64_t n, uint8_t* y, float* stats, cudaStream_t st);

@@ -63,6 +63,17 @@ typedef struct {
                           outputs; must be finite and >= 0                   */
   int32_t embed_norm;  /* 1: RMSNorm (no gain, eps = norm_eps) of each
                           embedding row before the first block; 0 or 1       */
+  /* The 8-bit training step (woshipm nanochat analysis §一.2 and §六.2 name
+   * FP8 as a speed lever without a recipe): 1 makes every block's four
+   * linear layers (q/k/v, output projection, MLP up and down) multiply E4M3
+   * operands in the forward: the bf16 input activation and the fp32 master
+   * weight are each quantised per tensor with current scaling (the
+   * nc_op_quantize_fp8 rule; [Wq; Wk; Wv] is one tensor), products
+   * accumulate in fp32 and are dequantised in the fused epilogues.  The
+   * backward is the bf16 one with the unquantised operands (the quantisers
+   * pass gradients through unchanged).  NC_BF16 only; n_embd and mlp_hidden
+   * multiples of 16; decoding (nc_kv_cache_create) is not offered.  0: off.  */
+  int32_t fp8;
 } nc_config;
 
 typedef struct nc_model nc_model;
@@ -352,7 +363,9 @@ enum { NC_PROF_GEMM = 0, NC_PROF_ATTN_FWD = 1, NC_PROF_ATTN_BWD = 2, NC_PROF_NOR
           applies (concurrent on side streams, timed as one phase), and the
           elementwise kernels (momentum and norms, scaling, AdamW) */
        NC_PROF_OPT_NS = 13, NC_PROF_OPT_EW = 14,
-       NC_PROF_CLASSES = 15 };
+       /* the 8-bit step's quantisation of GEMM operands (fp8 = 1) */
+       NC_PROF_QUANT = 15,
+       NC_PROF_CLASSES = 16 };
 nc_status nc_profile_enable(nc_model* m, int32_t on);
 nc_status nc_profile_read(nc_model* m, int32_t cls, double* ms, int64_t* launches,
                           double* flops, double* bytes);
@@ -467,7 +480,7 @@ nc_status nc_op_newton_schulz(int32_t dtype, int32_t rows, int32_t cols, int32_t
 /* Allocate (or reuse, if large enough) the cache for max_batch sequences of
  * max_len positions and empty it.  1 <= max_batch <= cfg.batch,
  * 1 <= max_len <= cfg.seq_len; NC_ERR_UNSUPPORTED unless hd is 64 or 128 and
- * n_head / n_kv_head is 1, 2, 3, 4 or 8. */
+ * n_head / n_kv_head is 1, 2, 3, 4 or 8, and for an 8-bit model (cfg.fp8). */
 nc_status nc_kv_cache_create(nc_model* m, int32_t max_batch, int32_t max_len);
 /* tokens_dev: int32 [B, T]; logits_dev: fp32 [B, V] (device).  Replaces the
  * cache contents; B <= max_batch, T <= max_len.  Does not synchronise. */

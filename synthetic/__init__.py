@@ -108,3 +108,13 @@ def fp8_codes(rows, cols, seed=FP8_SEED):
     mag = rng.integers(0x20, 0x60, size=(rows, cols), dtype=np.uint8)
     sign = rng.integers(0, 2, size=(rows, cols), dtype=np.uint8) << 7
     return mag | sign
+
+
+def fp8_codes_all(rows, cols, seed=FP8_SEED):
+    """Random E4M3 byte codes drawn uniformly from every finite code: the
+    subnormals (exponent field 0), the zeros, and the largest magnitude 448
+    (0x7e / 0xfe) included; only the two NaN codes 0x7f / 0xff are left out."""
+    rng = np.random.default_rng(seed)
+    c = rng.integers(0, 254, size=(rows, cols), dtype=np.int64)
+    c = c + (c >= 0x7f)                   # skip 0x7f: 0..0x7e, 0x80..0xfe
+    return c.astype(np.uint8)

@@ -85,6 +85,29 @@ def test_gemm_fp8_matches_oracle(M, N, K, out):
     _check_gemm(D, a, b, sa, sb)
 
 
+@pytest.mark.parametrize("out", ["fp32", "bf16"])
+def test_gemm_fp8_every_finite_code(out):
+    """Operands over every finite E4M3 code, with rows of subnormals only and
+    rows and columns of the saturated magnitude 448 (the quantiser's code for
+    amax), on CTA pairs with ragged tails."""
+    M, N, K = 384, 320, 512
+    a = S.fp8_codes_all(M, K, seed=21)
+    b = S.fp8_codes_all(N, K, seed=22)
+    a[5] = np.where(np.arange(K) % 2, 0x7E, 0xFE)          # +-448
+    b[7] = 0x7E
+    a[9] = (np.arange(K) % 7 + 1).astype(np.uint8)         # subnormals 2^-9 .. 7 * 2^-9
+    b[11] = (np.arange(K) % 7 + 0x81).astype(np.uint8)     # negative subnormals
+    assert np.all(np.isin(np.arange(256)[(np.arange(256) != 0x7F) & (np.arange(256) != 0xFF)], a))
+    sa, sb = np.float32(2.0 ** -7), np.float32(0.0371)
+    sc = torch.tensor([sa, sb], dtype=torch.float32, device="cuda")
+    D = torch.empty((M, N), dtype=torch.float32 if out == "fp32" else torch.bfloat16, device="cuda")
+    nc.ops.gemm_fp8(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), sc[0:1], sc[1:2], D)
+    _check_gemm(D, a, b, sa, sb)
+    if out == "fp32":
+        # 448 * 448 * K products of equal sign are exact in fp32: D(5, 7) is their alternating sum, 0
+        assert float(D[5, 7]) == 0.0
+
+
 def test_gemm_fp8_row_pitch_and_unaligned_k():
     """K = 40 inside rows of 48 bytes: the tail of each K block is read as zeros."""
     M, N, K = 260, 300, 40
