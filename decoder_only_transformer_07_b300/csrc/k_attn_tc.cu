@@ -14,8 +14,7 @@
 //   warps 1-3   MMA issuers (one thread each issues tcgen05.mma / tcgen05.commit;
 //               a single thread issues only about one MMA per ~100 cycles, so
 //               independent product chains get their own issuer); warp 2 also
-//               allocates and frees the 512 TMEM columns; in the dK/dV kernel
-//               warp 3 stages lse and D instead
+//               allocates and frees the 512 TMEM columns
 //   warps 4-11  "softmax" warps: each thread owns one TMEM lane = one row of
 //               the score tile, so row reductions need no shuffles.
 //
@@ -38,8 +37,8 @@
 //   dK/dV kernel per 128-key tile, over the group's query heads and the
 //                64-query tiles from the diagonal on: S^T = K Q^T (warp 1),
 //                dP^T = V dO^T (warp 2), double-buffered in TMEM; P^T and dS^T
-//                as bf16 over their own product's columns; dV += P^T dO
-//                (warp 1), dK += dS^T Q (warp 2).
+//                as bf16 over their own product's columns; dV += P^T dO and
+//                dK += dS^T Q (warp 3).
 // The 1/sqrt(hd) of dQ and dK is applied to the fp32 accumulators on output.
 // A TMEM region is only ever overwritten by the issuer whose earlier product
 // reads it, or by softmax warps after a barrier that follows that read.
@@ -787,8 +786,8 @@ struct DkvSmem {
   static constexpr uint32_t OFF_V = KT;
   static constexpr int NS = 4;
   static constexpr uint32_t OFF_QS = 2 * KT;                // NS stages of {Q, dO}
-  static constexpr uint32_t OFF_LD = OFF_QS + NS * 2 * QT;  // NS stages of {lse*log2e[64], D[64]}
-  static constexpr uint32_t OFF_BAR = OFF_LD + NS * 128 * 4;
+  static constexpr uint32_t OFF_LD = OFF_QS + NS * 2 * QT;  // per softmax warp {lse*log2e[32], D[32]}
+  static constexpr uint32_t OFF_BAR = OFF_LD + 8 * 64 * 4;
   static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
 };
 
@@ -804,16 +803,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint64_t* bar = (uint64_t*)(smem + L::OFF_BAR);
   constexpr int NS = L::NS;
   uint64_t* kv_full = bar;              // [1]
-  uint64_t* q_full = bar + 1;           // [NS] TMA bytes + 32 loader lanes
-  uint64_t* q_empty = q_full + NS;      // [NS]
-  uint64_t* st_full = q_empty + NS;     // [2] S^T, dP^T in TMEM buffer
-  uint64_t* st_free = st_full + 2;      // [2] buffer read (8 warps)
-  uint64_t* pt_full = st_free + 2;      // P^T, dS^T in TMEM (8 warps)
-  uint64_t* dkv_done = pt_full + 1;     // both issuers' products complete
-  uint64_t* drain = dkv_done + 1;       // [2] one per issuer
-  uint32_t* tmem_slot = (uint32_t*)(drain + 2);
+  uint64_t* q_full = bar + 1;           // [NS] TMA bytes of {Q, dO}
+  uint64_t* q_empty = q_full + NS;      // [NS] step's dV and dK products complete
+  uint64_t* st_full = q_empty + NS;     // [2] S^T and dP^T in TMEM buffer (two issuers)
+  uint64_t* pt_full = st_full + 2;      // [2] P^T, dS^T in that buffer (8 warps)
+  uint64_t* buf_free = pt_full + 2;     // [2] dV, dK of the buffer's step complete: it may take step i+2
+  uint64_t* dkv_done = buf_free + 2;    // every product complete
+  uint64_t* drain = dkv_done + 1;       // [3] one per issuer
+  uint32_t* tmem_slot = (uint32_t*)(drain + 3);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-  float* LD = (float*)(smem + L::OFF_LD);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntk = (sh.T + 127) >> 7;
@@ -829,10 +827,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    // stages are released, buffers filled and the step finished by both issuers
-    for (int s = 0; s < NS; ++s) { mbar_init(&q_full[s], 33); mbar_init(&q_empty[s], 2); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&st_full[i], 2); mbar_init(&st_free[i], 8); mbar_init(&drain[i], 1); }
-    mbar_init(pt_full, 8); mbar_init(dkv_done, 2);
+    for (int s = 0; s < NS; ++s) { mbar_init(&q_full[s], 1); mbar_init(&q_empty[s], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&st_full[i], 2); mbar_init(&pt_full[i], 8); mbar_init(&buf_free[i], 1); }
+    mbar_init(dkv_done, 1);
+    for (int r = 0; r < 3; ++r) mbar_init(&drain[r], 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_kv);
@@ -846,11 +844,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   // S^T[2] cols 0,64; dP^T[2] 128,192; dV 256..; dK 256+HD.  Warp half hf reads
   // columns [32 hf, 32 hf + 32) of S^T[buf] and of dP^T[buf] and overwrites the
   // first 16 of them with P^T and dS^T respectively, bf16 pairs of its 32
-  // queries.  Each product buffer is thus only ever written by the issuer that
-  // reads it back (warp 1: S^T, then dV += P^T dO; warp 2: dP^T, then dK +=
-  // dS^T Q), and in-order execution per issuer orders that read before the
-  // buffer's next S^T / dP^T.  (Were dS^T kept in the S^T columns, warp 1's
-  // S^T of step i+2 could overwrite it before warp 2's dK of step i read it.)
+  // queries.  Three issuers: warp 1 writes S^T, warp 2 dP^T, and warp 3 reads
+  // P^T and dS^T back (dV += P^T dO, dK += dS^T Q).  A buffer is written again
+  // (S^T, dP^T of step i+2) only after buf_free signals that warp 3's products
+  // of step i completed, and those were issued after the softmax warps had
+  // read the buffer and written P^T, dS^T into it.
   const uint32_t tbase = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
@@ -878,38 +876,19 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       const int uses = issued / NS + ((issued % NS) > s ? 1 : 0);
       if (uses > 0) mbar_wait_bounded(&q_full[s], (uses - 1) & 1, NC_DRAIN_NS);
     }
-  } else if (warp == 3) {
-    // ---------------- lse / D of each query tile into the stage (every lane arrives)
-    for (int i = 0; i < n && !*abort_flag; ++i) {
-      const int s = i % NS;
-      if (!at_wait_warp(&q_empty[s], ((i / NS) & 1) ^ 1, sh, abort_flag)) break;
-      const int h = step_h(i), q0 = step_q0(i);
-      float* ld = LD + s * 128;
-      const int64_t base = ((int64_t)b * sh.H + h) * sh.T;
-#pragma unroll
-      for (int e = lane; e < 64; e += 32) {
-        const int q = q0 + e;
-        ld[e] = q < sh.T ? lse[base + q] * LOG2E : INFINITY;   // rows past the end get P = 0
-        ld[64 + e] = q < sh.T ? Dv[base + q] : 0.f;
-      }
-      mbar_arrive(&q_full[s]);
-    }
   } else if ((warp == 1 || warp == 2) && lane == 0) {
-    // ---------------- two MMA issuers (a single thread issues about one MMA per
-    // ~100 cycles, more than these N <= 128 products take):
-    //   warp 1: S^T = K Q^T  and  dV += P^T dO
-    //   warp 2: dP^T = V dO^T and dK += dS^T Q
-    // S^T / dP^T of step i+2 reuse buffer i & 1; each issuer issues its product
-    // after its own dV_i / dK_i, which read P^T_i / dS^T_i from the columns that
-    // product overwrites.
+    // ---------------- two product issuers (a single thread issues about one MMA per
+    // ~100 cycles, so each chain has its own): warp 1 S^T = K Q^T, warp 2
+    // dP^T = V dO^T, into buffer i & 1, up to two steps ahead of the softmax
     const int role = warp - 1;
-    const uint32_t id_s = at_idesc(64, 0), id_kv = at_idesc(HD, 1);
+    const uint32_t id_s = at_idesc(64, 0);
     const uint32_t a_op = smem_u32(smem + (role ? L::OFF_V : L::OFF_K));
     const uint32_t sqs = smem_u32(smem + L::OFF_QS);
-    auto issue_st = [&](int i) -> bool {
+    bool ok = at_wait(kv_full, 0, sh, abort_flag);
+    for (int i = 0; ok && i < n; ++i) {
       const int s = i % NS, buf = i & 1;
-      if (!at_wait(&q_full[s], (i / NS) & 1, sh, abort_flag)) return false;
-      if (i >= 2 && !at_wait(&st_free[buf], ((i - 2) >> 1) & 1, sh, abort_flag)) return false;
+      if (!(ok = at_wait(&q_full[s], (i / NS) & 1, sh, abort_flag))) break;
+      if (i >= 2 && !(ok = at_wait(&buf_free[buf], ((i - 2) >> 1) & 1, sh, abort_flag))) break;
       tc_fence_after();
       const uint32_t bop = sqs + s * 2 * L::QT + (role ? L::QT : 0u);   // Q (S^T) or dO (dP^T)
 #pragma unroll
@@ -917,49 +896,71 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         tc_mma_f16(tbase + role * 128 + buf * 64, kdesc(a_op, kk, CHUNK128), kdesc(bop, kk, CHUNK64), id_s,
                    kk > 0 ? 1u : 0u);
       tc_commit(&st_full[buf]);
-      return true;
-    };
-    bool ok = at_wait(kv_full, 0, sh, abort_flag) && issue_st(0);
+      if (*abort_flag) ok = false;
+    }
+    tc_commit(&drain[role]);
+    mbar_wait_bounded(&drain[role], 0, NC_DRAIN_NS);
+  } else if (warp == 3 && lane == 0) {
+    // ---------------- the accumulating issuer: dV += P^T dO and dK += dS^T Q, A from TMEM
+    const uint32_t id_kv = at_idesc(HD, 1);
+    const uint32_t sqs = smem_u32(smem + L::OFF_QS);
+    bool ok = true;
     for (int i = 0; ok && i < n; ++i) {
-      if (i + 1 < n) ok = issue_st(i + 1);
-      if (ok) ok = at_wait(pt_full, i & 1, sh, abort_flag);
-      if (!ok) break;
+      const int s = i % NS, buf = i & 1;
+      if (!(ok = at_wait(&pt_full[buf], (i >> 1) & 1, sh, abort_flag))) break;
       tc_fence_after();
-      const int s = i % NS;
-      const uint32_t bop = sqs + s * 2 * L::QT + (role ? 0u : L::QT);    // dO (dV) or Q (dK)
-      // P^T (in S^T's columns) or dS^T (in dP^T's); query slice kk at 32 (kk/2) + 8 (kk%2)
-      const uint32_t pt = tbase + role * 128 + (i & 1) * 64;
+      const uint32_t sq = sqs + s * 2 * L::QT;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc_mma_f16_ts(tbase + 256 + role * HD, pt + 32 * (kk >> 1) + 8 * (kk & 1), mndesc(bop, kk, CHUNK64), id_kv,
-                      (i > 0 || kk > 0) ? 1u : 0u);
+      for (int role = 0; role < 2; ++role) {
+        // P^T (in S^T's columns) or dS^T (in dP^T's); query slice kk at 32 (kk/2) + 8 (kk%2)
+        const uint32_t pt = tbase + role * 128 + buf * 64;
+        const uint32_t bop = sq + (role ? 0u : L::QT);    // dO (dV) or Q (dK), MN-major
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_f16_ts(tbase + 256 + role * HD, pt + 32 * (kk >> 1) + 8 * (kk & 1), mndesc(bop, kk, CHUNK64),
+                        id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+      }
+      tc_commit(&buf_free[buf]);
       tc_commit(&q_empty[s]);
       if (*abort_flag) ok = false;
     }
     if (ok) tc_commit(dkv_done);
-    tc_commit(&drain[role]);
-    mbar_wait_bounded(&drain[role], 0, NC_DRAIN_NS);
+    tc_commit(&drain[2]);
+    mbar_wait_bounded(&drain[2], 0, NC_DRAIN_NS);
   } else if (warp >= 4) {
     const int quarter = warp & 3, hf = (warp - 4) >> 2;   // hf: query columns [32 hf, 32 hf + 32)
     const int r = quarter * 32 + lane;
     const int key = kt * 128 + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    // lse * log2(e) and D of this warp's 32 queries: lane e fetches query e's
+    // pair one step ahead (into registers), and the warp shares them through its
+    // own 256-byte slot of shared memory (rows past the end get P = 0)
+    float* ld = reinterpret_cast<float*>(smem + L::OFF_LD) + (warp - 4) * 64;
+    auto fetch = [&](int i, float& l2, float& d) {
+      const int q = step_q0(i) + 32 * hf + lane;
+      const int64_t base = ((int64_t)b * sh.H + step_h(i)) * sh.T;
+      l2 = q < sh.T ? __ldg(lse + base + q) * LOG2E : INFINITY;
+      d = q < sh.T ? __ldg(Dv + base + q) : 0.f;
+    };
+    float nl = 0.f, nd = 0.f;
+    if (n > 0) fetch(0, nl, nd);
     bool ok = true;
     for (int i = 0; i < n; ++i) {
-      const int buf = i & 1, s = i % NS;
+      const int buf = i & 1;
       if (!(ok = at_wait_warp(&st_full[buf], (i >> 1) & 1, sh, abort_flag))) break;
       tc_fence_after();
       uint32_t st[32], dp[32];
       tmem_ld_32x32b_x32(tbase + lane_off + buf * 64 + 32 * hf, st);
       tmem_ld_32x32b_x32(tbase + lane_off + 128 + buf * 64 + 32 * hf, dp);
-      tmem_ld_wait();
-      tc_fence_before();
+      ld[lane] = nl;
+      ld[32 + lane] = nd;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&st_free[buf]);
+      if (i + 1 < n) fetch(i + 1, nl, nd);
+      tmem_ld_wait();
       const int q0 = step_q0(i) + 32 * hf;
       const bool diag = step_q0(i) < kt * 128 + 128;
-      const float4* ld4 = reinterpret_cast<const float4*>(LD + s * 128 + 32 * hf);
-      const float4* dd4 = reinterpret_cast<const float4*>(LD + s * 128 + 64 + 32 * hf);
+      const float4* ld4 = reinterpret_cast<const float4*>(ld);
+      const float4* dd4 = reinterpret_cast<const float4*>(ld + 32);
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 l4 = ld4[c4], d4 = dd4[c4];
@@ -982,8 +983,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       tmem_st_32x32b_x16(tbase + lane_off + 128 + buf * 64 + 32 * hf, dp);
       tmem_st_wait();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pt_full);
+      __syncwarp();   // also: every lane has read the slot before the next step overwrites it
+      if (lane == 0) mbar_arrive(&pt_full[buf]);
     }
     if (ok && at_wait_warp(dkv_done, 0, sh, abort_flag)) {
       tc_fence_after();

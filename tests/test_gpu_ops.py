@@ -490,4 +490,3 @@ def test_embed_scatter_skips_out_of_range_ids():
     present = np.zeros(V, dtype=bool)
     present[tk] = True
     assert np.all(g[~present] == 0.0)
-
