@@ -115,25 +115,46 @@ __device__ __forceinline__ void st4(bf16* p, float4 v) {
 }
 
 // One warp per row; C % 4 == 0.  y = x * rstd, rstd = 1/sqrt(mean(x^2) + eps).
+// amax_bits (optional): atomic maximum of |y| as stored (after rounding to T),
+// as the bits of a non-negative float, for the 8-bit quantiser of y; one
+// atomic per block.
 template <typename T>
 __global__ void k_rmsnorm_fwd(int64_t rows, int C, const float* __restrict__ x,
-                              T* __restrict__ y, float* __restrict__ rstd, float eps) {
+                              T* __restrict__ y, float* __restrict__ rstd, float eps, unsigned* __restrict__ amax_bits) {
+  __shared__ float wmax[8];
   int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const float4* xr = reinterpret_cast<const float4*>(x + row * C);
-  float ss = 0.f;
-  for (int c = lane; c < C / 4; c += 32) {
-    float4 v = xr[c];
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  float am = 0.f;
+  if (row < rows) {
+    const float4* xr = reinterpret_cast<const float4*>(x + row * C);
+    float ss = 0.f;
+    for (int c = lane; c < C / 4; c += 32) {
+      float4 v = xr[c];
+      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    ss = warp_sum(ss);
+    float r = rsqrtf(ss / (float)C + eps);
+    if (lane == 0) rstd[row] = r;
+    T* yr = y + row * C;
+    for (int c = lane; c < C / 4; c += 32) {
+      float4 v = xr[c];
+      const float4 o = make_float4(v.x * r, v.y * r, v.z * r, v.w * r);
+      st4(yr + 4 * c, o);
+      if (amax_bits)
+        am = fmaxf(am, fmaxf(fmaxf(fabsf(round_act<T>(o.x)), fabsf(round_act<T>(o.y))),
+                             fmaxf(fabsf(round_act<T>(o.z)), fabsf(round_act<T>(o.w)))));
+    }
   }
-  ss = warp_sum(ss);
-  float r = rsqrtf(ss / (float)C + eps);
-  if (lane == 0) rstd[row] = r;
-  T* yr = y + row * C;
-  for (int c = lane; c < C / 4; c += 32) {
-    float4 v = xr[c];
-    st4(yr + 4 * c, make_float4(v.x * r, v.y * r, v.z * r, v.w * r));
+  if (amax_bits) {   // uniform across the block: every thread reaches this point
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+    if (lane == 0) wmax[threadIdx.x >> 5] = am;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float m = wmax[0];
+      for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, wmax[w]);
+      atomicMax(amax_bits, __float_as_uint(m));
+    }
   }
 }
 
@@ -169,10 +190,10 @@ __global__ void k_rmsnorm_bwd(int64_t rows, int C, const float* __restrict__ dy,
 
 template <typename T>
 nc_status launch_rmsnorm_fwd_t(int64_t rows, int C, const float* x, T* y, float* rstd, float eps,
-                               cudaStream_t st) {
+                               cudaStream_t st, unsigned* amax_bits = nullptr) {
   if (rows <= 0) return NC_OK;
   if (C % 4 || (((uintptr_t)x) & 15)) return NC_ERR_ARG;
-  k_rmsnorm_fwd<T><<<cdiv(rows, 8), 256, 0, st>>>(rows, C, x, y, rstd, eps);
+  k_rmsnorm_fwd<T><<<cdiv(rows, 8), 256, 0, st>>>(rows, C, x, y, rstd, eps, amax_bits);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 template <typename T>
@@ -185,9 +206,9 @@ nc_status launch_rmsnorm_bwd_t(int64_t rows, int C, const float* dy, const T* y,
 }
 
 nc_status launch_rmsnorm_fwd(int dtype, int64_t rows, int C, const float* x, void* y, float* rstd,
-                             float eps, cudaStream_t st) {
-  if (dtype == NC_BF16) return launch_rmsnorm_fwd_t<bf16>(rows, C, x, (bf16*)y, rstd, eps, st);
-  return launch_rmsnorm_fwd_t<float>(rows, C, x, (float*)y, rstd, eps, st);
+                             float eps, cudaStream_t st, unsigned* amax_bits) {
+  if (dtype == NC_BF16) return launch_rmsnorm_fwd_t<bf16>(rows, C, x, (bf16*)y, rstd, eps, st, amax_bits);
+  return launch_rmsnorm_fwd_t<float>(rows, C, x, (float*)y, rstd, eps, st, amax_bits);
 }
 nc_status launch_rmsnorm_bwd(int dtype, int64_t rows, int C, const float* dy, const void* y,
                              const float* rstd, float* dx, void* dx_act, cudaStream_t st) {

@@ -109,3 +109,119 @@ nc_status launch_quantize_fp8(int dtype, const void* x, int64_t n, uint8_t* y, f
   }
   return NC_OK;
 }
+
+// ---------------------------------------------------------------- the step's quantiser pieces
+// The same rule as above in fewer launches: the amax pass leaves out the
+// memset (the step zeroes every statistic slot of a step at once), and the
+// cast pass forms the scale itself (the scale kernel's formula), so a
+// quantisation is two launches, or one when the producer of x has already
+// taken its maximum.
+
+__device__ __forceinline__ float fp8_scale_of(float amax) {
+  float scale = 448.f / amax;
+  if (!(scale > 0.f) || !isfinite(scale)) scale = 1.f;
+  return scale;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(FP8_THREADS) k_fp8_cast_scaled(const T* __restrict__ x, int64_t n,
+                                                                 float* __restrict__ stats, uint8_t* __restrict__ y) {
+  const float s = fp8_scale_of(__uint_as_float(*reinterpret_cast<const unsigned*>(stats)));
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    stats[1] = s;
+    stats[2] = 1.f / s;
+  }
+  const int64_t n8 = n & ~(int64_t)7;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x * 8;
+  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < n8; i += stride) {
+    float f[8];
+    load8(x, i, f);
+    uint2 o;
+    o.x = e4m3(f[0] * s) | (e4m3(f[1] * s) << 8) | (e4m3(f[2] * s) << 16) | (e4m3(f[3] * s) << 24);
+    o.y = e4m3(f[4] * s) | (e4m3(f[5] * s) << 8) | (e4m3(f[6] * s) << 16) | (e4m3(f[7] * s) << 24);
+    *reinterpret_cast<uint2*>(y + i) = o;
+  }
+  if (blockIdx.x == 0 && threadIdx.x < n - n8) y[n8 + threadIdx.x] = (uint8_t)e4m3(to_f32(x[n8 + threadIdx.x]) * s);
+}
+
+static unsigned fp8_grid(int64_t n) {
+  if (!g_num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      g_num_sms = 148;
+  }
+  const long long want = std::max<long long>(1, (n / 8 + FP8_THREADS - 1) / FP8_THREADS);
+  return (unsigned)std::min<long long>(want, 8LL * g_num_sms);
+}
+
+nc_status launch_fp8_amax(int dtype, const void* x, int64_t n, float* stats, cudaStream_t st) {
+  if (n <= 0) return NC_OK;
+  if (!x || !stats || (((uintptr_t)x) & 15) || (((uintptr_t)stats) & 3)) return NC_ERR_ARG;
+  const unsigned grid = fp8_grid(n);
+  if (dtype == NC_BF16) k_fp8_amax<bf16><<<grid, FP8_THREADS, 0, st>>>((const bf16*)x, n, (unsigned*)stats);
+  else k_fp8_amax<float><<<grid, FP8_THREADS, 0, st>>>((const float*)x, n, (unsigned*)stats);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+nc_status launch_fp8_cast_scaled(int dtype, const void* x, int64_t n, uint8_t* y, float* stats, cudaStream_t st) {
+  if (n <= 0) return NC_OK;
+  if (!x || !y || !stats || (((uintptr_t)x) & 15) || (((uintptr_t)y) & 7) || (((uintptr_t)stats) & 3))
+    return NC_ERR_ARG;
+  const unsigned grid = fp8_grid(n);
+  if (dtype == NC_BF16) k_fp8_cast_scaled<bf16><<<grid, FP8_THREADS, 0, st>>>((const bf16*)x, n, stats, y);
+  else k_fp8_cast_scaled<float><<<grid, FP8_THREADS, 0, st>>>((const float*)x, n, stats, y);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+// Multi-tensor form over fp32 tensors (the weight operands of one step): block
+// b handles chunk b - chunk0[t] (OPT_CHUNK elements) of tensor t.
+__device__ __forceinline__ int fp8_tensor_of(const OptTensors& tl, int blk) {
+  int lo = 0, hi = tl.n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tl.chunk0[mid] <= blk) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(FP8_THREADS) k_fp8_amax_multi(const __grid_constant__ OptTensors tl,
+                                                                const float* __restrict__ master,
+                                                                float* __restrict__ stats) {
+  __shared__ float sh[32];
+  const int t = fp8_tensor_of(tl, blockIdx.x);
+  const int64_t e0 = (int64_t)(blockIdx.x - tl.chunk0[t]) * OPT_CHUNK;
+  const int64_t e1 = min(tl.len[t], e0 + OPT_CHUNK);
+  const float* x = master + tl.off[t];
+  float m = 0.f;
+  for (int64_t e = e0 + threadIdx.x; e < e1; e += FP8_THREADS) m = fmaxf(m, fabsf(x[e]));
+  m = block_max(m, sh);
+  if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned*>(stats + 4 * t), __float_as_uint(m));
+}
+
+__global__ void __launch_bounds__(FP8_THREADS) k_fp8_cast_multi(const __grid_constant__ OptTensors tl,
+                                                                const float* __restrict__ master,
+                                                                float* __restrict__ stats, uint8_t* __restrict__ y) {
+  const int t = fp8_tensor_of(tl, blockIdx.x);
+  const int64_t e0 = (int64_t)(blockIdx.x - tl.chunk0[t]) * OPT_CHUNK;
+  const int64_t e1 = min(tl.len[t], e0 + OPT_CHUNK);
+  float* st = stats + 4 * t;
+  const float s = fp8_scale_of(__uint_as_float(*reinterpret_cast<const unsigned*>(st)));
+  if (e0 == 0 && threadIdx.x == 0) {
+    st[1] = s;
+    st[2] = 1.f / s;
+  }
+  const float* x = master + tl.off[t];
+  uint8_t* out = y + tl.soff[t];
+  for (int64_t e = e0 + threadIdx.x; e < e1; e += FP8_THREADS) out[e] = (uint8_t)e4m3(x[e] * s);
+}
+
+nc_status launch_fp8_quantize_multi(const OptTensors& tl, const float* master, float* stats, uint8_t* y,
+                                    cudaStream_t st) {
+  const int nb = tl.chunk0[tl.n];
+  if (nb <= 0) return NC_OK;
+  k_fp8_amax_multi<<<nb, FP8_THREADS, 0, st>>>(tl, master, stats);
+  NC_CUDA_TRY(cudaGetLastError());
+  k_fp8_cast_multi<<<nb, FP8_THREADS, 0, st>>>(tl, master, stats, y);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}

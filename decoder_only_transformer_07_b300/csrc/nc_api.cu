@@ -42,8 +42,9 @@ struct nc_model {
   float* rstd_e = nullptr;           // [Nmax] its per-row rstd (emb_norm only)
   bool fp8 = false;                  // the blocks' forward linears on E4M3 operands
   uint8_t* q8a = nullptr;            // E4M3 codes of a linear layer's input [Nmax, max(C, F)]
-  uint8_t* q8w = nullptr;            // E4M3 codes of its weight (the largest block weight)
-  float* q8s = nullptr;              // {amax, scale, scale_inv} of the activation [0..3), weight [4..7)
+  uint8_t* q8w = nullptr;            // E4M3 codes of every block weight operand, quantised once per step
+  float* q8s = nullptr;              // per layer and linear {amax bits, scale, scale_inv, -}: inputs [L][4], weights [L][4]
+  OptTensors* q8tl = nullptr;        // the 4 L weight operands (fp32 master offset, code offset, length)
   int32_t* err = nullptr;            // device error flag
   float* result = nullptr;           // device: [0] loss, [1] error flag copy
   float* result_host = nullptr;      // pinned host copy
@@ -307,10 +308,32 @@ static nc_status allocate(nc_model* m) {
   if (m->emb_norm) NC_TRY(dalloc_t(m, (size_t)N, &m->rstd_e));
   if (m->fp8) {
     const int64_t kmax = std::max<int64_t>(m->C, m->F);
-    const int64_t wmax = std::max<int64_t>((int64_t)m->qkvw, 2 * (int64_t)m->F) * m->C;
     NC_TRY(dalloc(m, (size_t)(N * kmax), (void**)&m->q8a));
-    NC_TRY(dalloc(m, (size_t)wmax, (void**)&m->q8w));
-    NC_TRY(dalloc_t(m, 8, &m->q8s));
+    // the blocks' weight operands [Wq; Wk; Wv], Wo, Wfc, Wproj, each its own tensor
+    if (4 * L > NC_OPT_MAXT) return NC_ERR_UNSUPPORTED;
+    m->q8tl = new (std::nothrow) OptTensors;
+    if (!m->q8tl) return NC_ERR_ALLOC;
+    memset(m->q8tl, 0, sizeof(OptTensors));
+    m->q8tl->n = 4 * L;
+    int32_t c = 0;
+    int64_t so = 0;
+    for (int l = 0; l < L; ++l) {
+      const int64_t len[4] = {(int64_t)m->qkvw * m->C, (int64_t)m->C * m->H * m->hd, (int64_t)m->F * m->C,
+                              (int64_t)m->C * m->F};
+      const int which[4] = {0, 3, 4, 5};
+      for (int k = 0; k < 4; ++k) {
+        const int t = 4 * l + k;
+        m->q8tl->chunk0[t] = c;
+        m->q8tl->off[t] = tensor(m, l, which[k]).off;
+        m->q8tl->soff[t] = so;
+        m->q8tl->len[t] = len[k];
+        c += (int32_t)((len[k] + OPT_CHUNK - 1) / OPT_CHUNK);
+        so += (len[k] + 255) / 256 * 256;
+      }
+    }
+    m->q8tl->chunk0[4 * L] = c;
+    NC_TRY(dalloc(m, (size_t)so, (void**)&m->q8w));
+    NC_TRY(dalloc_t(m, (size_t)32 * L, &m->q8s));
   }
   NC_TRY(dalloc_t(m, (size_t)N, &m->rstd_f));
   // logits chunk: at most 1 GiB of compute-dtype logits per chunk, whole 128-row tiles
@@ -363,6 +386,7 @@ extern "C" void nc_model_destroy(nc_model* m) {
   for (void* p : m->allocs) cudaFree(p);
   if (m->result_host) cudaFreeHost(m->result_host);
   delete m->opt_tl;
+  delete m->q8tl;
   for (int k = 0; k < nc_model::NC_OPT_STREAMS; ++k) {
     if (m->opt_st[k]) cudaStreamDestroy(m->opt_st[k]);
     if (m->opt_join[k]) cudaEventDestroy(m->opt_join[k]);
@@ -496,20 +520,33 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
   const int nh = m->H + m->Hkv;
   const double attn_fl = 4.0 * B * m->H * m->hd * ((double)T * (T + 1) / 2.0);
   const double nrm_by = (double)N * (4.0 * C + a * C + 4);
-  // The 8-bit step's linear layer: quantise the bf16 input [N, K] and the fp32
-  // master weight [Nout, K] (per tensor, current scaling), then the E4M3 GEMM
-  // through the layer's epilogue (RoPE + QK-norm with rope, else `ep`).
-  auto lin8 = [&](const void* act_in, int K, const ParamTensor& w, int Nout, int ep, void* D, int64_t ldd,
-                  float* rstdqk) -> nc_status {
-    PROF(NC_PROF_QUANT, 0, 5.0 * N * K, launch_quantize_fp8(NC_BF16, act_in, N * K, m->q8a, m->q8s, st));
-    PROF(NC_PROF_QUANT, 0, 9.0 * Nout * K,
-         launch_quantize_fp8(NC_FP32, m->master + w.off, (int64_t)Nout * K, m->q8w, m->q8s + 4, st));
+  // The 8-bit step: every block weight operand is quantised once per step (two
+  // launches over all of them); a linear layer's bf16 input is quantised into
+  // q8a with its own statistics slot (the cast only, when the RMSNorm that
+  // produced it has taken its maximum), then the E4M3 GEMM runs through the
+  // layer's epilogue (RoPE + QK-norm with NC_EP_QKV_ROPE, else `ep`).
+  if (m->fp8) {
+    NC_CUDA_TRY(cudaMemsetAsync(m->q8s, 0, (size_t)32 * m->L * sizeof(float), st));
+    PROF(NC_PROF_QUANT, 0, 9.0 * (double)m->q8tl->soff[4 * m->L - 1],
+         launch_fp8_quantize_multi(*m->q8tl, m->master, m->q8s + 16 * m->L, m->q8w, st));
+    m->launches += 2;
+  }
+  auto lin8 = [&](int l, int k, const void* act_in, int K, int Nout, int ep, void* D, int64_t ldd, float* rstdqk,
+                  bool amax_ready) -> nc_status {
+    float* as = m->q8s + (4 * l + k) * 4;
+    float* ws = m->q8s + 16 * m->L + (4 * l + k) * 4;
+    const uint8_t* w8 = m->q8w + m->q8tl->soff[4 * l + k];
+    if (!amax_ready) {
+      PROF(NC_PROF_QUANT, 0, 2.0 * N * K, launch_fp8_amax(NC_BF16, act_in, N * K, as, st));
+      m->launches += 1;
+    }
+    PROF(NC_PROF_QUANT, 0, 3.0 * N * K, launch_fp8_cast_scaled(NC_BF16, act_in, N * K, m->q8a, as, st));
     const double out = ep == NC_EP_ACCUM_F32 ? 8.0 : 2.0;
     PROF_SUB(NC_PROF_GEMM, NC_PROF_GEMM_FWD, 2.0 * N * Nout * K, (double)N * K + (double)Nout * K + (double)N * Nout * out,
-             launch_gemm_fp8_ep((int)N, Nout, K, m->q8a, K, m->q8w, K, m->q8s + 2, m->q8s + 6, ep, D, ldd, T, nh,
-                                m->hd, m->rope_pairs ? m->rope_pairs : m->rope_tab, m->rope_pairs ? m->Tmax : 0,
-                                rstdqk, eps, m->err, st));
-    m->launches += 7;
+             launch_gemm_fp8_ep((int)N, Nout, K, m->q8a, K, w8, K, as + 2, ws + 2, ep, D, ldd, T, nh, m->hd,
+                                m->rope_pairs ? m->rope_pairs : m->rope_tab, m->rope_pairs ? m->Tmax : 0, rstdqk,
+                                eps, m->err, st));
+    m->launches += 2;
     return NC_OK;
   };
   for (int l = 0; l < m->L; ++l) {
@@ -522,18 +559,22 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
     float* rstd2 = m->rstd2 + (size_t)l * m->Nmax;
     float* rstdqk = m->rstdqk + (size_t)l * m->Nmax * (m->H + m->Hkv);
     float* lse = m->lse + (size_t)l * m->Nmax * m->H;
-    PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn1, rstd1, eps, st));
     if (m->fp8) {
-      NC_TRY(lin8(xn1, C, tensor(m, l, 0), W, NC_EP_QKV_ROPE, qkv, W, rstdqk));
+      // the norms take the maximum of the bf16 values they store: their inputs' quantisation is one cast
+      PROF(NC_PROF_NORM, 0, nrm_by,
+           launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn1, rstd1, eps, st, (unsigned*)(m->q8s + (4 * l + 0) * 4)));
+      NC_TRY(lin8(l, 0, xn1, C, W, NC_EP_QKV_ROPE, qkv, W, rstdqk, true));
       PROF(NC_PROF_ATTN_FWD, attn_fl, (double)N * (W + Hd) * a + 4.0 * N * m->H,
            attn_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->err, st));
-      NC_TRY(lin8(o, Hd, tensor(m, l, 3), C, NC_EP_ACCUM_F32, m->x, C, nullptr));
-      PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn2, rstd2, eps, st));
-      NC_TRY(lin8(xn2, C, tensor(m, l, 4), F, NC_EP_RELU2_SQ, h, F, nullptr));
-      NC_TRY(lin8(h, F, tensor(m, l, 5), C, NC_EP_ACCUM_F32, m->x, C, nullptr));
+      NC_TRY(lin8(l, 1, o, Hd, C, NC_EP_ACCUM_F32, m->x, C, nullptr, false));
+      PROF(NC_PROF_NORM, 0, nrm_by,
+           launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn2, rstd2, eps, st, (unsigned*)(m->q8s + (4 * l + 2) * 4)));
+      NC_TRY(lin8(l, 2, xn2, C, F, NC_EP_RELU2_SQ, h, F, nullptr, true));
+      NC_TRY(lin8(l, 3, h, F, C, NC_EP_ACCUM_F32, m->x, C, nullptr, false));
       m->launches += 3;
       continue;
     }
+    PROF(NC_PROF_NORM, 0, nrm_by, launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn1, rstd1, eps, st));
     if (m->dtype == NC_BF16) {
       // q/k/v projection with RoPE and the q/k RMSNorm in the GEMM epilogue
       PROF_SUB(NC_PROF_GEMM, NC_PROF_GEMM_FWD, 2.0 * N * W * C, ((double)N * C + (double)W * C + (double)N * W) * a,

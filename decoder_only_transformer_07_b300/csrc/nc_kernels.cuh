@@ -10,8 +10,9 @@ nc_status launch_cast_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t 
 // tab [T][hd/2][2] and/or pairs [hd/4][T][4] (pair-major copy); either may be NULL.
 nc_status launch_rope_table(int T, int hd, float base, float* tab, float* pairs, cudaStream_t st);
 
+// amax_bits (optional, pre-zeroed): atomic maximum of |y| as stored, float bits (8-bit quantiser input).
 nc_status launch_rmsnorm_fwd(int dtype, int64_t rows, int C, const float* x, void* y, float* rstd,
-                             float eps, cudaStream_t st);
+                             float eps, cudaStream_t st, unsigned* amax_bits = nullptr);
 nc_status launch_rmsnorm_bwd(int dtype, int64_t rows, int C, const float* dy, const void* y,
                              const float* rstd, float* dx, void* dx_act, cudaStream_t st);
 // pos0 (device, may be NULL): positions are *pos0 + row % T instead of row % T.
@@ -85,6 +86,13 @@ nc_status launch_gemm_fp8_ep(int M, int N, int K, const uint8_t* A, int64_t lda,
 // Per-tensor E4M3 quantisation of n fp32 / bf16 values: stats (device, 3
 // floats) gets {amax, scale, scale_inv}; y the codes.
 nc_status launch_quantize_fp8(int dtype, const void* x, int64_t n, uint8_t* y, float* stats, cudaStream_t st);
+// The step's 8-bit quantiser pieces.  stats = {amax bits, scale, scale_inv}
+// with stats[0] zeroed beforehand.  launch_fp8_amax: atomic maximum of |x|
+// into stats[0].  launch_fp8_cast_scaled: scale = fl32(448 / amax) (1 if not
+// finite and positive) formed by every block, codes of fl32(x * scale), and
+// stats[1], stats[2] written; the codes equal launch_quantize_fp8's.
+nc_status launch_fp8_amax(int dtype, const void* x, int64_t n, float* stats, cudaStream_t st);
+nc_status launch_fp8_cast_scaled(int dtype, const void* x, int64_t n, uint8_t* y, float* stats, cudaStream_t st);
 
 nc_status launch_attn_fwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv, void* o,
                                float* lse, cudaStream_t st);
@@ -127,6 +135,10 @@ struct OptTensors {
   int64_t len[NC_OPT_MAXT];    // elements
   float* norm;                 // device [n]: ||U||_F per tensor (written by launch_muon_momentum)
 };
+// Every tensor t of tl at once (fp32 master + tl.off[t], tl.len[t] elements):
+// stats + 4 t as above (stats[4 t] zeroed beforehand), codes at y + tl.soff[t].
+nc_status launch_fp8_quantize_multi(const OptTensors& tl, const float* master, float* stats, uint8_t* y,
+                                    cudaStream_t st);
 // M <- mu M + G; U = nesterov ? G + mu M : M; then tl.norm[t] = ||U_t||_F.
 // partial: one float per chunk.
 nc_status launch_muon_momentum(const OptTensors& tl, const float* G, float* M, float* U, float mu, int nesterov,
