@@ -224,6 +224,19 @@ def linear(cfg, x, w):
     return xq @ wq.T
 
 
+def linear_dx(cfg, dy, w):
+    """The input gradient of ``linear``: dX = dY w.
+
+    With cfg.fp8 both operands are E4M3 as well: the bf16 value of dY
+    quantised per tensor with current scaling (its own absolute maximum), and
+    the weight with the same codes and factor as in the forward (the same
+    tensor, read transposed).  The weight gradient dW = dY^T x is not
+    quantised."""
+    if not cfg.fp8:
+        return dy @ w
+    return quantize_dequantize(bf16_round(dy)) @ quantize_dequantize(w)
+
+
 def softcap(z, c):
     """Logit soft-cap: (c tanh(z / c), dzc/dz = 1 - tanh(z / c)^2); identity for c <= 0.
 
@@ -291,14 +304,14 @@ def block_backward(cfg, W, l, x, dx2, cos, sin, G):
     N = B * T
     # MLP: x2 = x1 + relu(bn Wfc^T)^2 Wproj^T
     G[p + "wproj"] += dx2.reshape(N, C).T @ s["hmid"].reshape(N, -1)
-    dh = dx2 @ W[p + "wproj"]
+    dh = linear_dx(cfg, dx2, W[p + "wproj"])
     du = dh * 2.0 * s["r"]
     G[p + "wfc"] += du.reshape(N, -1).T @ s["bn"].reshape(N, C)
-    dbn = du @ W[p + "wfc"]
+    dbn = linear_dx(cfg, du, W[p + "wfc"])
     dx1 = dx2 + rms_norm_bwd(dbn, s["bn"], s["rstd2"])
     # attention output projection: x1 = x + o2 Wo^T
     G[p + "wo"] += dx1.reshape(N, C).T @ s["o2"].reshape(N, -1)
-    do2 = dx1 @ W[p + "wo"]
+    do2 = linear_dx(cfg, dx1, W[p + "wo"])
     do = do2.reshape(B, T, H, hd).transpose(0, 2, 1, 3)
     dqn = np.zeros((B, H, T, hd))
     dkn = np.zeros((B, Hkv, T, hd))
@@ -319,7 +332,11 @@ def block_backward(cfg, W, l, x, dx2, cos, sin, G):
     G[p + "wq"] += dq2.T @ a
     G[p + "wk"] += dk2.T @ a
     G[p + "wv"] += dv2.T @ a
-    da = dq2 @ W[p + "wq"] + dk2 @ W[p + "wk"] + dv2 @ W[p + "wv"]
+    if cfg.fp8:   # one operand [dq | dk | dv] against [Wq; Wk; Wv], as the fused projection's backward multiplies them
+        da = linear_dx(cfg, np.concatenate([dq2, dk2, dv2], axis=-1),
+                       np.concatenate([W[p + "wq"], W[p + "wk"], W[p + "wv"]], axis=0))
+    else:
+        da = dq2 @ W[p + "wq"] + dk2 @ W[p + "wk"] + dv2 @ W[p + "wv"]
     return dx1 + rms_norm_bwd(da.reshape(B, T, C), s["a"], s["rstd1"])
 
 
@@ -378,12 +395,13 @@ def row_losses(cfg, params, tokens, targets):
     return out.reshape(B, T)
 
 
-def forward_backward(cfg, params, tokens, targets, chunk=512):
+def forward_backward(cfg, params, tokens, targets, chunk=512, grad_scale=1.0):
     """Mean next-token cross-entropy and its gradient for every parameter.
 
     Returns (loss, grads) with grads a dict of fp64 matrices in layout order
-    (use ``pack`` for the flat vector).  Only the residual stream entering
-    each layer is kept; each layer's forward is recomputed in the backward.
+    (use ``pack`` for the flat vector); the gradients are those of
+    grad_scale * loss.  Only the residual stream entering each layer is kept;
+    each layer's forward is recomputed in the backward.
     """
     W = unpack(cfg, params) if not isinstance(params, dict) else params
     tokens, targets = np.asarray(tokens), np.asarray(targets)
@@ -401,7 +419,7 @@ def forward_backward(cfg, params, tokens, targets, chunk=512):
         z, dcap = softcap(xf2[a:a + chunk] @ W["lm_head"].T, cfg.logit_softcap)
         l_rows, dz = cross_entropy(z, t[a:a + chunk])
         total += float(np.sum(l_rows))
-        dz /= N                                   # the loss is a mean over B*T
+        dz *= grad_scale / N                      # the loss is a mean over B*T
         if dcap is not None:
             dz *= dcap                            # through the soft-cap
         G["lm_head"] += dz.T @ xf2[a:a + chunk]

@@ -4,8 +4,10 @@ The reading (woshipm nanochat analysis §一.2 and §六.2 name FP8 without a
 recipe): each block's four linear layers multiply E4M3 operands, the bf16
 activation and the fp32 master weight, each quantised per tensor with
 current scaling (one tensor [Wq; Wk; Wv] for the fused projection); the
-backward passes through the quantisers as the identity (straight-through)
-and uses the unquantised operands.
+input-gradient products dX = dY W multiply E4M3 operands as well (dY's bf16
+value with its own per-tensor scale, W with its forward codes); the weight
+gradients use the unquantised operands, and the quantisers pass gradients
+through unchanged.
 
 Pins from outside the oracle:
 * with the quantiser and the bf16 rounding replaced by identities the step is
@@ -15,8 +17,11 @@ Pins from outside the oracle:
   Wo and Wproj are scaled by a power of two (the codes do not change, the
   dequantisation factors scale exactly, and the norms remove the scale);
 * every quantised product lies within the E4M3 error bound of the exact one;
-* the 8-bit step's loss stays close to the fp64 loss.
-Planted mistakes in the dequantisation are caught.
+* the 8-bit step's loss stays close to the fp64 loss;
+* the input-gradient products dX = dY w are E4M3 too (dY with its own
+  per-tensor scale): within the same bound, and scaling the loss by a power
+  of two scales every gradient exactly.
+Planted mistakes in the dequantisation and in the scaling of dY are caught.
 """
 import numpy as np
 import pytest
@@ -106,6 +111,42 @@ def test_8bit_step_loss_close_to_fp64():
         assert a @ b / (np.linalg.norm(a) * np.linalg.norm(b)) > 0.95, k
 
 
+def test_quantised_input_gradient_within_the_e4m3_bound():
+    """dX = dY w with both operands E4M3 (dY from its bf16 value): within the same bound as the forward product."""
+    rng = np.random.default_rng(48)
+    cfg = small_cfg()
+    dy = rng.normal(0.0, 1e-3, size=(41, 29)) * np.exp(rng.normal(0.0, 1.0, size=(41, 1)))
+    w = rng.normal(0.0, 0.05, size=(29, 48)).astype(np.float32).astype(np.float64)
+    got = M.linear_dx(cfg, dy, w)
+    exact = dy @ w
+    _, _, ys, _ = F8.quantize(M.bf16_round(dy).astype(np.float32))
+    _, _, ws, _ = F8.quantize(w.astype(np.float32))
+    qy, qw = 2.0 ** -10 / float(ys), 2.0 ** -10 / float(ws)
+    ay, aw = np.abs(dy), np.abs(w)
+    rel = (1 + 2.0 ** -9) * (1 + 2.0 ** -4) ** 2 - 1
+    bound = rel * (ay @ aw) + qy * (1 + 2.0 ** -4) * aw.sum(axis=0)[None, :] + \
+        qw * (1 + 2.0 ** -4) * ay.sum(axis=1)[:, None] * (1 + 2.0 ** -9) + qy * qw * dy.shape[1]
+    err = np.abs(got - exact)
+    assert np.all(err <= bound)
+    assert np.median(err / (ay @ aw)) > 2.0 ** -9
+
+
+def test_gradient_scale_by_a_power_of_two_is_exact():
+    """Current (per-tensor) scaling of every dY: scaling the loss by 2^k scales
+    every dY by 2^k, which leaves its codes unchanged and its factor exact, so
+    the 8-bit step's gradients are exactly 2^k times; a factor of 3 changes the
+    codes and the gradients are not exactly 3 times."""
+    cfg = small_cfg()
+    params = rand_params(cfg, 49, std=0.1)
+    tok, tgt = rand_tokens(cfg, 2, 6, 50)
+    _, G1 = M.forward_backward(cfg, params, tok, tgt)
+    _, G8 = M.forward_backward(cfg, params, tok, tgt, grad_scale=2.0 ** 5)
+    for k in G1:
+        assert np.array_equal(G8[k], G1[k] * 2.0 ** 5), k
+    _, G3 = M.forward_backward(cfg, params, tok, tgt, grad_scale=3.0)
+    assert any(not np.allclose(G3[k], 3.0 * G1[k], rtol=1e-9, atol=0) for k in G1 if not k.startswith("lm_head"))
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _dequantise_with_scale(x):
@@ -118,16 +159,27 @@ def _no_dequantisation(x):
     return F8.e4m3_decode(codes)
 
 
-MUTANTS = {"dequantised with the scale": _dequantise_with_scale,
-           "codes used without their factor": _no_dequantisation}
+def _linear_dx_fixed_scale(cfg, dy, w):
+    """dY quantised with a fixed unit scale instead of its own maximum."""
+    if not cfg.fp8:
+        return dy @ w
+    codes = F8.e4m3_encode(np.clip(M.bf16_round(dy).astype(np.float32), -448, 448))
+    return F8.e4m3_decode(codes) @ M.quantize_dequantize(w)
+
+
+MUTANTS = {"dequantised with the scale": ("quantize_dequantize", _dequantise_with_scale),
+           "codes used without their factor": ("quantize_dequantize", _no_dequantisation),
+           "input gradient with a fixed scale": ("linear_dx", _linear_dx_fixed_scale)}
 
 PINS = [test_power_of_two_scaling_leaves_the_8bit_model_unchanged, test_quantised_product_within_the_e4m3_bound,
-        test_8bit_step_loss_close_to_fp64]
+        test_8bit_step_loss_close_to_fp64, test_quantised_input_gradient_within_the_e4m3_bound,
+        test_gradient_scale_by_a_power_of_two_is_exact]
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_planted_8bit_mistake_is_caught(name, monkeypatch):
-    monkeypatch.setattr(M, "quantize_dequantize", MUTANTS[name])
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(M, attr, fn)
     failed = 0
     for pin in PINS:
         try:
