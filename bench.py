@@ -648,9 +648,10 @@ def main():
     fp8_step = None
     if (args.fp8_step if args.fp8_step is not None else (extras != "")) and w.dtype == "bf16":
         fp8_step = measure(w, args.config, args, world, rank, dev, fp8=True)
-        fp8_step["dtype"] = "e4m3 operands in the blocks' forward linears, bf16 elsewhere"
+        fp8_step["dtype"] = "e4m3 operands in the blocks' forward and input-gradient linears, bf16 elsewhere"
         fp8_step["note"] = ("the 8-bit training step (nc_config.fp8 = 1), same workload; MFU is quoted against the "
-                            "bf16 peak, and the GEMM roofline mixes 8-bit forward and bf16 backward products")
+                            "bf16 peak, and the GEMM roofline mixes 8-bit forward and input-gradient products with bf16 "
+                            "weight-gradient products")
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

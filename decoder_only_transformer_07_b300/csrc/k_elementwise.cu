@@ -160,31 +160,52 @@ __global__ void k_rmsnorm_fwd(int64_t rows, int C, const float* __restrict__ x,
 
 // dx += rstd * (dy - y * mean(dy * y)); dx_act = act(dx) if given.  One warp
 // per row, four columns per lane per step (C % 4 == 0).
+// amax_bits (optional, with dx_act): atomic maximum of |dx_act| as stored, as
+// float bits, for the 8-bit quantiser of dx_act; one atomic per block.
 template <typename T>
 __global__ void k_rmsnorm_bwd(int64_t rows, int C, const float* __restrict__ dy,
                               const T* __restrict__ y, const float* __restrict__ rstd,
-                              float* __restrict__ dx, T* __restrict__ dx_act) {
+                              float* __restrict__ dx, T* __restrict__ dx_act, unsigned* __restrict__ amax_bits) {
+  __shared__ float wmax[8];
   int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const float* dyr = dy + row * C;
-  const T* yr = y + row * C;
-  float dot = 0.f;
-  for (int c = lane * 4; c < C; c += 128) {
-    float4 a = ld4(dyr + c), b = ld4(yr + c);
-    dot += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+  float am = 0.f;
+  if (row < rows) {
+    const float* dyr = dy + row * C;
+    const T* yr = y + row * C;
+    float dot = 0.f;
+    for (int c = lane * 4; c < C; c += 128) {
+      float4 a = ld4(dyr + c), b = ld4(yr + c);
+      dot += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+    }
+    dot = warp_sum(dot) / (float)C;
+    const float r = rstd[row];
+    float* dxr = dx + row * C;
+    for (int c = lane * 4; c < C; c += 128) {
+      float4 a = ld4(dyr + c), b = ld4(yr + c), d = ld4(dxr + c);
+      d.x += r * (a.x - b.x * dot);
+      d.y += r * (a.y - b.y * dot);
+      d.z += r * (a.z - b.z * dot);
+      d.w += r * (a.w - b.w * dot);
+      st4(dxr + c, d);
+      if (dx_act) {
+        st4(dx_act + row * C + c, d);
+        if (amax_bits)
+          am = fmaxf(am, fmaxf(fmaxf(fabsf(round_act<T>(d.x)), fabsf(round_act<T>(d.y))),
+                               fmaxf(fabsf(round_act<T>(d.z)), fabsf(round_act<T>(d.w)))));
+      }
+    }
   }
-  dot = warp_sum(dot) / (float)C;
-  const float r = rstd[row];
-  float* dxr = dx + row * C;
-  for (int c = lane * 4; c < C; c += 128) {
-    float4 a = ld4(dyr + c), b = ld4(yr + c), d = ld4(dxr + c);
-    d.x += r * (a.x - b.x * dot);
-    d.y += r * (a.y - b.y * dot);
-    d.z += r * (a.z - b.z * dot);
-    d.w += r * (a.w - b.w * dot);
-    st4(dxr + c, d);
-    if (dx_act) st4(dx_act + row * C + c, d);
+  if (amax_bits) {   // uniform across the block: every thread reaches this point
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+    if (lane == 0) wmax[threadIdx.x >> 5] = am;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float m = wmax[0];
+      for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, wmax[w]);
+      atomicMax(amax_bits, __float_as_uint(m));
+    }
   }
 }
 
@@ -198,10 +219,10 @@ nc_status launch_rmsnorm_fwd_t(int64_t rows, int C, const float* x, T* y, float*
 }
 template <typename T>
 nc_status launch_rmsnorm_bwd_t(int64_t rows, int C, const float* dy, const T* y, const float* rstd,
-                               float* dx, T* dx_act, cudaStream_t st) {
+                               float* dx, T* dx_act, cudaStream_t st, unsigned* amax_bits = nullptr) {
   if (rows <= 0) return NC_OK;
   if (C % 4 || (((uintptr_t)dy) & 15) || (((uintptr_t)dx) & 15) || (((uintptr_t)y) & 7)) return NC_ERR_ARG;
-  k_rmsnorm_bwd<T><<<cdiv(rows, 8), 256, 0, st>>>(rows, C, dy, y, rstd, dx, dx_act);
+  k_rmsnorm_bwd<T><<<cdiv(rows, 8), 256, 0, st>>>(rows, C, dy, y, rstd, dx, dx_act, dx_act ? amax_bits : nullptr);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
@@ -211,10 +232,10 @@ nc_status launch_rmsnorm_fwd(int dtype, int64_t rows, int C, const float* x, voi
   return launch_rmsnorm_fwd_t<float>(rows, C, x, (float*)y, rstd, eps, st, amax_bits);
 }
 nc_status launch_rmsnorm_bwd(int dtype, int64_t rows, int C, const float* dy, const void* y,
-                             const float* rstd, float* dx, void* dx_act, cudaStream_t st) {
+                             const float* rstd, float* dx, void* dx_act, cudaStream_t st, unsigned* amax_bits) {
   if (dtype == NC_BF16)
-    return launch_rmsnorm_bwd_t<bf16>(rows, C, dy, (const bf16*)y, rstd, dx, (bf16*)dx_act, st);
-  return launch_rmsnorm_bwd_t<float>(rows, C, dy, (const float*)y, rstd, dx, (float*)dx_act, st);
+    return launch_rmsnorm_bwd_t<bf16>(rows, C, dy, (const bf16*)y, rstd, dx, (bf16*)dx_act, st, amax_bits);
+  return launch_rmsnorm_bwd_t<float>(rows, C, dy, (const float*)y, rstd, dx, (float*)dx_act, st, amax_bits);
 }
 
 // ---------------------------------------------------------------- RoPE + QK-norm

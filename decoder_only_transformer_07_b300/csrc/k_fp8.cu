@@ -225,3 +225,41 @@ nc_status launch_fp8_quantize_multi(const OptTensors& tl, const float* master, f
   k_fp8_cast_multi<<<nb, FP8_THREADS, 0, st>>>(tl, master, stats, y);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
+
+// Transposed copies of the weight codes, for the input-gradient products
+// dX = dY W, whose B operand is W^T in the K-major layout the 8-bit GEMM
+// reads: codes [rows][cols] of tensor t at src + tl.soff[t] become
+// [cols][rows] at dst + tl.soff[t] (the same factor applies).  One block per
+// 64 x 64 tile through shared memory; partial edge tiles are bounds-checked.
+__global__ void __launch_bounds__(256) k_fp8_transpose_multi(const __grid_constant__ Fp8Transposes tt,
+                                                             const uint8_t* __restrict__ src, uint8_t* __restrict__ dst) {
+  __shared__ uint8_t tile[64][68];
+  int t = 0, lo = 0, hi = tt.n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tt.tile0[mid] <= (int)blockIdx.x) lo = mid; else hi = mid;
+  }
+  t = lo;
+  const int rows = tt.rows[t], cols = tt.cols[t];
+  const int tc = (cols + 63) / 64;
+  const int k = (int)blockIdx.x - tt.tile0[t];
+  const int r0 = (k / tc) * 64, c0 = (k % tc) * 64;
+  const uint8_t* s = src + tt.off[t];
+  uint8_t* d = dst + tt.off[t];
+  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
+    const int r = i >> 6, c = i & 63;
+    if (r0 + r < rows && c0 + c < cols) tile[r][c] = s[(int64_t)(r0 + r) * cols + c0 + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
+    const int c = i >> 6, r = i & 63;
+    if (r0 + r < rows && c0 + c < cols) d[(int64_t)(c0 + c) * rows + r0 + r] = tile[r][c];
+  }
+}
+
+nc_status launch_fp8_transpose_multi(const Fp8Transposes& tt, const uint8_t* src, uint8_t* dst, cudaStream_t st) {
+  const int nb = tt.tile0[tt.n];
+  if (nb <= 0) return NC_OK;
+  k_fp8_transpose_multi<<<nb, 256, 0, st>>>(tt, src, dst);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}

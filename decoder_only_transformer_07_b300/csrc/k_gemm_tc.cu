@@ -1168,14 +1168,16 @@ nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_
 // single-CTA kernel otherwise; no split-K.
 static nc_status gemm_fp8_impl(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
                                const float* scale_a, const float* scale_b, int ep, void* D, int64_t ldd,
-                               const TcRope* rope, int32_t* err, cudaStream_t st) {
+                               const TcRope* rope, int32_t* err, cudaStream_t st, const void* aux = nullptr,
+                               int64_t ldaux = 0) {
   if (M <= 0 || N <= 0) return NC_OK;
   if (K <= 0 || !A || !B || !D || !scale_a || !scale_b) return NC_ERR_ARG;
   if ((lda % 16) || (ldb % 16) || lda < K || ldb < K || (((uintptr_t)A) & 15) || (((uintptr_t)B) & 15))
     return NC_ERR_ARG;
   if (ep != NC_EP_STORE && ep != NC_EP_STORE_F32 && ep != NC_EP_ACCUM_F32 && ep != NC_EP_RELU2_SQ &&
-      ep != NC_EP_QKV_ROPE)
+      ep != NC_EP_RELU2_SQ_BWD && ep != NC_EP_QKV_ROPE)
     return NC_ERR_ARG;
+  if ((ep == NC_EP_RELU2_SQ_BWD) != (aux != nullptr)) return NC_ERR_ARG;
   if ((ep == NC_EP_QKV_ROPE) != (rope != nullptr)) return NC_ERR_ARG;
   const bool out_f32 = (ep == NC_EP_STORE_F32 || ep == NC_EP_ACCUM_F32);
   if (ldd < N || ((ldd * (out_f32 ? 4 : 2)) % 16) || (((uintptr_t)D) & 15)) return NC_ERR_ARG;
@@ -1216,6 +1218,12 @@ static nc_status gemm_fp8_impl(int M, int N, int K, const uint8_t* A, int64_t ld
   if (!make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, ldb, 128, pair ? 128 : BN)) return NC_ERR_CUDA;
   p.tma_epi = out_f32 ? make_tmap_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, N, M, ldd, 32, 32)
                       : make_tmap_bf16_2d(&td, D, N, M, ldd, 64, 32);
+  if (p.tma_epi && aux) {   // relu^2 backward: the saved relu(u)^2 arrives by TMA in the epilogue
+    if ((ldaux % 8) || (((uintptr_t)aux) & 15)) return NC_ERR_ARG;
+    p.aux = const_cast<void*>(aux);
+    p.ldaux = ldaux;
+    p.tma_epi = make_tmap_bf16_2d(&tx, aux, N, M, ldaux, 64, 32);
+  }
   if (!p.tma_epi) return NC_ERR_CUDA;
   if (pair) return launch_tc_pair<true>(p, ta, tb, td, tx, 0, st);
   if (BN == 256) return launch_tc_bn<256, true>(p, ta, tb, td, tx, 0, st);
@@ -1232,9 +1240,9 @@ nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, co
 nc_status launch_gemm_fp8_ep(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
                              const float* scale_a, const float* scale_b, int ep, void* D, int64_t ldd, int T, int nh,
                              int hd, const float* tab, int pair_rows, float* rstd, float eps, int32_t* err,
-                             cudaStream_t st) {
+                             cudaStream_t st, const void* aux, int64_t ldaux) {
   if (ep != NC_EP_QKV_ROPE)
-    return gemm_fp8_impl(M, N, K, A, lda, B, ldb, scale_a, scale_b, ep, D, ldd, nullptr, err, st);
+    return gemm_fp8_impl(M, N, K, A, lda, B, ldb, scale_a, scale_b, ep, D, ldd, nullptr, err, st, aux, ldaux);
   TcRope r{tab, rstd, T, nh, hd, pair_rows, eps};
   return gemm_fp8_impl(M, N, K, A, lda, B, ldb, scale_a, scale_b, ep, D, ldd, &r, err, st);
 }

@@ -43,8 +43,11 @@ struct nc_model {
   bool fp8 = false;                  // the blocks' forward linears on E4M3 operands
   uint8_t* q8a = nullptr;            // E4M3 codes of a linear layer's input [Nmax, max(C, F)]
   uint8_t* q8w = nullptr;            // E4M3 codes of every block weight operand, quantised once per step
-  float* q8s = nullptr;              // per layer and linear {amax bits, scale, scale_inv, -}: inputs [L][4], weights [L][4]
+  uint8_t* q8wT = nullptr;           // the same codes transposed ([in][out]): B operands of the dX products
+  float* q8s = nullptr;              // per layer and linear {amax bits, scale, scale_inv, -}: inputs [L][4],
+                                     // weights [L][4], output gradients dY [L][4]
   OptTensors* q8tl = nullptr;        // the 4 L weight operands (fp32 master offset, code offset, length)
+  Fp8Transposes* q8tt = nullptr;     // the same operands as [out][in] byte matrices, for the transpose
   int32_t* err = nullptr;            // device error flag
   float* result = nullptr;           // device: [0] loss, [1] error flag copy
   float* result_host = nullptr;      // pinned host copy
@@ -307,7 +310,7 @@ static nc_status allocate(nc_model* m) {
   NC_TRY(dalloc(m, (size_t)N * m->C * a, &m->xf));
   if (m->emb_norm) NC_TRY(dalloc_t(m, (size_t)N, &m->rstd_e));
   if (m->fp8) {
-    const int64_t kmax = std::max<int64_t>(m->C, m->F);
+    const int64_t kmax = std::max<int64_t>(std::max<int64_t>(m->C, m->F), std::max<int64_t>(m->qkvw, m->H * m->hd));
     NC_TRY(dalloc(m, (size_t)(N * kmax), (void**)&m->q8a));
     // the blocks' weight operands [Wq; Wk; Wv], Wo, Wfc, Wproj, each its own tensor
     if (4 * L > NC_OPT_MAXT) return NC_ERR_UNSUPPORTED;
@@ -315,14 +318,24 @@ static nc_status allocate(nc_model* m) {
     if (!m->q8tl) return NC_ERR_ALLOC;
     memset(m->q8tl, 0, sizeof(OptTensors));
     m->q8tl->n = 4 * L;
-    int32_t c = 0;
+    m->q8tt = new (std::nothrow) Fp8Transposes;
+    if (!m->q8tt) return NC_ERR_ALLOC;
+    memset(m->q8tt, 0, sizeof(Fp8Transposes));
+    m->q8tt->n = 4 * L;
+    int32_t c = 0, tiles = 0;
     int64_t so = 0;
     for (int l = 0; l < L; ++l) {
       const int64_t len[4] = {(int64_t)m->qkvw * m->C, (int64_t)m->C * m->H * m->hd, (int64_t)m->F * m->C,
                               (int64_t)m->C * m->F};
       const int which[4] = {0, 3, 4, 5};
+      const int rows[4] = {m->qkvw, m->C, m->F, m->C}, cols[4] = {m->C, m->H * m->hd, m->C, m->F};
       for (int k = 0; k < 4; ++k) {
         const int t = 4 * l + k;
+        m->q8tt->tile0[t] = tiles;
+        m->q8tt->off[t] = so;
+        m->q8tt->rows[t] = rows[k];
+        m->q8tt->cols[t] = cols[k];
+        tiles += ((rows[k] + 63) / 64) * ((cols[k] + 63) / 64);
         m->q8tl->chunk0[t] = c;
         m->q8tl->off[t] = tensor(m, l, which[k]).off;
         m->q8tl->soff[t] = so;
@@ -332,8 +345,10 @@ static nc_status allocate(nc_model* m) {
       }
     }
     m->q8tl->chunk0[4 * L] = c;
+    m->q8tt->tile0[4 * L] = tiles;
     NC_TRY(dalloc(m, (size_t)so, (void**)&m->q8w));
-    NC_TRY(dalloc_t(m, (size_t)32 * L, &m->q8s));
+    NC_TRY(dalloc(m, (size_t)so, (void**)&m->q8wT));
+    NC_TRY(dalloc_t(m, (size_t)48 * L, &m->q8s));
   }
   NC_TRY(dalloc_t(m, (size_t)N, &m->rstd_f));
   // logits chunk: at most 1 GiB of compute-dtype logits per chunk, whole 128-row tiles
@@ -387,6 +402,7 @@ extern "C" void nc_model_destroy(nc_model* m) {
   if (m->result_host) cudaFreeHost(m->result_host);
   delete m->opt_tl;
   delete m->q8tl;
+  delete m->q8tt;
   for (int k = 0; k < nc_model::NC_OPT_STREAMS; ++k) {
     if (m->opt_st[k]) cudaStreamDestroy(m->opt_st[k]);
     if (m->opt_join[k]) cudaEventDestroy(m->opt_join[k]);
@@ -526,7 +542,7 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
   // produced it has taken its maximum), then the E4M3 GEMM runs through the
   // layer's epilogue (RoPE + QK-norm with NC_EP_QKV_ROPE, else `ep`).
   if (m->fp8) {
-    NC_CUDA_TRY(cudaMemsetAsync(m->q8s, 0, (size_t)32 * m->L * sizeof(float), st));
+    NC_CUDA_TRY(cudaMemsetAsync(m->q8s, 0, (size_t)48 * m->L * sizeof(float), st));
     PROF(NC_PROF_QUANT, 0, 9.0 * (double)m->q8tl->soff[4 * m->L - 1],
          launch_fp8_quantize_multi(*m->q8tl, m->master, m->q8s + 16 * m->L, m->q8w, st));
     m->launches += 2;
@@ -602,6 +618,70 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
   return NC_OK;
 }
 
+// One block's backward in the 8-bit step.  The weight gradients dW = dY^T X
+// are the bf16 products of the unquantised operands; each input gradient
+// dX = dY W multiplies E4M3 operands: dY's bf16 value quantised per tensor
+// into q8a with its own statistics slot (the cast alone when the RMSNorm
+// backward that wrote it has taken its maximum), and W's forward codes read
+// transposed, with the forward's factor.
+static nc_status backward_layer_fp8(nc_model* m, int l, int B, int T, float* grads, int gw, cudaStream_t st) {
+  const int64_t N = (int64_t)B * T;
+  const int C = m->C, F = m->F, Hd = m->H * m->hd, W = m->qkvw;
+  const int n = (int)N;
+  const double a = (double)m->act;
+  const double attn_fl = 8.0 * B * m->H * m->hd * ((double)T * (T + 1) / 2.0);
+  const double nb_by = (double)N * (4.0 * C + a * C + 4 + 8.0 * C + a * C);
+  uint8_t* xn1 = layer_act(m, m->xn1, l, C);
+  uint8_t* xn2 = layer_act(m, m->xn2, l, C);
+  uint8_t* qkv = layer_act(m, m->qkv, l, W);
+  uint8_t* o = layer_act(m, m->o, l, Hd);
+  uint8_t* h = layer_act(m, m->h, l, F);
+  float* rstd1 = m->rstd1 + (size_t)l * m->Nmax;
+  float* rstd2 = m->rstd2 + (size_t)l * m->Nmax;
+  float* rstdqk = m->rstdqk + (size_t)l * m->Nmax * (m->H + m->Hkv);
+  float* lse = m->lse + (size_t)l * m->Nmax * m->H;
+  const ParamTensor &tq = tensor(m, l, 0), &to = tensor(m, l, 3), &tfc = tensor(m, l, 4), &tpj = tensor(m, l, 5);
+  auto slot = [&](int ll, int k) { return m->q8s + 32 * m->L + (4 * ll + k) * 4; };
+  auto dx8 = [&](int k, const void* dy, int K, int Nout, int ep, void* D, const void* aux, bool amax_ready) -> nc_status {
+    float* ys = slot(l, k);
+    const float* ws = m->q8s + 16 * m->L + (4 * l + k) * 4;
+    const uint8_t* wT = m->q8wT + m->q8tl->soff[4 * l + k];
+    if (!amax_ready) {
+      PROF(NC_PROF_QUANT, 0, 2.0 * N * K, launch_fp8_amax(NC_BF16, dy, N * K, ys, st));
+      m->launches += 1;
+    }
+    PROF(NC_PROF_QUANT, 0, 3.0 * N * K, launch_fp8_cast_scaled(NC_BF16, dy, N * K, m->q8a, ys, st));
+    const double out = ep == NC_EP_STORE_F32 ? 4.0 : (aux ? 4.0 : 2.0);
+    PROF_SUB(NC_PROF_GEMM, NC_PROF_GEMM_DX, 2.0 * N * Nout * K,
+             (double)N * K + (double)Nout * K + (double)N * Nout * out,
+             launch_gemm_fp8_ep(n, Nout, K, m->q8a, K, wT, K, ys + 2, ws + 2, ep, D, Nout, 0, 0, 0, nullptr, 0,
+                                nullptr, 0.f, m->err, st, aux, aux ? Nout : 0));
+    m->launches += 2;
+    return NC_OK;
+  };
+  // MLP: x2 = x1 + relu(xn2 Wfc^T)^2 Wproj^T
+  NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, F, n, m->dx_act, C, 0, h, F, 0, gw, grads + tpj.off, F, nullptr, 0, st));
+  NC_TRY(dx8(3, m->dx_act, C, F, NC_EP_RELU2_SQ_BWD, m->du, h, true));
+  NC_TRY(gemm(m, NC_PROF_GEMM_DW, F, C, n, m->du, F, 0, xn2, C, 0, gw, grads + tfc.off, C, nullptr, 0, st));
+  NC_TRY(dx8(2, m->du, F, C, NC_EP_STORE_F32, m->dxn, nullptr, false));
+  PROF(NC_PROF_NORM, 0, nb_by,
+       launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, xn2, rstd2, m->dx, m->dx_act, st, (unsigned*)slot(l, 1)));
+  // attention: x1 = x + o Wo^T
+  NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, Hd, n, m->dx_act, C, 0, o, Hd, 0, gw, grads + to.off, Hd, nullptr, 0, st));
+  NC_TRY(dx8(1, m->dx_act, C, Hd, NC_EP_STORE, m->dout, nullptr, true));
+  PROF(NC_PROF_ATTN_BWD, attn_fl, (double)N * (2.0 * W + 2.0 * Hd) * a + 8.0 * N * m->H,
+       attn_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, rstdqk,
+                m->rope_pairs ? m->rope_pairs : m->rope_tab, m->rope_pairs ? m->Tmax : 0, m->err, st));
+  NC_TRY(gemm(m, NC_PROF_GEMM_DW, W, C, n, m->dqkv, W, 0, xn1, C, 0, gw, grads + tq.off, C, nullptr, 0, st));
+  NC_TRY(dx8(0, m->dqkv, W, C, NC_EP_STORE_F32, m->dxn, nullptr, false));
+  // the block's input gradient is the previous block's output gradient: its maximum, for that block's Wproj product
+  PROF(NC_PROF_NORM, 0, nb_by,
+       launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, xn1, rstd1, m->dx, m->dx_act, st,
+                          l > 0 ? (unsigned*)slot(l - 1, 3) : nullptr));
+  m->launches += 2 + 3;   // the two norms and the attention backward's three kernels
+  return NC_OK;
+}
+
 // accumulate: the weight gradients are added to `grads` instead of stored.
 static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int T, float* grads, bool accumulate,
                                  cudaStream_t st) {
@@ -625,6 +705,10 @@ static nc_status backward_layers(nc_model* m, const int32_t* tokens, int B, int 
     float* lse = m->lse + (size_t)l * m->Nmax * m->H;
     const ParamTensor &tq = tensor(m, l, 0), &to = tensor(m, l, 3), &tfc = tensor(m, l, 4),
                       &tpj = tensor(m, l, 5);
+    if (m->fp8) {
+      NC_TRY(backward_layer_fp8(m, l, B, T, grads, gw, st));
+      continue;
+    }
     // MLP: x2 = x1 + relu(xn2 Wfc^T)^2 Wproj^T
     NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, F, n, m->dx_act, C, 0, h, F, 0, gw, grads + tpj.off, F, nullptr, 0, st));
     NC_TRY(gemm(m, NC_PROF_GEMM_DX, n, F, C, m->dx_act, C, 1, wptr(m, tpj), F, 0, NC_EP_RELU2_SQ_BWD, m->du, F, h, F, st));
@@ -694,9 +778,18 @@ static nc_status step(nc_model* m, const int32_t* tokens, const int32_t* targets
                 grads + tl.off, C, nullptr, 0, st));
     m->launches += 1;
   }
+  // the 8-bit step's dX products read the weight codes transposed, and the
+  // final norm takes the maximum of the last block's output gradient
+  unsigned* amax_last = nullptr;
+  if (m->fp8) {
+    PROF(NC_PROF_QUANT, 0, 2.0 * (double)m->q8tl->soff[4 * m->L - 1],
+         launch_fp8_transpose_multi(*m->q8tt, m->q8w, m->q8wT, st));
+    m->launches += 1;
+    amax_last = (unsigned*)(m->q8s + 32 * m->L + (4 * (m->L - 1) + 3) * 4);
+  }
   PROF(NC_PROF_NORM, 0, (double)N * (4.0 * C + m->act * C + 4 + 8.0 * C + (m->dtype == NC_BF16 ? m->act * C : 0)),
        launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, m->xf, m->rstd_f, m->dx, m->dtype == NC_BF16 ? m->dx_act : nullptr,
-                          st));
+                          st, amax_last));
   m->launches += 1;
   NC_TRY(backward_layers(m, tokens, B, T, grads, accumulate, st));
   PROF(NC_PROF_OTHER, 0, 4.0 * N, launch_mean(N, m->rowloss, m->result, st));

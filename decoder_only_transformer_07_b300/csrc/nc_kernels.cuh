@@ -13,8 +13,10 @@ nc_status launch_rope_table(int T, int hd, float base, float* tab, float* pairs,
 // amax_bits (optional, pre-zeroed): atomic maximum of |y| as stored, float bits (8-bit quantiser input).
 nc_status launch_rmsnorm_fwd(int dtype, int64_t rows, int C, const float* x, void* y, float* rstd,
                              float eps, cudaStream_t st, unsigned* amax_bits = nullptr);
+// amax_bits (optional, with dx_act): atomic maximum of |dx_act| as stored, float bits.
 nc_status launch_rmsnorm_bwd(int dtype, int64_t rows, int C, const float* dy, const void* y,
-                             const float* rstd, float* dx, void* dx_act, cudaStream_t st);
+                             const float* rstd, float* dx, void* dx_act, cudaStream_t st,
+                             unsigned* amax_bits = nullptr);
 // pos0 (device, may be NULL): positions are *pos0 + row % T instead of row % T.
 // kc, vc (both or neither): also write every row's rotated, normalised k heads
 // and its v heads into a [B][Hkv][max_len][hd] cache at the row's position.
@@ -77,12 +79,13 @@ nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, co
                           const float* scale_a, const float* scale_b, int out_f32, void* D, int64_t ldd,
                           int32_t* err, cudaStream_t st);
 // The 8-bit GEMM through a step epilogue: NC_EP_STORE, NC_EP_STORE_F32,
-// NC_EP_ACCUM_F32, NC_EP_RELU2_SQ, or NC_EP_QKV_ROPE (then T, nh, hd, tab,
+// NC_EP_ACCUM_F32, NC_EP_RELU2_SQ, NC_EP_RELU2_SQ_BWD (with aux, bf16
+// relu(u)^2, row pitch ldaux), or NC_EP_QKV_ROPE (then T, nh, hd, tab,
 // pair_rows, rstd and eps as for launch_gemm_tc_qkv_rope; ignored otherwise).
 nc_status launch_gemm_fp8_ep(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
                              const float* scale_a, const float* scale_b, int ep, void* D, int64_t ldd, int T, int nh,
                              int hd, const float* tab, int pair_rows, float* rstd, float eps, int32_t* err,
-                             cudaStream_t st);
+                             cudaStream_t st, const void* aux = nullptr, int64_t ldaux = 0);
 // Per-tensor E4M3 quantisation of n fp32 / bf16 values: stats (device, 3
 // floats) gets {amax, scale, scale_inv}; y the codes.
 nc_status launch_quantize_fp8(int dtype, const void* x, int64_t n, uint8_t* y, float* stats, cudaStream_t st);
@@ -135,6 +138,15 @@ struct OptTensors {
   int64_t len[NC_OPT_MAXT];    // elements
   float* norm;                 // device [n]: ||U||_F per tensor (written by launch_muon_momentum)
 };
+// Tensors whose 8-bit codes are transposed for the backward: tensor t is
+// [rows[t]][cols[t]] bytes at offset off[t]; tile0 counts 64 x 64 tiles.
+struct Fp8Transposes {
+  int32_t n;
+  int32_t tile0[NC_OPT_MAXT + 1];
+  int64_t off[NC_OPT_MAXT];
+  int32_t rows[NC_OPT_MAXT], cols[NC_OPT_MAXT];
+};
+nc_status launch_fp8_transpose_multi(const Fp8Transposes& tt, const uint8_t* src, uint8_t* dst, cudaStream_t st);
 // Every tensor t of tl at once (fp32 master + tl.off[t], tl.len[t] elements):
 // stats + 4 t as above (stats[4 t] zeroed beforehand), codes at y + tl.soff[t].
 nc_status launch_fp8_quantize_multi(const OptTensors& tl, const float* master, float* stats, uint8_t* y,

@@ -3,12 +3,14 @@
 Recipe (the reading of woshipm nanochat analysis §一.2 and §六.2, which name
 FP8 without one): the blocks' four linear layers multiply E4M3 operands in
 the forward, the bf16 activation and the fp32 master weight quantised per
-tensor with current scaling; the backward is the bf16 one with the
+tensor with current scaling; their input gradients dX = dY W multiply E4M3
+operands too (dY's bf16 value with its own per-tensor scale, W's forward
+codes read transposed); the weight gradients are bf16 products of the
 unquantised operands.
 
 Tolerances.  Both sides quantise the same fp32 master weights, so the weight
-codes agree; the activation codes come from activations that differ by the
-bf16 path's rounding (about 2^-9 relative).  E4M3 codes are 2^-3 apart, so a
+codes agree; the activation and output-gradient codes come from tensors that
+differ by the bf16 path's rounding (about 2^-9 relative).  E4M3 codes are 2^-3 apart, so a
 few per cent of the activation codes land one step apart between the two
 evaluations: per element the two forwards then differ by about
 sqrt(0.03) * 2^-3 ~ 2 % of an operand, some twenty times the bf16 path's
