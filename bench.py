@@ -481,7 +481,7 @@ def measure(w, name, args, world, rank, dev, gpu_traffic=True, fp8=False):
     """Time `args.steps` training steps of workload w (device-resident inputs),
     then the same through the host-buffer entry point; returns the fields of
     the bench line for this workload.  fp8: the 8-bit step (the blocks'
-    forward linears on E4M3 operands)."""
+    forward and input-gradient linears on E4M3 operands)."""
     import ctypes
     import torch
     import decoder_only_transformer_07_b300 as nc

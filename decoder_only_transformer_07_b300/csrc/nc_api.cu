@@ -40,7 +40,7 @@ struct nc_model {
   float softcap = 0.f;               // logit soft-cap c (0: off)
   bool emb_norm = false;             // RMSNorm after the embedding lookup
   float* rstd_e = nullptr;           // [Nmax] its per-row rstd (emb_norm only)
-  bool fp8 = false;                  // the blocks' forward linears on E4M3 operands
+  bool fp8 = false;                  // the blocks' forward and dX linears on E4M3 operands
   uint8_t* q8a = nullptr;            // E4M3 codes of a linear layer's input [Nmax, max(C, F)]
   uint8_t* q8w = nullptr;            // E4M3 codes of every block weight operand, quantised once per step
   uint8_t* q8wT = nullptr;           // the same codes transposed ([in][out]): B operands of the dX products

@@ -69,9 +69,12 @@ typedef struct {
    * operands in the forward: the bf16 input activation and the fp32 master
    * weight are each quantised per tensor with current scaling (the
    * nc_op_quantize_fp8 rule; [Wq; Wk; Wv] is one tensor), products
-   * accumulate in fp32 and are dequantised in the fused epilogues.  The
-   * backward is the bf16 one with the unquantised operands (the quantisers
-   * pass gradients through unchanged).  NC_BF16 only; n_embd and mlp_hidden
+   * accumulate in fp32 and are dequantised in the fused epilogues.  In the
+   * backward their input gradients dX = dY W multiply E4M3 operands as well
+   * (dY's bf16 value with its own per-tensor scale, W's forward codes read
+   * transposed); the weight gradients are bf16 products of the unquantised
+   * operands (the quantisers pass gradients through unchanged).  The
+   * lm_head, attention and norms stay bf16.  NC_BF16 only; n_embd and mlp_hidden
    * multiples of 16; decoding (nc_kv_cache_create) is not offered.  0: off.  */
   int32_t fp8;
 } nc_config;
