@@ -344,17 +344,18 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       // (Moving a quarter of the exponentials to an FMA-pipe polynomial measured
       // 10 % slower: the softmax warps' issue slots, shared with the MMA-issuing
       // threads, bound this loop rather than the SFU.)
+      // (two scores per FFMA2 / FADD2 instruction)
       const float mc = m * sh.scale_log2;
-      float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const float2 sl2 = make_float2(sh.scale_log2, sh.scale_log2), nmc = make_float2(-mc, -mc);
+      float2 s4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < 64; ++c) {   // packed in place: x[c] <- bf16x2(p[2c], p[2c+1])
-        const float p0 = ex2_approx(fmaf(__uint_as_float(x[2 * c]), sh.scale_log2, -mc));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(x[2 * c + 1]), sh.scale_log2, -mc));
-        s8[(2 * c) & 7] += p0;
-        s8[(2 * c + 1) & 7] += p1;
-        x[c] = pack2(p0, p1);
+        const float2 a = fma2(make_float2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])), sl2, nmc);
+        const float2 p = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+        s4[c & 3] = add2(s4[c & 3], p);
+        x[c] = pack2(p.x, p.y);
       }
-      const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+      const float sum = ((s4[0].x + s4[0].y) + (s4[1].x + s4[1].y)) + ((s4[2].x + s4[2].y) + (s4[3].x + s4[3].y));
       // P_i into the first 64 columns of S_i (this warp's lanes, already read)
       tmem_st_32x32b_x32(tS, x);
       tmem_st_32x32b_x32(tS + 32, x + 32);
@@ -744,11 +745,20 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       if (lane == 0) mbar_arrive(sdp_free);
       const int k0 = j * 128 + 64 * hf;
       const bool diag = (j == qt) || (j * 128 + 128 > sh.T);
+      // two scores per FFMA2 / FADD2 / FMUL2 instruction
+      const float2 sl2 = make_float2(sh.scale_log2, sh.scale_log2), nl2 = make_float2(-lse2, -lse2),
+                   d2 = make_float2(Dr, Dr);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float p = ex2_approx(__uint_as_float(s[c]) * sh.scale_log2 - lse2);
-        if (diag && (k0 + c > qpos || k0 + c >= sh.T)) p = 0.f;
-        s[c] = __float_as_uint(p * (__uint_as_float(dp[c]) - Dr));
+      for (int c = 0; c < 64; c += 2) {
+        const float2 a = fma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2, nl2);
+        float2 p = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+        if (diag) {
+          if (k0 + c > qpos || k0 + c >= sh.T) p.x = 0.f;
+          if (k0 + c + 1 > qpos || k0 + c + 1 >= sh.T) p.y = 0.f;
+        }
+        const float2 ds = mul2(p, sub2(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), d2));
+        s[c] = __float_as_uint(ds.x);
+        s[c + 1] = __float_as_uint(ds.y);
       }
 #pragma unroll
       for (int c = 0; c < 32; ++c) s[c] = pack2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
@@ -932,7 +942,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int r = quarter * 32 + lane;
     const int key = kt * 128 + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    // lse * log2(e) and D of this warp's 32 queries: lane e fetches query e's
+    // -lse * log2(e) and D of this warp's 32 queries: lane e fetches query e's
     // pair one step ahead (into registers), and the warp shares them through its
     // own 256-byte slot of shared memory (rows past the end get P = 0)
     float* ld = reinterpret_cast<float*>(smem + L::OFF_LD) + (warp - 4) * 64;
@@ -952,7 +962,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       uint32_t st[32], dp[32];
       tmem_ld_32x32b_x32(tbase + lane_off + buf * 64 + 32 * hf, st);
       tmem_ld_32x32b_x32(tbase + lane_off + 128 + buf * 64 + 32 * hf, dp);
-      ld[lane] = nl;
+      ld[lane] = -nl;
       ld[32 + lane] = nd;
       __syncwarp();
       if (i + 1 < n) fetch(i + 1, nl, nd);
@@ -961,17 +971,27 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       const bool diag = step_q0(i) < kt * 128 + 128;
       const float4* ld4 = reinterpret_cast<const float4*>(ld);
       const float4* dd4 = reinterpret_cast<const float4*>(ld + 32);
+      // two queries per FFMA2 / FADD2 / FMUL2 instruction
+      const float2 sl2 = make_float2(sh.scale_log2, sh.scale_log2);
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 l4 = ld4[c4], d4 = dd4[c4];
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 4; e += 2) {
           const int c = 4 * c4 + e;
-          float p = ex2_approx(__uint_as_float(st[c]) * sh.scale_log2 - lv[e]);
-          if (diag && q0 + c < key) p = 0.f;
-          st[c] = __float_as_uint(p);
-          dp[c] = __float_as_uint(p * (__uint_as_float(dp[c]) - dv[e]));
+          const float2 nl2 = e ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
+          const float2 dv2 = e ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+          const float2 a = fma2(make_float2(__uint_as_float(st[c]), __uint_as_float(st[c + 1])), sl2, nl2);
+          float2 p = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+          if (diag) {
+            if (q0 + c < key) p.x = 0.f;
+            if (q0 + c + 1 < key) p.y = 0.f;
+          }
+          const float2 ds = mul2(p, sub2(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), dv2));
+          st[c] = __float_as_uint(p.x);
+          st[c + 1] = __float_as_uint(p.y);
+          dp[c] = __float_as_uint(ds.x);
+          dp[c + 1] = __float_as_uint(ds.y);
         }
       }
       // P^T and dS^T as bf16 pairs into the S^T and dP^T columns this warp just read
