@@ -437,9 +437,34 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 // (RMSNorm backward), and for its half of the rotation pairs (i, i + HD/2)
 // writes dx_i = dr_i cos - dr_{i+d} sin, dx_{i+d} = dr_i sin + dr_{i+d} cos
 // (the transpose of the forward rotation at the row's position).
+// What the fused output reads from global memory besides the accumulator: the
+// row's q/k-norm rstd and its half of the rotation table.  at_out_prefetch
+// loads them before the last products complete, so that their L2 round trips
+// overlap the tensor core's tail instead of following it.
+template <int HD>
+struct AtOutPre {
+  float rr;
+  float4 t[HD / 8];   // (cos_i, sin_i, cos_i+1, sin_i+1) for the thread's HD / 4 rotation pairs
+};
+template <int HD>
+__device__ __forceinline__ void at_out_prefetch(const AtShape& sh, int hf, bool valid, int pos, int64_t token,
+                                                int head, AtOutPre<HD>& pre) {
+  constexpr int PW = HD / 4;
+  pre.rr = 0.f;
+#pragma unroll
+  for (int k = 0; k < PW / 2; ++k) pre.t[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!sh.rope_tab || !valid) return;   // rows past the end read nothing (the table may end at T)
+  pre.rr = sh.rstd_qk[token * (sh.H + sh.Hkv) + head];
+  const size_t cstep = sh.rope_pair_rows ? (size_t)sh.rope_pair_rows : 1;
+  const float4* cs = reinterpret_cast<const float4*>(sh.rope_tab) +
+                     (sh.rope_pair_rows ? (size_t)pos : (size_t)pos * (HD / 4)) + (size_t)((hf * PW) >> 1) * cstep;
+#pragma unroll
+  for (int k = 0; k < PW / 2; ++k) pre.t[k] = __ldg(cs + (size_t)k * cstep);
+}
+
 template <int HD>
 __device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, const uint8_t* ytile, int r, int hf,
-                                            bool valid, int pos, int64_t token, int head, bf16* dst) {
+                                            bool valid, const AtOutPre<HD>& pre, bf16* dst) {
   if (!sh.rope_tab) {
 #pragma unroll 1
     for (int c = 0; c < HD / 64; ++c) {
@@ -483,12 +508,7 @@ __device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, co
     }
   }
   dot *= sh.scale / (float)HD;
-  // in range for every row (rows past the end are skipped below); the warp
-  // reconverges before the aligned TMEM loads
-  const int64_t ri = (valid ? token : 0) * (sh.H + sh.Hkv) + head;
-  float rr = 0.f;
-  if (valid) rr = sh.rstd_qk[ri];
-  __syncwarp();
+  const float rr = pre.rr;
   const int i0 = hf * PW;
   uint32_t g1[PW], g2[PW];
   if constexpr (PW == 32) {
@@ -500,9 +520,6 @@ __device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, co
   }
   tmem_ld_wait();
   if (!valid) return;
-  const size_t cstep = sh.rope_pair_rows ? (size_t)sh.rope_pair_rows : 1;
-  const float4* cs = reinterpret_cast<const float4*>(sh.rope_tab) +
-                     (sh.rope_pair_rows ? (size_t)pos : (size_t)pos * (HD / 4)) + (size_t)(i0 >> 1) * cstep;
 #pragma unroll
   for (int q = 0; q < PW; q += 8) {
     float y1[8], y2[8], o1[8], o2[8];
@@ -510,7 +527,7 @@ __device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, co
     y8(D + i0 + q, y2);
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
-      const float4 t = __ldg(cs + (size_t)((q + e) >> 1) * cstep);   // cos_i, sin_i, cos_i+1, sin_i+1
+      const float4 t = pre.t[(q + e) >> 1];   // cos_i, sin_i, cos_i+1, sin_i+1
       const float a0 = rr * (__uint_as_float(g1[q + e]) * sh.scale - y1[e] * dot);
       const float a1 = rr * (__uint_as_float(g1[q + e + 1]) * sh.scale - y1[e + 1] * dot);
       const float b0 = rr * (__uint_as_float(g2[q + e]) * sh.scale - y2[e] * dot);
@@ -768,6 +785,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ds_full[j & 1]);
     }
+    AtOutPre<HD> pre;
+    at_out_prefetch<HD>(sh, hf, ok && valid, qpos, (int64_t)row0 + qpos, h, pre);
     if (ok && at_wait_warp(dq_done, 0, sh, abort_flag)) {
       tc_fence_after();
       if (HD == 128 && !sh.rope_tab) {
@@ -776,7 +795,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                       h * HD + hf * 64, qt * 128 + quarter * 32, b, sh.T);
         if (lane == 0) bulk_wait_all();
       } else {
-        at_out_tile<HD>(sh, tbase + lane_off + 384, smem + L::OFF_Q, r, hf, valid, qpos, (int64_t)row0 + qpos, h,
+        at_out_tile<HD>(sh, tbase + lane_off + 384, smem + L::OFF_Q, r, hf, valid, pre,
                         dqkv + (int64_t)(row0 + qpos) * sh.ld_qkv + (int64_t)h * HD);
       }
     }
@@ -1006,9 +1025,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       __syncwarp();   // also: every lane has read the slot before the next step overwrites it
       if (lane == 0) mbar_arrive(&pt_full[buf]);
     }
+    const bool valid = key < sh.T;
+    AtOutPre<HD> pre;
+    at_out_prefetch<HD>(sh, hf, ok && valid, key, (int64_t)row0 + key, sh.H + g, pre);
     if (ok && at_wait_warp(dkv_done, 0, sh, abort_flag)) {
       tc_fence_after();
-      const bool valid = key < sh.T;
       if constexpr (HD == 128) {
         // dV, then dK (carries 1/sqrt(hd)), staged in the Q / dO stages, free
         // once every product has completed; a fused dK leaves through the k-norm
@@ -1020,8 +1041,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           at_out_box128(tbase + lane_off + 256 + HD, hf, sh.scale, smem + L::OFF_QS + 32768 + w8 * 4096, &tm_out,
                         (sh.H + g) * HD + hf * 64, kt * 128 + quarter * 32, b, sh.T);
         else
-          at_out_tile<HD>(sh, tbase + lane_off + 256 + HD, smem + L::OFF_K, r, hf, valid, key, (int64_t)row0 + key,
-                          sh.H + g, dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + g) * HD);
+          at_out_tile<HD>(sh, tbase + lane_off + 256 + HD, smem + L::OFF_K, r, hf, valid, pre,
+                          dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + g) * HD);
         if (lane == 0) bulk_wait_all();
       } else {
       bf16* dv = dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + sh.Hkv + g) * HD + hf * (HD / 2);
@@ -1043,8 +1064,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
       }
       // dK (carries 1/sqrt(hd)), through the k-norm and rotation backward when fused
-      at_out_tile<HD>(sh, tbase + lane_off + 256 + HD, smem + L::OFF_K, r, hf, valid, key, (int64_t)row0 + key,
-                      sh.H + g, dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + g) * HD);
+      at_out_tile<HD>(sh, tbase + lane_off + 256 + HD, smem + L::OFF_K, r, hf, valid, pre,
+                      dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + g) * HD);
       }
     }
   }
