@@ -101,6 +101,7 @@ _SIGS = {
     "nc_op_embed_bwd": (_i32, [_i64, _i32, _i32, _p, _p, _p, _p, _p]),
     "nc_debug_set_wait_limit_ns": (None, [_u64]),
     "nc_debug_set_gemm_pair": (None, [_i32]),
+    "nc_debug_set_ns_batched": (None, [_i32]),
     "nc_debug_stall_next_gemm": (None, [_i32]),
     "nc_debug_set_decode_graph": (None, [_i32]),
     "nc_op_gemm_rows": (_i32, [_i32, _i32, _i32, _i32, _p, _i64, _p, _i64, _i32, _p, _i64, _p]),

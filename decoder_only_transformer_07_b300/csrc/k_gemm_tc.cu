@@ -47,6 +47,11 @@ struct TcParams {
   void* aux;
   int64_t ldaux;
   int tiles_m, tiles_n, num_kb;
+  // Batched products (the NC_EP_STORE epilogue only): `batch` independent
+  // problems of the same shape stacked along the outer (row) dimension of each
+  // tensor map, problem b's rows starting b * {a,b,d}_bro rows further.  0 or 1:
+  // a single problem.
+  int batch, a_bro, b_bro, d_bro;
   int32_t* err;
   uint64_t wait_ns;
   int stall;               // test hook: the MMA issuer waits on a barrier nothing completes (single-CTA kernel)
@@ -79,7 +84,7 @@ struct TcSeg {
 struct TcSegIter {
   int u, stride, units, tiles;
   __device__ TcSegIter(const TcParams& p, int cta, int grid) {
-    tiles = p.tiles_m * p.tiles_n;
+    tiles = p.tiles_m * p.tiles_n * (p.batch > 1 ? p.batch : 1);
     units = tiles * p.splits;
     u = cta - grid;
     stride = grid;
@@ -130,6 +135,14 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn, int k) {
 #else
   return smem_desc(base + 2048u * k, 8192u, 1024u);
 #endif
+}
+
+__device__ __forceinline__ void tile_coords(const TcParams& p, int t, int& tm, int& tn);
+// Tile t of a batched launch: problem b, then the problem's own tile order.
+__device__ __forceinline__ void tile_coords_b(const TcParams& p, int t, int& b, int& tm, int& tn) {
+  const int per = p.tiles_m * p.tiles_n;
+  b = t / per;
+  tile_coords(p, t - b * per, tm, tn);
 }
 
 __device__ __forceinline__ void tile_coords(const TcParams& p, int t, int& tm, int& tn) {
@@ -506,8 +519,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     TcSegIter it(p, blockIdx.x, gridDim.x);
     TcSeg sg;
     while (!*abort_flag && it.next(p, sg)) {
-      int tm, tn;
-      tile_coords(p, sg.t, tm, tn);
+      int b, tm, tn;
+      tile_coords_b(p, sg.t, b, tm, tn);
+      const int ya = b * p.a_bro, yb = b * p.b_bro;   // the problem's first row in each map
       for (int kb = sg.k0; kb < sg.k1; ++kb) {
         if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, p.wait_ns)) { fail(); break; }
         if (*abort_flag) break;
@@ -516,16 +530,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         mbar_arrive_expect_tx(&full_bar[stage], Cfg::STAGE_BYTES);
         const int k0 = kb * (F8 ? 2 * TC_BK : TC_BK);   // elements: 128 bytes of K per slot
         if (!p.a_mn) {
-          tma_load_2d(sa, &tmA, &full_bar[stage], k0, tm * TC_BM);
+          tma_load_2d(sa, &tmA, &full_bar[stage], k0, tm * TC_BM + ya);
         } else {
-          tma_load_2d(sa, &tmA, &full_bar[stage], tm * TC_BM, k0);
-          tma_load_2d(sa + 8192, &tmA, &full_bar[stage], tm * TC_BM + 64, k0);
+          tma_load_2d(sa, &tmA, &full_bar[stage], tm * TC_BM, k0 + ya);
+          tma_load_2d(sa + 8192, &tmA, &full_bar[stage], tm * TC_BM + 64, k0 + ya);
         }
         if (!p.b_mn) {
-          tma_load_2d(sb, &tmB, &full_bar[stage], k0, tn * BN);
+          tma_load_2d(sb, &tmB, &full_bar[stage], k0, tn * BN + yb);
         } else {
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, &tmB, &full_bar[stage], tn * BN + 64 * j, k0);
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(sb + 8192 * j, &tmB, &full_bar[stage], tn * BN + 64 * j, k0 + yb);
         }
         ++issued;
         if (++stage == S) { stage = 0; phase ^= 1; }
@@ -588,8 +603,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     TcSegIter it(p, blockIdx.x, gridDim.x);
     TcSeg sg;
     for (; !*abort_flag && it.next(p, sg); ++local) {
-      int tm, tn;
-      tile_coords(p, sg.t, tm, tn);
+      int b, tm, tn;
+      tile_coords_b(p, sg.t, b, tm, tn);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait_bounded(&acc_full[acc], acc_phase, p.wait_ns)) { fail(); break; }
@@ -609,7 +624,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                     F8 ? __ldg(p.scale_a) * __ldg(p.scale_b) : 1.f);
       } else if (p.tma_epi && !part) {
         if (!tc_epilogue_staged<BN, F8>(p, p.ep, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
-                                        tn * BN + c_lo, p.N, m0, lane)) {
+                                        tn * BN + c_lo, p.N, m0 + b * p.d_bro, lane)) {
           fail();
           break;
         }
@@ -742,9 +757,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     TcSegIter it(p, cluster, nclusters);
     TcSeg sg;
     while (!*abort_flag && it.next(p, sg)) {
-      int tm, tn;
-      tile_coords(p, sg.t, tm, tn);
+      int b, tm, tn;
+      tile_coords_b(p, sg.t, b, tm, tn);
       const int arow = tm * 256 + (int)rank * 128, brow = tn * BN + (int)rank * 128;
+      const int ya = b * p.a_bro, yb = b * p.b_bro;   // the problem's first row in each map
       for (int kb = sg.k0; kb < sg.k1; ++kb) {
         if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, p.wait_ns)) { fail(); break; }
         if (*abort_flag) break;
@@ -757,16 +773,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
         for (int kc = 0; kc < 2; ++kc) {
           if (!p.a_mn) {
-            tma_load_2d_pair(sa + kc * 16384, &tmA, fb, k0 + 64 * KE * kc, arow);
+            tma_load_2d_pair(sa + kc * 16384, &tmA, fb, k0 + 64 * KE * kc, arow + ya);
           } else {
-            tma_load_2d_pair(sa + kc * 16384, &tmA, fb, arow, k0 + 64 * kc);
-            tma_load_2d_pair(sa + kc * 16384 + 8192, &tmA, fb, arow + 64, k0 + 64 * kc);
+            tma_load_2d_pair(sa + kc * 16384, &tmA, fb, arow, k0 + 64 * kc + ya);
+            tma_load_2d_pair(sa + kc * 16384 + 8192, &tmA, fb, arow + 64, k0 + 64 * kc + ya);
           }
           if (!p.b_mn) {
-            tma_load_2d_pair(sb + kc * 16384, &tmB, fb, k0 + 64 * KE * kc, brow);
+            tma_load_2d_pair(sb + kc * 16384, &tmB, fb, k0 + 64 * KE * kc, brow + yb);
           } else {
-            tma_load_2d_pair(sb + kc * 16384, &tmB, fb, brow, k0 + 64 * kc);
-            tma_load_2d_pair(sb + kc * 16384 + 8192, &tmB, fb, brow + 64, k0 + 64 * kc);
+            tma_load_2d_pair(sb + kc * 16384, &tmB, fb, brow, k0 + 64 * kc + yb);
+            tma_load_2d_pair(sb + kc * 16384 + 8192, &tmB, fb, brow + 64, k0 + 64 * kc + yb);
           }
         }
         if (++stage == S) { stage = 0; phase ^= 1; }
@@ -821,8 +837,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     TcSegIter it(p, cluster, nclusters);
     TcSeg sg;
     for (; !*abort_flag && it.next(p, sg); ++local) {
-      int tm, tn;
-      tile_coords(p, sg.t, tm, tn);
+      int b, tm, tn;
+      tile_coords_b(p, sg.t, b, tm, tn);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait_bounded(&acc_full[acc], acc_phase, p.wait_ns)) { fail(); break; }
@@ -846,7 +862,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
                                     F8 ? __ldg(p.scale_a) * __ldg(p.scale_b) : 1.f);
       } else if (p.tma_epi) {
         if (!tc_epilogue_staged<BN, F8>(p, p.ep, &tmD, &tmAux, stg, &aux_bar[warp - 4], aux_phase, taddr + c_lo,
-                                        tn * BN + c_lo, p.N, m0, lane)) {
+                                        tn * BN + c_lo, p.N, m0 + b * p.d_bro, lane)) {
           fail();
           break;
         }
@@ -967,7 +983,7 @@ static nc_status launch_tc_bn(TcParams p, const CUtensorMap& ta, const CUtensorM
     NC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<BN>::SMEM));
     attr_set = true;
   }
-  const int tiles = p.tiles_m * p.tiles_n;
+  const int tiles = p.tiles_m * p.tiles_n * (p.batch > 1 ? p.batch : 1);
   // Split K when whole tiles would leave the last wave badly filled (fp32
   // outputs only: the weight gradients and the lm_head input gradient, whose
   // K is the token count or the vocabulary).  Cost model per split count S:
@@ -1032,7 +1048,7 @@ static nc_status launch_tc_pair(TcParams p, const CUtensorMap& ta, const CUtenso
   p.num_kb = (p.K + bk - 1) / bk;
   p.splits = 1;
   p.kps = p.num_kb;
-  const int tiles = p.tiles_m * p.tiles_n;
+  const int tiles = p.tiles_m * p.tiles_n * (p.batch > 1 ? p.batch : 1);
   // Split K when whole 256 x 256 tiles would leave the last wave of clusters
   // badly filled (fp32 outputs only: the weight gradients, whose K is the token
   // count).  Cost per split count S: waves(S) * (k-blocks per slice) * t_kb plus
@@ -1082,8 +1098,9 @@ struct TcRope {
 
 static nc_status gemm_tc_impl(int M, int N, int K, const bf16* A, int64_t lda, int a_kmajor, const bf16* B,
                               int64_t ldb, int b_kmajor, int ep, void* D, int64_t ldd, void* aux, int64_t ldaux,
-                              const TcRope* rope, int32_t* err, void* ws, size_t ws_bytes, cudaStream_t st) {
-  if (M <= 0 || N <= 0) return NC_OK;
+                              const TcRope* rope, int32_t* err, void* ws, size_t ws_bytes, cudaStream_t st,
+                              int batch = 1, int64_t a_bro = 0, int64_t b_bro = 0, int64_t d_bro = 0) {
+  if (M <= 0 || N <= 0 || batch <= 0) return NC_OK;
   if (K <= 0) return NC_ERR_ARG;
   if ((lda % 8) || (ldb % 8) || (((uintptr_t)A) & 15) || (((uintptr_t)B) & 15)) return NC_ERR_ARG;
   if (!D || ((ep == NC_EP_RELU2 || ep == NC_EP_RELU2_BWD || ep == NC_EP_RELU2_SQ_BWD) && !aux))
@@ -1102,6 +1119,8 @@ static nc_status gemm_tc_impl(int M, int N, int K, const bf16* A, int64_t lda, i
   p.tiles_m = (M + TC_BM - 1) / TC_BM;
   p.tiles_n = (N + BN - 1) / BN;
   p.num_kb = (K + TC_BK - 1) / TC_BK;
+  p.batch = batch;
+  p.a_bro = (int)a_bro; p.b_bro = (int)b_bro; p.d_bro = (int)d_bro;
   p.err = err;
   p.wait_ns = g_tc_wait_ns;
   p.stall = 0;
@@ -1129,21 +1148,26 @@ static nc_status gemm_tc_impl(int M, int N, int K, const bf16* A, int64_t lda, i
   const bool f32_out = (ep == NC_EP_STORE_F32 || ep == NC_EP_ACCUM_F32);
   const bool pair = g_gemm_pair && BN == 256 && M >= 256;
   if (pair) p.tiles_m = (M + 255) / 256;
+  // outer (row) extents of the maps: the operand itself, or every problem's rows of a batch
+  const uint64_t ra = batch > 1 ? (uint64_t)batch * a_bro : (uint64_t)(a_kmajor ? M : K);
+  const uint64_t rb = batch > 1 ? (uint64_t)batch * b_bro : (uint64_t)(b_kmajor ? N : K);
+  const uint64_t rd = batch > 1 ? (uint64_t)batch * d_bro : (uint64_t)M;
   CUtensorMap ta, tb;
   bool ok;
-  if (a_kmajor) ok = make_tmap_bf16_2d(&ta, A, K, M, lda, TC_BK, TC_BM);
-  else ok = make_tmap_bf16_2d(&ta, A, M, K, lda, 64, TC_BK);
+  if (a_kmajor) ok = make_tmap_bf16_2d(&ta, A, K, ra, lda, TC_BK, TC_BM);
+  else ok = make_tmap_bf16_2d(&ta, A, M, ra, lda, 64, TC_BK);
   if (!ok) return NC_ERR_CUDA;
-  if (b_kmajor) ok = make_tmap_bf16_2d(&tb, B, K, N, ldb, TC_BK, pair ? 128 : BN);
-  else ok = make_tmap_bf16_2d(&tb, B, N, K, ldb, 64, TC_BK);
+  if (b_kmajor) ok = make_tmap_bf16_2d(&tb, B, K, rb, ldb, TC_BK, pair ? 128 : BN);
+  else ok = make_tmap_bf16_2d(&tb, B, N, rb, ldb, 64, TC_BK);
   if (!ok) return NC_ERR_CUDA;
   // Epilogue tensor maps: D (and aux for the relu^2 modes) in boxes of 32 rows
   // x 128 bytes; without them (unaligned D) the epilogue stores per thread.
   CUtensorMap td, tx;
   memset(&td, 0, sizeof(td));
   memset(&tx, 0, sizeof(tx));
-  p.tma_epi = f32_out ? make_tmap_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, N, M, ldd, 32, 32)
-                      : make_tmap_bf16_2d(&td, D, N, M, ldd, 64, 32);
+  p.tma_epi = f32_out ? make_tmap_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, N, rd, ldd, 32, 32)
+                      : make_tmap_bf16_2d(&td, D, N, rd, ldd, 64, 32);
+  if (batch > 1 && !p.tma_epi) return NC_ERR_ARG;
   if (p.tma_epi && (ep == NC_EP_RELU2 || ep == NC_EP_RELU2_BWD || ep == NC_EP_RELU2_SQ_BWD))
     p.tma_epi = make_tmap_bf16_2d(&tx, aux, N, M, ldaux, 64, 32);
   if (ep == NC_EP_QKV_ROPE && !p.tma_epi) return NC_ERR_ARG;
@@ -1158,6 +1182,22 @@ nc_status launch_gemm_tc(int M, int N, int K, const bf16* A, int64_t lda, int a_
   if (ep == NC_EP_QKV_ROPE) return NC_ERR_ARG;
   return gemm_tc_impl(M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, ep, D, ldd, aux, ldaux, nullptr, err, ws,
                       ws_bytes, st);
+}
+
+nc_status launch_gemm_tc_batched(int batch, int M, int N, int K, const bf16* A, int64_t lda, int a_kmajor,
+                                 int64_t a_bro, const bf16* B, int64_t ldb, int b_kmajor, int64_t b_bro, bf16* D,
+                                 int64_t ldd, int64_t d_bro, int32_t* err, cudaStream_t st) {
+  if (batch <= 0 || M <= 0 || N <= 0) return NC_OK;
+  if (K <= 0 || !A || !B || !D) return NC_ERR_ARG;
+  // every problem's own rows inside its stride; output tiles (up to 256 rows)
+  // inside the problem's output rows; K-rows of an MN-major operand in whole
+  // 128-row k-blocks, so that no load reaches the next problem
+  const int64_t ra = a_kmajor ? M : K, rb = b_kmajor ? N : K;
+  if (a_bro < ra || b_bro < rb || d_bro < (int64_t)(M + 255) / 256 * 256) return NC_ERR_ARG;
+  if ((!a_kmajor || !b_kmajor) && (K % 128)) return NC_ERR_ARG;
+  if ((int64_t)batch * std::max(std::max(a_bro, b_bro), d_bro) >= ((int64_t)1 << 31)) return NC_ERR_ARG;
+  return gemm_tc_impl(M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, NC_EP_STORE, D, ldd, nullptr, 0, nullptr, err,
+                      nullptr, 0, st, batch, a_bro, b_bro, d_bro);
 }
 
 // E4M3 GEMM: D[M,N] = (*scale_a) (*scale_b) A8 B8^T, both operands K-major

@@ -96,15 +96,53 @@ __global__ void __launch_bounds__(OPT_THREADS) k_ns_init(const __grid_constant__
   for (int64_t e = e0 + threadIdx.x; e < e1; e += OPT_THREADS) x[e] = to_act<T>(u[e] * inv);
 }
 
-// B = c A2 + b A + a I  (n x n, written over A2).
+// B = c A2 + b A + a I (n x n, written over A2), for `gridDim.y` matrices whose
+// rows start nr rows apart (padding rows after each are left alone).  One
+// block per row: eight elements per thread and step in 16-byte pieces when
+// the rows allow, else one at a time.
 template <typename T>
-__global__ void k_ns_poly(int n, const T* __restrict__ A, T* __restrict__ A2, float a, float b, float c) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (int64_t)n * n) return;
-  const int r = (int)(i / n), col = (int)(i % n);
-  float v = fmaf(c, act_f(A2[i]), b * act_f(A[i]));
-  if (r == col) v += a;
-  A2[i] = to_act<T>(v);
+__global__ void __launch_bounds__(256) k_ns_poly(int n, int64_t nr, const T* __restrict__ A, T* __restrict__ A2,
+                                                 float a, float b, float c) {
+  const int r = blockIdx.x;
+  const int64_t base = ((int64_t)blockIdx.y * nr + r) * n;
+  const T* ar = A + base;
+  T* br = A2 + base;
+  constexpr int V = 16 / sizeof(T);   // elements per 16-byte piece
+  if (n % V == 0) {
+    for (int c0 = threadIdx.x * V; c0 < n; c0 += blockDim.x * V) {
+      uint4 ua = *reinterpret_cast<const uint4*>(ar + c0);
+      uint4 ub = *reinterpret_cast<const uint4*>(br + c0);
+      const T* ea = reinterpret_cast<const T*>(&ua);
+      T* eb = reinterpret_cast<T*>(&ub);
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        float v = fmaf(c, act_f(eb[e]), b * act_f(ea[e]));
+        if (c0 + e == r) v += a;
+        eb[e] = to_act<T>(v);
+      }
+      *reinterpret_cast<uint4*>(br + c0) = ub;
+    }
+  } else {
+    for (int col = threadIdx.x; col < n; col += blockDim.x) {
+      float v = fmaf(c, act_f(br[col]), b * act_f(ar[col]));
+      if (col == r) v += a;
+      br[col] = to_act<T>(v);
+    }
+  }
+}
+
+// W <- W - lr X for every tensor t of tl: W at master + tl.off[t], X (compute
+// dtype) at X + tl.soff[t], tl.len[t] elements; one block per chunk.
+template <typename T>
+__global__ void __launch_bounds__(OPT_THREADS) k_muon_apply_multi(const __grid_constant__ OptTensors tl,
+                                                                  float* __restrict__ W, const T* __restrict__ X,
+                                                                  float lr) {
+  const int t = opt_tensor_of(tl, blockIdx.x);
+  const int64_t e0 = (int64_t)(blockIdx.x - tl.chunk0[t]) * OPT_CHUNK;
+  const int64_t e1 = min(tl.len[t], e0 + OPT_CHUNK);
+  float* w = W + tl.off[t];
+  const T* x = X + tl.soff[t];
+  for (int64_t e = e0 + threadIdx.x; e < e1; e += OPT_THREADS) w[e] = fmaf(-lr, act_f(x[e]), w[e]);
 }
 
 // W <- W - lr X over one tensor.
@@ -188,9 +226,8 @@ nc_status newton_schulz_run(int dtype, int rows, int cols, int steps, const void
       NC_TRY(gemm(n, n, rows, cur, cols, 0, cur, cols, 0, A, n));
       NC_TRY(gemm(n, n, n, A, n, 1, A, n, 1, A2, n));
     }
-    const int64_t nn = (int64_t)n * n;
-    if (dtype == NC_BF16) k_ns_poly<bf16><<<cdiv(nn, 256), 256, 0, st>>>(n, (const bf16*)A, (bf16*)A2, ca, cb, cc);
-    else k_ns_poly<float><<<cdiv(nn, 256), 256, 0, st>>>(n, (const float*)A, (float*)A2, ca, cb, cc);
+    if (dtype == NC_BF16) k_ns_poly<bf16><<<dim3(n, 1), 256, 0, st>>>(n, n, (const bf16*)A, (bf16*)A2, ca, cb, cc);
+    else k_ns_poly<float><<<dim3(n, 1), 256, 0, st>>>(n, n, (const float*)A, (float*)A2, ca, cb, cc);
     NC_CUDA_TRY(cudaGetLastError());
     if (!tall) NC_TRY(gemm(rows, cols, rows, A2, n, 1, cur, cols, 0, nxt, cols));
     else NC_TRY(gemm(rows, cols, cols, cur, cols, 1, A2, n, 1, nxt, cols));
@@ -200,10 +237,56 @@ nc_status newton_schulz_run(int dtype, int rows, int cols, int steps, const void
   return NC_OK;
 }
 
+// The iteration above on `batch` bf16 matrices X_b [rows, cols] at once (the
+// same products, one batched launch each, so that a step of many small
+// matrices fills the GPU).  X_b starts b * xr rows into ping0 (xr >= rows
+// rounded up to 256; the padding rows take the tiles' spill), A and A2 hold
+// the n x n products with row stride nr (>= n rounded up to 256).  rows must
+// be a multiple of 128 (an MN-major operand's K).  The result is left in
+// ping0 or ping1 (returned through *out).
+nc_status newton_schulz_batched(int batch, int rows, int cols, int steps, void* ping0, void* ping1, int64_t xr,
+                                void* A, void* A2, int64_t nr, const void** out, int32_t* err, cudaStream_t st) {
+  const float ca = 3.4445f, cb = -4.7750f, cc = 2.0315f;
+  const bool tall = rows > cols;
+  const int n = tall ? cols : rows;
+  if (rows % 128 || xr < (rows + 255) / 256 * 256 || nr < (n + 255) / 256 * 256) return NC_ERR_ARG;
+  bf16* ping[2] = {(bf16*)ping0, (bf16*)ping1};
+  bf16 *a = (bf16*)A, *a2 = (bf16*)A2;
+  for (int it = 0; it < steps; ++it) {
+    const bf16* cur = ping[it & 1];
+    bf16* nxt = ping[(it + 1) & 1];
+    if (!tall) {
+      // A = X X^T, A2 = A A (A symmetric), B = c A2 + b A + a I, X <- B X (X read MN-major)
+      NC_TRY(launch_gemm_tc_batched(batch, n, n, cols, cur, cols, 1, xr, cur, cols, 1, xr, a, n, nr, err, st));
+      NC_TRY(launch_gemm_tc_batched(batch, n, n, n, a, n, 1, nr, a, n, 1, nr, a2, n, nr, err, st));
+    } else {
+      // A = X^T X (both operands X read MN-major), X <- X B
+      NC_TRY(launch_gemm_tc_batched(batch, n, n, rows, cur, cols, 0, xr, cur, cols, 0, xr, a, n, nr, err, st));
+      NC_TRY(launch_gemm_tc_batched(batch, n, n, n, a, n, 1, nr, a, n, 1, nr, a2, n, nr, err, st));
+    }
+    k_ns_poly<bf16><<<dim3(n, batch), 256, 0, st>>>(n, nr, a, a2, ca, cb, cc);
+    NC_CUDA_TRY(cudaGetLastError());
+    if (!tall)
+      NC_TRY(launch_gemm_tc_batched(batch, rows, cols, rows, a2, n, 1, nr, cur, cols, 0, xr, nxt, cols, xr, err, st));
+    else
+      NC_TRY(launch_gemm_tc_batched(batch, rows, cols, cols, cur, cols, 1, xr, a2, n, 1, nr, nxt, cols, xr, err, st));
+  }
+  *out = ping[steps & 1];
+  return NC_OK;
+}
+
 nc_status launch_muon_apply(int dtype, int64_t n, float* W, const void* X, float lr, cudaStream_t st) {
   if (n <= 0) return NC_OK;
   if (dtype == NC_BF16) k_muon_apply<bf16><<<grid_for(n), 256, 0, st>>>(n, W, (const bf16*)X, lr);
   else k_muon_apply<float><<<grid_for(n), 256, 0, st>>>(n, W, (const float*)X, lr);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+nc_status launch_muon_apply_multi(int dtype, const OptTensors& tl, float* W, const void* X, float lr, cudaStream_t st) {
+  const int nb = tl.chunk0[tl.n];
+  if (nb <= 0) return NC_OK;
+  if (dtype == NC_BF16) k_muon_apply_multi<bf16><<<nb, OPT_THREADS, 0, st>>>(tl, W, (const bf16*)X, lr);
+  else k_muon_apply_multi<float><<<nb, OPT_THREADS, 0, st>>>(tl, W, (const float*)X, lr);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 

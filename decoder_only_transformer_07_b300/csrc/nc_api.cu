@@ -90,6 +90,16 @@ struct nc_model {
   void *opt_ping0[NC_OPT_STREAMS] = {}, *opt_ping1[NC_OPT_STREAMS] = {};
   void *opt_a[NC_OPT_STREAMS] = {}, *opt_a2[NC_OPT_STREAMS] = {};
   std::vector<int> opt_order, opt_lane;    // matrices by decreasing work, and each one's stream
+  // bf16 with every matrix's rows a multiple of 128: the matrices of one shape
+  // iterate together (batched GEMMs on the caller's stream) instead
+  struct NsGroup {
+    int rows, cols;
+    int64_t xr, nr;                        // row strides of the stacked X and n x n buffers
+    std::vector<int> members;              // optimizer tensor indices
+    OptTensors* apply = nullptr;           // the members' master offsets and stacked result offsets
+  };
+  std::vector<NsGroup> ns_groups;
+  void *nsb_ping0 = nullptr, *nsb_ping1 = nullptr, *nsb_a = nullptr, *nsb_a2 = nullptr;
   // key/value cache for incremental decoding (nc_kv_cache_create)
   void *kcache = nullptr, *vcache = nullptr;   // per layer [kv_b][Hkv][kv_max][hd], compute dtype
   float* dec_part = nullptr;                   // decode-attention partials
@@ -401,6 +411,7 @@ extern "C" void nc_model_destroy(nc_model* m) {
   for (void* p : m->allocs) cudaFree(p);
   if (m->result_host) cudaFreeHost(m->result_host);
   delete m->opt_tl;
+  for (auto& g : m->ns_groups) delete g.apply;
   delete m->q8tl;
   delete m->q8tt;
   for (int k = 0; k < nc_model::NC_OPT_STREAMS; ++k) {
@@ -1008,6 +1019,9 @@ extern "C" void nc_debug_set_gemm_pair(int32_t on) { g_gemm_pair = on != 0; }
 extern int g_tc_stall_next;
 extern "C" void nc_debug_stall_next_gemm(int32_t on) { g_tc_stall_next = on != 0; }
 
+static int g_ns_batched = 1;
+extern "C" void nc_debug_set_ns_batched(int32_t on) { g_ns_batched = on != 0; }
+
 // ------------------------------------------------------------------ optimizer
 // Muon for every weight matrix, AdamW for wte and lm_head (cosmicrealm
 // "noao-chat-0-项目总体介绍" §2.2, §4.2).
@@ -1066,11 +1080,62 @@ static nc_status opt_alloc(nc_model* m) {
   NC_TRY(dalloc_t(m, (size_t)std::max<int64_t>(nchunks, 1), &m->opt_partial));
   NC_TRY(dalloc_t(m, (size_t)nm, &m->opt_norm));
   NC_TRY(dalloc(m, (size_t)total * m->act, &m->opt_x0));
+  // matrices of one shape in one group, in order of first appearance
+  bool batched = g_ns_batched && m->dtype == NC_BF16;
+  m->ns_groups.clear();
+  for (int i = 0; i < nm; ++i) {
+    const ParamTensor& t = m->layout[1 + i];
+    if (t.rows % 128) batched = false;
+    size_t g = 0;
+    while (g < m->ns_groups.size() && (m->ns_groups[g].rows != t.rows || m->ns_groups[g].cols != t.cols)) ++g;
+    if (g == m->ns_groups.size()) {
+      nc_model::NsGroup ng;
+      ng.rows = (int)t.rows;
+      ng.cols = (int)t.cols;
+      ng.xr = (t.rows + 255) / 256 * 256;
+      ng.nr = (std::min(t.rows, t.cols) + 255) / 256 * 256;
+      m->ns_groups.push_back(ng);
+    }
+    m->ns_groups[g].members.push_back(i);
+  }
+  if (!batched) m->ns_groups.clear();
+  for (auto& g : m->ns_groups) {
+    const int nb = (int)g.members.size();
+    if (nb > NC_OPT_MAXT) return NC_ERR_UNSUPPORTED;
+    g.apply = new (std::nothrow) OptTensors;
+    if (!g.apply) return NC_ERR_ALLOC;
+    memset(g.apply, 0, sizeof(OptTensors));
+    g.apply->n = nb;
+    int32_t c = 0;
+    for (int b = 0; b < nb; ++b) {
+      const ParamTensor& t = m->layout[1 + g.members[b]];
+      g.apply->chunk0[b] = c;
+      g.apply->off[b] = t.off;
+      g.apply->soff[b] = (int64_t)b * g.xr * g.cols;
+      g.apply->len[b] = t.rows * t.cols;
+      c += (int32_t)((g.apply->len[b] + OPT_CHUNK - 1) / OPT_CHUNK);
+    }
+    g.apply->chunk0[nb] = c;
+  }
+  if (batched) {
+    int64_t xmax = 0, amax = 0;
+    for (const auto& g : m->ns_groups) {
+      const int64_t nb = (int64_t)g.members.size();
+      xmax = std::max(xmax, nb * g.xr * g.cols);
+      amax = std::max(amax, nb * g.nr * std::min(g.rows, g.cols));
+    }
+    NC_TRY(dalloc(m, (size_t)xmax * m->act, &m->nsb_ping0));
+    NC_TRY(dalloc(m, (size_t)xmax * m->act, &m->nsb_ping1));
+    NC_TRY(dalloc(m, (size_t)amax * m->act, &m->nsb_a));
+    NC_TRY(dalloc(m, (size_t)amax * m->act, &m->nsb_a2));
+  }
   for (int k = 0; k < nc_model::NC_OPT_STREAMS; ++k) {
-    NC_TRY(dalloc(m, (size_t)maxrc * m->act, &m->opt_ping0[k]));
-    NC_TRY(dalloc(m, (size_t)maxrc * m->act, &m->opt_ping1[k]));
-    NC_TRY(dalloc(m, (size_t)(maxn * maxn) * m->act, &m->opt_a[k]));
-    NC_TRY(dalloc(m, (size_t)(maxn * maxn) * m->act, &m->opt_a2[k]));
+    if (!batched) {
+      NC_TRY(dalloc(m, (size_t)maxrc * m->act, &m->opt_ping0[k]));
+      NC_TRY(dalloc(m, (size_t)maxrc * m->act, &m->opt_ping1[k]));
+      NC_TRY(dalloc(m, (size_t)(maxn * maxn) * m->act, &m->opt_a[k]));
+      NC_TRY(dalloc(m, (size_t)(maxn * maxn) * m->act, &m->opt_a2[k]));
+    }
     NC_CUDA_TRY(cudaStreamCreateWithFlags(&m->opt_st[k], cudaStreamNonBlocking));
     NC_CUDA_TRY(cudaEventCreateWithFlags(&m->opt_join[k], cudaEventDisableTiming));
   }
@@ -1118,11 +1183,31 @@ extern "C" nc_status nc_optimizer_reset(nc_model* m, void* stream) {
 
 extern "C" int64_t nc_optimizer_steps(const nc_model* m) { return m ? m->opt_t : -1; }
 
-// Newton-Schulz + apply for every matrix, forked onto the side streams and
-// joined back into `st`.  No split-K workspace: the side streams run
-// concurrently and must not share one.
+// Newton-Schulz + apply for every matrix.  Batched (bf16, rows multiples of
+// 128): per shape group, the members' X0 are copied into one stacked buffer,
+// iterate together and are applied one by one, on `st`.  Otherwise each
+// matrix runs on a side stream, forked from and joined back into `st`; no
+// split-K workspace, since the side streams run concurrently and must not
+// share one.
 static nc_status opt_matrices(nc_model* m, const nc_optim_config* oc, float lr_mult, cudaStream_t st) {
   const OptTensors& tl = *m->opt_tl;
+  if (!m->ns_groups.empty()) {
+    for (const auto& g : m->ns_groups) {
+      const int nb = (int)g.members.size();
+      const size_t xbytes = (size_t)g.xr * g.cols * m->act;   // one stacked matrix with its padding rows
+      for (int b = 0; b < nb; ++b)
+        NC_CUDA_TRY(cudaMemcpyAsync((uint8_t*)m->nsb_ping0 + b * xbytes,
+                                    (const uint8_t*)m->opt_x0 + tl.soff[g.members[b]] * m->act,
+                                    (size_t)g.rows * g.cols * m->act, cudaMemcpyDeviceToDevice, st));
+      const void* x = m->nsb_ping0;
+      if (oc->ns_steps > 0)
+        NC_TRY(newton_schulz_batched(nb, g.rows, g.cols, oc->ns_steps, m->nsb_ping0, m->nsb_ping1, g.xr, m->nsb_a,
+                                     m->nsb_a2, g.nr, &x, m->err, st));
+      const float scale = sqrtf(std::max(1.f, (float)g.rows / (float)g.cols));
+      NC_TRY(launch_muon_apply_multi(m->dtype, *g.apply, m->master, x, oc->matrix_lr * lr_mult * scale, st));
+    }
+    return NC_OK;
+  }
   NC_CUDA_TRY(cudaEventRecord(m->opt_fork, st));
   for (int k = 0; k < nc_model::NC_OPT_STREAMS; ++k) NC_CUDA_TRY(cudaStreamWaitEvent(m->opt_st[k], m->opt_fork, 0));
   nc_status s = NC_OK;

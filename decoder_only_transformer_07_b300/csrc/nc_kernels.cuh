@@ -68,6 +68,16 @@ size_t gemm_tc_workspace_bytes();
 // NC_ERR_UNSUPPORTED for N <= 128; hd 64 or 128.
 // tab: [T][hd/2][2] (pair_rows = 0) or pair-major [hd/4][pair_rows][4] with
 // pair_rows >= T (the coalesced layout the epilogue prefers).
+// `batch` products of the same shape, D_b = A_b B_b^T in bf16 (NC_EP_STORE),
+// operands as for launch_gemm_tc; problem b's rows start b * a_bro (A),
+// b * b_bro (B) and b * d_bro (D) rows after the first problem's, where a
+// row is the operand's outer dimension (M or N for K-major, K for MN-major).
+// Needs a_bro and b_bro at least the operand's rows, d_bro at least M rounded
+// up to 256 (output tiles past M land in that padding), and K a multiple of
+// 128 when an operand is MN-major.  The buffers hold batch * bro rows each.
+nc_status launch_gemm_tc_batched(int batch, int M, int N, int K, const bf16* A, int64_t lda, int a_kmajor,
+                                 int64_t a_bro, const bf16* B, int64_t ldb, int b_kmajor, int64_t b_bro, bf16* D,
+                                 int64_t ldd, int64_t d_bro, int32_t* err, cudaStream_t st);
 nc_status launch_gemm_tc_qkv_rope(int M, int N, int K, const bf16* A, int64_t lda, const bf16* Wqkv, int64_t ldb,
                                   bf16* qkv, int64_t ldd, int T, int nh, int hd, const float* tab, int pair_rows,
                                   float* rstd, float eps, int32_t* err, cudaStream_t st);
@@ -162,8 +172,16 @@ nc_status launch_ns_init(int dtype, const OptTensors& tl, const float* U, float 
 nc_status newton_schulz_run(int dtype, int rows, int cols, int steps, const void* x0, void* ping0, void* ping1,
                             void* A, void* A2, const void** out, int32_t* err, void* gemm_ws, size_t gemm_ws_bytes,
                             cudaStream_t st);
+// newton_schulz_run on `batch` bf16 matrices of one shape at once: X_b starts
+// b * xr rows into ping0, the n x n products b * nr rows into A and A2 (xr,
+// nr at least rows and n rounded up to 256; rows a multiple of 128).
+nc_status newton_schulz_batched(int batch, int rows, int cols, int steps, void* ping0, void* ping1, int64_t xr,
+                                void* A, void* A2, int64_t nr, const void** out, int32_t* err, cudaStream_t st);
 // W <- W - lr X (n elements, X in the compute dtype).
 nc_status launch_muon_apply(int dtype, int64_t n, float* W, const void* X, float lr, cudaStream_t st);
+// W <- W - lr X for every tensor t of tl at once: W = master + tl.off[t], X (compute
+// dtype) at X + tl.soff[t] elements, tl.len[t] elements each.
+nc_status launch_muon_apply_multi(int dtype, const OptTensors& tl, float* W, const void* X, float lr, cudaStream_t st);
 nc_status launch_cast_out(int dtype, int64_t n, const void* X, float* out, cudaStream_t st);
 // One bias-corrected AdamW step (t >= 1) with decoupled weight decay.
 nc_status launch_adamw(int64_t n, float* W, const float* G, float* m, float* v, float lr, float b1, float b2,

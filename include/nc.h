@@ -398,6 +398,14 @@ void nc_debug_stall_next_gemm(int32_t on);
  * compute the same sums; the switch exists to test and time either path. */
 void nc_debug_set_gemm_pair(int32_t on);
 
+/* Test hook.  on = 1 (default): a bf16 model whose weight matrices all have
+ * row counts that are multiples of 128 runs the optimizer's Newton-Schulz
+ * iterations batched, one launch per product for all matrices of a shape; on
+ * = 0 runs them matrix by matrix on side streams.  Both compute the same
+ * products.  Read when a model allocates its optimizer state (its first
+ * nc_optimizer_step), so it applies to models stepped after the call. */
+void nc_debug_set_ns_batched(int32_t on);
+
 /* Test hook.  on = 1 (default): a decode step replays a CUDA graph of the
  * step, captured once per batch size on an internal stream (its position
  * lives on the device, its tokens and logits pass through fixed buffers);

@@ -121,6 +121,32 @@ def test_optimizer_steps_bf16_small_gqa():
     _check(cfg, p0, got, ref, 3e-2, 0.999)
 
 
+def test_batched_newton_schulz_equals_per_matrix():
+    """The batched iteration (all matrices of a shape in one launch per product)
+    computes, tile for tile, the products the per-matrix iteration computes:
+    two bf16 steps leave bit-identical weights either way."""
+    w = S.workload("d12", depth=2, n_embd=256, n_head=2, n_kv_head=1, head_dim=128, mlp_hidden=1024, vocab=512,
+                   seq_len=128, batch=2)
+    P = OM.n_params(OM.Config.from_workload(w))
+    rng = np.random.default_rng(24)
+    params = torch.from_numpy((rng.standard_normal(P) * 0.02).astype(np.float32))
+    g = torch.from_numpy(rng.standard_normal(P).astype(np.float32)).cuda()
+    out = []
+    for batched in (1, 0):
+        nc.lib().nc_debug_set_ns_batched(batched)
+        try:
+            m = nc.Model(nc.config_from_workload(w), seed=1)
+            m.set_params(params)
+            m.optimizer_step(g)
+            m.optimizer_step(g, lr_mult=0.5)
+            out.append(m.get_params().cpu())
+            m.close()
+        finally:
+            nc.lib().nc_debug_set_ns_batched(1)
+    assert not torch.equal(out[0], params)
+    assert torch.equal(out[0], out[1])
+
+
 def test_optimizer_is_deterministic_and_reset_restarts():
     w = S.workload("tiny")
     P = OM.n_params(OM.Config.from_workload(w))
