@@ -104,6 +104,7 @@ _SIGS = {
     "nc_debug_set_ns_batched": (None, [_i32]),
     "nc_debug_stall_next_gemm": (None, [_i32]),
     "nc_debug_set_decode_graph": (None, [_i32]),
+    "nc_debug_set_decode_pdl": (None, [_i32]),
     "nc_op_gemm_rows": (_i32, [_i32, _i32, _i32, _i32, _p, _i64, _p, _i64, _i32, _p, _i64, _p]),
     "nc_op_quantize_fp8": (_i32, [_i32, _p, _i64, _p, _p, _p]),
     "nc_op_gemm_fp8": (_i32, [_i32, _i32, _i32, _p, _i64, _p, _i64, _p, _p, _i32, _p, _i64, _p]),

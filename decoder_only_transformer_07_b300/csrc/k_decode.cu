@@ -24,6 +24,29 @@
 #include "nc_kernels.cuh"
 #include "nc_ptx.cuh"
 
+int g_decode_pdl = 1;   // test hook: 0 launches the decode kernels with plain stream order
+
+namespace {
+// The decode kernels (skinny GEMM, attention, combine) are launched with
+// programmatic stream serialization: each may start while the previous kernel
+// drains, and waits (griddep_wait) before touching that kernel's data.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = g_decode_pdl ? 1 : 0;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+}  // namespace
+
 namespace {
 
 __device__ __forceinline__ float ld_f(const float* p) { return *p; }
@@ -89,6 +112,7 @@ __global__ void __launch_bounds__(DEC_THREADS)
   __shared__ float qs[G][HD];
   __shared__ float ps[G][CK];
   __shared__ float mh[G], sh[G];
+  griddep_wait();   // the projection's q/k/v, and `part` the previous combine read
   if (len_dev) len = *len_dev + 1;
   const int bg = blockIdx.x, s = blockIdx.y;
   const int b = bg / Hkv, g = bg % Hkv;
@@ -102,6 +126,7 @@ __global__ void __launch_bounds__(DEC_THREADS)
       pbase[(int64_t)tid * nsplit * (HD + 2)] = -INFINITY;
       pbase[(int64_t)tid * nsplit * (HD + 2) + 1] = 0.f;
     }
+    griddep_launch_dependents();
     return;
   }
   const int pos = len - 1;                             // the position just appended
@@ -246,6 +271,7 @@ __global__ void __launch_bounds__(DEC_THREADS)
       }
     }
   }
+  griddep_launch_dependents();   // the combine may launch now; it waits for this grid to complete
 }
 
 // o[b, h*HD + d] = merged output of row (b, h); one block of HD threads per
@@ -257,6 +283,7 @@ __global__ void __launch_bounds__(HD) k_decode_combine(int nsplit, const float* 
                                                        E* __restrict__ out, int64_t ldo, int H) {
   extern __shared__ float fw[];
   __shared__ float red[32];
+  griddep_wait();
   const int64_t r = blockIdx.x;
   const int tid = threadIdx.x;
   const float* pr = part + r * nsplit * (HD + 2);
@@ -275,6 +302,7 @@ __global__ void __launch_bounds__(HD) k_decode_combine(int nsplit, const float* 
   float acc = 0.f;
 #pragma unroll 8
   for (int s = 0; s < nsplit; ++s) acc = fmaf(fw[s], pr[(int64_t)s * (HD + 2) + 2 + tid], acc);
+  griddep_launch_dependents();
   const int64_t b = r / H;
   const int h = (int)(r % H);
   st_f(out + b * ldo + (int64_t)h * HD + tid, S > 0.f ? acc / S : 0.f);
@@ -289,11 +317,11 @@ nc_status decode_attn_t(int B, int H, int Hkv, int len, const int32_t* len_dev, 
   const int nsplit = ((len_dev ? max_len : len) + CK - 1) / CK;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   if ((size_t)nsplit * sizeof(float) > 48 * 1024) return NC_ERR_UNSUPPORTED;   // the combine's split weights
-  k_decode_attn<E, HD, G><<<dim3((unsigned)(B * Hkv), (unsigned)nsplit), DEC_THREADS, 0, st>>>(
-      H, Hkv, len, len_dev, nsplit, qkv, ld, kc, vc, max_len, scale_log2, part, tab, eps);
-  NC_CUDA_TRY(cudaGetLastError());
-  k_decode_combine<E, HD><<<(unsigned)(B * H), HD, nsplit * sizeof(float), st>>>(nsplit, part, o, ldo, H);
-  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+  NC_CUDA_TRY(launch_pdl(k_decode_attn<E, HD, G>, dim3((unsigned)(B * Hkv), (unsigned)nsplit), dim3(DEC_THREADS), 0,
+                         st, H, Hkv, len, len_dev, nsplit, qkv, ld, kc, vc, max_len, scale_log2, part, tab, eps));
+  NC_CUDA_TRY(launch_pdl(k_decode_combine<E, HD>, dim3((unsigned)(B * H)), dim3(HD), nsplit * sizeof(float), st,
+                         nsplit, (const float*)part, o, ldo, H));
+  return NC_OK;
 }
 
 template <typename E, int HD>
@@ -495,8 +523,9 @@ __global__ void __launch_bounds__(SK_WARPS * 32)
 
   uint4 w[SK_PIECES], wn[SK_PIECES];
   int g = blockIdx.x;
-  // the first pieces of W are in flight while A is prepared
+  // the first pieces of W are in flight while the previous kernel finishes and A is prepared
   if (g * SK_WARPS + warp < N) sk_load(W + (int64_t)(g * SK_WARPS + warp) * ldw, 0, min(KC, K), lane, w);
+  griddep_wait();   // A (or X) and D are the previous kernels' data
   if (NORM) {
     // sum of squares of each row: every thread a strided share, then the warps' partials in order
     float ss[MB];
@@ -554,6 +583,7 @@ __global__ void __launch_bounds__(SK_WARPS * 32)
       for (int u = 0; u < SK_PIECES; ++u) w[u] = wn[u];
       g = g2;
       b = b2;
+      if (g >= ngroups) griddep_launch_dependents();   // this warp's last store is issued
     }
     return;
   }
@@ -584,6 +614,7 @@ __global__ void __launch_bounds__(SK_WARPS * 32)
 #pragma unroll
     for (int m = 0; m < MB; ++m) acc[m] = 0.f;
   }
+  griddep_launch_dependents();
 }
 
 template <typename E, int MB>
@@ -599,9 +630,9 @@ nc_status skinny_t(int M, int N, int K, const void* A, int64_t lda, const E* W, 
   const int KC = (int)std::min<int64_t>((K + 7) / 8 * 8, fit);
   const int ngroups = (N + SK_WARPS - 1) / SK_WARPS;
   const int grid = std::min(ngroups, 2 * g_num_sms);
-  k_gemm_skinny<E, MB, NORM><<<grid, SK_WARPS * 32, sk_smem_bytes<E, MB>(KC), st>>>(M, N, K, KC, A, lda, W, ldw,
-                                                                                     ep, D, ldd, eps);
-  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+  NC_CUDA_TRY(launch_pdl(k_gemm_skinny<E, MB, NORM>, dim3(grid), dim3(SK_WARPS * 32), sk_smem_bytes<E, MB>(KC), st,
+                         M, N, K, KC, A, lda, W, ldw, ep, D, ldd, eps));
+  return NC_OK;
 }
 
 template <typename E, int MB, bool NORM>

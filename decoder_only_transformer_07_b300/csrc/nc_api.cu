@@ -1475,6 +1475,9 @@ extern "C" nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t 
 // Test hook: 0 makes decode steps run eagerly instead of through the captured graph.
 extern "C" void nc_debug_set_decode_graph(int32_t on) { g_decode_graph = on != 0; }
 
+extern int g_decode_pdl;
+extern "C" void nc_debug_set_decode_pdl(int32_t on) { g_decode_pdl = on != 0; }
+
 extern "C" nc_status nc_op_gemm_rows(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A, int64_t lda,
                                      const void* W, int64_t ldw, int32_t ep, void* D, int64_t ldd, void* stream) {
   if (!dtype_ok(dtype) || !A || !W || !D) return NC_ERR_ARG;

@@ -170,6 +170,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Programmatic dependent launch.  griddep_launch_dependents lets the next
+// kernel of the stream, when it was launched with programmatic stream
+// serialization, start before this one ends; that kernel's griddep_wait then
+// blocks until this grid (and so, transitively, every earlier one) has
+// completed with its writes visible.  A kernel launched that way may only read
+// data no kernel of the stream writes (weights) before its griddep_wait, and
+// writes nothing there.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Two fp32 lanes per instruction (the .f32x2 forms of fma / add / mul): each
 // lane is rounded to nearest as its scalar instruction would be, so results
 // are bit-identical to the scalar code; the FMA pipe issues half as many

@@ -412,6 +412,14 @@ void nc_debug_set_ns_batched(int32_t on);
  * on = 0 enqueues the same kernels directly.  Both compute the same values. */
 void nc_debug_set_decode_graph(int32_t on);
 
+/* Test hook.  on = 1 (default): the decode kernels (skinny projections,
+ * attention, combine) are launched with programmatic stream serialization, so
+ * each may start while the previous kernel drains (a projection streams its
+ * first weights then) and waits for it before touching its data; on = 0
+ * launches them in plain stream order.  Both compute the same values.  Read
+ * at launch time, so a step graph captured before the call keeps its form. */
+void nc_debug_set_decode_pdl(int32_t on);
+
 /* ------------------------------------------------------------------------
  * Optimizer step (cosmicrealm "noao-chat-0-项目总体介绍" §2.2 and §4.2;
  * woshipm nanochat analysis §六.1): the weight matrices (every Wq, Wk, Wv,

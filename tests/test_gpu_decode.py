@@ -126,3 +126,27 @@ def test_decode_graph_replay_equals_eager():
     nc.lib().nc_debug_set_decode_graph(1)
     assert torch.equal(outs[0], outs[1])
     m.close()
+
+
+def test_decode_overlapped_launches_equal_stream_order():
+    """Decode kernels launched to overlap their predecessor's tail (programmatic
+    dependent launch, in the captured step) give bitwise the logits of plain
+    stream order."""
+    w = S.Workload(name="dec", dtype="bf16", tokens="zipf", depth=2, n_embd=256, n_head=4, n_kv_head=2, head_dim=64,
+                   mlp_hidden=1024, vocab=1024, seq_len=320, batch=2)
+    tok, _ = S.batch_tokens(w, seq_len=270)
+    dev = torch.from_numpy(tok).cuda()
+    outs = []
+    for pdl in (1, 0):
+        nc.lib().nc_debug_set_decode_pdl(pdl)
+        try:
+            cfg, m, params = _model(w)
+            m.kv_cache_create(2, 270)
+            z = [m.prefill(dev[:, :250].contiguous()).cpu()]
+            for j in range(19):
+                z.append(m.decode_step(dev[:, 250 + j].contiguous()).cpu())
+            outs.append(torch.stack(z))
+            m.close()
+        finally:
+            nc.lib().nc_debug_set_decode_pdl(1)
+    assert torch.equal(outs[0], outs[1])
