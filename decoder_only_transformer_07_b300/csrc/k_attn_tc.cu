@@ -74,7 +74,22 @@ struct AtShape {
   const float* rope_tab;
   const float* rstd_qk;
   int rope_pair_rows;   // 0: rope_tab is [T][hd/2][2]; else pair-major [hd/4][rope_pair_rows][4]
+  // Optional: atomic maximum of |output| as stored (bf16), as float bits, over
+  // the rows inside T - O in the forward, all of dq, dk and dv in the backward -
+  // for a per-tensor quantiser of that output.
+  unsigned* amax;
 };
+
+// Commits a lane's maximum |value| (its row's, 0 past T) into sh.amax: warp
+// maximum, rounded to bf16 (monotonic, so the maximum of the stored values),
+// one atomic per warp.  The whole warp calls it.
+__device__ __forceinline__ void at_amax_commit(const AtShape& sh, float am) {
+  if (!sh.amax) return;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  if ((threadIdx.x & 31) == 0 && am > 0.f)
+    atomicMax(sh.amax, __float_as_uint(__bfloat162float(__float2bfloat16_rn(am))));
+}
 
 // tcgen05.mma kind::f16 instruction descriptor: fp32 accumulator, bf16 A and
 // B, A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), M = 128, N = n.
@@ -156,7 +171,7 @@ struct FwdSmem {
   static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
 };
 
-template <int HD>
+template <int HD, bool AMAX>
 __global__ void __launch_bounds__(AT_THREADS, 1)
     k_attn_fwd_tc(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_o, AtShape sh,
                   bf16* __restrict__ o, float* __restrict__ lse) {
@@ -368,6 +383,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (ok && n > 0 && at_wait_warp(&pv_done[i], (n - 1) & 1, sh, abort_flag)) {
       tc_fence_after();
       const float inv = 1.f / l;
+      float am = 0.f;   // max |O| of this row before the 1/l scale (a positive factor keeps the maximum)
       if constexpr (HD == 128) {
         // two 32 x 64 boxes per warp, staged in this tile's Q buffer (its last
         // S has completed) and stored by TMA
@@ -379,6 +395,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             uint32_t ov[32];
             tmem_ld_32x32b_x32(tO + 64 * c + 32 * cc, ov);
             tmem_ld_wait();
+            if (AMAX) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) am = fmaxf(am, fabsf(__uint_as_float(ov[e])));
+            }
 #pragma unroll
             for (int e = 0; e < 32; e += 8) {
               const uint32_t chunk = (uint32_t)(4 * cc + e / 8);
@@ -407,6 +427,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         tmem_ld_32x32b_x32(tO + 32 * c, ov);
         tmem_ld_wait();
         if (qpos < sh.T) {
+          if (AMAX) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) am = fmaxf(am, fabsf(__uint_as_float(ov[e])));
+          }
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 w;
@@ -419,6 +443,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
       }
       }
+      if (AMAX) at_amax_commit(sh, qpos < sh.T ? am * inv : 0.f);
       if (qpos < sh.T) lse[(int64_t)bh * sh.T + qpos] = (m * sh.scale_log2 + log2f(l)) * LN2;
     }
   }
@@ -462,9 +487,9 @@ __device__ __forceinline__ void at_out_prefetch(const AtShape& sh, int hf, bool 
   for (int k = 0; k < PW / 2; ++k) pre.t[k] = __ldg(cs + (size_t)k * cstep);
 }
 
-template <int HD>
+template <int HD, bool AMAX>
 __device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, const uint8_t* ytile, int r, int hf,
-                                            bool valid, const AtOutPre<HD>& pre, bf16* dst) {
+                                            bool valid, const AtOutPre<HD>& pre, bf16* dst, float& am) {
   if (!sh.rope_tab) {
 #pragma unroll 1
     for (int c = 0; c < HD / 64; ++c) {
@@ -472,6 +497,10 @@ __device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, co
       tmem_ld_32x32b_x32(tacc + hf * (HD / 2) + 32 * c, v);
       tmem_ld_wait();
       if (valid) {
+        if (AMAX) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) am = fmaxf(am, fabsf(__uint_as_float(v[e])) * sh.scale);
+        }
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           uint4 w;
@@ -537,6 +566,10 @@ __device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, co
       o1[e + 1] = a1 * t.z - b1 * t.w;
       o2[e + 1] = a1 * t.w + b1 * t.z;
     }
+    if (AMAX) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) am = fmaxf(am, fmaxf(fabsf(o1[e]), fabsf(o2[e])));
+    }
     uint4 w1, w2;
     w1.x = pack2(o1[0], o1[1]); w1.y = pack2(o1[2], o1[3]); w1.z = pack2(o1[4], o1[5]); w1.w = pack2(o1[6], o1[7]);
     w2.x = pack2(o2[0], o2[1]); w2.y = pack2(o2[2], o2[3]); w2.z = pack2(o2[4], o2[5]); w2.w = pack2(o2[6], o2[7]);
@@ -552,7 +585,7 @@ __device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, co
 // past T.  Every lane of the warp takes part, and the warp is converged again
 // on return (the caller may issue aligned tcgen05 instructions next).
 __device__ __forceinline__ void at_out_box128(uint32_t tacc, int hf, float mul, uint8_t* box, const CUtensorMap* tm,
-                                              int x, int y, int bz, int T) {
+                                              int x, int y, int bz, int T, float& am, bool track) {
   const int lane = threadIdx.x & 31;
   const uint32_t srow = smem_u32(box) + (uint32_t)lane * 128u;
 #pragma unroll 1
@@ -560,6 +593,10 @@ __device__ __forceinline__ void at_out_box128(uint32_t tacc, int hf, float mul, 
     uint32_t v[32];
     tmem_ld_32x32b_x32(tacc + hf * 64 + 32 * c, v);
     tmem_ld_wait();
+    if (track && y + lane < T) {   // rows past the end are not stored
+#pragma unroll
+      for (int e = 0; e < 32; ++e) am = fmaxf(am, fabsf(__uint_as_float(v[e])) * mul);
+    }
 #pragma unroll
     for (int e = 0; e < 32; e += 8)
       st_shared_v4(srow + ((((uint32_t)(4 * c + e / 8) ^ (uint32_t)lane) & 7u) << 4),
@@ -592,7 +629,7 @@ struct DqSmem {
   static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
 };
 
-template <int HD>
+template <int HD, bool AMAX>
 __global__ void __launch_bounds__(AT_THREADS, 1)
     k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_out, AtShape sh, const float* __restrict__ lse,
@@ -787,17 +824,19 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
     AtOutPre<HD> pre;
     at_out_prefetch<HD>(sh, hf, ok && valid, qpos, (int64_t)row0 + qpos, h, pre);
+    float am = 0.f;
     if (ok && at_wait_warp(dq_done, 0, sh, abort_flag)) {
       tc_fence_after();
       if (HD == 128 && !sh.rope_tab) {
         // staged in the K ring, free once every dQ product has completed
         at_out_box128(tbase + lane_off + 384, hf, sh.scale, smem + L::OFF_K + (hf * 4 + quarter) * 4096, &tm_out,
-                      h * HD + hf * 64, qt * 128 + quarter * 32, b, sh.T);
+                      h * HD + hf * 64, qt * 128 + quarter * 32, b, sh.T, am, AMAX);
         if (lane == 0) bulk_wait_all();
       } else {
-        at_out_tile<HD>(sh, tbase + lane_off + 384, smem + L::OFF_Q, r, hf, valid, pre,
-                        dqkv + (int64_t)(row0 + qpos) * sh.ld_qkv + (int64_t)h * HD);
+        at_out_tile<HD, AMAX>(sh, tbase + lane_off + 384, smem + L::OFF_Q, r, hf, valid, pre,
+                        dqkv + (int64_t)(row0 + qpos) * sh.ld_qkv + (int64_t)h * HD, am);
       }
+      if (AMAX) at_amax_commit(sh, am);
     }
   }
   tc_fence_before();
@@ -820,7 +859,7 @@ struct DkvSmem {
   static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
 };
 
-template <int HD>
+template <int HD, bool AMAX>
 __global__ void __launch_bounds__(AT_THREADS, 1)
     k_attn_bwd_dkv_tc(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_out,
@@ -1028,6 +1067,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const bool valid = key < sh.T;
     AtOutPre<HD> pre;
     at_out_prefetch<HD>(sh, hf, ok && valid, key, (int64_t)row0 + key, sh.H + g, pre);
+    float am = 0.f;
     if (ok && at_wait_warp(dkv_done, 0, sh, abort_flag)) {
       tc_fence_after();
       if constexpr (HD == 128) {
@@ -1036,13 +1076,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         // and rotation backward with per-thread stores
         const int w8 = hf * 4 + quarter;
         at_out_box128(tbase + lane_off + 256, hf, 1.f, smem + L::OFF_QS + w8 * 4096, &tm_out,
-                      (sh.H + sh.Hkv + g) * HD + hf * 64, kt * 128 + quarter * 32, b, sh.T);
+                      (sh.H + sh.Hkv + g) * HD + hf * 64, kt * 128 + quarter * 32, b, sh.T, am, AMAX);
         if (!sh.rope_tab)
           at_out_box128(tbase + lane_off + 256 + HD, hf, sh.scale, smem + L::OFF_QS + 32768 + w8 * 4096, &tm_out,
-                        (sh.H + g) * HD + hf * 64, kt * 128 + quarter * 32, b, sh.T);
+                        (sh.H + g) * HD + hf * 64, kt * 128 + quarter * 32, b, sh.T, am, AMAX);
         else
-          at_out_tile<HD>(sh, tbase + lane_off + 256 + HD, smem + L::OFF_K, r, hf, valid, pre,
-                          dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + g) * HD);
+          at_out_tile<HD, AMAX>(sh, tbase + lane_off + 256 + HD, smem + L::OFF_K, r, hf, valid, pre,
+                          dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + g) * HD, am);
         if (lane == 0) bulk_wait_all();
       } else {
       bf16* dv = dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + sh.Hkv + g) * HD + hf * (HD / 2);
@@ -1052,6 +1092,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         tmem_ld_32x32b_x32(tbase + lane_off + 256 + hf * (HD / 2) + 32 * c, v);
         tmem_ld_wait();
         if (valid) {
+          if (AMAX) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) am = fmaxf(am, fabsf(__uint_as_float(v[e])));
+          }
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 w;
@@ -1064,9 +1108,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
       }
       // dK (carries 1/sqrt(hd)), through the k-norm and rotation backward when fused
-      at_out_tile<HD>(sh, tbase + lane_off + 256 + HD, smem + L::OFF_K, r, hf, valid, pre,
-                      dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + g) * HD);
+      at_out_tile<HD, AMAX>(sh, tbase + lane_off + 256 + HD, smem + L::OFF_K, r, hf, valid, pre,
+                      dqkv + (int64_t)(row0 + key) * sh.ld_qkv + (int64_t)(sh.H + g) * HD, am);
       }
+      if (AMAX) at_amax_commit(sh, am);
     }
   }
   tc_fence_before();
@@ -1119,6 +1164,7 @@ bool at_shape(int B, int T, int H, int Hkv, int hd, int32_t* err, AtShape* sh) {
   sh->rope_tab = nullptr;
   sh->rstd_qk = nullptr;
   sh->rope_pair_rows = 0;
+  sh->amax = nullptr;
   return true;
 }
 
@@ -1132,12 +1178,16 @@ nc_status attn_fwd_tc(const AtShape& sh, const bf16* qkv, bf16* o, float* lse, c
     return NC_ERR_CUDA;
   static bool attr = false;
   if (!attr) {
-    NC_CUDA_TRY(cudaFuncSetAttribute(k_attn_fwd_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    NC_CUDA_TRY(cudaFuncSetAttribute(k_attn_fwd_tc<HD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)FwdSmem<HD>::BYTES));
+    NC_CUDA_TRY(cudaFuncSetAttribute(k_attn_fwd_tc<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)FwdSmem<HD>::BYTES));
     attr = true;
   }
   const unsigned grid = (unsigned)((sh.T + 255) / 256) * (unsigned)(sh.B * sh.H);
-  k_attn_fwd_tc<HD><<<grid, AT_THREADS, FwdSmem<HD>::BYTES, st>>>(tm, tm_o, sh, o, lse);
+  // the instantiation with the output maximum only when it is asked for
+  if (sh.amax) k_attn_fwd_tc<HD, true><<<grid, AT_THREADS, FwdSmem<HD>::BYTES, st>>>(tm, tm_o, sh, o, lse);
+  else k_attn_fwd_tc<HD, false><<<grid, AT_THREADS, FwdSmem<HD>::BYTES, st>>>(tm, tm_o, sh, o, lse);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
@@ -1156,36 +1206,51 @@ nc_status attn_bwd_tc(const AtShape& sh, const bf16* qkv, const bf16* o, const f
     return NC_ERR_CUDA;
   static bool attr = false;
   if (!attr) {
-    NC_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd_dq_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    NC_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd_dq_tc<HD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)DqSmem<HD>::BYTES));
-    NC_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd_dkv_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    NC_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd_dkv_tc<HD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)DkvSmem<HD>::BYTES));
+    NC_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd_dq_tc<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)DqSmem<HD>::BYTES));
+    NC_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd_dkv_tc<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)DkvSmem<HD>::BYTES));
     attr = true;
   }
   const unsigned nt = (unsigned)((sh.T + 127) / 128);
-  k_attn_bwd_dq_tc<HD><<<nt * (unsigned)(sh.B * sh.H), AT_THREADS, DqSmem<HD>::BYTES, st>>>(
-      tm_qkv128, tm_do128, tm_out, sh, lse, Dv, dqkv);
-  NC_CUDA_TRY(cudaGetLastError());
-  k_attn_bwd_dkv_tc<HD><<<nt * (unsigned)(sh.B * sh.Hkv), AT_THREADS, DkvSmem<HD>::BYTES, st>>>(
-      tm_qkv128, tm_qkv64, tm_do64, tm_out, sh, lse, Dv, dqkv);
+  const dim3 gq(nt * (unsigned)(sh.B * sh.H)), gkv(nt * (unsigned)(sh.B * sh.Hkv));
+  if (sh.amax) {   // the instantiations with the output maximum only when it is asked for
+    k_attn_bwd_dq_tc<HD, true><<<gq, AT_THREADS, DqSmem<HD>::BYTES, st>>>(tm_qkv128, tm_do128, tm_out, sh, lse, Dv,
+                                                                          dqkv);
+    NC_CUDA_TRY(cudaGetLastError());
+    k_attn_bwd_dkv_tc<HD, true><<<gkv, AT_THREADS, DkvSmem<HD>::BYTES, st>>>(tm_qkv128, tm_qkv64, tm_do64, tm_out,
+                                                                             sh, lse, Dv, dqkv);
+  } else {
+    k_attn_bwd_dq_tc<HD, false><<<gq, AT_THREADS, DqSmem<HD>::BYTES, st>>>(tm_qkv128, tm_do128, tm_out, sh, lse,
+                                                                           Dv, dqkv);
+    NC_CUDA_TRY(cudaGetLastError());
+    k_attn_bwd_dkv_tc<HD, false><<<gkv, AT_THREADS, DkvSmem<HD>::BYTES, st>>>(tm_qkv128, tm_qkv64, tm_do64, tm_out,
+                                                                              sh, lse, Dv, dqkv);
+  }
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
 }  // namespace
 
 nc_status launch_attn_fwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, bf16* o, float* lse,
-                             int32_t* err, cudaStream_t st) {
+                             int32_t* err, cudaStream_t st, unsigned* amax) {
   AtShape sh;
   if (!at_shape(B, T, H, Hkv, hd, err, &sh)) return NC_ERR_ARG;
+  sh.amax = amax;
   if (!aligned16(qkv) || !aligned16(o)) return NC_ERR_ARG;
   return hd == 128 ? attn_fwd_tc<128>(sh, qkv, o, lse, st) : attn_fwd_tc<64>(sh, qkv, o, lse, st);
 }
 
 nc_status launch_attn_bwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, const bf16* o, const float* lse,
                              const bf16* dout, bf16* dqkv, float* Dv, const float* rstd_qk, const float* rope_tab,
-                             int rope_pair_rows, int32_t* err, cudaStream_t st) {
+                             int rope_pair_rows, int32_t* err, cudaStream_t st, unsigned* amax) {
   AtShape sh;
   if (!at_shape(B, T, H, Hkv, hd, err, &sh)) return NC_ERR_ARG;
+  sh.amax = amax;
   if ((rstd_qk == nullptr) != (rope_tab == nullptr) || (rope_tab && !aligned16(rope_tab))) return NC_ERR_ARG;
   if (rope_pair_rows < 0 || (rope_pair_rows > 0 && (rope_pair_rows < T || hd % 4))) return NC_ERR_ARG;
   sh.rstd_qk = rstd_qk;

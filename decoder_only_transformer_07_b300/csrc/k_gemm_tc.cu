@@ -73,6 +73,9 @@ struct TcParams {
   // F8 kernels: D = (*scale_a) (*scale_b) sum_k A8(m,k) B8(n,k)
   const float* scale_a;
   const float* scale_b;
+  // optional (bf16 outputs of the staged epilogue): atomic maximum of |D| as
+  // stored, as float bits, for a per-tensor quantiser of D
+  unsigned* amax;
 };
 
 // One unit of work of a CTA: k-blocks [k0, k1) of output tile t (slice s).
@@ -278,6 +281,7 @@ __device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, int ep, co
   const uint32_t sa = smem_u32(stg);
   const int r = lane;
   const float alpha = F8 ? __ldg(p.scale_a) * __ldg(p.scale_b) : 1.f;
+  float am = 0.f;   // maximum |value| this warp stores (p.amax)
 #pragma unroll 1
   for (int oc = 0; oc < BN / 2; oc += cc) {
     const int n_out = n_base + oc;
@@ -340,6 +344,10 @@ __device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, int ep, co
               f[e] *= 2.f * (sq_bwd ? sqrt_approx(x) : x);
             }
           }
+          if (p.amax) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(f[e]));
+          }
           const uint4 o = pack8_bf16(f);
           st_shared_v4(sa + stg_off(r, u), o.x, o.y, o.z, o.w);
         }
@@ -375,6 +383,12 @@ __device__ __forceinline__ bool tc_epilogue_staged(const TcParams& p, int ep, co
         bulk_commit();
       }
     }
+  }
+  if (p.amax) {
+    // rounding to bf16 is monotonic, so the rounded maximum is the maximum of the stored values
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    if (lane == 0 && am > 0.f) atomicMax(p.amax, __float_as_uint(__bfloat162float(__float2bfloat16_rn(am))));
   }
   return true;
 }
@@ -1130,6 +1144,7 @@ static nc_status gemm_tc_impl(int M, int N, int K, const bf16* A, int64_t lda, i
   p.rope_tab = nullptr; p.rstd_qk = nullptr; p.rope_T = 1; p.rope_nh = 0; p.rope_hd = 0; p.rope_pair_rows = 0;
   p.rope_eps = 0.f;
   p.scale_a = nullptr; p.scale_b = nullptr;
+  p.amax = nullptr;
   if (rope) {
     // whole heads in each epilogue warp's 128 columns, 16-byte row segments
     if (ep != NC_EP_QKV_ROPE || BN != 256 || (rope->hd != 64 && rope->hd != 128) || (N % rope->hd) ||
@@ -1209,7 +1224,7 @@ nc_status launch_gemm_tc_batched(int batch, int M, int N, int K, const bf16* A, 
 static nc_status gemm_fp8_impl(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
                                const float* scale_a, const float* scale_b, int ep, void* D, int64_t ldd,
                                const TcRope* rope, int32_t* err, cudaStream_t st, const void* aux = nullptr,
-                               int64_t ldaux = 0) {
+                               int64_t ldaux = 0, unsigned* amax = nullptr) {
   if (M <= 0 || N <= 0) return NC_OK;
   if (K <= 0 || !A || !B || !D || !scale_a || !scale_b) return NC_ERR_ARG;
   if ((lda % 16) || (ldb % 16) || lda < K || ldb < K || (((uintptr_t)A) & 15) || (((uintptr_t)B) & 15))
@@ -1220,6 +1235,7 @@ static nc_status gemm_fp8_impl(int M, int N, int K, const uint8_t* A, int64_t ld
   if ((ep == NC_EP_RELU2_SQ_BWD) != (aux != nullptr)) return NC_ERR_ARG;
   if ((ep == NC_EP_QKV_ROPE) != (rope != nullptr)) return NC_ERR_ARG;
   const bool out_f32 = (ep == NC_EP_STORE_F32 || ep == NC_EP_ACCUM_F32);
+  if (amax && (out_f32 || ep == NC_EP_QKV_ROPE)) return NC_ERR_ARG;   // bf16 staged outputs only
   if (ldd < N || ((ldd * (out_f32 ? 4 : 2)) % 16) || (((uintptr_t)D) & 15)) return NC_ERR_ARG;
   if (!g_num_sms) {
     int dev = 0;
@@ -1243,6 +1259,7 @@ static nc_status gemm_fp8_impl(int M, int N, int K, const uint8_t* A, int64_t ld
   p.splits = 1;
   p.rope_T = 1;
   p.scale_a = scale_a; p.scale_b = scale_b;
+  p.amax = amax;
   if (rope) {
     if (BN != 256 || (rope->hd != 64 && rope->hd != 128) || (N % rope->hd) || rope->nh * rope->hd > N ||
         rope->T <= 0 || (((uintptr_t)rope->tab) & 15) || !rope->rstd)
@@ -1280,9 +1297,9 @@ nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, co
 nc_status launch_gemm_fp8_ep(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
                              const float* scale_a, const float* scale_b, int ep, void* D, int64_t ldd, int T, int nh,
                              int hd, const float* tab, int pair_rows, float* rstd, float eps, int32_t* err,
-                             cudaStream_t st, const void* aux, int64_t ldaux) {
+                             cudaStream_t st, const void* aux, int64_t ldaux, unsigned* amax) {
   if (ep != NC_EP_QKV_ROPE)
-    return gemm_fp8_impl(M, N, K, A, lda, B, ldb, scale_a, scale_b, ep, D, ldd, nullptr, err, st, aux, ldaux);
+    return gemm_fp8_impl(M, N, K, A, lda, B, ldb, scale_a, scale_b, ep, D, ldd, nullptr, err, st, aux, ldaux, amax);
   TcRope r{tab, rstd, T, nh, hd, pair_rows, eps};
   return gemm_fp8_impl(M, N, K, A, lda, B, ldb, scale_a, scale_b, ep, D, ldd, &r, err, st);
 }

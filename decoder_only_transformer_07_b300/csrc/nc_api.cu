@@ -227,18 +227,19 @@ static nc_status gemm(nc_model* m, int role, int M, int N, int K, const void* A,
 
 // Attention: bf16 runs on the tensor cores, fp32 on CUDA cores in fp32.
 static nc_status attn_fwd(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv, void* o, float* lse,
-                          int32_t* err, cudaStream_t st) {
-  if (dtype == NC_BF16) return launch_attn_fwd_tc(B, T, H, Hkv, hd, (const bf16*)qkv, (bf16*)o, lse, err, st);
+                          int32_t* err, cudaStream_t st, unsigned* amax = nullptr) {
+  if (dtype == NC_BF16) return launch_attn_fwd_tc(B, T, H, Hkv, hd, (const bf16*)qkv, (bf16*)o, lse, err, st, amax);
   return launch_attn_fwd_simt(dtype, B, T, H, Hkv, hd, qkv, o, lse, st);
 }
 // rstd_qk / rope_tab (bf16 only): fold the RoPE + QK-norm backward into the output;
 // pair_rows > 0 selects the pair-major table layout.
 static nc_status attn_bwd(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv, const void* o,
                           const float* lse, const void* dout, void* dqkv, float* Dv, const float* rstd_qk,
-                          const float* rope_tab, int pair_rows, int32_t* err, cudaStream_t st) {
+                          const float* rope_tab, int pair_rows, int32_t* err, cudaStream_t st,
+                          unsigned* amax = nullptr) {
   if (dtype == NC_BF16)
     return launch_attn_bwd_tc(B, T, H, Hkv, hd, (const bf16*)qkv, (const bf16*)o, lse, (const bf16*)dout,
-                              (bf16*)dqkv, Dv, rstd_qk, rope_tab, pair_rows, err, st);
+                              (bf16*)dqkv, Dv, rstd_qk, rope_tab, pair_rows, err, st, amax);
   if (rstd_qk || rope_tab) return NC_ERR_UNSUPPORTED;
   return launch_attn_bwd_simt(dtype, B, T, H, Hkv, hd, qkv, o, lse, dout, dqkv, Dv, st);
 }
@@ -559,7 +560,7 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
     m->launches += 2;
   }
   auto lin8 = [&](int l, int k, const void* act_in, int K, int Nout, int ep, void* D, int64_t ldd, float* rstdqk,
-                  bool amax_ready) -> nc_status {
+                  bool amax_ready, unsigned* amax_out = nullptr) -> nc_status {
     float* as = m->q8s + (4 * l + k) * 4;
     float* ws = m->q8s + 16 * m->L + (4 * l + k) * 4;
     const uint8_t* w8 = m->q8w + m->q8tl->soff[4 * l + k];
@@ -572,7 +573,7 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
     PROF_SUB(NC_PROF_GEMM, NC_PROF_GEMM_FWD, 2.0 * N * Nout * K, (double)N * K + (double)Nout * K + (double)N * Nout * out,
              launch_gemm_fp8_ep((int)N, Nout, K, m->q8a, K, w8, K, as + 2, ws + 2, ep, D, ldd, T, nh, m->hd,
                                 m->rope_pairs ? m->rope_pairs : m->rope_tab, m->rope_pairs ? m->Tmax : 0, rstdqk,
-                                eps, m->err, st));
+                                eps, m->err, st, nullptr, 0, amax_out));
     m->launches += 2;
     return NC_OK;
   };
@@ -591,13 +592,16 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
       PROF(NC_PROF_NORM, 0, nrm_by,
            launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn1, rstd1, eps, st, (unsigned*)(m->q8s + (4 * l + 0) * 4)));
       NC_TRY(lin8(l, 0, xn1, C, W, NC_EP_QKV_ROPE, qkv, W, rstdqk, true));
+      // the attention epilogue takes the maximum of O for the output projection's quantiser
       PROF(NC_PROF_ATTN_FWD, attn_fl, (double)N * (W + Hd) * a + 4.0 * N * m->H,
-           attn_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->err, st));
-      NC_TRY(lin8(l, 1, o, Hd, C, NC_EP_ACCUM_F32, m->x, C, nullptr, false));
+           attn_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->err, st,
+                    (unsigned*)(m->q8s + (4 * l + 1) * 4)));
+      NC_TRY(lin8(l, 1, o, Hd, C, NC_EP_ACCUM_F32, m->x, C, nullptr, true));
       PROF(NC_PROF_NORM, 0, nrm_by,
            launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn2, rstd2, eps, st, (unsigned*)(m->q8s + (4 * l + 2) * 4)));
-      NC_TRY(lin8(l, 2, xn2, C, F, NC_EP_RELU2_SQ, h, F, nullptr, true));
-      NC_TRY(lin8(l, 3, h, F, C, NC_EP_ACCUM_F32, m->x, C, nullptr, false));
+      // the up-projection's epilogue takes the maximum of relu(u)^2 for the down-projection's quantiser
+      NC_TRY(lin8(l, 2, xn2, C, F, NC_EP_RELU2_SQ, h, F, nullptr, true, (unsigned*)(m->q8s + (4 * l + 3) * 4)));
+      NC_TRY(lin8(l, 3, h, F, C, NC_EP_ACCUM_F32, m->x, C, nullptr, true));
       m->launches += 3;
       continue;
     }
@@ -653,7 +657,8 @@ static nc_status backward_layer_fp8(nc_model* m, int l, int B, int T, float* gra
   float* lse = m->lse + (size_t)l * m->Nmax * m->H;
   const ParamTensor &tq = tensor(m, l, 0), &to = tensor(m, l, 3), &tfc = tensor(m, l, 4), &tpj = tensor(m, l, 5);
   auto slot = [&](int ll, int k) { return m->q8s + 32 * m->L + (4 * ll + k) * 4; };
-  auto dx8 = [&](int k, const void* dy, int K, int Nout, int ep, void* D, const void* aux, bool amax_ready) -> nc_status {
+  auto dx8 = [&](int k, const void* dy, int K, int Nout, int ep, void* D, const void* aux, bool amax_ready,
+                 unsigned* amax_out = nullptr) -> nc_status {
     float* ys = slot(l, k);
     const float* ws = m->q8s + 16 * m->L + (4 * l + k) * 4;
     const uint8_t* wT = m->q8wT + m->q8tl->soff[4 * l + k];
@@ -666,25 +671,28 @@ static nc_status backward_layer_fp8(nc_model* m, int l, int B, int T, float* gra
     PROF_SUB(NC_PROF_GEMM, NC_PROF_GEMM_DX, 2.0 * N * Nout * K,
              (double)N * K + (double)Nout * K + (double)N * Nout * out,
              launch_gemm_fp8_ep(n, Nout, K, m->q8a, K, wT, K, ys + 2, ws + 2, ep, D, Nout, 0, 0, 0, nullptr, 0,
-                                nullptr, 0.f, m->err, st, aux, aux ? Nout : 0));
+                                nullptr, 0.f, m->err, st, aux, aux ? Nout : 0, amax_out));
     m->launches += 2;
     return NC_OK;
   };
   // MLP: x2 = x1 + relu(xn2 Wfc^T)^2 Wproj^T
   NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, F, n, m->dx_act, C, 0, h, F, 0, gw, grads + tpj.off, F, nullptr, 0, st));
-  NC_TRY(dx8(3, m->dx_act, C, F, NC_EP_RELU2_SQ_BWD, m->du, h, true));
+  // the relu^2-backward epilogue takes the maximum of du for the up-projection's dX quantiser
+  NC_TRY(dx8(3, m->dx_act, C, F, NC_EP_RELU2_SQ_BWD, m->du, h, true, (unsigned*)slot(l, 2)));
   NC_TRY(gemm(m, NC_PROF_GEMM_DW, F, C, n, m->du, F, 0, xn2, C, 0, gw, grads + tfc.off, C, nullptr, 0, st));
-  NC_TRY(dx8(2, m->du, F, C, NC_EP_STORE_F32, m->dxn, nullptr, false));
+  NC_TRY(dx8(2, m->du, F, C, NC_EP_STORE_F32, m->dxn, nullptr, true));
   PROF(NC_PROF_NORM, 0, nb_by,
        launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, xn2, rstd2, m->dx, m->dx_act, st, (unsigned*)slot(l, 1)));
   // attention: x1 = x + o Wo^T
   NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, Hd, n, m->dx_act, C, 0, o, Hd, 0, gw, grads + to.off, Hd, nullptr, 0, st));
   NC_TRY(dx8(1, m->dx_act, C, Hd, NC_EP_STORE, m->dout, nullptr, true));
+  // the attention backward's epilogues take the maximum of dq, dk and dv for the dX quantiser
   PROF(NC_PROF_ATTN_BWD, attn_fl, (double)N * (2.0 * W + 2.0 * Hd) * a + 8.0 * N * m->H,
        attn_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, rstdqk,
-                m->rope_pairs ? m->rope_pairs : m->rope_tab, m->rope_pairs ? m->Tmax : 0, m->err, st));
+                m->rope_pairs ? m->rope_pairs : m->rope_tab, m->rope_pairs ? m->Tmax : 0, m->err, st,
+                (unsigned*)slot(l, 0)));
   NC_TRY(gemm(m, NC_PROF_GEMM_DW, W, C, n, m->dqkv, W, 0, xn1, C, 0, gw, grads + tq.off, C, nullptr, 0, st));
-  NC_TRY(dx8(0, m->dqkv, W, C, NC_EP_STORE_F32, m->dxn, nullptr, false));
+  NC_TRY(dx8(0, m->dqkv, W, C, NC_EP_STORE_F32, m->dxn, nullptr, true));
   // the block's input gradient is the previous block's output gradient: its maximum, for that block's Wproj product
   PROF(NC_PROF_NORM, 0, nb_by,
        launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, xn1, rstd1, m->dx, m->dx_act, st,

@@ -92,10 +92,13 @@ nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, co
 // NC_EP_ACCUM_F32, NC_EP_RELU2_SQ, NC_EP_RELU2_SQ_BWD (with aux, bf16
 // relu(u)^2, row pitch ldaux), or NC_EP_QKV_ROPE (then T, nh, hd, tab,
 // pair_rows, rstd and eps as for launch_gemm_tc_qkv_rope; ignored otherwise).
+// amax (bf16 outputs but QKV_ROPE): atomic maximum of |D| as stored, as float
+// bits, for the per-tensor quantiser of D.
 nc_status launch_gemm_fp8_ep(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
                              const float* scale_a, const float* scale_b, int ep, void* D, int64_t ldd, int T, int nh,
                              int hd, const float* tab, int pair_rows, float* rstd, float eps, int32_t* err,
-                             cudaStream_t st, const void* aux = nullptr, int64_t ldaux = 0);
+                             cudaStream_t st, const void* aux = nullptr, int64_t ldaux = 0,
+                             unsigned* amax = nullptr);
 // Per-tensor E4M3 quantisation of n fp32 / bf16 values: stats (device, 3
 // floats) gets {amax, scale, scale_inv}; y the codes.
 nc_status launch_quantize_fp8(int dtype, const void* x, int64_t n, uint8_t* y, float* stats, cudaStream_t st);
@@ -115,14 +118,18 @@ nc_status launch_attn_bwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, 
 // bf16 causal GQA flash attention on tcgen05 tensor cores (head_dim 64 or 128).
 // err (device int32, may be NULL) receives NC_DEVERR_TIMEOUT if a bounded wait expires.
 nc_status launch_attn_fwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, bf16* o, float* lse,
-                             int32_t* err, cudaStream_t st);
+                             int32_t* err, cudaStream_t st,
+                             unsigned* amax = nullptr);
 // With rstd_qk and rope_tab (both or neither), dq and dk are returned through the
 // per-head RMSNorm backward and the transposed rotation (the RoPE + QK-norm
 // backward fused into the output epilogue).  rope_tab is [T][hd/2][2]
 // (rope_pair_rows = 0) or pair-major [hd/4][rope_pair_rows][4] (rope_pair_rows >= T).
+// amax (both directions, may be NULL): atomic maximum of |output| as stored (O;
+// dq, dk and dv), as float bits, for the per-tensor quantiser of that output.
 nc_status launch_attn_bwd_tc(int B, int T, int H, int Hkv, int hd, const bf16* qkv, const bf16* o, const float* lse,
                              const bf16* dout, bf16* dqkv, float* Dv, const float* rstd_qk, const float* rope_tab,
-                             int rope_pair_rows, int32_t* err, cudaStream_t st);
+                             int rope_pair_rows, int32_t* err, cudaStream_t st,
+                             unsigned* amax = nullptr);
 
 // 2D bf16 TMA descriptor over a row-major [outer][inner] matrix with leading
 // dimension ld (elements), box {box_inner, box_outer}, 128-byte swizzle.
