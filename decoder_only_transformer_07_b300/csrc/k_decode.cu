@@ -617,6 +617,203 @@ __global__ void __launch_bounds__(SK_WARPS * 32)
   griddep_launch_dependents();
 }
 
+// The bf16 skinny GEMM for 2 <= M <= 8 rows: each warp streams NCOL = 4
+// weight columns at once over a slice of K, so that every shared-memory load
+// and conversion of the A rows serves four columns, and the products run two
+// lanes per instruction (fma.rn.f32x2).  A CTA's 8 warps are 8 / ks column
+// groups times ks K slices; slice partials are summed through shared memory in
+// slice order (deterministic).  All of A is staged once (it must fit); with
+// NORM, A = act(x * rstd(x)) as in k_gemm_skinny.  W loads before griddep_wait.
+constexpr int SC_NCOL = 4;
+constexpr int SC_P = 2;   // 16-byte pieces per column and lane in one batch
+template <int MB, bool NORM>
+__global__ void __launch_bounds__(SK_WARPS * 32)
+    k_gemm_skinny_cols(int M, int N, int K, int ks, const void* __restrict__ Ain, int64_t lda,
+                       const bf16* __restrict__ W, int64_t ldw, int ep, void* __restrict__ D, int64_t ldd, float eps) {
+  constexpr int EPU = 8;
+  constexpr int BATCH = 32 * SC_P * EPU;                // K columns of one batch of a slice
+  extern __shared__ __align__(16) uint8_t sk_smem[];
+  bf16* xs = reinterpret_cast<bf16*>(sk_smem);          // [MB][K]
+  float* rs = reinterpret_cast<float*>(sk_smem + (size_t)MB * K * sizeof(bf16));
+  float* red = rs + MB;                                 // [SK_WARPS][MB] (NORM) then [SK_WARPS][NCOL][MB]
+  const bf16* A = reinterpret_cast<const bf16*>(Ain);
+  const float* X = reinterpret_cast<const float*>(Ain);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cg = warp / ks, sl = warp - cg * ks;        // column group and K slice of this warp
+  const int cpc = SC_NCOL * (SK_WARPS / ks);            // columns per CTA group
+  const int ngroups = (N + cpc - 1) / cpc;
+  const int ksl = ((K + ks - 1) / ks + EPU - 1) / EPU * EPU;
+  const int k_lo = min(K, sl * ksl), k_hi = min(K, k_lo + ksl);
+  const int nb = (ksl + BATCH - 1) / BATCH;   // the same for every warp: the group's end is a CTA barrier
+  auto load = [&](int g, int b, uint4 (*w)[SC_P]) {
+#pragma unroll
+    for (int c = 0; c < SC_NCOL; ++c) {
+      const int n = g * cpc + cg * SC_NCOL + c;
+#pragma unroll
+      for (int u = 0; u < SC_P; ++u) {
+        const int k = k_lo + b * BATCH + (32 * u + lane) * EPU;
+        if (n < N && k < k_hi) w[c][u] = __ldg(reinterpret_cast<const uint4*>(W + (int64_t)n * ldw + k));
+      }
+    }
+  };
+  uint4 w[SC_NCOL][SC_P], wn[SC_NCOL][SC_P];
+  int g = blockIdx.x;
+  if (g < ngroups) load(g, 0, w);   // in flight while the previous kernel finishes and A is prepared
+  griddep_wait();
+  if (NORM) {
+    float ss[MB];
+#pragma unroll
+    for (int m = 0; m < MB; ++m) ss[m] = 0.f;
+    for (int c = threadIdx.x; c < K / 4; c += SK_WARPS * 32) {
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        if (m < M) {
+          const float4 v = *reinterpret_cast<const float4*>(X + (int64_t)m * lda + 4 * c);
+          ss[m] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MB; ++m) {
+      float v = ss[m];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) red[warp * MB + m] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < M) {
+      float t = 0.f;
+      for (int q = 0; q < SK_WARPS; ++q) t += red[q * MB + threadIdx.x];
+      rs[threadIdx.x] = rsqrtf(t / (float)K + eps);
+    }
+    __syncthreads();
+  }
+  for (int i = threadIdx.x * 8; i < MB * K; i += SK_WARPS * 32 * 8) {   // all of A into xs
+    const int m = i / K, k = i - m * K;
+    if (m < M) {
+      if (NORM) {
+        const float r = rs[m];
+        const float4 a = *reinterpret_cast<const float4*>(X + (int64_t)m * lda + k);
+        const float4 b = *reinterpret_cast<const float4*>(X + (int64_t)m * lda + k + 4);
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) st_f(&xs[m * K + k + e], v[e] * r);
+      } else {
+        *reinterpret_cast<uint4*>(&xs[m * K + k]) = *reinterpret_cast<const uint4*>(A + (int64_t)m * lda + k);
+      }
+    }
+  }
+  __syncthreads();
+  float* part = red + SK_WARPS * MB;   // [SK_WARPS][NCOL][MB]
+  int b = 0;
+  float2 acc[SC_NCOL][MB];
+#pragma unroll
+  for (int c = 0; c < SC_NCOL; ++c)
+#pragma unroll
+    for (int m = 0; m < MB; ++m) acc[c][m] = make_float2(0.f, 0.f);
+  while (g < ngroups) {
+    int g2 = g, b2 = b + 1;
+    if (b2 == nb) {
+      b2 = 0;
+      g2 = g + gridDim.x;
+    }
+    if (g2 < ngroups) load(g2, b2, wn);
+#pragma unroll
+    for (int u = 0; u < SC_P; ++u) {
+      const int k = k_lo + b * BATCH + (32 * u + lane) * EPU;
+      if (k < k_hi) {
+        float2 wf[SC_NCOL][4];
+#pragma unroll
+        for (int c = 0; c < SC_NCOL; ++c) {
+          const uint32_t* q = reinterpret_cast<const uint32_t*>(&w[c][u]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) wf[c][e] = make_float2(__uint_as_float(q[e] << 16), __uint_as_float(q[e] & 0xffff0000u));
+        }
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+          if (m < M) {
+            const uint4 xa = *reinterpret_cast<const uint4*>(xs + (int64_t)m * K + k);
+            const uint32_t* q = reinterpret_cast<const uint32_t*>(&xa);
+            float2 x[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] = make_float2(__uint_as_float(q[e] << 16), __uint_as_float(q[e] & 0xffff0000u));
+#pragma unroll
+            for (int c = 0; c < SC_NCOL; ++c)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[c][m] = fma2(x[e], wf[c][e], acc[c][m]);
+          }
+        }
+      }
+    }
+    if (b == nb - 1) {
+      // lane sums, then the slices' partials in slice order
+#pragma unroll
+      for (int c = 0; c < SC_NCOL; ++c) {
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+          float v = acc[c][m].x + acc[c][m].y;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) part[(warp * SC_NCOL + c) * MB + m] = v;
+          acc[c][m] = make_float2(0.f, 0.f);
+        }
+      }
+      __syncthreads();
+      if (sl == 0 && lane < SC_NCOL * MB) {
+        const int c = lane / MB, m = lane - c * MB;
+        const int n = g * cpc + cg * SC_NCOL + c;
+        if (m < M && n < N) {
+          float v = 0.f;
+          for (int q = 0; q < ks; ++q) v += part[((cg * ks + q) * SC_NCOL + c) * MB + m];
+          if (ep == NC_EP_STORE_F32) reinterpret_cast<float*>(D)[(int64_t)m * ldd + n] = v;
+          else if (ep == NC_EP_ACCUM_F32) reinterpret_cast<float*>(D)[(int64_t)m * ldd + n] += v;
+          else {
+            if (ep == NC_EP_RELU2_SQ) { v = fmaxf(v, 0.f); v *= v; }
+            st_f(reinterpret_cast<bf16*>(D) + (int64_t)m * ldd + n, v);
+          }
+        }
+      }
+      __syncthreads();   // part is rewritten by the next group
+      if (g2 >= ngroups) griddep_launch_dependents();
+    }
+#pragma unroll
+    for (int c = 0; c < SC_NCOL; ++c)
+#pragma unroll
+      for (int u = 0; u < SC_P; ++u) w[c][u] = wn[c][u];
+    g = g2;
+    b = b2;
+  }
+  griddep_launch_dependents();
+}
+
+template <int MB>
+size_t sc_smem_bytes(int K) {
+  return (size_t)MB * K * sizeof(bf16) + (size_t)(MB + SK_WARPS * MB + SK_WARPS * SC_NCOL * MB) * sizeof(float);
+}
+constexpr int SC_SMEM_MAX = 110 * 1024;   // two CTAs per SM
+
+template <int MB, bool NORM>
+nc_status skinny_cols_t(int M, int N, int K, const void* A, int64_t lda, const bf16* W, int64_t ldw, int ep, void* D,
+                        int64_t ldd, float eps, cudaStream_t st) {
+  // K slices per column group: doubled while the CTAs do not cover the SMs and
+  // a slice keeps at least one 16-byte piece per lane
+  int ks = 1;
+  while (ks < SK_WARPS && (int64_t)((N + SC_NCOL * (SK_WARPS / ks) - 1) / (SC_NCOL * (SK_WARPS / ks))) < g_num_sms &&
+         K / (2 * ks) >= 32 * 8)
+    ks *= 2;
+  const int cpc = SC_NCOL * (SK_WARPS / ks);
+  const int ngroups = (N + cpc - 1) / cpc;
+  const int grid = std::min(ngroups, 2 * g_num_sms);
+  NC_CUDA_TRY(launch_pdl(k_gemm_skinny_cols<MB, NORM>, dim3(grid), dim3(SK_WARPS * 32), sc_smem_bytes<MB>(K), st,
+                         M, N, K, ks, A, lda, W, ldw, ep, D, ldd, eps));
+  return NC_OK;
+}
+
+template <int MB, bool NORM>
+cudaError_t sc_attr() {
+  return cudaFuncSetAttribute(k_gemm_skinny_cols<MB, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_SMEM_MAX);
+}
+
 template <typename E, int MB>
 size_t sk_smem_bytes(int KC) {
   return (size_t)MB * KC * sizeof(E) + (size_t)(MB + SK_WARPS * MB) * sizeof(float);
@@ -644,6 +841,13 @@ template <typename E, bool NORM>
 nc_status skinny_e(int M, int N, int K, const void* A, int64_t lda, const E* W, int64_t ldw, int ep, void* D,
                    int64_t ldd, float eps, cudaStream_t st) {
   if (M <= 1) return skinny_t<E, 1, NORM>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
+  if constexpr (sizeof(E) == 2) {
+    if (M <= 8 && sc_smem_bytes<8>(K) <= (size_t)SC_SMEM_MAX) {
+      if (M <= 2) return skinny_cols_t<2, NORM>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
+      if (M <= 4) return skinny_cols_t<4, NORM>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
+      return skinny_cols_t<8, NORM>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
+    }
+  }
   if (M <= 2) return skinny_t<E, 2, NORM>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
   if (M <= 4) return skinny_t<E, 4, NORM>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
   if (M <= 8 || NORM) return skinny_t<E, 8, NORM>(M, N, K, A, lda, W, ldw, ep, D, ldd, eps, st);
@@ -667,7 +871,8 @@ nc_status skinny_prepare() {
       sk_attr<bf16, 4, true>(), sk_attr<bf16, 8, true>(), sk_attr<float, 1, false>(), sk_attr<float, 2, false>(),
       sk_attr<float, 4, false>(), sk_attr<float, 8, false>(), sk_attr<float, 16, false>(),
       sk_attr<float, 32, false>(), sk_attr<float, 1, true>(), sk_attr<float, 2, true>(), sk_attr<float, 4, true>(),
-      sk_attr<float, 8, true>()};
+      sk_attr<float, 8, true>(), sc_attr<2, false>(), sc_attr<4, false>(), sc_attr<8, false>(),
+      sc_attr<2, true>(), sc_attr<4, true>(), sc_attr<8, true>()};
   for (cudaError_t x : e)
     if (x != cudaSuccess) return NC_ERR_CUDA;
   done = true;

@@ -138,7 +138,7 @@ def test_gemm_few_rows(M, dt):
     _assert_gemm(_gemm_case(M, 384, 256, 1, 1, nc.EP_ACCUM_F32, dt, seed=50 + M), dt, 256, nc.EP_ACCUM_F32)
 
 
-@pytest.mark.parametrize("M", [1, 5, 17, 32])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 17, 32])
 @pytest.mark.parametrize("dt", [BF16, F32])
 @pytest.mark.parametrize("ep", [nc.EP_STORE, nc.EP_STORE_F32, nc.EP_ACCUM_F32, nc.EP_RELU2_SQ])
 @pytest.mark.parametrize("K", [1096, 4104])
