@@ -524,12 +524,13 @@ __device__ __forceinline__ void at_out_tile(const AtShape& sh, uint32_t tacc, co
   };
   float dot = 0.f;
 #pragma unroll 1
-  for (int c = 0; c < HD; c += 32) {
-    uint32_t v[32];
+  for (int c = 0; c < HD; c += 64) {   // two loads under one wait
+    uint32_t v[64];
     tmem_ld_32x32b_x32(tacc + c, v);
+    tmem_ld_32x32b_x32(tacc + c + 32, v + 32);
     tmem_ld_wait();
 #pragma unroll
-    for (int q = 0; q < 32; q += 8) {
+    for (int q = 0; q < 64; q += 8) {
       float y[8];
       y8(c + q, y);
 #pragma unroll
@@ -588,23 +589,21 @@ __device__ __forceinline__ void at_out_box128(uint32_t tacc, int hf, float mul, 
                                               int x, int y, int bz, int T, float& am, bool track) {
   const int lane = threadIdx.x & 31;
   const uint32_t srow = smem_u32(box) + (uint32_t)lane * 128u;
-#pragma unroll 1
-  for (int c = 0; c < 2; ++c) {
-    uint32_t v[32];
-    tmem_ld_32x32b_x32(tacc + hf * 64 + 32 * c, v);
-    tmem_ld_wait();
-    if (track && y + lane < T) {   // rows past the end are not stored
+  uint32_t v[64];   // both loads under one wait
+  tmem_ld_32x32b_x32(tacc + hf * 64, v);
+  tmem_ld_32x32b_x32(tacc + hf * 64 + 32, v + 32);
+  tmem_ld_wait();
+  if (track && y + lane < T) {   // rows past the end are not stored
 #pragma unroll
-      for (int e = 0; e < 32; ++e) am = fmaxf(am, fabsf(__uint_as_float(v[e])) * mul);
-    }
-#pragma unroll
-    for (int e = 0; e < 32; e += 8)
-      st_shared_v4(srow + ((((uint32_t)(4 * c + e / 8) ^ (uint32_t)lane) & 7u) << 4),
-                   pack2(__uint_as_float(v[e]) * mul, __uint_as_float(v[e + 1]) * mul),
-                   pack2(__uint_as_float(v[e + 2]) * mul, __uint_as_float(v[e + 3]) * mul),
-                   pack2(__uint_as_float(v[e + 4]) * mul, __uint_as_float(v[e + 5]) * mul),
-                   pack2(__uint_as_float(v[e + 6]) * mul, __uint_as_float(v[e + 7]) * mul));
+    for (int e = 0; e < 64; ++e) am = fmaxf(am, fabsf(__uint_as_float(v[e])) * mul);
   }
+#pragma unroll
+  for (int e = 0; e < 64; e += 8)
+    st_shared_v4(srow + ((((uint32_t)(e / 8) ^ (uint32_t)lane) & 7u) << 4),
+                 pack2(__uint_as_float(v[e]) * mul, __uint_as_float(v[e + 1]) * mul),
+                 pack2(__uint_as_float(v[e + 2]) * mul, __uint_as_float(v[e + 3]) * mul),
+                 pack2(__uint_as_float(v[e + 4]) * mul, __uint_as_float(v[e + 5]) * mul),
+                 pack2(__uint_as_float(v[e + 6]) * mul, __uint_as_float(v[e + 7]) * mul));
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0 && y < T) {
