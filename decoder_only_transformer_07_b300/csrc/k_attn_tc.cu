@@ -390,11 +390,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const uint32_t sbox = smem_u32(smem + L::OFF_Q + i * L::TILE + quarter * 8192) + (uint32_t)lane * 128u;
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
-#pragma unroll 1
+          uint32_t ovp[64];   // a box's two accumulator loads under one wait
+          tmem_ld_32x32b_x32(tO + 64 * c, ovp);
+          tmem_ld_32x32b_x32(tO + 64 * c + 32, ovp + 32);
+          tmem_ld_wait();
+#pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
-            uint32_t ov[32];
-            tmem_ld_32x32b_x32(tO + 64 * c + 32 * cc, ov);
-            tmem_ld_wait();
+            const uint32_t* ov = ovp + 32 * cc;
             if (AMAX) {
 #pragma unroll
               for (int e = 0; e < 32; ++e) am = fmaxf(am, fabsf(__uint_as_float(ov[e])));
