@@ -52,7 +52,7 @@ DESCR = {
 # one step (`bench.py --op gemmset --config <w>`, each launch at full size),
 # weighted by the step's call counts.  A workload is left out (null traffic)
 # whenever the GEMM kernels change and the capture is not repeated.
-GEMM_DRAM_BYTES_PER_CALL = {"d26": 9.115e+08, "d20": 1.263e+09, "d24gqa": 7.147e+08, "d12": 6.807e+08}
+GEMM_DRAM_BYTES_PER_CALL = {"d26": 9.104e+08, "d20": 1.262e+09, "d24gqa": 7.151e+08, "d12": 6.803e+08}
 # CPU-oracle sample (tokens of one sequence) per workload: ~10-30 s of fp64 work
 CPU_SAMPLE_T = {"tiny": 64, "d12": 128, "d20": 64, "d26": 48, "d24gqa": 48}
 
