@@ -213,9 +213,9 @@ def linear(cfg, x, w):
     to E4M3 with current scaling, the activation from its bfloat16 value (the
     tensor the layer reads) and the weight from its float32 master value, and
     the product of the decoded values is taken exactly (fp32 accumulation on
-    the device).  The backward is unchanged: the gradient passes through each
-    quantiser as the identity, so dX = dY w and dW = dY^T x use the
-    unquantised operands.
+    the device).  The gradient passes through each quantiser as the identity
+    (straight-through); the backward's own products dX = dY w and
+    dW = dY^T x multiply E4M3 operands too (``linear_dx``, ``linear_dw``).
     """
     if not cfg.fp8:
         return x @ w.T
@@ -230,11 +230,22 @@ def linear_dx(cfg, dy, w):
     With cfg.fp8 both operands are E4M3 as well: the bf16 value of dY
     quantised per tensor with current scaling (its own absolute maximum), and
     the weight with the same codes and factor as in the forward (the same
-    tensor, read transposed).  The weight gradient dW = dY^T x is not
-    quantised."""
+    tensor, read transposed)."""
     if not cfg.fp8:
         return dy @ w
     return quantize_dequantize(bf16_round(dy)) @ quantize_dequantize(w)
+
+
+def linear_dw(cfg, dy, x):
+    """The weight gradient of ``linear``: dW = dY^T x (rows of dy and x are tokens).
+
+    With cfg.fp8 both operands are E4M3: dY with the codes and factor of its
+    input-gradient product (``linear_dx``), x with the codes and factor of the
+    forward product (``linear``), so each tensor is quantised once; the
+    products of the decoded values accumulate exactly (fp32 on the device)."""
+    if not cfg.fp8:
+        return dy.T @ x
+    return quantize_dequantize(bf16_round(dy)).T @ quantize_dequantize(bf16_round(x))
 
 
 def softcap(z, c):
@@ -303,14 +314,14 @@ def block_backward(cfg, W, l, x, dx2, cos, sin, G):
     _, s = block_forward(cfg, W, l, x, cos, sin, keep=True)
     N = B * T
     # MLP: x2 = x1 + relu(bn Wfc^T)^2 Wproj^T
-    G[p + "wproj"] += dx2.reshape(N, C).T @ s["hmid"].reshape(N, -1)
+    G[p + "wproj"] += linear_dw(cfg, dx2.reshape(N, C), s["hmid"].reshape(N, -1))
     dh = linear_dx(cfg, dx2, W[p + "wproj"])
     du = dh * 2.0 * s["r"]
-    G[p + "wfc"] += du.reshape(N, -1).T @ s["bn"].reshape(N, C)
+    G[p + "wfc"] += linear_dw(cfg, du.reshape(N, -1), s["bn"].reshape(N, C))
     dbn = linear_dx(cfg, du, W[p + "wfc"])
     dx1 = dx2 + rms_norm_bwd(dbn, s["bn"], s["rstd2"])
     # attention output projection: x1 = x + o2 Wo^T
-    G[p + "wo"] += dx1.reshape(N, C).T @ s["o2"].reshape(N, -1)
+    G[p + "wo"] += linear_dw(cfg, dx1.reshape(N, C), s["o2"].reshape(N, -1))
     do2 = linear_dx(cfg, dx1, W[p + "wo"])
     do = do2.reshape(B, T, H, hd).transpose(0, 2, 1, 3)
     dqn = np.zeros((B, H, T, hd))
@@ -329,9 +340,16 @@ def block_backward(cfg, W, l, x, dx2, cos, sin, G):
     dk2 = dk.transpose(0, 2, 1, 3).reshape(N, Hkv * hd)
     dv2 = dv.transpose(0, 2, 1, 3).reshape(N, Hkv * hd)
     a = s["a"].reshape(N, C)
-    G[p + "wq"] += dq2.T @ a
-    G[p + "wk"] += dk2.T @ a
-    G[p + "wv"] += dv2.T @ a
+    if cfg.fp8:   # one operand [dq | dk | dv], as the fused projection's weight gradient multiplies it
+        gqkv = linear_dw(cfg, np.concatenate([dq2, dk2, dv2], axis=-1), a)
+        nq, nk = dq2.shape[1], dk2.shape[1]
+        G[p + "wq"] += gqkv[:nq]
+        G[p + "wk"] += gqkv[nq:nq + nk]
+        G[p + "wv"] += gqkv[nq + nk:]
+    else:
+        G[p + "wq"] += dq2.T @ a
+        G[p + "wk"] += dk2.T @ a
+        G[p + "wv"] += dv2.T @ a
     if cfg.fp8:   # one operand [dq | dk | dv] against [Wq; Wk; Wv], as the fused projection's backward multiplies them
         da = linear_dx(cfg, np.concatenate([dq2, dk2, dv2], axis=-1),
                        np.concatenate([W[p + "wq"], W[p + "wk"], W[p + "wv"]], axis=0))

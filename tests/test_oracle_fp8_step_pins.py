@@ -5,9 +5,9 @@ recipe): each block's four linear layers multiply E4M3 operands, the bf16
 activation and the fp32 master weight, each quantised per tensor with
 current scaling (one tensor [Wq; Wk; Wv] for the fused projection); the
 input-gradient products dX = dY W multiply E4M3 operands as well (dY's bf16
-value with its own per-tensor scale, W with its forward codes); the weight
-gradients use the unquantised operands, and the quantisers pass gradients
-through unchanged.
+value with its own per-tensor scale, W with its forward codes), and so do the
+weight-gradient products dW = dY^T X (dY with those codes, X with its forward
+codes); the quantisers pass gradients through unchanged.
 
 Pins from outside the oracle:
 * with the quantiser and the bf16 rounding replaced by identities the step is
@@ -18,9 +18,9 @@ Pins from outside the oracle:
   dequantisation factors scale exactly, and the norms remove the scale);
 * every quantised product lies within the E4M3 error bound of the exact one;
 * the 8-bit step's loss stays close to the fp64 loss;
-* the input-gradient products dX = dY w are E4M3 too (dY with its own
-  per-tensor scale): within the same bound, and scaling the loss by a power
-  of two scales every gradient exactly.
+* the input-gradient products dX = dY w and the weight-gradient products
+  dW = dY^T x are E4M3 too (dY with its own per-tensor scale): within the same
+  bound, and scaling the loss by a power of two scales every gradient exactly.
 Planted mistakes in the dequantisation and in the scaling of dY are caught.
 """
 import numpy as np
@@ -131,6 +131,45 @@ def test_quantised_input_gradient_within_the_e4m3_bound():
     assert np.median(err / (ay @ aw)) > 2.0 ** -9
 
 
+def test_quantised_weight_gradient_within_the_e4m3_bound():
+    """dW = dY^T x with both operands E4M3 (dY and x from their bf16 values): the
+    bound of the forward product with the token sum as the contraction."""
+    rng = np.random.default_rng(51)
+    cfg = small_cfg()
+    dy = rng.normal(0.0, 1e-3, size=(53, 29)) * np.exp(rng.normal(0.0, 1.0, size=(53, 1)))
+    x = rng.normal(0.0, 1.0, size=(53, 48)) * np.exp(rng.normal(0.0, 1.0, size=(53, 1)))
+    got = M.linear_dw(cfg, dy, x)
+    exact = dy.T @ x
+    _, _, ys, _ = F8.quantize(M.bf16_round(dy).astype(np.float32))
+    _, _, xs, _ = F8.quantize(M.bf16_round(x).astype(np.float32))
+    qy, qx = 2.0 ** -10 / float(ys), 2.0 ** -10 / float(xs)
+    ay, ax = np.abs(dy), np.abs(x)
+    rel = (1 + 2.0 ** -9) ** 2 * (1 + 2.0 ** -4) ** 2 - 1
+    bound = rel * (ay.T @ ax) + qy * (1 + 2.0 ** -4) * (1 + 2.0 ** -9) * ax.sum(axis=0)[None, :] + \
+        qx * (1 + 2.0 ** -4) * (1 + 2.0 ** -9) * ay.sum(axis=0)[:, None] + qy * qx * dy.shape[0]
+    err = np.abs(got - exact)
+    assert np.all(err <= bound)
+    assert np.median(err / (ay.T @ ax)) > 2.0 ** -9
+    # and it is the plain product without the 8-bit reading
+    assert np.array_equal(M.linear_dw(small_cfg(fp8=False), dy, x), exact)
+
+
+def test_weight_gradient_lies_on_the_e4m3_product_grid():
+    """Every E4M3 value is a multiple of 2^-9 (the subnormal step), so a sum of
+    products of two of them is a multiple of 2^-18: dW divided by both
+    dequantisation factors lands on that grid (to fp64 rounding), which a dW
+    with either operand left unquantised does not."""
+    rng = np.random.default_rng(52)
+    cfg = small_cfg()
+    dy = rng.normal(0.0, 1e-3, size=(37, 21))
+    x = rng.normal(0.0, 1.0, size=(37, 19))
+    _, _, _, siy = F8.quantize(M.bf16_round(dy).astype(np.float32))
+    _, _, _, six = F8.quantize(M.bf16_round(x).astype(np.float32))
+    v = M.linear_dw(cfg, dy, x) / (float(siy) * float(six)) * 2.0 ** 18
+    assert np.max(np.abs(v - np.round(v))) < 1e-3
+    assert np.max(np.abs(v)) > 1e6          # far from trivially small
+
+
 def test_gradient_scale_by_a_power_of_two_is_exact():
     """Current (per-tensor) scaling of every dY: scaling the loss by 2^k scales
     every dY by 2^k, which leaves its codes unchanged and its factor exact, so
@@ -167,12 +206,30 @@ def _linear_dx_fixed_scale(cfg, dy, w):
     return F8.e4m3_decode(codes) @ M.quantize_dequantize(w)
 
 
+def _linear_dw_fixed_scale(cfg, dy, x):
+    """dY quantised with a fixed unit scale in the weight gradient."""
+    if not cfg.fp8:
+        return dy.T @ x
+    codes = F8.e4m3_encode(np.clip(M.bf16_round(dy).astype(np.float32), -448, 448))
+    return F8.e4m3_decode(codes).T @ M.quantize_dequantize(M.bf16_round(x))
+
+
+def _linear_dw_x_unquantised(cfg, dy, x):
+    """The weight gradient with x left at its bf16 value."""
+    if not cfg.fp8:
+        return dy.T @ x
+    return M.quantize_dequantize(M.bf16_round(dy)).T @ M.bf16_round(x)
+
+
 MUTANTS = {"dequantised with the scale": ("quantize_dequantize", _dequantise_with_scale),
            "codes used without their factor": ("quantize_dequantize", _no_dequantisation),
-           "input gradient with a fixed scale": ("linear_dx", _linear_dx_fixed_scale)}
+           "input gradient with a fixed scale": ("linear_dx", _linear_dx_fixed_scale),
+           "weight gradient with a fixed scale": ("linear_dw", _linear_dw_fixed_scale),
+           "weight gradient with x unquantised": ("linear_dw", _linear_dw_x_unquantised)}
 
 PINS = [test_power_of_two_scaling_leaves_the_8bit_model_unchanged, test_quantised_product_within_the_e4m3_bound,
         test_8bit_step_loss_close_to_fp64, test_quantised_input_gradient_within_the_e4m3_bound,
+        test_quantised_weight_gradient_within_the_e4m3_bound, test_weight_gradient_lies_on_the_e4m3_product_grid,
         test_gradient_scale_by_a_power_of_two_is_exact]
 
 
