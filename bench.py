@@ -481,7 +481,7 @@ def measure(w, name, args, world, rank, dev, gpu_traffic=True, fp8=False):
     """Time `args.steps` training steps of workload w (device-resident inputs),
     then the same through the host-buffer entry point; returns the fields of
     the bench line for this workload.  fp8: the 8-bit step (the blocks'
-    forward and input-gradient linears on E4M3 operands)."""
+    linear products on E4M3 operands)."""
     import ctypes
     import torch
     import decoder_only_transformer_07_b300 as nc
@@ -648,10 +648,9 @@ def main():
     fp8_step = None
     if (args.fp8_step if args.fp8_step is not None else (extras != "")) and w.dtype == "bf16":
         fp8_step = measure(w, args.config, args, world, rank, dev, fp8=True)
-        fp8_step["dtype"] = "e4m3 operands in the blocks' forward and input-gradient linears, bf16 elsewhere"
+        fp8_step["dtype"] = "e4m3 operands in the blocks' linear products (forward, dX, dW), bf16 elsewhere"
         fp8_step["note"] = ("the 8-bit training step (nc_config.fp8 = 1), same workload; MFU is quoted against the "
-                            "bf16 peak, and the GEMM roofline mixes 8-bit forward and input-gradient products with bf16 "
-                            "weight-gradient products")
+                            "bf16 peak, and the GEMM roofline mixes the blocks' 8-bit products with the bf16 lm_head")
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

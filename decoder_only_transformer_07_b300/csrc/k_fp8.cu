@@ -144,6 +144,77 @@ __global__ void __launch_bounds__(FP8_THREADS) k_fp8_cast_scaled(const T* __rest
   if (blockIdx.x == 0 && threadIdx.x < n - n8) y[n8 + threadIdx.x] = (uint8_t)e4m3(to_f32(x[n8 + threadIdx.x]) * s);
 }
 
+// The scaled cast of a [rows][cols] bf16 tensor written in both layouts: y
+// [rows][cols] as k_fp8_cast_scaled writes it, and yt [cols][ldt] (ldt >= rows,
+// a multiple of 16), its transpose: the K-major operand of a product that
+// contracts over rows.  One block per 64 x 64 tile through shared memory; the
+// tile's own rows and columns past the end are skipped.
+__global__ void __launch_bounds__(256) k_fp8_cast_dual(const bf16* __restrict__ x, int rows, int cols,
+                                                       float* __restrict__ stats, uint8_t* __restrict__ y,
+                                                       uint8_t* __restrict__ yt, int64_t ldt) {
+  __shared__ __align__(16) uint8_t tile[64][80];
+  const float s = fp8_scale_of(__uint_as_float(*reinterpret_cast<const unsigned*>(stats)));
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    stats[1] = s;
+    stats[2] = 1.f / s;
+  }
+  const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64, t = threadIdx.x;
+  {   // thread t: row r0 + t / 4, columns c0 + 16 (t % 4) .. +16
+    const int r = t >> 2, cc = (t & 3) * 16;
+    const int gr = r0 + r, gc = c0 + cc;
+    uint32_t q[4] = {0u, 0u, 0u, 0u};
+    if (gr < rows) {
+      const bf16* xr = x + (int64_t)gr * cols + gc;
+      uint8_t* yr = y + (int64_t)gr * cols + gc;
+      if (gc + 16 <= cols && (cols & 15) == 0) {
+        const uint4 a = *reinterpret_cast<const uint4*>(xr), b = *reinterpret_cast<const uint4*>(xr + 8);
+        const bf16* ha = reinterpret_cast<const bf16*>(&a);
+        const bf16* hb = reinterpret_cast<const bf16*>(&b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          q[e >> 2] |= e4m3(__bfloat162float(ha[e]) * s) << (8 * (e & 3));
+          q[2 + (e >> 2)] |= e4m3(__bfloat162float(hb[e]) * s) << (8 * (e & 3));
+        }
+        *reinterpret_cast<uint4*>(yr) = make_uint4(q[0], q[1], q[2], q[3]);
+      } else {
+        for (int e = 0; e < 16 && gc + e < cols; ++e) {
+          const uint32_t c = e4m3(__bfloat162float(xr[e]) * s);
+          q[e >> 2] |= c << (8 * (e & 3));
+          yr[e] = (uint8_t)c;
+        }
+      }
+    }
+    *reinterpret_cast<uint4*>(&tile[r][cc]) = make_uint4(q[0], q[1], q[2], q[3]);
+  }
+  __syncthreads();
+  {   // thread t: transposed row c0 + t / 4 (a column of x), rows r0 + 16 (t % 4) .. +16
+    const int c = t >> 2, rr = (t & 3) * 16;
+    const int gc = c0 + c, gr = r0 + rr;
+    if (gc < cols && gr < rows) {
+      uint32_t q[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) q[e >> 2] |= (uint32_t)tile[rr + e][c] << (8 * (e & 3));
+      uint8_t* yo = yt + (int64_t)gc * ldt + gr;
+      if (gr + 16 <= rows) {
+        *reinterpret_cast<uint4*>(yo) = make_uint4(q[0], q[1], q[2], q[3]);
+      } else {
+        for (int e = 0; gr + e < rows; ++e) yo[e] = (uint8_t)(q[e >> 2] >> (8 * (e & 3)));
+      }
+    }
+  }
+}
+
+nc_status launch_fp8_cast_dual(const void* x, int rows, int cols, float* stats, uint8_t* y, uint8_t* yt, int64_t ldt,
+                               cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return NC_OK;
+  if (!x || !stats || !y || !yt || ldt < rows || (ldt & 15) || (((uintptr_t)x) & 15) || (((uintptr_t)y) & 15) ||
+      (((uintptr_t)yt) & 15) || rows > 65535 * 64)
+    return NC_ERR_ARG;
+  k_fp8_cast_dual<<<dim3((unsigned)((cols + 63) / 64), (unsigned)((rows + 63) / 64)), 256, 0, st>>>(
+      (const bf16*)x, rows, cols, stats, y, yt, ldt);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
 static unsigned fp8_grid(int64_t n) {
   if (!g_num_sms) {
     int dev = 0;

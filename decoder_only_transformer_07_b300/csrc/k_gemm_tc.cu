@@ -865,9 +865,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       } else if (p.splits > 1) {
         // split-K slice: this CTA's 128 x 256 fp32 partial into the workspace
         // ws[s][t][256][256] (tensor map tmAux), summed in slice order afterwards
+        // (8-bit operands: the partial carries the dequantisation factor)
         const int wrow = (sg.s * (p.tiles_m * p.tiles_n) + sg.t) * 256 + (int)rank * 128 + quarter * 32;
-        if (!tc_epilogue_staged<BN>(p, NC_EP_STORE_F32, &tmAux, &tmAux, stg, &aux_bar[warp - 4], aux_phase,
-                                    taddr + c_lo, c_lo, BN, wrow, lane)) {
+        if (!tc_epilogue_staged<BN, F8>(p, NC_EP_STORE_F32, &tmAux, &tmAux, stg, &aux_bar[warp - 4], aux_phase,
+                                        taddr + c_lo, c_lo, BN, wrow, lane)) {
           fail();
           break;
         }
@@ -1224,7 +1225,8 @@ nc_status launch_gemm_tc_batched(int batch, int M, int N, int K, const bf16* A, 
 static nc_status gemm_fp8_impl(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
                                const float* scale_a, const float* scale_b, int ep, void* D, int64_t ldd,
                                const TcRope* rope, int32_t* err, cudaStream_t st, const void* aux = nullptr,
-                               int64_t ldaux = 0, unsigned* amax = nullptr) {
+                               int64_t ldaux = 0, unsigned* amax = nullptr, void* ws = nullptr,
+                               size_t ws_bytes = 0) {
   if (M <= 0 || N <= 0) return NC_OK;
   if (K <= 0 || !A || !B || !D || !scale_a || !scale_b) return NC_ERR_ARG;
   if ((lda % 16) || (ldb % 16) || lda < K || ldb < K || (((uintptr_t)A) & 15) || (((uintptr_t)B) & 15))
@@ -1282,6 +1284,12 @@ static nc_status gemm_fp8_impl(int M, int N, int K, const uint8_t* A, int64_t ld
     p.tma_epi = make_tmap_bf16_2d(&tx, aux, N, M, ldaux, 64, 32);
   }
   if (!p.tma_epi) return NC_ERR_CUDA;
+  // split K (fp32 outputs, CTA pairs only, with a workspace): partials carry the factor
+  if (pair && ws && out_f32) {
+    if (((uintptr_t)ws) & 15) return NC_ERR_ARG;
+    p.ws = (float*)ws;
+    return launch_tc_pair<true>(p, ta, tb, td, tx, ws_bytes, st);
+  }
   if (pair) return launch_tc_pair<true>(p, ta, tb, td, tx, 0, st);
   if (BN == 256) return launch_tc_bn<256, true>(p, ta, tb, td, tx, 0, st);
   return launch_tc_bn<128, true>(p, ta, tb, td, tx, 0, st);
@@ -1297,9 +1305,11 @@ nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, co
 nc_status launch_gemm_fp8_ep(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
                              const float* scale_a, const float* scale_b, int ep, void* D, int64_t ldd, int T, int nh,
                              int hd, const float* tab, int pair_rows, float* rstd, float eps, int32_t* err,
-                             cudaStream_t st, const void* aux, int64_t ldaux, unsigned* amax) {
+                             cudaStream_t st, const void* aux, int64_t ldaux, unsigned* amax, void* ws,
+                             size_t ws_bytes) {
   if (ep != NC_EP_QKV_ROPE)
-    return gemm_fp8_impl(M, N, K, A, lda, B, ldb, scale_a, scale_b, ep, D, ldd, nullptr, err, st, aux, ldaux, amax);
+    return gemm_fp8_impl(M, N, K, A, lda, B, ldb, scale_a, scale_b, ep, D, ldd, nullptr, err, st, aux, ldaux, amax,
+                         ws, ws_bytes);
   TcRope r{tab, rstd, T, nh, hd, pair_rows, eps};
   return gemm_fp8_impl(M, N, K, A, lda, B, ldb, scale_a, scale_b, ep, D, ldd, &r, err, st);
 }

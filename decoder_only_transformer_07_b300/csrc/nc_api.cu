@@ -44,6 +44,9 @@ struct nc_model {
   uint8_t* q8a = nullptr;            // E4M3 codes of a linear layer's input [Nmax, max(C, F)]
   uint8_t* q8w = nullptr;            // E4M3 codes of every block weight operand, quantised once per step
   uint8_t* q8wT = nullptr;           // the same codes transposed ([in][out]): B operands of the dX products
+  uint8_t* q8xT = nullptr;           // per layer, the four linears' input codes transposed [in][q8np]: dW operands
+  uint8_t* q8dyT = nullptr;          // one output gradient's codes transposed [out][q8np]
+  int64_t q8np = 0;                  // row pitch of the transposed codes: the token count rounded up to 16
   float* q8s = nullptr;              // per layer and linear {amax bits, scale, scale_inv, -}: inputs [L][4],
                                      // weights [L][4], output gradients dY [L][4]
   OptTensors* q8tl = nullptr;        // the 4 L weight operands (fp32 master offset, code offset, length)
@@ -249,6 +252,14 @@ static uint8_t* layer_act(const nc_model* m, uint8_t* base, int l, int64_t width
   return base + (size_t)l * m->Nmax * width * m->act;
 }
 
+// The transposed input codes of layer l's linear k (0 qkv, 1 proj, 2 fc, 3
+// c_proj) in q8xT: [in][q8np] bytes, the layer's four blocks back to back.
+static uint8_t* q8x_t(const nc_model* m, int l, int k) {
+  const int64_t C = m->C, Hd = (int64_t)m->H * m->hd, F = m->F;
+  const int64_t off[4] = {0, C, C + Hd, 2 * C + Hd};
+  return m->q8xT + ((int64_t)l * (2 * C + Hd + F) + off[k]) * m->q8np;
+}
+
 // ------------------------------------------------------------------ config
 
 static nc_status validate(const nc_config* c, nc_config* out) {
@@ -359,6 +370,10 @@ static nc_status allocate(nc_model* m) {
     m->q8tt->tile0[4 * L] = tiles;
     NC_TRY(dalloc(m, (size_t)so, (void**)&m->q8w));
     NC_TRY(dalloc(m, (size_t)so, (void**)&m->q8wT));
+    m->q8np = (N + 15) / 16 * 16;
+    const int64_t xrows = 2 * (int64_t)m->C + (int64_t)m->H * m->hd + m->F;   // the four inputs' widths
+    NC_TRY(dalloc(m, (size_t)(L * xrows * m->q8np), (void**)&m->q8xT));
+    NC_TRY(dalloc(m, (size_t)(kmax * m->q8np), (void**)&m->q8dyT));
     NC_TRY(dalloc_t(m, (size_t)48 * L, &m->q8s));
   }
   NC_TRY(dalloc_t(m, (size_t)N, &m->rstd_f));
@@ -568,7 +583,9 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
       PROF(NC_PROF_QUANT, 0, 2.0 * N * K, launch_fp8_amax(NC_BF16, act_in, N * K, as, st));
       m->launches += 1;
     }
-    PROF(NC_PROF_QUANT, 0, 3.0 * N * K, launch_fp8_cast_scaled(NC_BF16, act_in, N * K, m->q8a, as, st));
+    // the codes in both layouts: row-major for this product, transposed for its weight gradient
+    PROF(NC_PROF_QUANT, 0, 4.0 * N * K,
+         launch_fp8_cast_dual(act_in, (int)N, K, as, m->q8a, q8x_t(m, l, k), m->q8np, st));
     const double out = ep == NC_EP_ACCUM_F32 ? 8.0 : 2.0;
     PROF_SUB(NC_PROF_GEMM, NC_PROF_GEMM_FWD, 2.0 * N * Nout * K, (double)N * K + (double)Nout * K + (double)N * Nout * out,
              launch_gemm_fp8_ep((int)N, Nout, K, m->q8a, K, w8, K, as + 2, ws + 2, ep, D, ldd, T, nh, m->hd,
@@ -633,12 +650,13 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
   return NC_OK;
 }
 
-// One block's backward in the 8-bit step.  The weight gradients dW = dY^T X
-// are the bf16 products of the unquantised operands; each input gradient
-// dX = dY W multiplies E4M3 operands: dY's bf16 value quantised per tensor
-// into q8a with its own statistics slot (the cast alone when the RMSNorm
-// backward that wrote it has taken its maximum), and W's forward codes read
-// transposed, with the forward's factor.
+// One block's backward in the 8-bit step.  Each linear's output gradient dY
+// is quantised once, per tensor, with its own statistics slot (its producer
+// has taken the maximum), into q8a and transposed into q8dyT.  The input
+// gradient dX = dY W multiplies those codes with W's forward codes read
+// transposed; the weight gradient dW = dY^T X multiplies the transposed codes
+// of dY and of X (kept from the forward), each with its own factor, split
+// over K (the tokens) when the output has few tiles.
 static nc_status backward_layer_fp8(nc_model* m, int l, int B, int T, float* grads, int gw, cudaStream_t st) {
   const int64_t N = (int64_t)B * T;
   const int C = m->C, F = m->F, Hd = m->H * m->hd, W = m->qkvw;
@@ -657,42 +675,41 @@ static nc_status backward_layer_fp8(nc_model* m, int l, int B, int T, float* gra
   float* lse = m->lse + (size_t)l * m->Nmax * m->H;
   const ParamTensor &tq = tensor(m, l, 0), &to = tensor(m, l, 3), &tfc = tensor(m, l, 4), &tpj = tensor(m, l, 5);
   auto slot = [&](int ll, int k) { return m->q8s + 32 * m->L + (4 * ll + k) * 4; };
-  auto dx8 = [&](int k, const void* dy, int K, int Nout, int ep, void* D, const void* aux, bool amax_ready,
-                 unsigned* amax_out = nullptr) -> nc_status {
+  // k: the linear (0 qkv, 1 proj, 2 fc, 3 c_proj); dy [N][K]; Nout: its input width
+  auto bwd8 = [&](int k, const void* dy, int K, int Nout, int ep, void* D, const void* aux, float* dw,
+                  unsigned* amax_out = nullptr) -> nc_status {
     float* ys = slot(l, k);
     const float* ws = m->q8s + 16 * m->L + (4 * l + k) * 4;
+    const float* xs = m->q8s + (4 * l + k) * 4;   // the forward input's factor
     const uint8_t* wT = m->q8wT + m->q8tl->soff[4 * l + k];
-    if (!amax_ready) {
-      PROF(NC_PROF_QUANT, 0, 2.0 * N * K, launch_fp8_amax(NC_BF16, dy, N * K, ys, st));
-      m->launches += 1;
-    }
-    PROF(NC_PROF_QUANT, 0, 3.0 * N * K, launch_fp8_cast_scaled(NC_BF16, dy, N * K, m->q8a, ys, st));
+    PROF(NC_PROF_QUANT, 0, 4.0 * N * K, launch_fp8_cast_dual(dy, n, K, ys, m->q8a, m->q8dyT, m->q8np, st));
     const double out = ep == NC_EP_STORE_F32 ? 4.0 : (aux ? 4.0 : 2.0);
     PROF_SUB(NC_PROF_GEMM, NC_PROF_GEMM_DX, 2.0 * N * Nout * K,
              (double)N * K + (double)Nout * K + (double)N * Nout * out,
              launch_gemm_fp8_ep(n, Nout, K, m->q8a, K, wT, K, ys + 2, ws + 2, ep, D, Nout, 0, 0, 0, nullptr, 0,
                                 nullptr, 0.f, m->err, st, aux, aux ? Nout : 0, amax_out));
-    m->launches += 2;
+    PROF_SUB(NC_PROF_GEMM, NC_PROF_GEMM_DW, 2.0 * N * Nout * K,
+             (double)N * K + (double)Nout * N + (double)K * Nout * (gw == NC_EP_ACCUM_F32 ? 8.0 : 4.0),
+             launch_gemm_fp8_ep(K, Nout, n, m->q8dyT, m->q8np, q8x_t(m, l, k), m->q8np, ys + 2, xs + 2, gw, dw, Nout,
+                                0, 0, 0, nullptr, 0, nullptr, 0.f, m->err, st, nullptr, 0, nullptr, m->gemm_ws,
+                                m->gemm_ws_bytes));
+    m->launches += 3;
     return NC_OK;
   };
-  // MLP: x2 = x1 + relu(xn2 Wfc^T)^2 Wproj^T
-  NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, F, n, m->dx_act, C, 0, h, F, 0, gw, grads + tpj.off, F, nullptr, 0, st));
-  // the relu^2-backward epilogue takes the maximum of du for the up-projection's dX quantiser
-  NC_TRY(dx8(3, m->dx_act, C, F, NC_EP_RELU2_SQ_BWD, m->du, h, true, (unsigned*)slot(l, 2)));
-  NC_TRY(gemm(m, NC_PROF_GEMM_DW, F, C, n, m->du, F, 0, xn2, C, 0, gw, grads + tfc.off, C, nullptr, 0, st));
-  NC_TRY(dx8(2, m->du, F, C, NC_EP_STORE_F32, m->dxn, nullptr, true));
+  // MLP: x2 = x1 + relu(xn2 Wfc^T)^2 Wproj^T; the relu^2-backward epilogue
+  // takes the maximum of du for the up-projection's quantiser
+  NC_TRY(bwd8(3, m->dx_act, C, F, NC_EP_RELU2_SQ_BWD, m->du, h, grads + tpj.off, (unsigned*)slot(l, 2)));
+  NC_TRY(bwd8(2, m->du, F, C, NC_EP_STORE_F32, m->dxn, nullptr, grads + tfc.off));
   PROF(NC_PROF_NORM, 0, nb_by,
        launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, xn2, rstd2, m->dx, m->dx_act, st, (unsigned*)slot(l, 1)));
   // attention: x1 = x + o Wo^T
-  NC_TRY(gemm(m, NC_PROF_GEMM_DW, C, Hd, n, m->dx_act, C, 0, o, Hd, 0, gw, grads + to.off, Hd, nullptr, 0, st));
-  NC_TRY(dx8(1, m->dx_act, C, Hd, NC_EP_STORE, m->dout, nullptr, true));
+  NC_TRY(bwd8(1, m->dx_act, C, Hd, NC_EP_STORE, m->dout, nullptr, grads + to.off));
   // the attention backward's epilogues take the maximum of dq, dk and dv for the dX quantiser
   PROF(NC_PROF_ATTN_BWD, attn_fl, (double)N * (2.0 * W + 2.0 * Hd) * a + 8.0 * N * m->H,
        attn_bwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->dout, m->dqkv, m->Dv, rstdqk,
                 m->rope_pairs ? m->rope_pairs : m->rope_tab, m->rope_pairs ? m->Tmax : 0, m->err, st,
                 (unsigned*)slot(l, 0)));
-  NC_TRY(gemm(m, NC_PROF_GEMM_DW, W, C, n, m->dqkv, W, 0, xn1, C, 0, gw, grads + tq.off, C, nullptr, 0, st));
-  NC_TRY(dx8(0, m->dqkv, W, C, NC_EP_STORE_F32, m->dxn, nullptr, true));
+  NC_TRY(bwd8(0, m->dqkv, W, C, NC_EP_STORE_F32, m->dxn, nullptr, grads + tq.off));
   // the block's input gradient is the previous block's output gradient: its maximum, for that block's Wproj product
   PROF(NC_PROF_NORM, 0, nb_by,
        launch_rmsnorm_bwd(m->dtype, N, C, m->dxn, xn1, rstd1, m->dx, m->dx_act, st,

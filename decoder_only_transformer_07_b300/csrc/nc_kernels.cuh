@@ -93,12 +93,13 @@ nc_status launch_gemm_fp8(int M, int N, int K, const uint8_t* A, int64_t lda, co
 // relu(u)^2, row pitch ldaux), or NC_EP_QKV_ROPE (then T, nh, hd, tab,
 // pair_rows, rstd and eps as for launch_gemm_tc_qkv_rope; ignored otherwise).
 // amax (bf16 outputs but QKV_ROPE): atomic maximum of |D| as stored, as float
-// bits, for the per-tensor quantiser of D.
+// bits, for the per-tensor quantiser of D.  ws (fp32 outputs on CTA pairs): a
+// split-K workspace of ws_bytes, as for launch_gemm_tc.
 nc_status launch_gemm_fp8_ep(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
                              const float* scale_a, const float* scale_b, int ep, void* D, int64_t ldd, int T, int nh,
                              int hd, const float* tab, int pair_rows, float* rstd, float eps, int32_t* err,
                              cudaStream_t st, const void* aux = nullptr, int64_t ldaux = 0,
-                             unsigned* amax = nullptr);
+                             unsigned* amax = nullptr, void* ws = nullptr, size_t ws_bytes = 0);
 // Per-tensor E4M3 quantisation of n fp32 / bf16 values: stats (device, 3
 // floats) gets {amax, scale, scale_inv}; y the codes.
 nc_status launch_quantize_fp8(int dtype, const void* x, int64_t n, uint8_t* y, float* stats, cudaStream_t st);
@@ -109,6 +110,11 @@ nc_status launch_quantize_fp8(int dtype, const void* x, int64_t n, uint8_t* y, f
 // stats[1], stats[2] written; the codes equal launch_quantize_fp8's.
 nc_status launch_fp8_amax(int dtype, const void* x, int64_t n, float* stats, cudaStream_t st);
 nc_status launch_fp8_cast_scaled(int dtype, const void* x, int64_t n, uint8_t* y, float* stats, cudaStream_t st);
+// The same cast of a [rows][cols] bf16 tensor, also written transposed into yt
+// [cols][ldt] (ldt >= rows, a multiple of 16): the codes of a product that
+// contracts over the rows.
+nc_status launch_fp8_cast_dual(const void* x, int rows, int cols, float* stats, uint8_t* y, uint8_t* yt, int64_t ldt,
+                               cudaStream_t st);
 
 nc_status launch_attn_fwd_simt(int dtype, int B, int T, int H, int Hkv, int hd, const void* qkv, void* o,
                                float* lse, cudaStream_t st);

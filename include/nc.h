@@ -72,8 +72,9 @@ typedef struct {
    * accumulate in fp32 and are dequantised in the fused epilogues.  In the
    * backward their input gradients dX = dY W multiply E4M3 operands as well
    * (dY's bf16 value with its own per-tensor scale, W's forward codes read
-   * transposed); the weight gradients are bf16 products of the unquantised
-   * operands (the quantisers pass gradients through unchanged).  The
+   * transposed), and so do their weight gradients dW = dY^T X (the transposed
+   * codes of dY and of the forward input); the quantisers pass gradients
+   * through unchanged.  The
    * lm_head, attention and norms stay bf16.  NC_BF16 only; n_embd and mlp_hidden
    * multiples of 16; decoding (nc_kv_cache_create) is not offered.  0: off.  */
   int32_t fp8;
