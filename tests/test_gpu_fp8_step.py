@@ -5,8 +5,8 @@ FP8 without one): the blocks' four linear layers multiply E4M3 operands in
 the forward, the bf16 activation and the fp32 master weight quantised per
 tensor with current scaling; their input gradients dX = dY W multiply E4M3
 operands too (dY's bf16 value with its own per-tensor scale, W's forward
-codes read transposed); the weight gradients are bf16 products of the
-unquantised operands.
+codes read transposed), and so do their weight gradients dW = dY^T X (the
+same codes of dY and of X, transposed).
 
 Tolerances.  Both sides quantise the same fp32 master weights, so the weight
 codes agree; the activation and output-gradient codes come from tensors that
