@@ -107,3 +107,29 @@ def test_fp8_config_rules():
         m.kv_cache_create(1, 64)
     assert e.value.status == 7
     m.close()
+
+
+def test_fp8_step_accumulates_micro_batches():
+    """Accumulating a second micro-batch adds its 8-bit gradient to the first's:
+    the buffer equals the sum of the two steps' gradients taken separately (each
+    micro-batch quantised with its own per-tensor scales either way), through the
+    reduce-add epilogues and the split-K fix-up of the 8-bit weight gradients."""
+    w = S.Workload(name="small", dtype="bf16", tokens="zipf", **SHAPES[2])
+    cfg8, m, params = _models(w)
+    tok, tgt = S.batch_tokens(w)                          # [3, 333]
+    parts = [(tok[:2], tgt[:2]), (tok[2:], tgt[2:])]
+    dev = [(torch.from_numpy(np.ascontiguousarray(t)).cuda(), torch.from_numpy(np.ascontiguousarray(g)).cuda())
+           for t, g in parts]
+    separate = []
+    for t, g in dev:
+        _, grads = m.forward_backward(t, g)
+        separate.append(grads.clone())
+    acc = torch.empty(m.n_params, dtype=torch.float32, device="cuda")
+    for i, (t, g) in enumerate(dev):
+        m.forward_backward_accumulate(t, g, acc, 1.0, accumulate=i > 0)
+    want = (separate[0] + separate[1]).cpu().numpy().astype(np.float64)
+    got = acc.cpu().numpy().astype(np.float64)
+    for name, r, c, off in m.layout:
+        a, b = got[off:off + r * c], want[off:off + r * c]
+        assert np.linalg.norm(a - b) <= 1e-6 * np.linalg.norm(b), name
+    m.close()
