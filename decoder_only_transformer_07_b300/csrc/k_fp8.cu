@@ -123,29 +123,9 @@ __device__ __forceinline__ float fp8_scale_of(float amax) {
   return scale;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(FP8_THREADS) k_fp8_cast_scaled(const T* __restrict__ x, int64_t n,
-                                                                 float* __restrict__ stats, uint8_t* __restrict__ y) {
-  const float s = fp8_scale_of(__uint_as_float(*reinterpret_cast<const unsigned*>(stats)));
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    stats[1] = s;
-    stats[2] = 1.f / s;
-  }
-  const int64_t n8 = n & ~(int64_t)7;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x * 8;
-  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < n8; i += stride) {
-    float f[8];
-    load8(x, i, f);
-    uint2 o;
-    o.x = e4m3(f[0] * s) | (e4m3(f[1] * s) << 8) | (e4m3(f[2] * s) << 16) | (e4m3(f[3] * s) << 24);
-    o.y = e4m3(f[4] * s) | (e4m3(f[5] * s) << 8) | (e4m3(f[6] * s) << 16) | (e4m3(f[7] * s) << 24);
-    *reinterpret_cast<uint2*>(y + i) = o;
-  }
-  if (blockIdx.x == 0 && threadIdx.x < n - n8) y[n8 + threadIdx.x] = (uint8_t)e4m3(to_f32(x[n8 + threadIdx.x]) * s);
-}
-
 // The scaled cast of a [rows][cols] bf16 tensor written in both layouts: y
-// [rows][cols] as k_fp8_cast_scaled writes it, and yt [cols][ldt] (ldt >= rows,
+// [rows][cols] (codes as the standalone quantiser's cast writes them, the
+// scale formed here from the maximum in stats[0]), and yt [cols][ldt] (ldt >= rows,
 // a multiple of 16), its transpose: the K-major operand of a product that
 // contracts over rows.  One block per 64 x 64 tile through shared memory; the
 // tile's own rows and columns past the end are skipped.
@@ -226,24 +206,6 @@ static unsigned fp8_grid(int64_t n) {
   return (unsigned)std::min<long long>(want, 8LL * g_num_sms);
 }
 
-nc_status launch_fp8_amax(int dtype, const void* x, int64_t n, float* stats, cudaStream_t st) {
-  if (n <= 0) return NC_OK;
-  if (!x || !stats || (((uintptr_t)x) & 15) || (((uintptr_t)stats) & 3)) return NC_ERR_ARG;
-  const unsigned grid = fp8_grid(n);
-  if (dtype == NC_BF16) k_fp8_amax<bf16><<<grid, FP8_THREADS, 0, st>>>((const bf16*)x, n, (unsigned*)stats);
-  else k_fp8_amax<float><<<grid, FP8_THREADS, 0, st>>>((const float*)x, n, (unsigned*)stats);
-  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
-}
-
-nc_status launch_fp8_cast_scaled(int dtype, const void* x, int64_t n, uint8_t* y, float* stats, cudaStream_t st) {
-  if (n <= 0) return NC_OK;
-  if (!x || !y || !stats || (((uintptr_t)x) & 15) || (((uintptr_t)y) & 7) || (((uintptr_t)stats) & 3))
-    return NC_ERR_ARG;
-  const unsigned grid = fp8_grid(n);
-  if (dtype == NC_BF16) k_fp8_cast_scaled<bf16><<<grid, FP8_THREADS, 0, st>>>((const bf16*)x, n, stats, y);
-  else k_fp8_cast_scaled<float><<<grid, FP8_THREADS, 0, st>>>((const float*)x, n, stats, y);
-  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
-}
 
 // Multi-tensor form over fp32 tensors (the weight operands of one step): block
 // b handles chunk b - chunk0[t] (OPT_CHUNK elements) of tensor t.

@@ -574,15 +574,12 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
          launch_fp8_quantize_multi(*m->q8tl, m->master, m->q8s + 16 * m->L, m->q8w, st));
     m->launches += 2;
   }
+  // (the input's maximum is already in its slot: its producer took it)
   auto lin8 = [&](int l, int k, const void* act_in, int K, int Nout, int ep, void* D, int64_t ldd, float* rstdqk,
-                  bool amax_ready, unsigned* amax_out = nullptr) -> nc_status {
+                  unsigned* amax_out = nullptr) -> nc_status {
     float* as = m->q8s + (4 * l + k) * 4;
     float* ws = m->q8s + 16 * m->L + (4 * l + k) * 4;
     const uint8_t* w8 = m->q8w + m->q8tl->soff[4 * l + k];
-    if (!amax_ready) {
-      PROF(NC_PROF_QUANT, 0, 2.0 * N * K, launch_fp8_amax(NC_BF16, act_in, N * K, as, st));
-      m->launches += 1;
-    }
     // the codes in both layouts: row-major for this product, transposed for its weight gradient
     PROF(NC_PROF_QUANT, 0, 4.0 * N * K,
          launch_fp8_cast_dual(act_in, (int)N, K, as, m->q8a, q8x_t(m, l, k), m->q8np, st));
@@ -608,17 +605,17 @@ static nc_status forward_trunk(nc_model* m, const int32_t* tokens, int B, int T,
       // the norms take the maximum of the bf16 values they store: their inputs' quantisation is one cast
       PROF(NC_PROF_NORM, 0, nrm_by,
            launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn1, rstd1, eps, st, (unsigned*)(m->q8s + (4 * l + 0) * 4)));
-      NC_TRY(lin8(l, 0, xn1, C, W, NC_EP_QKV_ROPE, qkv, W, rstdqk, true));
+      NC_TRY(lin8(l, 0, xn1, C, W, NC_EP_QKV_ROPE, qkv, W, rstdqk));
       // the attention epilogue takes the maximum of O for the output projection's quantiser
       PROF(NC_PROF_ATTN_FWD, attn_fl, (double)N * (W + Hd) * a + 4.0 * N * m->H,
            attn_fwd(m->dtype, B, T, m->H, m->Hkv, m->hd, qkv, o, lse, m->err, st,
                     (unsigned*)(m->q8s + (4 * l + 1) * 4)));
-      NC_TRY(lin8(l, 1, o, Hd, C, NC_EP_ACCUM_F32, m->x, C, nullptr, true));
+      NC_TRY(lin8(l, 1, o, Hd, C, NC_EP_ACCUM_F32, m->x, C, nullptr));
       PROF(NC_PROF_NORM, 0, nrm_by,
            launch_rmsnorm_fwd(m->dtype, N, C, m->x, xn2, rstd2, eps, st, (unsigned*)(m->q8s + (4 * l + 2) * 4)));
       // the up-projection's epilogue takes the maximum of relu(u)^2 for the down-projection's quantiser
-      NC_TRY(lin8(l, 2, xn2, C, F, NC_EP_RELU2_SQ, h, F, nullptr, true, (unsigned*)(m->q8s + (4 * l + 3) * 4)));
-      NC_TRY(lin8(l, 3, h, F, C, NC_EP_ACCUM_F32, m->x, C, nullptr, true));
+      NC_TRY(lin8(l, 2, xn2, C, F, NC_EP_RELU2_SQ, h, F, nullptr, (unsigned*)(m->q8s + (4 * l + 3) * 4)));
+      NC_TRY(lin8(l, 3, h, F, C, NC_EP_ACCUM_F32, m->x, C, nullptr));
       m->launches += 3;
       continue;
     }

@@ -103,16 +103,13 @@ nc_status launch_gemm_fp8_ep(int M, int N, int K, const uint8_t* A, int64_t lda,
 // Per-tensor E4M3 quantisation of n fp32 / bf16 values: stats (device, 3
 // floats) gets {amax, scale, scale_inv}; y the codes.
 nc_status launch_quantize_fp8(int dtype, const void* x, int64_t n, uint8_t* y, float* stats, cudaStream_t st);
-// The step's 8-bit quantiser pieces.  stats = {amax bits, scale, scale_inv}
-// with stats[0] zeroed beforehand.  launch_fp8_amax: atomic maximum of |x|
-// into stats[0].  launch_fp8_cast_scaled: scale = fl32(448 / amax) (1 if not
-// finite and positive) formed by every block, codes of fl32(x * scale), and
-// stats[1], stats[2] written; the codes equal launch_quantize_fp8's.
-nc_status launch_fp8_amax(int dtype, const void* x, int64_t n, float* stats, cudaStream_t st);
-nc_status launch_fp8_cast_scaled(int dtype, const void* x, int64_t n, uint8_t* y, float* stats, cudaStream_t st);
-// The same cast of a [rows][cols] bf16 tensor, also written transposed into yt
-// [cols][ldt] (ldt >= rows, a multiple of 16): the codes of a product that
-// contracts over the rows.
+// The step's 8-bit cast.  stats = {amax bits, scale, scale_inv}, stats[0]
+// holding the maximum |x| its producer took (as float bits): scale = fl32(448
+// / amax) (1 if not finite and positive), formed by every block; the codes of
+// fl32(x * scale) of a [rows][cols] bf16 tensor go to y [rows][cols] (equal
+// to launch_quantize_fp8's) and transposed into yt [cols][ldt] (ldt >= rows, a
+// multiple of 16): the codes of a product that contracts over the rows;
+// stats[1], stats[2] are written.
 nc_status launch_fp8_cast_dual(const void* x, int rows, int cols, float* stats, uint8_t* y, uint8_t* yt, int64_t ldt,
                                cudaStream_t st);
 
