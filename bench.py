@@ -208,10 +208,11 @@ def run_reference(args, w):
     t_sample = CPU_SAMPLE_T.get(args.config, 64)
     tps, threads, times = oracle_sample(w, t_sample, args.steps, args.warmup)
     fs, fw = sample_flops_per_token(w, t_sample), flops_per_token(w)["causal"]
-    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": 0,
+    # the host cores run it; n_gpus is the N the arm was launched for
+    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": DESCR[args.config], "sample": f"1 x {t_sample} tokens"},
+            "data": "synthetic", "config": {**arm_config(args.config, w, world), "sample": f"1 x {t_sample} tokens"},
             "cpu_baseline": {"value": tps, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": f"one sequence of {t_sample} tokens of the {args.config} workload, "
                                        f"fp64 NumPy forward+backward",
@@ -576,9 +577,13 @@ def measure(w, name, args, world, rank, dev, gpu_traffic=True, fp8=False):
     return {"value": value, "ms_per_step": ms_step, "mfu": mfu, "flops_per_token": fpt["causal"],
             "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches_per_step * args.steps), "clocks": clk,
             "kernels": kernels, "loss": losses[-1],
-            "config": {"workload": DESCR[name], "global_batch": world * w.batch, "seq_len": w.seq_len,
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "working set >> L2 (no flush needed)"}}
+            "config": arm_config(name, w, world)}
+
+
+def arm_config(name, w, world):
+    """The bench line's config for workload w on `world` GPUs (both arms)."""
+    return {"workload": DESCR[name], "global_batch": world * w.batch, "seq_len": w.seq_len,
+            "parallelism": "replicas" if world > 1 else "single", "l2": "working set >> L2 (no flush needed)"}
 
 
 def main():
