@@ -74,9 +74,11 @@ typedef struct {
    * (dY's bf16 value with its own per-tensor scale, W's forward codes read
    * transposed), and so do their weight gradients dW = dY^T X (the transposed
    * codes of dY and of the forward input); the quantisers pass gradients
-   * through unchanged.  The
-   * lm_head, attention and norms stay bf16.  NC_BF16 only; n_embd and mlp_hidden
-   * multiples of 16; decoding (nc_kv_cache_create) is not offered.  0: off.  */
+   * through unchanged.  The lm_head, attention and norms stay bf16.  The
+   * model then also holds every layer's transposed input codes,
+   * batch * seq_len * (2 n_embd + n_head head_dim + mlp_hidden) bytes per
+   * layer.  NC_BF16 only; n_embd and mlp_hidden multiples of 16; decoding
+   * (nc_kv_cache_create) is not offered.  0: off.  */
   int32_t fp8;
 } nc_config;
 
