@@ -195,18 +195,6 @@ nc_status launch_fp8_cast_dual(const void* x, int rows, int cols, float* stats, 
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
-static unsigned fp8_grid(int64_t n) {
-  if (!g_num_sms) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      g_num_sms = 148;
-  }
-  const long long want = std::max<long long>(1, (n / 8 + FP8_THREADS - 1) / FP8_THREADS);
-  return (unsigned)std::min<long long>(want, 8LL * g_num_sms);
-}
-
-
 // Multi-tensor form over fp32 tensors (the weight operands of one step): block
 // b handles chunk b - chunk0[t] (OPT_CHUNK elements) of tensor t.
 __device__ __forceinline__ int fp8_tensor_of(const OptTensors& tl, int blk) {
