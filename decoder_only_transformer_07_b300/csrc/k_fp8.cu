@@ -249,32 +249,55 @@ nc_status launch_fp8_quantize_multi(const OptTensors& tl, const float* master, f
 
 // Transposed copies of the weight codes, for the input-gradient products
 // dX = dY W, whose B operand is W^T in the K-major layout the 8-bit GEMM
-// reads: codes [rows][cols] of tensor t at src + tl.soff[t] become
-// [cols][rows] at dst + tl.soff[t] (the same factor applies).  One block per
-// 64 x 64 tile through shared memory; partial edge tiles are bounds-checked.
+// reads: codes [rows][cols] of tensor t at src + tt.off[t] become
+// [cols][rows] at dst + tt.off[t] (the same factor applies).  One block per
+// 64 x 64 tile through shared memory: 16-byte loads of the tile's rows, then
+// each thread gathers 16 bytes of one column and stores them as one piece;
+// partial edge pieces go byte by byte.
 __global__ void __launch_bounds__(256) k_fp8_transpose_multi(const __grid_constant__ Fp8Transposes tt,
                                                              const uint8_t* __restrict__ src, uint8_t* __restrict__ dst) {
-  __shared__ uint8_t tile[64][68];
-  int t = 0, lo = 0, hi = tt.n;
+  __shared__ __align__(16) uint8_t tile[64][80];
+  int lo = 0, hi = tt.n;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (tt.tile0[mid] <= (int)blockIdx.x) lo = mid; else hi = mid;
   }
-  t = lo;
+  const int t = lo;
   const int rows = tt.rows[t], cols = tt.cols[t];
   const int tc = (cols + 63) / 64;
   const int k = (int)blockIdx.x - tt.tile0[t];
   const int r0 = (k / tc) * 64, c0 = (k % tc) * 64;
   const uint8_t* s = src + tt.off[t];
   uint8_t* d = dst + tt.off[t];
-  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
-    const int r = i >> 6, c = i & 63;
-    if (r0 + r < rows && c0 + c < cols) tile[r][c] = s[(int64_t)(r0 + r) * cols + c0 + c];
+  const int th = threadIdx.x;
+  {   // row r0 + th / 4, columns c0 + 16 (th % 4) .. +16
+    const int r = th >> 2, cc = (th & 3) * 16;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r0 + r < rows) {
+      const uint8_t* sr = s + (int64_t)(r0 + r) * cols + c0 + cc;
+      if (c0 + cc + 16 <= cols && (cols & 15) == 0) {
+        v = *reinterpret_cast<const uint4*>(sr);
+      } else {
+        uint8_t* vb = reinterpret_cast<uint8_t*>(&v);
+        for (int e = 0; e < 16 && c0 + cc + e < cols; ++e) vb[e] = sr[e];
+      }
+    }
+    *reinterpret_cast<uint4*>(&tile[r][cc]) = v;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
-    const int c = i >> 6, r = i & 63;
-    if (r0 + r < rows && c0 + c < cols) d[(int64_t)(c0 + c) * rows + r0 + r] = tile[r][c];
+  {   // transposed row c0 + th / 4 (a column), rows r0 + 16 (th % 4) .. +16
+    const int c = th >> 2, rr = (th & 3) * 16;
+    if (c0 + c < cols && r0 + rr < rows) {
+      uint32_t q[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) q[e >> 2] |= (uint32_t)tile[rr + e][c] << (8 * (e & 3));
+      uint8_t* o = d + (int64_t)(c0 + c) * rows + r0 + rr;
+      if (r0 + rr + 16 <= rows && (rows & 15) == 0) {
+        *reinterpret_cast<uint4*>(o) = make_uint4(q[0], q[1], q[2], q[3]);
+      } else {
+        for (int e = 0; r0 + rr + e < rows && e < 16; ++e) o[e] = (uint8_t)(q[e >> 2] >> (8 * (e & 3)));
+      }
+    }
   }
 }
 
