@@ -41,6 +41,9 @@ SHAPES = [
     dict(depth=2, n_embd=256, n_head=4, n_kv_head=2, head_dim=64, mlp_hidden=1024, vocab=1024, seq_len=200, batch=2),
     # rows past one 256-row pair tile and a ragged tail: CTA-pair 8-bit GEMMs with every epilogue
     dict(depth=1, n_embd=384, n_head=3, n_kv_head=1, head_dim=128, mlp_hidden=1536, vocab=4096, seq_len=333, batch=3),
+    # an MLP width that is a multiple of 16 but not of 64: partial column tiles in the casts and the weight-code
+    # transposes, and N, K tails in the 8-bit products
+    dict(depth=1, n_embd=256, n_head=2, n_kv_head=2, head_dim=128, mlp_hidden=1040, vocab=1024, seq_len=200, batch=2),
 ]
 
 
@@ -52,7 +55,7 @@ def _models(w):
     return cfg8, m, params
 
 
-@pytest.mark.parametrize("shape", SHAPES, ids=["mha_hd128", "gqa_hd64", "gqa3_ragged"])
+@pytest.mark.parametrize("shape", SHAPES, ids=["mha_hd128", "gqa_hd64", "gqa3_ragged", "mlp1040"])
 def test_fp8_step_matches_oracle(shape):
     w = S.Workload(name="small", dtype="bf16", tokens="zipf", **shape)
     cfg8, m, params = _models(w)
